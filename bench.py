@@ -1,0 +1,492 @@
+#!/usr/bin/env python3
+"""Benchmark of the selective-scan (S6) hot path on B300.
+
+One step = one pass of the hot path over one batch of the Mamba-1.4B-shaped
+layer (batch 8, d_inner 4096, d_state 16, L 16384, bf16 activations, fp32
+state, zero-order hold): causal conv1d + SiLU -> fused selective-scan forward
+(-> backward with recompute, when the library provides it).  Inputs are
+synthetic (seeded counter-based generator), resident in HBM and larger than
+L2 (several GB per step), so no L2 flush is needed between steps.
+
+Prints ONE JSON line on rank 0.  ``--impl reference`` times the fp64 CPU
+oracle instead (the method's plain definition), on a bounded sample of the
+same workload.  Multi-GPU (torchrun): every rank runs its own replica of the
+workload (the path has no exchange step), timing is max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "selective-scan fwd GB/s & channel-tokens/s vs HBM roofline; decode µs/step"
+UNIT = "channel-tokens/s"
+
+# Mamba-1.4B-shaped layer (the workload the >= 70%-of-roofline target names)
+WORK = dict(batch=8, dim=4096, dstate=16, seqlen=16384, width=4)
+# Mamba-2.8B-shaped decode (64 layers, batch 128)
+DECODE = dict(batch=128, dim=5120, dstate=16, width=4, layers=64, steps=128)
+
+SM_FP32_LANES = 128     # FP32 lanes per SM per clock (sm_100 family)
+SM_SFU_EX2 = 32         # MUFU ex2 results per SM per clock on B300 (measured 29.8 at ~2 GHz)
+FALLBACK_HBM_GBS = 6400.0
+
+
+# ---------------------------------------------------------------------------
+# environment
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world: int, backend: str):
+    if world > 1 and not torch.distributed.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world: int):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world <= 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.device_index = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            uuid = str(torch.cuda.get_device_properties(self.device_index).uuid)
+            sel = f"GPU-{uuid}" if uuid and not uuid.startswith("GPU-") else uuid
+        except Exception:
+            sel = str(self.device_index)
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", sel, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 8:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        smax = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(rows), "reasons": reasons}
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work per kernel (bytes moved; FP32 and SFU operations)
+def conv_work(b, d, L):
+    ct = b * d * L
+    return dict(bytes=4 * ct, fp32=0, sfu=0)
+
+
+def fwd_work(b, d, L, N, zoh=True, io_bytes=2):
+    """Compulsory HBM bytes: u, delta, z read + out written (io_bytes each per
+    channel-token) + B, C read once (shared by all channels).  Operations per
+    (channel, step, state): ZOH 3 mul + 1 add + 2 FMA = 6 FP32 and one exp
+    (simplified rule: 2 mul + 2 FMA = 4); per (channel, step): bias add, D*u FMA
+    and the gate multiply (3 FP32; +1 for delta*u in the simplified rule) and
+    4 SFU (softplus exp+log, sigmoid exp+reciprocal)."""
+    ct = b * d * L
+    byts = 4 * io_bytes * ct + 2 * N * io_bytes * b * L
+    per_n = 6 if zoh else 4
+    per_ct = 3 if zoh else 4
+    return dict(bytes=byts, fp32=ct * (N * per_n + per_ct), sfu=ct * (N + 4))
+
+
+def roofline(work, seconds, hbm_gbs, sms, sm_mhz, hbm_src, clock_src):
+    """Slowest of HBM, FP32 pipe and SFU for this kernel's algorithmic work."""
+    f = sm_mhz * 1e6
+    t_hbm = work["bytes"] / (hbm_gbs * 1e9)
+    t_fp32 = work["fp32"] / (sms * SM_FP32_LANES * f)
+    t_sfu = work["sfu"] / (sms * SM_SFU_EX2 * f)
+    bound = max((t_hbm, "hbm"), (t_fp32, "alu"), (t_sfu, "sfu"))[1]
+    if bound == "hbm":
+        ach, peak, unit = work["bytes"] / seconds / 1e9, hbm_gbs, "GB/s"
+        note = f"peak = HBM copy bandwidth, {hbm_src}"
+    elif bound == "alu":
+        ach, peak, unit = work["fp32"] / seconds / 1e12, sms * SM_FP32_LANES * f / 1e12, "TFP32op/s"
+        note = (f"peak = {sms} SMs x {SM_FP32_LANES} FP32 lanes x {sm_mhz:.0f} MHz ({clock_src}); "
+                "one FP32 op = one FMA, MUL or ADD lane-instruction")
+    else:
+        ach, peak, unit = work["sfu"] / seconds / 1e12, sms * SM_SFU_EX2 * f / 1e12, "TSFUop/s"
+        note = f"peak = {sms} SMs x {SM_SFU_EX2} SFU ops x {sm_mhz:.0f} MHz ({clock_src})"
+    return {"bound": "alu" if bound in ("alu", "sfu") else bound, "achieved": round(ach, 3),
+            "peak": round(peak, 3), "unit": unit, "frac": round(ach / peak, 4),
+            "hbm_gbs": round(work["bytes"] / seconds / 1e9, 1),
+            "hbm_frac": round(work["bytes"] / seconds / 1e9 / hbm_gbs, 4),
+            "bound_times_us": {"hbm": round(t_hbm * 1e6, 1), "fp32": round(t_fp32 * 1e6, 1),
+                               "sfu": round(t_sfu * 1e6, 1)},
+            "note": note}
+
+
+# ---------------------------------------------------------------------------
+def make_inputs(device, seed, cfg):
+    import synthetic as S
+    b, d, L, N, W = cfg["batch"], cfg["dim"], cfg["seqlen"], cfg["dstate"], cfg["width"]
+    g = S.scan_inputs(seed, b, d, L, N, dtype=torch.bfloat16, device=device)
+    c = S.conv_inputs(seed, b, d, L, W, dtype=torch.bfloat16, device=device)
+    g["x"], g["w"] = c["x"], c["w"]
+    g["xc"] = torch.empty_like(g["x"])
+    g["y"] = torch.empty(b, d, L, dtype=torch.bfloat16, device=device)
+    return g
+
+
+def step(L, g, ev=None):
+    if ev is not None:
+        ev[0].record()
+    L.causal_conv1d_silu(g["x"], g["w"], out=g["xc"])
+    if ev is not None:
+        ev[1].record()
+    L.ssm_scan_fwd(g["xc"], g["dt"], g["A"], g["B"], g["C"], D=g["D"], delta_bias=g["bias"], z=g["z"],
+                   out=g["y"], bbar_mode=L.SSM_BBAR_ZOH, delta_softplus=True,
+                   workspace=g.get("ws"))
+    if ev is not None:
+        ev[2].record()
+
+
+def bench_decode(L, device, cfg, reps: int):
+    """64-layer single-token decode step (conv update + state update per layer),
+    captured once in a CUDA graph and replayed; microseconds per token step."""
+    import synthetic as S
+    b, d, N, W, layers = cfg["batch"], cfg["dim"], cfg["dstate"], cfg["width"], cfg["layers"]
+    seed = S.config_seed(3)
+    st, cst, tok = [], [], []
+    A = S.A_matrix(d, N, device)
+    Dp = S.normal(seed, S.STREAM["D"], (d,), torch.float32, device)
+    bias = S.delta_bias(seed, d, 1e-3, 1e-1, device)
+    w = S.normal(seed, S.STREAM["w"], (d, W), torch.float32, device, std=0.5)
+    for l in range(layers):
+        st.append(S.normal(seed, S.decode_stream("h0", l, 0), (b, d, N), torch.float32, device))
+        cst.append(S.normal(seed, S.decode_stream("conv_state", l, 0), (b, d, W), torch.bfloat16, device))
+        tok.append({k: S.normal(seed, S.decode_stream(k, l, 0), (b, d), torch.bfloat16, device)
+                    for k in ("x", "dt", "z")})
+        tok[-1]["B"] = S.normal(seed, S.decode_stream("B", l, 0), (b, N), torch.bfloat16, device)
+        tok[-1]["C"] = S.normal(seed, S.decode_stream("C", l, 0), (b, N), torch.bfloat16, device)
+        tok[-1]["xc"] = torch.empty(b, d, dtype=torch.bfloat16, device=device)
+        tok[-1]["y"] = torch.empty(b, d, dtype=torch.bfloat16, device=device)
+
+    def token_step():
+        for l in range(layers):
+            t = tok[l]
+            L.causal_conv1d_silu_update(cst[l], t["x"], w, out=t["xc"])
+            L.ssm_state_update(st[l], t["xc"], t["dt"], A, t["B"], t["C"], D=Dp, delta_bias=bias, z=t["z"],
+                               out=t["y"])
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            token_step()
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        token_step()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / reps
+    # algorithmic bytes per layer-step: state r+w, conv window r+w, token rows
+    # (x, dt, z read; conv output written then read; y written), B, C, params
+    per_layer = (2 * b * d * N * 4 + 2 * b * d * W * 2 + 6 * b * d * 2 + 2 * b * N * 2
+                 + d * N * 4 + d * W * 4 + 2 * d * 4)
+    del graph
+    return {"us_per_token_step": round(us, 2), "layers": layers, "batch": b, "dim": d, "dstate": N,
+            "bytes_per_token_step": per_layer * layers, "gbs": round(per_layer * layers / (us * 1e-6) / 1e9, 1),
+            "kernels_per_token_step": 2 * layers, "cuda_graph": True, "token_steps": reps,
+            "note": "per layer: causal_conv1d_silu_update + ssm_state_update; 64 distinct layer states "
+                    "(2.7 GB) so nothing stays in L2"}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline arm)
+def oracle_sample_rate(channels: int, threads: int, cfg, seed: int):
+    """Run the fp64 oracle (conv + ZOH scan) on `channels` channels of batch row 0
+    over the full sequence; returns (channel-tokens/s, wall seconds)."""
+    import oracle
+    import synthetic as S
+    L, N, W = cfg["seqlen"], cfg["dstate"], cfg["width"]
+    d = cfg["dim"]
+    rows = list(range(channels))            # batch row 0, channels 0 .. channels-1
+    x = S.rows_at(seed, S.STREAM["x"], rows, L).to(torch.bfloat16).double()[None]
+    dt = S.rows_at(seed, S.STREAM["dt"], rows, L).to(torch.bfloat16).double()[None]
+    z = S.rows_at(seed, S.STREAM["z"], rows, L).to(torch.bfloat16).double()[None]
+    B = S.normal(seed, S.STREAM["B"], (1, N, L), torch.bfloat16).double()
+    C = S.normal(seed, S.STREAM["C"], (1, N, L), torch.bfloat16).double()
+    w = S.normal(seed, S.STREAM["w"], (d, W), torch.float32, std=0.5)[:channels].double()
+    A = S.A_matrix(d, N)[:channels].double()
+    Dp = S.normal(seed, S.STREAM["D"], (d,), torch.float32)[:channels].double()
+    bias = S.delta_bias(seed, d, 1e-3, 1e-1)[:channels].double()
+    t0 = time.perf_counter()
+    xc = oracle.conv1d_silu(x, w)
+    oracle.scan_fwd(xc, dt, A, B, C, Dp, bias, z, zoh=True, threads=threads)
+    wall = time.perf_counter() - t0
+    return channels * L / wall, wall
+
+
+def calibrated_channels(threads: int, cfg, seed: int, target_s: float) -> int:
+    rate1, _ = oracle_sample_rate(2, 1, cfg, seed)          # single-thread ct/s
+    per_channel_s = cfg["seqlen"] / rate1
+    n = int(target_s * threads / per_channel_s)
+    n = max(threads, min(cfg["dim"], n))
+    return (n // threads) * threads if n >= threads else n
+
+
+def cpu_baseline(cfg, seed: int, target_s: float = 10.0):
+    import oracle
+    threads = oracle.default_threads()
+    n = calibrated_channels(threads, cfg, seed, target_s)
+    rate, wall = oracle_sample_rate(n, threads, cfg, seed)
+    return {"value": round(rate, 1), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{n} channels of batch row 0, full L={cfg['seqlen']}, conv1d+SiLU then ZOH scan "
+                      f"forward in fp64 ({wall:.1f} s wall on {threads} threads)"}
+
+
+def run_reference(args):
+    rank, world, local = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    cfg = dict(WORK)
+    if args.sample_channels:
+        n = args.sample_channels
+    else:
+        n = calibrated_channels(oracle.default_threads(), cfg, 0x55AA0002, 3.0)
+    threads = oracle.default_threads()
+    for _ in range(args.warmup):
+        oracle_sample_rate(n, threads, cfg, 0x55AA0002)
+    walls = []
+    for _ in range(args.steps):
+        _, wall = oracle_sample_rate(n, threads, cfg, 0x55AA0002)
+        walls.append(wall)
+    total = sum(walls)
+    value = n * cfg["seqlen"] * args.steps / total
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "impl": "reference",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total / args.steps * 1e3, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(cfg),
+        "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"each step: {n} channels of batch row 0, full L={cfg['seqlen']}, "
+                                   "conv1d+SiLU then ZOH scan forward, fp64 oracle"},
+        "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(cfg):
+    return {"workload": "mamba-1.4b-layer: causal conv1d+SiLU -> fused selective-scan forward "
+                        f"(batch {cfg['batch']}, d_inner {cfg['dim']}, d_state {cfg['dstate']}, "
+                        f"L {cfg['seqlen']}, ZOH, softplus delta, D skip, silu(z) gate)",
+            "batch": cfg["batch"], "dim": cfg["dim"], "dstate": cfg["dstate"], "seqlen": cfg["seqlen"],
+            "io_dtype": "bf16", "state_dtype": "f32",
+            "l2": "inputs larger than L2 (about 4.3 GB read+written per step), no flush",
+            "parallelism": "replicas (one independent layer problem per GPU)"}
+
+
+# ---------------------------------------------------------------------------
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--sample-channels", type=int, default=0, help="reference arm: channels per step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    args = ap.parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    import selective_state_space_147_b300 as L
+    import synthetic as S
+
+    cfg = dict(WORK)
+    seed = S.config_seed(2) + 1000 * rank          # every rank its own batch (weak scaling)
+    g = make_inputs(device, seed, cfg)
+    ws_bytes = L.ssm_scan_fwd_workspace_size(g["xc"], g["A"])
+    if ws_bytes:
+        g["ws"] = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
+    props = torch.cuda.get_device_properties(device)
+    sms = props.multi_processor_count
+
+    for _ in range(max(3, args.warmup)):
+        step(L, g)
+    torch.cuda.synchronize()
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    sampler.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    n0 = L.launch_count()
+    start.record()
+    for k in range(K):
+        step(L, g, evs[k])
+    end.record()
+    torch.cuda.synchronize()
+    launches = L.launch_count() - n0
+    barrier(world)
+    clocks = sampler.stop()
+    ms_total = start.elapsed_time(end)
+    ms_total = max_over_ranks(ms_total, world, device)
+    conv_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    fwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+
+    b, d, Lq, N = cfg["batch"], cfg["dim"], cfg["seqlen"], cfg["dstate"]
+    ct_step = b * d * Lq
+    value = ct_step * K * world / (ms_total * 1e-3)
+    hbm_gbs, hbm_src = measured_peaks()
+    sm_mhz = (clocks or {}).get("sm_mhz") or 2032.0
+    clock_src = "median sampled under load" if clocks and clocks.get("sm_mhz") else "max clock, unsampled"
+    fw = fwd_work(b, d, Lq, N)
+    cw = conv_work(b, d, Lq)
+    kern = {
+        "causal_conv1d_silu": dict(ms=round(conv_ms, 4), share=round(conv_ms / (ms_total / K), 4),
+                                   roofline=roofline(cw, conv_ms * 1e-3, hbm_gbs, sms, sm_mhz, hbm_src, clock_src)),
+        "ssm_scan_fwd": dict(ms=round(fwd_ms, 4), share=round(fwd_ms / (ms_total / K), 4),
+                             channel_tokens_per_s=round(ct_step / (fwd_ms * 1e-3), 1),
+                             roofline=roofline(fw, fwd_ms * 1e-3, hbm_gbs, sms, sm_mhz, hbm_src, clock_src)),
+    }
+    dominant = max(kern, key=lambda k: kern[k]["ms"])
+    roof = dict(kern[dominant]["roofline"])
+    roof["kernel"] = dominant
+    roof["traffic"] = None
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if args.e2e_steps > 0:
+        names_in = ("x", "dt", "z", "B", "C")
+        host = {k: torch.empty(g[k].shape, dtype=g[k].dtype, pin_memory=True) for k in names_in}
+        for k in names_in:
+            host[k].copy_(g[k])
+        y_host = torch.empty(g["y"].shape, dtype=g["y"].dtype, pin_memory=True)
+        h2d = sum(host[k].numel() * host[k].element_size() for k in names_in)
+        d2h = y_host.numel() * y_host.element_size()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.e2e_steps):
+            for k in names_in:
+                g[k].copy_(host[k], non_blocking=True)
+            step(L, g)
+            y_host.copy_(g["y"], non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, device)
+        e2e = {"value": round(ct_step * args.e2e_steps * world / (e2e_ms * 1e-3), 1), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+               "ms_per_step": round(e2e_ms / args.e2e_steps, 2)}
+        del host, y_host
+
+    decode = None
+    if not args.no_decode:
+        del g
+        torch.cuda.empty_cache()
+        decode = bench_decode(L, device, DECODE, DECODE["steps"])
+        decode["us_per_token_step"] = max_over_ranks(decode["us_per_token_step"], world, device)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(cfg, S.config_seed(2))
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": max(3, args.warmup), "ms_per_step": round(ms_total / K, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "io_dtype": "bf16", "data": "synthetic",
+            "config": workload_config(cfg),
+            "roofline": roof, "kernels": kern,
+            "fwd_gbs": kern["ssm_scan_fwd"]["roofline"]["hbm_gbs"],
+            "fwd_channel_tokens_per_s": kern["ssm_scan_fwd"]["channel_tokens_per_s"],
+            "decode": decode, "cpu_baseline": cpu, "e2e": e2e,
+            "clocks": clocks, "gpu_launches": launches, "gpu": props.name,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,224 @@
+/*
+ * ssm.h -- C ABI of libssm.so, the selective state-space (S6, "Mamba-1")
+ * hot path on NVIDIA B300 (sm_103a).
+ *
+ * What the library computes (notation of the pages on the selective state
+ * space model; b = batch index, d = channel, t = time step, n = state index):
+ *
+ *   delta_t = softplus(dt_t + bias_d)            (or dt_t + bias_d)
+ *   Abar    = exp(delta_t * A[d,n])
+ *   Bbar    = (exp(delta_t*A[d,n]) - 1)/A[d,n] * B[b,n,t]   zero-order hold
+ *           = delta_t * B[b,n,t]                           simplified rule
+ *   h[n]    = Abar * h[n] + Bbar * u_t                     (fp32 state)
+ *   y_t     = sum_n C[b,n,t] h[n] + D[d] u_t
+ *   out_t   = y_t * silu(z_t)                              (or y_t)
+ *
+ * Sources: "Mamba 模型" (gaos6e.github.io), the block flowchart's softplus,
+ * discretise, selective-scan, readout and gate nodes and the decode section
+ * ("为什么 Mamba 推理更省"); "Mamba 与状态空间模型" (world.lapla.si),
+ * section 07 (fused on-chip scan, the (B,D,L,N) state never written out,
+ * recompute in the backward) and section "模型省略了什么" (the simplified
+ * Bbar = Delta*B); mhpn.cn section 3.1 (Bbar = (Abar - I) A^-1 B).
+ *
+ * Conventions for every entry point
+ *  - All tensor pointers are DEVICE pointers owned by the caller.  The
+ *    library never allocates, frees or retains device memory.  Where an
+ *    entry point needs scratch space it says so and the caller passes a
+ *    workspace of at least the size the matching *_workspace_size() returns.
+ *  - Calls are asynchronous on the given stream (NULL = legacy default
+ *    stream).  Arguments are validated on the host before anything is
+ *    launched; a failed validation launches nothing and returns a negative
+ *    ssm_status.  Kernel launch errors are returned as SSM_ERR_CUDA.  The
+ *    library never aborts, traps or exits.  ssm_last_error() gives a
+ *    thread-local message for the last failure of the calling thread.
+ *  - Sequence tensors are (batch, rows, seqlen) with the seqlen stride equal
+ *    to 1; their batch and row strides are given in ELEMENTS.  Vectorised
+ *    (16-byte) access is used when the base pointer and both strides keep
+ *    every row 16-byte aligned; otherwise a slower scalar path runs.  No
+ *    other layout is accepted.
+ *  - Floating-point parameters (A, D, biases, weights) and recurrent states
+ *    are float32.  Activations are float32 or bfloat16 (ssm_dtype).
+ *  - Outputs are written, never accumulated into.
+ */
+#ifndef SSM_H
+#define SSM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SSM_API __attribute__((visibility("default")))
+#else
+#define SSM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; declared here so that this header does not
+ * need the CUDA headers. */
+typedef struct CUstream_st* ssm_stream_t;
+
+typedef enum {
+    SSM_OK = 0,
+    SSM_ERR_INVALID_ARG = -1, /* a NULL required pointer, a negative size, ... */
+    SSM_ERR_UNSUPPORTED = -2, /* a valid request this build does not implement */
+    SSM_ERR_MISALIGNED = -3,  /* a stride of the innermost (seqlen) axis is not 1 */
+    SSM_ERR_WORKSPACE = -4,   /* workspace missing or smaller than required */
+    SSM_ERR_CUDA = -5         /* a CUDA runtime error (see ssm_last_error) */
+} ssm_status;
+
+typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype;
+
+/* Bbar rule: zero-order hold, or the simplified Bbar = delta * B. */
+typedef enum { SSM_BBAR_ZOH = 0, SSM_BBAR_SIMPLE = 1 } ssm_bbar_mode;
+
+/* Element strides of the two outer axes of a (batch, rows, seqlen) tensor. */
+typedef struct {
+    int64_t batch;
+    int64_t row;
+} ssm_strides;
+
+/* ------------------------------------------------------------------------
+ * Selective scan, forward (fused discretisation + recurrence + readout +
+ * gate; the per-step state never leaves the chip).
+ * "Mamba 模型", flowchart nodes softplus .. gate; world.lapla.si section 07.
+ *
+ *   u, delta, z, out : (batch, dim, seqlen)   in_dtype (out: out_dtype)
+ *   B, C             : (batch, dstate, seqlen) in_dtype, shared by all d
+ *   A                : (dim, dstate) float32, contiguous
+ *   D, delta_bias    : (dim) float32 or NULL (= 0)
+ *   z                : NULL = no gate
+ *   h0               : (batch, dim, dstate) float32 contiguous or NULL (= 0)
+ *   final_state      : (batch, dim, dstate) float32 contiguous or NULL
+ *   checkpoints      : (batch, dim, ceil(seqlen/K), dstate) float32
+ *                      contiguous or NULL; entry k holds the state before
+ *                      step k*K (entry 0 = h0).  K = checkpoint_every must be
+ *                      a positive multiple of 8 when checkpoints != NULL.
+ *                      ssm_scan_bwd can take these instead of recomputing.
+ * dstate: 1..16.  dim, batch >= 1; seqlen >= 0 (seqlen 0 only copies h0
+ * to final_state).
+ * Workspace: ssm_scan_fwd_workspace_size() bytes (0 for many shapes; the
+ * long-sequence schedule stores per-segment carries there).  Pointer
+ * must be 256-byte aligned when the size is non-zero.
+ * Accuracy: bfloat16 inputs use the SFU fast exponentials; float32
+ * inputs use correctly-rounded-class library exp/expm1/log1p.  A value
+ * A[d,n] == 0 is handled as the limit Bbar = delta * B. */
+typedef struct {
+    int64_t batch, dim, seqlen, dstate;
+    ssm_dtype in_dtype;
+    ssm_dtype out_dtype;
+    int bbar_mode;      /* ssm_bbar_mode */
+    int delta_softplus; /* 1: delta = softplus(dt + bias); 0: dt + bias */
+    const void* u;     ssm_strides u_strides;
+    const void* delta; ssm_strides delta_strides;
+    const void* z;     ssm_strides z_strides;
+    const void* B;     ssm_strides B_strides;
+    const void* C;     ssm_strides C_strides;
+    void* out;         ssm_strides out_strides;
+    const float* A;
+    const float* D;
+    const float* delta_bias;
+    const float* h0;
+    float* final_state;
+    float* checkpoints;
+    int64_t checkpoint_every;
+} ssm_scan_fwd_params;
+
+SSM_API size_t ssm_scan_fwd_workspace_size(const ssm_scan_fwd_params* p);
+SSM_API ssm_status ssm_scan_fwd(const ssm_scan_fwd_params* p, void* workspace,
+                        size_t workspace_bytes, ssm_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Single-token decode step: state <- update(state, x_t), then readout and
+ * gate for that token.  "Mamba 模型", section "为什么 Mamba 推理更省".
+ *
+ *   x, delta, z, out : (batch, dim), rows of length dim, batch stride in
+ *                      elements (x_stride etc.), unit dim stride.  x is the
+ *                      scan input u_t (the conv output).  z may be NULL.
+ *   B, C             : (batch, dstate), batch stride in elements
+ *   state            : (batch, dim, dstate) float32 contiguous, updated IN
+ *                      PLACE
+ *   A, D, delta_bias : as for ssm_scan_fwd
+ * Memory-bound: reads and writes the state once. */
+typedef struct {
+    int64_t batch, dim, dstate;
+    ssm_dtype in_dtype;
+    ssm_dtype out_dtype;
+    int bbar_mode;
+    int delta_softplus;
+    const void* x;     int64_t x_stride;
+    const void* delta; int64_t delta_stride;
+    const void* z;     int64_t z_stride;
+    const void* B;     int64_t B_stride;
+    const void* C;     int64_t C_stride;
+    void* out;         int64_t out_stride;
+    const float* A;
+    const float* D;
+    const float* delta_bias;
+    float* state;
+} ssm_state_update_params;
+
+SSM_API ssm_status ssm_state_update(const ssm_state_update_params* p, ssm_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Causal depthwise conv1d + SiLU over a sequence.
+ * "Mamba 模型" conv node Uc_t = sum_i W_i U_{t-i} (tap i = 0 is the current
+ * token) and SiLU node; world.lapla.si section 03 (the short conv keeps the
+ * last 4 inputs).
+ *
+ *   x, out     : (batch, dim, seqlen) dtype, strides as above
+ *   weight     : (dim, width) float32 contiguous; weight[d,i] multiplies
+ *                x[t-i].  (PyTorch's Conv1d stores the taps in the reverse
+ *                order.)
+ *   bias       : (dim) float32 or NULL
+ *   state_in   : (batch, dim, width) dtype contiguous or NULL: the `width`
+ *                inputs before t = 0, oldest first; NULL = zeros
+ *   state_out  : (batch, dim, width) dtype contiguous or NULL: the last
+ *                `width` inputs, oldest first (for a following decode)
+ * width: 1..4.  Memory-bound: reads x once, writes out once. */
+typedef struct {
+    int64_t batch, dim, seqlen, width;
+    ssm_dtype dtype;
+    const void* x;  ssm_strides x_strides;
+    void* out;      ssm_strides out_strides;
+    const float* weight;
+    const float* bias;
+    const void* state_in;
+    void* state_out;
+} ssm_conv_params;
+
+SSM_API ssm_status causal_conv1d_silu(const ssm_conv_params* p, ssm_stream_t stream);
+
+/* One-token conv update: shift x_t into the window, then conv + SiLU.
+ *   state : (batch, dim, width) dtype contiguous, oldest first, IN PLACE
+ *   x,out : (batch, dim), batch stride in elements, unit dim stride */
+typedef struct {
+    int64_t batch, dim, width;
+    ssm_dtype dtype;
+    const void* x;  int64_t x_stride;
+    void* out;      int64_t out_stride;
+    const float* weight;
+    const float* bias;
+    void* state;
+} ssm_conv_update_params;
+
+SSM_API ssm_status causal_conv1d_silu_update(const ssm_conv_update_params* p, ssm_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Human-readable name of a status code (static string). */
+SSM_API const char* ssm_status_string(ssm_status s);
+/* Message describing the calling thread's last failure ("" if none). */
+SSM_API const char* ssm_last_error(void);
+/* Library ABI version, incremented on any incompatible change. */
+SSM_API int ssm_abi_version(void);
+/* Number of CUDA kernels this library has launched in the process so far
+ * (all devices, all threads; a diagnostic for counting launches inside a
+ * timed region). */
+SSM_API uint64_t ssm_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SSM_H */

@@ -1,0 +1,334 @@
+"""Thin ctypes binding of libssm.so (declared in include/ssm.h).
+
+Argument marshalling only: every function below checks devices, dtypes and
+layouts, allocates the outputs (and a workspace, when the caller passes none)
+through PyTorch, fills the C parameter struct with device pointers, strides and
+the current CUDA stream, and calls the entry point of the same name.  All
+arithmetic happens in the library's CUDA kernels; there is no CPU or PyTorch
+fallback.  If libssm.so is missing the import fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libssm.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it with `python -m selective_state_space_147_b300.build` "
+        "(nvcc, sm_103a). There is no fallback implementation.")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+# ---- enums (include/ssm.h) -------------------------------------------------
+SSM_OK = 0
+SSM_F32, SSM_BF16 = 0, 1
+SSM_BBAR_ZOH, SSM_BBAR_SIMPLE = 0, 1
+STATUS_NAMES = {0: "SSM_OK", -1: "SSM_ERR_INVALID_ARG", -2: "SSM_ERR_UNSUPPORTED",
+                -3: "SSM_ERR_MISALIGNED", -4: "SSM_ERR_WORKSPACE", -5: "SSM_ERR_CUDA"}
+
+_i64, _int, _vp, _fp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p
+
+
+class Strides(ctypes.Structure):
+    _fields_ = [("batch", _i64), ("row", _i64)]
+
+
+class ScanFwdParams(ctypes.Structure):
+    _fields_ = [
+        ("batch", _i64), ("dim", _i64), ("seqlen", _i64), ("dstate", _i64),
+        ("in_dtype", _int), ("out_dtype", _int), ("bbar_mode", _int), ("delta_softplus", _int),
+        ("u", _vp), ("u_strides", Strides),
+        ("delta", _vp), ("delta_strides", Strides),
+        ("z", _vp), ("z_strides", Strides),
+        ("B", _vp), ("B_strides", Strides),
+        ("C", _vp), ("C_strides", Strides),
+        ("out", _vp), ("out_strides", Strides),
+        ("A", _fp), ("D", _fp), ("delta_bias", _fp), ("h0", _fp),
+        ("final_state", _fp), ("checkpoints", _fp), ("checkpoint_every", _i64),
+    ]
+
+
+class StateUpdateParams(ctypes.Structure):
+    _fields_ = [
+        ("batch", _i64), ("dim", _i64), ("dstate", _i64),
+        ("in_dtype", _int), ("out_dtype", _int), ("bbar_mode", _int), ("delta_softplus", _int),
+        ("x", _vp), ("x_stride", _i64),
+        ("delta", _vp), ("delta_stride", _i64),
+        ("z", _vp), ("z_stride", _i64),
+        ("B", _vp), ("B_stride", _i64),
+        ("C", _vp), ("C_stride", _i64),
+        ("out", _vp), ("out_stride", _i64),
+        ("A", _fp), ("D", _fp), ("delta_bias", _fp), ("state", _fp),
+    ]
+
+
+class ConvParams(ctypes.Structure):
+    _fields_ = [
+        ("batch", _i64), ("dim", _i64), ("seqlen", _i64), ("width", _i64),
+        ("dtype", _int),
+        ("x", _vp), ("x_strides", Strides),
+        ("out", _vp), ("out_strides", Strides),
+        ("weight", _fp), ("bias", _fp), ("state_in", _vp), ("state_out", _vp),
+    ]
+
+
+class ConvUpdateParams(ctypes.Structure):
+    _fields_ = [
+        ("batch", _i64), ("dim", _i64), ("width", _i64),
+        ("dtype", _int),
+        ("x", _vp), ("x_stride", _i64),
+        ("out", _vp), ("out_stride", _i64),
+        ("weight", _fp), ("bias", _fp), ("state", _vp),
+    ]
+
+
+_lib.ssm_scan_fwd_workspace_size.argtypes = [ctypes.POINTER(ScanFwdParams)]
+_lib.ssm_scan_fwd_workspace_size.restype = ctypes.c_size_t
+_lib.ssm_scan_fwd.argtypes = [ctypes.POINTER(ScanFwdParams), _vp, ctypes.c_size_t, _vp]
+_lib.ssm_scan_fwd.restype = _int
+_lib.ssm_state_update.argtypes = [ctypes.POINTER(StateUpdateParams), _vp]
+_lib.ssm_state_update.restype = _int
+_lib.causal_conv1d_silu.argtypes = [ctypes.POINTER(ConvParams), _vp]
+_lib.causal_conv1d_silu.restype = _int
+_lib.causal_conv1d_silu_update.argtypes = [ctypes.POINTER(ConvUpdateParams), _vp]
+_lib.causal_conv1d_silu_update.restype = _int
+_lib.ssm_status_string.argtypes = [_int]
+_lib.ssm_status_string.restype = ctypes.c_char_p
+_lib.ssm_last_error.argtypes = []
+_lib.ssm_last_error.restype = ctypes.c_char_p
+_lib.ssm_abi_version.argtypes = []
+_lib.ssm_abi_version.restype = _int
+_lib.ssm_launch_count.argtypes = []
+_lib.ssm_launch_count.restype = ctypes.c_uint64
+
+
+class SSMError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+def _check(status: int):
+    if status != SSM_OK:
+        raise SSMError(status, _lib.ssm_last_error().decode(errors="replace"))
+
+
+def lib() -> ctypes.CDLL:
+    return _lib
+
+
+def abi_version() -> int:
+    return _lib.ssm_abi_version()
+
+
+def launch_count() -> int:
+    """Kernels libssm.so has launched in this process so far."""
+    return int(_lib.ssm_launch_count())
+
+
+# ---- marshalling helpers -------------------------------------------------------
+def _dtype_code(t: torch.dtype) -> int:
+    if t == torch.float32:
+        return SSM_F32
+    if t == torch.bfloat16:
+        return SSM_BF16
+    raise TypeError(f"unsupported dtype {t} (float32 or bfloat16)")
+
+
+def _torch_dtype(code_or_dtype) -> torch.dtype:
+    if isinstance(code_or_dtype, torch.dtype):
+        return code_or_dtype
+    return torch.float32 if code_or_dtype == SSM_F32 else torch.bfloat16
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _need_cuda(name: str, t: Optional[torch.Tensor]):
+    if t is not None and not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+
+
+def _seq_strides(name: str, t: Optional[torch.Tensor]) -> Strides:
+    if t is None:
+        return Strides(0, 0)
+    if t.dim() != 3 or (t.shape[2] > 1 and t.stride(2) != 1):
+        raise ValueError(f"{name} must be 3-D with unit stride along the last axis")
+    return Strides(t.stride(0), t.stride(1))
+
+
+def _row_stride(name: str, t: Optional[torch.Tensor]) -> int:
+    if t is None:
+        return 0
+    if t.dim() != 2 or (t.shape[1] > 1 and t.stride(1) != 1):
+        raise ValueError(f"{name} must be 2-D with unit stride along the last axis")
+    return t.stride(0)
+
+
+def _f32c(name: str, t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if t.dtype != torch.float32 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous float32 tensor")
+    _need_cuda(name, t)
+    return t
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+# ---- entry points --------------------------------------------------------------
+def _fwd_params(u, delta, A, B, C, D, delta_bias, z, h0, bbar_mode, delta_softplus,
+                out, final_state, checkpoints, checkpoint_every) -> ScanFwdParams:
+    batch, dim, L = u.shape
+    N = A.shape[1]
+    p = ScanFwdParams()
+    p.batch, p.dim, p.seqlen, p.dstate = batch, dim, L, N
+    p.in_dtype = _dtype_code(u.dtype)
+    p.out_dtype = _dtype_code(out.dtype)
+    p.bbar_mode = int(bbar_mode)
+    p.delta_softplus = 1 if delta_softplus else 0
+    p.u, p.u_strides = _ptr(u), _seq_strides("u", u)
+    p.delta, p.delta_strides = _ptr(delta), _seq_strides("delta", delta)
+    p.z, p.z_strides = _ptr(z), _seq_strides("z", z)
+    p.B, p.B_strides = _ptr(B), _seq_strides("B", B)
+    p.C, p.C_strides = _ptr(C), _seq_strides("C", C)
+    p.out, p.out_strides = _ptr(out), _seq_strides("out", out)
+    p.A, p.D, p.delta_bias, p.h0 = _ptr(A), _ptr(D), _ptr(delta_bias), _ptr(h0)
+    p.final_state, p.checkpoints = _ptr(final_state), _ptr(checkpoints)
+    p.checkpoint_every = int(checkpoint_every)
+    return p
+
+
+def ssm_scan_fwd(u, delta, A, B, C, *, D=None, delta_bias=None, z=None, h0=None,
+                 bbar_mode: int = SSM_BBAR_ZOH, delta_softplus: bool = True,
+                 out: Optional[torch.Tensor] = None, out_dtype=None,
+                 final_state: Optional[torch.Tensor] = None, return_final_state: bool = False,
+                 checkpoints: Optional[torch.Tensor] = None, checkpoint_every: int = 0,
+                 workspace: Optional[torch.Tensor] = None, stream=None):
+    """Fused selective-scan forward.  u, delta, z: (batch, dim, L); B, C: (batch, N, L)
+    (same dtype as u); A: (dim, N) f32; D, delta_bias: (dim,) f32; h0: (batch, dim, N) f32.
+    Returns ``out`` (and the final state when requested)."""
+    for name, t in (("u", u), ("delta", delta), ("B", B), ("C", C), ("z", z)):
+        _need_cuda(name, t)
+        if t is not None and t.dtype != u.dtype:
+            raise ValueError(f"{name} must have the dtype of u")
+    A, D, delta_bias, h0 = (_f32c("A", A), _f32c("D", D), _f32c("delta_bias", delta_bias), _f32c("h0", h0))
+    batch, dim, L = u.shape
+    N = A.shape[1]
+    if out is None:
+        out = torch.empty(batch, dim, L, dtype=_torch_dtype(out_dtype or u.dtype), device=u.device)
+    if final_state is None and return_final_state:
+        final_state = torch.empty(batch, dim, N, dtype=torch.float32, device=u.device)
+    _f32c("final_state", final_state)
+    _f32c("checkpoints", checkpoints)
+    p = _fwd_params(u, delta, A, B, C, D, delta_bias, z, h0, bbar_mode, delta_softplus,
+                    out, final_state, checkpoints, checkpoint_every)
+    need = _lib.ssm_scan_fwd_workspace_size(ctypes.byref(p))
+    if need > 0 and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=u.device)
+    ws_ptr = _ptr(workspace)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_lib.ssm_scan_fwd(ctypes.byref(p), ws_ptr, ws_bytes, _stream(stream)))
+    if return_final_state:
+        return out, final_state
+    return out
+
+
+def ssm_scan_fwd_workspace_size(u, A, **kw) -> int:
+    """Workspace bytes ssm_scan_fwd needs for this problem shape."""
+    p = ScanFwdParams()
+    p.batch, p.dim, p.seqlen = u.shape
+    p.dstate = A.shape[1]
+    p.in_dtype = _dtype_code(u.dtype)
+    p.out_dtype = _dtype_code(kw.get("out_dtype", u.dtype))
+    p.bbar_mode = int(kw.get("bbar_mode", SSM_BBAR_ZOH))
+    p.delta_softplus = 1
+    p.u = p.delta = p.B = p.C = p.out = p.A = 1   # any non-NULL value: only sizes matter here
+    return _lib.ssm_scan_fwd_workspace_size(ctypes.byref(p))
+
+
+def ssm_state_update(state, x, delta, A, B, C, *, D=None, delta_bias=None, z=None,
+                     bbar_mode: int = SSM_BBAR_ZOH, delta_softplus: bool = True,
+                     out: Optional[torch.Tensor] = None, out_dtype=None, stream=None):
+    """One decode step; ``state`` (batch, dim, N) f32 is updated in place.
+    x, delta, z: (batch, dim); B, C: (batch, N).  Returns out (batch, dim)."""
+    for name, t in (("x", x), ("delta", delta), ("B", B), ("C", C), ("z", z)):
+        _need_cuda(name, t)
+    _f32c("state", state)
+    A, D, delta_bias = _f32c("A", A), _f32c("D", D), _f32c("delta_bias", delta_bias)
+    batch, dim = x.shape
+    if out is None:
+        out = torch.empty(batch, dim, dtype=_torch_dtype(out_dtype or x.dtype), device=x.device)
+    p = StateUpdateParams()
+    p.batch, p.dim, p.dstate = batch, dim, A.shape[1]
+    p.in_dtype, p.out_dtype = _dtype_code(x.dtype), _dtype_code(out.dtype)
+    p.bbar_mode, p.delta_softplus = int(bbar_mode), 1 if delta_softplus else 0
+    p.x, p.x_stride = _ptr(x), _row_stride("x", x)
+    p.delta, p.delta_stride = _ptr(delta), _row_stride("delta", delta)
+    p.z, p.z_stride = _ptr(z), _row_stride("z", z)
+    p.B, p.B_stride = _ptr(B), _row_stride("B", B)
+    p.C, p.C_stride = _ptr(C), _row_stride("C", C)
+    p.out, p.out_stride = _ptr(out), _row_stride("out", out)
+    p.A, p.D, p.delta_bias, p.state = _ptr(A), _ptr(D), _ptr(delta_bias), _ptr(state)
+    _check(_lib.ssm_state_update(ctypes.byref(p), _stream(stream)))
+    return out
+
+
+def causal_conv1d_silu(x, weight, *, bias=None, state_in=None, state_out=None,
+                       out: Optional[torch.Tensor] = None, stream=None):
+    """Causal depthwise conv + SiLU.  x: (batch, dim, L); weight: (dim, W) f32 with
+    weight[d, i] multiplying x[t - i]; state_in/state_out: (batch, dim, W) windows."""
+    _need_cuda("x", x)
+    weight, bias = _f32c("weight", weight), _f32c("bias", bias)
+    batch, dim, L = x.shape
+    if out is None:
+        out = torch.empty_like(x, memory_format=torch.contiguous_format)
+    for name, t in (("state_in", state_in), ("state_out", state_out)):
+        if t is not None:
+            _need_cuda(name, t)
+            if t.dtype != x.dtype or not t.is_contiguous():
+                raise ValueError(f"{name} must be contiguous with the dtype of x")
+    p = ConvParams()
+    p.batch, p.dim, p.seqlen, p.width = batch, dim, L, weight.shape[1]
+    p.dtype = _dtype_code(x.dtype)
+    p.x, p.x_strides = _ptr(x), _seq_strides("x", x)
+    p.out, p.out_strides = _ptr(out), _seq_strides("out", out)
+    p.weight, p.bias = _ptr(weight), _ptr(bias)
+    p.state_in, p.state_out = _ptr(state_in), _ptr(state_out)
+    _check(_lib.causal_conv1d_silu(ctypes.byref(p), _stream(stream)))
+    return out
+
+
+def causal_conv1d_silu_update(state, x, weight, *, bias=None, out: Optional[torch.Tensor] = None,
+                              stream=None):
+    """One-token conv update; ``state`` (batch, dim, W) is shifted in place.
+    x: (batch, dim).  Returns out (batch, dim)."""
+    _need_cuda("x", x)
+    _need_cuda("state", state)
+    weight, bias = _f32c("weight", weight), _f32c("bias", bias)
+    if state.dtype != x.dtype or not state.is_contiguous():
+        raise ValueError("state must be contiguous with the dtype of x")
+    batch, dim = x.shape
+    if out is None:
+        out = torch.empty(batch, dim, dtype=x.dtype, device=x.device)
+    p = ConvUpdateParams()
+    p.batch, p.dim, p.width = batch, dim, weight.shape[1]
+    p.dtype = _dtype_code(x.dtype)
+    p.x, p.x_stride = _ptr(x), _row_stride("x", x)
+    p.out, p.out_stride = _ptr(out), _row_stride("out", out)
+    p.weight, p.bias, p.state = _ptr(weight), _ptr(bias), _ptr(state)
+    _check(_lib.causal_conv1d_silu_update(ctypes.byref(p), _stream(stream)))
+    return out

@@ -1,0 +1,167 @@
+// api.cu -- the extern "C" entry points of libssm.so: argument validation,
+// error reporting and dispatch to the kernels.  See include/ssm.h.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include <atomic>
+
+#include "internal.h"
+
+namespace ssm {
+static std::atomic<unsigned long long> g_launches{0};
+void count_launches(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+static uint64_t ssm_launch_count_value() { return g_launches.load(std::memory_order_relaxed); }
+}  // namespace ssm
+
+namespace {
+
+thread_local char g_err[512] = {0};
+
+ssm_status fail(ssm_status s, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    std::vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+ssm_status ok() {
+    g_err[0] = 0;
+    return SSM_OK;
+}
+
+ssm_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(SSM_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool dtype_ok(ssm_dtype t) { return t == SSM_F32 || t == SSM_BF16; }
+
+ssm_status num_sms(int* out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    e = cudaDeviceGetAttribute(out, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    return SSM_OK;
+}
+
+ssm_status check_fwd(const ssm_scan_fwd_params* p) {
+    if (p == nullptr) return fail(SSM_ERR_INVALID_ARG, "params is NULL");
+    if (p->batch < 1 || p->dim < 1 || p->seqlen < 0 || p->dstate < 1)
+        return fail(SSM_ERR_INVALID_ARG, "bad sizes batch=%lld dim=%lld seqlen=%lld dstate=%lld",
+                    (long long)p->batch, (long long)p->dim, (long long)p->seqlen, (long long)p->dstate);
+    if (p->dstate > 16) return fail(SSM_ERR_UNSUPPORTED, "dstate=%lld > 16", (long long)p->dstate);
+    if (p->batch > 65535) return fail(SSM_ERR_UNSUPPORTED, "batch=%lld > 65535", (long long)p->batch);
+    if (!dtype_ok(p->in_dtype) || !dtype_ok(p->out_dtype)) return fail(SSM_ERR_INVALID_ARG, "unknown dtype");
+    if (p->bbar_mode != SSM_BBAR_ZOH && p->bbar_mode != SSM_BBAR_SIMPLE)
+        return fail(SSM_ERR_INVALID_ARG, "unknown bbar_mode %d", p->bbar_mode);
+    if (p->seqlen > 0) {
+        if (!p->u || !p->delta || !p->B || !p->C || !p->out || !p->A)
+            return fail(SSM_ERR_INVALID_ARG, "u, delta, B, C, out and A are required");
+    }
+    const ssm_strides* all[] = {&p->u_strides, &p->delta_strides, &p->z_strides, &p->B_strides,
+                                &p->C_strides, &p->out_strides};
+    for (const ssm_strides* s : all)
+        if (s->batch < 0 || s->row < 0) return fail(SSM_ERR_INVALID_ARG, "negative stride");
+    if (p->checkpoints != nullptr && (p->checkpoint_every <= 0 || p->checkpoint_every % 8 != 0))
+        return fail(SSM_ERR_UNSUPPORTED, "checkpoint_every=%lld must be a positive multiple of 8",
+                    (long long)p->checkpoint_every);
+    return SSM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ssm_status_string(ssm_status s) {
+    switch (s) {
+        case SSM_OK: return "SSM_OK";
+        case SSM_ERR_INVALID_ARG: return "SSM_ERR_INVALID_ARG";
+        case SSM_ERR_UNSUPPORTED: return "SSM_ERR_UNSUPPORTED";
+        case SSM_ERR_MISALIGNED: return "SSM_ERR_MISALIGNED";
+        case SSM_ERR_WORKSPACE: return "SSM_ERR_WORKSPACE";
+        case SSM_ERR_CUDA: return "SSM_ERR_CUDA";
+    }
+    return "SSM_ERR_UNKNOWN";
+}
+
+const char* ssm_last_error(void) { return g_err; }
+
+int ssm_abi_version(void) { return 1; }
+
+uint64_t ssm_launch_count(void) { return ssm::ssm_launch_count_value(); }
+
+size_t ssm_scan_fwd_workspace_size(const ssm_scan_fwd_params* p) {
+    if (check_fwd(p) != SSM_OK) return 0;
+    int sms = 0;
+    if (num_sms(&sms) != SSM_OK) return 0;
+    return ssm::fwd_workspace_bytes(p, sms);
+}
+
+ssm_status ssm_scan_fwd(const ssm_scan_fwd_params* p, void* workspace, size_t workspace_bytes,
+                        ssm_stream_t stream) {
+    ssm_status s = check_fwd(p);
+    if (s != SSM_OK) return s;
+    int sms = 0;
+    if ((s = num_sms(&sms)) != SSM_OK) return s;
+    const size_t need = ssm::fwd_workspace_bytes(p, sms);
+    if (need > 0) {
+        if (workspace == nullptr || workspace_bytes < need)
+            return fail(SSM_ERR_WORKSPACE, "workspace of %zu bytes required, got %zu", need,
+                        workspace == nullptr ? (size_t)0 : workspace_bytes);
+        if ((uintptr_t)workspace % 256 != 0) return fail(SSM_ERR_MISALIGNED, "workspace must be 256-byte aligned");
+    }
+    cudaError_t e = ssm::launch_scan_fwd(p, workspace, sms, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "ssm_scan_fwd launch");
+    return ok();
+}
+
+ssm_status causal_conv1d_silu(const ssm_conv_params* p, ssm_stream_t stream) {
+    if (p == nullptr) return fail(SSM_ERR_INVALID_ARG, "params is NULL");
+    if (p->batch < 1 || p->dim < 1 || p->seqlen < 0 || p->width < 1)
+        return fail(SSM_ERR_INVALID_ARG, "bad sizes");
+    if (p->width > 4) return fail(SSM_ERR_UNSUPPORTED, "width=%lld > 4", (long long)p->width);
+    if (p->batch > 65535 || p->dim > 65535) return fail(SSM_ERR_UNSUPPORTED, "batch or dim > 65535");
+    if (!dtype_ok(p->dtype)) return fail(SSM_ERR_INVALID_ARG, "unknown dtype");
+    if (!p->weight || (p->seqlen > 0 && (!p->x || !p->out)))
+        return fail(SSM_ERR_INVALID_ARG, "x, out and weight are required");
+    if (p->x_strides.batch < 0 || p->x_strides.row < 0 || p->out_strides.batch < 0 || p->out_strides.row < 0)
+        return fail(SSM_ERR_INVALID_ARG, "negative stride");
+    cudaError_t e = ssm::launch_conv1d_silu(p, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "causal_conv1d_silu launch");
+    return ok();
+}
+
+ssm_status causal_conv1d_silu_update(const ssm_conv_update_params* p, ssm_stream_t stream) {
+    if (p == nullptr) return fail(SSM_ERR_INVALID_ARG, "params is NULL");
+    if (p->batch < 1 || p->dim < 1 || p->width < 1) return fail(SSM_ERR_INVALID_ARG, "bad sizes");
+    if (p->width > 4) return fail(SSM_ERR_UNSUPPORTED, "width=%lld > 4", (long long)p->width);
+    if (!dtype_ok(p->dtype)) return fail(SSM_ERR_INVALID_ARG, "unknown dtype");
+    if (!p->x || !p->out || !p->weight || !p->state)
+        return fail(SSM_ERR_INVALID_ARG, "x, out, weight and state are required");
+    if (p->x_stride < 0 || p->out_stride < 0) return fail(SSM_ERR_INVALID_ARG, "negative stride");
+    cudaError_t e = ssm::launch_conv1d_silu_update(p, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "causal_conv1d_silu_update launch");
+    return ok();
+}
+
+ssm_status ssm_state_update(const ssm_state_update_params* p, ssm_stream_t stream) {
+    if (p == nullptr) return fail(SSM_ERR_INVALID_ARG, "params is NULL");
+    if (p->batch < 1 || p->dim < 1 || p->dstate < 1) return fail(SSM_ERR_INVALID_ARG, "bad sizes");
+    if (p->dstate > 16) return fail(SSM_ERR_UNSUPPORTED, "dstate=%lld > 16", (long long)p->dstate);
+    if (!dtype_ok(p->in_dtype) || !dtype_ok(p->out_dtype)) return fail(SSM_ERR_INVALID_ARG, "unknown dtype");
+    if (p->bbar_mode != SSM_BBAR_ZOH && p->bbar_mode != SSM_BBAR_SIMPLE)
+        return fail(SSM_ERR_INVALID_ARG, "unknown bbar_mode %d", p->bbar_mode);
+    if (!p->x || !p->delta || !p->B || !p->C || !p->out || !p->A || !p->state)
+        return fail(SSM_ERR_INVALID_ARG, "x, delta, B, C, out, A and state are required");
+    if (p->x_stride < 0 || p->delta_stride < 0 || p->z_stride < 0 || p->B_stride < 0 || p->C_stride < 0 ||
+        p->out_stride < 0)
+        return fail(SSM_ERR_INVALID_ARG, "negative stride");
+    cudaError_t e = ssm::launch_state_update(p, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "ssm_state_update launch");
+    return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,175 @@
+// conv.cu -- causal depthwise conv1d + SiLU (sequence and one-token update).
+//
+// "Mamba 模型" flowchart: conv node Uc_t = sum_i W_i U_{t-i} (tap 0 is the
+// current token), SiLU node Xc_t = Uc_t sigmoid(Uc_t); world.lapla.si section
+// 03: the short conv keeps the last 4 inputs (the decode window).
+//
+// Both kernels are HBM-streaming: each input element is read once and each
+// output written once, with 16-byte vectors along L.  A thread owns 16
+// consecutive steps of one row; the 3-step halo comes from the neighbouring
+// lane by shuffle (lane 0 of a warp loads its halo itself, or takes it from the
+// caller's window at t = 0).
+#include <cstdint>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace ssm {
+
+constexpr int kConvPerThread = 16;
+constexpr int kConvThreads = 128;
+
+struct ConvArgs {
+    int64_t batch, dim, seqlen;
+    int width;
+    const void* x; void* out;
+    int64_t sx_b, sx_d, so_b, so_d;
+    const float* w; const float* bias;
+    const void* state_in; void* state_out;
+    int vec_x, vec_out;
+};
+
+template <typename T, bool ACC>
+__global__ void __launch_bounds__(kConvThreads)
+conv1d_silu_kernel(const ConvArgs a) {
+    const int64_t d = blockIdx.y;
+    const int64_t b = blockIdx.z;
+    const int lane = threadIdx.x & 31;
+    const int64_t t0 = ((int64_t)blockIdx.x * kConvThreads + threadIdx.x) * kConvPerThread;
+    const T* xrow = reinterpret_cast<const T*>(a.x) + b * a.sx_b + d * a.sx_d;
+    T* orow = reinterpret_cast<T*>(a.out) + b * a.so_b + d * a.so_d;
+    const T* sin = a.state_in ? reinterpret_cast<const T*>(a.state_in) + (b * a.dim + d) * a.width : nullptr;
+
+    // this thread's 16 inputs (zero past the end)
+    float xv[kConvPerThread];
+    const int64_t rem = a.seqlen - t0;
+    const int lim0 = rem <= 0 ? 0 : (rem >= 8 ? 8 : (int)rem);
+    const int lim1 = rem - 8 <= 0 ? 0 : (rem - 8 >= 8 ? 8 : (int)(rem - 8));
+    if (lim0 > 0) load8<T>(xrow + t0, lim0, a.vec_x, xv);
+    else for (int j = 0; j < 8; j++) xv[j] = 0.f;
+    if (lim1 > 0) load8<T>(xrow + t0 + 8, lim1, a.vec_x, xv + 8);
+    else for (int j = 8; j < 16; j++) xv[j] = 0.f;
+
+    // halo: x[t0-3], x[t0-2], x[t0-1]
+    float h3 = __shfl_up_sync(0xffffffffu, xv[13], 1);
+    float h2 = __shfl_up_sync(0xffffffffu, xv[14], 1);
+    float h1 = __shfl_up_sync(0xffffffffu, xv[15], 1);
+    if (lane == 0) {
+        float hv[3];
+        for (int k = 0; k < 3; k++) {
+            const int64_t tt = t0 - 3 + k;
+            float v = 0.f;
+            if (tt >= 0 && tt < a.seqlen) v = Elem<T>::load(xrow + tt);
+            else if (tt < 0 && sin != nullptr && tt >= -(int64_t)a.width) v = Elem<T>::load(sin + a.width + tt);
+            hv[k] = v;
+        }
+        h3 = hv[0]; h2 = hv[1]; h1 = hv[2];
+    }
+
+    float w[4];
+#pragma unroll
+    for (int i = 0; i < 4; i++) w[i] = (i < a.width) ? __ldg(a.w + d * a.width + i) : 0.f;
+    const float bias = a.bias ? __ldg(a.bias + d) : 0.f;
+
+    float ov[kConvPerThread];
+#pragma unroll
+    for (int j = 0; j < kConvPerThread; j++) {
+        const float xm1 = (j >= 1) ? xv[j - 1] : h1;
+        const float xm2 = (j >= 2) ? xv[j - 2] : (j == 1 ? h1 : h2);
+        const float xm3 = (j >= 3) ? xv[j - 3] : (j == 2 ? h1 : (j == 1 ? h2 : h3));
+        float acc = fmaf(w[0], xv[j], bias);
+        acc = fmaf(w[1], xm1, acc);
+        acc = fmaf(w[2], xm2, acc);
+        acc = fmaf(w[3], xm3, acc);
+        ov[j] = ACC ? silu_accurate(acc) : silu_fast(acc);
+    }
+    if (lim0 > 0) store8<T>(orow + t0, lim0, a.vec_out, ov);
+    if (lim1 > 0) store8<T>(orow + t0 + 8, lim1, a.vec_out, ov + 8);
+
+    // window for a following decode: the last `width` inputs, oldest first.
+    if (blockIdx.x == 0 && a.state_out != nullptr) {
+        float v = 0.f;
+        const int k = threadIdx.x;
+        if (k < a.width) {
+            const int64_t tt = a.seqlen - a.width + k;
+            if (tt >= 0) v = Elem<T>::load(xrow + tt);
+            else if (sin != nullptr) v = Elem<T>::load(sin + a.width + tt);
+        }
+        __syncthreads();   // every read of state_in in this block is done
+        if (k < a.width)
+            Elem<T>::store(reinterpret_cast<T*>(a.state_out) + (b * a.dim + d) * a.width + k, v);
+    }
+}
+
+static bool aligned16(const void* ptr, int64_t s0, int64_t s1, int esize) {
+    return ((uintptr_t)ptr % 16 == 0) && ((s0 * esize) % 16 == 0) && ((s1 * esize) % 16 == 0);
+}
+
+cudaError_t launch_conv1d_silu(const ssm_conv_params* p, cudaStream_t st) {
+    ConvArgs a;
+    a.batch = p->batch; a.dim = p->dim; a.seqlen = p->seqlen; a.width = (int)p->width;
+    a.x = p->x; a.out = p->out;
+    a.sx_b = p->x_strides.batch; a.sx_d = p->x_strides.row;
+    a.so_b = p->out_strides.batch; a.so_d = p->out_strides.row;
+    a.w = p->weight; a.bias = p->bias; a.state_in = p->state_in; a.state_out = p->state_out;
+    const int esz = p->dtype == SSM_BF16 ? 2 : 4;
+    a.vec_x = p->x ? aligned16(p->x, a.sx_b, a.sx_d, esz) : 0;
+    a.vec_out = p->out ? aligned16(p->out, a.so_b, a.so_d, esz) : 0;
+    const int64_t per_block = (int64_t)kConvThreads * kConvPerThread;
+    int64_t gx = ceil_div(p->seqlen, per_block);
+    if (gx < 1) gx = 1;   // seqlen 0 still writes the window
+    const dim3 grid((unsigned)gx, (unsigned)p->dim, (unsigned)p->batch);
+    if (p->dtype == SSM_BF16) conv1d_silu_kernel<__nv_bfloat16, false><<<grid, kConvThreads, 0, st>>>(a);
+    else conv1d_silu_kernel<float, true><<<grid, kConvThreads, 0, st>>>(a);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// One-token update: state (batch, dim, width) oldest first, shifted in place.
+struct ConvUpdArgs {
+    int64_t batch, dim;
+    int width;
+    const void* x; void* out; int64_t sx, so;
+    const float* w; const float* bias;
+    void* state;
+};
+
+template <typename T, bool ACC>
+__global__ void conv1d_silu_update_kernel(const ConvUpdArgs a) {
+    const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= a.batch * a.dim) return;
+    const int64_t b = c / a.dim, d = c % a.dim;
+    T* s = reinterpret_cast<T*>(a.state) + c * a.width;
+    const float xt = Elem<T>::load(reinterpret_cast<const T*>(a.x) + b * a.sx + d);
+    float win[4];
+#pragma unroll
+    for (int k = 0; k < 4; k++) win[k] = (k + 1 < a.width) ? Elem<T>::load(s + k + 1) : 0.f;
+    // new window: [s1 .. s_{W-1}, x_t]
+    float acc = a.bias ? __ldg(a.bias + d) : 0.f;
+    acc = fmaf(__ldg(a.w + d * a.width + 0), xt, acc);
+#pragma unroll
+    for (int i = 1; i < 4; i++)
+        if (i < a.width) acc = fmaf(__ldg(a.w + d * a.width + i), win[a.width - 1 - i], acc);
+#pragma unroll
+    for (int k = 0; k < 4; k++)
+        if (k + 1 < a.width) Elem<T>::store(s + k, win[k]);
+    Elem<T>::store(s + a.width - 1, xt);
+    const float o = ACC ? silu_accurate(acc) : silu_fast(acc);
+    Elem<T>::store(reinterpret_cast<T*>(a.out) + b * a.so + d, o);
+}
+
+cudaError_t launch_conv1d_silu_update(const ssm_conv_update_params* p, cudaStream_t st) {
+    ConvUpdArgs a;
+    a.batch = p->batch; a.dim = p->dim; a.width = (int)p->width;
+    a.x = p->x; a.out = p->out; a.sx = p->x_stride; a.so = p->out_stride;
+    a.w = p->weight; a.bias = p->bias; a.state = p->state;
+    const int64_t n = p->batch * p->dim;
+    const unsigned blocks = (unsigned)ceil_div(n, 256);
+    if (p->dtype == SSM_BF16) conv1d_silu_update_kernel<__nv_bfloat16, false><<<blocks, 256, 0, st>>>(a);
+    else conv1d_silu_update_kernel<float, true><<<blocks, 256, 0, st>>>(a);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace ssm

@@ -1,0 +1,129 @@
+// decode.cu -- single-token selective-scan step (recurrent inference).
+//
+// "Mamba 模型", section "为什么 Mamba 推理更省": per token only the fixed-size
+// state is updated, state <- update(state, x_t); the update is the scan node
+// for one t followed by the readout and gate nodes.  world.lapla.si section
+// 03: the state is dim x 16 numbers per layer, independent of context length.
+//
+// HBM-bound: the kernel reads and writes the fp32 state once (128 bytes per
+// channel for N = 16).  Four lanes share a channel, each owning four state
+// entries, so a warp reads 512 contiguous state bytes per instruction; the
+// readout is reduced over the four lanes with two xor shuffles.
+#include <cstdint>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace ssm {
+
+struct DecArgs {
+    int64_t batch, dim;
+    int dstate;
+    const void* x; const void* dt; const void* z; const void* B; const void* C; void* out;
+    int64_t sx, sdt, sz, sB, sC, so;
+    const float* A; const float* D; const float* bias;
+    float* state;
+    int softplus;
+};
+
+template <typename Tin, typename Tout, bool ZOH, bool ACC>
+__global__ void __launch_bounds__(256) state_update_kernel(const DecArgs a) {
+    constexpr int G = 4, NPL = 4;
+    const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t chan_raw = gid / G;
+    const int g = (int)(gid % G);
+    const bool active = chan_raw < a.batch * a.dim;
+    const int64_t chan = active ? chan_raw : 0;
+    const int64_t b = chan / a.dim, d = chan % a.dim;
+
+    const float xt = Elem<Tin>::load(reinterpret_cast<const Tin*>(a.x) + b * a.sx + d);
+    const float v = Elem<Tin>::load(reinterpret_cast<const Tin*>(a.dt) + b * a.sdt + d) +
+                    (a.bias ? __ldg(a.bias + d) : 0.f);
+    const float dl = a.softplus ? (ACC ? softplus_accurate(v) : softplus_fast(v)) : v;
+
+    float* st = a.state + chan * a.dstate;
+    const bool full = (a.dstate == 16) && (((uintptr_t)a.state & 15) == 0);
+    float h[NPL];
+    if (full) {
+        const float4 q = *reinterpret_cast<const float4*>(st + g * NPL);
+        h[0] = q.x; h[1] = q.y; h[2] = q.z; h[3] = q.w;
+    } else {
+#pragma unroll
+        for (int j = 0; j < NPL; j++) {
+            const int n = g * NPL + j;
+            h[j] = (n < a.dstate) ? st[n] : 0.f;
+        }
+    }
+    float y = 0.f;
+#pragma unroll
+    for (int j = 0; j < NPL; j++) {
+        const int n = g * NPL + j;
+        if (n < a.dstate) {
+            const float Av = __ldg(a.A + d * a.dstate + n);
+            const float Bv = Elem<Tin>::load(reinterpret_cast<const Tin*>(a.B) + b * a.sB + n);
+            const float Cv = Elem<Tin>::load(reinterpret_cast<const Tin*>(a.C) + b * a.sC + n);
+            const float x = dl * Av;
+            float ab, coef;
+            if (ACC) {
+                ab = expf(x);
+                coef = ZOH ? (Av != 0.f ? expm1f(x) / Av : dl) : dl;
+            } else {
+                ab = ex2_approx(x * kLog2e);
+                coef = ZOH ? (Av != 0.f ? (ab - 1.f) / Av : dl) : dl;
+            }
+            h[j] = fmaf(ab, h[j], coef * Bv * xt);
+            y = fmaf(Cv, h[j], y);
+        }
+    }
+    y += __shfl_xor_sync(0xffffffffu, y, 1);
+    y += __shfl_xor_sync(0xffffffffu, y, 2);
+    if (!active) return;
+    if (full) {
+        *reinterpret_cast<float4*>(st + g * NPL) = make_float4(h[0], h[1], h[2], h[3]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < NPL; j++) {
+            const int n = g * NPL + j;
+            if (n < a.dstate) st[n] = h[j];
+        }
+    }
+    if (g == 0) {
+        y = fmaf(a.D ? __ldg(a.D + d) : 0.f, xt, y);
+        if (a.z != nullptr) {
+            const float zt = Elem<Tin>::load(reinterpret_cast<const Tin*>(a.z) + b * a.sz + d);
+            y *= ACC ? silu_accurate(zt) : silu_fast(zt);
+        }
+        Elem<Tout>::store(reinterpret_cast<Tout*>(a.out) + b * a.so + d, y);
+    }
+}
+
+template <typename Tin, typename Tout>
+static void launch_typed(const DecArgs& a, bool zoh, unsigned blocks, cudaStream_t st) {
+    constexpr bool ACC = sizeof(Tin) == 4;
+    if (zoh) state_update_kernel<Tin, Tout, true, ACC><<<blocks, 256, 0, st>>>(a);
+    else state_update_kernel<Tin, Tout, false, ACC><<<blocks, 256, 0, st>>>(a);
+}
+
+cudaError_t launch_state_update(const ssm_state_update_params* p, cudaStream_t st) {
+    DecArgs a;
+    a.batch = p->batch; a.dim = p->dim; a.dstate = (int)p->dstate;
+    a.x = p->x; a.dt = p->delta; a.z = p->z; a.B = p->B; a.C = p->C; a.out = p->out;
+    a.sx = p->x_stride; a.sdt = p->delta_stride; a.sz = p->z_stride; a.sB = p->B_stride;
+    a.sC = p->C_stride; a.so = p->out_stride;
+    a.A = p->A; a.D = p->D; a.bias = p->delta_bias; a.state = p->state;
+    a.softplus = p->delta_softplus ? 1 : 0;
+    const int64_t threads = p->batch * p->dim * 4;
+    const unsigned blocks = (unsigned)ceil_div(threads, 256);
+    const bool zoh = p->bbar_mode == SSM_BBAR_ZOH;
+    if (p->in_dtype == SSM_BF16) {
+        if (p->out_dtype == SSM_BF16) launch_typed<__nv_bfloat16, __nv_bfloat16>(a, zoh, blocks, st);
+        else launch_typed<__nv_bfloat16, float>(a, zoh, blocks, st);
+    } else {
+        if (p->out_dtype == SSM_BF16) launch_typed<float, __nv_bfloat16>(a, zoh, blocks, st);
+        else launch_typed<float, float>(a, zoh, blocks, st);
+    }
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace ssm

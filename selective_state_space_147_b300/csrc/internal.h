@@ -1,0 +1,20 @@
+// internal.h -- declarations shared by the libssm translation units (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstddef>
+
+#include "ssm.h"
+
+namespace ssm {
+
+// Adds n to the process-wide launch counter reported by ssm_launch_count().
+void count_launches(unsigned n);
+
+size_t fwd_workspace_bytes(const ssm_scan_fwd_params* p, int num_sms);
+cudaError_t launch_scan_fwd(const ssm_scan_fwd_params* p, void* ws, int num_sms, cudaStream_t st);
+cudaError_t launch_conv1d_silu(const ssm_conv_params* p, cudaStream_t st);
+cudaError_t launch_conv1d_silu_update(const ssm_conv_update_params* p, cudaStream_t st);
+cudaError_t launch_state_update(const ssm_state_update_params* p, cudaStream_t st);
+
+}  // namespace ssm

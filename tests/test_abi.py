@@ -1,0 +1,83 @@
+"""The C-ABI library loads on a machine without a GPU, exports every entry point
+include/*.h declares, and rejects bad arguments on the host before touching CUDA."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+LIB = os.path.join(ROOT, "selective_state_space_147_b300", "libssm.so")
+
+
+def declared_functions():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        names += re.findall(r"SSM_API\s+[\w\s\*]+?\b(\w+)\s*\(", src)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(LIB):
+        from selective_state_space_147_b300 import build
+        build.build()
+    return ctypes.CDLL(LIB)
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for must in ("ssm_scan_fwd", "ssm_scan_fwd_workspace_size", "ssm_state_update",
+                 "causal_conv1d_silu", "causal_conv1d_silu_update", "ssm_status_string",
+                 "ssm_last_error", "ssm_abi_version"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings_and_version(lib):
+    lib.ssm_status_string.restype = ctypes.c_char_p
+    lib.ssm_status_string.argtypes = [ctypes.c_int]
+    names = {c: lib.ssm_status_string(c).decode() for c in (0, -1, -2, -3, -4, -5, -99)}
+    assert names[0] == "SSM_OK" and names[-1] == "SSM_ERR_INVALID_ARG"
+    assert names[-5] == "SSM_ERR_CUDA" and names[-99] == "SSM_ERR_UNKNOWN"
+    assert lib.ssm_abi_version() == 1
+
+
+def test_host_validation_without_gpu():
+    import selective_state_space_147_b300.binding as B
+    lib = B.lib()
+    # NULL parameter blocks
+    assert lib.ssm_scan_fwd(None, None, 0, None) == -1
+    assert lib.ssm_state_update(None, None) == -1
+    assert lib.causal_conv1d_silu(None, None) == -1
+    assert lib.causal_conv1d_silu_update(None, None) == -1
+    assert b"NULL" in lib.ssm_last_error()
+    # sizes
+    p = B.ScanFwdParams()
+    p.batch, p.dim, p.seqlen, p.dstate = 1, 1, 8, 17
+    assert lib.ssm_scan_fwd(ctypes.byref(p), None, 0, None) == -2      # dstate > 16
+    p.dstate = 0
+    assert lib.ssm_scan_fwd(ctypes.byref(p), None, 0, None) == -1
+    p.dstate = 16
+    assert lib.ssm_scan_fwd(ctypes.byref(p), None, 0, None) == -1      # missing pointers
+    p.u = p.delta = p.B = p.C = p.out = p.A = 16
+    p.bbar_mode = 7
+    assert lib.ssm_scan_fwd(ctypes.byref(p), None, 0, None) == -1
+    p.bbar_mode = 0
+    p.checkpoints, p.checkpoint_every = 16, 12
+    assert lib.ssm_scan_fwd(ctypes.byref(p), None, 0, None) == -2      # not a multiple of 8
+    p.checkpoint_every = 8
+    p.u_strides.row = -1
+    assert lib.ssm_scan_fwd(ctypes.byref(p), None, 0, None) == -1
+    c = B.ConvParams()
+    c.batch, c.dim, c.seqlen, c.width = 1, 1, 4, 5
+    assert lib.causal_conv1d_silu(ctypes.byref(c), None) == -2         # width > 4
+    s = B.StateUpdateParams()
+    s.batch, s.dim, s.dstate = 1, 1, 16
+    assert lib.ssm_state_update(ctypes.byref(s), None) == -1
