@@ -130,6 +130,27 @@ SSM_API size_t ssm_scan_fwd_workspace_size(const ssm_scan_fwd_params* p);
 SSM_API ssm_status ssm_scan_fwd(const ssm_scan_fwd_params* p, void* workspace,
                         size_t workspace_bytes, ssm_stream_t stream);
 
+/* ssm_scan_fwd for callers that cannot allocate device memory.  The pages
+ * have no counterpart to this entry point: it exists for callers that are
+ * not allowed to call cudaMalloc, such as a plugin inside an inference
+ * runtime that receives only its input and output buffers and must keep to
+ * a memory plan fixed at load time (an allocation can also synchronise the
+ * device), and that therefore cannot supply the workspace ssm_scan_fwd's
+ * long-sequence schedule needs.
+ * Same parameters, results and asynchrony as ssm_scan_fwd, but no workspace:
+ * the scratch is a 4 MiB array built into the library, reserved on every GPU
+ * that loads the library until the process exits.  The call allocates and
+ * frees nothing.
+ *  - A problem that needs more scratch than 4 MiB (ssm_scan_fwd_workspace_size
+ *    tells) returns SSM_ERR_UNSUPPORTED and launches nothing.
+ *  - All calls on a device share that array: calls that may overlap on the GPU
+ *    (other streams, other host threads) race on it and must be ordered by
+ *    the caller.  No part of the array needs clearing between calls.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture on the device. */
+SSM_API ssm_status ssm_scan_fwd_static_ws(const ssm_scan_fwd_params* p, ssm_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * Single-token decode step: state <- update(state, x_t), then readout and
  * gate for that token.  "Mamba 模型", section "为什么 Mamba 推理更省".

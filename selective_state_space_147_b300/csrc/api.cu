@@ -118,6 +118,22 @@ ssm_status ssm_scan_fwd(const ssm_scan_fwd_params* p, void* workspace, size_t wo
     return ok();
 }
 
+ssm_status ssm_scan_fwd_static_ws(const ssm_scan_fwd_params* p, ssm_stream_t stream) {
+    ssm_status s = check_fwd(p);
+    if (s != SSM_OK) return s;
+    int sms = 0;
+    if ((s = num_sms(&sms)) != SSM_OK) return s;
+    const size_t need = ssm::fwd_workspace_bytes(p, sms);
+    if (need > ssm::static_scratch_bytes())
+        return fail(SSM_ERR_UNSUPPORTED,
+                    "ssm_scan_fwd_static_ws: this problem needs %zu bytes of scratch, more than the "
+                    "%zu-byte built-in scratch array; use ssm_scan_fwd with a caller workspace",
+                    need, ssm::static_scratch_bytes());
+    cudaError_t e = ssm::launch_scan_fwd_static(p, sms, need, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "ssm_scan_fwd_static_ws");
+    return ok();
+}
+
 ssm_status causal_conv1d_silu(const ssm_conv_params* p, ssm_stream_t stream) {
     if (p == nullptr) return fail(SSM_ERR_INVALID_ARG, "params is NULL");
     if (p->batch < 1 || p->dim < 1 || p->seqlen < 0 || p->width < 1)
