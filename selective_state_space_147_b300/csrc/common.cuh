@@ -184,6 +184,60 @@ __device__ __forceinline__ float2 f2_fma(float2 a, float2 b, float2 c) {
     return d;
 }
 
+// ---- f32x2 values held in one 64-bit register ------------------------------
+// A `pf2` keeps two fp32 lanes in a single .b64 register, so state, constants
+// and shared-memory loads stay in aligned register pairs and feed the f32x2
+// instructions directly; only the SFU exponentials unpack them.
+typedef unsigned long long pf2;
+
+__device__ __forceinline__ pf2 pf2_make(float lo, float hi) {
+    pf2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ float pf2_lo(pf2 v) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+    return lo;
+}
+__device__ __forceinline__ float pf2_hi(pf2 v) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+    return hi;
+}
+__device__ __forceinline__ float pf2_sum(pf2 v) { return pf2_lo(v) + pf2_hi(v); }
+__device__ __forceinline__ pf2 pf2_mul(pf2 a, pf2 b) {
+    pf2 d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ pf2 pf2_add(pf2 a, pf2 b) {
+    pf2 d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ pf2 pf2_sub(pf2 a, pf2 b) {
+    pf2 d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ pf2 pf2_fma(pf2 a, pf2 b, pf2 c) {
+    pf2 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+// 2^x on each lane (SFU)
+__device__ __forceinline__ pf2 pf2_ex2(pf2 x) {
+    pf2 r;
+    asm("{.reg .f32 lo, hi;\n\t"
+        "mov.b64 {lo, hi}, %1;\n\t"
+        "ex2.approx.ftz.f32 lo, lo;\n\t"
+        "ex2.approx.ftz.f32 hi, hi;\n\t"
+        "mov.b64 %0, {lo, hi};}"
+        : "=l"(r) : "l"(x));
+    return r;
+}
+
 // ---- misc --------------------------------------------------------------------
 __host__ __device__ __forceinline__ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 

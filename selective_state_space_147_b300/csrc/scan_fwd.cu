@@ -34,347 +34,18 @@
 //    its carry-in and writes the outputs.
 #include <cstdint>
 #include <cstdlib>
-#include <cstdio>
 
-#include "common.cuh"
-#include "internal.h"
+#include "scan_fwd.cuh"
 
 namespace ssm {
 
-constexpr int kNMax = 16;     // state size handled per channel (padded)
-constexpr int kTile = 64;     // time steps per B/C shared-memory tile
-constexpr int kRow = 36;      // floats per staged time step: B[16] C[16] pad[4]
-constexpr int kSub = 8;       // time steps per vector load
-
-enum FwdMode { kFull = 0, kSummary = 1 };
-
-struct FwdArgs {
-    int64_t batch, dim, seqlen;
-    int dstate;
-    const void* u; const void* dt; const void* z; const void* B; const void* C; void* out;
-    int64_t su_b, su_d, sdt_b, sdt_d, sz_b, sz_d, sB_b, sB_n, sC_b, sC_n, so_b, so_d;
-    const float* A; const float* D; const float* bias; const float* h0;
-    float* final_state; float* ckpt; int64_t ckpt_K, n_ckpt;
-    int softplus;
-    int vec_u, vec_dt, vec_z, vec_out, vec_BC;
-    int64_t seg_len; int nseg;
-    float* ws_hend;    // (channels, nseg, 16)
-    float* ws_sdelta;  // (channels, nseg)
-    float* ws_carry;   // (channels, nseg, 16)
-};
-
-// Raw 8-element chunk of a row, kept packed until used.
-template <typename T> struct Raw8;
-template <> struct Raw8<__nv_bfloat16> {
-    uint4 w;
-    __device__ __forceinline__ void load(const __nv_bfloat16* p, int limit, bool vec) {
-        if (vec && limit >= 8) {
-            w = __ldg(reinterpret_cast<const uint4*>(p));
-        } else {
-            const unsigned short* q = reinterpret_cast<const unsigned short*>(p);
-            uint32_t e[8];
-#pragma unroll
-            for (int j = 0; j < 8; j++) e[j] = (j < limit) ? (uint32_t)__ldg(q + j) : 0u;
-            w.x = e[0] | (e[1] << 16); w.y = e[2] | (e[3] << 16);
-            w.z = e[4] | (e[5] << 16); w.w = e[6] | (e[7] << 16);
-        }
-    }
-    __device__ __forceinline__ float get(int j) const {
-        const uint32_t x = (j < 2) ? w.x : (j < 4) ? w.y : (j < 6) ? w.z : w.w;
-        return (j & 1) ? bf16hi(x) : bf16lo(x);
-    }
-};
-template <> struct Raw8<float> {
-    float4 a, b;
-    __device__ __forceinline__ void load(const float* p, int limit, bool vec) {
-        if (vec && limit >= 8) {
-            a = __ldg(reinterpret_cast<const float4*>(p));
-            b = __ldg(reinterpret_cast<const float4*>(p) + 1);
-        } else {
-            float e[8];
-#pragma unroll
-            for (int j = 0; j < 8; j++) e[j] = (j < limit) ? __ldg(p + j) : 0.f;
-            a = make_float4(e[0], e[1], e[2], e[3]);
-            b = make_float4(e[4], e[5], e[6], e[7]);
-        }
-    }
-    __device__ __forceinline__ float get(int j) const {
-        switch (j) {
-            case 0: return a.x; case 1: return a.y; case 2: return a.z; case 3: return a.w;
-            case 4: return b.x; case 5: return b.y; case 6: return b.z; default: return b.w;
-        }
-    }
-};
-
-// Stage B[b, :, t0 : t0+kTile] and C[...] into sbc as fp32 rows [t][B0..15 C0..15 pad].
-// Lane l fills time steps t0 + 2l and t0 + 2l + 1.  Entries past seqlen or
-// dstate are zero.
-template <typename Tin>
-__device__ __forceinline__ void stage_bc(float* sbc, const FwdArgs& a, const Tin* Bb, const Tin* Cb,
-                                         int64_t t0, int lane) {
-    const int64_t t = t0 + 2 * lane;
-    float bv[2][kNMax], cv[2][kNMax];
-#pragma unroll
-    for (int n = 0; n < kNMax; n++) {
-        bv[0][n] = bv[1][n] = cv[0][n] = cv[1][n] = 0.f;
-        if (n < a.dstate) {
-            const Tin* pb = Bb + n * a.sB_n + t;
-            const Tin* pc = Cb + n * a.sC_n + t;
-            if (a.vec_BC && t + 1 < a.seqlen) {
-                if constexpr (sizeof(Tin) == 2) {
-                    const uint32_t wb = __ldg(reinterpret_cast<const uint32_t*>(pb));
-                    const uint32_t wc = __ldg(reinterpret_cast<const uint32_t*>(pc));
-                    bv[0][n] = bf16lo(wb); bv[1][n] = bf16hi(wb);
-                    cv[0][n] = bf16lo(wc); cv[1][n] = bf16hi(wc);
-                } else {
-                    const float2 wb = __ldg(reinterpret_cast<const float2*>(pb));
-                    const float2 wc = __ldg(reinterpret_cast<const float2*>(pc));
-                    bv[0][n] = wb.x; bv[1][n] = wb.y; cv[0][n] = wc.x; cv[1][n] = wc.y;
-                }
-            } else {
-                if (t < a.seqlen) { bv[0][n] = Elem<Tin>::load(pb); cv[0][n] = Elem<Tin>::load(pc); }
-                if (t + 1 < a.seqlen) { bv[1][n] = Elem<Tin>::load(pb + 1); cv[1][n] = Elem<Tin>::load(pc + 1); }
-            }
-        }
-    }
-#pragma unroll
-    for (int r = 0; r < 2; r++) {
-        float4* row = reinterpret_cast<float4*>(sbc + (2 * lane + r) * kRow);
-#pragma unroll
-        for (int q = 0; q < kNMax / 4; q++) {
-            row[q] = make_float4(bv[r][4 * q], bv[r][4 * q + 1], bv[r][4 * q + 2], bv[r][4 * q + 3]);
-            row[4 + q] = make_float4(cv[r][4 * q], cv[r][4 * q + 1], cv[r][4 * q + 2], cv[r][4 * q + 3]);
-        }
-    }
+static int env_int(const char* name, int dflt) {
+    const char* s = std::getenv(name);
+    return (s && *s) ? std::atoi(s) : dflt;
 }
 
-// One warp: channels [d_base, d_base + 32/G) of batch row b, time steps
-// [t_begin, t_end).  Returns the state in h (this lane's NPL entries).
-template <typename Tin, typename Tout, int G, bool ZOH, bool ACC, bool HAS_Z, int MODE>
-__device__ __forceinline__ void scan_warp(const FwdArgs& a, float* sbc_all, int64_t b, int64_t d,
-                                          bool active, int lane, int64_t t_begin, int64_t t_end,
-                                          float (&h)[kNMax / G], float& sdelta_out) {
-    constexpr int NPL = kNMax / G;   // states per lane
-    constexpr int NP = NPL / 2;      // f32x2 pairs per lane
-    const int g = lane % G;
-    const int n_base = g * NPL;
-
-    // per-lane constants
-    float Ak[NPL];   // fast: A*log2(e); accurate: A
-    float Ik[NPL];   // fast ZOH: -1/A; accurate ZOH: 1/A (0 where A == 0)
-#pragma unroll
-    for (int j = 0; j < NPL; j++) {
-        const int n = n_base + j;
-        const float Av = (n < a.dstate) ? __ldg(a.A + d * a.dstate + n) : 0.f;
-        if constexpr (ACC) {
-            Ak[j] = Av;
-            Ik[j] = (Av != 0.f) ? 1.f / Av : 0.f;
-        } else {
-            Ak[j] = Av * kLog2e;
-            Ik[j] = (Av != 0.f) ? -1.f / Av : 0.f;
-        }
-    }
-    const float Dd = (a.D != nullptr) ? __ldg(a.D + d) : 0.f;
-    const float bias = (a.bias != nullptr) ? __ldg(a.bias + d) : 0.f;
-
-    const Tin* urow = reinterpret_cast<const Tin*>(a.u) + b * a.su_b + d * a.su_d;
-    const Tin* drow = reinterpret_cast<const Tin*>(a.dt) + b * a.sdt_b + d * a.sdt_d;
-    const Tin* zrow = HAS_Z ? reinterpret_cast<const Tin*>(a.z) + b * a.sz_b + d * a.sz_d : nullptr;
-    Tout* orow = (MODE == kFull) ? reinterpret_cast<Tout*>(a.out) + b * a.so_b + d * a.so_d : nullptr;
-    const Tin* Bb = reinterpret_cast<const Tin*>(a.B) + b * a.sB_b;
-    const Tin* Cb = reinterpret_cast<const Tin*>(a.C) + b * a.sC_b;
-    float* ck = (MODE == kFull && a.ckpt != nullptr)
-                    ? a.ckpt + (b * a.dim + d) * a.n_ckpt * a.dstate : nullptr;
-
-    // Kahan sum of delta (summary pass only)
-    float sd = 0.f, sd_c = 0.f;
-
-    // prefetch ring for u, dt, z
-    Raw8<Tin> ru[3], rd[3], rz[3];
-    auto load_sub = [&](int slot, int64_t t0) {
-        const int lim = (int)((t_end - t0) < 8 ? (t_end - t0) : 8);
-        if (t0 < t_end) {
-            ru[slot].load(urow + t0, lim, a.vec_u);
-            rd[slot].load(drow + t0, lim, a.vec_dt);
-            if constexpr (HAS_Z && MODE == kFull) rz[slot].load(zrow + t0, lim, a.vec_z);
-        }
-    };
-    load_sub(0, t_begin);
-    load_sub(1, t_begin + kSub);
-
-    for (int64_t tt = t_begin; tt < t_end; tt += kTile) {
-        __syncwarp();
-        stage_bc<Tin>(sbc_all, a, Bb, Cb, tt, lane);
-        __syncwarp();
-        const int64_t tile_end = (tt + kTile < t_end) ? tt + kTile : t_end;
-        for (int64_t t0 = tt; t0 < tile_end; t0 += kSub) {
-            // rotate the ring: slot 0 is current
-            load_sub(2, t0 + 2 * kSub);
-            const int cnt = (int)((tile_end - t0) < kSub ? (tile_end - t0) : kSub);
-            if (ck != nullptr && (t0 % a.ckpt_K) == 0 && active) {
-#pragma unroll
-                for (int j = 0; j < NPL; j++)
-                    if (n_base + j < a.dstate) ck[(t0 / a.ckpt_K) * a.dstate + n_base + j] = h[j];
-            }
-            float yout[kSub];
-#pragma unroll
-            for (int j = 0; j < kSub; j++) {
-                const float uj = ru[0].get(j);
-                const float v = rd[0].get(j) + bias;
-                float dl = a.softplus ? (ACC ? softplus_accurate(v) : softplus_fast(v)) : v;
-                const bool live = j < cnt;
-                if (!live) dl = 0.f;
-                const float* row = sbc_all + (t0 - tt + j) * kRow;
-                float y = 0.f;
-                if constexpr (ACC) {
-#pragma unroll
-                    for (int k = 0; k < NPL; k++) {
-                        const int n = n_base + k;
-                        const float x = dl * Ak[k];
-                        const float ab = expf(x);
-                        float coef;
-                        if constexpr (ZOH) coef = (Ik[k] != 0.f) ? expm1f(x) * Ik[k] : dl;
-                        else coef = dl;
-                        const float hn = fmaf(ab, h[k], coef * row[n] * uj);
-                        if (live) h[k] = hn;
-                        y = fmaf(row[16 + n], h[k], y);
-                    }
-                } else {
-                    const float2 dl2 = make_float2(dl, dl);
-                    const float2 u2 = ZOH ? make_float2(uj, uj) : make_float2(dl * uj, dl * uj);
-                    float2 y2 = make_float2(0.f, 0.f);
-#pragma unroll
-                    for (int p = 0; p < NP; p++) {
-                        const int n = n_base + 2 * p;
-                        const float2 Bp = *reinterpret_cast<const float2*>(row + n);
-                        const float2 x = f2_mul(dl2, make_float2(Ak[2 * p], Ak[2 * p + 1]));
-                        const float2 ab = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-                        float2 hp = make_float2(h[2 * p], h[2 * p + 1]);
-                        if constexpr (ZOH) {
-                            const float2 w = f2_mul(Bp, u2);
-                            const float2 kn = f2_mul(w, make_float2(Ik[2 * p], Ik[2 * p + 1]));  // -k
-                            const float2 s = f2_sub(hp, kn);                                      // h + k
-                            hp = f2_fma(ab, s, kn);                                               // Abar(h+k) - k
-                        } else {
-                            hp = f2_fma(ab, hp, f2_mul(Bp, u2));                                  // Abar h + delta B u
-                        }
-                        // steps past the end leave the state unchanged (dl = 0 gives
-                        // Abar = 1 and a zero input term; the select keeps it exact)
-                        if (live) { h[2 * p] = hp.x; h[2 * p + 1] = hp.y; }
-                        if constexpr (MODE == kFull) {
-                            const float2 Cp = *reinterpret_cast<const float2*>(row + 16 + n);
-                            y2 = f2_fma(Cp, make_float2(h[2 * p], h[2 * p + 1]), y2);
-                        }
-                    }
-                    y = y2.x + y2.y;
-                }
-                if constexpr (MODE == kSummary) {
-                    // compensated running sum of delta
-                    const float yk = dl - sd_c;
-                    const float tk = sd + yk;
-                    sd_c = (tk - sd) - yk;
-                    sd = tk;
-                }
-                if constexpr (MODE == kFull) {
-#pragma unroll
-                    for (int o = 1; o < G; o <<= 1) y += __shfl_xor_sync(0xffffffffu, y, o);
-                    y = fmaf(Dd, uj, y);
-                    if constexpr (HAS_Z) {
-                        const float zj = rz[0].get(j);
-                        y *= ACC ? silu_accurate(zj) : silu_fast(zj);
-                    }
-                    yout[j] = y;
-                }
-            }
-            if constexpr (MODE == kFull) {
-                if (active && g == 0) store8<Tout>(orow + t0, cnt, a.vec_out, yout);
-            }
-            ru[0] = ru[1]; rd[0] = rd[1]; ru[1] = ru[2]; rd[1] = rd[2];
-            if constexpr (HAS_Z && MODE == kFull) { rz[0] = rz[1]; rz[1] = rz[2]; }
-        }
-    }
-    sdelta_out = sd;
-}
-
-template <typename Tin, typename Tout, int G, bool ZOH, bool HAS_Z, int MODE>
-__global__ void __launch_bounds__(32)
-scan_fwd_kernel(const FwdArgs a) {
-    constexpr int NPL = kNMax / G;
-    __shared__ __align__(16) float sbc[kTile * kRow];
-    const int lane = threadIdx.x;
-    const int64_t b = blockIdx.y;
-    const int64_t d_raw = (int64_t)blockIdx.x * (32 / G) + lane / G;
-    const bool active = d_raw < a.dim;
-    const int64_t d = active ? d_raw : a.dim - 1;   // idle lanes shadow a valid channel
-    const int seg = blockIdx.z;
-    const int g = lane % G;
-    const int64_t chan = b * a.dim + d;
-
-    const int64_t t_begin = (int64_t)seg * a.seg_len;
-    const int64_t t_end = (t_begin + a.seg_len < a.seqlen) ? t_begin + a.seg_len : a.seqlen;
-
-    float h[NPL];
-#pragma unroll
-    for (int j = 0; j < NPL; j++) {
-        const int n = g * NPL + j;
-        float v = 0.f;
-        if (MODE == kFull && n < a.dstate) {
-            if (seg == 0) { if (a.h0 != nullptr) v = __ldg(a.h0 + chan * a.dstate + n); }
-            else v = a.ws_carry[(chan * a.nseg + seg) * kNMax + n];
-        }
-        h[j] = v;
-    }
-
-    // Fast SFU path unless inputs are fp32 or this warp sees A == 0 (ZOH limit).
-    bool acc = (sizeof(Tin) == 4);
-    if constexpr (ZOH) {
-        bool zero = false;
-        for (int j = 0; j < NPL; j++) {
-            const int n = g * NPL + j;
-            if (n < a.dstate && __ldg(a.A + d * a.dstate + n) == 0.f) zero = true;
-        }
-        acc = acc || __any_sync(0xffffffffu, zero);
-    }
-    float sdelta = 0.f;
-    if (acc) scan_warp<Tin, Tout, G, ZOH, true, HAS_Z, MODE>(a, sbc, b, d, active, lane, t_begin, t_end, h, sdelta);
-    else if constexpr (sizeof(Tin) == 2)
-        scan_warp<Tin, Tout, G, ZOH, false, HAS_Z, MODE>(a, sbc, b, d, active, lane, t_begin, t_end, h, sdelta);
-
-    if (!active) return;
-    if constexpr (MODE == kSummary) {
-#pragma unroll
-        for (int j = 0; j < NPL; j++) a.ws_hend[(chan * a.nseg + seg) * kNMax + g * NPL + j] = h[j];
-        if (g == 0) a.ws_sdelta[chan * a.nseg + seg] = sdelta;
-    } else {
-        if (seg == a.nseg - 1) {
-            if (a.final_state != nullptr)
-#pragma unroll
-                for (int j = 0; j < NPL; j++) {
-                    const int n = g * NPL + j;
-                    if (n < a.dstate) a.final_state[chan * a.dstate + n] = h[j];
-                }
-        }
-    }
-}
-
-// Pass 2 of the segmented schedule: carry-in of every segment, per (channel, n):
-// carry_0 = h0, carry_{s+1} = exp(A sum_delta_s) carry_s + h_end_s.
-__global__ void scan_carry_kernel(const FwdArgs a) {
-    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const int64_t chans = a.batch * a.dim;
-    if (idx >= chans * kNMax) return;
-    const int64_t chan = idx / kNMax;
-    const int n = (int)(idx % kNMax);
-    const int64_t d = chan % a.dim;
-    const float Av = (n < a.dstate) ? a.A[d * a.dstate + n] : 0.f;
-    float c = (a.h0 != nullptr && n < a.dstate) ? a.h0[chan * a.dstate + n] : 0.f;
-    for (int s = 0; s < a.nseg; s++) {
-        a.ws_carry[(chan * a.nseg + s) * kNMax + n] = c;
-        if (s + 1 < a.nseg) {
-            const float P = expf(Av * a.ws_sdelta[chan * a.nseg + s]);
-            c = fmaf(P, c, a.ws_hend[(chan * a.nseg + s) * kNMax + n]);
-        }
-    }
+static bool aligned16(const void* ptr, int64_t s0, int64_t s1, int esize) {
+    return ((uintptr_t)ptr % 16 == 0) && ((s0 * esize) % 16 == 0) && ((s1 * esize) % 16 == 0);
 }
 
 // seqlen == 0: final_state = h0 (or zero)
@@ -383,24 +54,17 @@ __global__ void copy_state_kernel(const float* h0, float* out, int64_t n) {
     if (i < n) out[i] = h0 ? h0[i] : 0.f;
 }
 
-// ---------------------------------------------------------------------------
-// Host side
-
 struct FwdPlan {
     int G;
     int nseg;
     int64_t seg_len;
 };
 
-static int env_int(const char* name, int dflt) {
-    const char* s = std::getenv(name);
-    return (s && *s) ? std::atoi(s) : dflt;
-}
 
 static FwdPlan plan_fwd(const ssm_scan_fwd_params* p, int num_sms) {
     FwdPlan pl;
     const int64_t chans = p->batch * p->dim;
-    const int64_t want_warps = (int64_t)num_sms * 8;
+    const int64_t want_warps = (int64_t)num_sms * 4;
     pl.G = 4;
     for (int G : {1, 2, 4}) {
         const int64_t warps = ceil_div(p->dim, 32 / G) * p->batch;
@@ -432,41 +96,6 @@ size_t fwd_workspace_bytes(const ssm_scan_fwd_params* p, int num_sms) {
     return (size_t)(ceil_div(floats * 4, 256) * 256);
 }
 
-static bool aligned16(const void* ptr, int64_t s0, int64_t s1, int esize) {
-    return ((uintptr_t)ptr % 16 == 0) && ((s0 * esize) % 16 == 0) && ((s1 * esize) % 16 == 0);
-}
-
-template <typename Tin, typename Tout, int G, bool ZOH, bool HAS_Z>
-static cudaError_t launch_passes(const FwdArgs& a, cudaStream_t st) {
-    const dim3 grid((unsigned)ceil_div(a.dim, 32 / G), (unsigned)a.batch, (unsigned)a.nseg);
-    if (a.nseg > 1) {
-        const FwdArgs& s = a;
-        // pass 1: every segment but the last produces (h_end, sum delta)
-        const dim3 g1((unsigned)ceil_div(a.dim, 32 / G), (unsigned)a.batch, (unsigned)(a.nseg - 1));
-        scan_fwd_kernel<Tin, Tout, G, ZOH, false, kSummary><<<g1, 32, 0, st>>>(s);
-        const int64_t n = a.batch * a.dim * kNMax;
-        scan_carry_kernel<<<(unsigned)ceil_div(n, 256), 256, 0, st>>>(s);
-        count_launches(2);
-    }
-    scan_fwd_kernel<Tin, Tout, G, ZOH, HAS_Z, kFull><<<grid, 32, 0, st>>>(a);
-    count_launches(1);
-    return cudaGetLastError();
-}
-
-template <typename Tin, typename Tout, int G>
-static cudaError_t dispatch_mode(const FwdArgs& a, bool zoh, bool has_z, cudaStream_t st) {
-    if (zoh) return has_z ? launch_passes<Tin, Tout, G, true, true>(a, st) : launch_passes<Tin, Tout, G, true, false>(a, st);
-    return has_z ? launch_passes<Tin, Tout, G, false, true>(a, st) : launch_passes<Tin, Tout, G, false, false>(a, st);
-}
-
-template <typename Tin, typename Tout>
-static cudaError_t dispatch_G(const FwdArgs& a, int G, bool zoh, bool has_z, cudaStream_t st) {
-    switch (G) {
-        case 1: return dispatch_mode<Tin, Tout, 1>(a, zoh, has_z, st);
-        case 2: return dispatch_mode<Tin, Tout, 2>(a, zoh, has_z, st);
-        default: return dispatch_mode<Tin, Tout, 4>(a, zoh, has_z, st);
-    }
-}
 
 cudaError_t launch_scan_fwd(const ssm_scan_fwd_params* p, void* ws, int num_sms, cudaStream_t st) {
     const int64_t chans = p->batch * p->dim;
@@ -513,11 +142,19 @@ cudaError_t launch_scan_fwd(const ssm_scan_fwd_params* p, void* ws, int num_sms,
     const bool zoh = p->bbar_mode == SSM_BBAR_ZOH;
     const bool has_z = p->z != nullptr;
     if (p->in_dtype == SSM_BF16) {
-        if (p->out_dtype == SSM_BF16) return dispatch_G<__nv_bfloat16, __nv_bfloat16>(a, pl.G, zoh, has_z, st);
-        return dispatch_G<__nv_bfloat16, float>(a, pl.G, zoh, has_z, st);
+        // the cp.async pipeline needs every u/delta/z/B/C row 16-byte aligned
+        const bool bc16 = ((uintptr_t)p->B % 16 == 0) && ((uintptr_t)p->C % 16 == 0) &&
+                          (a.sB_b % 8 == 0) && (a.sB_n % 8 == 0) && (a.sC_b % 8 == 0) && (a.sC_n % 8 == 0);
+        const bool async = a.vec_u && a.vec_dt && (!has_z || a.vec_z) && bc16 && env_int("SSM_FWD_NOASYNC", 0) == 0;
+        if (async) {
+            if (p->out_dtype == SSM_BF16) return dispatch_G<__nv_bfloat16, __nv_bfloat16, true>(a, pl.G, zoh, has_z, st);
+            return dispatch_G<__nv_bfloat16, float, true>(a, pl.G, zoh, has_z, st);
+        }
+        if (p->out_dtype == SSM_BF16) return dispatch_G<__nv_bfloat16, __nv_bfloat16, false>(a, pl.G, zoh, has_z, st);
+        return dispatch_G<__nv_bfloat16, float, false>(a, pl.G, zoh, has_z, st);
     }
-    if (p->out_dtype == SSM_BF16) return dispatch_G<float, __nv_bfloat16>(a, pl.G, zoh, has_z, st);
-    return dispatch_G<float, float>(a, pl.G, zoh, has_z, st);
+    if (p->out_dtype == SSM_BF16) return dispatch_G<float, __nv_bfloat16, false>(a, pl.G, zoh, has_z, st);
+    return dispatch_G<float, float, false>(a, pl.G, zoh, has_z, st);
 }
 
 }  // namespace ssm
