@@ -154,6 +154,7 @@ ssm_status causal_conv1d_silu_update(const ssm_conv_update_params* p, ssm_stream
     if (p == nullptr) return fail(SSM_ERR_INVALID_ARG, "params is NULL");
     if (p->batch < 1 || p->dim < 1 || p->width < 1) return fail(SSM_ERR_INVALID_ARG, "bad sizes");
     if (p->width > 4) return fail(SSM_ERR_UNSUPPORTED, "width=%lld > 4", (long long)p->width);
+    if (p->batch > 65535) return fail(SSM_ERR_UNSUPPORTED, "batch=%lld > 65535", (long long)p->batch);
     if (!dtype_ok(p->dtype)) return fail(SSM_ERR_INVALID_ARG, "unknown dtype");
     if (!p->x || !p->out || !p->weight || !p->state)
         return fail(SSM_ERR_INVALID_ARG, "x, out, weight and state are required");
@@ -167,6 +168,8 @@ ssm_status ssm_state_update(const ssm_state_update_params* p, ssm_stream_t strea
     if (p == nullptr) return fail(SSM_ERR_INVALID_ARG, "params is NULL");
     if (p->batch < 1 || p->dim < 1 || p->dstate < 1) return fail(SSM_ERR_INVALID_ARG, "bad sizes");
     if (p->dstate > 16) return fail(SSM_ERR_UNSUPPORTED, "dstate=%lld > 16", (long long)p->dstate);
+    if (p->batch > 65535 || p->dim > (1 << 28))
+        return fail(SSM_ERR_UNSUPPORTED, "batch > 65535 or dim > 2^28");
     if (!dtype_ok(p->in_dtype) || !dtype_ok(p->out_dtype)) return fail(SSM_ERR_INVALID_ARG, "unknown dtype");
     if (p->bbar_mode != SSM_BBAR_ZOH && p->bbar_mode != SSM_BBAR_SIMPLE)
         return fail(SSM_ERR_INVALID_ARG, "unknown bbar_mode %d", p->bbar_mode);

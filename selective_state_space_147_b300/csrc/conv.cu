@@ -159,12 +159,53 @@ __global__ void conv1d_silu_update_kernel(const ConvUpdArgs a) {
     Elem<T>::store(reinterpret_cast<T*>(a.out) + b * a.so + d, o);
 }
 
+// Fast path: width 4, bf16, even dim, aligned rows.  A thread updates two
+// neighbouring channels: one 16-byte load and store of their two windows, two
+// float4 weight loads, one 4-byte token load and store.
+__global__ void __launch_bounds__(256) conv1d_silu_update_w4x2_kernel(const ConvUpdArgs a) {
+    const int pair = blockIdx.x * blockDim.x + threadIdx.x;      // grid (dim/2 blocks, batch)
+    if (2 * pair >= a.dim) return;
+    const int64_t b = blockIdx.y, d = 2 * pair;
+    uint4* s = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.state) + (b * a.dim + d) * 4);
+    const uint4 w8 = *s;                        // [c0: s0 s1 s2 s3][c1: s0 s1 s2 s3]
+    const uint32_t xw = *reinterpret_cast<const uint32_t*>(reinterpret_cast<const __nv_bfloat16*>(a.x) + b * a.sx + d);
+    const float4 wa = __ldg(reinterpret_cast<const float4*>(a.w + d * 4));
+    const float4 wb = __ldg(reinterpret_cast<const float4*>(a.w + d * 4) + 1);
+    const float ba = a.bias ? __ldg(a.bias + d) : 0.f, bb = a.bias ? __ldg(a.bias + d + 1) : 0.f;
+    // channel d: window after the shift = [s1 s2 s3 x]
+    const float xa = bf16lo(xw), xb = bf16hi(xw);
+    const float a1 = bf16hi(w8.x), a2 = bf16lo(w8.y), a3 = bf16hi(w8.y);
+    const float b1 = bf16hi(w8.z), b2 = bf16lo(w8.w), b3 = bf16hi(w8.w);
+    // tap i multiplies x[t - i]: tap 0 -> x, tap 1 -> s3, tap 2 -> s2, tap 3 -> s1
+    float acc_a = fmaf(wa.x, xa, ba); acc_a = fmaf(wa.y, a3, acc_a); acc_a = fmaf(wa.z, a2, acc_a); acc_a = fmaf(wa.w, a1, acc_a);
+    float acc_b = fmaf(wb.x, xb, bb); acc_b = fmaf(wb.y, b3, acc_b); acc_b = fmaf(wb.z, b2, acc_b); acc_b = fmaf(wb.w, b1, acc_b);
+    // shifted windows, keeping the stored bf16 bits exactly
+    const uint32_t xa16 = xw & 0xffffu, xb16 = xw >> 16;
+    uint4 nw;
+    nw.x = (w8.x >> 16) | (w8.y << 16);          // s1 s2
+    nw.y = (w8.y >> 16) | (xa16 << 16);          // s3 x
+    nw.z = (w8.z >> 16) | (w8.w << 16);
+    nw.w = (w8.w >> 16) | (xb16 << 16);
+    *s = nw;
+    *reinterpret_cast<uint32_t*>(reinterpret_cast<__nv_bfloat16*>(a.out) + b * a.so + d) =
+        pack_bf16x2(silu_fast(acc_a), silu_fast(acc_b));
+}
+
 cudaError_t launch_conv1d_silu_update(const ssm_conv_update_params* p, cudaStream_t st) {
     ConvUpdArgs a;
     a.batch = p->batch; a.dim = p->dim; a.width = (int)p->width;
     a.x = p->x; a.out = p->out; a.sx = p->x_stride; a.so = p->out_stride;
     a.w = p->weight; a.bias = p->bias; a.state = p->state;
     const int64_t n = p->batch * p->dim;
+    const bool fast = p->width == 4 && p->dtype == SSM_BF16 && (p->dim % 2 == 0) &&
+                      ((uintptr_t)p->state % 16 == 0) && ((uintptr_t)p->weight % 16 == 0) &&
+                      ((uintptr_t)p->x % 4 == 0) && ((uintptr_t)p->out % 4 == 0) &&
+                      (p->x_stride % 2 == 0) && (p->out_stride % 2 == 0);
+    if (fast) {
+        conv1d_silu_update_w4x2_kernel<<<dim3((unsigned)ceil_div(p->dim / 2, 256), (unsigned)p->batch), 256, 0, st>>>(a);
+        count_launches(1);
+        return cudaGetLastError();
+    }
     const unsigned blocks = (unsigned)ceil_div(n, 256);
     if (p->dtype == SSM_BF16) conv1d_silu_update_kernel<__nv_bfloat16, false><<<blocks, 256, 0, st>>>(a);
     else conv1d_silu_update_kernel<float, true><<<blocks, 256, 0, st>>>(a);

@@ -69,7 +69,7 @@ __global__ void __launch_bounds__(256) state_update_kernel(const DecArgs a) {
                 coef = ZOH ? (Av != 0.f ? expm1f(x) / Av : dl) : dl;
             } else {
                 ab = ex2_approx(x * kLog2e);
-                coef = ZOH ? (Av != 0.f ? (ab - 1.f) / Av : dl) : dl;
+                coef = ZOH ? (Av != 0.f ? (ab - 1.f) * rcp_approx(Av) : dl) : dl;
             }
             h[j] = fmaf(ab, h[j], coef * Bv * xt);
             y = fmaf(Cv, h[j], y);
@@ -97,6 +97,60 @@ __global__ void __launch_bounds__(256) state_update_kernel(const DecArgs a) {
     }
 }
 
+// Fast path for the common layout: dstate == 16, bf16 token inputs, every
+// row 16-byte aligned.  Two lanes per channel, eight states each: a lane moves
+// 32 bytes of state with two streaming (evict-first) 16-byte loads and stores,
+// reads its eight B, C values with one 16-byte load each and its eight A values
+// with two float4 loads; the readout is reduced over the two lanes with one
+// shuffle.  The grid is (channel blocks, batch), so no index needs a division.
+// (Walking several batch rows per thread with software prefetch, or one lane
+// per channel, measured slower on B300: register spills, fewer bytes in flight.)
+template <typename Tout, bool ZOH>
+__global__ void __launch_bounds__(256) state_update16_kernel(const DecArgs a) {
+    const int item = blockIdx.x * blockDim.x + threadIdx.x;      // 2 d + g
+    const int64_t b = blockIdx.y;
+    const bool active = item < 2 * a.dim;
+    const int d = active ? (item >> 1) : (int)a.dim - 1;
+    const int g = item & 1;
+    const int64_t chan = b * a.dim + d;
+    float4* st = reinterpret_cast<float4*>(a.state + chan * 16 + g * 8);
+    const float4 s0 = __ldcs(st), s1 = __ldcs(st + 1);
+    const float4 a0 = __ldg(reinterpret_cast<const float4*>(a.A + d * 16 + g * 8));
+    const float4 a1 = __ldg(reinterpret_cast<const float4*>(a.A + d * 16 + g * 8) + 1);
+    const uint4 bw = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.B) + b * a.sB + g * 8));
+    const uint4 cw = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.C) + b * a.sC + g * 8));
+    const float xt = Elem<__nv_bfloat16>::load(reinterpret_cast<const __nv_bfloat16*>(a.x) + b * a.sx + d);
+    const float v = Elem<__nv_bfloat16>::load(reinterpret_cast<const __nv_bfloat16*>(a.dt) + b * a.sdt + d) +
+                    (a.bias ? __ldg(a.bias + d) : 0.f);
+    const float zt = a.z ? Elem<__nv_bfloat16>::load(reinterpret_cast<const __nv_bfloat16*>(a.z) + b * a.sz + d) : 0.f;
+    const float dl = a.softplus ? softplus_fast(v) : v;
+
+    float h[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+    const float Av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+    const uint32_t bb[4] = {bw.x, bw.y, bw.z, bw.w};
+    const uint32_t cc[4] = {cw.x, cw.y, cw.z, cw.w};
+    float y = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+        const float Bv = (j & 1) ? bf16hi(bb[j >> 1]) : bf16lo(bb[j >> 1]);
+        const float Cv = (j & 1) ? bf16hi(cc[j >> 1]) : bf16lo(cc[j >> 1]);
+        const float ab = ex2_approx(dl * Av[j] * kLog2e);
+        // ZOH input coefficient (Abar - 1)/A with the SFU reciprocal; delta where A == 0
+        const float coef = (ZOH && Av[j] != 0.f) ? (ab - 1.f) * rcp_approx(Av[j]) : dl;
+        h[j] = fmaf(ab, h[j], coef * Bv * xt);
+        y = fmaf(Cv, h[j], y);
+    }
+    y += __shfl_xor_sync(0xffffffffu, y, 1);
+    if (!active) return;
+    __stcs(st, make_float4(h[0], h[1], h[2], h[3]));
+    __stcs(st + 1, make_float4(h[4], h[5], h[6], h[7]));
+    if (g == 0) {
+        y = fmaf(a.D ? __ldg(a.D + d) : 0.f, xt, y);
+        if (a.z != nullptr) y *= silu_fast(zt);
+        Elem<Tout>::store(reinterpret_cast<Tout*>(a.out) + b * a.so + d, y);
+    }
+}
+
 template <typename Tin, typename Tout>
 static void launch_typed(const DecArgs& a, bool zoh, unsigned blocks, cudaStream_t st) {
     constexpr bool ACC = sizeof(Tin) == 4;
@@ -112,9 +166,25 @@ cudaError_t launch_state_update(const ssm_state_update_params* p, cudaStream_t s
     a.sC = p->C_stride; a.so = p->out_stride;
     a.A = p->A; a.D = p->D; a.bias = p->delta_bias; a.state = p->state;
     a.softplus = p->delta_softplus ? 1 : 0;
+    const bool zoh = p->bbar_mode == SSM_BBAR_ZOH;
+    const bool fast16 = p->dstate == 16 && p->in_dtype == SSM_BF16 &&
+                        ((uintptr_t)p->state % 16 == 0) && ((uintptr_t)p->A % 16 == 0) &&
+                        ((uintptr_t)p->B % 16 == 0) && ((uintptr_t)p->C % 16 == 0) &&
+                        (p->B_stride % 8 == 0) && (p->C_stride % 8 == 0);
+    if (fast16) {
+        const dim3 blocks2((unsigned)ceil_div(p->dim * 2, 256), (unsigned)p->batch);
+        if (p->out_dtype == SSM_BF16) {
+            if (zoh) state_update16_kernel<__nv_bfloat16, true><<<blocks2, 256, 0, st>>>(a);
+            else state_update16_kernel<__nv_bfloat16, false><<<blocks2, 256, 0, st>>>(a);
+        } else {
+            if (zoh) state_update16_kernel<float, true><<<blocks2, 256, 0, st>>>(a);
+            else state_update16_kernel<float, false><<<blocks2, 256, 0, st>>>(a);
+        }
+        count_launches(1);
+        return cudaGetLastError();
+    }
     const int64_t threads = p->batch * p->dim * 4;
     const unsigned blocks = (unsigned)ceil_div(threads, 256);
-    const bool zoh = p->bbar_mode == SSM_BBAR_ZOH;
     if (p->in_dtype == SSM_BF16) {
         if (p->out_dtype == SSM_BF16) launch_typed<__nv_bfloat16, __nv_bfloat16>(a, zoh, blocks, st);
         else launch_typed<__nv_bfloat16, float>(a, zoh, blocks, st);
