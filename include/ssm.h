@@ -152,6 +152,64 @@ SSM_API ssm_status ssm_scan_fwd(const ssm_scan_fwd_params* p, void* workspace,
 SSM_API ssm_status ssm_scan_fwd_static_ws(const ssm_scan_fwd_params* p, ssm_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Selective scan, backward, with recompute of h (the states are not stored by
+ * the forward; they are recomputed on chip from checkpoints).
+ * world.lapla.si section 07 ("训练时反向传播要用的中间状态不存，到时候重新算
+ * 一遍"); deepseek.csdn.net section 3.2.3 C.  The pages give no gradient
+ * formulas: these are the chain rule of the forward above for the loss
+ * sum(dout * out) + sum(dfinal_state * final_state).
+ *
+ *   forward inputs   : as ssm_scan_fwd (same shapes, strides and flags)
+ *   dout             : (batch, dim, seqlen) in_dtype
+ *   dfinal_state     : (batch, dim, dstate) float32 or NULL (= 0)
+ *   checkpoints      : the forward's checkpoints with checkpoint_every == 8,
+ *                      or NULL / another interval: the backward then
+ *                      recomputes them into the workspace first
+ *   du, ddelta, dz   : (batch, dim, seqlen) grad_dtype, strides as above;
+ *                      ddelta is the gradient with respect to the delta INPUT
+ *                      (before bias and softplus); dz required iff z != NULL
+ *   dB, dC           : (batch, dstate, seqlen) float32 contiguous (summed over
+ *                      the channels d)
+ *   dA               : (dim, dstate) float32; dD, ddelta_bias: (dim) float32 or
+ *                      NULL; dh0: (batch, dim, dstate) float32 or NULL
+ * Workspace: ssm_scan_bwd_workspace_size() bytes, 256-byte aligned (per-CTA
+ * partial sums, and recomputed checkpoints when none are passed).
+ * Results are deterministic (fixed-order reductions, no atomics). */
+typedef struct {
+    int64_t batch, dim, seqlen, dstate;
+    ssm_dtype in_dtype;
+    ssm_dtype grad_dtype;
+    int bbar_mode;
+    int delta_softplus;
+    const void* u;     ssm_strides u_strides;
+    const void* delta; ssm_strides delta_strides;
+    const void* z;     ssm_strides z_strides;
+    const void* B;     ssm_strides B_strides;
+    const void* C;     ssm_strides C_strides;
+    const void* dout;  ssm_strides dout_strides;
+    const float* A;
+    const float* D;
+    const float* delta_bias;
+    const float* h0;
+    const float* dfinal_state;
+    const float* checkpoints;
+    int64_t checkpoint_every;
+    void* du;          ssm_strides du_strides;
+    void* ddelta;      ssm_strides ddelta_strides;
+    void* dz;          ssm_strides dz_strides;
+    float* dB;
+    float* dC;
+    float* dA;
+    float* dD;
+    float* ddelta_bias;
+    float* dh0;
+} ssm_scan_bwd_params;
+
+SSM_API size_t ssm_scan_bwd_workspace_size(const ssm_scan_bwd_params* p);
+SSM_API ssm_status ssm_scan_bwd(const ssm_scan_bwd_params* p, void* workspace,
+                        size_t workspace_bytes, ssm_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Single-token decode step: state <- update(state, x_t), then readout and
  * gate for that token.  "Mamba 模型", section "为什么 Mamba 推理更省".
  *

@@ -54,6 +54,25 @@ class ScanFwdParams(ctypes.Structure):
     ]
 
 
+class ScanBwdParams(ctypes.Structure):
+    _fields_ = [
+        ("batch", _i64), ("dim", _i64), ("seqlen", _i64), ("dstate", _i64),
+        ("in_dtype", _int), ("grad_dtype", _int), ("bbar_mode", _int), ("delta_softplus", _int),
+        ("u", _vp), ("u_strides", Strides),
+        ("delta", _vp), ("delta_strides", Strides),
+        ("z", _vp), ("z_strides", Strides),
+        ("B", _vp), ("B_strides", Strides),
+        ("C", _vp), ("C_strides", Strides),
+        ("dout", _vp), ("dout_strides", Strides),
+        ("A", _fp), ("D", _fp), ("delta_bias", _fp), ("h0", _fp),
+        ("dfinal_state", _fp), ("checkpoints", _fp), ("checkpoint_every", _i64),
+        ("du", _vp), ("du_strides", Strides),
+        ("ddelta", _vp), ("ddelta_strides", Strides),
+        ("dz", _vp), ("dz_strides", Strides),
+        ("dB", _fp), ("dC", _fp), ("dA", _fp), ("dD", _fp), ("ddelta_bias", _fp), ("dh0", _fp),
+    ]
+
+
 class StateUpdateParams(ctypes.Structure):
     _fields_ = [
         ("batch", _i64), ("dim", _i64), ("dstate", _i64),
@@ -92,6 +111,10 @@ _lib.ssm_scan_fwd_workspace_size.argtypes = [ctypes.POINTER(ScanFwdParams)]
 _lib.ssm_scan_fwd_workspace_size.restype = ctypes.c_size_t
 _lib.ssm_scan_fwd.argtypes = [ctypes.POINTER(ScanFwdParams), _vp, ctypes.c_size_t, _vp]
 _lib.ssm_scan_fwd.restype = _int
+_lib.ssm_scan_bwd_workspace_size.argtypes = [ctypes.POINTER(ScanBwdParams)]
+_lib.ssm_scan_bwd_workspace_size.restype = ctypes.c_size_t
+_lib.ssm_scan_bwd.argtypes = [ctypes.POINTER(ScanBwdParams), _vp, ctypes.c_size_t, _vp]
+_lib.ssm_scan_bwd.restype = _int
 _lib.ssm_state_update.argtypes = [ctypes.POINTER(StateUpdateParams), _vp]
 _lib.ssm_state_update.restype = _int
 _lib.causal_conv1d_silu.argtypes = [ctypes.POINTER(ConvParams), _vp]
@@ -258,6 +281,76 @@ def ssm_scan_fwd_workspace_size(u, A, **kw) -> int:
     p.delta_softplus = 1
     p.u = p.delta = p.B = p.C = p.out = p.A = 1   # any non-NULL value: only sizes matter here
     return _lib.ssm_scan_fwd_workspace_size(ctypes.byref(p))
+
+
+def ssm_scan_bwd(u, delta, A, B, C, dout, *, D=None, delta_bias=None, z=None, h0=None,
+                 dfinal_state=None, checkpoints=None, checkpoint_every: int = 0,
+                 bbar_mode: int = SSM_BBAR_ZOH, delta_softplus: bool = True, grad_dtype=None,
+                 grads: Optional[dict] = None, workspace: Optional[torch.Tensor] = None, stream=None):
+    """Backward of ssm_scan_fwd for the loss sum(dout * out) + sum(dfinal_state * final_state).
+    Pass the forward's checkpoints (checkpoint_every=8) to skip their recomputation.
+    Returns a dict: du, ddelta, dz (like u, in grad_dtype), dB, dC (batch, N, L) f32,
+    dA (dim, N), dD, ddelta_bias (dim,), dh0 (batch, dim, N), all float32 except du/ddelta/dz."""
+    for name, t in (("u", u), ("delta", delta), ("B", B), ("C", C), ("z", z), ("dout", dout)):
+        _need_cuda(name, t)
+        if t is not None and t.dtype != u.dtype:
+            raise ValueError(f"{name} must have the dtype of u")
+    A, D, delta_bias, h0 = (_f32c("A", A), _f32c("D", D), _f32c("delta_bias", delta_bias), _f32c("h0", h0))
+    _f32c("dfinal_state", dfinal_state)
+    _f32c("checkpoints", checkpoints)
+    batch, dim, L = u.shape
+    N = A.shape[1]
+    gd = _torch_dtype(grad_dtype or u.dtype)
+    dev = u.device
+    g = dict(grads or {})
+    g.setdefault("du", torch.empty(batch, dim, L, dtype=gd, device=dev))
+    g.setdefault("ddelta", torch.empty(batch, dim, L, dtype=gd, device=dev))
+    g.setdefault("dz", torch.empty(batch, dim, L, dtype=gd, device=dev) if z is not None else None)
+    g.setdefault("dB", torch.empty(batch, N, L, dtype=torch.float32, device=dev))
+    g.setdefault("dC", torch.empty(batch, N, L, dtype=torch.float32, device=dev))
+    g.setdefault("dA", torch.empty(dim, N, dtype=torch.float32, device=dev))
+    g.setdefault("dD", torch.empty(dim, dtype=torch.float32, device=dev))
+    g.setdefault("ddelta_bias", torch.empty(dim, dtype=torch.float32, device=dev))
+    g.setdefault("dh0", torch.empty(batch, dim, N, dtype=torch.float32, device=dev))
+    for k in ("dB", "dC", "dA", "dD", "ddelta_bias", "dh0"):
+        _f32c(k, g[k])
+    p = ScanBwdParams()
+    p.batch, p.dim, p.seqlen, p.dstate = batch, dim, L, N
+    p.in_dtype, p.grad_dtype = _dtype_code(u.dtype), _dtype_code(gd)
+    p.bbar_mode, p.delta_softplus = int(bbar_mode), 1 if delta_softplus else 0
+    p.u, p.u_strides = _ptr(u), _seq_strides("u", u)
+    p.delta, p.delta_strides = _ptr(delta), _seq_strides("delta", delta)
+    p.z, p.z_strides = _ptr(z), _seq_strides("z", z)
+    p.B, p.B_strides = _ptr(B), _seq_strides("B", B)
+    p.C, p.C_strides = _ptr(C), _seq_strides("C", C)
+    p.dout, p.dout_strides = _ptr(dout), _seq_strides("dout", dout)
+    p.A, p.D, p.delta_bias, p.h0 = _ptr(A), _ptr(D), _ptr(delta_bias), _ptr(h0)
+    p.dfinal_state, p.checkpoints, p.checkpoint_every = _ptr(dfinal_state), _ptr(checkpoints), int(checkpoint_every)
+    p.du, p.du_strides = _ptr(g["du"]), _seq_strides("du", g["du"])
+    p.ddelta, p.ddelta_strides = _ptr(g["ddelta"]), _seq_strides("ddelta", g["ddelta"])
+    p.dz, p.dz_strides = _ptr(g["dz"]), _seq_strides("dz", g["dz"])
+    p.dB, p.dC, p.dA = _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g["dA"])
+    p.dD, p.ddelta_bias, p.dh0 = _ptr(g["dD"]), _ptr(g["ddelta_bias"]), _ptr(g["dh0"])
+    need = _lib.ssm_scan_bwd_workspace_size(ctypes.byref(p))
+    if need > 0 and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_lib.ssm_scan_bwd(ctypes.byref(p), _ptr(workspace), ws_bytes, _stream(stream)))
+    return g
+
+
+def ssm_scan_bwd_workspace_size(u, A, *, checkpoints_given: bool = True, **kw) -> int:
+    """Workspace bytes ssm_scan_bwd needs for this problem shape."""
+    p = ScanBwdParams()
+    p.batch, p.dim, p.seqlen = u.shape
+    p.dstate = A.shape[1]
+    p.in_dtype = p.grad_dtype = _dtype_code(u.dtype)
+    p.bbar_mode = int(kw.get("bbar_mode", SSM_BBAR_ZOH))
+    p.delta_softplus = 1
+    p.u = p.delta = p.B = p.C = p.dout = p.A = p.du = p.ddelta = p.dB = p.dC = p.dA = 1  # sizes only
+    if checkpoints_given:
+        p.checkpoints, p.checkpoint_every = 1, 8
+    return _lib.ssm_scan_bwd_workspace_size(ctypes.byref(p))
 
 
 def ssm_state_update(state, x, delta, A, B, C, *, D=None, delta_bias=None, z=None,

@@ -71,6 +71,31 @@ ssm_status check_fwd(const ssm_scan_fwd_params* p) {
     return SSM_OK;
 }
 
+ssm_status check_bwd(const ssm_scan_bwd_params* p) {
+    if (p == nullptr) return fail(SSM_ERR_INVALID_ARG, "params is NULL");
+    if (p->batch < 1 || p->dim < 1 || p->seqlen < 0 || p->dstate < 1)
+        return fail(SSM_ERR_INVALID_ARG, "bad sizes batch=%lld dim=%lld seqlen=%lld dstate=%lld",
+                    (long long)p->batch, (long long)p->dim, (long long)p->seqlen, (long long)p->dstate);
+    if (p->dstate > 16) return fail(SSM_ERR_UNSUPPORTED, "dstate=%lld > 16", (long long)p->dstate);
+    if (p->batch > 65535) return fail(SSM_ERR_UNSUPPORTED, "batch=%lld > 65535", (long long)p->batch);
+    if (!dtype_ok(p->in_dtype) || !dtype_ok(p->grad_dtype)) return fail(SSM_ERR_INVALID_ARG, "unknown dtype");
+    if (p->bbar_mode != SSM_BBAR_ZOH && p->bbar_mode != SSM_BBAR_SIMPLE)
+        return fail(SSM_ERR_INVALID_ARG, "unknown bbar_mode %d", p->bbar_mode);
+    if (p->seqlen > 0) {
+        if (!p->u || !p->delta || !p->B || !p->C || !p->dout || !p->A || !p->du || !p->ddelta || !p->dB ||
+            !p->dC || !p->dA)
+            return fail(SSM_ERR_INVALID_ARG, "u, delta, B, C, dout, A, du, ddelta, dB, dC and dA are required");
+        if ((p->z == nullptr) != (p->dz == nullptr)) return fail(SSM_ERR_INVALID_ARG, "dz is required iff z is given");
+    }
+    const ssm_strides* all[] = {&p->u_strides, &p->delta_strides, &p->z_strides, &p->B_strides, &p->C_strides,
+                                &p->dout_strides, &p->du_strides, &p->ddelta_strides, &p->dz_strides};
+    for (const ssm_strides* s : all)
+        if (s->batch < 0 || s->row < 0) return fail(SSM_ERR_INVALID_ARG, "negative stride");
+    if (p->checkpoints != nullptr && p->checkpoint_every <= 0)
+        return fail(SSM_ERR_INVALID_ARG, "checkpoint_every must be positive when checkpoints are given");
+    return SSM_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -131,6 +156,31 @@ ssm_status ssm_scan_fwd_static_ws(const ssm_scan_fwd_params* p, ssm_stream_t str
                     need, ssm::static_scratch_bytes());
     cudaError_t e = ssm::launch_scan_fwd_static(p, sms, need, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "ssm_scan_fwd_static_ws");
+    return ok();
+}
+
+size_t ssm_scan_bwd_workspace_size(const ssm_scan_bwd_params* p) {
+    if (check_bwd(p) != SSM_OK) return 0;
+    int sms = 0;
+    if (num_sms(&sms) != SSM_OK) return 0;
+    return ssm::bwd_workspace_bytes(p, sms);
+}
+
+ssm_status ssm_scan_bwd(const ssm_scan_bwd_params* p, void* workspace, size_t workspace_bytes,
+                        ssm_stream_t stream) {
+    ssm_status s = check_bwd(p);
+    if (s != SSM_OK) return s;
+    int sms = 0;
+    if ((s = num_sms(&sms)) != SSM_OK) return s;
+    const size_t need = ssm::bwd_workspace_bytes(p, sms);
+    if (need > 0) {
+        if (workspace == nullptr || workspace_bytes < need)
+            return fail(SSM_ERR_WORKSPACE, "workspace of %zu bytes required, got %zu", need,
+                        workspace == nullptr ? (size_t)0 : workspace_bytes);
+        if ((uintptr_t)workspace % 256 != 0) return fail(SSM_ERR_MISALIGNED, "workspace must be 256-byte aligned");
+    }
+    cudaError_t e = ssm::launch_scan_bwd(p, workspace, sms, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "ssm_scan_bwd launch");
     return ok();
 }
 

@@ -14,6 +14,8 @@ void count_launches(unsigned n);
 size_t fwd_workspace_bytes(const ssm_scan_fwd_params* p, int num_sms);
 cudaError_t launch_scan_fwd(const ssm_scan_fwd_params* p, void* ws, int num_sms, cudaStream_t st);
 cudaError_t launch_conv1d_silu(const ssm_conv_params* p, cudaStream_t st);
+size_t bwd_workspace_bytes(const ssm_scan_bwd_params* p, int num_sms);
+cudaError_t launch_scan_bwd(const ssm_scan_bwd_params* p, void* ws, int num_sms, cudaStream_t st);
 size_t static_scratch_bytes();
 cudaError_t launch_scan_fwd_static(const ssm_scan_fwd_params* p, int num_sms, size_t need, cudaStream_t st);
 cudaError_t launch_conv1d_silu_update(const ssm_conv_update_params* p, cudaStream_t st);

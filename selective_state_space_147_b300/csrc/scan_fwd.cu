@@ -127,7 +127,7 @@ cudaError_t launch_scan_fwd(const ssm_scan_fwd_params* p, void* ws, int num_sms,
     a.vec_u = aligned16(p->u, a.su_b, a.su_d, isz);
     a.vec_dt = aligned16(p->delta, a.sdt_b, a.sdt_d, isz);
     a.vec_z = p->z ? aligned16(p->z, a.sz_b, a.sz_d, isz) : 0;
-    a.vec_out = aligned16(p->out, a.so_b, a.so_d, osz);
+    a.vec_out = p->out ? aligned16(p->out, a.so_b, a.so_d, osz) : 0;
     // B/C are read two steps at a time
     a.vec_BC = ((uintptr_t)p->B % (2 * isz) == 0) && ((uintptr_t)p->C % (2 * isz) == 0) &&
                (a.sB_b % 2 == 0) && (a.sB_n % 2 == 0) && (a.sC_b % 2 == 0) && (a.sC_n % 2 == 0);

@@ -248,7 +248,8 @@ __device__ __forceinline__ void scan_warp(const FwdArgs& a, float* sbc_all, int6
     const Tin* urow = reinterpret_cast<const Tin*>(a.u) + b * a.su_b + d * a.su_d;
     const Tin* drow = reinterpret_cast<const Tin*>(a.dt) + b * a.sdt_b + d * a.sdt_d;
     const Tin* zrow = HAS_Z ? reinterpret_cast<const Tin*>(a.z) + b * a.sz_b + d * a.sz_d : nullptr;
-    Tout* orow = (MODE == kFull) ? reinterpret_cast<Tout*>(a.out) + b * a.so_b + d * a.so_d : nullptr;
+    // out == NULL: checkpoint-only pass (used by the backward), nothing is stored
+    Tout* orow = (MODE == kFull && a.out != nullptr) ? reinterpret_cast<Tout*>(a.out) + b * a.so_b + d * a.so_d : nullptr;
     const Tin* Bb = reinterpret_cast<const Tin*>(a.B) + b * a.sB_b;
     const Tin* Cb = reinterpret_cast<const Tin*>(a.C) + b * a.sC_b;
     float* ck = (MODE == kFull && a.ckpt != nullptr)
@@ -299,7 +300,7 @@ __device__ __forceinline__ void scan_warp(const FwdArgs& a, float* sbc_all, int6
                 }
             }
             if constexpr (MODE == kFull) {
-                if (active && g == 0) store8<Tout>(orow + t0, cnt, a.vec_out, yout);
+                if (active && g == 0 && orow != nullptr) store8<Tout>(orow + t0, cnt, a.vec_out, yout);
             }
             ru[0] = ru[1]; rd[0] = rd[1]; ru[1] = ru[2]; rd[1] = rd[2];
             if constexpr (HAS_Z && MODE == kFull) { rz[0] = rz[1]; rz[1] = rz[2]; }
@@ -461,7 +462,8 @@ __device__ __forceinline__ void scan_cta_async(const FwdArgs& a, unsigned char* 
     }
     const float Dd = (a.D != nullptr) ? __ldg(a.D + d) : 0.f;
     const float bias = (a.bias != nullptr) ? __ldg(a.bias + d) : 0.f;
-    Tout* orow = (MODE == kFull) ? reinterpret_cast<Tout*>(a.out) + b * a.so_b + d * a.so_d : nullptr;
+    // out == NULL: checkpoint-only pass (used by the backward), nothing is stored
+    Tout* orow = (MODE == kFull && a.out != nullptr) ? reinterpret_cast<Tout*>(a.out) + b * a.so_b + d * a.so_d : nullptr;
     float* ck = (MODE == kFull && a.ckpt != nullptr)
                     ? a.ckpt + (b * a.dim + d) * a.n_ckpt * a.dstate : nullptr;
     float* bcf = reinterpret_cast<float*>(smem + kStages * kStage);
@@ -578,7 +580,7 @@ __device__ __forceinline__ void scan_cta_async(const FwdArgs& a, unsigned char* 
                     yo[i] = yj;
                 }
                 const int lim = cnt - jb;
-                if (active && lim > 0) storeN<Tout, SPL>(orow + t0 + jb, lim, a.vec_out, yo);
+                if (active && lim > 0 && orow != nullptr) storeN<Tout, SPL>(orow + t0 + jb, lim, a.vec_out, yo);
             }
         }
         __syncthreads();   // everyone is done with this stage and with bcf

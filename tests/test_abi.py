@@ -29,7 +29,8 @@ def lib():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for must in ("ssm_scan_fwd", "ssm_scan_fwd_workspace_size", "ssm_state_update",
+    for must in ("ssm_scan_fwd", "ssm_scan_fwd_workspace_size", "ssm_scan_bwd", "ssm_scan_bwd_workspace_size",
+                 "ssm_state_update",
                  "causal_conv1d_silu", "causal_conv1d_silu_update", "ssm_status_string",
                  "ssm_last_error", "ssm_abi_version"):
         assert must in names
@@ -75,6 +76,13 @@ def test_host_validation_without_gpu():
     p.checkpoint_every = 8
     p.u_strides.row = -1
     assert lib.ssm_scan_fwd(ctypes.byref(p), None, 0, None) == -1
+    q = B.ScanBwdParams()
+    q.batch, q.dim, q.seqlen, q.dstate = 1, 1, 8, 16
+    assert lib.ssm_scan_bwd(ctypes.byref(q), None, 0, None) == -1      # missing pointers
+    q.u = q.delta = q.B = q.C = q.dout = q.A = q.du = q.ddelta = q.dB = q.dC = q.dA = 16
+    q.z = 16                                                            # z without dz
+    assert lib.ssm_scan_bwd(ctypes.byref(q), None, 0, None) == -1
+    assert b"dz" in lib.ssm_last_error()
     c = B.ConvParams()
     c.batch, c.dim, c.seqlen, c.width = 1, 1, 4, 5
     assert lib.causal_conv1d_silu(ctypes.byref(c), None) == -2         # width > 4
