@@ -64,7 +64,7 @@ typedef enum {
     SSM_OK = 0,
     SSM_ERR_INVALID_ARG = -1, /* a NULL required pointer, a negative size, ... */
     SSM_ERR_UNSUPPORTED = -2, /* a valid request this build does not implement */
-    SSM_ERR_MISALIGNED = -3,  /* a stride of the innermost (seqlen) axis is not 1 */
+    SSM_ERR_MISALIGNED = -3,  /* a pointer that must be aligned (workspace, checkpoints) is not */
     SSM_ERR_WORKSPACE = -4,   /* workspace missing or smaller than required */
     SSM_ERR_CUDA = -5         /* a CUDA runtime error (see ssm_last_error) */
 } ssm_status;
@@ -93,9 +93,10 @@ typedef struct {
  *   h0               : (batch, dim, dstate) float32 contiguous or NULL (= 0)
  *   final_state      : (batch, dim, dstate) float32 contiguous or NULL
  *   checkpoints      : (batch, dim, ceil(seqlen/K), dstate) float32
- *                      contiguous or NULL; entry k holds the state before
- *                      step k*K (entry 0 = h0).  K = checkpoint_every must be
- *                      a positive multiple of 8 when checkpoints != NULL.
+ *                      contiguous, 16-byte aligned, or NULL; entry k holds the
+ *                      state before step k*K (entry 0 = h0).  K =
+ *                      checkpoint_every must be a positive multiple of 8 when
+ *                      checkpoints != NULL.
  *                      ssm_scan_bwd can take these instead of recomputing.
  * dstate: 1..16.  dim, batch >= 1; seqlen >= 0 (seqlen 0 only copies h0
  * to final_state).
@@ -162,9 +163,9 @@ SSM_API ssm_status ssm_scan_fwd_static_ws(const ssm_scan_fwd_params* p, ssm_stre
  *   forward inputs   : as ssm_scan_fwd (same shapes, strides and flags)
  *   dout             : (batch, dim, seqlen) in_dtype
  *   dfinal_state     : (batch, dim, dstate) float32 or NULL (= 0)
- *   checkpoints      : the forward's checkpoints with checkpoint_every == 8,
- *                      or NULL / another interval: the backward then
- *                      recomputes them into the workspace first
+ *   checkpoints      : the forward's checkpoints (16-byte aligned) with
+ *                      checkpoint_every == 8, or NULL / another interval: the
+ *                      backward then recomputes them into the workspace first
  *   du, ddelta, dz   : (batch, dim, seqlen) grad_dtype, strides as above;
  *                      ddelta is the gradient with respect to the delta INPUT
  *                      (before bias and softplus); dz required iff z != NULL

@@ -279,7 +279,7 @@ def ssm_scan_fwd_workspace_size(u, A, **kw) -> int:
     p.out_dtype = _dtype_code(kw.get("out_dtype", u.dtype))
     p.bbar_mode = int(kw.get("bbar_mode", SSM_BBAR_ZOH))
     p.delta_softplus = 1
-    p.u = p.delta = p.B = p.C = p.out = p.A = 1   # any non-NULL value: only sizes matter here
+    p.u = p.delta = p.B = p.C = p.out = p.A = 256   # any aligned non-NULL value: only sizes matter here
     return _lib.ssm_scan_fwd_workspace_size(ctypes.byref(p))
 
 
@@ -347,9 +347,9 @@ def ssm_scan_bwd_workspace_size(u, A, *, checkpoints_given: bool = True, **kw) -
     p.in_dtype = p.grad_dtype = _dtype_code(u.dtype)
     p.bbar_mode = int(kw.get("bbar_mode", SSM_BBAR_ZOH))
     p.delta_softplus = 1
-    p.u = p.delta = p.B = p.C = p.dout = p.A = p.du = p.ddelta = p.dB = p.dC = p.dA = 1  # sizes only
+    p.u = p.delta = p.B = p.C = p.dout = p.A = p.du = p.ddelta = p.dB = p.dC = p.dA = 256  # sizes only
     if checkpoints_given:
-        p.checkpoints, p.checkpoint_every = 1, 8
+        p.checkpoints, p.checkpoint_every = 256, 8
     return _lib.ssm_scan_bwd_workspace_size(ctypes.byref(p))
 
 

@@ -68,6 +68,8 @@ ssm_status check_fwd(const ssm_scan_fwd_params* p) {
     if (p->checkpoints != nullptr && (p->checkpoint_every <= 0 || p->checkpoint_every % 8 != 0))
         return fail(SSM_ERR_UNSUPPORTED, "checkpoint_every=%lld must be a positive multiple of 8",
                     (long long)p->checkpoint_every);
+    if (p->checkpoints != nullptr && (uintptr_t)p->checkpoints % 16 != 0)
+        return fail(SSM_ERR_MISALIGNED, "checkpoints must be 16-byte aligned");
     return SSM_OK;
 }
 
@@ -93,6 +95,8 @@ ssm_status check_bwd(const ssm_scan_bwd_params* p) {
         if (s->batch < 0 || s->row < 0) return fail(SSM_ERR_INVALID_ARG, "negative stride");
     if (p->checkpoints != nullptr && p->checkpoint_every <= 0)
         return fail(SSM_ERR_INVALID_ARG, "checkpoint_every must be positive when checkpoints are given");
+    if (p->checkpoints != nullptr && (uintptr_t)p->checkpoints % 16 != 0)
+        return fail(SSM_ERR_MISALIGNED, "checkpoints must be 16-byte aligned");
     return SSM_OK;
 }
 

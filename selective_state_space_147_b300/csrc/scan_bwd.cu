@@ -84,12 +84,15 @@ template <typename Tin, typename Tg, bool ZOH, bool ACC, bool HAS_Z>
 __device__ __forceinline__ void bwd_channel(const BwdArgs& a, float* sbc, float* red, float* red2, float* hb,
                                             int64_t b, int64_t d, int64_t chan, bool active, int tid) {
     const int lane = tid & 31, warp = tid >> 5;
-    float An[16], invA[16];
+    float An[16];
 #pragma unroll
-    for (int n = 0; n < 16; n++) {
-        An[n] = (n < a.dstate) ? __ldg(a.A + d * a.dstate + n) : 0.f;
-        invA[n] = (An[n] != 0.f) ? 1.f / An[n] : 0.f;
-    }
+    for (int n = 0; n < 16; n++) An[n] = (n < a.dstate) ? __ldg(a.A + d * a.dstate + n) : 0.f;
+    // 1/A at each use (SFU reciprocal on the fast path) instead of 16 more live registers;
+    // A == 0 never reaches the fast path (the flag routes it to the accurate kernel)
+    auto invA = [&](int n) -> float {
+        if constexpr (ACC) return (An[n] != 0.f) ? 1.f / An[n] : 0.f;
+        else return rcp_approx(An[n]);
+    };
     const float Dd = a.D ? __ldg(a.D + d) : 0.f;
     const float bias = a.bias ? __ldg(a.bias + d) : 0.f;
     // Idle lanes (d past dim) shadow the last channel to keep the warp uniform;
@@ -112,11 +115,26 @@ __device__ __forceinline__ void bwd_channel(const BwdArgs& a, float* sbc, float*
     const Tin* Cb = reinterpret_cast<const Tin*>(a.C) + b * a.sC_b;
     const float* ck = a.ckpt + chan * a.n_ckpt * a.dstate;
 
+    // 8-step sub-blocks, last to first; the inputs of the previous (earlier)
+    // sub-block are loaded while the current one is computed.
     const int64_t nsb = ceil_div(a.seqlen, (int64_t)kSub);
+    auto limit = [&](int64_t sb) -> int {
+        const int64_t r = a.seqlen - sb * kSub;
+        return (int)(r < kSub ? r : kSub);
+    };
+    Raw8<Tin> nu, nd, no, nz;
+    {
+        const int64_t t0 = (nsb - 1) * kSub;
+        const int lim = limit(nsb - 1);
+        nu.load(urow + t0, lim, a.vec_u);
+        nd.load(drow + t0, lim, a.vec_dt);
+        no.load(orow + t0, lim, a.vec_do);
+        if constexpr (HAS_Z) nz.load(zrow + t0, lim, a.vec_z);
+    }
     int64_t cur_tile = -1;
     for (int64_t sb = nsb - 1; sb >= 0; --sb) {
         const int64_t t0 = sb * kSub;
-        const int cnt = (int)((a.seqlen - t0) < kSub ? (a.seqlen - t0) : kSub);
+        const int cnt = limit(sb);
         const int64_t tile = t0 / kTile;
         if (tile != cur_tile) {
             __syncthreads();
@@ -125,36 +143,37 @@ __device__ __forceinline__ void bwd_channel(const BwdArgs& a, float* sbc, float*
             cur_tile = tile;
         }
         const float* bc0 = sbc + (t0 - tile * kTile) * kRow;
-
-        // inputs of the sub-block (zero past the end)
-        Raw8<Tin> ru, rd, rz, ro;
-        ru.load(urow + t0, cnt, a.vec_u);
-        rd.load(drow + t0, cnt, a.vec_dt);
-        ro.load(orow + t0, cnt, a.vec_do);
-        if constexpr (HAS_Z) rz.load(zrow + t0, cnt, a.vec_z);
-        float uj[kSub], dl[kSub], sg[kSub];
+        const Raw8<Tin> ru = nu, rd = nd, ro = no, rz = nz;
+        if (sb > 0) {
+            const int64_t tp = t0 - kSub;
+            nu.load(urow + tp, kSub, a.vec_u);
+            nd.load(drow + tp, kSub, a.vec_dt);
+            no.load(orow + tp, kSub, a.vec_do);
+            if constexpr (HAS_Z) nz.load(zrow + tp, kSub, a.vec_z);
+        }
+        float uj[kSub], dl[kSub];
 #pragma unroll
         for (int j = 0; j < kSub; j++) {
             uj[j] = ru.get(j);
             const float v = rd.get(j) + bias;
-            if (a.softplus) {
-                // delta = softplus(v), d delta / d v = sigmoid(v)
-                dl[j] = ACC ? softplus_accurate(v) : softplus_fast(v);
-                sg[j] = ACC ? 1.f / (1.f + expf(-v)) : rcp_approx(1.f + ex2_approx(-v * kLog2e));
-            } else {
-                dl[j] = v;
-                sg[j] = 1.f;
-            }
+            dl[j] = a.softplus ? (ACC ? softplus_accurate(v) : softplus_fast(v)) : v;
             if (j >= cnt) dl[j] = 0.f;
         }
 
         // forward recompute of the sub-block from its checkpoint into hb rows 0..8
         float h[16];
+        if (a.dstate == 16) {
 #pragma unroll
-        for (int n = 0; n < 16; n++) {
-            h[n] = (n < a.dstate) ? __ldg(ck + sb * a.dstate + n) : 0.f;
-            hb[n * 32] = h[n];
+            for (int q = 0; q < 4; q++) {
+                const float4 c4 = __ldg(reinterpret_cast<const float4*>(ck + sb * 16) + q);
+                h[4 * q] = c4.x; h[4 * q + 1] = c4.y; h[4 * q + 2] = c4.z; h[4 * q + 3] = c4.w;
+            }
+        } else {
+#pragma unroll
+            for (int n = 0; n < 16; n++) h[n] = (n < a.dstate) ? __ldg(ck + sb * a.dstate + n) : 0.f;
         }
+#pragma unroll
+        for (int n = 0; n < 16; n++) hb[n * 32] = h[n];
         float yv[kSub];
 #pragma unroll
         for (int j = 0; j < kSub; j++) {
@@ -165,7 +184,7 @@ __device__ __forceinline__ void bwd_channel(const BwdArgs& a, float* sbc, float*
                 const float x = dl[j] * An[n];
                 const float ab = ACC ? expf(x) : ex2_approx(x * kLog2e);
                 float coef;
-                if constexpr (ZOH) coef = ACC ? ((An[n] != 0.f) ? expm1f(x) * invA[n] : dl[j]) : (ab - 1.f) * invA[n];
+                if constexpr (ZOH) coef = ACC ? ((An[n] != 0.f) ? expm1f(x) * invA(n) : dl[j]) : (ab - 1.f) * invA(n);
                 else coef = dl[j];
                 h[n] = fmaf(ab, h[n], coef * row[n] * uj[j]);
                 hb[((j + 1) * 16 + n) * 32] = h[n];
@@ -200,7 +219,7 @@ __device__ __forceinline__ void bwd_channel(const BwdArgs& a, float* sbc, float*
                 const float x = dl[j] * An[n];
                 const float ab = ACC ? expf(x) : ex2_approx(x * kLog2e);
                 float coef;
-                if constexpr (ZOH) coef = ACC ? ((An[n] != 0.f) ? expm1f(x) * invA[n] : dl[j]) : (ab - 1.f) * invA[n];
+                if constexpr (ZOH) coef = ACC ? ((An[n] != 0.f) ? expm1f(x) * invA(n) : dl[j]) : (ab - 1.f) * invA(n);
                 else coef = dl[j];
                 const float G = fmaf(dy, Cv, Gc[n]);
                 r2[16 + n] = dy * hcur;                          // dC partial
@@ -218,7 +237,7 @@ __device__ __forceinline__ void bwd_channel(const BwdArgs& a, float* sbc, float*
                         dAacc[n] = fmaf(dcoef * dl[j] * dl[j], phi_zoh(x, ab), dAacc[n]);
                     } else {
                         // dcoef/dA = (delta Abar - coef)/A
-                        dAacc[n] = fmaf(dcoef * invA[n], q - coef, dAacc[n]);
+                        dAacc[n] = fmaf(dcoef * invA(n), q - coef, dAacc[n]);
                     }
                 } else {
                     dd = fmaf(da * An[n], ab, dd + dcoef);
@@ -234,7 +253,12 @@ __device__ __forceinline__ void bwd_channel(const BwdArgs& a, float* sbc, float*
             red[(warp * kSub + j) * 32 + lane] = s;
             __syncwarp();
             dDacc = fmaf(dy, uj[j], dDacc);
-            const float dv = dd * sg[j];
+            float dv = dd;
+            if (a.softplus) {
+                // d softplus(v) / dv = sigmoid(v)
+                const float v = rd.get(j) + bias;
+                dv *= ACC ? 1.f / (1.f + expf(-v)) : rcp_approx(1.f + ex2_approx(-v * kLog2e));
+            }
             dbacc += dv;
             duo[j] = du;
             ddo[j] = dv;
@@ -267,9 +291,26 @@ __device__ __forceinline__ void bwd_channel(const BwdArgs& a, float* sbc, float*
     a.part_bias[chan] = dbacc;
 }
 
-template <typename Tin, typename Tg, bool ZOH, bool HAS_Z>
+// flag[0] = 1 when some A[d, n] == 0 (the ZOH limit needs the accurate path)
+__global__ void bwd_check_A_kernel(const float* A, int64_t n, int* flag) {
+    int found = 0;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        if (A[i] == 0.f) found = 1;
+    if (__syncthreads_or(found) && threadIdx.x == 0) flag[0] = 1;
+}
+
+// ACC = true: accurate library math (float32 inputs, or any A == 0 with ZOH);
+// ACC = false: SFU fast math.  Both variants are launched; the one that does
+// not apply returns at once after reading the flag, so the choice needs no
+// host synchronisation and each variant keeps its own register budget.
+template <typename Tin, typename Tg, bool ZOH, bool HAS_Z, bool ACC>
 __global__ void __launch_bounds__(kBwdThreads)
-scan_bwd_kernel(const BwdArgs a) {
+scan_bwd_kernel(const BwdArgs a, const int* flag) {
+    if constexpr (!ACC) {
+        if (*flag) return;
+    } else if constexpr (sizeof(Tin) == 2) {
+        if (!*flag) return;
+    }
     extern __shared__ __align__(16) float smem_f[];
     float* sbc = smem_f;                                   // kTile x kRow
     float* red = sbc + kTile * kRow;                       // [warp][8][32]
@@ -283,16 +324,7 @@ scan_bwd_kernel(const BwdArgs a) {
     const int64_t chan = b * a.dim + d;
     float* hb = hbuf + warp * 9 * 16 * 32 + lane;
     float* r2 = red2 + warp * 32 * kRed2;
-    // fast SFU path unless inputs are fp32 or the CTA sees A == 0 (ZOH limit)
-    bool acc = sizeof(Tin) == 4;
-    if constexpr (ZOH) {
-        bool zero = false;
-        for (int n = 0; n < a.dstate; n++)
-            if (__ldg(a.A + d * a.dstate + n) == 0.f) zero = true;
-        acc = acc || __syncthreads_or(zero);
-    }
-    if (acc) bwd_channel<Tin, Tg, ZOH, true, HAS_Z>(a, sbc, red, r2, hb, b, d, chan, active, tid);
-    else if constexpr (sizeof(Tin) == 2) bwd_channel<Tin, Tg, ZOH, false, HAS_Z>(a, sbc, red, r2, hb, b, d, chan, active, tid);
+    bwd_channel<Tin, Tg, ZOH, ACC, HAS_Z>(a, sbc, red, r2, hb, b, d, chan, active, tid);
 }
 
 constexpr int kBwdSmemBytes = (kTile * kRow + kBwdWarps * kSub * 32 + kBwdWarps * 32 * kRed2 + kBwdWarps * 9 * 16 * 32) * 4;
@@ -373,7 +405,7 @@ static BwdLayout bwd_layout(const ssm_scan_bwd_params* p, int num_sms) {
     l.part_bc = round256((size_t)(p->batch * nblk * 2 * 16 * p->seqlen) * 4);
     l.part_A = round256((size_t)(chans * 16) * 4);
     l.part_D = round256((size_t)chans * 4);
-    l.total = l.ckpt + l.fwd_ws + l.part_bc + l.part_A + 2 * l.part_D;
+    l.total = l.ckpt + l.fwd_ws + l.part_bc + l.part_A + 2 * l.part_D + 256;   // + the A == 0 flag
     return l;
 }
 
@@ -387,17 +419,28 @@ static bool al16(const void* ptr, ssm_strides s, int esize) {
 }
 
 template <typename Tin, typename Tg>
-static cudaError_t launch_bwd_typed(const BwdArgs& a, bool zoh, bool has_z, cudaStream_t st) {
+static cudaError_t launch_bwd_typed(const BwdArgs& a, bool zoh, bool has_z, int* flag, cudaStream_t st) {
     const dim3 grid((unsigned)a.nblk, (unsigned)a.batch);
     auto go = [&](auto kern) -> cudaError_t {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kBwdSmemBytes);
         if (e != cudaSuccess) return e;
-        kern<<<grid, kBwdThreads, kBwdSmemBytes, st>>>(a);
+        kern<<<grid, kBwdThreads, kBwdSmemBytes, st>>>(a, flag);
         count_launches(1);
         return cudaGetLastError();
     };
-    if (zoh) return has_z ? go(scan_bwd_kernel<Tin, Tg, true, true>) : go(scan_bwd_kernel<Tin, Tg, true, false>);
-    return has_z ? go(scan_bwd_kernel<Tin, Tg, false, true>) : go(scan_bwd_kernel<Tin, Tg, false, false>);
+    auto pair = [&](auto fast, auto acc) -> cudaError_t {
+        if constexpr (sizeof(Tin) == 2) {
+            cudaError_t e = go(fast);
+            if (e != cudaSuccess) return e;
+        }
+        return go(acc);
+    };
+    if (zoh) return has_z ? pair(scan_bwd_kernel<Tin, Tg, true, true, false>, scan_bwd_kernel<Tin, Tg, true, true, true>)
+                          : pair(scan_bwd_kernel<Tin, Tg, true, false, false>, scan_bwd_kernel<Tin, Tg, true, false, true>);
+    // the simplified rule has no A == 0 limit: the fast path always applies to bf16
+    if constexpr (sizeof(Tin) == 2)
+        return has_z ? go(scan_bwd_kernel<Tin, Tg, false, true, false>) : go(scan_bwd_kernel<Tin, Tg, false, false, false>);
+    return has_z ? go(scan_bwd_kernel<Tin, Tg, false, true, true>) : go(scan_bwd_kernel<Tin, Tg, false, false, true>);
 }
 
 cudaError_t launch_scan_bwd(const ssm_scan_bwd_params* p, void* ws, int num_sms, cudaStream_t st) {
@@ -463,13 +506,20 @@ cudaError_t launch_scan_bwd(const ssm_scan_bwd_params* p, void* ws, int num_sms,
     a.part_bias = reinterpret_cast<float*>(wp + l.part_bc + l.part_A + l.part_D);
     const bool zoh = p->bbar_mode == SSM_BBAR_ZOH;
     const bool has_z = p->z != nullptr;
-    cudaError_t e;
+    int* flag = reinterpret_cast<int*>(wp + l.part_bc + l.part_A + 2 * l.part_D);
+    cudaError_t e = cudaMemsetAsync(flag, 0, sizeof(int), st);
+    if (e != cudaSuccess) return e;
+    if (zoh) {
+        const int64_t nA = p->dim * p->dstate;
+        bwd_check_A_kernel<<<(unsigned)(ceil_div(nA, 256) < 1024 ? ceil_div(nA, 256) : 1024), 256, 0, st>>>(p->A, nA, flag);
+        count_launches(1);
+    }
     if (p->in_dtype == SSM_BF16) {
-        e = p->grad_dtype == SSM_BF16 ? launch_bwd_typed<__nv_bfloat16, __nv_bfloat16>(a, zoh, has_z, st)
-                                      : launch_bwd_typed<__nv_bfloat16, float>(a, zoh, has_z, st);
+        e = p->grad_dtype == SSM_BF16 ? launch_bwd_typed<__nv_bfloat16, __nv_bfloat16>(a, zoh, has_z, flag, st)
+                                      : launch_bwd_typed<__nv_bfloat16, float>(a, zoh, has_z, flag, st);
     } else {
-        e = p->grad_dtype == SSM_BF16 ? launch_bwd_typed<float, __nv_bfloat16>(a, zoh, has_z, st)
-                                      : launch_bwd_typed<float, float>(a, zoh, has_z, st);
+        e = p->grad_dtype == SSM_BF16 ? launch_bwd_typed<float, __nv_bfloat16>(a, zoh, has_z, flag, st)
+                                      : launch_bwd_typed<float, float>(a, zoh, has_z, flag, st);
     }
     if (e != cudaSuccess) return e;
     const dim3 g2((unsigned)ceil_div(p->seqlen, 256), (unsigned)p->dstate, (unsigned)(2 * p->batch));

@@ -219,6 +219,21 @@ __device__ __forceinline__ void scan_block8(pf2 (&h2)[NP], const pf2 (&A2)[NP], 
     for (int j = 0; j < kSub; j++) yacc[j] = pf2_sum(y2[j]);
 }
 
+// Store this lane's NPL checkpoint values (states n_base ..): 16-byte vector
+// stores when the row has all 16 states, element stores otherwise.
+template <int NPL>
+__device__ __forceinline__ void store_ckpt(float* row, int n_base, int dstate, const float (&v)[NPL]) {
+    if (dstate == kNMax) {
+#pragma unroll
+        for (int q = 0; q < NPL / 4; q++)
+            reinterpret_cast<float4*>(row + n_base)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < NPL; j++)
+            if (n_base + j < dstate) row[n_base + j] = v[j];
+    }
+}
+
 // Per-step epilogue shared by both paths: reduce C.h over the G lanes of the
 // channel, add D u, apply the gate.
 template <int G, bool ACC, bool HAS_Z>
@@ -254,6 +269,7 @@ __device__ __forceinline__ void scan_warp(const FwdArgs& a, float* sbc_all, int6
     const Tin* Cb = reinterpret_cast<const Tin*>(a.C) + b * a.sC_b;
     float* ck = (MODE == kFull && a.ckpt != nullptr)
                     ? a.ckpt + (b * a.dim + d) * a.n_ckpt * a.dstate : nullptr;
+    int64_t next_ck = ceil_div(t_begin, a.ckpt_K) * a.ckpt_K;   // next step that starts a checkpoint
 
     float sd = 0.f, sd_c = 0.f;   // Kahan sum of delta (summary pass)
     Raw8<Tin> ru[3], rd[3], rz[3];
@@ -276,10 +292,9 @@ __device__ __forceinline__ void scan_warp(const FwdArgs& a, float* sbc_all, int6
         for (int64_t t0 = tt; t0 < tile_end; t0 += kSub) {
             load_sub(2, t0 + 2 * kSub);
             const int cnt = (int)((tile_end - t0) < kSub ? (tile_end - t0) : kSub);
-            if (ck != nullptr && (t0 % a.ckpt_K) == 0 && active) {
-#pragma unroll
-                for (int j = 0; j < NPL; j++)
-                    if (n_base + j < a.dstate) ck[(t0 / a.ckpt_K) * a.dstate + n_base + j] = h[j];
+            if (ck != nullptr && t0 == next_ck) {
+                if (active) store_ckpt<NPL>(ck + (t0 / a.ckpt_K) * a.dstate, n_base, a.dstate, h);
+                next_ck += a.ckpt_K;
             }
             float yout[kSub];
 #pragma unroll
@@ -466,6 +481,7 @@ __device__ __forceinline__ void scan_cta_async(const FwdArgs& a, unsigned char* 
     Tout* orow = (MODE == kFull && a.out != nullptr) ? reinterpret_cast<Tout*>(a.out) + b * a.so_b + d * a.so_d : nullptr;
     float* ck = (MODE == kFull && a.ckpt != nullptr)
                     ? a.ckpt + (b * a.dim + d) * a.n_ckpt * a.dstate : nullptr;
+    int64_t next_ck = ceil_div(t_begin, a.ckpt_K) * a.ckpt_K;   // next step that starts a checkpoint
     float* bcf = reinterpret_cast<float*>(smem + kStages * kStage);
     constexpr bool kZ = HAS_Z && MODE == kFull;
 
@@ -515,12 +531,14 @@ __device__ __forceinline__ void scan_cta_async(const FwdArgs& a, unsigned char* 
             const int64_t t0 = tt + c * kSub;
             if (t0 >= t_end) break;
             const int cnt = (int)((t_end - t0) < kSub ? (t_end - t0) : kSub);
-            if (ck != nullptr && (t0 % a.ckpt_K) == 0 && active) {
+            if (ck != nullptr && t0 == next_ck) {
+                if (active) {
+                    float hv[NPL];
 #pragma unroll
-                for (int j = 0; j < NPL; j++) {
-                    const float hv = (j & 1) ? pf2_hi(h2[j >> 1]) : pf2_lo(h2[j >> 1]);
-                    if (n_base + j < a.dstate) ck[(t0 / a.ckpt_K) * a.dstate + n_base + j] = hv;
+                    for (int j = 0; j < NPL; j++) hv[j] = (j & 1) ? pf2_hi(h2[j >> 1]) : pf2_lo(h2[j >> 1]);
+                    store_ckpt<NPL>(ck + (t0 / a.ckpt_K) * a.dstate, n_base, a.dstate, hv);
                 }
+                next_ck += a.ckpt_K;
             }
             const uint4 wu = *reinterpret_cast<const uint4*>(st + 0 * kSeq + swz(row, c));
             const uint4 wd = *reinterpret_cast<const uint4*>(st + 1 * kSeq + swz(row, c));
