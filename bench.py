@@ -4,7 +4,8 @@
 One step = one pass of the hot path over one batch of the Mamba-1.4B-shaped
 layer (batch 8, d_inner 4096, d_state 16, L 16384, bf16 activations, fp32
 state, zero-order hold): causal conv1d + SiLU -> fused selective-scan forward
-(-> backward with recompute, when the library provides it).  Inputs are
+(writing h checkpoints every 8 steps) -> selective-scan backward with
+recompute of h (all nine gradients).  Inputs are
 synthetic (seeded counter-based generator), resident in HBM and larger than
 L2 (several GB per step), so no L2 flush is needed between steps.
 
@@ -158,6 +159,24 @@ def fwd_work(b, d, L, N, zoh=True, io_bytes=2):
     return dict(bytes=byts, fp32=ct * (N * per_n + per_ct), sfu=ct * (N + 4))
 
 
+def fwd_ckpt_bytes(b, d, L, N):
+    """Checkpoints of h every 8 steps written by the forward (fp32)."""
+    return b * d * ((L + 7) // 8) * N * 4
+
+
+def bwd_work(b, d, L, N, io_bytes=2):
+    """Compulsory HBM bytes: u, delta, z, dout read and du, ddelta, dz written
+    (io_bytes each per channel-token), the fp32 checkpoints read (N floats per
+    8 steps), B, C read and dB, dC written (fp32).  Operations per (channel,
+    step, state): forward recompute 5 FP32 + readout for the gate 1, reverse
+    adjoint and gradient terms 20, the cross-channel sums of dB, dC 2 -> 28
+    FP32, and 2 exponentials; per (channel, step) about 15 FP32 and 4 SFU
+    (softplus and its derivative, the gate and its derivative)."""
+    ct = b * d * L
+    byts = 7 * io_bytes * ct + (ct // 8) * N * 4 + 2 * N * io_bytes * b * L + 2 * N * 4 * b * L
+    return dict(bytes=byts, fp32=ct * (N * 28 + 15), sfu=ct * (N * 2 + 4))
+
+
 def roofline(work, seconds, hbm_gbs, sms, sm_mhz, hbm_src, clock_src):
     """Slowest of HBM, FP32 pipe and SFU for this kernel's algorithmic work."""
     f = sm_mhz * 1e6
@@ -188,15 +207,18 @@ def roofline(work, seconds, hbm_gbs, sms, sm_mhz, hbm_src, clock_src):
 def make_inputs(device, seed, cfg):
     import synthetic as S
     b, d, L, N, W = cfg["batch"], cfg["dim"], cfg["seqlen"], cfg["dstate"], cfg["width"]
-    g = S.scan_inputs(seed, b, d, L, N, dtype=torch.bfloat16, device=device)
+    g = S.scan_inputs(seed, b, d, L, N, dtype=torch.bfloat16, device=device, with_dout=True)
     c = S.conv_inputs(seed, b, d, L, W, dtype=torch.bfloat16, device=device)
     g["x"], g["w"] = c["x"], c["w"]
     g["xc"] = torch.empty_like(g["x"])
     g["y"] = torch.empty(b, d, L, dtype=torch.bfloat16, device=device)
+    g["ckpt"] = torch.empty(b, d, (L + 7) // 8, N, dtype=torch.float32, device=device)
+    g["grads"] = None
     return g
 
 
 def step(L, g, ev=None):
+    """conv1d + SiLU -> scan forward (with checkpoints) -> scan backward."""
     if ev is not None:
         ev[0].record()
     L.causal_conv1d_silu(g["x"], g["w"], out=g["xc"])
@@ -204,9 +226,15 @@ def step(L, g, ev=None):
         ev[1].record()
     L.ssm_scan_fwd(g["xc"], g["dt"], g["A"], g["B"], g["C"], D=g["D"], delta_bias=g["bias"], z=g["z"],
                    out=g["y"], bbar_mode=L.SSM_BBAR_ZOH, delta_softplus=True,
-                   workspace=g.get("ws"))
+                   checkpoints=g["ckpt"], checkpoint_every=8, workspace=g.get("ws"))
     if ev is not None:
         ev[2].record()
+    g["grads"] = L.ssm_scan_bwd(g["xc"], g["dt"], g["A"], g["B"], g["C"], g["dout"], D=g["D"],
+                                delta_bias=g["bias"], z=g["z"], checkpoints=g["ckpt"], checkpoint_every=8,
+                                bbar_mode=L.SSM_BBAR_ZOH, delta_softplus=True, grads=g["grads"],
+                                workspace=g.get("ws_bwd"))
+    if ev is not None:
+        ev[3].record()
 
 
 def bench_decode(L, device, cfg, reps: int):
@@ -271,8 +299,9 @@ def bench_decode(L, device, cfg, reps: int):
 # ---------------------------------------------------------------------------
 # CPU oracle (baseline arm)
 def oracle_sample_rate(channels: int, threads: int, cfg, seed: int):
-    """Run the fp64 oracle (conv + ZOH scan) on `channels` channels of batch row 0
-    over the full sequence; returns (channel-tokens/s, wall seconds)."""
+    """Run the fp64 oracle over the step's hot path -- conv + SiLU, ZOH scan
+    forward, scan backward -- on `channels` channels of batch row 0 over the full
+    sequence; returns (channel-tokens/s, wall seconds)."""
     import oracle
     import synthetic as S
     L, N, W = cfg["seqlen"], cfg["dstate"], cfg["width"]
@@ -281,6 +310,7 @@ def oracle_sample_rate(channels: int, threads: int, cfg, seed: int):
     x = S.rows_at(seed, S.STREAM["x"], rows, L).to(torch.bfloat16).double()[None]
     dt = S.rows_at(seed, S.STREAM["dt"], rows, L).to(torch.bfloat16).double()[None]
     z = S.rows_at(seed, S.STREAM["z"], rows, L).to(torch.bfloat16).double()[None]
+    dout = S.rows_at(seed, S.STREAM["dout"], rows, L).to(torch.bfloat16).double()[None]
     B = S.normal(seed, S.STREAM["B"], (1, N, L), torch.bfloat16).double()
     C = S.normal(seed, S.STREAM["C"], (1, N, L), torch.bfloat16).double()
     w = S.normal(seed, S.STREAM["w"], (d, W), torch.float32, std=0.5)[:channels].double()
@@ -290,6 +320,7 @@ def oracle_sample_rate(channels: int, threads: int, cfg, seed: int):
     t0 = time.perf_counter()
     xc = oracle.conv1d_silu(x, w)
     oracle.scan_fwd(xc, dt, A, B, C, Dp, bias, z, zoh=True, threads=threads)
+    oracle.scan_bwd(xc, dt, A, B, C, dout, Dp, bias, z, zoh=True, threads=threads)
     wall = time.perf_counter() - t0
     return channels * L / wall, wall
 
@@ -308,8 +339,8 @@ def cpu_baseline(cfg, seed: int, target_s: float = 10.0):
     n = calibrated_channels(threads, cfg, seed, target_s)
     rate, wall = oracle_sample_rate(n, threads, cfg, seed)
     return {"value": round(rate, 1), "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"{n} channels of batch row 0, full L={cfg['seqlen']}, conv1d+SiLU then ZOH scan "
-                      f"forward in fp64 ({wall:.1f} s wall on {threads} threads)"}
+            "sample": f"{n} channels of batch row 0, full L={cfg['seqlen']}: conv1d+SiLU, ZOH scan forward "
+                      f"and backward in fp64 ({wall:.1f} s wall on {threads} threads)"}
 
 
 def run_reference(args):
@@ -338,8 +369,8 @@ def run_reference(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(cfg),
         "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": threads, "kind": "oracle",
-                         "sample": f"each step: {n} channels of batch row 0, full L={cfg['seqlen']}, "
-                                   "conv1d+SiLU then ZOH scan forward, fp64 oracle"},
+                         "sample": f"each step: {n} channels of batch row 0, full L={cfg['seqlen']}: "
+                                   "conv1d+SiLU, ZOH scan forward and backward, fp64 oracle"},
         "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -347,12 +378,13 @@ def run_reference(args):
 
 
 def workload_config(cfg):
-    return {"workload": "mamba-1.4b-layer: causal conv1d+SiLU -> fused selective-scan forward "
+    return {"workload": "mamba-1.4b-layer training pass: causal conv1d+SiLU -> fused selective-scan forward "
+                        "(checkpoints every 8 steps) -> selective-scan backward with recompute "
                         f"(batch {cfg['batch']}, d_inner {cfg['dim']}, d_state {cfg['dstate']}, "
                         f"L {cfg['seqlen']}, ZOH, softplus delta, D skip, silu(z) gate)",
             "batch": cfg["batch"], "dim": cfg["dim"], "dstate": cfg["dstate"], "seqlen": cfg["seqlen"],
             "io_dtype": "bf16", "state_dtype": "f32",
-            "l2": "inputs larger than L2 (about 4.3 GB read+written per step), no flush",
+            "l2": "inputs larger than L2 (about 30 GB read+written per step), no flush",
             "parallelism": "replicas (one independent layer problem per GPU)"}
 
 
@@ -384,6 +416,7 @@ def main(argv=None):
     ws_bytes = L.ssm_scan_fwd_workspace_size(g["xc"], g["A"])
     if ws_bytes:
         g["ws"] = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
+    g["ws_bwd"] = torch.empty(L.ssm_scan_bwd_workspace_size(g["xc"], g["A"]), dtype=torch.uint8, device=device)
     props = torch.cuda.get_device_properties(device)
     sms = props.multi_processor_count
 
@@ -392,7 +425,7 @@ def main(argv=None):
     torch.cuda.synchronize()
 
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local)
     sampler.start()
@@ -411,6 +444,7 @@ def main(argv=None):
     ms_total = max_over_ranks(ms_total, world, device)
     conv_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     fwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    bwd_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
 
     b, d, Lq, N = cfg["batch"], cfg["dim"], cfg["seqlen"], cfg["dstate"]
     ct_step = b * d * Lq
@@ -419,13 +453,18 @@ def main(argv=None):
     sm_mhz = (clocks or {}).get("sm_mhz") or 2032.0
     clock_src = "median sampled under load" if clocks and clocks.get("sm_mhz") else "max clock, unsampled"
     fw = fwd_work(b, d, Lq, N)
+    fw["bytes"] += fwd_ckpt_bytes(b, d, Lq, N)
     cw = conv_work(b, d, Lq)
+    bw = bwd_work(b, d, Lq, N)
     kern = {
         "causal_conv1d_silu": dict(ms=round(conv_ms, 4), share=round(conv_ms / (ms_total / K), 4),
                                    roofline=roofline(cw, conv_ms * 1e-3, hbm_gbs, sms, sm_mhz, hbm_src, clock_src)),
         "ssm_scan_fwd": dict(ms=round(fwd_ms, 4), share=round(fwd_ms / (ms_total / K), 4),
                              channel_tokens_per_s=round(ct_step / (fwd_ms * 1e-3), 1),
                              roofline=roofline(fw, fwd_ms * 1e-3, hbm_gbs, sms, sm_mhz, hbm_src, clock_src)),
+        "ssm_scan_bwd": dict(ms=round(bwd_ms, 4), share=round(bwd_ms / (ms_total / K), 4),
+                             channel_tokens_per_s=round(ct_step / (bwd_ms * 1e-3), 1),
+                             roofline=roofline(bw, bwd_ms * 1e-3, hbm_gbs, sms, sm_mhz, hbm_src, clock_src)),
     }
     dominant = max(kern, key=lambda k: kern[k]["ms"])
     roof = dict(kern[dominant]["roofline"])
@@ -435,13 +474,15 @@ def main(argv=None):
     # end to end through the public API with host buffers
     e2e = None
     if args.e2e_steps > 0:
-        names_in = ("x", "dt", "z", "B", "C")
+        names_in = ("x", "dt", "z", "B", "C", "dout")
         host = {k: torch.empty(g[k].shape, dtype=g[k].dtype, pin_memory=True) for k in names_in}
         for k in names_in:
             host[k].copy_(g[k])
-        y_host = torch.empty(g["y"].shape, dtype=g["y"].dtype, pin_memory=True)
+        outs = {"y": g["y"]}
+        outs.update({k: v for k, v in g["grads"].items() if v is not None and k != "dh0"})
+        out_host = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs.items()}
         h2d = sum(host[k].numel() * host[k].element_size() for k in names_in)
-        d2h = y_host.numel() * y_host.element_size()
+        d2h = sum(v.numel() * v.element_size() for v in out_host.values())
         torch.cuda.synchronize()
         barrier(world)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -450,14 +491,17 @@ def main(argv=None):
             for k in names_in:
                 g[k].copy_(host[k], non_blocking=True)
             step(L, g)
-            y_host.copy_(g["y"], non_blocking=True)
+            out_host["y"].copy_(g["y"], non_blocking=True)
+            for k in out_host:
+                if k != "y":
+                    out_host[k].copy_(g["grads"][k], non_blocking=True)
         e1.record()
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, device)
         e2e = {"value": round(ct_step * args.e2e_steps * world / (e2e_ms * 1e-3), 1), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
                "ms_per_step": round(e2e_ms / args.e2e_steps, 2)}
-        del host, y_host
+        del host, out_host
 
     decode = None
     if not args.no_decode:
