@@ -291,6 +291,269 @@ __device__ __forceinline__ void bwd_channel(const BwdArgs& a, float* sbc, float*
     a.part_bias[chan] = dbacc;
 }
 
+// ---------------------------------------------------------------------------
+// Fast (SFU) backward of one channel per thread on packed f32x2 registers.
+//
+// The adjoint recurrence G_t = dy_t C_t + Abar_{t+1} G_{t+1} is independent per
+// state, so the loop over state pairs is the outer one: for each pair the 8
+// steps of the sub-block are recomputed forward from the checkpoint (h, Abar
+// and the input coefficient stay in registers) and then walked in reverse.
+// Only the per-step sums over states (du, ddelta and, with the gate, the
+// readout y used by dz) live across pairs, as packed per-step accumulators.
+// After each pair the lane's 32 dB/dC partials (8 steps x 2 states x 2
+// tensors) are summed over the warp's 32 channels through a shared-memory
+// transpose (128-bit writes, 64-bit reads, both at the minimum number of
+// wavefronts with rows of 36 floats).
+constexpr int kRowF = 36;   // B/C row of one step: [pair p: B_2p B_2p+1 C_2p C_2p+1] x 8, pad
+constexpr int kRedF = 36;   // transpose row
+constexpr int kBwdFastSmemFloats = kTile * kRowF + kBwdWarps * 8 * 32 + kBwdWarps * 32 * kRedF + kBwdWarps * 8 * 32 * 4;
+
+// B[b, :, t0 : t0+64] and C as fp32 rows with B and C of a state pair adjacent,
+// so that one 128-bit broadcast read gives both: thread s (< 64) stages B of step
+// t0+s, thread 64+s C of step t0+s.  Entries past seqlen or dstate are zero.
+template <typename Tin>
+__device__ __forceinline__ void stage_bc_pairs(float* sbc, const BwdArgs& a, const Tin* Bb, const Tin* Cb,
+                                               int64_t t0, int tid) {
+    const int s = tid & 63, tsr = tid >> 6;
+    const int64_t t = t0 + s;
+    const Tin* base = tsr == 0 ? Bb : Cb;
+    const int64_t sn = tsr == 0 ? a.sB_n : a.sC_n;
+    float2* row = reinterpret_cast<float2*>(sbc + s * kRowF + tsr * 2);
+#pragma unroll
+    for (int p = 0; p < 8; p++) {
+        const int n = 2 * p;
+        const float v0 = (n < a.dstate && t < a.seqlen) ? Elem<Tin>::load(base + n * sn + t) : 0.f;
+        const float v1 = (n + 1 < a.dstate && t < a.seqlen) ? Elem<Tin>::load(base + (n + 1) * sn + t) : 0.f;
+        row[2 * p] = make_float2(v0, v1);
+    }
+}
+
+// scalar x packed: (s * v.lo, s * v.hi) and (s * v.lo + c.lo, s * v.hi + c.hi)
+__device__ __forceinline__ pf2 pf2_scale(float s, pf2 v) { return pf2_make(s * pf2_lo(v), s * pf2_hi(v)); }
+__device__ __forceinline__ pf2 pf2_scale_add(float s, pf2 v, pf2 c) {
+    return pf2_make(fmaf(s, pf2_lo(v), pf2_lo(c)), fmaf(s, pf2_hi(v), pf2_hi(c)));
+}
+
+template <typename Tin, typename Tg, bool ZOH, bool HAS_Z>
+__device__ __forceinline__ void bwd_channel_fast(const BwdArgs& a, float* sbc, float* red, float* r2w, ulonglong2* cst,
+                                                 int64_t b, int64_t d, int64_t chan, bool active, int tid) {
+    constexpr int NP = 8;
+    const int lane = tid & 31, warp = tid >> 5;
+    // per-pair constants {A, 1/A} of this lane's channel in shared memory (own entries only);
+    // states past dstate get A = -1 with B = C = h = G = 0, so they contribute nothing
+    pf2 Gc[NP], dA1[NP], dA2[NP];
+#pragma unroll
+    for (int p = 0; p < NP; p++) {
+        float av[2], ia[2], gv[2];
+#pragma unroll
+        for (int q = 0; q < 2; q++) {
+            const int n = 2 * p + q;
+            const bool on = n < a.dstate;
+            av[q] = on ? __ldg(a.A + d * a.dstate + n) : -1.f;
+            ia[q] = ZOH ? rcp_approx(av[q]) : 0.f;   // A != 0 here (A == 0 takes the accurate kernel)
+            gv[q] = (active && on && a.dhN != nullptr) ? __ldg(a.dhN + chan * a.dstate + n) : 0.f;
+        }
+        cst[p * 32 + lane] = make_ulonglong2(pf2_make(av[0], av[1]), pf2_make(ia[0], ia[1]));
+        Gc[p] = pf2_make(gv[0], gv[1]);
+        dA1[p] = 0ull;
+        dA2[p] = 0ull;
+    }
+    const pf2 LOG2E2 = pf2_make(kLog2e, kLog2e);
+    const float Dd = a.D ? __ldg(a.D + d) : 0.f;
+    const float bias = a.bias ? __ldg(a.bias + d) : 0.f;
+    float dDacc = 0.f, dbacc = 0.f;
+    const Tin* urow = reinterpret_cast<const Tin*>(a.u) + b * a.su_b + d * a.su_d;
+    const Tin* drow = reinterpret_cast<const Tin*>(a.dt) + b * a.sdt_b + d * a.sdt_d;
+    const Tin* zrow = HAS_Z ? reinterpret_cast<const Tin*>(a.z) + b * a.sz_b + d * a.sz_d : nullptr;
+    const Tin* orow = reinterpret_cast<const Tin*>(a.dout) + b * a.sdo_b + d * a.sdo_d;
+    Tg* durow = reinterpret_cast<Tg*>(a.du) + b * a.sdu_b + d * a.sdu_d;
+    Tg* ddrow = reinterpret_cast<Tg*>(a.ddt) + b * a.sddt_b + d * a.sddt_d;
+    Tg* dzrow = HAS_Z ? reinterpret_cast<Tg*>(a.dz) + b * a.sdz_b + d * a.sdz_d : nullptr;
+    const Tin* Bb = reinterpret_cast<const Tin*>(a.B) + b * a.sB_b;
+    const Tin* Cb = reinterpret_cast<const Tin*>(a.C) + b * a.sC_b;
+    const float* ck = a.ckpt + chan * a.n_ckpt * a.dstate;
+    float* r2 = r2w + lane * kRedF;
+
+    const int64_t nsb = ceil_div(a.seqlen, (int64_t)kSub);
+    auto limit = [&](int64_t sb) -> int {
+        const int64_t r = a.seqlen - sb * kSub;
+        return (int)(r < kSub ? r : kSub);
+    };
+    Raw8<Tin> nu, nd, no, nz;
+    {
+        const int64_t t0 = (nsb - 1) * kSub;
+        const int lim = limit(nsb - 1);
+        nu.load(urow + t0, lim, a.vec_u);
+        nd.load(drow + t0, lim, a.vec_dt);
+        no.load(orow + t0, lim, a.vec_do);
+        if constexpr (HAS_Z) nz.load(zrow + t0, lim, a.vec_z);
+    }
+    int64_t cur_tile = -1;
+#pragma unroll 1
+    for (int64_t sb = nsb - 1; sb >= 0; --sb) {
+        const int64_t t0 = sb * kSub;
+        const int cnt = limit(sb);
+        const int64_t tile = t0 / kTile;
+        if (tile != cur_tile) {
+            __syncthreads();
+            stage_bc_pairs<Tin>(sbc, a, Bb, Cb, tile * kTile, tid);
+            __syncthreads();
+            cur_tile = tile;
+        }
+        const float* bc0 = sbc + (t0 - tile * kTile) * kRowF;
+        const Raw8<Tin> ru = nu, rd = nd, ro = no, rz = nz;
+        if (sb > 0) {
+            const int64_t tp = t0 - kSub;
+            nu.load(urow + tp, kSub, a.vec_u);
+            nd.load(drow + tp, kSub, a.vec_dt);
+            no.load(orow + tp, kSub, a.vec_do);
+            if constexpr (HAS_Z) nz.load(zrow + tp, kSub, a.vec_z);
+        }
+        // per-step scalars; steps past the end get delta = u = dy = 0, which makes
+        // them identity steps that add nothing to any gradient
+        float dl[kSub], uj[kSub], dy[kSub];
+#pragma unroll
+        for (int j = 0; j < kSub; j++) {
+            const bool in = j < cnt;
+            const float v = rd.get(j) + bias;
+            dl[j] = in ? (a.softplus ? softplus_fast(v) : v) : 0.f;
+            uj[j] = in ? ru.get(j) : 0.f;
+            const float go = (active && in) ? ro.get(j) : 0.f;
+            if constexpr (HAS_Z) {
+                const float zj = rz.get(j);
+                dy[j] = go * zj * rcp_approx(1.f + ex2_approx(-zj * kLog2e));
+            } else {
+                dy[j] = go;
+            }
+        }
+        pf2 du2[kSub], dd2[kSub], yv2[kSub];
+#pragma unroll
+        for (int j = 0; j < kSub; j++) du2[j] = dd2[j] = yv2[j] = 0ull;
+
+#pragma unroll
+        for (int p = 0; p < NP; p++) {
+            const ulonglong2 kc = cst[p * 32 + lane];
+            const pf2 A2 = kc.x, IA = kc.y;
+            const pf2 A2L = pf2_mul(A2, LOG2E2);
+            const pf2 NI = pf2_sub(0ull, IA);
+            // forward recompute of the pair over the sub-block
+            pf2 hs[kSub + 1], ab[kSub], cf[kSub];
+            hs[0] = (a.dstate == 16) ? *reinterpret_cast<const pf2*>(ck + sb * 16 + 2 * p)
+                                     : pf2_make((2 * p < a.dstate) ? ck[sb * a.dstate + 2 * p] : 0.f,
+                                                (2 * p + 1 < a.dstate) ? ck[sb * a.dstate + 2 * p + 1] : 0.f);
+#pragma unroll
+            for (int j = 0; j < kSub; j++) {
+                const ulonglong2 bc = *reinterpret_cast<const ulonglong2*>(bc0 + j * kRowF + 4 * p);
+                ab[j] = pf2_ex2(pf2_scale(dl[j], A2L));
+                pf2 inc;
+                if constexpr (ZOH) {
+                    cf[j] = pf2_fma(ab[j], IA, NI);                  // (Abar - 1) / A
+                    inc = pf2_mul(cf[j], pf2_scale(uj[j], bc.x));
+                } else {
+                    inc = pf2_scale(dl[j] * uj[j], bc.x);
+                }
+                hs[j + 1] = pf2_fma(ab[j], hs[j], inc);
+                if constexpr (HAS_Z) yv2[j] = pf2_fma(bc.y, hs[j + 1], yv2[j]);
+            }
+            // reverse walk of the pair
+            pf2 G = Gc[p], a1 = dA1[p], a2 = dA2[p];
+#pragma unroll
+            for (int jj = 0; jj < kSub; jj++) {
+                const int j = kSub - 1 - jj;
+                const ulonglong2 bc = *reinterpret_cast<const ulonglong2*>(bc0 + j * kRowF + 4 * p);
+                const pf2 Gt = pf2_scale_add(dy[j], bc.y, G);
+                const pf2 dC = pf2_scale(dy[j], hs[j + 1]);
+                const pf2 da = pf2_mul(Gt, hs[j]);                   // dL/dAbar
+                const pf2 gb = pf2_mul(Gt, bc.x);
+                const pf2 q = pf2_scale(dl[j], ab[j]);               // dAbar/dA
+                pf2 dB;
+                if constexpr (ZOH) {
+                    du2[j] = pf2_fma(gb, cf[j], du2[j]);
+                    dB = pf2_scale(uj[j], pf2_mul(Gt, cf[j]));
+                    const pf2 dcf = pf2_scale(uj[j], gb);            // dL/dcoef
+                    dd2[j] = pf2_fma(ab[j], pf2_fma(da, A2, dcf), dd2[j]);
+                    a1 = pf2_fma(da, q, a1);
+                    a2 = pf2_fma(dcf, pf2_sub(q, cf[j]), a2);        // times 1/A at the end
+                } else {
+                    du2[j] = pf2_scale_add(dl[j], gb, du2[j]);
+                    dB = pf2_scale(dl[j] * uj[j], Gt);
+                    dd2[j] = pf2_add(pf2_fma(pf2_mul(da, A2), ab[j], dd2[j]), pf2_scale(uj[j], gb));
+                    a1 = pf2_fma(da, q, a1);
+                }
+                G = pf2_mul(Gt, ab[j]);
+                *reinterpret_cast<ulonglong2*>(r2 + 4 * j) = make_ulonglong2(dB, dC);
+            }
+            Gc[p] = G;
+            dA1[p] = a1;
+            dA2[p] = a2;
+            // lane l sums float columns 2(l&15), 2(l&15)+1 over half the rows, then
+            // the halves combine; it keeps column f = 2(l&15) + (l>>4), which is
+            // step f>>2, tensor (f>>1)&1 (0 = dB, 1 = dC), state 2p + (f&1)
+            __syncwarp();
+            pf2 sum = 0ull;
+            const float* col = r2w + (lane >> 4) * 16 * kRedF + 2 * (lane & 15);
+#pragma unroll
+            for (int i = 0; i < 16; i++) sum = pf2_add(sum, *reinterpret_cast<const pf2*>(col + i * kRedF));
+            sum = pf2_add(sum, __shfl_xor_sync(0xffffffffu, sum, 16));
+            red[(warp * NP + p) * 32 + 2 * (lane & 15) + (lane >> 4)] = (lane >> 4) ? pf2_hi(sum) : pf2_lo(sum);
+            __syncwarp();
+        }
+        // per-step outputs
+        float duo[kSub], ddo[kSub], dzo[kSub];
+#pragma unroll
+        for (int j = 0; j < kSub; j++) {
+            duo[j] = fmaf(Dd, dy[j], pf2_sum(du2[j]));
+            float dv = pf2_sum(dd2[j]);
+            if (a.softplus) dv *= rcp_approx(1.f + ex2_approx(-(rd.get(j) + bias) * kLog2e));   // sigmoid(v)
+            ddo[j] = j < cnt ? dv : 0.f;
+            dbacc += ddo[j];
+            dDacc = fmaf(dy[j], uj[j], dDacc);
+            dzo[j] = 0.f;
+            if constexpr (HAS_Z) {
+                const float go = (active && j < cnt) ? ro.get(j) : 0.f;
+                const float zj = rz.get(j);
+                const float sgz = rcp_approx(1.f + ex2_approx(-zj * kLog2e));
+                const float yv = fmaf(Dd, uj[j], pf2_sum(yv2[j]));
+                dzo[j] = go * yv * sgz * fmaf(zj, 1.f - sgz, 1.f);
+            }
+        }
+        if (active) {
+            store8<Tg>(durow + t0, cnt, a.vec_du, duo);
+            store8<Tg>(ddrow + t0, cnt, a.vec_ddt, ddo);
+            if constexpr (HAS_Z) store8<Tg>(dzrow + t0, cnt, a.vec_dz, dzo);
+        }
+        // fixed-order sum over the CTA's warps -> one partial per CTA; thread
+        // idx handles (tensor, state n, step j) with j fastest
+        __syncthreads();
+#pragma unroll
+        for (int idx = tid; idx < NP * 32; idx += kBwdThreads) {
+            const int j = idx & 7, n = (idx >> 3) & 15, tsr = idx >> 7;
+            if (j < cnt) {
+                const int f = j * 4 + tsr * 2 + (n & 1);
+                float s2 = 0.f;
+#pragma unroll
+                for (int w = 0; w < kBwdWarps; w++) s2 += red[(w * NP + (n >> 1)) * 32 + f];
+                a.part_bc[(((b * a.nblk + blockIdx.x) * 2 + tsr) * 16 + n) * a.seqlen + t0 + j] = s2;
+            }
+        }
+        __syncthreads();
+    }
+    if (!active) return;
+#pragma unroll
+    for (int p = 0; p < NP; p++) {
+        pf2 dA = dA1[p];
+        if constexpr (ZOH) dA = pf2_fma(dA2[p], cst[p * 32 + lane].y, dA);
+        if (a.dh0 != nullptr) {
+            if (2 * p < a.dstate) a.dh0[chan * a.dstate + 2 * p] = pf2_lo(Gc[p]);
+            if (2 * p + 1 < a.dstate) a.dh0[chan * a.dstate + 2 * p + 1] = pf2_hi(Gc[p]);
+        }
+        a.part_A[chan * 16 + 2 * p] = pf2_lo(dA);
+        a.part_A[chan * 16 + 2 * p + 1] = pf2_hi(dA);
+    }
+    a.part_D[chan] = dDacc;
+    a.part_bias[chan] = dbacc;
+}
+
 // flag[0] = 1 when some A[d, n] == 0 (the ZOH limit needs the accurate path)
 __global__ void bwd_check_A_kernel(const float* A, int64_t n, int* flag) {
     int found = 0;
@@ -322,12 +585,23 @@ scan_bwd_kernel(const BwdArgs a, const int* flag) {
     const bool active = d_raw < a.dim;
     const int64_t d = active ? d_raw : a.dim - 1;
     const int64_t chan = b * a.dim + d;
-    float* hb = hbuf + warp * 9 * 16 * 32 + lane;
-    float* r2 = red2 + warp * 32 * kRed2;
-    bwd_channel<Tin, Tg, ZOH, ACC, HAS_Z>(a, sbc, red, r2, hb, b, d, chan, active, tid);
+    if constexpr (ACC || sizeof(Tin) == 4) {
+        float* hb = hbuf + warp * 9 * 16 * 32 + lane;
+        float* r2 = red2 + warp * 32 * kRed2;
+        bwd_channel<Tin, Tg, ZOH, ACC, HAS_Z>(a, sbc, red, r2, hb, b, d, chan, active, tid);
+    } else {
+        float* sbcf = smem_f;                                   // kTile x kRowF
+        float* redf = sbcf + kTile * kRowF;                     // [warp][8 pairs][32]
+        float* r2f = redf + kBwdWarps * 8 * 32;                 // [warp][32][kRedF]
+        ulonglong2* cst = reinterpret_cast<ulonglong2*>(r2f + kBwdWarps * 32 * kRedF);   // [warp][8][32]
+        bwd_channel_fast<Tin, Tg, ZOH, HAS_Z>(a, sbcf, redf, r2f + warp * 32 * kRedF, cst + warp * 8 * 32,
+                                              b, d, chan, active, tid);
+    }
 }
 
-constexpr int kBwdSmemBytes = (kTile * kRow + kBwdWarps * kSub * 32 + kBwdWarps * 32 * kRed2 + kBwdWarps * 9 * 16 * 32) * 4;
+constexpr int kBwdAccSmemFloats = kTile * kRow + kBwdWarps * kSub * 32 + kBwdWarps * 32 * kRed2 + kBwdWarps * 9 * 16 * 32;
+constexpr int kBwdAccSmemBytes = 4 * kBwdAccSmemFloats;
+constexpr int kBwdFastSmemBytes = 4 * kBwdFastSmemFloats;
 
 // dB[b, n, t] = sum over CTAs of the partials, in CTA order.
 __global__ void bwd_reduce_bc_kernel(const BwdArgs a, float* dB, float* dC) {
@@ -421,26 +695,30 @@ static bool al16(const void* ptr, ssm_strides s, int esize) {
 template <typename Tin, typename Tg>
 static cudaError_t launch_bwd_typed(const BwdArgs& a, bool zoh, bool has_z, int* flag, cudaStream_t st) {
     const dim3 grid((unsigned)a.nblk, (unsigned)a.batch);
-    auto go = [&](auto kern) -> cudaError_t {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kBwdSmemBytes);
+    // the packed fast path is the bf16-input, approximate-math kernel
+    auto go = [&](auto kern, bool fast) -> cudaError_t {
+        const int bytes = fast ? kBwdFastSmemBytes : kBwdAccSmemBytes;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
         if (e != cudaSuccess) return e;
-        kern<<<grid, kBwdThreads, kBwdSmemBytes, st>>>(a, flag);
+        kern<<<grid, kBwdThreads, bytes, st>>>(a, flag);
         count_launches(1);
         return cudaGetLastError();
     };
     auto pair = [&](auto fast, auto acc) -> cudaError_t {
         if constexpr (sizeof(Tin) == 2) {
-            cudaError_t e = go(fast);
+            cudaError_t e = go(fast, true);
             if (e != cudaSuccess) return e;
         }
-        return go(acc);
+        return go(acc, false);
     };
     if (zoh) return has_z ? pair(scan_bwd_kernel<Tin, Tg, true, true, false>, scan_bwd_kernel<Tin, Tg, true, true, true>)
                           : pair(scan_bwd_kernel<Tin, Tg, true, false, false>, scan_bwd_kernel<Tin, Tg, true, false, true>);
     // the simplified rule has no A == 0 limit: the fast path always applies to bf16
     if constexpr (sizeof(Tin) == 2)
-        return has_z ? go(scan_bwd_kernel<Tin, Tg, false, true, false>) : go(scan_bwd_kernel<Tin, Tg, false, false, false>);
-    return has_z ? go(scan_bwd_kernel<Tin, Tg, false, true, true>) : go(scan_bwd_kernel<Tin, Tg, false, false, true>);
+        return has_z ? go(scan_bwd_kernel<Tin, Tg, false, true, false>, true)
+                     : go(scan_bwd_kernel<Tin, Tg, false, false, false>, true);
+    return has_z ? go(scan_bwd_kernel<Tin, Tg, false, true, true>, false)
+                 : go(scan_bwd_kernel<Tin, Tg, false, false, true>, false);
 }
 
 cudaError_t launch_scan_bwd(const ssm_scan_bwd_params* p, void* ws, int num_sms, cudaStream_t st) {
