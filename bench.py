@@ -4,7 +4,7 @@
 One step = one pass of the hot path over one batch of the Mamba-1.4B-shaped
 layer (batch 8, d_inner 4096, d_state 16, L 16384, bf16 activations, fp32
 state, zero-order hold): causal conv1d + SiLU -> fused selective-scan forward
-(writing h checkpoints every 8 steps) -> selective-scan backward with
+(writing h checkpoints every 4 steps) -> selective-scan backward with
 recompute of h (all nine gradients).  Inputs are
 synthetic (seeded counter-based generator), resident in HBM and larger than
 L2 (several GB per step), so no L2 flush is needed between steps.
@@ -160,21 +160,21 @@ def fwd_work(b, d, L, N, zoh=True, io_bytes=2):
 
 
 def fwd_ckpt_bytes(b, d, L, N):
-    """Checkpoints of h every 8 steps written by the forward (fp32)."""
-    return b * d * ((L + 7) // 8) * N * 4
+    """Checkpoints of h every 4 steps written by the forward (fp32)."""
+    return b * d * ((L + 3) // 4) * N * 4
 
 
 def bwd_work(b, d, L, N, io_bytes=2):
     """Compulsory HBM bytes: u, delta, z, dout read and du, ddelta, dz written
     (io_bytes each per channel-token), the fp32 checkpoints read (N floats per
-    8 steps), B, C read and dB, dC written (fp32).  Operations per (channel,
+    4 steps), B, C read and dB, dC written (fp32).  Operations per (channel,
     step, state): forward recompute 5 FP32 + readout for the gate 1, reverse
-    adjoint and gradient terms 20, the cross-channel sums of dB, dC 2 -> 28
-    FP32, and 2 exponentials; per (channel, step) about 15 FP32 and 4 SFU
+    adjoint and gradient terms 15, the cross-channel sums of dB, dC 2 -> 23
+    FP32, and 1 exponential; per (channel, step) about 15 FP32 and 4 SFU
     (softplus and its derivative, the gate and its derivative)."""
     ct = b * d * L
-    byts = 7 * io_bytes * ct + (ct // 8) * N * 4 + 2 * N * io_bytes * b * L + 2 * N * 4 * b * L
-    return dict(bytes=byts, fp32=ct * (N * 28 + 15), sfu=ct * (N * 2 + 4))
+    byts = 7 * io_bytes * ct + (ct // 4) * N * 4 + 2 * N * io_bytes * b * L + 2 * N * 4 * b * L
+    return dict(bytes=byts, fp32=ct * (N * 23 + 15), sfu=ct * (N + 4))
 
 
 def roofline(work, seconds, hbm_gbs, sms, sm_mhz, hbm_src, clock_src):
@@ -212,7 +212,7 @@ def make_inputs(device, seed, cfg):
     g["x"], g["w"] = c["x"], c["w"]
     g["xc"] = torch.empty_like(g["x"])
     g["y"] = torch.empty(b, d, L, dtype=torch.bfloat16, device=device)
-    g["ckpt"] = torch.empty(b, d, (L + 7) // 8, N, dtype=torch.float32, device=device)
+    g["ckpt"] = torch.empty(b, (L + 3) // 4, (N + 1) // 2, d, 2, dtype=torch.float32, device=device)
     g["grads"] = None
     return g
 
@@ -226,11 +226,11 @@ def step(L, g, ev=None):
         ev[1].record()
     L.ssm_scan_fwd(g["xc"], g["dt"], g["A"], g["B"], g["C"], D=g["D"], delta_bias=g["bias"], z=g["z"],
                    out=g["y"], bbar_mode=L.SSM_BBAR_ZOH, delta_softplus=True,
-                   checkpoints=g["ckpt"], checkpoint_every=8, workspace=g.get("ws"))
+                   checkpoints=g["ckpt"], checkpoint_every=4, workspace=g.get("ws"))
     if ev is not None:
         ev[2].record()
     g["grads"] = L.ssm_scan_bwd(g["xc"], g["dt"], g["A"], g["B"], g["C"], g["dout"], D=g["D"],
-                                delta_bias=g["bias"], z=g["z"], checkpoints=g["ckpt"], checkpoint_every=8,
+                                delta_bias=g["bias"], z=g["z"], checkpoints=g["ckpt"], checkpoint_every=4,
                                 bbar_mode=L.SSM_BBAR_ZOH, delta_softplus=True, grads=g["grads"],
                                 workspace=g.get("ws_bwd"))
     if ev is not None:
@@ -379,7 +379,7 @@ def run_reference(args):
 
 def workload_config(cfg):
     return {"workload": "mamba-1.4b-layer training pass: causal conv1d+SiLU -> fused selective-scan forward "
-                        "(checkpoints every 8 steps) -> selective-scan backward with recompute "
+                        "(checkpoints every 4 steps) -> selective-scan backward with recompute "
                         f"(batch {cfg['batch']}, d_inner {cfg['dim']}, d_state {cfg['dstate']}, "
                         f"L {cfg['seqlen']}, ZOH, softplus delta, D skip, silu(z) gate)",
             "batch": cfg["batch"], "dim": cfg["dim"], "dstate": cfg["dstate"], "seqlen": cfg["seqlen"],
@@ -399,6 +399,10 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--seqlen", type=int, default=0,
+                    help="shorter sequence for small profiling captures (the headline uses the default)")
+    ap.add_argument("--decode-layers", type=int, default=0,
+                    help="fewer decode layers for small profiling captures")
     args = ap.parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
@@ -411,6 +415,8 @@ def main(argv=None):
     import synthetic as S
 
     cfg = dict(WORK)
+    if args.seqlen > 0:
+        cfg["seqlen"] = args.seqlen
     seed = S.config_seed(2) + 1000 * rank          # every rank its own batch (weak scaling)
     g = make_inputs(device, seed, cfg)
     ws_bytes = L.ssm_scan_fwd_workspace_size(g["xc"], g["A"])
@@ -507,7 +513,8 @@ def main(argv=None):
     if not args.no_decode:
         del g
         torch.cuda.empty_cache()
-        decode = bench_decode(L, device, DECODE, DECODE["steps"])
+        dcfg = dict(DECODE, layers=args.decode_layers or DECODE["layers"])
+        decode = bench_decode(L, device, dcfg, dcfg["steps"])
         decode["us_per_token_step"] = max_over_ranks(decode["us_per_token_step"], world, device)
 
     cpu = None

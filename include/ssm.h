@@ -92,11 +92,14 @@ typedef struct {
  *   z                : NULL = no gate
  *   h0               : (batch, dim, dstate) float32 contiguous or NULL (= 0)
  *   final_state      : (batch, dim, dstate) float32 contiguous or NULL
- *   checkpoints      : (batch, dim, ceil(seqlen/K), dstate) float32
- *                      contiguous, 16-byte aligned, or NULL; entry k holds the
- *                      state before step k*K (entry 0 = h0).  K =
- *                      checkpoint_every must be a positive multiple of 8 when
- *                      checkpoints != NULL.
+ *   checkpoints      : (batch, ceil(seqlen/K), ceil(dstate/2), dim, 2)
+ *                      float32 contiguous, 16-byte aligned, or NULL; entry
+ *                      [b, k, p, d, q] holds state 2p+q of channel (b, d)
+ *                      before step k*K (k = 0: h0); the state pairs of
+ *                      neighbouring channels are adjacent so that the kernels'
+ *                      accesses coalesce (the partner of a last odd state is
+ *                      0).  K = checkpoint_every must be a positive multiple
+ *                      of 4 when checkpoints != NULL.
  *                      ssm_scan_bwd can take these instead of recomputing.
  * dstate: 1..16.  dim, batch >= 1; seqlen >= 0 (seqlen 0 only copies h0
  * to final_state).
@@ -164,7 +167,7 @@ SSM_API ssm_status ssm_scan_fwd_static_ws(const ssm_scan_fwd_params* p, ssm_stre
  *   dout             : (batch, dim, seqlen) in_dtype
  *   dfinal_state     : (batch, dim, dstate) float32 or NULL (= 0)
  *   checkpoints      : the forward's checkpoints (16-byte aligned) with
- *                      checkpoint_every == 8, or NULL / another interval: the
+ *                      checkpoint_every == 4, or NULL / another interval: the
  *                      backward then recomputes them into the workspace first
  *   du, ddelta, dz   : (batch, dim, seqlen) grad_dtype, strides as above;
  *                      ddelta is the gradient with respect to the delta INPUT

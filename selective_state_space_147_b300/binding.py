@@ -235,6 +235,27 @@ def _fwd_params(u, delta, A, B, C, D, delta_bias, z, h0, bbar_mode, delta_softpl
     return p
 
 
+def checkpoint_buffer(batch: int, dim: int, seqlen: int, dstate: int, every: int = 4, device="cuda") -> torch.Tensor:
+    """The forward's checkpoint buffer: (batch, ceil(seqlen/every), ceil(dstate/2), dim, 2)
+    float32, entry [b, k, p, d, q] = state 2p+q of channel (b, d) before step k*every (the
+    state pairs of neighbouring channels are adjacent)."""
+    return torch.empty(batch, -(-seqlen // every), (dstate + 1) // 2, dim, 2, dtype=torch.float32, device=device)
+
+
+def checkpoint_states(checkpoints: torch.Tensor, dstate: int) -> torch.Tensor:
+    """A checkpoint buffer as (batch, n_ckpt, dim, dstate) states (a copy)."""
+    b, k, P, d, _ = checkpoints.shape
+    return checkpoints.permute(0, 1, 3, 2, 4).reshape(b, k, d, 2 * P)[..., :dstate]
+
+
+def _check_ckpt(checkpoints, batch, dim, L, N, every):
+    if checkpoints is None:
+        return
+    want = (batch, -(-L // max(every, 1)), (N + 1) // 2, dim, 2)
+    if tuple(checkpoints.shape) != want:
+        raise ValueError(f"checkpoints must have shape {want} (see checkpoint_buffer), got {tuple(checkpoints.shape)}")
+
+
 def ssm_scan_fwd(u, delta, A, B, C, *, D=None, delta_bias=None, z=None, h0=None,
                  bbar_mode: int = SSM_BBAR_ZOH, delta_softplus: bool = True,
                  out: Optional[torch.Tensor] = None, out_dtype=None,
@@ -257,6 +278,7 @@ def ssm_scan_fwd(u, delta, A, B, C, *, D=None, delta_bias=None, z=None, h0=None,
         final_state = torch.empty(batch, dim, N, dtype=torch.float32, device=u.device)
     _f32c("final_state", final_state)
     _f32c("checkpoints", checkpoints)
+    _check_ckpt(checkpoints, batch, dim, L, N, checkpoint_every)
     p = _fwd_params(u, delta, A, B, C, D, delta_bias, z, h0, bbar_mode, delta_softplus,
                     out, final_state, checkpoints, checkpoint_every)
     need = _lib.ssm_scan_fwd_workspace_size(ctypes.byref(p))
@@ -288,7 +310,7 @@ def ssm_scan_bwd(u, delta, A, B, C, dout, *, D=None, delta_bias=None, z=None, h0
                  bbar_mode: int = SSM_BBAR_ZOH, delta_softplus: bool = True, grad_dtype=None,
                  grads: Optional[dict] = None, workspace: Optional[torch.Tensor] = None, stream=None):
     """Backward of ssm_scan_fwd for the loss sum(dout * out) + sum(dfinal_state * final_state).
-    Pass the forward's checkpoints (checkpoint_every=8) to skip their recomputation.
+    Pass the forward's checkpoints (checkpoint_every=4) to skip their recomputation.
     Returns a dict: du, ddelta, dz (like u, in grad_dtype), dB, dC (batch, N, L) f32,
     dA (dim, N), dD, ddelta_bias (dim,), dh0 (batch, dim, N), all float32 except du/ddelta/dz."""
     for name, t in (("u", u), ("delta", delta), ("B", B), ("C", C), ("z", z), ("dout", dout)):
@@ -298,6 +320,7 @@ def ssm_scan_bwd(u, delta, A, B, C, dout, *, D=None, delta_bias=None, z=None, h0
     A, D, delta_bias, h0 = (_f32c("A", A), _f32c("D", D), _f32c("delta_bias", delta_bias), _f32c("h0", h0))
     _f32c("dfinal_state", dfinal_state)
     _f32c("checkpoints", checkpoints)
+    _check_ckpt(checkpoints, u.shape[0], u.shape[1], u.shape[2], A.shape[1], checkpoint_every)
     batch, dim, L = u.shape
     N = A.shape[1]
     gd = _torch_dtype(grad_dtype or u.dtype)
@@ -349,7 +372,7 @@ def ssm_scan_bwd_workspace_size(u, A, *, checkpoints_given: bool = True, **kw) -
     p.delta_softplus = 1
     p.u = p.delta = p.B = p.C = p.dout = p.A = p.du = p.ddelta = p.dB = p.dC = p.dA = 256  # sizes only
     if checkpoints_given:
-        p.checkpoints, p.checkpoint_every = 256, 8
+        p.checkpoints, p.checkpoint_every = 256, 4
     return _lib.ssm_scan_bwd_workspace_size(ctypes.byref(p))
 
 

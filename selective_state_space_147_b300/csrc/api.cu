@@ -65,8 +65,8 @@ ssm_status check_fwd(const ssm_scan_fwd_params* p) {
                                 &p->C_strides, &p->out_strides};
     for (const ssm_strides* s : all)
         if (s->batch < 0 || s->row < 0) return fail(SSM_ERR_INVALID_ARG, "negative stride");
-    if (p->checkpoints != nullptr && (p->checkpoint_every <= 0 || p->checkpoint_every % 8 != 0))
-        return fail(SSM_ERR_UNSUPPORTED, "checkpoint_every=%lld must be a positive multiple of 8",
+    if (p->checkpoints != nullptr && (p->checkpoint_every <= 0 || p->checkpoint_every % 4 != 0))
+        return fail(SSM_ERR_UNSUPPORTED, "checkpoint_every=%lld must be a positive multiple of 4",
                     (long long)p->checkpoint_every);
     if (p->checkpoints != nullptr && (uintptr_t)p->checkpoints % 16 != 0)
         return fail(SSM_ERR_MISALIGNED, "checkpoints must be 16-byte aligned");

@@ -28,7 +28,8 @@ namespace ssm {
 
 constexpr int kBwdWarps = 4;
 constexpr int kBwdThreads = 32 * kBwdWarps;
-constexpr int kBwdK = 8;                    // checkpoint interval the backward consumes
+constexpr int kBwdK = 4;                    // checkpoint interval the backward consumes
+constexpr int kAccCk = kSub / kBwdK;        // checkpoints per 8-step sub-block of the accurate kernel
 constexpr int kRed2 = 33;                   // padded row of the in-warp transpose
 
 struct BwdArgs {
@@ -39,7 +40,7 @@ struct BwdArgs {
     void* du; void* ddt; void* dz;
     int64_t sdu_b, sdu_d, sddt_b, sddt_d, sdz_b, sdz_d;
     const float* A; const float* D; const float* bias; const float* dhN;
-    const float* ckpt;          // (batch, dim, n_ckpt, dstate), state before step 8k
+    const float* ckpt;          // (batch, n_ckpt, ceil(dstate/2), dim, 2), state before step 4k
     int64_t n_ckpt;
     float* dh0;
     int softplus;
@@ -50,6 +51,13 @@ struct BwdArgs {
     float* part_bias;           // (batch, dim)
     int nblk;
 };
+
+// Checkpoint k of channel (b, d), state pair `pair`: the forward's layout
+// (batch, n_ckpt, ceil(dstate/2), dim, 2), the pairs of neighbouring channels adjacent.
+__device__ __forceinline__ const float* ckpt_at(const BwdArgs& a, int64_t b, int64_t k, int64_t d, int pair) {
+    const int64_t P = (a.dstate + 1) >> 1;
+    return a.ckpt + (((b * a.n_ckpt + k) * P + pair) * a.dim + d) * 2;
+}
 
 // B[b, :, t0 : t0+64] and C[...] as fp32 rows [t][B0..15 C0..15 pad] for the
 // whole CTA: thread s (< 64) stages B of step t0+s, thread 64+s C of step t0+s.
@@ -113,7 +121,6 @@ __device__ __forceinline__ void bwd_channel(const BwdArgs& a, float* sbc, float*
     Tg* dzrow = HAS_Z ? reinterpret_cast<Tg*>(a.dz) + b * a.sdz_b + d * a.sdz_d : nullptr;
     const Tin* Bb = reinterpret_cast<const Tin*>(a.B) + b * a.sB_b;
     const Tin* Cb = reinterpret_cast<const Tin*>(a.C) + b * a.sC_b;
-    const float* ck = a.ckpt + chan * a.n_ckpt * a.dstate;
 
     // 8-step sub-blocks, last to first; the inputs of the previous (earlier)
     // sub-block are loaded while the current one is computed.
@@ -162,15 +169,12 @@ __device__ __forceinline__ void bwd_channel(const BwdArgs& a, float* sbc, float*
 
         // forward recompute of the sub-block from its checkpoint into hb rows 0..8
         float h[16];
-        if (a.dstate == 16) {
 #pragma unroll
-            for (int q = 0; q < 4; q++) {
-                const float4 c4 = __ldg(reinterpret_cast<const float4*>(ck + sb * 16) + q);
-                h[4 * q] = c4.x; h[4 * q + 1] = c4.y; h[4 * q + 2] = c4.z; h[4 * q + 3] = c4.w;
-            }
-        } else {
-#pragma unroll
-            for (int n = 0; n < 16; n++) h[n] = (n < a.dstate) ? __ldg(ck + sb * a.dstate + n) : 0.f;
+        for (int pp = 0; pp < 8; pp++) {
+            const float2 c2 = (2 * pp < a.dstate) ? __ldg(reinterpret_cast<const float2*>(ckpt_at(a, b, sb * kAccCk, d, pp)))
+                                                  : make_float2(0.f, 0.f);
+            h[2 * pp] = c2.x;
+            h[2 * pp + 1] = c2.y;
         }
 #pragma unroll
         for (int n = 0; n < 16; n++) hb[n * 32] = h[n];
@@ -292,21 +296,40 @@ __device__ __forceinline__ void bwd_channel(const BwdArgs& a, float* sbc, float*
 }
 
 // ---------------------------------------------------------------------------
-// Fast (SFU) backward of one channel per thread on packed f32x2 registers.
+// Fast (SFU) backward for bf16 inputs.
 //
-// The adjoint recurrence G_t = dy_t C_t + Abar_{t+1} G_{t+1} is independent per
-// state, so the loop over state pairs is the outer one: for each pair the 8
-// steps of the sub-block are recomputed forward from the checkpoint (h, Abar
-// and the input coefficient stay in registers) and then walked in reverse.
-// Only the per-step sums over states (du, ddelta and, with the gate, the
-// readout y used by dz) live across pairs, as packed per-step accumulators.
-// After each pair the lane's 32 dB/dC partials (8 steps x 2 states x 2
-// tensors) are summed over the warp's 32 channels through a shared-memory
-// transpose (128-bit writes, 64-bit reads, both at the minimum number of
-// wavefronts with rows of 36 floats).
-constexpr int kRowF = 36;   // B/C row of one step: [pair p: B_2p B_2p+1 C_2p C_2p+1] x 8, pad
-constexpr int kRedF = 36;   // transpose row
-constexpr int kBwdFastSmemFloats = kTile * kRowF + kBwdWarps * 8 * 32 + kBwdWarps * 32 * kRedF + kBwdWarps * 8 * 32 * 4;
+// One thread per channel (a CTA of 4 warps covers 128 channels), the sequence
+// walked backwards in 4-step sub-blocks, one per forward checkpoint.  The
+// adjoint recurrence G_t = dy_t C_t + Abar_{t+1} G_{t+1} is independent per
+// state, so state pairs are the outer loop, two at a time for instruction-level
+// parallelism: the two pairs' 4 steps are recomputed forward from the
+// checkpoint (h, Abar and the input coefficient stay in registers) and then
+// walked in reverse.  Only the per-step sums over states (du, ddelta and, with
+// the gate, the readout y that dz needs) live across pairs, as packed f32x2
+// accumulators.  After each couple of pairs the lane's 32 dB/dC partials
+// (4 steps x 4 states x 2 tensors) are summed over the warp's 32 channels
+// through a shared-memory transpose, and once per sub-block the CTA's 4 warps
+// in a fixed order into one partial per CTA.  u, delta, dout, z rows (8 steps)
+// and the checkpoints arrive ahead by cp.async into shared memory.
+constexpr int kRowF = 36;                     // B/C row of one step: [pair: B B C C] x 8, pad
+constexpr int kRedF = 36;                     // transpose row (32 floats + pad, 16-byte aligned)
+constexpr int kFSub = kBwdK;                  // steps per sub-block (= checkpoint interval)
+constexpr int kFWarps = 4;
+constexpr int kFThreads = 32 * kFWarps;
+constexpr int kFChans = kFThreads;            // channels per CTA = per dB/dC partial
+constexpr int kFNP = 8;                       // state pairs per thread
+// shared memory (byte offsets)
+constexpr int kFOffRed = kTile * kRowF * 4;                      // float [2][warp][couple][32]
+constexpr int kFOffTr = kFOffRed + 2 * kFWarps * 4 * 32 * 4;     // float [warp][32 rows][kRedF]
+constexpr int kFOffCst = kFOffTr + kFWarps * 32 * kRedF * 4;     // ulonglong2 {A, 1/A} [warp][pair][32]
+constexpr int kFOffCk = kFOffCst + kFWarps * kFNP * 32 * 16;     // pf2 checkpoint [warp][2][pair][32]
+constexpr int kFOffRaw = kFOffCk + kFWarps * 2 * kFNP * 32 * 8;  // uint4 u, delta, dout, z [warp][2][4][32]
+constexpr int kBwdFastSmemBytes = kFOffRaw + kFWarps * 2 * 4 * 32 * 16;
+
+__device__ __forceinline__ void cp_async8(void* smem, const void* gmem) {
+    const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(sa), "l"(gmem) : "memory");
+}
 
 // B[b, :, t0 : t0+64] and C as fp32 rows with B and C of a state pair adjacent,
 // so that one 128-bit broadcast read gives both: thread s (< 64) stages B of step
@@ -333,24 +356,57 @@ __device__ __forceinline__ pf2 pf2_scale(float s, pf2 v) { return pf2_make(s * p
 __device__ __forceinline__ pf2 pf2_scale_add(float s, pf2 v, pf2 c) {
     return pf2_make(fmaf(s, pf2_lo(v), pf2_lo(c)), fmaf(s, pf2_hi(v), pf2_hi(c)));
 }
+__device__ __forceinline__ float bf16_of(uint32_t w, int hi) { return hi ? bf16hi(w) : bf16lo(w); }
 
-template <typename Tin, typename Tg, bool ZOH, bool HAS_Z>
-__device__ __forceinline__ void bwd_channel_fast(const BwdArgs& a, float* sbc, float* red, float* r2w, ulonglong2* cst,
-                                                 int64_t b, int64_t d, int64_t chan, bool active, int tid) {
-    constexpr int NP = 8;
-    const int lane = tid & 31, warp = tid >> 5;
-    // per-pair constants {A, 1/A} of this lane's channel in shared memory (own entries only);
-    // states past dstate get A = -1 with B = C = h = G = 0, so they contribute nothing
-    pf2 Gc[NP], dA1[NP], dA2[NP];
+// four consecutive gradient values (steps t .. t+3) of one row; n of them valid
+template <typename Tg>
+__device__ __forceinline__ void store4(Tg* p, int n, bool vec, const float (&v)[4]) {
+    if (n >= 4 && vec) {
+        if constexpr (sizeof(Tg) == 2) {
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(v[0], v[1]), hi = __floats2bfloat162_rn(v[2], v[3]);
+            *reinterpret_cast<uint2*>(p) = make_uint2(*reinterpret_cast<const uint32_t*>(&lo),
+                                                      *reinterpret_cast<const uint32_t*>(&hi));
+        } else {
+            *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+        }
+    } else {
 #pragma unroll
-    for (int p = 0; p < NP; p++) {
+        for (int j = 0; j < 4; j++)
+            if (j < n) Elem<Tg>::store(p + j, v[j]);
+    }
+}
+
+template <typename Tg, bool ZOH, bool HAS_Z>
+__global__ void __launch_bounds__(kFThreads)
+scan_bwd_fast_kernel(const BwdArgs a, const int* flag) {
+    using Tin = __nv_bfloat16;
+    if (ZOH && *flag) return;   // some A == 0: the accurate kernel takes this call
+    extern __shared__ __align__(16) unsigned char smem_b[];
+    float* sbc = reinterpret_cast<float*>(smem_b);
+    float* red = reinterpret_cast<float*>(smem_b + kFOffRed);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    float* tr = reinterpret_cast<float*>(smem_b + kFOffTr) + warp * 32 * kRedF;
+    ulonglong2* cst = reinterpret_cast<ulonglong2*>(smem_b + kFOffCst) + warp * kFNP * 32;
+    pf2* ckb = reinterpret_cast<pf2*>(smem_b + kFOffCk) + warp * 2 * kFNP * 32;
+    uint4* raw = reinterpret_cast<uint4*>(smem_b + kFOffRaw) + warp * 2 * 4 * 32;
+    const int64_t b = blockIdx.y;
+    const int64_t d_raw = (int64_t)blockIdx.x * kFChans + tid;
+    const bool active = d_raw < a.dim;
+    const int64_t d = active ? d_raw : a.dim - 1;   // idle threads shadow a valid channel
+    const int64_t chan = b * a.dim + d;
+
+    // {A, 1/A} per pair in shared memory (own entries only); states past dstate
+    // get A = -1 with B = C = h = G = 0, so they contribute nothing
+    pf2 Gc[kFNP], dA1[kFNP], dA2[kFNP];
+#pragma unroll
+    for (int p = 0; p < kFNP; p++) {
         float av[2], ia[2], gv[2];
 #pragma unroll
         for (int q = 0; q < 2; q++) {
             const int n = 2 * p + q;
             const bool on = n < a.dstate;
             av[q] = on ? __ldg(a.A + d * a.dstate + n) : -1.f;
-            ia[q] = ZOH ? rcp_approx(av[q]) : 0.f;   // A != 0 here (A == 0 takes the accurate kernel)
+            ia[q] = ZOH ? rcp_approx(av[q]) : 0.f;   // A != 0 here
             gv[q] = (active && on && a.dhN != nullptr) ? __ldg(a.dhN + chan * a.dstate + n) : 0.f;
         }
         cst[p * 32 + lane] = make_ulonglong2(pf2_make(av[0], av[1]), pf2_make(ia[0], ia[1]));
@@ -366,34 +422,64 @@ __device__ __forceinline__ void bwd_channel_fast(const BwdArgs& a, float* sbc, f
     const Tin* drow = reinterpret_cast<const Tin*>(a.dt) + b * a.sdt_b + d * a.sdt_d;
     const Tin* zrow = HAS_Z ? reinterpret_cast<const Tin*>(a.z) + b * a.sz_b + d * a.sz_d : nullptr;
     const Tin* orow = reinterpret_cast<const Tin*>(a.dout) + b * a.sdo_b + d * a.sdo_d;
-    Tg* durow = reinterpret_cast<Tg*>(a.du) + b * a.sdu_b + d * a.sdu_d;
-    Tg* ddrow = reinterpret_cast<Tg*>(a.ddt) + b * a.sddt_b + d * a.sddt_d;
-    Tg* dzrow = HAS_Z ? reinterpret_cast<Tg*>(a.dz) + b * a.sdz_b + d * a.sdz_d : nullptr;
     const Tin* Bb = reinterpret_cast<const Tin*>(a.B) + b * a.sB_b;
     const Tin* Cb = reinterpret_cast<const Tin*>(a.C) + b * a.sC_b;
-    const float* ck = a.ckpt + chan * a.n_ckpt * a.dstate;
-    float* r2 = r2w + lane * kRedF;
-
-    const int64_t nsb = ceil_div(a.seqlen, (int64_t)kSub);
+    const bool vec_in = a.vec_u && a.vec_dt && a.vec_do && (!HAS_Z || a.vec_z);
+    const bool ck16 = a.dstate == 16;
+    const int64_t nsb = ceil_div(a.seqlen, (int64_t)kFSub);
     auto limit = [&](int64_t sb) -> int {
-        const int64_t r = a.seqlen - sb * kSub;
-        return (int)(r < kSub ? r : kSub);
+        const int64_t r = a.seqlen - sb * kFSub;
+        return (int)(r < kFSub ? r : kFSub);
     };
-    Raw8<Tin> nu, nd, no, nz;
-    {
-        const int64_t t0 = (nsb - 1) * kSub;
-        const int lim = limit(nsb - 1);
-        nu.load(urow + t0, lim, a.vec_u);
-        nd.load(drow + t0, lim, a.vec_dt);
-        no.load(orow + t0, lim, a.vec_do);
-        if constexpr (HAS_Z) nz.load(zrow + t0, lim, a.vec_z);
-    }
+    // one commit group per sub-block sb: its checkpoint (-> buffer sb & 1) and,
+    // when sb is the first sub-block walked of its 8-step block, that block's
+    // u, delta, dout, z rows (-> buffer (sb >> 1) & 1)
+    auto prefetch = [&](int64_t sb) {
+        if (sb == nsb - 1 || (sb & 1)) {
+            const int64_t t0 = (sb >> 1) * 8;
+            const int64_t r = a.seqlen - t0;
+            const int lim = (int)(r < 8 ? r : 8);
+            uint4* dst = raw + ((sb >> 1) & 1) * 4 * 32 + lane;
+            const Tin* src[4] = {urow + t0, drow + t0, orow + t0, HAS_Z ? zrow + t0 : urow + t0};
+#pragma unroll
+            for (int q = 0; q < (HAS_Z ? 4 : 3); q++) {
+                if (vec_in) {
+                    cp_async16(dst + q * 32, src[q], 2 * lim);
+                } else {
+                    const unsigned short* e = reinterpret_cast<const unsigned short*>(src[q]);
+                    uint32_t w[8];
+#pragma unroll
+                    for (int k = 0; k < 8; k++) w[k] = (k < lim) ? (uint32_t)__ldg(e + k) : 0u;
+                    dst[q * 32] = make_uint4(w[0] | (w[1] << 16), w[2] | (w[3] << 16), w[4] | (w[5] << 16),
+                                             w[6] | (w[7] << 16));
+                }
+            }
+        }
+        if (ck16) {
+#pragma unroll
+            for (int p = 0; p < kFNP; p++) cp_async8(ckb + ((sb & 1) * kFNP + p) * 32 + lane, ckpt_at(a, b, sb, d, p));
+        }
+        cp_async_commit();
+    };
+    prefetch(nsb - 1);
+
+    // transpose: lane l sums float columns 2(l&15), 2(l&15)+1 over half the rows,
+    // then the halves combine; it keeps column f = 2(l&15) + (l>>4) of the row
+    // layout f = 8 j + 4 q + 2 tensor + s (step j, pair q of the couple, tensor
+    // 0 = dB / 1 = dC, state s of the pair)
+    float* t_row = tr + lane * kRedF;
+    const float* t_col = tr + (lane >> 4) * 16 * kRedF + 2 * (lane & 15);
+
     int64_t cur_tile = -1;
+    int it = 0;
 #pragma unroll 1
-    for (int64_t sb = nsb - 1; sb >= 0; --sb) {
-        const int64_t t0 = sb * kSub;
+    for (int64_t sb = nsb - 1; sb >= 0; --sb, ++it) {
+        const int64_t t0 = sb * kFSub;
         const int cnt = limit(sb);
         const int64_t tile = t0 / kTile;
+        if (sb > 0) prefetch(sb - 1);
+        else cp_async_commit();
+        cp_async_wait<1>();                                   // this sub-block's slots have landed
         if (tile != cur_tile) {
             __syncthreads();
             stage_bc_pairs<Tin>(sbc, a, Bb, Cb, tile * kTile, tid);
@@ -401,154 +487,184 @@ __device__ __forceinline__ void bwd_channel_fast(const BwdArgs& a, float* sbc, f
             cur_tile = tile;
         }
         const float* bc0 = sbc + (t0 - tile * kTile) * kRowF;
-        const Raw8<Tin> ru = nu, rd = nd, ro = no, rz = nz;
-        if (sb > 0) {
-            const int64_t tp = t0 - kSub;
-            nu.load(urow + tp, kSub, a.vec_u);
-            nd.load(drow + tp, kSub, a.vec_dt);
-            no.load(orow + tp, kSub, a.vec_do);
-            if constexpr (HAS_Z) nz.load(zrow + tp, kSub, a.vec_z);
-        }
-        // per-step scalars; steps past the end get delta = u = dy = 0, which makes
-        // them identity steps that add nothing to any gradient
-        float dl[kSub], uj[kSub], dy[kSub];
+        // this sub-block's half of the 8-step rows
+        const uint4* rw = raw + ((sb >> 1) & 1) * 4 * 32 + lane;
+        const int hi = (int)(sb & 1);
+        const uint4 wu4 = rw[0], wd4 = rw[32], wo4 = rw[64];
+        const uint4 wz4 = HAS_Z ? rw[96] : make_uint4(0u, 0u, 0u, 0u);
+        const uint2 wu = hi ? make_uint2(wu4.z, wu4.w) : make_uint2(wu4.x, wu4.y);
+        const uint2 wd = hi ? make_uint2(wd4.z, wd4.w) : make_uint2(wd4.x, wd4.y);
+        const uint2 wo = hi ? make_uint2(wo4.z, wo4.w) : make_uint2(wo4.x, wo4.y);
+        const uint2 wz = hi ? make_uint2(wz4.z, wz4.w) : make_uint2(wz4.x, wz4.y);
+        auto at = [](uint2 w, int j) -> float { return bf16_of(j < 2 ? w.x : w.y, j & 1); };
+        // per-step scalars; steps past the end get delta = u = dy = 0, which
+        // makes them identity steps that add nothing to any gradient
+        float dl[kFSub], uj[kFSub], dy[kFSub];
 #pragma unroll
-        for (int j = 0; j < kSub; j++) {
+        for (int j = 0; j < kFSub; j++) {
             const bool in = j < cnt;
-            const float v = rd.get(j) + bias;
+            const float v = at(wd, j) + bias;
             dl[j] = in ? (a.softplus ? softplus_fast(v) : v) : 0.f;
-            uj[j] = in ? ru.get(j) : 0.f;
-            const float go = (active && in) ? ro.get(j) : 0.f;
+            uj[j] = in ? at(wu, j) : 0.f;
+            const float go = (active && in) ? at(wo, j) : 0.f;
             if constexpr (HAS_Z) {
-                const float zj = rz.get(j);
+                const float zj = at(wz, j);
                 dy[j] = go * zj * rcp_approx(1.f + ex2_approx(-zj * kLog2e));
             } else {
                 dy[j] = go;
             }
         }
-        pf2 du2[kSub], dd2[kSub], yv2[kSub];
+        pf2 du2[kFSub], dd2[kFSub], yv2[kFSub];
 #pragma unroll
-        for (int j = 0; j < kSub; j++) du2[j] = dd2[j] = yv2[j] = 0ull;
+        for (int j = 0; j < kFSub; j++) du2[j] = dd2[j] = yv2[j] = 0ull;
+        float* redw = red + ((it & 1) * kFWarps + warp) * 4 * 32;
 
 #pragma unroll
-        for (int p = 0; p < NP; p++) {
-            const ulonglong2 kc = cst[p * 32 + lane];
-            const pf2 A2 = kc.x, IA = kc.y;
-            const pf2 A2L = pf2_mul(A2, LOG2E2);
-            const pf2 NI = pf2_sub(0ull, IA);
-            // forward recompute of the pair over the sub-block
-            pf2 hs[kSub + 1], ab[kSub], cf[kSub];
-            hs[0] = (a.dstate == 16) ? *reinterpret_cast<const pf2*>(ck + sb * 16 + 2 * p)
-                                     : pf2_make((2 * p < a.dstate) ? ck[sb * a.dstate + 2 * p] : 0.f,
-                                                (2 * p + 1 < a.dstate) ? ck[sb * a.dstate + 2 * p + 1] : 0.f);
+        for (int c = 0; c < kFNP / 2; c++) {
+            pf2 A2[2], IA[2], A2L[2], NI[2], hs[2][kFSub + 1], ab[2][kFSub], cf[2][kFSub];
 #pragma unroll
-            for (int j = 0; j < kSub; j++) {
-                const ulonglong2 bc = *reinterpret_cast<const ulonglong2*>(bc0 + j * kRowF + 4 * p);
-                ab[j] = pf2_ex2(pf2_scale(dl[j], A2L));
-                pf2 inc;
-                if constexpr (ZOH) {
-                    cf[j] = pf2_fma(ab[j], IA, NI);                  // (Abar - 1) / A
-                    inc = pf2_mul(cf[j], pf2_scale(uj[j], bc.x));
+            for (int q = 0; q < 2; q++) {
+                const int p = 2 * c + q;
+                const ulonglong2 kc = cst[p * 32 + lane];
+                A2[q] = kc.x;
+                IA[q] = kc.y;
+                A2L[q] = pf2_mul(A2[q], LOG2E2);
+                NI[q] = pf2_sub(0ull, IA[q]);
+                if (ck16) {
+                    hs[q][0] = ckb[((sb & 1) * kFNP + p) * 32 + lane];
+                } else if (2 * p < a.dstate) {
+                    const float2 c2 = __ldg(reinterpret_cast<const float2*>(ckpt_at(a, b, sb, d, p)));
+                    hs[q][0] = pf2_make(c2.x, c2.y);
                 } else {
-                    inc = pf2_scale(dl[j] * uj[j], bc.x);
+                    hs[q][0] = 0ull;
                 }
-                hs[j + 1] = pf2_fma(ab[j], hs[j], inc);
-                if constexpr (HAS_Z) yv2[j] = pf2_fma(bc.y, hs[j + 1], yv2[j]);
             }
-            // reverse walk of the pair
-            pf2 G = Gc[p], a1 = dA1[p], a2 = dA2[p];
+            // forward recompute of the two pairs over the sub-block
 #pragma unroll
-            for (int jj = 0; jj < kSub; jj++) {
-                const int j = kSub - 1 - jj;
-                const ulonglong2 bc = *reinterpret_cast<const ulonglong2*>(bc0 + j * kRowF + 4 * p);
-                const pf2 Gt = pf2_scale_add(dy[j], bc.y, G);
-                const pf2 dC = pf2_scale(dy[j], hs[j + 1]);
-                const pf2 da = pf2_mul(Gt, hs[j]);                   // dL/dAbar
-                const pf2 gb = pf2_mul(Gt, bc.x);
-                const pf2 q = pf2_scale(dl[j], ab[j]);               // dAbar/dA
-                pf2 dB;
-                if constexpr (ZOH) {
-                    du2[j] = pf2_fma(gb, cf[j], du2[j]);
-                    dB = pf2_scale(uj[j], pf2_mul(Gt, cf[j]));
-                    const pf2 dcf = pf2_scale(uj[j], gb);            // dL/dcoef
-                    dd2[j] = pf2_fma(ab[j], pf2_fma(da, A2, dcf), dd2[j]);
-                    a1 = pf2_fma(da, q, a1);
-                    a2 = pf2_fma(dcf, pf2_sub(q, cf[j]), a2);        // times 1/A at the end
-                } else {
-                    du2[j] = pf2_scale_add(dl[j], gb, du2[j]);
-                    dB = pf2_scale(dl[j] * uj[j], Gt);
-                    dd2[j] = pf2_add(pf2_fma(pf2_mul(da, A2), ab[j], dd2[j]), pf2_scale(uj[j], gb));
-                    a1 = pf2_fma(da, q, a1);
+            for (int j = 0; j < kFSub; j++) {
+#pragma unroll
+                for (int q = 0; q < 2; q++) {
+                    const ulonglong2 bc = *reinterpret_cast<const ulonglong2*>(bc0 + j * kRowF + 4 * (2 * c + q));
+                    ab[q][j] = pf2_ex2(pf2_scale(dl[j], A2L[q]));
+                    pf2 inc;
+                    if constexpr (ZOH) {
+                        cf[q][j] = pf2_fma(ab[q][j], IA[q], NI[q]);          // (Abar - 1) / A
+                        inc = pf2_mul(cf[q][j], pf2_scale(uj[j], bc.x));
+                    } else {
+                        inc = pf2_scale(dl[j] * uj[j], bc.x);
+                    }
+                    hs[q][j + 1] = pf2_fma(ab[q][j], hs[q][j], inc);
+                    if constexpr (HAS_Z) yv2[j] = pf2_fma(bc.y, hs[q][j + 1], yv2[j]);
                 }
-                G = pf2_mul(Gt, ab[j]);
-                *reinterpret_cast<ulonglong2*>(r2 + 4 * j) = make_ulonglong2(dB, dC);
             }
-            Gc[p] = G;
-            dA1[p] = a1;
-            dA2[p] = a2;
-            // lane l sums float columns 2(l&15), 2(l&15)+1 over half the rows, then
-            // the halves combine; it keeps column f = 2(l&15) + (l>>4), which is
-            // step f>>2, tensor (f>>1)&1 (0 = dB, 1 = dC), state 2p + (f&1)
+            // reverse walk of the two pairs
+            pf2 G[2], a1[2], a2[2];
+#pragma unroll
+            for (int q = 0; q < 2; q++) {
+                G[q] = Gc[2 * c + q];
+                a1[q] = dA1[2 * c + q];
+                a2[q] = dA2[2 * c + q];
+            }
+#pragma unroll
+            for (int jj = 0; jj < kFSub; jj++) {
+                const int j = kFSub - 1 - jj;
+#pragma unroll
+                for (int q = 0; q < 2; q++) {
+                    const ulonglong2 bc = *reinterpret_cast<const ulonglong2*>(bc0 + j * kRowF + 4 * (2 * c + q));
+                    const pf2 Gt = pf2_scale_add(dy[j], bc.y, G[q]);
+                    const pf2 dC = pf2_scale(dy[j], hs[q][j + 1]);
+                    const pf2 da = pf2_mul(Gt, hs[q][j]);                // dL/dAbar
+                    const pf2 gb = pf2_mul(Gt, bc.x);
+                    const pf2 qa = pf2_scale(dl[j], ab[q][j]);           // dAbar/dA
+                    pf2 dB;
+                    if constexpr (ZOH) {
+                        du2[j] = pf2_fma(gb, cf[q][j], du2[j]);
+                        dB = pf2_scale(uj[j], pf2_mul(Gt, cf[q][j]));
+                        const pf2 dcf = pf2_scale(uj[j], gb);            // dL/dcoef
+                        dd2[j] = pf2_fma(ab[q][j], pf2_fma(da, A2[q], dcf), dd2[j]);
+                        a1[q] = pf2_fma(da, qa, a1[q]);
+                        a2[q] = pf2_fma(dcf, pf2_sub(qa, cf[q][j]), a2[q]);   // times 1/A at the end
+                    } else {
+                        du2[j] = pf2_scale_add(dl[j], gb, du2[j]);
+                        dB = pf2_scale(dl[j] * uj[j], Gt);
+                        dd2[j] = pf2_add(pf2_fma(pf2_mul(da, A2[q]), ab[q][j], dd2[j]), pf2_scale(uj[j], gb));
+                        a1[q] = pf2_fma(da, qa, a1[q]);
+                    }
+                    G[q] = pf2_mul(Gt, ab[q][j]);
+                    *reinterpret_cast<ulonglong2*>(t_row + 8 * j + 4 * q) = make_ulonglong2(dB, dC);
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < 2; q++) {
+                Gc[2 * c + q] = G[q];
+                dA1[2 * c + q] = a1[q];
+                dA2[2 * c + q] = a2[q];
+            }
             __syncwarp();
-            pf2 sum = 0ull;
-            const float* col = r2w + (lane >> 4) * 16 * kRedF + 2 * (lane & 15);
+            pf2 s4[4];
 #pragma unroll
-            for (int i = 0; i < 16; i++) sum = pf2_add(sum, *reinterpret_cast<const pf2*>(col + i * kRedF));
+            for (int i = 0; i < 4; i++) s4[i] = *reinterpret_cast<const pf2*>(t_col + i * kRedF);
+#pragma unroll
+            for (int i = 4; i < 16; i++) s4[i & 3] = pf2_add(s4[i & 3], *reinterpret_cast<const pf2*>(t_col + i * kRedF));
+            pf2 sum = pf2_add(pf2_add(s4[0], s4[1]), pf2_add(s4[2], s4[3]));
             sum = pf2_add(sum, __shfl_xor_sync(0xffffffffu, sum, 16));
-            red[(warp * NP + p) * 32 + 2 * (lane & 15) + (lane >> 4)] = (lane >> 4) ? pf2_hi(sum) : pf2_lo(sum);
+            redw[c * 32 + lane] = (lane >> 4) ? pf2_hi(sum) : pf2_lo(sum);
             __syncwarp();
         }
         // per-step outputs
-        float duo[kSub], ddo[kSub], dzo[kSub];
+        float duo[kFSub], ddo[kFSub], dzo[kFSub];
 #pragma unroll
-        for (int j = 0; j < kSub; j++) {
+        for (int j = 0; j < kFSub; j++) {
+            const bool in = j < cnt;
             duo[j] = fmaf(Dd, dy[j], pf2_sum(du2[j]));
             float dv = pf2_sum(dd2[j]);
-            if (a.softplus) dv *= rcp_approx(1.f + ex2_approx(-(rd.get(j) + bias) * kLog2e));   // sigmoid(v)
-            ddo[j] = j < cnt ? dv : 0.f;
+            if (a.softplus) dv *= rcp_approx(1.f + ex2_approx(-(at(wd, j) + bias) * kLog2e));   // sigmoid(v)
+            ddo[j] = in ? dv : 0.f;
             dbacc += ddo[j];
             dDacc = fmaf(dy[j], uj[j], dDacc);
             dzo[j] = 0.f;
             if constexpr (HAS_Z) {
-                const float go = (active && j < cnt) ? ro.get(j) : 0.f;
-                const float zj = rz.get(j);
+                const float go = (active && in) ? at(wo, j) : 0.f;
+                const float zj = at(wz, j);
                 const float sgz = rcp_approx(1.f + ex2_approx(-zj * kLog2e));
-                const float yv = fmaf(Dd, uj[j], pf2_sum(yv2[j]));
-                dzo[j] = go * yv * sgz * fmaf(zj, 1.f - sgz, 1.f);
+                dzo[j] = go * fmaf(Dd, uj[j], pf2_sum(yv2[j])) * sgz * fmaf(zj, 1.f - sgz, 1.f);
             }
         }
         if (active) {
-            store8<Tg>(durow + t0, cnt, a.vec_du, duo);
-            store8<Tg>(ddrow + t0, cnt, a.vec_ddt, ddo);
-            if constexpr (HAS_Z) store8<Tg>(dzrow + t0, cnt, a.vec_dz, dzo);
+            store4<Tg>(reinterpret_cast<Tg*>(a.du) + b * a.sdu_b + d * a.sdu_d + t0, cnt, a.vec_du, duo);
+            store4<Tg>(reinterpret_cast<Tg*>(a.ddt) + b * a.sddt_b + d * a.sddt_d + t0, cnt, a.vec_ddt, ddo);
+            if constexpr (HAS_Z)
+                store4<Tg>(reinterpret_cast<Tg*>(a.dz) + b * a.sdz_b + d * a.sdz_d + t0, cnt, a.vec_dz, dzo);
         }
-        // fixed-order sum over the CTA's warps -> one partial per CTA; thread
-        // idx handles (tensor, state n, step j) with j fastest
+        // fixed-order sum over the CTA's warps -> one partial per CTA; thread tid
+        // handles (tensor, state n, step j) with j fastest
         __syncthreads();
-#pragma unroll
-        for (int idx = tid; idx < NP * 32; idx += kBwdThreads) {
-            const int j = idx & 7, n = (idx >> 3) & 15, tsr = idx >> 7;
+        {
+            const int j = tid & 3, n = (tid >> 2) & 15, tsr = tid >> 6;
             if (j < cnt) {
-                const int f = j * 4 + tsr * 2 + (n & 1);
+                const int f = 8 * j + 4 * ((n >> 1) & 1) + 2 * tsr + (n & 1);
+                const int l = ((f & 1) << 4) | (f >> 1);
+                const float* rs = red + (it & 1) * kFWarps * 4 * 32 + (n >> 2) * 32 + l;
                 float s2 = 0.f;
 #pragma unroll
-                for (int w = 0; w < kBwdWarps; w++) s2 += red[(w * NP + (n >> 1)) * 32 + f];
+                for (int w = 0; w < kFWarps; w++) s2 += rs[w * 4 * 32];
                 a.part_bc[(((b * a.nblk + blockIdx.x) * 2 + tsr) * 16 + n) * a.seqlen + t0 + j] = s2;
             }
         }
-        __syncthreads();
     }
+    cp_async_wait<0>();
     if (!active) return;
 #pragma unroll
-    for (int p = 0; p < NP; p++) {
+    for (int p = 0; p < kFNP; p++) {
         pf2 dA = dA1[p];
         if constexpr (ZOH) dA = pf2_fma(dA2[p], cst[p * 32 + lane].y, dA);
+        const int n = 2 * p;
         if (a.dh0 != nullptr) {
-            if (2 * p < a.dstate) a.dh0[chan * a.dstate + 2 * p] = pf2_lo(Gc[p]);
-            if (2 * p + 1 < a.dstate) a.dh0[chan * a.dstate + 2 * p + 1] = pf2_hi(Gc[p]);
+            if (n < a.dstate) a.dh0[chan * a.dstate + n] = pf2_lo(Gc[p]);
+            if (n + 1 < a.dstate) a.dh0[chan * a.dstate + n + 1] = pf2_hi(Gc[p]);
         }
-        a.part_A[chan * 16 + 2 * p] = pf2_lo(dA);
-        a.part_A[chan * 16 + 2 * p + 1] = pf2_hi(dA);
+        a.part_A[chan * 16 + n] = pf2_lo(dA);
+        a.part_A[chan * 16 + n + 1] = pf2_hi(dA);
     }
     a.part_D[chan] = dDacc;
     a.part_bias[chan] = dbacc;
@@ -566,13 +682,12 @@ __global__ void bwd_check_A_kernel(const float* A, int64_t n, int* flag) {
 // ACC = false: SFU fast math.  Both variants are launched; the one that does
 // not apply returns at once after reading the flag, so the choice needs no
 // host synchronisation and each variant keeps its own register budget.
-template <typename Tin, typename Tg, bool ZOH, bool HAS_Z, bool ACC>
+template <typename Tin, typename Tg, bool ZOH, bool HAS_Z>
 __global__ void __launch_bounds__(kBwdThreads)
 scan_bwd_kernel(const BwdArgs a, const int* flag) {
-    if constexpr (!ACC) {
-        if (*flag) return;
-    } else if constexpr (sizeof(Tin) == 2) {
-        if (!*flag) return;
+    constexpr bool ACC = true;
+    if constexpr (sizeof(Tin) == 2) {
+        if (!*flag) return;   // bf16 inputs take this kernel only when some A == 0 (ZOH)
     }
     extern __shared__ __align__(16) float smem_f[];
     float* sbc = smem_f;                                   // kTile x kRow
@@ -585,23 +700,13 @@ scan_bwd_kernel(const BwdArgs a, const int* flag) {
     const bool active = d_raw < a.dim;
     const int64_t d = active ? d_raw : a.dim - 1;
     const int64_t chan = b * a.dim + d;
-    if constexpr (ACC || sizeof(Tin) == 4) {
-        float* hb = hbuf + warp * 9 * 16 * 32 + lane;
-        float* r2 = red2 + warp * 32 * kRed2;
-        bwd_channel<Tin, Tg, ZOH, ACC, HAS_Z>(a, sbc, red, r2, hb, b, d, chan, active, tid);
-    } else {
-        float* sbcf = smem_f;                                   // kTile x kRowF
-        float* redf = sbcf + kTile * kRowF;                     // [warp][8 pairs][32]
-        float* r2f = redf + kBwdWarps * 8 * 32;                 // [warp][32][kRedF]
-        ulonglong2* cst = reinterpret_cast<ulonglong2*>(r2f + kBwdWarps * 32 * kRedF);   // [warp][8][32]
-        bwd_channel_fast<Tin, Tg, ZOH, HAS_Z>(a, sbcf, redf, r2f + warp * 32 * kRedF, cst + warp * 8 * 32,
-                                              b, d, chan, active, tid);
-    }
+    float* hb = hbuf + warp * 9 * 16 * 32 + lane;
+    float* r2 = red2 + warp * 32 * kRed2;
+    bwd_channel<Tin, Tg, ZOH, ACC, HAS_Z>(a, sbc, red, r2, hb, b, d, chan, active, tid);
 }
 
 constexpr int kBwdAccSmemFloats = kTile * kRow + kBwdWarps * kSub * 32 + kBwdWarps * 32 * kRed2 + kBwdWarps * 9 * 16 * 32;
 constexpr int kBwdAccSmemBytes = 4 * kBwdAccSmemFloats;
-constexpr int kBwdFastSmemBytes = 4 * kBwdFastSmemFloats;
 
 // dB[b, n, t] = sum over CTAs of the partials, in CTA order.
 __global__ void bwd_reduce_bc_kernel(const BwdArgs a, float* dB, float* dC) {
@@ -675,7 +780,7 @@ static BwdLayout bwd_layout(const ssm_scan_bwd_params* p, int num_sms) {
         f.checkpoints = reinterpret_cast<float*>(16);   // only sizes matter here
         l.fwd_ws = round256(fwd_workspace_bytes(&f, num_sms));
     }
-    const int64_t nblk = ceil_div(p->dim, (int64_t)kBwdThreads);
+    const int64_t nblk = ceil_div(p->dim, (int64_t)kFChans);
     l.part_bc = round256((size_t)(p->batch * nblk * 2 * 16 * p->seqlen) * 4);
     l.part_A = round256((size_t)(chans * 16) * 4);
     l.part_D = round256((size_t)chans * 4);
@@ -694,31 +799,30 @@ static bool al16(const void* ptr, ssm_strides s, int esize) {
 
 template <typename Tin, typename Tg>
 static cudaError_t launch_bwd_typed(const BwdArgs& a, bool zoh, bool has_z, int* flag, cudaStream_t st) {
-    const dim3 grid((unsigned)a.nblk, (unsigned)a.batch);
-    // the packed fast path is the bf16-input, approximate-math kernel
-    auto go = [&](auto kern, bool fast) -> cudaError_t {
-        const int bytes = fast ? kBwdFastSmemBytes : kBwdAccSmemBytes;
+    auto go = [&](auto kern, int threads, int64_t chans_per_cta, int bytes) -> cudaError_t {
+        const dim3 grid((unsigned)ceil_div(a.dim, chans_per_cta), (unsigned)a.batch);
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
         if (e != cudaSuccess) return e;
-        kern<<<grid, kBwdThreads, bytes, st>>>(a, flag);
+        kern<<<grid, threads, bytes, st>>>(a, flag);
         count_launches(1);
         return cudaGetLastError();
     };
-    auto pair = [&](auto fast, auto acc) -> cudaError_t {
-        if constexpr (sizeof(Tin) == 2) {
-            cudaError_t e = go(fast, true);
+    auto acc = [&](auto kern) { return go(kern, kBwdThreads, kBwdThreads, kBwdAccSmemBytes); };
+    auto fast = [&](auto kern) { return go(kern, kFThreads, kFChans, kBwdFastSmemBytes); };
+    if constexpr (sizeof(Tin) == 2) {
+        // bf16: the fast kernel; with ZOH the accurate one is queued too and runs
+        // instead when the device-side check finds an A == 0
+        if (zoh) {
+            cudaError_t e = has_z ? fast(scan_bwd_fast_kernel<Tg, true, true>) : fast(scan_bwd_fast_kernel<Tg, true, false>);
             if (e != cudaSuccess) return e;
+            return has_z ? acc(scan_bwd_kernel<Tin, Tg, true, true>) : acc(scan_bwd_kernel<Tin, Tg, true, false>);
         }
-        return go(acc, false);
-    };
-    if (zoh) return has_z ? pair(scan_bwd_kernel<Tin, Tg, true, true, false>, scan_bwd_kernel<Tin, Tg, true, true, true>)
-                          : pair(scan_bwd_kernel<Tin, Tg, true, false, false>, scan_bwd_kernel<Tin, Tg, true, false, true>);
-    // the simplified rule has no A == 0 limit: the fast path always applies to bf16
-    if constexpr (sizeof(Tin) == 2)
-        return has_z ? go(scan_bwd_kernel<Tin, Tg, false, true, false>, true)
-                     : go(scan_bwd_kernel<Tin, Tg, false, false, false>, true);
-    return has_z ? go(scan_bwd_kernel<Tin, Tg, false, true, true>, false)
-                 : go(scan_bwd_kernel<Tin, Tg, false, false, true>, false);
+        return has_z ? fast(scan_bwd_fast_kernel<Tg, false, true>) : fast(scan_bwd_fast_kernel<Tg, false, false>);
+    } else {
+        if (zoh) return has_z ? acc(scan_bwd_kernel<Tin, Tg, true, true>) : acc(scan_bwd_kernel<Tin, Tg, true, false>);
+        return has_z ? acc(scan_bwd_kernel<Tin, Tg, false, true>) : acc(scan_bwd_kernel<Tin, Tg, false, false>);
+    }
 }
 
 cudaError_t launch_scan_bwd(const ssm_scan_bwd_params* p, void* ws, int num_sms, cudaStream_t st) {
@@ -777,7 +881,7 @@ cudaError_t launch_scan_bwd(const ssm_scan_bwd_params* p, void* ws, int num_sms,
     a.vec_du = al16(p->du, p->du_strides, gsz);
     a.vec_ddt = al16(p->ddelta, p->ddelta_strides, gsz);
     a.vec_dz = al16(p->dz, p->dz_strides, gsz);
-    a.nblk = (int)ceil_div(p->dim, (int64_t)kBwdThreads);
+    a.nblk = (int)ceil_div(p->dim, (int64_t)kFChans);
     a.part_bc = reinterpret_cast<float*>(wp);
     a.part_A = reinterpret_cast<float*>(wp + l.part_bc);
     a.part_D = reinterpret_cast<float*>(wp + l.part_bc + l.part_A);

@@ -167,6 +167,12 @@ __device__ __forceinline__ float scan_step(float (&h)[NPL], const float (&Ak)[NP
     return y;
 }
 
+// 8-byte global store of a packed pair under a predicate (no branch)
+__device__ __forceinline__ void st_global_pf2_if(uintptr_t addr, pf2 v, bool pred) {
+    asm volatile("{\n .reg .pred q;\n setp.ne.u32 q, %2, 0;\n @q st.global.b64 [%0], %1;\n}\n" ::"l"(addr), "l"(v),
+                 "r"((unsigned)pred));
+}
+
 // Eight consecutive steps for this lane's NP state pairs, fast (SFU)
 // arithmetic on packed f32x2 registers.  Groups of two pairs are the outer
 // loop and steps the inner one: for one group the exponentials and input
@@ -175,10 +181,14 @@ __device__ __forceinline__ float scan_step(float (&h)[NPL], const float (&Ak)[NP
 // serially; one 16-byte shared load brings the group's four B (or C) values
 // of a step.  `bc` points at the staged fp32 row of the first step; yacc[j]
 // receives this lane's part of C.h for step j.  A2 = A log2(e), I2 = -1/A.
+// `mid`, when not null, points at pair 0 of the checkpoint that receives the
+// state after the fourth step (the state before step t0 + 4); consecutive
+// pairs are `pstride` floats apart.
 template <int NP, bool ZOH, bool READOUT>
 __device__ __forceinline__ void scan_block8(pf2 (&h2)[NP], const pf2 (&A2)[NP], const pf2 (&I2)[NP],
                                             const float (&dl8)[kSub], const float (&u8)[kSub], const float* bc,
-                                            int n_base, float (&yacc)[kSub]) {
+                                            int n_base, float (&yacc)[kSub], float* mid, int64_t pstride,
+                                            int dstate) {
     static_assert(NP % 2 == 0, "pairs are processed two at a time");
     pf2 dl2[kSub], u2[kSub], y2[kSub];
 #pragma unroll
@@ -211,6 +221,13 @@ __device__ __forceinline__ void scan_block8(pf2 (&h2)[NP], const pf2 (&A2)[NP], 
                 y2[j] = pf2_fma(C4.x, ha, y2[j]);
                 y2[j] = pf2_fma(C4.y, hb, y2[j]);
             }
+            if (j == kSub / 2 - 1) {
+                // predicated stores, no branch: the unrolled steps stay one block
+                const int n = n_base + 2 * p;   // states past dstate are zero
+                const uintptr_t m = reinterpret_cast<uintptr_t>(mid);
+                st_global_pf2_if(m + (uintptr_t)((n >> 1) * pstride) * 4, ha, m != 0 && n < dstate);
+                st_global_pf2_if(m + (uintptr_t)(((n >> 1) + 1) * pstride) * 4, hb, m != 0 && n + 2 < dstate);
+            }
         }
         h2[p] = ha;
         h2[p + 1] = hb;
@@ -219,18 +236,26 @@ __device__ __forceinline__ void scan_block8(pf2 (&h2)[NP], const pf2 (&A2)[NP], 
     for (int j = 0; j < kSub; j++) yacc[j] = pf2_sum(y2[j]);
 }
 
-// Store this lane's NPL checkpoint values (states n_base ..): 16-byte vector
-// stores when the row has all 16 states, element stores otherwise.
+// Checkpoints are laid out (batch, n_ckpt, ceil(dstate/2), dim, 2): the state
+// pairs of neighbouring channels sit side by side, so a warp's 8-byte stores
+// (and the backward's loads) coalesce.  Pointer to pair `pair` of checkpoint k
+// of channel (b, d):
+__device__ __forceinline__ float* ckpt_pair(const FwdArgs& a, int64_t b, int64_t k, int64_t d, int pair) {
+    const int64_t P = (a.dstate + 1) >> 1;
+    return a.ckpt + (((b * a.n_ckpt + k) * P + pair) * a.dim + d) * 2;
+}
+
+// Store this lane's NPL checkpoint values (states n_base ..) of checkpoint k;
+// the partner of a last odd state is written as zero.
 template <int NPL>
-__device__ __forceinline__ void store_ckpt(float* row, int n_base, int dstate, const float (&v)[NPL]) {
-    if (dstate == kNMax) {
+__device__ __forceinline__ void store_ckpt(const FwdArgs& a, int64_t b, int64_t k, int64_t d, int n_base,
+                                           const float (&v)[NPL]) {
 #pragma unroll
-        for (int q = 0; q < NPL / 4; q++)
-            reinterpret_cast<float4*>(row + n_base)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-    } else {
-#pragma unroll
-        for (int j = 0; j < NPL; j++)
-            if (n_base + j < dstate) row[n_base + j] = v[j];
+    for (int i = 0; i < NPL / 2; i++) {
+        const int n = n_base + 2 * i;
+        if (n < a.dstate)
+            *reinterpret_cast<float2*>(ckpt_pair(a, b, k, d, n >> 1)) =
+                make_float2(v[2 * i], (n + 1 < a.dstate) ? v[2 * i + 1] : 0.f);
     }
 }
 
@@ -267,8 +292,7 @@ __device__ __forceinline__ void scan_warp(const FwdArgs& a, float* sbc_all, int6
     Tout* orow = (MODE == kFull && a.out != nullptr) ? reinterpret_cast<Tout*>(a.out) + b * a.so_b + d * a.so_d : nullptr;
     const Tin* Bb = reinterpret_cast<const Tin*>(a.B) + b * a.sB_b;
     const Tin* Cb = reinterpret_cast<const Tin*>(a.C) + b * a.sC_b;
-    float* ck = (MODE == kFull && a.ckpt != nullptr)
-                    ? a.ckpt + (b * a.dim + d) * a.n_ckpt * a.dstate : nullptr;
+    const bool ck = MODE == kFull && a.ckpt != nullptr;
     int64_t next_ck = ceil_div(t_begin, a.ckpt_K) * a.ckpt_K;   // next step that starts a checkpoint
 
     float sd = 0.f, sd_c = 0.f;   // Kahan sum of delta (summary pass)
@@ -292,8 +316,8 @@ __device__ __forceinline__ void scan_warp(const FwdArgs& a, float* sbc_all, int6
         for (int64_t t0 = tt; t0 < tile_end; t0 += kSub) {
             load_sub(2, t0 + 2 * kSub);
             const int cnt = (int)((tile_end - t0) < kSub ? (tile_end - t0) : kSub);
-            if (ck != nullptr && t0 == next_ck) {
-                if (active) store_ckpt<NPL>(ck + (t0 / a.ckpt_K) * a.dstate, n_base, a.dstate, h);
+            if (ck && t0 == next_ck) {
+                if (active) store_ckpt<NPL>(a, b, t0 / a.ckpt_K, d, n_base, h);
                 next_ck += a.ckpt_K;
             }
             float yout[kSub];
@@ -303,6 +327,10 @@ __device__ __forceinline__ void scan_warp(const FwdArgs& a, float* sbc_all, int6
                 const float v = rd[0].get(j) + bias;
                 float dl = a.softplus ? (ACC ? softplus_accurate(v) : softplus_fast(v)) : v;
                 if (j >= cnt) dl = 0.f;
+                if (j == kSub / 2 && ck && t0 + j == next_ck && j < cnt) {
+                    if (active) store_ckpt<NPL>(a, b, (t0 + j) / a.ckpt_K, d, n_base, h);
+                    next_ck += a.ckpt_K;
+                }
                 const float* row = sbc_all + (t0 - tt + j) * kRow;
                 float y = scan_step<NPL, ZOH, ACC, MODE == kFull>(h, Ak, Ik, dl, uj, row, n_base);
                 if constexpr (MODE == kSummary) {
@@ -479,8 +507,7 @@ __device__ __forceinline__ void scan_cta_async(const FwdArgs& a, unsigned char* 
     const float bias = (a.bias != nullptr) ? __ldg(a.bias + d) : 0.f;
     // out == NULL: checkpoint-only pass (used by the backward), nothing is stored
     Tout* orow = (MODE == kFull && a.out != nullptr) ? reinterpret_cast<Tout*>(a.out) + b * a.so_b + d * a.so_d : nullptr;
-    float* ck = (MODE == kFull && a.ckpt != nullptr)
-                    ? a.ckpt + (b * a.dim + d) * a.n_ckpt * a.dstate : nullptr;
+    const bool ck = MODE == kFull && a.ckpt != nullptr;
     int64_t next_ck = ceil_div(t_begin, a.ckpt_K) * a.ckpt_K;   // next step that starts a checkpoint
     float* bcf = reinterpret_cast<float*>(smem + kStages * kStage);
     constexpr bool kZ = HAS_Z && MODE == kFull;
@@ -531,12 +558,12 @@ __device__ __forceinline__ void scan_cta_async(const FwdArgs& a, unsigned char* 
             const int64_t t0 = tt + c * kSub;
             if (t0 >= t_end) break;
             const int cnt = (int)((t_end - t0) < kSub ? (t_end - t0) : kSub);
-            if (ck != nullptr && t0 == next_ck) {
+            if (ck && t0 == next_ck) {
                 if (active) {
                     float hv[NPL];
 #pragma unroll
                     for (int j = 0; j < NPL; j++) hv[j] = (j & 1) ? pf2_hi(h2[j >> 1]) : pf2_lo(h2[j >> 1]);
-                    store_ckpt<NPL>(ck + (t0 / a.ckpt_K) * a.dstate, n_base, a.dstate, hv);
+                    store_ckpt<NPL>(a, b, t0 / a.ckpt_K, d, n_base, hv);
                 }
                 next_ck += a.ckpt_K;
             }
@@ -569,8 +596,14 @@ __device__ __forceinline__ void scan_cta_async(const FwdArgs& a, unsigned char* 
                         dl8[j] = __shfl_sync(0xffffffffu, spm[j % SPL], (lane & ~(G - 1)) | (j / SPL));
                 }
             }
+            float* mid = nullptr;   // checkpoint of the state before step t0 + 4, if one is due
+            if (ck && t0 + kSub / 2 == next_ck && t0 + kSub / 2 < t_end) {
+                if (active) mid = ckpt_pair(a, b, (t0 + kSub / 2) / a.ckpt_K, d, 0);
+                next_ck += a.ckpt_K;
+            }
             float yp[kSub];
-            scan_block8<NP, ZOH, MODE == kFull>(h2, A2, I2, dl8, u8, bcf + c * kSub * kRow, n_base, yp);
+            scan_block8<NP, ZOH, MODE == kFull>(h2, A2, I2, dl8, u8, bcf + c * kSub * kRow, n_base, yp, mid,
+                                                2 * a.dim, a.dstate);
             if constexpr (MODE == kSummary) {
 #pragma unroll
                 for (int j = 0; j < kSub; j++) {

@@ -71,9 +71,9 @@ def test_host_validation_without_gpu():
     p.bbar_mode = 7
     assert lib.ssm_scan_fwd(ctypes.byref(p), None, 0, None) == -1
     p.bbar_mode = 0
-    p.checkpoints, p.checkpoint_every = 16, 12
-    assert lib.ssm_scan_fwd(ctypes.byref(p), None, 0, None) == -2      # not a multiple of 8
-    p.checkpoint_every = 8
+    p.checkpoints, p.checkpoint_every = 16, 6
+    assert lib.ssm_scan_fwd(ctypes.byref(p), None, 0, None) == -2      # not a multiple of 4
+    p.checkpoint_every = 4
     p.u_strides.row = -1
     assert lib.ssm_scan_fwd(ctypes.byref(p), None, 0, None) == -1
     q = B.ScanBwdParams()

@@ -49,11 +49,11 @@ def layer_1p4b():
     seed = S.config_seed(2)
     b, d, T, N = 8, 4096, 16384, 16
     g = S.scan_inputs(seed, b, d, T, N, dtype=torch.bfloat16, device="cuda", with_dout=True)
-    ck = torch.empty(b, d, (T + 7) // 8, N, device="cuda")
+    ck = L.checkpoint_buffer(b, d, T, N)
     y = L.ssm_scan_fwd(g["u"], g["dt"], g["A"], g["B"], g["C"], D=g["D"], delta_bias=g["bias"], z=g["z"],
-                       checkpoints=ck, checkpoint_every=8)
+                       checkpoints=ck, checkpoint_every=4)
     grads = L.ssm_scan_bwd(g["u"], g["dt"], g["A"], g["B"], g["C"], g["dout"], D=g["D"], delta_bias=g["bias"],
-                           z=g["z"], checkpoints=ck, checkpoint_every=8, grad_dtype=torch.float32)
+                           z=g["z"], checkpoints=ck, checkpoint_every=4, grad_dtype=torch.float32)
     torch.cuda.synchronize()
     rng = np.random.default_rng(7)
     chans = sorted(rng.choice(b * d, size=12, replace=False).tolist())
@@ -111,7 +111,7 @@ def test_1p4b_backward_dB_dC_masked(layer_1p4b):
     mask[chans] = 1
     dout_m = (g["dout"].view(b * d, T) * mask).view(b, d, T)
     gr = L.ssm_scan_bwd(g["u"], g["dt"], g["A"], g["B"], g["C"], dout_m, D=g["D"], delta_bias=g["bias"], z=g["z"],
-                        checkpoints=ck, checkpoint_every=8, grad_dtype=torch.float32)
+                        checkpoints=ck, checkpoint_every=4, grad_dtype=torch.float32)
     ref_dB = np.zeros((b, N, T))
     ref_dC = np.zeros((b, N, T))
     for c in chans:

@@ -34,12 +34,12 @@ def run_and_check(g, dtype, zoh=True, softplus=True, use_D=True, use_bias=True, 
     ck = None
     if use_ckpt:
         batch, dim, Lq = g["u"].shape
-        ck = torch.empty(batch, dim, (Lq + 7) // 8, g["A"].shape[1], device="cuda")
-        L.ssm_scan_fwd(dev["u"], dev["dt"], dev["A"], dev["B"], dev["C"], checkpoints=ck, checkpoint_every=8,
+        ck = L.checkpoint_buffer(batch, dim, Lq, g["A"].shape[1])
+        L.ssm_scan_fwd(dev["u"], dev["dt"], dev["A"], dev["B"], dev["C"], checkpoints=ck, checkpoint_every=4,
                        out_dtype=torch.float32, **kw)
     grads = L.ssm_scan_bwd(dev["u"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["dout"],
                            dfinal_state=dev["dhN"] if use_dhN else None, checkpoints=ck,
-                           checkpoint_every=8 if use_ckpt else 0, grad_dtype=torch.float32, **kw)
+                           checkpoint_every=4 if use_ckpt else 0, grad_dtype=torch.float32, **kw)
     ref = oracle.scan_bwd(g["u"], g["dt"], g["A"], g["B"], g["C"], g["dout"], g["D"] if use_D else None,
                           g["bias"] if use_bias else None, g["z"], g["h0"], g["dhN"] if use_dhN else None,
                           zoh=zoh, delta_softplus=softplus, threads=THREADS)
