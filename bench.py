@@ -41,6 +41,14 @@ WORK = dict(batch=8, dim=4096, dstate=16, seqlen=16384, width=4)
 # Mamba-2.8B-shaped decode (64 layers, batch 128)
 DECODE = dict(batch=128, dim=5120, dstate=16, width=4, layers=64, steps=128)
 
+# DRAM traffic of each entry point per channel-token (dram__bytes_read.sum +
+# dram__bytes_write.sum summed over the entry point's launches) from one ncu
+# capture at batch 8, d_inner 4096, L 2048 (the command is in profiles/).  The
+# figures hold only while the CUDA sources hash to TRAFFIC_SOURCES_SHA; after
+# any kernel change the traffic is reported as null until it is captured again.
+TRAFFIC_PER_CT = {"ssm_scan_bwd": 35.11, "ssm_scan_fwd": 23.15, "causal_conv1d_silu": 3.20}
+TRAFFIC_SOURCES_SHA = "52bd1fc438d3f028"
+
 SM_FP32_LANES = 128     # FP32 lanes per SM per clock (sm_100 family)
 SM_SFU_EX2 = 32         # MUFU ex2 results per SM per clock on B300 (measured 29.8 at ~2 GHz)
 FALLBACK_HBM_GBS = 6400.0
@@ -136,6 +144,26 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
                 "samples": len(rows), "reasons": reasons}
+
+
+def kernel_sources_sha() -> str:
+    """sha256 (first 16 hex digits) of the CUDA sources of the library."""
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "selective_state_space_147_b300", "csrc", "*"))):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(f, "rb") as fh:
+                h.update(os.path.basename(f).encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_bytes(kernel: str, channel_tokens: int):
+    """Captured DRAM bytes of one launch of `kernel`'s entry point, scaled to
+    `channel_tokens`, or None when no capture matches the current sources."""
+    if TRAFFIC_SOURCES_SHA is None or kernel not in TRAFFIC_PER_CT or kernel_sources_sha() != TRAFFIC_SOURCES_SHA:
+        return None
+    return int(TRAFFIC_PER_CT[kernel] * channel_tokens)
 
 
 # ---------------------------------------------------------------------------
@@ -472,10 +500,14 @@ def main(argv=None):
                              channel_tokens_per_s=round(ct_step / (bwd_ms * 1e-3), 1),
                              roofline=roofline(bw, bwd_ms * 1e-3, hbm_gbs, sms, sm_mhz, hbm_src, clock_src)),
     }
+    for k in kern:
+        kern[k]["roofline"]["traffic"] = traffic_bytes(k, ct_step)
     dominant = max(kern, key=lambda k: kern[k]["ms"])
     roof = dict(kern[dominant]["roofline"])
     roof["kernel"] = dominant
-    roof["traffic"] = None
+    roof["traffic"] = traffic_bytes(dominant, ct_step)
+    roof["traffic_unit"] = "bytes per launch of the entry point (ncu capture scaled by channel-tokens)"
+    roof["sources_sha"] = kernel_sources_sha()
 
     # end to end through the public API with host buffers
     e2e = None

@@ -514,6 +514,15 @@ scan_bwd_fast_kernel(const BwdArgs a, const int* flag) {
                 dy[j] = go;
             }
         }
+        // the per-step scalars duplicated into both halves of a packed register
+        pf2 dl2[kFSub], u2[kFSub], dy2[kFSub];
+#pragma unroll
+        for (int j = 0; j < kFSub; j++) {
+            dl2[j] = pf2_make(dl[j], dl[j]);
+            const float uu = ZOH ? uj[j] : dl[j] * uj[j];   // simplified rule: delta u
+            u2[j] = pf2_make(uu, uu);
+            dy2[j] = pf2_make(dy[j], dy[j]);
+        }
         pf2 du2[kFSub], dd2[kFSub], yv2[kFSub];
 #pragma unroll
         for (int j = 0; j < kFSub; j++) du2[j] = dd2[j] = yv2[j] = 0ull;
@@ -545,13 +554,13 @@ scan_bwd_fast_kernel(const BwdArgs a, const int* flag) {
 #pragma unroll
                 for (int q = 0; q < 2; q++) {
                     const ulonglong2 bc = *reinterpret_cast<const ulonglong2*>(bc0 + j * kRowF + 4 * (2 * c + q));
-                    ab[q][j] = pf2_ex2(pf2_scale(dl[j], A2L[q]));
+                    ab[q][j] = pf2_ex2(pf2_mul(dl2[j], A2L[q]));
                     pf2 inc;
                     if constexpr (ZOH) {
                         cf[q][j] = pf2_fma(ab[q][j], IA[q], NI[q]);          // (Abar - 1) / A
-                        inc = pf2_mul(cf[q][j], pf2_scale(uj[j], bc.x));
+                        inc = pf2_mul(cf[q][j], pf2_mul(u2[j], bc.x));
                     } else {
-                        inc = pf2_scale(dl[j] * uj[j], bc.x);
+                        inc = pf2_mul(u2[j], bc.x);                          // delta u B
                     }
                     hs[q][j + 1] = pf2_fma(ab[q][j], hs[q][j], inc);
                     if constexpr (HAS_Z) yv2[j] = pf2_fma(bc.y, hs[q][j + 1], yv2[j]);
@@ -571,23 +580,23 @@ scan_bwd_fast_kernel(const BwdArgs a, const int* flag) {
 #pragma unroll
                 for (int q = 0; q < 2; q++) {
                     const ulonglong2 bc = *reinterpret_cast<const ulonglong2*>(bc0 + j * kRowF + 4 * (2 * c + q));
-                    const pf2 Gt = pf2_scale_add(dy[j], bc.y, G[q]);
-                    const pf2 dC = pf2_scale(dy[j], hs[q][j + 1]);
+                    const pf2 Gt = pf2_fma(dy2[j], bc.y, G[q]);
+                    const pf2 dC = pf2_mul(dy2[j], hs[q][j + 1]);
                     const pf2 da = pf2_mul(Gt, hs[q][j]);                // dL/dAbar
                     const pf2 gb = pf2_mul(Gt, bc.x);
-                    const pf2 qa = pf2_scale(dl[j], ab[q][j]);           // dAbar/dA
+                    const pf2 qa = pf2_mul(dl2[j], ab[q][j]);            // dAbar/dA
                     pf2 dB;
                     if constexpr (ZOH) {
                         du2[j] = pf2_fma(gb, cf[q][j], du2[j]);
-                        dB = pf2_scale(uj[j], pf2_mul(Gt, cf[q][j]));
-                        const pf2 dcf = pf2_scale(uj[j], gb);            // dL/dcoef
+                        dB = pf2_mul(u2[j], pf2_mul(Gt, cf[q][j]));
+                        const pf2 dcf = pf2_mul(u2[j], gb);              // dL/dcoef
                         dd2[j] = pf2_fma(ab[q][j], pf2_fma(da, A2[q], dcf), dd2[j]);
                         a1[q] = pf2_fma(da, qa, a1[q]);
                         a2[q] = pf2_fma(dcf, pf2_sub(qa, cf[q][j]), a2[q]);   // times 1/A at the end
                     } else {
-                        du2[j] = pf2_scale_add(dl[j], gb, du2[j]);
-                        dB = pf2_scale(dl[j] * uj[j], Gt);
-                        dd2[j] = pf2_add(pf2_fma(pf2_mul(da, A2[q]), ab[q][j], dd2[j]), pf2_scale(uj[j], gb));
+                        du2[j] = pf2_fma(dl2[j], gb, du2[j]);
+                        dB = pf2_mul(u2[j], Gt);                         // delta u G
+                        dd2[j] = pf2_fma(pf2_mul(da, A2[q]), ab[q][j], pf2_fma(pf2_make(uj[j], uj[j]), gb, dd2[j]));
                         a1[q] = pf2_fma(da, qa, a1[q]);
                     }
                     G[q] = pf2_mul(Gt, ab[q][j]);
