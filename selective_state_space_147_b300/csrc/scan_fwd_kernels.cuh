@@ -173,6 +173,58 @@ __device__ __forceinline__ void st_global_pf2_if(uintptr_t addr, pf2 v, bool pre
                  "r"((unsigned)pred));
 }
 
+// Store this lane's NP state pairs (states n_base ..) into a checkpoint whose
+// pair n_base/2 is at p0, consecutive pairs pstride floats apart (states past
+// dstate hold zero, so a last odd state's partner is written as zero).
+template <int NP>
+__device__ __forceinline__ void store_ckpt_pairs(float* p0, int64_t pstride, int n_base, int dstate,
+                                                 const pf2 (&h2)[NP]) {
+    if (n_base + 2 * NP <= dstate) {
+#pragma unroll
+        for (int p = 0; p < NP; p++) *reinterpret_cast<pf2*>(p0 + p * pstride) = h2[p];
+    } else {
+#pragma unroll
+        for (int p = 0; p < NP; p++)
+            if (n_base + 2 * p < dstate) *reinterpret_cast<pf2*>(p0 + p * pstride) = h2[p];
+    }
+}
+
+// ZOH form of the eight steps with steps as the outer loop: every step updates
+// all NP pairs, whose exponentials and updates are independent, so each step
+// offers NP-way instruction-level parallelism; the readout uses two packed
+// accumulators.  The optional mid-block checkpoint is stored between the
+// fourth and the fifth step, outside the unrolled updates.
+template <int NP, bool READOUT>
+__device__ __forceinline__ void scan_block8_steps(pf2 (&h2)[NP], const pf2 (&A2)[NP], const pf2 (&I2)[NP],
+                                                  const float (&dl8)[kSub], const float (&u8)[kSub],
+                                                  const float* bc, int n_base, float (&yacc)[kSub], float* mid,
+                                                  int64_t pstride, int dstate) {
+#pragma unroll
+    for (int j = 0; j < kSub; j++) {
+        if (j == kSub / 2 && mid != nullptr) store_ckpt_pairs<NP>(mid + (n_base >> 1) * pstride, pstride, n_base, dstate, h2);
+        const pf2 dl2 = pf2_make(dl8[j], dl8[j]);
+        const pf2 u2 = pf2_make(u8[j], u8[j]);
+        const float* row = bc + j * kRow + n_base;
+        pf2 ya = 0ull, yb = 0ull;
+#pragma unroll
+        for (int p = 0; p < NP; p += 2) {
+            const ulonglong2 B4 = *reinterpret_cast<const ulonglong2*>(row + 2 * p);
+            const pf2 aba = pf2_ex2(pf2_mul(dl2, A2[p]));
+            const pf2 abb = pf2_ex2(pf2_mul(dl2, A2[p + 1]));
+            const pf2 kna = pf2_mul(pf2_mul(B4.x, u2), I2[p]);          // -k = -B u / A
+            const pf2 knb = pf2_mul(pf2_mul(B4.y, u2), I2[p + 1]);
+            h2[p] = pf2_fma(aba, pf2_sub(h2[p], kna), kna);             // Abar (h + k) - k
+            h2[p + 1] = pf2_fma(abb, pf2_sub(h2[p + 1], knb), knb);
+            if constexpr (READOUT) {
+                const ulonglong2 C4 = *reinterpret_cast<const ulonglong2*>(row + 16 + 2 * p);
+                ya = pf2_fma(C4.x, h2[p], ya);
+                yb = pf2_fma(C4.y, h2[p + 1], yb);
+            }
+        }
+        yacc[j] = READOUT ? pf2_sum(pf2_add(ya, yb)) : 0.f;
+    }
+}
+
 // Eight consecutive steps for this lane's NP state pairs, fast (SFU)
 // arithmetic on packed f32x2 registers.  Groups of two pairs are the outer
 // loop and steps the inner one: for one group the exponentials and input
@@ -190,6 +242,10 @@ __device__ __forceinline__ void scan_block8(pf2 (&h2)[NP], const pf2 (&A2)[NP], 
                                             int n_base, float (&yacc)[kSub], float* mid, int64_t pstride,
                                             int dstate) {
     static_assert(NP % 2 == 0, "pairs are processed two at a time");
+    if constexpr (ZOH) {
+        scan_block8_steps<NP, READOUT>(h2, A2, I2, dl8, u8, bc, n_base, yacc, mid, pstride, dstate);
+        return;
+    }
     pf2 dl2[kSub], u2[kSub], y2[kSub];
 #pragma unroll
     for (int j = 0; j < kSub; j++) {
@@ -559,12 +615,8 @@ __device__ __forceinline__ void scan_cta_async(const FwdArgs& a, unsigned char* 
             if (t0 >= t_end) break;
             const int cnt = (int)((t_end - t0) < kSub ? (t_end - t0) : kSub);
             if (ck && t0 == next_ck) {
-                if (active) {
-                    float hv[NPL];
-#pragma unroll
-                    for (int j = 0; j < NPL; j++) hv[j] = (j & 1) ? pf2_hi(h2[j >> 1]) : pf2_lo(h2[j >> 1]);
-                    store_ckpt<NPL>(a, b, t0 / a.ckpt_K, d, n_base, hv);
-                }
+                if (active)
+                    store_ckpt_pairs<NP>(ckpt_pair(a, b, t0 / a.ckpt_K, d, n_base >> 1), 2 * a.dim, n_base, a.dstate, h2);
                 next_ck += a.ckpt_K;
             }
             const uint4 wu = *reinterpret_cast<const uint4*>(st + 0 * kSeq + swz(row, c));
