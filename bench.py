@@ -266,8 +266,9 @@ def step(L, g, ev=None):
 
 
 def bench_decode(L, device, cfg, reps: int):
-    """64-layer single-token decode step (conv update + state update per layer),
-    captured once in a CUDA graph and replayed; microseconds per token step."""
+    """64-layer single-token decode step (conv update + state update per layer, as
+    the fused ssm_decode_step and as the two separate kernels), each captured once
+    in a CUDA graph and replayed; microseconds per token step."""
     import synthetic as S
     b, d, N, W, layers = cfg["batch"], cfg["dim"], cfg["dstate"], cfg["width"], cfg["layers"]
     seed = S.config_seed(3)
@@ -286,42 +287,56 @@ def bench_decode(L, device, cfg, reps: int):
         tok[-1]["xc"] = torch.empty(b, d, dtype=torch.bfloat16, device=device)
         tok[-1]["y"] = torch.empty(b, d, dtype=torch.bfloat16, device=device)
 
-    def token_step():
+    def token_step_unfused():
         for l in range(layers):
             t = tok[l]
             L.causal_conv1d_silu_update(cst[l], t["x"], w, out=t["xc"])
             L.ssm_state_update(st[l], t["xc"], t["dt"], A, t["B"], t["C"], D=Dp, delta_bias=bias, z=t["z"],
                                out=t["y"])
 
-    s = torch.cuda.Stream()
-    s.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(s):
+    def token_step_fused():
+        for l in range(layers):
+            t = tok[l]
+            L.ssm_decode_step(st[l], cst[l], t["x"], t["dt"], A, t["B"], t["C"], w, D=Dp, delta_bias=bias,
+                              z=t["z"], out=t["y"])
+
+    def time_graph(fn):
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                fn()
+        torch.cuda.current_stream().wait_stream(s)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            fn()
         for _ in range(3):
-            token_step()
-    torch.cuda.current_stream().wait_stream(s)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        token_step()
-    for _ in range(3):
-        graph.replay()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(reps):
-        graph.replay()
-    e1.record()
-    torch.cuda.synchronize()
-    us = e0.elapsed_time(e1) * 1e3 / reps
+            graph.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        del graph
+        return e0.elapsed_time(e1) * 1e3 / reps
+
+    us_unfused = time_graph(token_step_unfused)
+    us = time_graph(token_step_fused)
     # algorithmic bytes per layer-step: state r+w, conv window r+w, token rows
     # (x, dt, z read; conv output written then read; y written), B, C, params
-    per_layer = (2 * b * d * N * 4 + 2 * b * d * W * 2 + 6 * b * d * 2 + 2 * b * N * 2
+    per_layer = (2 * b * d * N * 4 + 2 * b * d * W * 2 + 4 * b * d * 2 + 2 * b * N * 2
                  + d * N * 4 + d * W * 4 + 2 * d * 4)
-    del graph
+    per_layer_unfused = per_layer + 2 * b * d * 2      # the conv output written, then read back
     return {"us_per_token_step": round(us, 2), "layers": layers, "batch": b, "dim": d, "dstate": N,
             "bytes_per_token_step": per_layer * layers, "gbs": round(per_layer * layers / (us * 1e-6) / 1e9, 1),
-            "kernels_per_token_step": 2 * layers, "cuda_graph": True, "token_steps": reps,
-            "note": "per layer: causal_conv1d_silu_update + ssm_state_update; 64 distinct layer states "
-                    "(2.7 GB) so nothing stays in L2"}
+            "kernels_per_token_step": layers, "cuda_graph": True, "token_steps": reps,
+            "unfused": {"us_per_token_step": round(us_unfused, 2), "kernels_per_token_step": 2 * layers,
+                        "gbs": round(per_layer_unfused * layers / (us_unfused * 1e-6) / 1e9, 1)},
+            "note": "per layer: one ssm_decode_step (conv update + state update fused); unfused = "
+                    "causal_conv1d_silu_update + ssm_state_update; 64 distinct layer states (2.7 GB) so "
+                    "nothing stays in L2"}
 
 
 # ---------------------------------------------------------------------------

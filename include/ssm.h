@@ -289,6 +289,50 @@ typedef struct {
 
 SSM_API ssm_status causal_conv1d_silu_update(const ssm_conv_update_params* p, ssm_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Fused single-token decode step: the conv update followed by the state
+ * update, in one kernel.  "Mamba 模型" flowchart for one token (conv node,
+ * SiLU, scan node, readout and gate) and its decode section "为什么 Mamba
+ * 推理更省" (per token only the fixed-size conv window and state change).
+ * The conv output xc_t = silu(sum_i weight[d,i] x_{t-i} + conv_bias[d]) is
+ * the scan input u_t; it stays in registers (fp32), so the result equals
+ * causal_conv1d_silu_update followed by ssm_state_update on an fp32 xc, and
+ * it is valid when delta, B, C and z of the token do not depend on xc_t
+ * (they are inputs here).
+ *
+ *   x                : (batch, dim) raw token input (before the conv), in_dtype
+ *   conv_state       : (batch, dim, width) in_dtype contiguous, oldest first,
+ *                      shifted IN PLACE; width 1..4
+ *   conv_weight      : (dim, width) float32 contiguous, weight[d,i] multiplies
+ *                      x_{t-i}; conv_bias: (dim) float32 or NULL
+ *   delta, z, B, C, A, D, delta_bias, state, out : as for ssm_state_update
+ *   xc_out           : (batch, dim) in_dtype or NULL: the conv output, if the
+ *                      caller wants it
+ * Memory-bound: reads and writes the state and the conv window once. */
+typedef struct {
+    int64_t batch, dim, dstate, width;
+    ssm_dtype in_dtype;
+    ssm_dtype out_dtype;
+    int bbar_mode;
+    int delta_softplus;
+    const void* x;     int64_t x_stride;
+    const void* delta; int64_t delta_stride;
+    const void* z;     int64_t z_stride;
+    const void* B;     int64_t B_stride;
+    const void* C;     int64_t C_stride;
+    void* out;         int64_t out_stride;
+    void* xc_out;      int64_t xc_stride;
+    void* conv_state;
+    const float* conv_weight;
+    const float* conv_bias;
+    const float* A;
+    const float* D;
+    const float* delta_bias;
+    float* state;
+} ssm_decode_step_params;
+
+SSM_API ssm_status ssm_decode_step(const ssm_decode_step_params* p, ssm_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Human-readable name of a status code (static string). */
 SSM_API const char* ssm_status_string(ssm_status s);

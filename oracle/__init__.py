@@ -189,6 +189,17 @@ def conv1d_silu(x, w, bias=None, state_in=None, want_state: bool = False):
     return (out, st) if want_state else out
 
 
+def decode_step(state, conv_state, x, dt, A, B, C, w, conv_bias=None, D=None, bias=None, z=None, zoh=True,
+                delta_softplus=True):
+    """One decode token through the conv node and the scan node ("Mamba 模型"
+    flowchart, decode section): the conv update of the raw token x, then the state
+    update with the conv output as the scan input.  Nothing is modified in place.
+    Returns (out, new_state, new_conv_state, conv_output)."""
+    xc, cs = conv1d_silu_update(conv_state, x, w, conv_bias)
+    out, st = state_update(state, xc, dt, A, B, C, D, bias, z, zoh=zoh, delta_softplus=delta_softplus)
+    return out, st, cs, xc
+
+
 def conv1d_silu_update(state, x, w, bias=None):
     """One decode conv step.  state: (batch, dim, W) (a new array is returned);
     x: (batch, dim).  Returns (out (batch, dim), new_state)."""

@@ -87,6 +87,22 @@ class StateUpdateParams(ctypes.Structure):
     ]
 
 
+class DecodeStepParams(ctypes.Structure):
+    _fields_ = [
+        ("batch", _i64), ("dim", _i64), ("dstate", _i64), ("width", _i64),
+        ("in_dtype", _int), ("out_dtype", _int), ("bbar_mode", _int), ("delta_softplus", _int),
+        ("x", _vp), ("x_stride", _i64),
+        ("delta", _vp), ("delta_stride", _i64),
+        ("z", _vp), ("z_stride", _i64),
+        ("B", _vp), ("B_stride", _i64),
+        ("C", _vp), ("C_stride", _i64),
+        ("out", _vp), ("out_stride", _i64),
+        ("xc_out", _vp), ("xc_stride", _i64),
+        ("conv_state", _vp), ("conv_weight", _fp), ("conv_bias", _fp),
+        ("A", _fp), ("D", _fp), ("delta_bias", _fp), ("state", _fp),
+    ]
+
+
 class ConvParams(ctypes.Structure):
     _fields_ = [
         ("batch", _i64), ("dim", _i64), ("seqlen", _i64), ("width", _i64),
@@ -117,6 +133,8 @@ _lib.ssm_scan_bwd.argtypes = [ctypes.POINTER(ScanBwdParams), _vp, ctypes.c_size_
 _lib.ssm_scan_bwd.restype = _int
 _lib.ssm_state_update.argtypes = [ctypes.POINTER(StateUpdateParams), _vp]
 _lib.ssm_state_update.restype = _int
+_lib.ssm_decode_step.argtypes = [ctypes.POINTER(DecodeStepParams), _vp]
+_lib.ssm_decode_step.restype = _int
 _lib.causal_conv1d_silu.argtypes = [ctypes.POINTER(ConvParams), _vp]
 _lib.causal_conv1d_silu.restype = _int
 _lib.causal_conv1d_silu_update.argtypes = [ctypes.POINTER(ConvUpdateParams), _vp]
@@ -400,6 +418,43 @@ def ssm_state_update(state, x, delta, A, B, C, *, D=None, delta_bias=None, z=Non
     p.out, p.out_stride = _ptr(out), _row_stride("out", out)
     p.A, p.D, p.delta_bias, p.state = _ptr(A), _ptr(D), _ptr(delta_bias), _ptr(state)
     _check(_lib.ssm_state_update(ctypes.byref(p), _stream(stream)))
+    return out
+
+
+def ssm_decode_step(state, conv_state, x, delta, A, B, C, conv_weight, *, conv_bias=None, D=None,
+                    delta_bias=None, z=None, bbar_mode: int = SSM_BBAR_ZOH, delta_softplus: bool = True,
+                    out: Optional[torch.Tensor] = None, out_dtype=None, xc_out: Optional[torch.Tensor] = None,
+                    stream=None):
+    """Fused decode step: conv update of the raw token x (batch, dim) through
+    ``conv_state`` (batch, dim, W, updated in place) and ``conv_weight`` (dim, W)
+    f32, then the state update of ``state`` (batch, dim, N) f32 (in place) with the
+    conv output as the scan input.  delta, z: (batch, dim); B, C: (batch, N).
+    Returns out (batch, dim); the conv output goes to ``xc_out`` when given."""
+    for name, t in (("x", x), ("delta", delta), ("B", B), ("C", C), ("z", z), ("conv_state", conv_state),
+                    ("xc_out", xc_out)):
+        _need_cuda(name, t)
+    _f32c("state", state)
+    if conv_state.dtype != x.dtype or not conv_state.is_contiguous():
+        raise ValueError("conv_state must be contiguous with the dtype of x")
+    A, D, delta_bias = _f32c("A", A), _f32c("D", D), _f32c("delta_bias", delta_bias)
+    conv_weight, conv_bias = _f32c("conv_weight", conv_weight), _f32c("conv_bias", conv_bias)
+    batch, dim = x.shape
+    if out is None:
+        out = torch.empty(batch, dim, dtype=_torch_dtype(out_dtype or x.dtype), device=x.device)
+    p = DecodeStepParams()
+    p.batch, p.dim, p.dstate, p.width = batch, dim, A.shape[1], conv_weight.shape[1]
+    p.in_dtype, p.out_dtype = _dtype_code(x.dtype), _dtype_code(out.dtype)
+    p.bbar_mode, p.delta_softplus = int(bbar_mode), 1 if delta_softplus else 0
+    p.x, p.x_stride = _ptr(x), _row_stride("x", x)
+    p.delta, p.delta_stride = _ptr(delta), _row_stride("delta", delta)
+    p.z, p.z_stride = _ptr(z), _row_stride("z", z)
+    p.B, p.B_stride = _ptr(B), _row_stride("B", B)
+    p.C, p.C_stride = _ptr(C), _row_stride("C", C)
+    p.out, p.out_stride = _ptr(out), _row_stride("out", out)
+    p.xc_out, p.xc_stride = _ptr(xc_out), _row_stride("xc_out", xc_out)
+    p.conv_state, p.conv_weight, p.conv_bias = _ptr(conv_state), _ptr(conv_weight), _ptr(conv_bias)
+    p.A, p.D, p.delta_bias, p.state = _ptr(A), _ptr(D), _ptr(delta_bias), _ptr(state)
+    _check(_lib.ssm_decode_step(ctypes.byref(p), _stream(stream)))
     return out
 
 

@@ -118,7 +118,7 @@ const char* ssm_status_string(ssm_status s) {
 
 const char* ssm_last_error(void) { return g_err; }
 
-int ssm_abi_version(void) { return 1; }
+int ssm_abi_version(void) { return 2; }
 
 uint64_t ssm_launch_count(void) { return ssm::ssm_launch_count_value(); }
 
@@ -215,6 +215,26 @@ ssm_status causal_conv1d_silu_update(const ssm_conv_update_params* p, ssm_stream
     if (p->x_stride < 0 || p->out_stride < 0) return fail(SSM_ERR_INVALID_ARG, "negative stride");
     cudaError_t e = ssm::launch_conv1d_silu_update(p, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "causal_conv1d_silu_update launch");
+    return ok();
+}
+
+ssm_status ssm_decode_step(const ssm_decode_step_params* p, ssm_stream_t stream) {
+    if (p == nullptr) return fail(SSM_ERR_INVALID_ARG, "params is NULL");
+    if (p->batch < 1 || p->dim < 1 || p->dstate < 1 || p->width < 1) return fail(SSM_ERR_INVALID_ARG, "bad sizes");
+    if (p->dstate > 16) return fail(SSM_ERR_UNSUPPORTED, "dstate=%lld > 16", (long long)p->dstate);
+    if (p->width > 4) return fail(SSM_ERR_UNSUPPORTED, "width=%lld > 4", (long long)p->width);
+    if (p->batch > 65535 || p->dim > (1 << 28))
+        return fail(SSM_ERR_UNSUPPORTED, "batch > 65535 or dim > 2^28");
+    if (!dtype_ok(p->in_dtype) || !dtype_ok(p->out_dtype)) return fail(SSM_ERR_INVALID_ARG, "unknown dtype");
+    if (p->bbar_mode != SSM_BBAR_ZOH && p->bbar_mode != SSM_BBAR_SIMPLE)
+        return fail(SSM_ERR_INVALID_ARG, "unknown bbar_mode %d", p->bbar_mode);
+    if (!p->x || !p->delta || !p->B || !p->C || !p->out || !p->A || !p->state || !p->conv_state || !p->conv_weight)
+        return fail(SSM_ERR_INVALID_ARG, "x, delta, B, C, out, A, state, conv_state and conv_weight are required");
+    if (p->x_stride < 0 || p->delta_stride < 0 || p->z_stride < 0 || p->B_stride < 0 || p->C_stride < 0 ||
+        p->out_stride < 0 || p->xc_stride < 0)
+        return fail(SSM_ERR_INVALID_ARG, "negative stride");
+    cudaError_t e = ssm::launch_decode_step(p, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "ssm_decode_step launch");
     return ok();
 }
 

@@ -30,7 +30,7 @@ def lib():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for must in ("ssm_scan_fwd", "ssm_scan_fwd_workspace_size", "ssm_scan_bwd", "ssm_scan_bwd_workspace_size",
-                 "ssm_state_update",
+                 "ssm_state_update", "ssm_decode_step",
                  "causal_conv1d_silu", "causal_conv1d_silu_update", "ssm_status_string",
                  "ssm_last_error", "ssm_abi_version"):
         assert must in names
@@ -47,7 +47,7 @@ def test_status_strings_and_version(lib):
     names = {c: lib.ssm_status_string(c).decode() for c in (0, -1, -2, -3, -4, -5, -99)}
     assert names[0] == "SSM_OK" and names[-1] == "SSM_ERR_INVALID_ARG"
     assert names[-5] == "SSM_ERR_CUDA" and names[-99] == "SSM_ERR_UNKNOWN"
-    assert lib.ssm_abi_version() == 1
+    assert lib.ssm_abi_version() == 2
 
 
 def test_host_validation_without_gpu():
@@ -56,6 +56,7 @@ def test_host_validation_without_gpu():
     # NULL parameter blocks
     assert lib.ssm_scan_fwd(None, None, 0, None) == -1
     assert lib.ssm_state_update(None, None) == -1
+    assert lib.ssm_decode_step(None, None) == -1
     assert lib.causal_conv1d_silu(None, None) == -1
     assert lib.causal_conv1d_silu_update(None, None) == -1
     assert b"NULL" in lib.ssm_last_error()
@@ -89,3 +90,8 @@ def test_host_validation_without_gpu():
     s = B.StateUpdateParams()
     s.batch, s.dim, s.dstate = 1, 1, 16
     assert lib.ssm_state_update(ctypes.byref(s), None) == -1
+    ds = B.DecodeStepParams()
+    ds.batch, ds.dim, ds.dstate, ds.width = 1, 1, 16, 4
+    assert lib.ssm_decode_step(ctypes.byref(ds), None) == -1           # missing pointers
+    ds.width = 5
+    assert lib.ssm_decode_step(ctypes.byref(ds), None) == -2           # width > 4

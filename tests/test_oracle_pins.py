@@ -291,6 +291,36 @@ def test_conv_state_handoff_and_replay(L1):
 
 
 # --- Backward: central finite differences of the forward ------------------------
+@pytest.mark.parametrize("zoh", [True, False])
+def test_decode_steps_replay_conv_then_scan(zoh):
+    """Token-by-token decode steps (conv update, then state update on its output)
+    reproduce the sequence definitions: the conv over the whole sequence followed
+    by the selective scan with the conv output as its input."""
+    r = rng(9)
+    batch, dim, N, L, W = 2, 3, 5, 11, 4
+    x = r.normal(size=(batch, dim, L))
+    dt = r.normal(size=(batch, dim, L))
+    z = r.normal(size=(batch, dim, L))
+    Bm = r.normal(size=(batch, N, L))
+    Cm = r.normal(size=(batch, N, L))
+    A = -np.exp(r.normal(size=(dim, N)))
+    w = r.normal(size=(dim, W))
+    cb = r.normal(size=dim)
+    D = r.normal(size=dim)
+    bias = r.normal(size=dim) * 0.1
+    h0 = r.normal(size=(batch, dim, N))
+    xc = oracle.conv1d_silu(x, w, cb)
+    ref, href = oracle.scan_fwd(xc, dt, A, Bm, Cm, D, bias, z, h0, zoh=zoh)
+    st, cs = h0.copy(), np.zeros((batch, dim, W))
+    for t in range(L):
+        o, st, cs, xct = oracle.decode_step(st, cs, x[..., t], dt[..., t], A, Bm[..., t], Cm[..., t], w, cb, D,
+                                            bias, z[..., t], zoh=zoh)
+        assert rel_err(xct, xc[..., t]) < 1e-13
+        assert rel_err(o, ref[..., t]) < 1e-12
+    assert rel_err(st, href) < 1e-12
+    assert np.array_equal(cs, x[..., L - W:])
+
+
 def _loss(g, zoh, soft, dout, dhN):
     out, hN = oracle.scan_fwd(g["u"], g["dt"], g["A"], g["B"], g["C"], g["D"], g["bias"], g["z"],
                               g["h0"], zoh=zoh, delta_softplus=soft)
