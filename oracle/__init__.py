@@ -53,8 +53,9 @@ def _load():
             lib.oracle_state_update.argtypes = [i64, i64, i64] + [p] * 8 + [i32, i32, p, p]
             lib.oracle_conv1d_silu.argtypes = [i64, i64, i64, i64] + [p] * 6
             lib.oracle_conv1d_silu_update.argtypes = [i64, i64, i64] + [p] * 5
+            lib.oracle_conv1d_silu_bwd.argtypes = [i64, i64, i64, i64] + [p] * 9
             for f in (lib.oracle_scan_fwd, lib.oracle_scan_bwd, lib.oracle_state_update,
-                      lib.oracle_conv1d_silu, lib.oracle_conv1d_silu_update):
+                      lib.oracle_conv1d_silu, lib.oracle_conv1d_silu_update, lib.oracle_conv1d_silu_bwd):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -187,6 +188,25 @@ def conv1d_silu(x, w, bias=None, state_in=None, want_state: bool = False):
     if rc != 0:
         raise ValueError("oracle_conv1d_silu rejected its arguments")
     return (out, st) if want_state else out
+
+
+def conv1d_silu_bwd(x, w, dout, bias=None, state_in=None):
+    """Backward of conv1d_silu for the loss sum(dout * out) ("Mamba 模型" conv and
+    SiLU nodes).  Returns dict dx (batch, dim, L), dw (dim, W) and dbias (dim,)
+    summed over the batch, dstate_in (batch, dim, W) (None without state_in)."""
+    lib = _load()
+    x, w, dout, bias, state_in = map(_f64, (x, w, dout, bias, state_in))
+    batch, dim, L = x.shape
+    W = w.shape[1]
+    dx = np.zeros((batch, dim, L))
+    dw = np.zeros((dim, W))
+    db = np.zeros(dim)
+    ds = np.zeros((batch, dim, W)) if state_in is not None else None
+    rc = lib.oracle_conv1d_silu_bwd(batch, dim, L, W, _ptr(x), _ptr(w), _ptr(bias), _ptr(state_in), _ptr(dout),
+                                    _ptr(dx), _ptr(dw), _ptr(db), _ptr(ds))
+    if rc != 0:
+        raise ValueError("oracle_conv1d_silu_bwd rejected its arguments")
+    return dict(dx=dx, dw=dw, dbias=db, dstate_in=ds)
 
 
 def decode_step(state, conv_state, x, dt, A, B, C, w, conv_bias=None, D=None, bias=None, z=None, zoh=True,

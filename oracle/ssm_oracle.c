@@ -328,6 +328,70 @@ int oracle_conv1d_silu(int64_t batch, int64_t dim, int64_t seqlen, int64_t width
     return 0;
 }
 
+/* Backward of oracle_conv1d_silu for the loss sum(dout * out): the chain rule
+ * of the conv node and the SiLU node of [P1], one channel and one step at a
+ * time.  With pre_t = bias + sum_i w_i x_(t-i) and out_t = silu(pre_t):
+ *   dpre_t       = dout_t * silu'(pre_t),  silu'(p) = s (1 + p (1 - s)), s = sigmoid(p)
+ *   dx_s         = sum_i w_i dpre_(s+i)                  (s + i < seqlen)
+ *   dw[d, i]     = sum over b, t of dpre_t x_(t-i)       (x before t = 0 from state_in)
+ *   dbias[d]     = sum over b, t of dpre_t
+ *   dstate_in[k] = sum_i w_i dpre_(k-width+i)            (0 <= k-width+i < seqlen)
+ *   dout, dx : (batch, dim, seqlen); dw (dim, width); dbias (dim) or NULL;
+ *   dstate_in (batch, dim, width) or NULL */
+int oracle_conv1d_silu_bwd(int64_t batch, int64_t dim, int64_t seqlen, int64_t width,
+                           const double* x, const double* w, const double* bias,
+                           const double* state_in, const double* dout,
+                           double* dx, double* dw, double* dbias, double* dstate_in)
+{
+    if (batch < 0 || dim < 0 || seqlen < 0 || width < 1) return -1;
+    double* dpre = (double*)malloc((size_t)(seqlen > 0 ? seqlen : 1) * sizeof(double));
+    if (!dpre) return -2;
+    for (int64_t i = 0; i < dim * width; i++) dw[i] = 0.0;
+    if (dbias) for (int64_t d = 0; d < dim; d++) dbias[d] = 0.0;
+    for (int64_t c = 0; c < batch * dim; c++) {
+        const int64_t d = c % dim;
+        const double* xc = x + c * seqlen;
+#define XAT(tt) ((tt) >= 0 ? xc[(tt)] : (state_in ? state_in[c * width + width + (tt)] : 0.0))
+        for (int64_t t = 0; t < seqlen; t++) {
+            double pre = bias ? bias[d] : 0.0;
+            for (int64_t i = 0; i < width; i++) {
+                const int64_t tt = t - i;
+                if (tt < -width) continue;
+                pre += w[d * width + i] * XAT(tt);
+            }
+            const double s = o_sigmoid(pre);
+            dpre[t] = dout[c * seqlen + t] * s * (1.0 + pre * (1.0 - s));
+        }
+        for (int64_t t = 0; t < seqlen; t++) {
+            if (dbias) dbias[d] += dpre[t];
+            for (int64_t i = 0; i < width; i++) {
+                const int64_t tt = t - i;
+                if (tt < -width) continue;
+                dw[d * width + i] += dpre[t] * XAT(tt);
+            }
+        }
+        for (int64_t s = 0; s < seqlen; s++) {
+            double g = 0.0;
+            for (int64_t i = 0; i < width; i++)
+                if (s + i < seqlen) g += w[d * width + i] * dpre[s + i];
+            dx[c * seqlen + s] = g;
+        }
+        if (dstate_in) {
+            for (int64_t k = 0; k < width; k++) {
+                double g = 0.0;
+                for (int64_t i = 0; i < width; i++) {
+                    const int64_t t = k - width + i;
+                    if (t >= 0 && t < seqlen) g += w[d * width + i] * dpre[t];
+                }
+                dstate_in[c * width + k] = g;
+            }
+        }
+#undef XAT
+    }
+    free(dpre);
+    return 0;
+}
+
 /* One-token conv update: shift x_t into the stored window, then the conv and
  * SiLU for that token.  [P1] conv node for one t; [P3] section 03.
  *   state : (batch, dim, width), oldest first, read and overwritten

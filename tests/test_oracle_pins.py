@@ -269,6 +269,60 @@ def test_conv_matches_library_conv1d(with_bias):
     assert rel_err(out, _torch_conv(x, w, bias, 4)) < 1e-13
 
 
+@pytest.mark.parametrize("W", [1, 2, 3, 4])
+@pytest.mark.parametrize("with_state", [False, True])
+def test_conv_backward_matches_library_autograd(W, with_state):
+    """The conv backward equals autograd through torch's conv1d (fp64, CPU); the
+    state window is the first W inputs of an extended sequence."""
+    r = rng(11)
+    batch, dim, L = 2, 4, 19
+    x = r.normal(size=(batch, dim, L))
+    w = r.normal(size=(dim, W)) * 0.5
+    bias = r.normal(size=dim)
+    st = r.normal(size=(batch, dim, W)) if with_state else None
+    dout = r.normal(size=(batch, dim, L))
+    got = oracle.conv1d_silu_bwd(x, w, dout, bias, st)
+    xt = torch.from_numpy(np.concatenate([st, x], axis=2) if with_state else x).requires_grad_(True)
+    wt = torch.from_numpy(w).requires_grad_(True)
+    bt = torch.from_numpy(bias).requires_grad_(True)
+    pad = 0 if with_state else W - 1
+    y = torch.nn.functional.conv1d(torch.nn.functional.pad(xt, (pad, 0)), wt.flip(1)[:, None, :], bt, groups=dim)
+    y = torch.nn.functional.silu(y)[..., -L:]
+    (y * torch.from_numpy(dout)).sum().backward()
+    gx = xt.grad.numpy()
+    assert rel_err(got["dx"], gx[..., -L:]) < 1e-13
+    assert rel_err(got["dw"], wt.grad.numpy()) < 1e-13
+    assert rel_err(got["dbias"], bt.grad.numpy()) < 1e-13
+    if with_state:
+        assert rel_err(got["dstate_in"], gx[..., :W]) < 1e-13
+
+
+def test_conv_backward_matches_finite_differences():
+    r = rng(12)
+    batch, dim, L, W = 1, 2, 6, 3
+    x = r.normal(size=(batch, dim, L))
+    w = r.normal(size=(dim, W))
+    bias = r.normal(size=dim)
+    st = r.normal(size=(batch, dim, W))
+    dout = r.normal(size=(batch, dim, L))
+    got = oracle.conv1d_silu_bwd(x, w, dout, bias, st)
+    loss = lambda x_, w_, b_, s_: float(np.sum(dout * oracle.conv1d_silu(x_, w_, b_, s_)))
+    eps = 1e-6
+    for name, arr, key in (("x", x, "dx"), ("w", w, "dw"), ("bias", bias, "dbias"), ("state", st, "dstate_in")):
+        num = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            args = {"x": x, "w": w, "bias": bias, "state": st}
+            hi, lo = arr.copy(), arr.copy()
+            hi[idx] += eps
+            lo[idx] -= eps
+            args[name] = hi
+            fp = loss(args["x"], args["w"], args["bias"], args["state"])
+            args[name] = lo
+            fm = loss(args["x"], args["w"], args["bias"], args["state"])
+            num[idx] = (fp - fm) / (2 * eps)
+        assert rel_err(got[key], num) < 1e-7, name
+
+
 @pytest.mark.parametrize("L1", [0, 1, 2, 3, 4, 9])
 def test_conv_state_handoff_and_replay(L1):
     r = rng(8)
