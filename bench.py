@@ -5,7 +5,8 @@ One step = one pass of the hot path over one batch of the Mamba-1.4B-shaped
 layer (batch 8, d_inner 4096, d_state 16, L 16384, bf16 activations, fp32
 state, zero-order hold): causal conv1d + SiLU -> fused selective-scan forward
 (writing h checkpoints every 4 steps) -> selective-scan backward with
-recompute of h (all nine gradients).  Inputs are
+recompute of h (all nine gradients) -> conv1d + SiLU backward (dx, dweight).
+Inputs are
 synthetic (seeded counter-based generator), resident in HBM and larger than
 L2 (several GB per step), so no L2 flush is needed between steps.
 
@@ -173,6 +174,13 @@ def conv_work(b, d, L):
     return dict(bytes=4 * ct, fp32=0, sfu=0)
 
 
+def conv_bwd_work(b, d, L):
+    """x and dout read, dx written (bf16); per ct: conv recompute 4 FMA, SiLU
+    derivative ~5 FP32 + 2 SFU, dx 4 FMA, dw/dbias 5 FMA."""
+    ct = b * d * L
+    return dict(bytes=6 * ct, fp32=18 * ct, sfu=2 * ct)
+
+
 def fwd_work(b, d, L, N, zoh=True, io_bytes=2):
     """Compulsory HBM bytes: u, delta, z read + out written (io_bytes each per
     channel-token) + B, C read once (shared by all channels).  Operations per
@@ -242,11 +250,12 @@ def make_inputs(device, seed, cfg):
     g["y"] = torch.empty(b, d, L, dtype=torch.bfloat16, device=device)
     g["ckpt"] = torch.empty(b, (L + 3) // 4, (N + 1) // 2, d, 2, dtype=torch.float32, device=device)
     g["grads"] = None
+    g["cgrads"] = None
     return g
 
 
 def step(L, g, ev=None):
-    """conv1d + SiLU -> scan forward (with checkpoints) -> scan backward."""
+    """conv1d + SiLU -> scan forward (with checkpoints) -> scan backward -> conv backward."""
     if ev is not None:
         ev[0].record()
     L.causal_conv1d_silu(g["x"], g["w"], out=g["xc"])
@@ -263,6 +272,11 @@ def step(L, g, ev=None):
                                 workspace=g.get("ws_bwd"))
     if ev is not None:
         ev[3].record()
+    # du is the gradient of the conv output: back through the conv and SiLU
+    g["cgrads"] = L.causal_conv1d_silu_bwd(g["x"], g["w"], g["grads"]["du"], grads=g["cgrads"],
+                                           workspace=g.get("ws_cbwd"))
+    if ev is not None:
+        ev[4].record()
 
 
 def bench_decode(L, device, cfg, reps: int):
@@ -343,8 +357,8 @@ def bench_decode(L, device, cfg, reps: int):
 # CPU oracle (baseline arm)
 def oracle_sample_rate(channels: int, threads: int, cfg, seed: int):
     """Run the fp64 oracle over the step's hot path -- conv + SiLU, ZOH scan
-    forward, scan backward -- on `channels` channels of batch row 0 over the full
-    sequence; returns (channel-tokens/s, wall seconds)."""
+    forward, scan backward, conv backward -- on `channels` channels of batch row 0
+    over the full sequence; returns (channel-tokens/s, wall seconds)."""
     import oracle
     import synthetic as S
     L, N, W = cfg["seqlen"], cfg["dstate"], cfg["width"]
@@ -363,7 +377,8 @@ def oracle_sample_rate(channels: int, threads: int, cfg, seed: int):
     t0 = time.perf_counter()
     xc = oracle.conv1d_silu(x, w)
     oracle.scan_fwd(xc, dt, A, B, C, Dp, bias, z, zoh=True, threads=threads)
-    oracle.scan_bwd(xc, dt, A, B, C, dout, Dp, bias, z, zoh=True, threads=threads)
+    gr = oracle.scan_bwd(xc, dt, A, B, C, dout, Dp, bias, z, zoh=True, threads=threads)
+    oracle.conv1d_silu_bwd(x, w, gr["du"])
     wall = time.perf_counter() - t0
     return channels * L / wall, wall
 
@@ -383,7 +398,7 @@ def cpu_baseline(cfg, seed: int, target_s: float = 10.0):
     rate, wall = oracle_sample_rate(n, threads, cfg, seed)
     return {"value": round(rate, 1), "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"{n} channels of batch row 0, full L={cfg['seqlen']}: conv1d+SiLU, ZOH scan forward "
-                      f"and backward in fp64 ({wall:.1f} s wall on {threads} threads)"}
+                      f"and backward, conv backward in fp64 ({wall:.1f} s wall on {threads} threads)"}
 
 
 def run_reference(args):
@@ -413,7 +428,7 @@ def run_reference(args):
         "config": workload_config(cfg),
         "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": f"each step: {n} channels of batch row 0, full L={cfg['seqlen']}: "
-                                   "conv1d+SiLU, ZOH scan forward and backward, fp64 oracle"},
+                                   "conv1d+SiLU, ZOH scan forward and backward, conv backward, fp64 oracle"},
         "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -422,7 +437,8 @@ def run_reference(args):
 
 def workload_config(cfg):
     return {"workload": "mamba-1.4b-layer training pass: causal conv1d+SiLU -> fused selective-scan forward "
-                        "(checkpoints every 4 steps) -> selective-scan backward with recompute "
+                        "(checkpoints every 4 steps) -> selective-scan backward with recompute -> "
+                        "conv1d+SiLU backward "
                         f"(batch {cfg['batch']}, d_inner {cfg['dim']}, d_state {cfg['dstate']}, "
                         f"L {cfg['seqlen']}, ZOH, softplus delta, D skip, silu(z) gate)",
             "batch": cfg["batch"], "dim": cfg["dim"], "dstate": cfg["dstate"], "seqlen": cfg["seqlen"],
@@ -466,6 +482,8 @@ def main(argv=None):
     if ws_bytes:
         g["ws"] = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
     g["ws_bwd"] = torch.empty(L.ssm_scan_bwd_workspace_size(g["xc"], g["A"]), dtype=torch.uint8, device=device)
+    g["ws_cbwd"] = torch.empty(L.causal_conv1d_silu_bwd_workspace_size(g["x"], g["w"]), dtype=torch.uint8,
+                               device=device)
     props = torch.cuda.get_device_properties(device)
     sms = props.multi_processor_count
 
@@ -474,7 +492,7 @@ def main(argv=None):
     torch.cuda.synchronize()
 
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local)
     sampler.start()
@@ -494,6 +512,7 @@ def main(argv=None):
     conv_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     fwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
     bwd_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    cbwd_ms = statistics.mean(e[3].elapsed_time(e[4]) for e in evs)
 
     b, d, Lq, N = cfg["batch"], cfg["dim"], cfg["seqlen"], cfg["dstate"]
     ct_step = b * d * Lq
@@ -514,6 +533,9 @@ def main(argv=None):
         "ssm_scan_bwd": dict(ms=round(bwd_ms, 4), share=round(bwd_ms / (ms_total / K), 4),
                              channel_tokens_per_s=round(ct_step / (bwd_ms * 1e-3), 1),
                              roofline=roofline(bw, bwd_ms * 1e-3, hbm_gbs, sms, sm_mhz, hbm_src, clock_src)),
+        "causal_conv1d_silu_bwd": dict(ms=round(cbwd_ms, 4), share=round(cbwd_ms / (ms_total / K), 4),
+                                       roofline=roofline(conv_bwd_work(b, d, Lq), cbwd_ms * 1e-3, hbm_gbs, sms,
+                                                         sm_mhz, hbm_src, clock_src)),
     }
     for k in kern:
         kern[k]["roofline"]["traffic"] = traffic_bytes(k, ct_step)
@@ -533,6 +555,7 @@ def main(argv=None):
             host[k].copy_(g[k])
         outs = {"y": g["y"]}
         outs.update({k: v for k, v in g["grads"].items() if v is not None and k != "dh0"})
+        outs.update({"c_" + k: v for k, v in g["cgrads"].items() if v is not None})
         out_host = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs.items()}
         h2d = sum(host[k].numel() * host[k].element_size() for k in names_in)
         d2h = sum(v.numel() * v.element_size() for v in out_host.values())
@@ -546,7 +569,9 @@ def main(argv=None):
             step(L, g)
             out_host["y"].copy_(g["y"], non_blocking=True)
             for k in out_host:
-                if k != "y":
+                if k.startswith("c_"):
+                    out_host[k].copy_(g["cgrads"][k[2:]], non_blocking=True)
+                elif k != "y":
                     out_host[k].copy_(g["grads"][k], non_blocking=True)
         e1.record()
         torch.cuda.synchronize()

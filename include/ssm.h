@@ -274,6 +274,38 @@ typedef struct {
 
 SSM_API ssm_status causal_conv1d_silu(const ssm_conv_params* p, ssm_stream_t stream);
 
+/* Backward of causal_conv1d_silu for the loss sum(dout * out): the chain rule
+ * of the conv and SiLU nodes of the "Mamba 模型" flowchart.
+ *   x, weight, bias, state_in : as for causal_conv1d_silu (dtype of x)
+ *   dout       : (batch, dim, seqlen) dtype, strides as x
+ *   dx         : (batch, dim, seqlen) grad_dtype, strides dx_strides
+ *   dweight    : (dim, width) float32, summed over batch and t
+ *   dbias      : (dim) float32 or NULL
+ *   dstate_in  : (batch, dim, width) float32 or NULL: gradient of state_in
+ *                (zero where state_in is NULL)
+ * Memory-bound: reads x and dout once, writes dx once.  dweight and dbias
+ * are summed in a fixed order through per-block partials in the workspace
+ * (causal_conv1d_silu_bwd_workspace_size bytes, 256-byte aligned), so the
+ * result is bitwise reproducible. */
+typedef struct {
+    int64_t batch, dim, seqlen, width;
+    ssm_dtype dtype;
+    ssm_dtype grad_dtype;
+    const void* x;     ssm_strides x_strides;
+    const void* dout;  ssm_strides dout_strides;
+    void* dx;          ssm_strides dx_strides;
+    const float* weight;
+    const float* bias;
+    const void* state_in;
+    float* dweight;
+    float* dbias;
+    float* dstate_in;
+} ssm_conv_bwd_params;
+
+SSM_API size_t causal_conv1d_silu_bwd_workspace_size(const ssm_conv_bwd_params* p);
+SSM_API ssm_status causal_conv1d_silu_bwd(const ssm_conv_bwd_params* p, void* workspace, size_t workspace_bytes,
+                                          ssm_stream_t stream);
+
 /* One-token conv update: shift x_t into the window, then conv + SiLU.
  *   state : (batch, dim, width) dtype contiguous, oldest first, IN PLACE
  *   x,out : (batch, dim), batch stride in elements, unit dim stride */

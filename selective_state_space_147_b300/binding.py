@@ -113,6 +113,18 @@ class ConvParams(ctypes.Structure):
     ]
 
 
+class ConvBwdParams(ctypes.Structure):
+    _fields_ = [
+        ("batch", _i64), ("dim", _i64), ("seqlen", _i64), ("width", _i64),
+        ("dtype", _int), ("grad_dtype", _int),
+        ("x", _vp), ("x_strides", Strides),
+        ("dout", _vp), ("dout_strides", Strides),
+        ("dx", _vp), ("dx_strides", Strides),
+        ("weight", _fp), ("bias", _fp), ("state_in", _vp),
+        ("dweight", _fp), ("dbias", _fp), ("dstate_in", _fp),
+    ]
+
+
 class ConvUpdateParams(ctypes.Structure):
     _fields_ = [
         ("batch", _i64), ("dim", _i64), ("width", _i64),
@@ -135,6 +147,10 @@ _lib.ssm_state_update.argtypes = [ctypes.POINTER(StateUpdateParams), _vp]
 _lib.ssm_state_update.restype = _int
 _lib.ssm_decode_step.argtypes = [ctypes.POINTER(DecodeStepParams), _vp]
 _lib.ssm_decode_step.restype = _int
+_lib.causal_conv1d_silu_bwd.argtypes = [ctypes.POINTER(ConvBwdParams), _vp, ctypes.c_size_t, _vp]
+_lib.causal_conv1d_silu_bwd.restype = _int
+_lib.causal_conv1d_silu_bwd_workspace_size.argtypes = [ctypes.POINTER(ConvBwdParams)]
+_lib.causal_conv1d_silu_bwd_workspace_size.restype = ctypes.c_size_t
 _lib.causal_conv1d_silu.argtypes = [ctypes.POINTER(ConvParams), _vp]
 _lib.causal_conv1d_silu.restype = _int
 _lib.causal_conv1d_silu_update.argtypes = [ctypes.POINTER(ConvUpdateParams), _vp]
@@ -481,6 +497,65 @@ def causal_conv1d_silu(x, weight, *, bias=None, state_in=None, state_out=None,
     p.state_in, p.state_out = _ptr(state_in), _ptr(state_out)
     _check(_lib.causal_conv1d_silu(ctypes.byref(p), _stream(stream)))
     return out
+
+
+def _conv_bwd_params(x, weight, dout, bias, state_in, dx, dweight, dbias, dstate_in) -> ConvBwdParams:
+    batch, dim, L = x.shape
+    p = ConvBwdParams()
+    p.batch, p.dim, p.seqlen, p.width = batch, dim, L, weight.shape[1]
+    p.dtype, p.grad_dtype = _dtype_code(x.dtype), _dtype_code(dx.dtype)
+    p.x, p.x_strides = _ptr(x), _seq_strides("x", x)
+    p.dout, p.dout_strides = _ptr(dout), _seq_strides("dout", dout)
+    p.dx, p.dx_strides = _ptr(dx), _seq_strides("dx", dx)
+    p.weight, p.bias, p.state_in = _ptr(weight), _ptr(bias), _ptr(state_in)
+    p.dweight, p.dbias, p.dstate_in = _ptr(dweight), _ptr(dbias), _ptr(dstate_in)
+    return p
+
+
+def causal_conv1d_silu_bwd_workspace_size(x, weight) -> int:
+    """Workspace bytes causal_conv1d_silu_bwd needs for x (batch, dim, L) and weight (dim, W)."""
+    batch, dim, L = x.shape
+    p = ConvBwdParams()
+    p.batch, p.dim, p.seqlen, p.width = batch, dim, L, weight.shape[1]
+    return int(_lib.causal_conv1d_silu_bwd_workspace_size(ctypes.byref(p)))
+
+
+def causal_conv1d_silu_bwd(x, weight, dout, *, bias=None, state_in=None, grad_dtype=None,
+                           want_dstate: bool = False, grads: Optional[dict] = None,
+                           workspace: Optional[torch.Tensor] = None, stream=None):
+    """Backward of causal_conv1d_silu for the loss sum(dout * out).  Returns a dict with
+    dx (batch, dim, L) in grad_dtype (default: x's dtype), dweight (dim, W) and dbias (dim,)
+    f32 summed over the batch, and dstate_in (batch, dim, W) f32 when want_dstate.
+    ``grads`` may hold preallocated outputs under the same names."""
+    for name, t in (("x", x), ("dout", dout), ("state_in", state_in)):
+        _need_cuda(name, t)
+    if dout.dtype != x.dtype:
+        raise ValueError("dout must have the dtype of x")
+    if state_in is not None and (state_in.dtype != x.dtype or not state_in.is_contiguous()):
+        raise ValueError("state_in must be contiguous with the dtype of x")
+    weight, bias = _f32c("weight", weight), _f32c("bias", bias)
+    batch, dim, L = x.shape
+    W = weight.shape[1]
+    g = dict(grads or {})
+    dev = x.device
+    if g.get("dx") is None:
+        g["dx"] = torch.empty(batch, dim, L, dtype=_torch_dtype(grad_dtype or x.dtype), device=dev)
+    if g.get("dweight") is None:
+        g["dweight"] = torch.empty(dim, W, dtype=torch.float32, device=dev)
+    if g.get("dbias") is None and bias is not None:
+        g["dbias"] = torch.empty(dim, dtype=torch.float32, device=dev)
+    if want_dstate and g.get("dstate_in") is None:
+        g["dstate_in"] = torch.empty(batch, dim, W, dtype=torch.float32, device=dev)
+    for k in ("dweight", "dbias", "dstate_in"):
+        _f32c(k, g.get(k))
+    p = _conv_bwd_params(x, weight, dout, bias, state_in, g["dx"], g["dweight"], g.get("dbias"),
+                         g.get("dstate_in") if want_dstate else None)
+    need = int(_lib.causal_conv1d_silu_bwd_workspace_size(ctypes.byref(p)))
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    _check(_lib.causal_conv1d_silu_bwd(ctypes.byref(p), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                       _stream(stream)))
+    return g
 
 
 def causal_conv1d_silu_update(state, x, weight, *, bias=None, out: Optional[torch.Tensor] = None,

@@ -204,6 +204,33 @@ ssm_status causal_conv1d_silu(const ssm_conv_params* p, ssm_stream_t stream) {
     return ok();
 }
 
+size_t causal_conv1d_silu_bwd_workspace_size(const ssm_conv_bwd_params* p) {
+    if (p == nullptr || p->batch < 1 || p->dim < 1 || p->seqlen < 0 || p->width < 1 || p->width > 4) return 0;
+    return ssm::conv_bwd_workspace_bytes(p);
+}
+
+ssm_status causal_conv1d_silu_bwd(const ssm_conv_bwd_params* p, void* workspace, size_t workspace_bytes,
+                                  ssm_stream_t stream) {
+    if (p == nullptr) return fail(SSM_ERR_INVALID_ARG, "params is NULL");
+    if (p->batch < 1 || p->dim < 1 || p->seqlen < 0 || p->width < 1) return fail(SSM_ERR_INVALID_ARG, "bad sizes");
+    if (p->width > 4) return fail(SSM_ERR_UNSUPPORTED, "width=%lld > 4", (long long)p->width);
+    if (p->batch > 65535 || p->dim > 65535)
+        return fail(SSM_ERR_UNSUPPORTED, "batch or dim > 65535");
+    if (!dtype_ok(p->dtype) || !dtype_ok(p->grad_dtype)) return fail(SSM_ERR_INVALID_ARG, "unknown dtype");
+    if (!p->x || !p->dout || !p->dx || !p->weight || !p->dweight)
+        return fail(SSM_ERR_INVALID_ARG, "x, dout, dx, weight and dweight are required");
+    if (p->x_strides.batch < 0 || p->x_strides.row < 0 || p->dout_strides.batch < 0 || p->dout_strides.row < 0 ||
+        p->dx_strides.batch < 0 || p->dx_strides.row < 0)
+        return fail(SSM_ERR_INVALID_ARG, "negative stride");
+    const size_t need = ssm::conv_bwd_workspace_bytes(p);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need))
+        return fail(SSM_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace_bytes);
+    if (need > 0 && (uintptr_t)workspace % 256 != 0) return fail(SSM_ERR_MISALIGNED, "workspace must be 256-byte aligned");
+    cudaError_t e = ssm::launch_conv1d_silu_bwd(p, workspace, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "causal_conv1d_silu_bwd launch");
+    return ok();
+}
+
 ssm_status causal_conv1d_silu_update(const ssm_conv_update_params* p, ssm_stream_t stream) {
     if (p == nullptr) return fail(SSM_ERR_INVALID_ARG, "params is NULL");
     if (p->batch < 1 || p->dim < 1 || p->width < 1) return fail(SSM_ERR_INVALID_ARG, "bad sizes");

@@ -19,6 +19,8 @@ cudaError_t launch_scan_bwd(const ssm_scan_bwd_params* p, void* ws, int num_sms,
 size_t static_scratch_bytes();
 cudaError_t launch_scan_fwd_static(const ssm_scan_fwd_params* p, int num_sms, size_t need, cudaStream_t st);
 cudaError_t launch_conv1d_silu_update(const ssm_conv_update_params* p, cudaStream_t st);
+size_t conv_bwd_workspace_bytes(const ssm_conv_bwd_params* p);
+cudaError_t launch_conv1d_silu_bwd(const ssm_conv_bwd_params* p, void* ws, cudaStream_t st);
 cudaError_t launch_decode_step(const ssm_decode_step_params* p, cudaStream_t st);
 cudaError_t launch_state_update(const ssm_state_update_params* p, cudaStream_t st);
 

@@ -30,7 +30,7 @@ def lib():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for must in ("ssm_scan_fwd", "ssm_scan_fwd_workspace_size", "ssm_scan_bwd", "ssm_scan_bwd_workspace_size",
-                 "ssm_state_update", "ssm_decode_step",
+                 "ssm_state_update", "ssm_decode_step", "causal_conv1d_silu_bwd",
                  "causal_conv1d_silu", "causal_conv1d_silu_update", "ssm_status_string",
                  "ssm_last_error", "ssm_abi_version"):
         assert must in names
@@ -57,6 +57,13 @@ def test_host_validation_without_gpu():
     assert lib.ssm_scan_fwd(None, None, 0, None) == -1
     assert lib.ssm_state_update(None, None) == -1
     assert lib.ssm_decode_step(None, None) == -1
+    assert lib.causal_conv1d_silu_bwd(None, None, 0, None) == -1
+    cb = B.ConvBwdParams()
+    cb.batch, cb.dim, cb.seqlen, cb.width = 1, 1, 8, 4
+    assert lib.causal_conv1d_silu_bwd(ctypes.byref(cb), None, 0, None) == -1     # missing pointers
+    cb.x = cb.dout = cb.dx = cb.weight = cb.dweight = 256
+    assert lib.causal_conv1d_silu_bwd_workspace_size(ctypes.byref(cb)) > 0
+    assert lib.causal_conv1d_silu_bwd(ctypes.byref(cb), None, 0, None) == -4     # workspace too small
     assert lib.causal_conv1d_silu(None, None) == -1
     assert lib.causal_conv1d_silu_update(None, None) == -1
     assert b"NULL" in lib.ssm_last_error()
