@@ -47,8 +47,9 @@ DECODE = dict(batch=128, dim=5120, dstate=16, width=4, layers=64, steps=128)
 # capture at batch 8, d_inner 4096, L 2048 (the command is in profiles/).  The
 # figures hold only while the CUDA sources hash to TRAFFIC_SOURCES_SHA; after
 # any kernel change the traffic is reported as null until it is captured again.
-TRAFFIC_PER_CT = {"ssm_scan_bwd": 35.11, "ssm_scan_fwd": 23.15, "causal_conv1d_silu": 3.20}
-TRAFFIC_SOURCES_SHA = "52bd1fc438d3f028"
+TRAFFIC_PER_CT = {"ssm_scan_bwd": 35.13, "ssm_scan_fwd": 23.16, "causal_conv1d_silu": 3.20,
+                  "causal_conv1d_silu_bwd": 5.51}
+TRAFFIC_SOURCES_SHA = "780c03febadef8a9"
 
 SM_FP32_LANES = 128     # FP32 lanes per SM per clock (sm_100 family)
 SM_SFU_EX2 = 32         # MUFU ex2 results per SM per clock on B300 (measured 29.8 at ~2 GHz)
