@@ -101,7 +101,9 @@ typedef struct {
  *                      0).  K = checkpoint_every must be a positive multiple
  *                      of 4 when checkpoints != NULL.
  *                      ssm_scan_bwd can take these instead of recomputing.
- * dstate: 1..16.  dim, batch >= 1; seqlen >= 0 (seqlen 0 only copies h0
+ * dstate: 1..64 (above 16 the state runs as groups of 16 states, one pass
+ * each, the readout summed across them in an fp32 workspace buffer).  dim,
+ * batch >= 1; seqlen >= 0 (seqlen 0 only copies h0
  * to final_state).
  * Workspace: ssm_scan_fwd_workspace_size() bytes (0 for many shapes; the
  * long-sequence schedule stores per-segment carries there).  Pointer

@@ -52,7 +52,7 @@ ssm_status check_fwd(const ssm_scan_fwd_params* p) {
     if (p->batch < 1 || p->dim < 1 || p->seqlen < 0 || p->dstate < 1)
         return fail(SSM_ERR_INVALID_ARG, "bad sizes batch=%lld dim=%lld seqlen=%lld dstate=%lld",
                     (long long)p->batch, (long long)p->dim, (long long)p->seqlen, (long long)p->dstate);
-    if (p->dstate > 16) return fail(SSM_ERR_UNSUPPORTED, "dstate=%lld > 16", (long long)p->dstate);
+    if (p->dstate > 64) return fail(SSM_ERR_UNSUPPORTED, "dstate=%lld > 64", (long long)p->dstate);
     if (p->batch > 65535) return fail(SSM_ERR_UNSUPPORTED, "batch=%lld > 65535", (long long)p->batch);
     if (!dtype_ok(p->in_dtype) || !dtype_ok(p->out_dtype)) return fail(SSM_ERR_INVALID_ARG, "unknown dtype");
     if (p->bbar_mode != SSM_BBAR_ZOH && p->bbar_mode != SSM_BBAR_SIMPLE)
@@ -78,7 +78,7 @@ ssm_status check_bwd(const ssm_scan_bwd_params* p) {
     if (p->batch < 1 || p->dim < 1 || p->seqlen < 0 || p->dstate < 1)
         return fail(SSM_ERR_INVALID_ARG, "bad sizes batch=%lld dim=%lld seqlen=%lld dstate=%lld",
                     (long long)p->batch, (long long)p->dim, (long long)p->seqlen, (long long)p->dstate);
-    if (p->dstate > 16) return fail(SSM_ERR_UNSUPPORTED, "dstate=%lld > 16", (long long)p->dstate);
+    if (p->dstate > 64) return fail(SSM_ERR_UNSUPPORTED, "dstate=%lld > 64", (long long)p->dstate);
     if (p->batch > 65535) return fail(SSM_ERR_UNSUPPORTED, "batch=%lld > 65535", (long long)p->batch);
     if (!dtype_ok(p->in_dtype) || !dtype_ok(p->grad_dtype)) return fail(SSM_ERR_INVALID_ARG, "unknown dtype");
     if (p->bbar_mode != SSM_BBAR_ZOH && p->bbar_mode != SSM_BBAR_SIMPLE)
@@ -248,7 +248,7 @@ ssm_status causal_conv1d_silu_update(const ssm_conv_update_params* p, ssm_stream
 ssm_status ssm_decode_step(const ssm_decode_step_params* p, ssm_stream_t stream) {
     if (p == nullptr) return fail(SSM_ERR_INVALID_ARG, "params is NULL");
     if (p->batch < 1 || p->dim < 1 || p->dstate < 1 || p->width < 1) return fail(SSM_ERR_INVALID_ARG, "bad sizes");
-    if (p->dstate > 16) return fail(SSM_ERR_UNSUPPORTED, "dstate=%lld > 16", (long long)p->dstate);
+    if (p->dstate > 64) return fail(SSM_ERR_UNSUPPORTED, "dstate=%lld > 64", (long long)p->dstate);
     if (p->width > 4) return fail(SSM_ERR_UNSUPPORTED, "width=%lld > 4", (long long)p->width);
     if (p->batch > 65535 || p->dim > (1 << 28))
         return fail(SSM_ERR_UNSUPPORTED, "batch > 65535 or dim > 2^28");
@@ -268,7 +268,7 @@ ssm_status ssm_decode_step(const ssm_decode_step_params* p, ssm_stream_t stream)
 ssm_status ssm_state_update(const ssm_state_update_params* p, ssm_stream_t stream) {
     if (p == nullptr) return fail(SSM_ERR_INVALID_ARG, "params is NULL");
     if (p->batch < 1 || p->dim < 1 || p->dstate < 1) return fail(SSM_ERR_INVALID_ARG, "bad sizes");
-    if (p->dstate > 16) return fail(SSM_ERR_UNSUPPORTED, "dstate=%lld > 16", (long long)p->dstate);
+    if (p->dstate > 64) return fail(SSM_ERR_UNSUPPORTED, "dstate=%lld > 64", (long long)p->dstate);
     if (p->batch > 65535 || p->dim > (1 << 28))
         return fail(SSM_ERR_UNSUPPORTED, "batch > 65535 or dim > 2^28");
     if (!dtype_ok(p->in_dtype) || !dtype_ok(p->out_dtype)) return fail(SSM_ERR_INVALID_ARG, "unknown dtype");

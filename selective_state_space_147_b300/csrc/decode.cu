@@ -28,7 +28,8 @@ struct DecArgs {
 
 template <typename Tin, typename Tout, bool ZOH, bool ACC>
 __global__ void __launch_bounds__(256) state_update_kernel(const DecArgs a) {
-    constexpr int G = 4, NPL = 4;
+    // four lanes per channel; lane g owns states n = g, g + 4, g + 8, ... (up to 64)
+    constexpr int G = 4, NPL = 16;
     const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t chan_raw = gid / G;
     const int g = (int)(gid % G);
@@ -42,22 +43,10 @@ __global__ void __launch_bounds__(256) state_update_kernel(const DecArgs a) {
     const float dl = a.softplus ? (ACC ? softplus_accurate(v) : softplus_fast(v)) : v;
 
     float* st = a.state + chan * a.dstate;
-    const bool full = (a.dstate == 16) && (((uintptr_t)a.state & 15) == 0);
-    float h[NPL];
-    if (full) {
-        const float4 q = *reinterpret_cast<const float4*>(st + g * NPL);
-        h[0] = q.x; h[1] = q.y; h[2] = q.z; h[3] = q.w;
-    } else {
-#pragma unroll
-        for (int j = 0; j < NPL; j++) {
-            const int n = g * NPL + j;
-            h[j] = (n < a.dstate) ? st[n] : 0.f;
-        }
-    }
     float y = 0.f;
 #pragma unroll
     for (int j = 0; j < NPL; j++) {
-        const int n = g * NPL + j;
+        const int n = g + G * j;
         if (n < a.dstate) {
             const float Av = __ldg(a.A + d * a.dstate + n);
             const float Bv = Elem<Tin>::load(reinterpret_cast<const Tin*>(a.B) + b * a.sB + n);
@@ -71,22 +60,14 @@ __global__ void __launch_bounds__(256) state_update_kernel(const DecArgs a) {
                 ab = ex2_approx(x * kLog2e);
                 coef = ZOH ? (Av != 0.f ? (ab - 1.f) * rcp_approx(Av) : dl) : dl;
             }
-            h[j] = fmaf(ab, h[j], coef * Bv * xt);
-            y = fmaf(Cv, h[j], y);
+            const float h = fmaf(ab, st[n], coef * Bv * xt);
+            if (active) st[n] = h;
+            y = fmaf(Cv, h, y);
         }
     }
     y += __shfl_xor_sync(0xffffffffu, y, 1);
     y += __shfl_xor_sync(0xffffffffu, y, 2);
     if (!active) return;
-    if (full) {
-        *reinterpret_cast<float4*>(st + g * NPL) = make_float4(h[0], h[1], h[2], h[3]);
-    } else {
-#pragma unroll
-        for (int j = 0; j < NPL; j++) {
-            const int n = g * NPL + j;
-            if (n < a.dstate) st[n] = h[j];
-        }
-    }
     if (g == 0) {
         y = fmaf(a.D ? __ldg(a.D + d) : 0.f, xt, y);
         if (a.z != nullptr) {

@@ -50,13 +50,49 @@ struct BwdArgs {
     float* part_D;              // (batch, dim)
     float* part_bias;           // (batch, dim)
     int nblk;
+    // one group of at most 16 states of a larger state: row strides of A and of
+    // the states (dfinal, dh0), checkpoint pairs in total and the group's first
+    int64_t sA, sst, ck_P, ck_p0;
+    int64_t sBo;                // rows per batch of dB, dC (the full state size)
+    // du, ddelta, dz summed across state groups in fp32 (NULL with one group)
+    float* gacc;                // 3 x (batch * dim * seqlen)
+    int g_first, g_last;
 };
+
+// With more than 16 states the backward runs once per group of 16; du, ddelta
+// and dz are sums over all states, so each group adds its part to fp32 buffers
+// (the first writes them) and the last one stores the gradients.  Returns true
+// when this call must store.
+template <int NV>
+__device__ __forceinline__ bool accumulate_grads(const BwdArgs& a, int64_t chan, int64_t t0, int cnt,
+                                                 float (&du)[NV], float (&dd)[NV], float (&dz)[NV], bool has_z) {
+    if (a.gacc == nullptr) return true;
+    const int64_t CL = a.batch * a.dim * a.seqlen;
+    float* pu = a.gacc + chan * a.seqlen + t0;
+    float* pd = pu + CL;
+    float* pz = pd + CL;
+#pragma unroll
+    for (int j = 0; j < NV; j++) {
+        if (j < cnt) {
+            if (!a.g_first) {
+                du[j] += pu[j];
+                dd[j] += pd[j];
+                if (has_z) dz[j] += pz[j];
+            }
+            if (!a.g_last) {
+                pu[j] = du[j];
+                pd[j] = dd[j];
+                if (has_z) pz[j] = dz[j];
+            }
+        }
+    }
+    return a.g_last != 0;
+}
 
 // Checkpoint k of channel (b, d), state pair `pair`: the forward's layout
 // (batch, n_ckpt, ceil(dstate/2), dim, 2), the pairs of neighbouring channels adjacent.
 __device__ __forceinline__ const float* ckpt_at(const BwdArgs& a, int64_t b, int64_t k, int64_t d, int pair) {
-    const int64_t P = (a.dstate + 1) >> 1;
-    return a.ckpt + (((b * a.n_ckpt + k) * P + pair) * a.dim + d) * 2;
+    return a.ckpt + (((b * a.n_ckpt + k) * a.ck_P + a.ck_p0 + pair) * a.dim + d) * 2;
 }
 
 // B[b, :, t0 : t0+64] and C[...] as fp32 rows [t][B0..15 C0..15 pad] for the
@@ -94,21 +130,21 @@ __device__ __forceinline__ void bwd_channel(const BwdArgs& a, float* sbc, float*
     const int lane = tid & 31, warp = tid >> 5;
     float An[16];
 #pragma unroll
-    for (int n = 0; n < 16; n++) An[n] = (n < a.dstate) ? __ldg(a.A + d * a.dstate + n) : 0.f;
+    for (int n = 0; n < 16; n++) An[n] = (n < a.dstate) ? __ldg(a.A + d * a.sA + n) : 0.f;
     // 1/A at each use (SFU reciprocal on the fast path) instead of 16 more live registers;
     // A == 0 never reaches the fast path (the flag routes it to the accurate kernel)
     auto invA = [&](int n) -> float {
         if constexpr (ACC) return (An[n] != 0.f) ? 1.f / An[n] : 0.f;
         else return rcp_approx(An[n]);
     };
-    const float Dd = a.D ? __ldg(a.D + d) : 0.f;
+    const float Dd = (a.D && a.g_first) ? __ldg(a.D + d) : 0.f;   // the D skip enters once
     const float bias = a.bias ? __ldg(a.bias + d) : 0.f;
     // Idle lanes (d past dim) shadow the last channel to keep the warp uniform;
     // a zero upstream gradient makes every partial they add to dB, dC zero.
     float Gc[16], dAacc[16];
 #pragma unroll
     for (int n = 0; n < 16; n++) {
-        Gc[n] = (active && a.dhN != nullptr && n < a.dstate) ? __ldg(a.dhN + chan * a.dstate + n) : 0.f;
+        Gc[n] = (active && a.dhN != nullptr && n < a.dstate) ? __ldg(a.dhN + chan * a.sst + n) : 0.f;
         dAacc[n] = 0.f;
     }
     float dDacc = 0.f, dbacc = 0.f;
@@ -267,7 +303,7 @@ __device__ __forceinline__ void bwd_channel(const BwdArgs& a, float* sbc, float*
             duo[j] = du;
             ddo[j] = dv;
         }
-        if (active) {
+        if (active && accumulate_grads<kSub>(a, chan, t0, cnt, duo, ddo, dzo, HAS_Z)) {
             store8<Tg>(durow + t0, cnt, a.vec_du, duo);
             store8<Tg>(ddrow + t0, cnt, a.vec_ddt, ddo);
             if constexpr (HAS_Z) store8<Tg>(dzrow + t0, cnt, a.vec_dz, dzo);
@@ -288,7 +324,7 @@ __device__ __forceinline__ void bwd_channel(const BwdArgs& a, float* sbc, float*
     if (!active) return;
 #pragma unroll
     for (int n = 0; n < 16; n++) {
-        if (a.dh0 != nullptr && n < a.dstate) a.dh0[chan * a.dstate + n] = Gc[n];
+        if (a.dh0 != nullptr && n < a.dstate) a.dh0[chan * a.sst + n] = Gc[n];
         a.part_A[chan * 16 + n] = dAacc[n];
     }
     a.part_D[chan] = dDacc;
@@ -405,9 +441,9 @@ scan_bwd_fast_kernel(const BwdArgs a, const int* flag) {
         for (int q = 0; q < 2; q++) {
             const int n = 2 * p + q;
             const bool on = n < a.dstate;
-            av[q] = on ? __ldg(a.A + d * a.dstate + n) : -1.f;
+            av[q] = on ? __ldg(a.A + d * a.sA + n) : -1.f;
             ia[q] = ZOH ? rcp_approx(av[q]) : 0.f;   // A != 0 here
-            gv[q] = (active && on && a.dhN != nullptr) ? __ldg(a.dhN + chan * a.dstate + n) : 0.f;
+            gv[q] = (active && on && a.dhN != nullptr) ? __ldg(a.dhN + chan * a.sst + n) : 0.f;
         }
         cst[p * 32 + lane] = make_ulonglong2(pf2_make(av[0], av[1]), pf2_make(ia[0], ia[1]));
         Gc[p] = pf2_make(gv[0], gv[1]);
@@ -415,7 +451,7 @@ scan_bwd_fast_kernel(const BwdArgs a, const int* flag) {
         dA2[p] = 0ull;
     }
     const pf2 LOG2E2 = pf2_make(kLog2e, kLog2e);
-    const float Dd = a.D ? __ldg(a.D + d) : 0.f;
+    const float Dd = (a.D && a.g_first) ? __ldg(a.D + d) : 0.f;   // the D skip enters once
     const float bias = a.bias ? __ldg(a.bias + d) : 0.f;
     float dDacc = 0.f, dbacc = 0.f;
     const Tin* urow = reinterpret_cast<const Tin*>(a.u) + b * a.su_b + d * a.su_d;
@@ -639,7 +675,7 @@ scan_bwd_fast_kernel(const BwdArgs a, const int* flag) {
                 dzo[j] = go * fmaf(Dd, uj[j], pf2_sum(yv2[j])) * sgz * fmaf(zj, 1.f - sgz, 1.f);
             }
         }
-        if (active) {
+        if (active && accumulate_grads<kFSub>(a, chan, t0, cnt, duo, ddo, dzo, HAS_Z)) {
             store4<Tg>(reinterpret_cast<Tg*>(a.du) + b * a.sdu_b + d * a.sdu_d + t0, cnt, a.vec_du, duo);
             store4<Tg>(reinterpret_cast<Tg*>(a.ddt) + b * a.sddt_b + d * a.sddt_d + t0, cnt, a.vec_ddt, ddo);
             if constexpr (HAS_Z)
@@ -669,8 +705,8 @@ scan_bwd_fast_kernel(const BwdArgs a, const int* flag) {
         if constexpr (ZOH) dA = pf2_fma(dA2[p], cst[p * 32 + lane].y, dA);
         const int n = 2 * p;
         if (a.dh0 != nullptr) {
-            if (n < a.dstate) a.dh0[chan * a.dstate + n] = pf2_lo(Gc[p]);
-            if (n + 1 < a.dstate) a.dh0[chan * a.dstate + n + 1] = pf2_hi(Gc[p]);
+            if (n < a.dstate) a.dh0[chan * a.sst + n] = pf2_lo(Gc[p]);
+            if (n + 1 < a.dstate) a.dh0[chan * a.sst + n + 1] = pf2_hi(Gc[p]);
         }
         a.part_A[chan * 16 + n] = pf2_lo(dA);
         a.part_A[chan * 16 + n + 1] = pf2_hi(dA);
@@ -727,7 +763,7 @@ __global__ void bwd_reduce_bc_kernel(const BwdArgs a, float* dB, float* dC) {
     float s = 0.f;
     for (int k = 0; k < a.nblk; k++) s += a.part_bc[(((b * a.nblk + k) * 2 + tsr) * 16 + n) * a.seqlen + t];
     float* out = tsr == 0 ? dB : dC;
-    if (out) out[(b * a.dstate + n) * a.seqlen + t] = s;
+    if (out) out[(b * a.sBo + n) * a.seqlen + t] = s;
 }
 
 // dA[d, n], dD[d], dbias[d]: sums over the batch, in batch order.
@@ -740,13 +776,13 @@ __global__ void bwd_reduce_params_kernel(const BwdArgs a, float* dA, float* dD, 
     if (k < 16) {
         if (k >= a.dstate) return;
         for (int64_t b = 0; b < a.batch; b++) s += a.part_A[(b * a.dim + d) * 16 + k];
-        if (dA) dA[d * a.dstate + k] = s;
+        if (dA) dA[d * a.sA + k] = s;
     } else if (k == 16) {
         for (int64_t b = 0; b < a.batch; b++) s += a.part_D[b * a.dim + d];
-        if (dD) dD[d] = s;
+        if (dD && a.g_first) dD[d] = s;                   // the same in every state group
     } else {
         for (int64_t b = 0; b < a.batch; b++) s += a.part_bias[b * a.dim + d];
-        if (dbias) dbias[d] = s;
+        if (dbias) dbias[d] = a.g_first ? s : dbias[d] + s;   // summed across state groups
     }
 }
 
@@ -754,7 +790,7 @@ __global__ void bwd_reduce_params_kernel(const BwdArgs a, float* dA, float* dD, 
 // Host side
 
 struct BwdLayout {
-    size_t ckpt, fwd_ws, part_bc, part_A, part_D, total;
+    size_t ckpt, fwd_ws, part_bc, part_A, part_D, gacc, total;
     bool own_ckpt;
 };
 
@@ -783,7 +819,8 @@ static BwdLayout bwd_layout(const ssm_scan_bwd_params* p, int num_sms) {
     const int64_t chans = p->batch * p->dim;
     const int64_t nck = ceil_div(p->seqlen, (int64_t)kBwdK);
     l.own_ckpt = !(p->checkpoints != nullptr && p->checkpoint_every == kBwdK);
-    l.ckpt = l.own_ckpt ? round256((size_t)(chans * nck * p->dstate) * 4) : 0;
+    // checkpoint pairs: ceil(dstate / 2) of them, two floats each
+    l.ckpt = l.own_ckpt ? round256((size_t)(chans * nck * 2 * ((p->dstate + 1) / 2)) * 4) : 0;
     if (l.own_ckpt) {
         ssm_scan_fwd_params f = ckpt_fwd_params(p);
         f.checkpoints = reinterpret_cast<float*>(16);   // only sizes matter here
@@ -793,7 +830,8 @@ static BwdLayout bwd_layout(const ssm_scan_bwd_params* p, int num_sms) {
     l.part_bc = round256((size_t)(p->batch * nblk * 2 * 16 * p->seqlen) * 4);
     l.part_A = round256((size_t)(chans * 16) * 4);
     l.part_D = round256((size_t)chans * 4);
-    l.total = l.ckpt + l.fwd_ws + l.part_bc + l.part_A + 2 * l.part_D + 256;   // + the A == 0 flag
+    l.gacc = p->dstate > 16 ? round256((size_t)(3 * chans * p->seqlen) * 4) : 0;   // cross-group sums
+    l.total = l.ckpt + l.fwd_ws + l.part_bc + l.part_A + 2 * l.part_D + 256 + l.gacc;   // + the A == 0 flag
     return l;
 }
 
@@ -905,19 +943,41 @@ cudaError_t launch_scan_bwd(const ssm_scan_bwd_params* p, void* ws, int num_sms,
         bwd_check_A_kernel<<<(unsigned)(ceil_div(nA, 256) < 1024 ? ceil_div(nA, 256) : 1024), 256, 0, st>>>(p->A, nA, flag);
         count_launches(1);
     }
-    if (p->in_dtype == SSM_BF16) {
-        e = p->grad_dtype == SSM_BF16 ? launch_bwd_typed<__nv_bfloat16, __nv_bfloat16>(a, zoh, has_z, flag, st)
-                                      : launch_bwd_typed<__nv_bfloat16, float>(a, zoh, has_z, flag, st);
-    } else {
-        e = p->grad_dtype == SSM_BF16 ? launch_bwd_typed<float, __nv_bfloat16>(a, zoh, has_z, flag, st)
-                                      : launch_bwd_typed<float, float>(a, zoh, has_z, flag, st);
+    a.sA = p->dstate; a.sst = p->dstate; a.sBo = p->dstate;
+    a.ck_P = (p->dstate + 1) / 2; a.ck_p0 = 0;
+    a.gacc = l.gacc ? reinterpret_cast<float*>(wp + l.part_bc + l.part_A + 2 * l.part_D + 256) : nullptr;
+    // one pass per group of at most 16 states (a single pass for d_state <= 16)
+    const int ngroups = (int)ceil_div(p->dstate, (int64_t)16);
+    for (int gi = 0; gi < ngroups; gi++) {
+        BwdArgs ga = a;
+        const int n0 = gi * 16;
+        ga.dstate = (int)((p->dstate - n0) < 16 ? (p->dstate - n0) : 16);
+        ga.A = p->A + n0;
+        ga.B = static_cast<const char*>(p->B) + (int64_t)n0 * a.sB_n * isz;
+        ga.C = static_cast<const char*>(p->C) + (int64_t)n0 * a.sC_n * isz;
+        ga.dhN = p->dfinal_state ? p->dfinal_state + n0 : nullptr;
+        ga.dh0 = p->dh0 ? p->dh0 + n0 : nullptr;
+        ga.ck_p0 = n0 / 2;
+        ga.g_first = gi == 0;
+        ga.g_last = gi == ngroups - 1;
+        if (p->in_dtype == SSM_BF16) {
+            e = p->grad_dtype == SSM_BF16 ? launch_bwd_typed<__nv_bfloat16, __nv_bfloat16>(ga, zoh, has_z, flag, st)
+                                          : launch_bwd_typed<__nv_bfloat16, float>(ga, zoh, has_z, flag, st);
+        } else {
+            e = p->grad_dtype == SSM_BF16 ? launch_bwd_typed<float, __nv_bfloat16>(ga, zoh, has_z, flag, st)
+                                          : launch_bwd_typed<float, float>(ga, zoh, has_z, flag, st);
+        }
+        if (e != cudaSuccess) return e;
+        const dim3 g2((unsigned)ceil_div(p->seqlen, 256), (unsigned)ga.dstate, (unsigned)(2 * p->batch));
+        bwd_reduce_bc_kernel<<<g2, 256, 0, st>>>(ga, p->dB ? p->dB + (int64_t)n0 * p->seqlen : nullptr,
+                                                 p->dC ? p->dC + (int64_t)n0 * p->seqlen : nullptr);
+        bwd_reduce_params_kernel<<<(unsigned)ceil_div(p->dim * 18, 256), 256, 0, st>>>(
+            ga, p->dA ? p->dA + n0 : nullptr, p->dD, p->ddelta_bias);
+        count_launches(2);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
     }
-    if (e != cudaSuccess) return e;
-    const dim3 g2((unsigned)ceil_div(p->seqlen, 256), (unsigned)p->dstate, (unsigned)(2 * p->batch));
-    bwd_reduce_bc_kernel<<<g2, 256, 0, st>>>(a, p->dB, p->dC);
-    bwd_reduce_params_kernel<<<(unsigned)ceil_div(p->dim * 18, 256), 256, 0, st>>>(a, p->dA, p->dD, p->ddelta_bias);
-    count_launches(2);
-    return cudaGetLastError();
+    return cudaSuccess;
 }
 
 }  // namespace ssm

@@ -87,13 +87,22 @@ static FwdPlan plan_fwd(const ssm_scan_fwd_params* p, int num_sms) {
     return pl;
 }
 
+// Workspace: the segmented schedule's carries, then (more than 16 states) the
+// fp32 readout sum shared by the state groups.
+static size_t seg_ws_bytes(const ssm_scan_fwd_params* p, const FwdPlan& pl) {
+    if (pl.nseg <= 1) return 0;
+    const int64_t floats = p->batch * p->dim * pl.nseg * (2 * kNMax + 1);
+    return (size_t)(ceil_div(floats * 4, 256) * 256);
+}
+static size_t yacc_bytes(const ssm_scan_fwd_params* p) {
+    if (p->dstate <= kNMax || p->out == nullptr) return 0;
+    return (size_t)(ceil_div(p->batch * p->dim * p->seqlen * 4, 256) * 256);
+}
+
 size_t fwd_workspace_bytes(const ssm_scan_fwd_params* p, int num_sms) {
     if (p->seqlen == 0) return 0;
     const FwdPlan pl = plan_fwd(p, num_sms);
-    if (pl.nseg <= 1) return 0;
-    const int64_t chans = p->batch * p->dim;
-    const int64_t floats = chans * pl.nseg * (2 * kNMax + 1);
-    return (size_t)(ceil_div(floats * 4, 256) * 256);
+    return seg_ws_bytes(p, pl) + yacc_bytes(p);
 }
 
 
@@ -141,20 +150,47 @@ cudaError_t launch_scan_fwd(const ssm_scan_fwd_params* p, void* ws, int num_sms,
     }
     const bool zoh = p->bbar_mode == SSM_BBAR_ZOH;
     const bool has_z = p->z != nullptr;
-    if (p->in_dtype == SSM_BF16) {
-        // the cp.async pipeline needs every u/delta/z/B/C row 16-byte aligned
-        const bool bc16 = ((uintptr_t)p->B % 16 == 0) && ((uintptr_t)p->C % 16 == 0) &&
-                          (a.sB_b % 8 == 0) && (a.sB_n % 8 == 0) && (a.sC_b % 8 == 0) && (a.sC_n % 8 == 0);
-        const bool async = a.vec_u && a.vec_dt && (!has_z || a.vec_z) && bc16 && env_int("SSM_FWD_NOASYNC", 0) == 0;
-        if (async) {
-            if (p->out_dtype == SSM_BF16) return dispatch_G<__nv_bfloat16, __nv_bfloat16, true>(a, pl.G, zoh, has_z, st);
-            return dispatch_G<__nv_bfloat16, float, true>(a, pl.G, zoh, has_z, st);
+    auto run = [&](const FwdArgs& ga) -> cudaError_t {
+        if (p->in_dtype == SSM_BF16) {
+            // the cp.async pipeline needs every u/delta/z/B/C row 16-byte aligned
+            const bool bc16 = ((uintptr_t)ga.B % 16 == 0) && ((uintptr_t)ga.C % 16 == 0) &&
+                              (ga.sB_b % 8 == 0) && (ga.sB_n % 8 == 0) && (ga.sC_b % 8 == 0) && (ga.sC_n % 8 == 0);
+            const bool async = ga.vec_u && ga.vec_dt && (!has_z || ga.vec_z) && bc16 && env_int("SSM_FWD_NOASYNC", 0) == 0;
+            if (async) {
+                if (p->out_dtype == SSM_BF16) return dispatch_G<__nv_bfloat16, __nv_bfloat16, true>(ga, pl.G, zoh, has_z, st);
+                return dispatch_G<__nv_bfloat16, float, true>(ga, pl.G, zoh, has_z, st);
+            }
+            if (p->out_dtype == SSM_BF16) return dispatch_G<__nv_bfloat16, __nv_bfloat16, false>(ga, pl.G, zoh, has_z, st);
+            return dispatch_G<__nv_bfloat16, float, false>(ga, pl.G, zoh, has_z, st);
         }
-        if (p->out_dtype == SSM_BF16) return dispatch_G<__nv_bfloat16, __nv_bfloat16, false>(a, pl.G, zoh, has_z, st);
-        return dispatch_G<__nv_bfloat16, float, false>(a, pl.G, zoh, has_z, st);
+        if (p->out_dtype == SSM_BF16) return dispatch_G<float, __nv_bfloat16, false>(ga, pl.G, zoh, has_z, st);
+        return dispatch_G<float, float, false>(ga, pl.G, zoh, has_z, st);
+    };
+    a.sA = p->dstate; a.sst = p->dstate;
+    a.ck_P = (p->dstate + 1) / 2; a.ck_p0 = 0;
+    a.yacc = nullptr; a.y_first = a.y_last = 1;
+    if (p->dstate <= kNMax) return run(a);
+    // more than 16 states: one pass per group of 16, the readout summed across them
+    const int ngroups = (int)ceil_div(p->dstate, (int64_t)kNMax);
+    a.yacc = p->out != nullptr ? reinterpret_cast<float*>(static_cast<char*>(ws) + seg_ws_bytes(p, pl)) : nullptr;
+    for (int gi = 0; gi < ngroups; gi++) {
+        FwdArgs ga = a;
+        const int n0 = gi * kNMax;
+        ga.dstate = (int)((p->dstate - n0) < kNMax ? (p->dstate - n0) : kNMax);
+        ga.A = p->A + n0;
+        ga.B = static_cast<const char*>(p->B) + (int64_t)n0 * a.sB_n * isz;
+        ga.C = static_cast<const char*>(p->C) + (int64_t)n0 * a.sC_n * isz;
+        ga.h0 = p->h0 ? p->h0 + n0 : nullptr;
+        ga.final_state = p->final_state ? p->final_state + n0 : nullptr;
+        ga.ck_p0 = n0 / 2;
+        ga.y_first = gi == 0;
+        ga.y_last = gi == ngroups - 1;
+        ga.vec_BC = ((uintptr_t)ga.B % (2 * isz) == 0) && ((uintptr_t)ga.C % (2 * isz) == 0) &&
+                    (a.sB_b % 2 == 0) && (a.sB_n % 2 == 0) && (a.sC_b % 2 == 0) && (a.sC_n % 2 == 0);
+        cudaError_t e = run(ga);
+        if (e != cudaSuccess) return e;
     }
-    if (p->out_dtype == SSM_BF16) return dispatch_G<float, __nv_bfloat16, false>(a, pl.G, zoh, has_z, st);
-    return dispatch_G<float, float, false>(a, pl.G, zoh, has_z, st);
+    return cudaSuccess;
 }
 
 }  // namespace ssm

@@ -28,6 +28,13 @@ struct FwdArgs {
     float* ws_hend;    // (channels, nseg, 16)
     float* ws_sdelta;  // (channels, nseg)
     float* ws_carry;   // (channels, nseg, 16)
+    // one group of at most 16 states of a larger state: row strides of A and of
+    // the (h0, final) states, checkpoint pairs in total and the group's first one
+    int64_t sA, sst;
+    int64_t ck_P, ck_p0;
+    // readout sum across state groups (NULL with a single group)
+    float* yacc;       // (channels, seqlen) fp32
+    int y_first, y_last;
 };
 
 template <typename Tin, typename Tout, bool ASYNC>

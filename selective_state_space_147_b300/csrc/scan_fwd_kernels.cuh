@@ -102,7 +102,7 @@ __device__ __forceinline__ void load_A(const FwdArgs& a, int64_t d, int n_base, 
 #pragma unroll
     for (int j = 0; j < NPL; j++) {
         const int n = n_base + j;
-        const float Av = (n < a.dstate) ? __ldg(a.A + d * a.dstate + n) : 0.f;
+        const float Av = (n < a.dstate) ? __ldg(a.A + d * a.sA + n) : 0.f;
         if constexpr (ACC) {
             Ak[j] = Av;
             Ik[j] = (Av != 0.f) ? 1.f / Av : 0.f;
@@ -297,8 +297,7 @@ __device__ __forceinline__ void scan_block8(pf2 (&h2)[NP], const pf2 (&A2)[NP], 
 // (and the backward's loads) coalesce.  Pointer to pair `pair` of checkpoint k
 // of channel (b, d):
 __device__ __forceinline__ float* ckpt_pair(const FwdArgs& a, int64_t b, int64_t k, int64_t d, int pair) {
-    const int64_t P = (a.dstate + 1) >> 1;
-    return a.ckpt + (((b * a.n_ckpt + k) * P + pair) * a.dim + d) * 2;
+    return a.ckpt + (((b * a.n_ckpt + k) * a.ck_P + a.ck_p0 + pair) * a.dim + d) * 2;
 }
 
 // Store this lane's NPL checkpoint values (states n_base ..) of checkpoint k;
@@ -324,6 +323,21 @@ __device__ __forceinline__ float finish_y(float y, float Dd, float uj, float zj)
     y = fmaf(Dd, uj, y);
     if constexpr (HAS_Z) y *= ACC ? silu_accurate(zj) : silu_fast(zj);
     return y;
+}
+
+// With more than 16 states the forward runs once per group of 16 and the
+// readout sum over states crosses the groups: each group adds its C.h to an fp32
+// buffer (the first one writes it), and the last group finishes the output.
+// Returns true when this call must write the output.
+__device__ __forceinline__ bool accumulate_readout(const FwdArgs& a, int64_t chan, int64_t t, float& y) {
+    if (a.yacc == nullptr) return true;
+    float* ya = a.yacc + chan * a.seqlen + t;
+    if (!a.y_first) y += *ya;
+    if (!a.y_last) {
+        *ya = y;
+        return false;
+    }
+    return true;
 }
 
 // ---------------------------------------------------------------------------
@@ -395,11 +409,19 @@ __device__ __forceinline__ void scan_warp(const FwdArgs& a, float* sbc_all, int6
                     sd_c = (tk - sd) - yk;
                     sd = tk;
                 } else {
-                    yout[j] = finish_y<G, ACC, HAS_Z>(y, Dd, uj, HAS_Z ? rz[0].get(j) : 0.f);
+                    // reduce over the channel's lanes first, then across state groups
+#pragma unroll
+                    for (int o = 1; o < G; o <<= 1) y += __shfl_xor_sync(0xffffffffu, y, o);
+                    if (a.yacc != nullptr) {
+                        if (active && g == 0 && j < cnt) accumulate_readout(a, b * a.dim + d, t0 + j, y);
+                        if (!a.y_last) continue;
+                    }
+                    yout[j] = finish_y<1, ACC, HAS_Z>(y, Dd, uj, HAS_Z ? rz[0].get(j) : 0.f);
                 }
             }
             if constexpr (MODE == kFull) {
-                if (active && g == 0 && orow != nullptr) store8<Tout>(orow + t0, cnt, a.vec_out, yout);
+                if (active && g == 0 && orow != nullptr && (a.yacc == nullptr || a.y_last))
+                    store8<Tout>(orow + t0, cnt, a.vec_out, yout);
             }
             ru[0] = ru[1]; rd[0] = rd[1]; ru[1] = ru[2]; rd[1] = rd[2];
             if constexpr (HAS_Z && MODE == kFull) { rz[0] = rz[1]; rz[1] = rz[2]; }
@@ -677,13 +699,16 @@ __device__ __forceinline__ void scan_cta_async(const FwdArgs& a, unsigned char* 
 #pragma unroll
                     for (int q = 1; q < G; q++)
                         if (g == q) yj = yp[q * SPL + i];
+                    if (a.yacc != nullptr && active && jb + i < cnt)
+                        accumulate_readout(a, b * a.dim + d, t0 + jb + i, yj);
                     const float uj = (G == 1) ? u8[i] : own_bf16<G>(wu, g, i);
                     yj = fmaf(Dd, uj, yj);
                     if constexpr (HAS_Z) yj *= silu_fast(own_bf16<G>(wz, g, i));
                     yo[i] = yj;
                 }
                 const int lim = cnt - jb;
-                if (active && lim > 0 && orow != nullptr) storeN<Tout, SPL>(orow + t0 + jb, lim, a.vec_out, yo);
+                if (active && lim > 0 && orow != nullptr && (a.yacc == nullptr || a.y_last))
+                    storeN<Tout, SPL>(orow + t0 + jb, lim, a.vec_out, yo);
             }
         }
         __syncthreads();   // everyone is done with this stage and with bcf
@@ -735,7 +760,7 @@ scan_fwd_kernel(const FwdArgs a) {
         const int n = g * NPL + j;
         float v = 0.f;
         if (MODE == kFull && n < a.dstate) {
-            if (seg == 0) { if (a.h0 != nullptr) v = __ldg(a.h0 + chan * a.dstate + n); }
+            if (seg == 0) { if (a.h0 != nullptr) v = __ldg(a.h0 + chan * a.sst + n); }
             else v = a.ws_carry[(chan * a.nseg + seg) * kNMax + n];
         }
         h[j] = v;
@@ -747,7 +772,7 @@ scan_fwd_kernel(const FwdArgs a) {
         bool zero = false;
         for (int j = 0; j < NPL; j++) {
             const int n = g * NPL + j;
-            if (n < a.dstate && __ldg(a.A + d * a.dstate + n) == 0.f) zero = true;
+            if (n < a.dstate && __ldg(a.A + d * a.sA + n) == 0.f) zero = true;
         }
         if constexpr (kAsync) acc = acc || __syncthreads_or(zero);
         else acc = acc || __any_sync(0xffffffffu, zero);
@@ -775,7 +800,7 @@ scan_fwd_kernel(const FwdArgs a) {
 #pragma unroll
                 for (int j = 0; j < NPL; j++) {
                     const int n = g * NPL + j;
-                    if (n < a.dstate) a.final_state[chan * a.dstate + n] = h[j];
+                    if (n < a.dstate) a.final_state[chan * a.sst + n] = h[j];
                 }
         }
     }
@@ -790,8 +815,8 @@ static __global__ void scan_carry_kernel(const FwdArgs a) {
     const int64_t chan = idx / kNMax;
     const int n = (int)(idx % kNMax);
     const int64_t d = chan % a.dim;
-    const float Av = (n < a.dstate) ? a.A[d * a.dstate + n] : 0.f;
-    float c = (a.h0 != nullptr && n < a.dstate) ? a.h0[chan * a.dstate + n] : 0.f;
+    const float Av = (n < a.dstate) ? a.A[d * a.sA + n] : 0.f;
+    float c = (a.h0 != nullptr && n < a.dstate) ? a.h0[chan * a.sst + n] : 0.f;
     for (int s = 0; s < a.nseg; s++) {
         a.ws_carry[(chan * a.nseg + s) * kNMax + n] = c;
         if (s + 1 < a.nseg) {

@@ -69,8 +69,8 @@ def test_host_validation_without_gpu():
     assert b"NULL" in lib.ssm_last_error()
     # sizes
     p = B.ScanFwdParams()
-    p.batch, p.dim, p.seqlen, p.dstate = 1, 1, 8, 17
-    assert lib.ssm_scan_fwd(ctypes.byref(p), None, 0, None) == -2      # dstate > 16
+    p.batch, p.dim, p.seqlen, p.dstate = 1, 1, 8, 65
+    assert lib.ssm_scan_fwd(ctypes.byref(p), None, 0, None) == -2      # dstate > 64
     p.dstate = 0
     assert lib.ssm_scan_fwd(ctypes.byref(p), None, 0, None) == -1
     p.dstate = 16

@@ -79,7 +79,7 @@ def _decode_inputs(seed, batch, dim, N, dtype):
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("zoh", [True, False])
-@pytest.mark.parametrize("N", [16, 5])
+@pytest.mark.parametrize("N", [16, 5, 40, 64])
 def test_state_update(dtype, zoh, N):
     g = _decode_inputs(41, 3, 70, N, dtype)
     L = _lib()

@@ -73,7 +73,7 @@ def test_fast_path(zoh, dim):
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
-@pytest.mark.parametrize("N,W", [(5, 3), (16, 2), (1, 1), (16, 4)])
+@pytest.mark.parametrize("N,W", [(5, 3), (16, 2), (1, 1), (16, 4), (33, 4), (64, 2)])
 def test_general_path(dtype, N, W):
     g = _inputs(62, 2, 37, N, W, dtype)
     got, ref = _run(g, strided=True)

@@ -77,9 +77,16 @@ def test_lengths(L):
     run_and_check(make(53, 2, 33, L, 16, torch.float32), torch.float32)
 
 
-@pytest.mark.parametrize("N", [1, 5, 16])
+@pytest.mark.parametrize("N", [1, 5, 16, 20, 33, 64])
 def test_state_sizes(N):
     run_and_check(make(54, 1, 64, 90, N, torch.float32), torch.float32)
+
+
+@pytest.mark.parametrize("zoh", [True, False])
+@pytest.mark.parametrize("N", [17, 32, 48])
+def test_large_state_bf16(zoh, N):
+    """More than 16 states run as groups of 16: every gradient, the fast kernel."""
+    run_and_check(make(55, 2, 96, 333, N, torch.bfloat16), torch.bfloat16, zoh=zoh)
 
 
 def test_optional_inputs_off():

@@ -82,13 +82,35 @@ def test_schedules_and_modes(schedule, zoh, dtype, G, nseg):
     assert_close(hN, href, dtype, what="final_state")
 
 
-@pytest.mark.parametrize("N", [1, 3, 4, 8, 13, 16])
+@pytest.mark.parametrize("N", [1, 3, 4, 8, 13, 16, 17, 24, 32, 33, 48, 64])
 def test_state_sizes(N):
     g = make(8, 1, 40, 300, N, torch.bfloat16)
     out, hN = run_gpu(g, final=True)
     ref, href = run_oracle(g)
     assert_close(out, ref, torch.bfloat16, what="out")
     assert_close(hN, href, torch.bfloat16, what="final_state")
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("zoh", [True, False])
+def test_large_state_with_checkpoints_and_segments(dtype, zoh, schedule):
+    """d_state 40 (three state groups): outputs, final state and every checkpoint,
+    also under the segmented schedule."""
+    schedule(None, 3)
+    N, L, K = 40, 600, 8
+    g = make(16, 2, 36, L, N, dtype, with_h0=True)
+    lib = _lib()
+    ck = lib.checkpoint_buffer(2, 36, L, N, every=K).fill_(float("nan"))
+    out, hN = run_gpu(g, final=True, checkpoints=ck, checkpoint_every=K, zoh=zoh)
+    ref, href = run_oracle(g, zoh=zoh)
+    assert_close(out, ref, dtype, what="out")
+    assert_close(hN, href, dtype, what="final_state")
+    cs = lib.checkpoint_states(ck, N)
+    for k in (1, 37, (L - 1) // K):
+        _, hk = oracle.scan_fwd(g["u"][..., :k * K], g["dt"][..., :k * K], g["A"], g["B"][..., :k * K],
+                                g["C"][..., :k * K], g["D"], g["bias"], g["z"][..., :k * K], g["h0"], zoh=zoh,
+                                threads=THREADS)
+        assert_close(cs[:, k], hk, dtype, what=f"checkpoint {k}")
 
 
 @pytest.mark.parametrize("L", [1, 3, 7, 8, 9, 63, 64, 65, 129])
