@@ -130,6 +130,12 @@ typedef struct {
     float* final_state;
     float* checkpoints;
     int64_t checkpoint_every;
+    /* B/C groups: channel d reads B, C of group d / (dim / ngroups); B is then
+     * (batch, ngroups, dstate, L) with group stride B_group_stride elements
+     * (C likewise).  0 or 1 = one group shared by all channels.  With more than
+     * one group, dim / ngroups must be a multiple of 128. */
+    int64_t ngroups;
+    int64_t B_group_stride, C_group_stride;
 } ssm_scan_fwd_params;
 
 SSM_API size_t ssm_scan_fwd_workspace_size(const ssm_scan_fwd_params* p);
@@ -209,6 +215,13 @@ typedef struct {
     float* dD;
     float* ddelta_bias;
     float* dh0;
+    /* B/C groups: channel d reads B, C of group d / (dim / ngroups); B is then
+     * (batch, ngroups, dstate, L) with group stride B_group_stride elements
+     * (C likewise); dB, dC are then
+     * (batch, ngroups, dstate, L), each group summed over its own channels.  0 or 1 = one group shared by all channels.  With more than
+     * one group, dim / ngroups must be a multiple of 128. */
+    int64_t ngroups;
+    int64_t B_group_stride, C_group_stride;
 } ssm_scan_bwd_params;
 
 SSM_API size_t ssm_scan_bwd_workspace_size(const ssm_scan_bwd_params* p);
@@ -243,6 +256,11 @@ typedef struct {
     const float* D;
     const float* delta_bias;
     float* state;
+    /* B/C groups: channel d reads row d / (dim / ngroups) of group rows
+     * B + b * B_stride + group * B_group_stride (C likewise); 0 or 1 = shared.
+     * ngroups must divide dim. */
+    int64_t ngroups;
+    int64_t B_group_stride, C_group_stride;
 } ssm_state_update_params;
 
 SSM_API ssm_status ssm_state_update(const ssm_state_update_params* p, ssm_stream_t stream);
@@ -363,6 +381,11 @@ typedef struct {
     const float* D;
     const float* delta_bias;
     float* state;
+    /* B/C groups: channel d reads row d / (dim / ngroups) of group rows
+     * B + b * B_stride + group * B_group_stride (C likewise); 0 or 1 = shared.
+     * ngroups must divide dim. */
+    int64_t ngroups;
+    int64_t B_group_stride, C_group_stride;
 } ssm_decode_step_params;
 
 SSM_API ssm_status ssm_decode_step(const ssm_decode_step_params* p, ssm_stream_t stream);

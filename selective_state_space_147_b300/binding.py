@@ -51,6 +51,7 @@ class ScanFwdParams(ctypes.Structure):
         ("out", _vp), ("out_strides", Strides),
         ("A", _fp), ("D", _fp), ("delta_bias", _fp), ("h0", _fp),
         ("final_state", _fp), ("checkpoints", _fp), ("checkpoint_every", _i64),
+        ("ngroups", _i64), ("B_group_stride", _i64), ("C_group_stride", _i64),
     ]
 
 
@@ -70,6 +71,7 @@ class ScanBwdParams(ctypes.Structure):
         ("ddelta", _vp), ("ddelta_strides", Strides),
         ("dz", _vp), ("dz_strides", Strides),
         ("dB", _fp), ("dC", _fp), ("dA", _fp), ("dD", _fp), ("ddelta_bias", _fp), ("dh0", _fp),
+        ("ngroups", _i64), ("B_group_stride", _i64), ("C_group_stride", _i64),
     ]
 
 
@@ -84,6 +86,7 @@ class StateUpdateParams(ctypes.Structure):
         ("C", _vp), ("C_stride", _i64),
         ("out", _vp), ("out_stride", _i64),
         ("A", _fp), ("D", _fp), ("delta_bias", _fp), ("state", _fp),
+        ("ngroups", _i64), ("B_group_stride", _i64), ("C_group_stride", _i64),
     ]
 
 
@@ -100,6 +103,7 @@ class DecodeStepParams(ctypes.Structure):
         ("xc_out", _vp), ("xc_stride", _i64),
         ("conv_state", _vp), ("conv_weight", _fp), ("conv_bias", _fp),
         ("A", _fp), ("D", _fp), ("delta_bias", _fp), ("state", _fp),
+        ("ngroups", _i64), ("B_group_stride", _i64), ("C_group_stride", _i64),
     ]
 
 
@@ -221,6 +225,31 @@ def _seq_strides(name: str, t: Optional[torch.Tensor]) -> Strides:
     return Strides(t.stride(0), t.stride(1))
 
 
+def _bc_seq(name: str, t: torch.Tensor):
+    """B or C of a sequence call: (batch, N, L), or (batch, ngroups, N, L) for B/C
+    groups.  Returns (Strides(batch, row), ngroups, group stride)."""
+    if t.dim() == 4:
+        if t.shape[3] > 1 and t.stride(3) != 1:
+            raise ValueError(f"{name} must have unit stride along the last axis")
+        return Strides(t.stride(0), t.stride(2)), t.shape[1], t.stride(1)
+    return _seq_strides(name, t), 1, 0
+
+
+def _bc_row(name: str, t: torch.Tensor):
+    """B or C of a decode call: (batch, N), or (batch, ngroups, N)."""
+    if t.dim() == 3:
+        if t.shape[2] > 1 and t.stride(2) != 1:
+            raise ValueError(f"{name} must have unit stride along the last axis")
+        return t.stride(0), t.shape[1], t.stride(1)
+    return _row_stride(name, t), 1, 0
+
+
+def _set_groups(p, B, C, gB, gC, sgB, sgC):
+    if gB != gC:
+        raise ValueError("B and C must have the same number of groups")
+    p.ngroups, p.B_group_stride, p.C_group_stride = gB, (sgB if gB > 1 else 0), (sgC if gC > 1 else 0)
+
+
 def _row_stride(name: str, t: Optional[torch.Tensor]) -> int:
     if t is None:
         return 0
@@ -260,8 +289,9 @@ def _fwd_params(u, delta, A, B, C, D, delta_bias, z, h0, bbar_mode, delta_softpl
     p.u, p.u_strides = _ptr(u), _seq_strides("u", u)
     p.delta, p.delta_strides = _ptr(delta), _seq_strides("delta", delta)
     p.z, p.z_strides = _ptr(z), _seq_strides("z", z)
-    p.B, p.B_strides = _ptr(B), _seq_strides("B", B)
-    p.C, p.C_strides = _ptr(C), _seq_strides("C", C)
+    (p.B_strides, gB, sgB), (p.C_strides, gC, sgC) = _bc_seq("B", B), _bc_seq("C", C)
+    p.B, p.C = _ptr(B), _ptr(C)
+    _set_groups(p, B, C, gB, gC, sgB, sgC)
     p.out, p.out_strides = _ptr(out), _seq_strides("out", out)
     p.A, p.D, p.delta_bias, p.h0 = _ptr(A), _ptr(D), _ptr(delta_bias), _ptr(h0)
     p.final_state, p.checkpoints = _ptr(final_state), _ptr(checkpoints)
@@ -363,8 +393,9 @@ def ssm_scan_bwd(u, delta, A, B, C, dout, *, D=None, delta_bias=None, z=None, h0
     g.setdefault("du", torch.empty(batch, dim, L, dtype=gd, device=dev))
     g.setdefault("ddelta", torch.empty(batch, dim, L, dtype=gd, device=dev))
     g.setdefault("dz", torch.empty(batch, dim, L, dtype=gd, device=dev) if z is not None else None)
-    g.setdefault("dB", torch.empty(batch, N, L, dtype=torch.float32, device=dev))
-    g.setdefault("dC", torch.empty(batch, N, L, dtype=torch.float32, device=dev))
+    bc_shape = (batch, B.shape[1], N, L) if B.dim() == 4 else (batch, N, L)   # per B/C group
+    g.setdefault("dB", torch.empty(*bc_shape, dtype=torch.float32, device=dev))
+    g.setdefault("dC", torch.empty(*bc_shape, dtype=torch.float32, device=dev))
     g.setdefault("dA", torch.empty(dim, N, dtype=torch.float32, device=dev))
     g.setdefault("dD", torch.empty(dim, dtype=torch.float32, device=dev))
     g.setdefault("ddelta_bias", torch.empty(dim, dtype=torch.float32, device=dev))
@@ -378,8 +409,9 @@ def ssm_scan_bwd(u, delta, A, B, C, dout, *, D=None, delta_bias=None, z=None, h0
     p.u, p.u_strides = _ptr(u), _seq_strides("u", u)
     p.delta, p.delta_strides = _ptr(delta), _seq_strides("delta", delta)
     p.z, p.z_strides = _ptr(z), _seq_strides("z", z)
-    p.B, p.B_strides = _ptr(B), _seq_strides("B", B)
-    p.C, p.C_strides = _ptr(C), _seq_strides("C", C)
+    (p.B_strides, gB, sgB), (p.C_strides, gC, sgC) = _bc_seq("B", B), _bc_seq("C", C)
+    p.B, p.C = _ptr(B), _ptr(C)
+    _set_groups(p, B, C, gB, gC, sgB, sgC)
     p.dout, p.dout_strides = _ptr(dout), _seq_strides("dout", dout)
     p.A, p.D, p.delta_bias, p.h0 = _ptr(A), _ptr(D), _ptr(delta_bias), _ptr(h0)
     p.dfinal_state, p.checkpoints, p.checkpoint_every = _ptr(dfinal_state), _ptr(checkpoints), int(checkpoint_every)
@@ -429,8 +461,9 @@ def ssm_state_update(state, x, delta, A, B, C, *, D=None, delta_bias=None, z=Non
     p.x, p.x_stride = _ptr(x), _row_stride("x", x)
     p.delta, p.delta_stride = _ptr(delta), _row_stride("delta", delta)
     p.z, p.z_stride = _ptr(z), _row_stride("z", z)
-    p.B, p.B_stride = _ptr(B), _row_stride("B", B)
-    p.C, p.C_stride = _ptr(C), _row_stride("C", C)
+    (p.B_stride, gB, sgB), (p.C_stride, gC, sgC) = _bc_row("B", B), _bc_row("C", C)
+    p.B, p.C = _ptr(B), _ptr(C)
+    _set_groups(p, B, C, gB, gC, sgB, sgC)
     p.out, p.out_stride = _ptr(out), _row_stride("out", out)
     p.A, p.D, p.delta_bias, p.state = _ptr(A), _ptr(D), _ptr(delta_bias), _ptr(state)
     _check(_lib.ssm_state_update(ctypes.byref(p), _stream(stream)))
@@ -464,8 +497,9 @@ def ssm_decode_step(state, conv_state, x, delta, A, B, C, conv_weight, *, conv_b
     p.x, p.x_stride = _ptr(x), _row_stride("x", x)
     p.delta, p.delta_stride = _ptr(delta), _row_stride("delta", delta)
     p.z, p.z_stride = _ptr(z), _row_stride("z", z)
-    p.B, p.B_stride = _ptr(B), _row_stride("B", B)
-    p.C, p.C_stride = _ptr(C), _row_stride("C", C)
+    (p.B_stride, gB, sgB), (p.C_stride, gC, sgC) = _bc_row("B", B), _bc_row("C", C)
+    p.B, p.C = _ptr(B), _ptr(C)
+    _set_groups(p, B, C, gB, gC, sgB, sgC)
     p.out, p.out_stride = _ptr(out), _row_stride("out", out)
     p.xc_out, p.xc_stride = _ptr(xc_out), _row_stride("xc_out", xc_out)
     p.conv_state, p.conv_weight, p.conv_bias = _ptr(conv_state), _ptr(conv_weight), _ptr(conv_bias)

@@ -19,6 +19,20 @@ namespace {
 
 thread_local char g_err[512] = {0};
 
+ssm_status fail(ssm_status s, const char* fmt, ...);
+
+// B/C groups: ngroups 0 or 1 = shared; otherwise it divides dim (and, for the
+// sequence kernels, dim / ngroups is a multiple of their 128-channel blocks)
+ssm_status check_groups(int64_t ngroups, int64_t dim, int64_t Bg, int64_t Cg, bool blocks) {
+    if (ngroups < 0 || Bg < 0 || Cg < 0) return fail(SSM_ERR_INVALID_ARG, "negative ngroups or group stride");
+    if (ngroups <= 1) return SSM_OK;
+    if (dim % ngroups != 0) return fail(SSM_ERR_INVALID_ARG, "ngroups=%lld does not divide dim=%lld",
+                                        (long long)ngroups, (long long)dim);
+    if (blocks && (dim / ngroups) % 128 != 0)
+        return fail(SSM_ERR_UNSUPPORTED, "dim / ngroups = %lld is not a multiple of 128", (long long)(dim / ngroups));
+    return SSM_OK;
+}
+
 ssm_status fail(ssm_status s, const char* fmt, ...) {
     va_list ap;
     va_start(ap, fmt);
@@ -70,7 +84,7 @@ ssm_status check_fwd(const ssm_scan_fwd_params* p) {
                     (long long)p->checkpoint_every);
     if (p->checkpoints != nullptr && (uintptr_t)p->checkpoints % 16 != 0)
         return fail(SSM_ERR_MISALIGNED, "checkpoints must be 16-byte aligned");
-    return SSM_OK;
+    return check_groups(p->ngroups, p->dim, p->B_group_stride, p->C_group_stride, true);
 }
 
 ssm_status check_bwd(const ssm_scan_bwd_params* p) {
@@ -97,7 +111,7 @@ ssm_status check_bwd(const ssm_scan_bwd_params* p) {
         return fail(SSM_ERR_INVALID_ARG, "checkpoint_every must be positive when checkpoints are given");
     if (p->checkpoints != nullptr && (uintptr_t)p->checkpoints % 16 != 0)
         return fail(SSM_ERR_MISALIGNED, "checkpoints must be 16-byte aligned");
-    return SSM_OK;
+    return check_groups(p->ngroups, p->dim, p->B_group_stride, p->C_group_stride, true);
 }
 
 }  // namespace
@@ -118,7 +132,7 @@ const char* ssm_status_string(ssm_status s) {
 
 const char* ssm_last_error(void) { return g_err; }
 
-int ssm_abi_version(void) { return 2; }
+int ssm_abi_version(void) { return 3; }
 
 uint64_t ssm_launch_count(void) { return ssm::ssm_launch_count_value(); }
 
@@ -260,6 +274,10 @@ ssm_status ssm_decode_step(const ssm_decode_step_params* p, ssm_stream_t stream)
     if (p->x_stride < 0 || p->delta_stride < 0 || p->z_stride < 0 || p->B_stride < 0 || p->C_stride < 0 ||
         p->out_stride < 0 || p->xc_stride < 0)
         return fail(SSM_ERR_INVALID_ARG, "negative stride");
+    {
+        const ssm_status g = check_groups(p->ngroups, p->dim, p->B_group_stride, p->C_group_stride, false);
+        if (g != SSM_OK) return g;
+    }
     cudaError_t e = ssm::launch_decode_step(p, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "ssm_decode_step launch");
     return ok();
@@ -279,6 +297,10 @@ ssm_status ssm_state_update(const ssm_state_update_params* p, ssm_stream_t strea
     if (p->x_stride < 0 || p->delta_stride < 0 || p->z_stride < 0 || p->B_stride < 0 || p->C_stride < 0 ||
         p->out_stride < 0)
         return fail(SSM_ERR_INVALID_ARG, "negative stride");
+    {
+        const ssm_status g = check_groups(p->ngroups, p->dim, p->B_group_stride, p->C_group_stride, false);
+        if (g != SSM_OK) return g;
+    }
     cudaError_t e = ssm::launch_state_update(p, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "ssm_state_update launch");
     return ok();

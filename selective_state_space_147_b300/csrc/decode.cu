@@ -24,6 +24,7 @@ struct DecArgs {
     const float* A; const float* D; const float* bias;
     float* state;
     int softplus;
+    int64_t cpg, sBg, sCg;        // B/C groups: channel d reads group d / cpg
 };
 
 template <typename Tin, typename Tout, bool ZOH, bool ACC>
@@ -49,8 +50,8 @@ __global__ void __launch_bounds__(256) state_update_kernel(const DecArgs a) {
         const int n = g + G * j;
         if (n < a.dstate) {
             const float Av = __ldg(a.A + d * a.dstate + n);
-            const float Bv = Elem<Tin>::load(reinterpret_cast<const Tin*>(a.B) + b * a.sB + n);
-            const float Cv = Elem<Tin>::load(reinterpret_cast<const Tin*>(a.C) + b * a.sC + n);
+            const float Bv = Elem<Tin>::load(reinterpret_cast<const Tin*>(a.B) + b * a.sB + (d / a.cpg) * a.sBg + n);
+            const float Cv = Elem<Tin>::load(reinterpret_cast<const Tin*>(a.C) + b * a.sC + (d / a.cpg) * a.sCg + n);
             const float x = dl * Av;
             float ab, coef;
             if (ACC) {
@@ -98,8 +99,9 @@ __global__ void __launch_bounds__(256) state_update16_kernel(const DecArgs a) {
     const float4 s0 = __ldcs(st), s1 = __ldcs(st + 1);
     const float4 a0 = __ldg(reinterpret_cast<const float4*>(a.A + d * 16 + g * 8));
     const float4 a1 = __ldg(reinterpret_cast<const float4*>(a.A + d * 16 + g * 8) + 1);
-    const uint4 bw = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.B) + b * a.sB + g * 8));
-    const uint4 cw = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.C) + b * a.sC + g * 8));
+    const int64_t grp = (a.cpg >= a.dim) ? 0 : (int)d / (int)a.cpg;   // one group: no division
+    const uint4 bw = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.B) + b * a.sB + grp * a.sBg + g * 8));
+    const uint4 cw = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.C) + b * a.sC + grp * a.sCg + g * 8));
     const float xt = Elem<__nv_bfloat16>::load(reinterpret_cast<const __nv_bfloat16*>(a.x) + b * a.sx + d);
     const float v = Elem<__nv_bfloat16>::load(reinterpret_cast<const __nv_bfloat16*>(a.dt) + b * a.sdt + d) +
                     (a.bias ? __ldg(a.bias + d) : 0.f);
@@ -145,6 +147,7 @@ struct DecStepArgs {
     const float* A; const float* D; const float* bias;
     float* state;
     int softplus;
+    int64_t cpg, sBg, sCg;        // B/C groups: channel d reads group d / cpg
 };
 
 // Any layout: one thread per channel, every state and tap in a loop.
@@ -179,8 +182,8 @@ __global__ void __launch_bounds__(256) decode_step_kernel(const DecStepArgs a) {
     float y = 0.f;
     for (int n = 0; n < a.dstate; n++) {
         const float Av = __ldg(a.A + d * a.dstate + n);
-        const float Bv = Elem<Tin>::load(reinterpret_cast<const Tin*>(a.B) + b * a.sB + n);
-        const float Cv = Elem<Tin>::load(reinterpret_cast<const Tin*>(a.C) + b * a.sC + n);
+        const float Bv = Elem<Tin>::load(reinterpret_cast<const Tin*>(a.B) + b * a.sB + (d / a.cpg) * a.sBg + n);
+        const float Cv = Elem<Tin>::load(reinterpret_cast<const Tin*>(a.C) + b * a.sC + (d / a.cpg) * a.sCg + n);
         const float x = dl * Av;
         float ab, coef;
         if (ACC) {
@@ -223,8 +226,9 @@ __global__ void __launch_bounds__(256) decode_step16_kernel(const DecStepArgs a)
     const float4 a0 = __ldg(reinterpret_cast<const float4*>(a.A + d * 16 + g * 8));
     const float4 a1 = __ldg(reinterpret_cast<const float4*>(a.A + d * 16 + g * 8) + 1);
     const float4 cw = __ldg(reinterpret_cast<const float4*>(a.cw + d * 4));
-    const uint4 bw = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.B) + b * a.sB + g * 8));
-    const uint4 cwd = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.C) + b * a.sC + g * 8));
+    const int64_t grp = (a.cpg >= a.dim) ? 0 : (int)d / (int)a.cpg;   // one group: no division
+    const uint4 bw = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.B) + b * a.sB + grp * a.sBg + g * 8));
+    const uint4 cwd = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.C) + b * a.sC + grp * a.sCg + g * 8));
     const uint32_t xbits = __ldg(reinterpret_cast<const unsigned short*>(a.x) + b * a.sx + d);
     const float v = Elem<__nv_bfloat16>::load(reinterpret_cast<const __nv_bfloat16*>(a.dt) + b * a.sdt + d) +
                     (a.bias ? __ldg(a.bias + d) : 0.f);
@@ -283,8 +287,11 @@ cudaError_t launch_decode_step(const ssm_decode_step_params* p, cudaStream_t st)
     a.cstate = p->conv_state; a.cw = p->conv_weight; a.cb = p->conv_bias;
     a.A = p->A; a.D = p->D; a.bias = p->delta_bias; a.state = p->state;
     a.softplus = p->delta_softplus ? 1 : 0;
+    a.cpg = p->ngroups > 1 ? p->dim / p->ngroups : p->dim;
+    a.sBg = p->ngroups > 1 ? p->B_group_stride : 0;
+    a.sCg = p->ngroups > 1 ? p->C_group_stride : 0;
     const bool zoh = p->bbar_mode == SSM_BBAR_ZOH;
-    const bool fast16 = p->dstate == 16 && p->width == 4 && p->in_dtype == SSM_BF16 &&
+    const bool fast16 = p->dstate == 16 && p->width == 4 && p->in_dtype == SSM_BF16 && (a.sBg % 8 == 0) && (a.sCg % 8 == 0) &&
                         ((uintptr_t)p->state % 16 == 0) && ((uintptr_t)p->A % 16 == 0) &&
                         ((uintptr_t)p->B % 16 == 0) && ((uintptr_t)p->C % 16 == 0) &&
                         (p->B_stride % 8 == 0) && (p->C_stride % 8 == 0) &&
@@ -328,11 +335,14 @@ cudaError_t launch_state_update(const ssm_state_update_params* p, cudaStream_t s
     a.sC = p->C_stride; a.so = p->out_stride;
     a.A = p->A; a.D = p->D; a.bias = p->delta_bias; a.state = p->state;
     a.softplus = p->delta_softplus ? 1 : 0;
+    a.cpg = p->ngroups > 1 ? p->dim / p->ngroups : p->dim;
+    a.sBg = p->ngroups > 1 ? p->B_group_stride : 0;
+    a.sCg = p->ngroups > 1 ? p->C_group_stride : 0;
     const bool zoh = p->bbar_mode == SSM_BBAR_ZOH;
     const bool fast16 = p->dstate == 16 && p->in_dtype == SSM_BF16 &&
                         ((uintptr_t)p->state % 16 == 0) && ((uintptr_t)p->A % 16 == 0) &&
                         ((uintptr_t)p->B % 16 == 0) && ((uintptr_t)p->C % 16 == 0) &&
-                        (p->B_stride % 8 == 0) && (p->C_stride % 8 == 0);
+                        (p->B_stride % 8 == 0) && (p->C_stride % 8 == 0) && (a.sBg % 8 == 0) && (a.sCg % 8 == 0);
     if (fast16) {
         const dim3 blocks2((unsigned)ceil_div(p->dim * 2, 256), (unsigned)p->batch);
         if (p->out_dtype == SSM_BF16) {

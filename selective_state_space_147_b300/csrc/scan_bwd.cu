@@ -57,6 +57,9 @@ struct BwdArgs {
     // du, ddelta, dz summed across state groups in fp32 (NULL with one group)
     float* gacc;                // 3 x (batch * dim * seqlen)
     int g_first, g_last;
+    // B/C groups: channel d reads group d / cpg; dB, dC are (batch, ngroups, N, L)
+    int64_t cpg, sB_g, sC_g;
+    int ngroups;
 };
 
 // With more than 16 states the backward runs once per group of 16; du, ddelta
@@ -155,8 +158,9 @@ __device__ __forceinline__ void bwd_channel(const BwdArgs& a, float* sbc, float*
     Tg* durow = reinterpret_cast<Tg*>(a.du) + b * a.sdu_b + d * a.sdu_d;
     Tg* ddrow = reinterpret_cast<Tg*>(a.ddt) + b * a.sddt_b + d * a.sddt_d;
     Tg* dzrow = HAS_Z ? reinterpret_cast<Tg*>(a.dz) + b * a.sdz_b + d * a.sdz_d : nullptr;
-    const Tin* Bb = reinterpret_cast<const Tin*>(a.B) + b * a.sB_b;
-    const Tin* Cb = reinterpret_cast<const Tin*>(a.C) + b * a.sC_b;
+    // B/C group of the CTA's channels (groups span multiples of 128 channels)
+    const Tin* Bb = reinterpret_cast<const Tin*>(a.B) + b * a.sB_b + (d / a.cpg) * a.sB_g;
+    const Tin* Cb = reinterpret_cast<const Tin*>(a.C) + b * a.sC_b + (d / a.cpg) * a.sC_g;
 
     // 8-step sub-blocks, last to first; the inputs of the previous (earlier)
     // sub-block are loaded while the current one is computed.
@@ -458,8 +462,9 @@ scan_bwd_fast_kernel(const BwdArgs a, const int* flag) {
     const Tin* drow = reinterpret_cast<const Tin*>(a.dt) + b * a.sdt_b + d * a.sdt_d;
     const Tin* zrow = HAS_Z ? reinterpret_cast<const Tin*>(a.z) + b * a.sz_b + d * a.sz_d : nullptr;
     const Tin* orow = reinterpret_cast<const Tin*>(a.dout) + b * a.sdo_b + d * a.sdo_d;
-    const Tin* Bb = reinterpret_cast<const Tin*>(a.B) + b * a.sB_b;
-    const Tin* Cb = reinterpret_cast<const Tin*>(a.C) + b * a.sC_b;
+    // B/C group of the CTA's channels (groups span multiples of 128 channels)
+    const Tin* Bb = reinterpret_cast<const Tin*>(a.B) + b * a.sB_b + (d / a.cpg) * a.sB_g;
+    const Tin* Cb = reinterpret_cast<const Tin*>(a.C) + b * a.sC_b + (d / a.cpg) * a.sC_g;
     const bool vec_in = a.vec_u && a.vec_dt && a.vec_do && (!HAS_Z || a.vec_z);
     const bool ck16 = a.dstate == 16;
     const int64_t nsb = ceil_div(a.seqlen, (int64_t)kFSub);
@@ -753,17 +758,21 @@ scan_bwd_kernel(const BwdArgs a, const int* flag) {
 constexpr int kBwdAccSmemFloats = kTile * kRow + kBwdWarps * kSub * 32 + kBwdWarps * 32 * kRed2 + kBwdWarps * 9 * 16 * 32;
 constexpr int kBwdAccSmemBytes = 4 * kBwdAccSmemFloats;
 
-// dB[b, n, t] = sum over CTAs of the partials, in CTA order.
+// dB[b, grp, n, t] = sum over the CTAs of that B/C group of the partials, in CTA order.
 __global__ void bwd_reduce_bc_kernel(const BwdArgs a, float* dB, float* dC) {
     const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int n = blockIdx.y;
-    const int64_t b = blockIdx.z >> 1;
-    const int tsr = blockIdx.z & 1;
+    const int64_t z = blockIdx.z;                 // (b, grp, tsr), tsr fastest
+    const int tsr = (int)(z & 1);
+    const int64_t grp = (z >> 1) % a.ngroups;
+    const int64_t b = (z >> 1) / a.ngroups;
     if (t >= a.seqlen || n >= a.dstate) return;
+    const int64_t per = a.ngroups > 1 ? a.cpg / kFChans : a.nblk;    // CTAs per group
     float s = 0.f;
-    for (int k = 0; k < a.nblk; k++) s += a.part_bc[(((b * a.nblk + k) * 2 + tsr) * 16 + n) * a.seqlen + t];
+    for (int64_t k = grp * per; k < (grp + 1) * per && k < a.nblk; k++)
+        s += a.part_bc[(((b * a.nblk + k) * 2 + tsr) * 16 + n) * a.seqlen + t];
     float* out = tsr == 0 ? dB : dC;
-    if (out) out[(b * a.sBo + n) * a.seqlen + t] = s;
+    if (out) out[((b * a.ngroups + grp) * a.sBo + n) * a.seqlen + t] = s;
 }
 
 // dA[d, n], dD[d], dbias[d]: sums over the batch, in batch order.
@@ -806,6 +815,7 @@ static ssm_scan_fwd_params ckpt_fwd_params(const ssm_scan_bwd_params* p) {
     f.z = nullptr; f.z_strides = ssm_strides{0, 0};
     f.B = p->B; f.B_strides = p->B_strides;
     f.C = p->C; f.C_strides = p->C_strides;
+    f.ngroups = p->ngroups; f.B_group_stride = p->B_group_stride; f.C_group_stride = p->C_group_stride;
     f.out = nullptr; f.out_strides = ssm_strides{0, 0};
     f.A = p->A; f.D = p->D; f.delta_bias = p->delta_bias; f.h0 = p->h0;
     f.final_state = nullptr;
@@ -944,6 +954,10 @@ cudaError_t launch_scan_bwd(const ssm_scan_bwd_params* p, void* ws, int num_sms,
         count_launches(1);
     }
     a.sA = p->dstate; a.sst = p->dstate; a.sBo = p->dstate;
+    a.ngroups = p->ngroups > 1 ? (int)p->ngroups : 1;
+    a.cpg = p->ngroups > 1 ? p->dim / p->ngroups : p->dim;
+    a.sB_g = p->ngroups > 1 ? p->B_group_stride : 0;
+    a.sC_g = p->ngroups > 1 ? p->C_group_stride : 0;
     a.ck_P = (p->dstate + 1) / 2; a.ck_p0 = 0;
     a.gacc = l.gacc ? reinterpret_cast<float*>(wp + l.part_bc + l.part_A + 2 * l.part_D + 256) : nullptr;
     // one pass per group of at most 16 states (a single pass for d_state <= 16)
@@ -968,7 +982,7 @@ cudaError_t launch_scan_bwd(const ssm_scan_bwd_params* p, void* ws, int num_sms,
                                           : launch_bwd_typed<float, float>(ga, zoh, has_z, flag, st);
         }
         if (e != cudaSuccess) return e;
-        const dim3 g2((unsigned)ceil_div(p->seqlen, 256), (unsigned)ga.dstate, (unsigned)(2 * p->batch));
+        const dim3 g2((unsigned)ceil_div(p->seqlen, 256), (unsigned)ga.dstate, (unsigned)(2 * p->batch * ga.ngroups));
         bwd_reduce_bc_kernel<<<g2, 256, 0, st>>>(ga, p->dB ? p->dB + (int64_t)n0 * p->seqlen : nullptr,
                                                  p->dC ? p->dC + (int64_t)n0 * p->seqlen : nullptr);
         bwd_reduce_params_kernel<<<(unsigned)ceil_div(p->dim * 18, 256), 256, 0, st>>>(

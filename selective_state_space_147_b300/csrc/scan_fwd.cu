@@ -139,7 +139,8 @@ cudaError_t launch_scan_fwd(const ssm_scan_fwd_params* p, void* ws, int num_sms,
     a.vec_out = p->out ? aligned16(p->out, a.so_b, a.so_d, osz) : 0;
     // B/C are read two steps at a time
     a.vec_BC = ((uintptr_t)p->B % (2 * isz) == 0) && ((uintptr_t)p->C % (2 * isz) == 0) &&
-               (a.sB_b % 2 == 0) && (a.sB_n % 2 == 0) && (a.sC_b % 2 == 0) && (a.sC_n % 2 == 0);
+               (a.sB_b % 2 == 0) && (a.sB_n % 2 == 0) && (a.sC_b % 2 == 0) && (a.sC_n % 2 == 0) &&
+               (p->ngroups <= 1 || (p->B_group_stride % 2 == 0 && p->C_group_stride % 2 == 0));
     a.seg_len = pl.seg_len; a.nseg = pl.nseg;
     a.ws_hend = a.ws_sdelta = a.ws_carry = nullptr;
     if (pl.nseg > 1) {
@@ -154,7 +155,8 @@ cudaError_t launch_scan_fwd(const ssm_scan_fwd_params* p, void* ws, int num_sms,
         if (p->in_dtype == SSM_BF16) {
             // the cp.async pipeline needs every u/delta/z/B/C row 16-byte aligned
             const bool bc16 = ((uintptr_t)ga.B % 16 == 0) && ((uintptr_t)ga.C % 16 == 0) &&
-                              (ga.sB_b % 8 == 0) && (ga.sB_n % 8 == 0) && (ga.sC_b % 8 == 0) && (ga.sC_n % 8 == 0);
+                              (ga.sB_b % 8 == 0) && (ga.sB_n % 8 == 0) && (ga.sC_b % 8 == 0) && (ga.sC_n % 8 == 0) &&
+                              (ga.sB_g % 8 == 0) && (ga.sC_g % 8 == 0);
             const bool async = ga.vec_u && ga.vec_dt && (!has_z || ga.vec_z) && bc16 && env_int("SSM_FWD_NOASYNC", 0) == 0;
             if (async) {
                 if (p->out_dtype == SSM_BF16) return dispatch_G<__nv_bfloat16, __nv_bfloat16, true>(ga, pl.G, zoh, has_z, st);
@@ -166,6 +168,9 @@ cudaError_t launch_scan_fwd(const ssm_scan_fwd_params* p, void* ws, int num_sms,
         if (p->out_dtype == SSM_BF16) return dispatch_G<float, __nv_bfloat16, false>(ga, pl.G, zoh, has_z, st);
         return dispatch_G<float, float, false>(ga, pl.G, zoh, has_z, st);
     };
+    a.cpg = p->ngroups > 1 ? p->dim / p->ngroups : p->dim;
+    a.sB_g = p->ngroups > 1 ? p->B_group_stride : 0;
+    a.sC_g = p->ngroups > 1 ? p->C_group_stride : 0;
     a.sA = p->dstate; a.sst = p->dstate;
     a.ck_P = (p->dstate + 1) / 2; a.ck_p0 = 0;
     a.yacc = nullptr; a.y_first = a.y_last = 1;

@@ -35,6 +35,8 @@ struct FwdArgs {
     // readout sum across state groups (NULL with a single group)
     float* yacc;       // (channels, seqlen) fp32
     int y_first, y_last;
+    // B/C groups: channel d reads group d / cpg (group strides in elements)
+    int64_t cpg, sB_g, sC_g;
 };
 
 template <typename Tin, typename Tout, bool ASYNC>

@@ -360,8 +360,9 @@ __device__ __forceinline__ void scan_warp(const FwdArgs& a, float* sbc_all, int6
     const Tin* zrow = HAS_Z ? reinterpret_cast<const Tin*>(a.z) + b * a.sz_b + d * a.sz_d : nullptr;
     // out == NULL: checkpoint-only pass (used by the backward), nothing is stored
     Tout* orow = (MODE == kFull && a.out != nullptr) ? reinterpret_cast<Tout*>(a.out) + b * a.so_b + d * a.so_d : nullptr;
-    const Tin* Bb = reinterpret_cast<const Tin*>(a.B) + b * a.sB_b;
-    const Tin* Cb = reinterpret_cast<const Tin*>(a.C) + b * a.sC_b;
+    // B/C group of the warp's channels (one group per warp: groups span multiples of 128 channels)
+    const Tin* Bb = reinterpret_cast<const Tin*>(a.B) + b * a.sB_b + (d / a.cpg) * a.sB_g;
+    const Tin* Cb = reinterpret_cast<const Tin*>(a.C) + b * a.sC_b + (d / a.cpg) * a.sC_g;
     const bool ck = MODE == kFull && a.ckpt != nullptr;
     int64_t next_ck = ceil_div(t_begin, a.ckpt_K) * a.ckpt_K;   // next step that starts a checkpoint
 
@@ -500,8 +501,10 @@ __device__ __forceinline__ void issue_tile(const FwdArgs& a, unsigned char* stag
         int64_t n = (row < a.dstate) ? a.seqlen - t : 0;
         n = n < 0 ? 0 : (n > 8 ? 8 : n);
         const __nv_bfloat16* base = tsr == 0
-            ? reinterpret_cast<const __nv_bfloat16*>(a.B) + b * a.sB_b + (row < a.dstate ? row : 0) * a.sB_n
-            : reinterpret_cast<const __nv_bfloat16*>(a.C) + b * a.sC_b + (row < a.dstate ? row : 0) * a.sC_n;
+            ? reinterpret_cast<const __nv_bfloat16*>(a.B) + b * a.sB_b + (d_first / a.cpg) * a.sB_g +
+                  (row < a.dstate ? row : 0) * a.sB_n
+            : reinterpret_cast<const __nv_bfloat16*>(a.C) + b * a.sC_b + (d_first / a.cpg) * a.sC_g +
+                  (row < a.dstate ? row : 0) * a.sC_n;
         cp_async16(bc + tsr * 1024 + swz(row, chunk), base + (n > 0 ? t : 0), (int)(n * 2));
     }
 }
