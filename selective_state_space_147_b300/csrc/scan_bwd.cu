@@ -54,43 +54,11 @@ struct BwdArgs {
     // the states (dfinal, dh0), checkpoint pairs in total and the group's first
     int64_t sA, sst, ck_P, ck_p0;
     int64_t sBo;                // rows per batch of dB, dC (the full state size)
-    // du, ddelta, dz summed across state groups in fp32 (NULL with one group)
-    float* gacc;                // 3 x (batch * dim * seqlen)
-    int g_first, g_last;
+    int g_first;                // first group of states (more than 16 states run in groups)
     // B/C groups: channel d reads group d / cpg; dB, dC are (batch, ngroups, N, L)
     int64_t cpg, sB_g, sC_g;
     int ngroups;
 };
-
-// With more than 16 states the backward runs once per group of 16; du, ddelta
-// and dz are sums over all states, so each group adds its part to fp32 buffers
-// (the first writes them) and the last one stores the gradients.  Returns true
-// when this call must store.
-template <int NV>
-__device__ __forceinline__ bool accumulate_grads(const BwdArgs& a, int64_t chan, int64_t t0, int cnt,
-                                                 float (&du)[NV], float (&dd)[NV], float (&dz)[NV], bool has_z) {
-    if (a.gacc == nullptr) return true;
-    const int64_t CL = a.batch * a.dim * a.seqlen;
-    float* pu = a.gacc + chan * a.seqlen + t0;
-    float* pd = pu + CL;
-    float* pz = pd + CL;
-#pragma unroll
-    for (int j = 0; j < NV; j++) {
-        if (j < cnt) {
-            if (!a.g_first) {
-                du[j] += pu[j];
-                dd[j] += pd[j];
-                if (has_z) dz[j] += pz[j];
-            }
-            if (!a.g_last) {
-                pu[j] = du[j];
-                pd[j] = dd[j];
-                if (has_z) pz[j] = dz[j];
-            }
-        }
-    }
-    return a.g_last != 0;
-}
 
 // Checkpoint k of channel (b, d), state pair `pair`: the forward's layout
 // (batch, n_ckpt, ceil(dstate/2), dim, 2), the pairs of neighbouring channels adjacent.
@@ -140,7 +108,7 @@ __device__ __forceinline__ void bwd_channel(const BwdArgs& a, float* sbc, float*
         if constexpr (ACC) return (An[n] != 0.f) ? 1.f / An[n] : 0.f;
         else return rcp_approx(An[n]);
     };
-    const float Dd = (a.D && a.g_first) ? __ldg(a.D + d) : 0.f;   // the D skip enters once
+    const float Dd = a.D ? __ldg(a.D + d) : 0.f;
     const float bias = a.bias ? __ldg(a.bias + d) : 0.f;
     // Idle lanes (d past dim) shadow the last channel to keep the warp uniform;
     // a zero upstream gradient makes every partial they add to dB, dC zero.
@@ -159,8 +127,10 @@ __device__ __forceinline__ void bwd_channel(const BwdArgs& a, float* sbc, float*
     Tg* ddrow = reinterpret_cast<Tg*>(a.ddt) + b * a.sddt_b + d * a.sddt_d;
     Tg* dzrow = HAS_Z ? reinterpret_cast<Tg*>(a.dz) + b * a.sdz_b + d * a.sdz_d : nullptr;
     // B/C group of the CTA's channels (groups span multiples of 128 channels)
-    const Tin* Bb = reinterpret_cast<const Tin*>(a.B) + b * a.sB_b + (d / a.cpg) * a.sB_g;
-    const Tin* Cb = reinterpret_cast<const Tin*>(a.C) + b * a.sC_b + (d / a.cpg) * a.sC_g;
+    // B/C group of the CTA's channels (groups span multiples of 128 channels)
+    const int64_t grp = (a.cpg >= a.dim) ? 0 : d / a.cpg;       // one group: no division
+    const Tin* Bb = reinterpret_cast<const Tin*>(a.B) + b * a.sB_b + grp * a.sB_g;
+    const Tin* Cb = reinterpret_cast<const Tin*>(a.C) + b * a.sC_b + grp * a.sC_g;
 
     // 8-step sub-blocks, last to first; the inputs of the previous (earlier)
     // sub-block are loaded while the current one is computed.
@@ -307,7 +277,7 @@ __device__ __forceinline__ void bwd_channel(const BwdArgs& a, float* sbc, float*
             duo[j] = du;
             ddo[j] = dv;
         }
-        if (active && accumulate_grads<kSub>(a, chan, t0, cnt, duo, ddo, dzo, HAS_Z)) {
+        if (active) {
             store8<Tg>(durow + t0, cnt, a.vec_du, duo);
             store8<Tg>(ddrow + t0, cnt, a.vec_ddt, ddo);
             if constexpr (HAS_Z) store8<Tg>(dzrow + t0, cnt, a.vec_dz, dzo);
@@ -455,7 +425,7 @@ scan_bwd_fast_kernel(const BwdArgs a, const int* flag) {
         dA2[p] = 0ull;
     }
     const pf2 LOG2E2 = pf2_make(kLog2e, kLog2e);
-    const float Dd = (a.D && a.g_first) ? __ldg(a.D + d) : 0.f;   // the D skip enters once
+    const float Dd = a.D ? __ldg(a.D + d) : 0.f;
     const float bias = a.bias ? __ldg(a.bias + d) : 0.f;
     float dDacc = 0.f, dbacc = 0.f;
     const Tin* urow = reinterpret_cast<const Tin*>(a.u) + b * a.su_b + d * a.su_d;
@@ -463,8 +433,10 @@ scan_bwd_fast_kernel(const BwdArgs a, const int* flag) {
     const Tin* zrow = HAS_Z ? reinterpret_cast<const Tin*>(a.z) + b * a.sz_b + d * a.sz_d : nullptr;
     const Tin* orow = reinterpret_cast<const Tin*>(a.dout) + b * a.sdo_b + d * a.sdo_d;
     // B/C group of the CTA's channels (groups span multiples of 128 channels)
-    const Tin* Bb = reinterpret_cast<const Tin*>(a.B) + b * a.sB_b + (d / a.cpg) * a.sB_g;
-    const Tin* Cb = reinterpret_cast<const Tin*>(a.C) + b * a.sC_b + (d / a.cpg) * a.sC_g;
+    // B/C group of the CTA's channels (groups span multiples of 128 channels)
+    const int64_t grp = (a.cpg >= a.dim) ? 0 : d / a.cpg;       // one group: no division
+    const Tin* Bb = reinterpret_cast<const Tin*>(a.B) + b * a.sB_b + grp * a.sB_g;
+    const Tin* Cb = reinterpret_cast<const Tin*>(a.C) + b * a.sC_b + grp * a.sC_g;
     const bool vec_in = a.vec_u && a.vec_dt && a.vec_do && (!HAS_Z || a.vec_z);
     const bool ck16 = a.dstate == 16;
     const int64_t nsb = ceil_div(a.seqlen, (int64_t)kFSub);
@@ -680,7 +652,7 @@ scan_bwd_fast_kernel(const BwdArgs a, const int* flag) {
                 dzo[j] = go * fmaf(Dd, uj[j], pf2_sum(yv2[j])) * sgz * fmaf(zj, 1.f - sgz, 1.f);
             }
         }
-        if (active && accumulate_grads<kFSub>(a, chan, t0, cnt, duo, ddo, dzo, HAS_Z)) {
+        if (active) {
             store4<Tg>(reinterpret_cast<Tg*>(a.du) + b * a.sdu_b + d * a.sdu_d + t0, cnt, a.vec_du, duo);
             store4<Tg>(reinterpret_cast<Tg*>(a.ddt) + b * a.sddt_b + d * a.sddt_d + t0, cnt, a.vec_ddt, ddo);
             if constexpr (HAS_Z)
@@ -762,8 +734,8 @@ constexpr int kBwdAccSmemBytes = 4 * kBwdAccSmemFloats;
 __global__ void bwd_reduce_bc_kernel(const BwdArgs a, float* dB, float* dC) {
     const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int n = blockIdx.y;
-    const int64_t z = blockIdx.z;                 // (b, grp, tsr), tsr fastest
-    const int tsr = (int)(z & 1);
+    const int z = (int)blockIdx.z;                // (b, grp, tsr), tsr fastest
+    const int tsr = z & 1;
     const int64_t grp = (z >> 1) % a.ngroups;
     const int64_t b = (z >> 1) / a.ngroups;
     if (t >= a.seqlen || n >= a.dstate) return;
@@ -799,7 +771,7 @@ __global__ void bwd_reduce_params_kernel(const BwdArgs a, float* dA, float* dD, 
 // Host side
 
 struct BwdLayout {
-    size_t ckpt, fwd_ws, part_bc, part_A, part_D, gacc, total;
+    size_t ckpt, fwd_ws, part_bc, part_A, part_D, gacc, total;   // gacc: state-group slices
     bool own_ckpt;
 };
 
@@ -840,7 +812,8 @@ static BwdLayout bwd_layout(const ssm_scan_bwd_params* p, int num_sms) {
     l.part_bc = round256((size_t)(p->batch * nblk * 2 * 16 * p->seqlen) * 4);
     l.part_A = round256((size_t)(chans * 16) * 4);
     l.part_D = round256((size_t)chans * 4);
-    l.gacc = p->dstate > 16 ? round256((size_t)(3 * chans * p->seqlen) * 4) : 0;   // cross-group sums
+    // more than 16 states: du, ddelta, dz of every state group in fp32 slices
+    l.gacc = p->dstate > 16 ? round256((size_t)(3 * ceil_div(p->dstate, (int64_t)16) * chans * p->seqlen) * 4) : 0;
     l.total = l.ckpt + l.fwd_ws + l.part_bc + l.part_A + 2 * l.part_D + 256 + l.gacc;   // + the A == 0 flag
     return l;
 }
@@ -848,6 +821,40 @@ static BwdLayout bwd_layout(const ssm_scan_bwd_params* p, int num_sms) {
 size_t bwd_workspace_bytes(const ssm_scan_bwd_params* p, int num_sms) {
     if (p->seqlen == 0) return 0;
     return bwd_layout(p, num_sms).total;
+}
+
+// More than 16 states: sum the state groups' fp32 du, ddelta, dz slices (in
+// group order) into the caller's gradients.
+template <typename Tg>
+__global__ void bwd_group_finish_kernel(const float* __restrict__ gbuf, int ngroups, int64_t slice,
+                                        Tg* du, int64_t sdu_b, int64_t sdu_d, Tg* ddt, int64_t sddt_b, int64_t sddt_d,
+                                        Tg* dz, int64_t sdz_b, int64_t sdz_d, int64_t dim, int64_t seqlen, int64_t ntile) {
+    const int64_t chan = blockIdx.x / ntile;
+    const int64_t t = (blockIdx.x % ntile) * blockDim.x + threadIdx.x;
+    if (t >= seqlen) return;
+    const int64_t b = chan / dim, d = chan - b * dim, i = chan * seqlen + t;
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f;
+    for (int g = 0; g < ngroups; g++) {
+        const float* gb = gbuf + (int64_t)g * 3 * slice + i;
+        s0 += gb[0]; s1 += gb[slice];
+        if (dz != nullptr) s2 += gb[2 * slice];
+    }
+    if (du != nullptr) Elem<Tg>::store(du + b * sdu_b + d * sdu_d + t, s0);
+    if (ddt != nullptr) Elem<Tg>::store(ddt + b * sddt_b + d * sddt_d + t, s1);
+    if (dz != nullptr) Elem<Tg>::store(dz + b * sdz_b + d * sdz_d + t, s2);
+}
+
+template <typename Tg>
+static cudaError_t launch_bwd_group_finish(const ssm_scan_bwd_params* p, const float* gbuf, int ngroups,
+                                           cudaStream_t st) {
+    const int64_t chans = p->batch * p->dim, ntile = ceil_div(p->seqlen, (int64_t)256);
+    bwd_group_finish_kernel<Tg><<<(unsigned)(chans * ntile), 256, 0, st>>>(
+        gbuf, ngroups, chans * p->seqlen, static_cast<Tg*>(p->du), p->du_strides.batch, p->du_strides.row,
+        static_cast<Tg*>(p->ddelta), p->ddelta_strides.batch, p->ddelta_strides.row,
+        static_cast<Tg*>(p->z != nullptr ? p->dz : nullptr), p->dz_strides.batch, p->dz_strides.row,
+        p->dim, p->seqlen, ntile);
+    count_launches(1);
+    return cudaGetLastError();
 }
 
 static bool al16(const void* ptr, ssm_strides s, int esize) {
@@ -959,9 +966,12 @@ cudaError_t launch_scan_bwd(const ssm_scan_bwd_params* p, void* ws, int num_sms,
     a.sB_g = p->ngroups > 1 ? p->B_group_stride : 0;
     a.sC_g = p->ngroups > 1 ? p->C_group_stride : 0;
     a.ck_P = (p->dstate + 1) / 2; a.ck_p0 = 0;
-    a.gacc = l.gacc ? reinterpret_cast<float*>(wp + l.part_bc + l.part_A + 2 * l.part_D + 256) : nullptr;
-    // one pass per group of at most 16 states (a single pass for d_state <= 16)
+    float* gbuf = l.gacc ? reinterpret_cast<float*>(wp + l.part_bc + l.part_A + 2 * l.part_D + 256) : nullptr;
+    // one pass per group of at most 16 states (a single pass for d_state <= 16);
+    // with several groups each writes fp32 du, ddelta, dz to its own slices and
+    // only the first adds the D skip
     const int ngroups = (int)ceil_div(p->dstate, (int64_t)16);
+    const int64_t slice = chans * p->seqlen;
     for (int gi = 0; gi < ngroups; gi++) {
         BwdArgs ga = a;
         const int n0 = gi * 16;
@@ -973,8 +983,16 @@ cudaError_t launch_scan_bwd(const ssm_scan_bwd_params* p, void* ws, int num_sms,
         ga.dh0 = p->dh0 ? p->dh0 + n0 : nullptr;
         ga.ck_p0 = n0 / 2;
         ga.g_first = gi == 0;
-        ga.g_last = gi == ngroups - 1;
-        if (p->in_dtype == SSM_BF16) {
+        if (gbuf != nullptr) {
+            float* gs = gbuf + (int64_t)gi * 3 * slice;
+            ga.du = gs; ga.ddt = gs + slice; ga.dz = has_z ? gs + 2 * slice : nullptr;
+            ga.sdu_b = ga.sddt_b = ga.sdz_b = p->dim * p->seqlen;
+            ga.sdu_d = ga.sddt_d = ga.sdz_d = p->seqlen;
+            ga.vec_du = ga.vec_ddt = ga.vec_dz = (p->seqlen % 4 == 0) ? 1 : 0;
+            if (gi > 0) ga.D = nullptr;
+            e = p->in_dtype == SSM_BF16 ? launch_bwd_typed<__nv_bfloat16, float>(ga, zoh, has_z, flag, st)
+                                        : launch_bwd_typed<float, float>(ga, zoh, has_z, flag, st);
+        } else if (p->in_dtype == SSM_BF16) {
             e = p->grad_dtype == SSM_BF16 ? launch_bwd_typed<__nv_bfloat16, __nv_bfloat16>(ga, zoh, has_z, flag, st)
                                           : launch_bwd_typed<__nv_bfloat16, float>(ga, zoh, has_z, flag, st);
         } else {
@@ -991,7 +1009,9 @@ cudaError_t launch_scan_bwd(const ssm_scan_bwd_params* p, void* ws, int num_sms,
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    return cudaSuccess;
+    if (gbuf == nullptr) return cudaSuccess;
+    return p->grad_dtype == SSM_BF16 ? launch_bwd_group_finish<__nv_bfloat16>(p, gbuf, ngroups, st)
+                                     : launch_bwd_group_finish<float>(p, gbuf, ngroups, st);
 }
 
 }  // namespace ssm

@@ -87,8 +87,8 @@ static FwdPlan plan_fwd(const ssm_scan_fwd_params* p, int num_sms) {
     return pl;
 }
 
-// Workspace: the segmented schedule's carries, then (more than 16 states) the
-// fp32 readout sum shared by the state groups.
+// Workspace: the segmented schedule's carries, then (more than 16 states) one
+// fp32 readout slice per state group.
 static size_t seg_ws_bytes(const ssm_scan_fwd_params* p, const FwdPlan& pl) {
     if (pl.nseg <= 1) return 0;
     const int64_t floats = p->batch * p->dim * pl.nseg * (2 * kNMax + 1);
@@ -96,7 +96,41 @@ static size_t seg_ws_bytes(const ssm_scan_fwd_params* p, const FwdPlan& pl) {
 }
 static size_t yacc_bytes(const ssm_scan_fwd_params* p) {
     if (p->dstate <= kNMax || p->out == nullptr) return 0;
-    return (size_t)(ceil_div(p->batch * p->dim * p->seqlen * 4, 256) * 256);
+    const int64_t ngroups = ceil_div(p->dstate, (int64_t)kNMax);
+    return (size_t)(ceil_div(ngroups * p->batch * p->dim * p->seqlen * 4, 256) * 256);
+}
+
+// More than 16 states: every state group wrote its readout sum_n C h (no D
+// skip, no gate) as fp32 into its own slice; out = (sum of the slices + D u)
+// silu(z), the slices summed in group order.
+template <typename Tin, typename Tout>
+__global__ void fwd_group_finish_kernel(const float* __restrict__ ybuf, int ngroups, int64_t slice,
+                                        const Tin* __restrict__ u, int64_t su_b, int64_t su_d,
+                                        const Tin* __restrict__ z, int64_t sz_b, int64_t sz_d,
+                                        const float* __restrict__ D, Tout* __restrict__ out,
+                                        int64_t so_b, int64_t so_d, int64_t dim, int64_t seqlen, int64_t ntile) {
+    const int64_t chan = blockIdx.x / ntile;
+    const int64_t t = (blockIdx.x % ntile) * blockDim.x + threadIdx.x;
+    if (t >= seqlen) return;
+    const int64_t b = chan / dim, d = chan - b * dim;
+    float y = 0.f;
+    for (int g = 0; g < ngroups; g++) y += ybuf[g * slice + chan * seqlen + t];
+    const float uv = Elem<Tin>::load(u + b * su_b + d * su_d + t);
+    y = fmaf(D ? __ldg(D + d) : 0.f, uv, y);
+    if (z != nullptr) y *= silu_accurate(Elem<Tin>::load(z + b * sz_b + d * sz_d + t));
+    Elem<Tout>::store(out + b * so_b + d * so_d + t, y);
+}
+
+template <typename Tin, typename Tout>
+static cudaError_t launch_fwd_group_finish(const ssm_scan_fwd_params* p, const float* ybuf, int ngroups,
+                                           cudaStream_t st) {
+    const int64_t chans = p->batch * p->dim, ntile = ceil_div(p->seqlen, (int64_t)256);
+    fwd_group_finish_kernel<Tin, Tout><<<(unsigned)(chans * ntile), 256, 0, st>>>(
+        ybuf, ngroups, chans * p->seqlen, static_cast<const Tin*>(p->u), p->u_strides.batch, p->u_strides.row,
+        static_cast<const Tin*>(p->z), p->z_strides.batch, p->z_strides.row, p->D, static_cast<Tout*>(p->out),
+        p->out_strides.batch, p->out_strides.row, p->dim, p->seqlen, ntile);
+    count_launches(1);
+    return cudaGetLastError();
 }
 
 size_t fwd_workspace_bytes(const ssm_scan_fwd_params* p, int num_sms) {
@@ -151,7 +185,7 @@ cudaError_t launch_scan_fwd(const ssm_scan_fwd_params* p, void* ws, int num_sms,
     }
     const bool zoh = p->bbar_mode == SSM_BBAR_ZOH;
     const bool has_z = p->z != nullptr;
-    auto run = [&](const FwdArgs& ga) -> cudaError_t {
+    auto run = [&](const FwdArgs& ga, bool out_bf16, bool has_z) -> cudaError_t {
         if (p->in_dtype == SSM_BF16) {
             // the cp.async pipeline needs every u/delta/z/B/C row 16-byte aligned
             const bool bc16 = ((uintptr_t)ga.B % 16 == 0) && ((uintptr_t)ga.C % 16 == 0) &&
@@ -159,13 +193,13 @@ cudaError_t launch_scan_fwd(const ssm_scan_fwd_params* p, void* ws, int num_sms,
                               (ga.sB_g % 8 == 0) && (ga.sC_g % 8 == 0);
             const bool async = ga.vec_u && ga.vec_dt && (!has_z || ga.vec_z) && bc16 && env_int("SSM_FWD_NOASYNC", 0) == 0;
             if (async) {
-                if (p->out_dtype == SSM_BF16) return dispatch_G<__nv_bfloat16, __nv_bfloat16, true>(ga, pl.G, zoh, has_z, st);
+                if (out_bf16) return dispatch_G<__nv_bfloat16, __nv_bfloat16, true>(ga, pl.G, zoh, has_z, st);
                 return dispatch_G<__nv_bfloat16, float, true>(ga, pl.G, zoh, has_z, st);
             }
-            if (p->out_dtype == SSM_BF16) return dispatch_G<__nv_bfloat16, __nv_bfloat16, false>(ga, pl.G, zoh, has_z, st);
+            if (out_bf16) return dispatch_G<__nv_bfloat16, __nv_bfloat16, false>(ga, pl.G, zoh, has_z, st);
             return dispatch_G<__nv_bfloat16, float, false>(ga, pl.G, zoh, has_z, st);
         }
-        if (p->out_dtype == SSM_BF16) return dispatch_G<float, __nv_bfloat16, false>(ga, pl.G, zoh, has_z, st);
+        if (out_bf16) return dispatch_G<float, __nv_bfloat16, false>(ga, pl.G, zoh, has_z, st);
         return dispatch_G<float, float, false>(ga, pl.G, zoh, has_z, st);
     };
     a.cpg = p->ngroups > 1 ? p->dim / p->ngroups : p->dim;
@@ -173,11 +207,11 @@ cudaError_t launch_scan_fwd(const ssm_scan_fwd_params* p, void* ws, int num_sms,
     a.sC_g = p->ngroups > 1 ? p->C_group_stride : 0;
     a.sA = p->dstate; a.sst = p->dstate;
     a.ck_P = (p->dstate + 1) / 2; a.ck_p0 = 0;
-    a.yacc = nullptr; a.y_first = a.y_last = 1;
-    if (p->dstate <= kNMax) return run(a);
-    // more than 16 states: one pass per group of 16, the readout summed across them
+    if (p->dstate <= kNMax) return run(a, p->out_dtype == SSM_BF16, has_z);
+    // more than 16 states: one pass per group of 16 into its own fp32 readout
+    // slice, then one pass that sums the slices, adds D u and gates
     const int ngroups = (int)ceil_div(p->dstate, (int64_t)kNMax);
-    a.yacc = p->out != nullptr ? reinterpret_cast<float*>(static_cast<char*>(ws) + seg_ws_bytes(p, pl)) : nullptr;
+    float* ybuf = p->out != nullptr ? reinterpret_cast<float*>(static_cast<char*>(ws) + seg_ws_bytes(p, pl)) : nullptr;
     for (int gi = 0; gi < ngroups; gi++) {
         FwdArgs ga = a;
         const int n0 = gi * kNMax;
@@ -188,14 +222,23 @@ cudaError_t launch_scan_fwd(const ssm_scan_fwd_params* p, void* ws, int num_sms,
         ga.h0 = p->h0 ? p->h0 + n0 : nullptr;
         ga.final_state = p->final_state ? p->final_state + n0 : nullptr;
         ga.ck_p0 = n0 / 2;
-        ga.y_first = gi == 0;
-        ga.y_last = gi == ngroups - 1;
+        ga.D = nullptr; ga.z = nullptr;
+        if (ybuf != nullptr) {
+            ga.out = ybuf + (int64_t)gi * chans * p->seqlen;
+            ga.so_b = p->dim * p->seqlen; ga.so_d = p->seqlen;
+            ga.vec_out = aligned16(ga.out, ga.so_b, ga.so_d, 4);
+        }
         ga.vec_BC = ((uintptr_t)ga.B % (2 * isz) == 0) && ((uintptr_t)ga.C % (2 * isz) == 0) &&
                     (a.sB_b % 2 == 0) && (a.sB_n % 2 == 0) && (a.sC_b % 2 == 0) && (a.sC_n % 2 == 0);
-        cudaError_t e = run(ga);
+        cudaError_t e = run(ga, false, false);
         if (e != cudaSuccess) return e;
     }
-    return cudaSuccess;
+    if (ybuf == nullptr) return cudaSuccess;
+    if (p->in_dtype == SSM_BF16)
+        return p->out_dtype == SSM_BF16 ? launch_fwd_group_finish<__nv_bfloat16, __nv_bfloat16>(p, ybuf, ngroups, st)
+                                        : launch_fwd_group_finish<__nv_bfloat16, float>(p, ybuf, ngroups, st);
+    return p->out_dtype == SSM_BF16 ? launch_fwd_group_finish<float, __nv_bfloat16>(p, ybuf, ngroups, st)
+                                    : launch_fwd_group_finish<float, float>(p, ybuf, ngroups, st);
 }
 
 }  // namespace ssm

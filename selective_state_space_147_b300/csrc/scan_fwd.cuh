@@ -32,9 +32,6 @@ struct FwdArgs {
     // the (h0, final) states, checkpoint pairs in total and the group's first one
     int64_t sA, sst;
     int64_t ck_P, ck_p0;
-    // readout sum across state groups (NULL with a single group)
-    float* yacc;       // (channels, seqlen) fp32
-    int y_first, y_last;
     // B/C groups: channel d reads group d / cpg (group strides in elements)
     int64_t cpg, sB_g, sC_g;
 };

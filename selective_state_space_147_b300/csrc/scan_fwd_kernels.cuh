@@ -325,21 +325,6 @@ __device__ __forceinline__ float finish_y(float y, float Dd, float uj, float zj)
     return y;
 }
 
-// With more than 16 states the forward runs once per group of 16 and the
-// readout sum over states crosses the groups: each group adds its C.h to an fp32
-// buffer (the first one writes it), and the last group finishes the output.
-// Returns true when this call must write the output.
-__device__ __forceinline__ bool accumulate_readout(const FwdArgs& a, int64_t chan, int64_t t, float& y) {
-    if (a.yacc == nullptr) return true;
-    float* ya = a.yacc + chan * a.seqlen + t;
-    if (!a.y_first) y += *ya;
-    if (!a.y_last) {
-        *ya = y;
-        return false;
-    }
-    return true;
-}
-
 // ---------------------------------------------------------------------------
 // Generic path (any alignment, float32 or bfloat16): u, delta, z come through
 // a three-deep register prefetch ring, B/C through a 64-step fp32 tile.
@@ -361,8 +346,10 @@ __device__ __forceinline__ void scan_warp(const FwdArgs& a, float* sbc_all, int6
     // out == NULL: checkpoint-only pass (used by the backward), nothing is stored
     Tout* orow = (MODE == kFull && a.out != nullptr) ? reinterpret_cast<Tout*>(a.out) + b * a.so_b + d * a.so_d : nullptr;
     // B/C group of the warp's channels (one group per warp: groups span multiples of 128 channels)
-    const Tin* Bb = reinterpret_cast<const Tin*>(a.B) + b * a.sB_b + (d / a.cpg) * a.sB_g;
-    const Tin* Cb = reinterpret_cast<const Tin*>(a.C) + b * a.sC_b + (d / a.cpg) * a.sC_g;
+    // B/C group of the warp's channels (one group per warp: groups span multiples of 128 channels)
+    const int64_t grp = (a.cpg >= a.dim) ? 0 : d / a.cpg;       // one group: no division
+    const Tin* Bb = reinterpret_cast<const Tin*>(a.B) + b * a.sB_b + grp * a.sB_g;
+    const Tin* Cb = reinterpret_cast<const Tin*>(a.C) + b * a.sC_b + grp * a.sC_g;
     const bool ck = MODE == kFull && a.ckpt != nullptr;
     int64_t next_ck = ceil_div(t_begin, a.ckpt_K) * a.ckpt_K;   // next step that starts a checkpoint
 
@@ -410,19 +397,11 @@ __device__ __forceinline__ void scan_warp(const FwdArgs& a, float* sbc_all, int6
                     sd_c = (tk - sd) - yk;
                     sd = tk;
                 } else {
-                    // reduce over the channel's lanes first, then across state groups
-#pragma unroll
-                    for (int o = 1; o < G; o <<= 1) y += __shfl_xor_sync(0xffffffffu, y, o);
-                    if (a.yacc != nullptr) {
-                        if (active && g == 0 && j < cnt) accumulate_readout(a, b * a.dim + d, t0 + j, y);
-                        if (!a.y_last) continue;
-                    }
-                    yout[j] = finish_y<1, ACC, HAS_Z>(y, Dd, uj, HAS_Z ? rz[0].get(j) : 0.f);
+                    yout[j] = finish_y<G, ACC, HAS_Z>(y, Dd, uj, HAS_Z ? rz[0].get(j) : 0.f);
                 }
             }
             if constexpr (MODE == kFull) {
-                if (active && g == 0 && orow != nullptr && (a.yacc == nullptr || a.y_last))
-                    store8<Tout>(orow + t0, cnt, a.vec_out, yout);
+                if (active && g == 0 && orow != nullptr) store8<Tout>(orow + t0, cnt, a.vec_out, yout);
             }
             ru[0] = ru[1]; rd[0] = rd[1]; ru[1] = ru[2]; rd[1] = rd[2];
             if constexpr (HAS_Z && MODE == kFull) { rz[0] = rz[1]; rz[1] = rz[2]; }
@@ -465,7 +444,8 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 
 template <int G, bool HAS_Z>
 __device__ __forceinline__ void issue_tile(const FwdArgs& a, unsigned char* stage, int tid, int64_t b,
-                                           int64_t d_first, int64_t tt, int64_t t_end) {
+                                           int64_t d_first, int64_t tt, int64_t t_end,
+                                           const __nv_bfloat16* Bg, const __nv_bfloat16* Cg) {
     constexpr int R = AsyncLayout<G>::kRows;
     constexpr int T = AsyncLayout<G>::kThreads;
     constexpr int kSeq = AsyncLayout<G>::kSeqBytes;
@@ -500,11 +480,8 @@ __device__ __forceinline__ void issue_tile(const FwdArgs& a, unsigned char* stag
         const int64_t t = tt + chunk * 8;
         int64_t n = (row < a.dstate) ? a.seqlen - t : 0;
         n = n < 0 ? 0 : (n > 8 ? 8 : n);
-        const __nv_bfloat16* base = tsr == 0
-            ? reinterpret_cast<const __nv_bfloat16*>(a.B) + b * a.sB_b + (d_first / a.cpg) * a.sB_g +
-                  (row < a.dstate ? row : 0) * a.sB_n
-            : reinterpret_cast<const __nv_bfloat16*>(a.C) + b * a.sC_b + (d_first / a.cpg) * a.sC_g +
-                  (row < a.dstate ? row : 0) * a.sC_n;
+        const __nv_bfloat16* base = tsr == 0 ? Bg + (row < a.dstate ? row : 0) * a.sB_n
+                                             : Cg + (row < a.dstate ? row : 0) * a.sC_n;
         cp_async16(bc + tsr * 1024 + swz(row, chunk), base + (n > 0 ? t : 0), (int)(n * 2));
     }
 }
@@ -590,13 +567,20 @@ __device__ __forceinline__ void scan_cta_async(const FwdArgs& a, unsigned char* 
     Tout* orow = (MODE == kFull && a.out != nullptr) ? reinterpret_cast<Tout*>(a.out) + b * a.so_b + d * a.so_d : nullptr;
     const bool ck = MODE == kFull && a.ckpt != nullptr;
     int64_t next_ck = ceil_div(t_begin, a.ckpt_K) * a.ckpt_K;   // next step that starts a checkpoint
+    // pair 0 of that checkpoint for this channel, advanced one checkpoint at a time
+    float* ck_next = ck ? ckpt_pair(a, b, next_ck / a.ckpt_K, d, 0) : nullptr;
+    const int64_t ck_kstride = a.ck_P * a.dim * 2;
+    // B/C rows of this batch row and of the CTA's B/C group (groups span whole CTAs)
+    const int64_t grp = (a.cpg >= a.dim) ? 0 : d_first / a.cpg;   // one group: no division
+    const __nv_bfloat16* Bg = reinterpret_cast<const __nv_bfloat16*>(a.B) + b * a.sB_b + grp * a.sB_g;
+    const __nv_bfloat16* Cg = reinterpret_cast<const __nv_bfloat16*>(a.C) + b * a.sC_b + grp * a.sC_g;
     float* bcf = reinterpret_cast<float*>(smem + kStages * kStage);
     constexpr bool kZ = HAS_Z && MODE == kFull;
 
     const int64_t ntiles = ceil_div(t_end - t_begin, kATile);
 #pragma unroll
     for (int s = 0; s < kStages - 1; s++) {
-        if (s < ntiles) issue_tile<G, kZ>(a, smem + s * kStage, tid, b, d_first, t_begin + s * kATile, t_end);
+        if (s < ntiles) issue_tile<G, kZ>(a, smem + s * kStage, tid, b, d_first, t_begin + s * kATile, t_end, Bg, Cg);
         cp_async_commit();
     }
     float sd = 0.f, sd_c = 0.f;
@@ -605,7 +589,7 @@ __device__ __forceinline__ void scan_cta_async(const FwdArgs& a, unsigned char* 
         {
             const int64_t kn = k + kStages - 1;
             if (kn < ntiles)
-                issue_tile<G, kZ>(a, smem + (kn % kStages) * kStage, tid, b, d_first, t_begin + kn * kATile, t_end);
+                issue_tile<G, kZ>(a, smem + (kn % kStages) * kStage, tid, b, d_first, t_begin + kn * kATile, t_end, Bg, Cg);
             cp_async_commit();
         }
         cp_async_wait<kStages - 1>();
@@ -640,9 +624,9 @@ __device__ __forceinline__ void scan_cta_async(const FwdArgs& a, unsigned char* 
             if (t0 >= t_end) break;
             const int cnt = (int)((t_end - t0) < kSub ? (t_end - t0) : kSub);
             if (ck && t0 == next_ck) {
-                if (active)
-                    store_ckpt_pairs<NP>(ckpt_pair(a, b, t0 / a.ckpt_K, d, n_base >> 1), 2 * a.dim, n_base, a.dstate, h2);
+                if (active) store_ckpt_pairs<NP>(ck_next + (n_base >> 1) * 2 * a.dim, 2 * a.dim, n_base, a.dstate, h2);
                 next_ck += a.ckpt_K;
+                ck_next += ck_kstride;
             }
             const uint4 wu = *reinterpret_cast<const uint4*>(st + 0 * kSeq + swz(row, c));
             const uint4 wd = *reinterpret_cast<const uint4*>(st + 1 * kSeq + swz(row, c));
@@ -675,8 +659,9 @@ __device__ __forceinline__ void scan_cta_async(const FwdArgs& a, unsigned char* 
             }
             float* mid = nullptr;   // checkpoint of the state before step t0 + 4, if one is due
             if (ck && t0 + kSub / 2 == next_ck && t0 + kSub / 2 < t_end) {
-                if (active) mid = ckpt_pair(a, b, (t0 + kSub / 2) / a.ckpt_K, d, 0);
+                if (active) mid = ck_next;
                 next_ck += a.ckpt_K;
+                ck_next += ck_kstride;
             }
             float yp[kSub];
             scan_block8<NP, ZOH, MODE == kFull>(h2, A2, I2, dl8, u8, bcf + c * kSub * kRow, n_base, yp, mid,
@@ -702,16 +687,13 @@ __device__ __forceinline__ void scan_cta_async(const FwdArgs& a, unsigned char* 
 #pragma unroll
                     for (int q = 1; q < G; q++)
                         if (g == q) yj = yp[q * SPL + i];
-                    if (a.yacc != nullptr && active && jb + i < cnt)
-                        accumulate_readout(a, b * a.dim + d, t0 + jb + i, yj);
                     const float uj = (G == 1) ? u8[i] : own_bf16<G>(wu, g, i);
                     yj = fmaf(Dd, uj, yj);
                     if constexpr (HAS_Z) yj *= silu_fast(own_bf16<G>(wz, g, i));
                     yo[i] = yj;
                 }
                 const int lim = cnt - jb;
-                if (active && lim > 0 && orow != nullptr && (a.yacc == nullptr || a.y_last))
-                    storeN<Tout, SPL>(orow + t0 + jb, lim, a.vec_out, yo);
+                if (active && lim > 0 && orow != nullptr) storeN<Tout, SPL>(orow + t0 + jb, lim, a.vec_out, yo);
             }
         }
         __syncthreads();   // everyone is done with this stage and with bcf
