@@ -54,8 +54,10 @@ def _load():
             lib.oracle_conv1d_silu.argtypes = [i64, i64, i64, i64] + [p] * 6
             lib.oracle_conv1d_silu_update.argtypes = [i64, i64, i64] + [p] * 5
             lib.oracle_conv1d_silu_bwd.argtypes = [i64, i64, i64, i64] + [p] * 9
+            lib.oracle_ssd_fwd.argtypes = [i64] * 6 + [p] * 8 + [i32, p, p, i64, i64]
             for f in (lib.oracle_scan_fwd, lib.oracle_scan_bwd, lib.oracle_state_update,
-                      lib.oracle_conv1d_silu, lib.oracle_conv1d_silu_update, lib.oracle_conv1d_silu_bwd):
+                      lib.oracle_conv1d_silu, lib.oracle_conv1d_silu_update, lib.oracle_conv1d_silu_bwd,
+                      lib.oracle_ssd_fwd):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -232,3 +234,31 @@ def conv1d_silu_update(state, x, w, bias=None):
     if rc != 0:
         raise ValueError("oracle_conv1d_silu_update rejected its arguments")
     return out, st
+
+
+def ssd_fwd(x, dt, A, B, C, D=None, dt_bias=None, h0=None, delta_softplus=True, threads: int = 1):
+    """Mamba-2 state-space-duality layer by its recurrence.  x: (batch, L, H, P);
+    dt: (batch, L, H); A, D, dt_bias: (H,); B, C: (batch, L, G, N); h0: (batch, H, N, P).
+    Returns (out (batch, L, H, P), final_state (batch, H, N, P)) as float64."""
+    lib = _load()
+    x, dt, A, B, C, D, dt_bias, h0 = map(_f64, (x, dt, A, B, C, D, dt_bias, h0))
+    batch, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    out = np.zeros((batch, L, H, P))
+    hN = np.zeros((batch, H, N, P))
+
+    def run(r):
+        rc = lib.oracle_ssd_fwd(batch, L, H, P, N, G, _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                                _ptr(dt_bias), _ptr(h0), int(bool(delta_softplus)), _ptr(out), _ptr(hN),
+                                r[0], r[1])
+        if rc != 0:
+            raise ValueError("oracle_ssd_fwd rejected its arguments")
+
+    rs = _ranges(batch * H, threads)
+    if len(rs) <= 1:
+        for r in rs:
+            run(r)
+    else:
+        with ThreadPoolExecutor(len(rs)) as ex:
+            list(ex.map(run, rs))
+    return out, hN

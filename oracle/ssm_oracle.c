@@ -412,3 +412,62 @@ int oracle_conv1d_silu_update(int64_t batch, int64_t dim, int64_t width,
     }
     return 0;
 }
+
+/*
+ * Mamba-2 state-space-duality layer, computed as its recurrence.
+ *
+ * [P3] "Mamba 与状态空间模型", section "09 Mamba-2：两种算法": A is one number
+ * times the identity (per head), and the layer is the product with a lower
+ * triangular matrix whose (i, j) entry is C at step i times B at step j times
+ * the whole decay between the two steps; the recurrence is one of the two
+ * algorithms that evaluate it.  [P4] pnsm.cn overview, section "Mamba-2：状态
+ * 空间对偶性": scalar transition, blocks inside / recurrence between.  The
+ * input enters scaled by the step size (Bbar = Delta B, the simplified rule of
+ * [P3] "模型省略了什么"), so per (b, head h), with state H (N x P):
+ *
+ *   Delta_t = softplus(dt[b,t,h] + dt_bias[h])   (or dt + dt_bias)
+ *   H       = exp(Delta_t A[h]) H + Delta_t B_t x_t^T
+ *   y_t     = C_t^T H + D[h] x_t
+ *
+ * Layouts: x, out (batch, L, H, P); dt (batch, L, H); B, C (batch, L, G, N)
+ * with head h reading group h / (H / G); h0, hN (batch, H, N, P).  Units
+ * [u_begin, u_end) index (b, h) pairs.
+ */
+int oracle_ssd_fwd(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, int64_t dstate,
+                   int64_t ngroups, const double* x, const double* dt, const double* A,
+                   const double* Bm, const double* Cm, const double* Dskip, const double* dt_bias,
+                   const double* h0, int delta_softplus, double* out, double* hN,
+                   int64_t u_begin, int64_t u_end)
+{
+    if (batch < 0 || seqlen < 0 || nheads < 1 || headdim < 1 || dstate < 1 || ngroups < 1) return -1;
+    if (nheads % ngroups != 0) return -1;
+    if (u_begin < 0 || u_end > batch * nheads || u_begin > u_end) return -1;
+    const int64_t P = headdim, N = dstate, H = nheads, G = ngroups;
+    double* S = (double*)malloc(sizeof(double) * (size_t)(N * P));
+    if (!S) return -1;
+    for (int64_t unit = u_begin; unit < u_end; unit++) {
+        const int64_t b = unit / H, h = unit % H, g = h / (H / G);
+        for (int64_t i = 0; i < N * P; i++) S[i] = h0 ? h0[unit * N * P + i] : 0.0;
+        for (int64_t t = 0; t < seqlen; t++) {
+            const double v = dt[(b * seqlen + t) * H + h] + (dt_bias ? dt_bias[h] : 0.0);
+            const double delta = delta_softplus ? o_softplus(v) : v;
+            const double a = exp(delta * A[h]);
+            const double* Bt = Bm + ((b * seqlen + t) * G + g) * N;
+            const double* Ct = Cm + ((b * seqlen + t) * G + g) * N;
+            const double* xt = x + ((b * seqlen + t) * H + h) * P;
+            double* yt = out + ((b * seqlen + t) * H + h) * P;
+            for (int64_t n = 0; n < N; n++)
+                for (int64_t p = 0; p < P; p++)
+                    S[n * P + p] = a * S[n * P + p] + delta * Bt[n] * xt[p];
+            for (int64_t p = 0; p < P; p++) {
+                double y = 0.0;
+                for (int64_t n = 0; n < N; n++) y += Ct[n] * S[n * P + p];
+                yt[p] = y + (Dskip ? Dskip[h] : 0.0) * xt[p];
+            }
+        }
+        if (hN)
+            for (int64_t i = 0; i < N * P; i++) hN[unit * N * P + i] = S[i];
+    }
+    free(S);
+    return 0;
+}

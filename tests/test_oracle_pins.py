@@ -489,3 +489,91 @@ def test_generator_rows_match_full_tensor_and_moments():
     b = S.delta_bias(3, 1000, 1e-3, 1e-1)
     s = torch.nn.functional.softplus(b.double())
     assert s.min().item() >= 1e-3 * 0.999 and s.max().item() <= 1e-1 * 1.001
+
+
+# ---------------------------------------------------------------------------
+# Mamba-2 state-space-duality layer (oracle.ssd_fwd, a recurrence)
+
+def _ssd_inputs(seed, b=2, L=11, H=4, P=3, N=5, G=2, h0=False):
+    r = rng(seed)
+    return dict(x=r.normal(size=(b, L, H, P)), dt=r.normal(size=(b, L, H)), A=-r.uniform(0.2, 2.0, H),
+                B=r.normal(size=(b, L, G, N)), C=r.normal(size=(b, L, G, N)), D=r.normal(size=H),
+                dt_bias=r.normal(size=H) * 0.3, h0=r.normal(size=(b, H, N, P)) if h0 else None)
+
+
+def _ssd_dual(g, delta_softplus=True):
+    """The layer as the product with a lower-triangular matrix: entry (i, j) is
+    C_i . B_j times the decay exp(sum over r in (j, i] of Delta_r A) between the
+    two steps; the input enters as Delta_j x_j.  An initial state adds
+    exp(sum over r <= i of Delta_r A) C_i^T h0.  Built entry by entry."""
+    x, dt, A, B, C, D = g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"]
+    b, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    y = np.zeros_like(x)
+    hN = np.zeros((b, H, N, P))
+    for bb in range(b):
+        for h in range(H):
+            gi = h // (H // G)
+            v = dt[bb, :, h] + g["dt_bias"][h]
+            delta = np.logaddexp(0.0, v) if delta_softplus else v
+            for i in range(L):
+                acc = np.zeros(P)
+                for j in range(i + 1):
+                    decay = math.exp(sum(delta[r] * A[h] for r in range(j + 1, i + 1)))
+                    acc += float(C[bb, i, gi] @ B[bb, j, gi]) * decay * delta[j] * x[bb, j, h]
+                if g["h0"] is not None:
+                    decay0 = math.exp(sum(delta[r] * A[h] for r in range(0, i + 1)))
+                    acc += decay0 * (C[bb, i, gi] @ g["h0"][bb, h])
+                y[bb, i, h] = acc + D[h] * x[bb, i, h]
+            # final state: every step's input decayed to the end, plus h0 decayed over all steps
+            S_ = np.zeros((N, P))
+            for j in range(L):
+                decay = math.exp(sum(delta[r] * A[h] for r in range(j + 1, L)))
+                S_ += decay * delta[j] * np.outer(B[bb, j, gi], x[bb, j, h])
+            if g["h0"] is not None:
+                S_ += math.exp(sum(delta[r] * A[h] for r in range(L))) * g["h0"][bb, h]
+            hN[bb, h] = S_
+    return y, hN
+
+
+@pytest.mark.parametrize("softplus", [True, False])
+@pytest.mark.parametrize("with_h0", [False, True])
+def test_ssd_recurrence_equals_the_lower_triangular_product(softplus, with_h0):
+    g = _ssd_inputs(31, h0=with_h0)
+    if not softplus:
+        g["dt"] = np.abs(g["dt"]) + 0.05        # a valid step size without softplus
+    y, hN = oracle.ssd_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"], g["dt_bias"], g["h0"],
+                           delta_softplus=softplus)
+    y_ref, h_ref = _ssd_dual(g, softplus)
+    assert rel_err(y, y_ref) <= 1e-12
+    assert rel_err(hN, h_ref) <= 1e-12
+
+
+def test_ssd_with_one_head_dim_is_the_selective_scan_with_equal_A():
+    """P = 1: every head is one Mamba-1 channel whose N states share A[h] and use
+    Bbar = Delta B -- the (separately pinned) selective-scan oracle, simple rule."""
+    g = _ssd_inputs(32, b=2, L=13, H=3, P=1, N=4, G=1)
+    y, hN = oracle.ssd_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"], g["dt_bias"])
+    u = g["x"][..., 0].transpose(0, 2, 1)                  # (batch, H, L)
+    dt = g["dt"].transpose(0, 2, 1)
+    A = np.repeat(g["A"][:, None], 4, axis=1)              # (H, N)
+    Bm = g["B"][:, :, 0, :].transpose(0, 2, 1)             # (batch, N, L)
+    Cm = g["C"][:, :, 0, :].transpose(0, 2, 1)
+    ref, href = oracle.scan_fwd(u, dt, A, Bm, Cm, g["D"], g["dt_bias"], zoh=False)
+    assert rel_err(y[..., 0].transpose(0, 2, 1), ref) <= 1e-12
+    assert rel_err(hN[..., 0], href) <= 1e-12
+
+
+def test_ssd_chunk_invariance():
+    """Scanning [0, m) and then [m, L) from the first part's final state equals
+    one scan over [0, L)."""
+    g = _ssd_inputs(33, L=17, h0=True)
+    full, hfull = oracle.ssd_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"], g["dt_bias"], g["h0"])
+    m = 6
+    cut = lambda a, s: None if a is None else a[:, s]
+    y1, h1 = oracle.ssd_fwd(cut(g["x"], slice(0, m)), cut(g["dt"], slice(0, m)), g["A"], cut(g["B"], slice(0, m)),
+                            cut(g["C"], slice(0, m)), g["D"], g["dt_bias"], g["h0"])
+    y2, h2 = oracle.ssd_fwd(cut(g["x"], slice(m, None)), cut(g["dt"], slice(m, None)), g["A"],
+                            cut(g["B"], slice(m, None)), cut(g["C"], slice(m, None)), g["D"], g["dt_bias"], h1)
+    assert rel_err(np.concatenate([y1, y2], axis=1), full) <= 1e-12
+    assert rel_err(h2, hfull) <= 1e-12
