@@ -41,15 +41,17 @@ UNIT = "channel-tokens/s"
 WORK = dict(batch=8, dim=4096, dstate=16, seqlen=16384, width=4)
 # Mamba-2.8B-shaped decode (64 layers, batch 128)
 DECODE = dict(batch=128, dim=5120, dstate=16, width=4, layers=64, steps=128)
+# Mamba-2-2.7B-shaped state-space-duality layer (d_inner 5120 = 80 heads of 64, state 128)
+SSD = dict(batch=8, seqlen=2048, nheads=80, headdim=64, dstate=128, ngroups=1, chunk=64)
 
 # DRAM traffic of each entry point per channel-token (dram__bytes_read.sum +
 # dram__bytes_write.sum summed over the entry point's launches) from one ncu
 # capture at batch 8, d_inner 4096, L 2048 (the command is in profiles/).  The
-# figures hold only while the CUDA sources hash to TRAFFIC_SOURCES_SHA; after
-# any kernel change the traffic is reported as null until it is captured again.
-TRAFFIC_PER_CT = {"ssm_scan_bwd": 35.13, "ssm_scan_fwd": 23.16, "causal_conv1d_silu": 3.20,
-                  "causal_conv1d_silu_bwd": 5.51}
-TRAFFIC_SOURCES_SHA = "780c03febadef8a9"
+# figures hold only while the step's kernel sources hash to TRAFFIC_SOURCES_SHA;
+# after any change to them the traffic is reported as null until it is captured again.
+TRAFFIC_PER_CT = {"ssm_scan_bwd": 35.08, "ssm_scan_fwd": 23.17, "causal_conv1d_silu": 3.19,
+                  "causal_conv1d_silu_bwd": 5.50}
+TRAFFIC_SOURCES_SHA = "07498381fee3b7c2"
 
 SM_FP32_LANES = 128     # FP32 lanes per SM per clock (sm_100 family)
 SM_SFU_EX2 = 32         # MUFU ex2 results per SM per clock on B300 (measured 29.8 at ~2 GHz)
@@ -148,15 +150,18 @@ class ClockSampler:
                 "samples": len(rows), "reasons": reasons}
 
 
+# the CUDA sources of the training step's kernels (conv, scan forward and backward)
+STEP_KERNEL_SOURCES = ("common.cuh", "scan_fwd.cuh", "scan_fwd_kernels.cuh", "scan_fwd.cu", "scan_fwd_inst_bb.cu",
+                       "scan_fwd_inst_bf.cu", "scan_fwd_inst_ff.cu", "scan_bwd.cu", "conv.cu")
+
+
 def kernel_sources_sha() -> str:
-    """sha256 (first 16 hex digits) of the CUDA sources of the library."""
-    import glob
+    """sha256 (first 16 hex digits) of the CUDA sources of the training step's kernels."""
     import hashlib
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "selective_state_space_147_b300", "csrc", "*"))):
-        if f.endswith((".cu", ".cuh", ".h")):
-            with open(f, "rb") as fh:
-                h.update(os.path.basename(f).encode() + b"\0" + fh.read())
+    for name in STEP_KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "selective_state_space_147_b300", "csrc", name), "rb") as fh:
+            h.update(name.encode() + b"\0" + fh.read())
     return h.hexdigest()[:16]
 
 
@@ -278,6 +283,52 @@ def step(L, g, ev=None):
                                            workspace=g.get("ws_cbwd"))
     if ev is not None:
         ev[4].record()
+
+
+def bench_ssd(L, device, cfg, reps: int = 10):
+    """Mamba-2 state-space-duality layer forward (ssm_ssd_fwd), bf16 in and out:
+    milliseconds per call, its algorithmic HBM bytes (x, dt, B, C in; out) and
+    tensor FLOPs of the chunked algorithm (C B^T, the masked product with x, C H
+    and the state update, full blocks, no operand splits) against the measured
+    copy bandwidth and bf16 tensor peak."""
+    import synthetic as S
+    b, T, H, P, N, G, Q = (cfg[k] for k in ("batch", "seqlen", "nheads", "headdim", "dstate", "ngroups", "chunk"))
+    g = S.ssd_inputs(S.config_seed(6), b, T, H, P, N, G, device=device)
+    out = torch.empty(b, T, H, P, dtype=torch.bfloat16, device=device)
+
+    def call():
+        L.ssm_ssd_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], D=g["D"], dt_bias=g["dt_bias"], out=out)
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(reps):
+        call()
+    e1.record(st)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    nbytes = b * T * (H * (2 * P * 2 + 2) + 2 * G * N * 2)
+    flops = b * H * T * (2 * Q * N + 2 * Q * P + 4 * N * P)
+    hbm, _ = measured_peaks()
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            tpk, tsrc = float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        tpk, tsrc = 1800.0, "fallback"
+    gbs, tfl = nbytes / (ms * 1e-3) / 1e9, flops / (ms * 1e-3) / 1e12
+    t_hbm, t_tc = nbytes / (hbm * 1e9), flops / (tpk * 1e12)
+    return {"workload": f"mamba2-2.7b-layer SSD forward (batch {b}, L {T}, {H} heads x {P}, d_state {N}, "
+                        f"{G} B/C group, chunk {Q}, bf16 in/out, inputs larger than L2)",
+            "ms": round(ms, 4), "tokens_per_s": round(b * T / (ms * 1e-3), 1),
+            "bytes": nbytes, "flops": flops,
+            "hbm_gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm, 4),
+            "tensor_tflops": round(tfl, 2), "tensor_frac": round(tfl / tpk, 4),
+            "bound": "hbm" if t_hbm >= t_tc else "tensor",
+            "roofline_frac": round(max(t_hbm, t_tc) / (ms * 1e-3), 4),
+            "peaks": f"HBM {hbm} GB/s, bf16 tensor {tpk} TFLOP/s ({tsrc}, burst)"}
 
 
 def bench_decode(L, device, cfg, reps: int):
@@ -458,6 +509,7 @@ def main(argv=None):
     ap.add_argument("--sample-channels", type=int, default=0, help="reference arm: channels per step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-ssd", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=6)
     ap.add_argument("--seqlen", type=int, default=0,
                     help="shorter sequence for small profiling captures (the headline uses the default)")
@@ -621,6 +673,11 @@ def main(argv=None):
         decode = bench_decode(L, device, dcfg, dcfg["steps"])
         decode["us_per_token_step"] = max_over_ranks(decode["us_per_token_step"], world, device)
 
+    ssd = None
+    if not args.no_ssd:
+        torch.cuda.empty_cache()
+        ssd = bench_ssd(L, device, SSD)
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(cfg, S.config_seed(2))
@@ -634,7 +691,7 @@ def main(argv=None):
             "roofline": roof, "kernels": kern,
             "fwd_gbs": kern["ssm_scan_fwd"]["roofline"]["hbm_gbs"],
             "fwd_channel_tokens_per_s": kern["ssm_scan_fwd"]["channel_tokens_per_s"],
-            "decode": decode, "cpu_baseline": cpu, "e2e": e2e,
+            "decode": decode, "ssd": ssd, "cpu_baseline": cpu, "e2e": e2e,
             "clocks": clocks, "gpu_launches": launches, "gpu": props.name,
         }
         print(json.dumps(line), flush=True)

@@ -390,6 +390,50 @@ typedef struct {
 
 SSM_API ssm_status ssm_decode_step(const ssm_decode_step_params* p, ssm_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Mamba-2 state-space-duality (SSD) layer, forward, by the chunked algorithm.
+ * world.lapla.si section 09 ("Mamba-2：两种算法"): A is one number per head times
+ * the identity; the layer is the product with a lower-triangular matrix whose
+ * (i, j) entry is C_i . B_j times the decay between steps j and i, evaluated in
+ * chunks -- matrix products inside a chunk, only the state passed between
+ * chunks (pnsm.cn overview, section "Mamba-2：状态空间对偶性").  The input enters
+ * scaled by the step size (Bbar = Delta B).  Per (b, head h), state H (N x P):
+ *
+ *   Delta_t = softplus(dt[b,t,h] + dt_bias[h])   (delta_softplus = 0: dt + dt_bias)
+ *   H       = exp(Delta_t A[h]) H + Delta_t B_t x_t^T
+ *   y_t     = C_t^T H + D[h] x_t
+ *
+ *   x      : (batch, seqlen, nheads, headdim) bf16, contiguous; headdim = 64
+ *   dt     : (batch, seqlen, nheads) bf16, contiguous
+ *   A      : (nheads) fp32, expected <= 0 (a decay); D, dt_bias: (nheads) fp32 or NULL
+ *   B, C   : (batch, seqlen, ngroups, dstate) bf16, contiguous; head h reads
+ *            group h / (nheads / ngroups); dstate in {16, 32, 64, 128}
+ *   h0     : (batch, nheads, dstate, headdim) fp32 or NULL (zero state)
+ *   final_state : same layout, written when not NULL
+ *   out    : (batch, seqlen, nheads, headdim), out_dtype (bf16 or fp32), contiguous
+ * x, B, C must be 16-byte aligned and out 8-byte aligned (SSM_ERR_MISALIGNED
+ * otherwise).  Contractions run on the tensor cores in bf16 with fp32
+ * accumulation; operands that are not inputs (decay-weighted C B^T, the state,
+ * decay-weighted B) are split into a bf16 value and a bf16 residual, so results
+ * carry about 16 significant bits.  No workspace; asynchronous on `stream`. */
+typedef struct {
+    int64_t batch, seqlen, nheads, headdim, dstate, ngroups;
+    const void* x;
+    const void* dt;
+    const float* A;
+    const void* B;
+    const void* C;
+    const float* D;
+    const float* dt_bias;
+    int delta_softplus;
+    ssm_dtype out_dtype;
+    const float* h0;
+    float* final_state;
+    void* out;
+} ssm_ssd_fwd_params;
+
+SSM_API ssm_status ssm_ssd_fwd(const ssm_ssd_fwd_params* p, ssm_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Human-readable name of a status code (static string). */
 SSM_API const char* ssm_status_string(ssm_status s);

@@ -13,7 +13,7 @@ _EXPORTS = {
     "causal_conv1d_silu", "causal_conv1d_silu_update", "lib", "ssm_scan_fwd",
     "ssm_scan_fwd_workspace_size", "ssm_state_update", "LIB_PATH", "launch_count",
     "ssm_scan_bwd", "ssm_scan_bwd_workspace_size", "checkpoint_buffer", "checkpoint_states",
-    "ssm_decode_step", "causal_conv1d_silu_bwd", "causal_conv1d_silu_bwd_workspace_size",
+    "ssm_decode_step", "causal_conv1d_silu_bwd", "causal_conv1d_silu_bwd_workspace_size", "ssm_ssd_fwd",
 }
 
 

@@ -139,6 +139,15 @@ class ConvUpdateParams(ctypes.Structure):
     ]
 
 
+class SsdFwdParams(ctypes.Structure):
+    _fields_ = [
+        ("batch", _i64), ("seqlen", _i64), ("nheads", _i64), ("headdim", _i64), ("dstate", _i64),
+        ("ngroups", _i64), ("x", _vp), ("dt", _vp), ("A", _vp), ("B", _vp), ("C", _vp), ("D", _vp),
+        ("dt_bias", _vp), ("delta_softplus", _int), ("out_dtype", _int), ("h0", _vp), ("final_state", _vp),
+        ("out", _vp),
+    ]
+
+
 _lib.ssm_scan_fwd_workspace_size.argtypes = [ctypes.POINTER(ScanFwdParams)]
 _lib.ssm_scan_fwd_workspace_size.restype = ctypes.c_size_t
 _lib.ssm_scan_fwd.argtypes = [ctypes.POINTER(ScanFwdParams), _vp, ctypes.c_size_t, _vp]
@@ -159,6 +168,8 @@ _lib.causal_conv1d_silu.argtypes = [ctypes.POINTER(ConvParams), _vp]
 _lib.causal_conv1d_silu.restype = _int
 _lib.causal_conv1d_silu_update.argtypes = [ctypes.POINTER(ConvUpdateParams), _vp]
 _lib.causal_conv1d_silu_update.restype = _int
+_lib.ssm_ssd_fwd.argtypes = [ctypes.POINTER(SsdFwdParams), _vp]
+_lib.ssm_ssd_fwd.restype = _int
 _lib.ssm_status_string.argtypes = [_int]
 _lib.ssm_status_string.restype = ctypes.c_char_p
 _lib.ssm_last_error.argtypes = []
@@ -612,3 +623,36 @@ def causal_conv1d_silu_update(state, x, weight, *, bias=None, out: Optional[torc
     p.weight, p.bias, p.state = _ptr(weight), _ptr(bias), _ptr(state)
     _check(_lib.causal_conv1d_silu_update(ctypes.byref(p), _stream(stream)))
     return out
+
+
+def ssm_ssd_fwd(x, dt, A, B, C, *, D=None, dt_bias=None, h0=None, delta_softplus: bool = True,
+                out: Optional[torch.Tensor] = None, out_dtype=None, return_final_state: bool = False,
+                final_state: Optional[torch.Tensor] = None, stream=None):
+    """Mamba-2 state-space-duality layer, forward (chunked, tensor cores).
+    x: (batch, L, H, 64) bf16; dt: (batch, L, H) bf16; A, D, dt_bias: (H,) f32;
+    B, C: (batch, L, G, N) bf16 with N in {16, 32, 64, 128}; h0: (batch, H, N, 64) f32.
+    Returns out (batch, L, H, 64) [, final_state (batch, H, N, 64) f32]."""
+    for name, t in (("x", x), ("dt", dt), ("B", B), ("C", C)):
+        _need_cuda(name, t)
+        if t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bfloat16 tensor")
+    A, D, dt_bias, h0 = _f32c("A", A), _f32c("D", D), _f32c("dt_bias", dt_bias), _f32c("h0", h0)
+    batch, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    if tuple(dt.shape) != (batch, L, H) or tuple(B.shape) != (batch, L, G, N) or tuple(C.shape) != tuple(B.shape):
+        raise ValueError("dt must be (batch, L, H) and B, C (batch, L, G, N)")
+    if out is None:
+        out = torch.empty(batch, L, H, P, dtype=_torch_dtype(out_dtype or torch.bfloat16), device=x.device)
+    elif not out.is_contiguous():
+        raise ValueError("out must be contiguous")
+    if return_final_state and final_state is None:
+        final_state = torch.empty(batch, H, N, P, dtype=torch.float32, device=x.device)
+    _f32c("final_state", final_state)
+    p = SsdFwdParams()
+    p.batch, p.seqlen, p.nheads, p.headdim, p.dstate, p.ngroups = batch, L, H, P, N, G
+    p.x, p.dt, p.A, p.B, p.C = _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C)
+    p.D, p.dt_bias, p.h0, p.final_state, p.out = _ptr(D), _ptr(dt_bias), _ptr(h0), _ptr(final_state), _ptr(out)
+    p.delta_softplus = 1 if delta_softplus else 0
+    p.out_dtype = _dtype_code(out.dtype)
+    _check(_lib.ssm_ssd_fwd(ctypes.byref(p), _stream(stream)))
+    return (out, final_state) if (return_final_state or final_state is not None) else out

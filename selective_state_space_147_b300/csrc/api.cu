@@ -283,6 +283,25 @@ ssm_status ssm_decode_step(const ssm_decode_step_params* p, ssm_stream_t stream)
     return ok();
 }
 
+ssm_status ssm_ssd_fwd(const ssm_ssd_fwd_params* p, ssm_stream_t stream) {
+    if (p == nullptr) return fail(SSM_ERR_INVALID_ARG, "params is NULL");
+    if (p->batch < 1 || p->seqlen < 0 || p->nheads < 1 || p->ngroups < 1)
+        return fail(SSM_ERR_INVALID_ARG, "bad sizes");
+    if (p->headdim != 64) return fail(SSM_ERR_UNSUPPORTED, "headdim=%lld (64 supported)", (long long)p->headdim);
+    if (p->dstate != 16 && p->dstate != 32 && p->dstate != 64 && p->dstate != 128)
+        return fail(SSM_ERR_UNSUPPORTED, "dstate=%lld (16, 32, 64 or 128 supported)", (long long)p->dstate);
+    if (p->nheads % p->ngroups != 0) return fail(SSM_ERR_INVALID_ARG, "ngroups must divide nheads");
+    if (p->batch * p->nheads > 0x7fffffffLL) return fail(SSM_ERR_UNSUPPORTED, "batch * nheads too large");
+    if (!dtype_ok(p->out_dtype)) return fail(SSM_ERR_INVALID_ARG, "unknown dtype");
+    if (!p->A || (p->seqlen > 0 && (!p->x || !p->dt || !p->B || !p->C || !p->out)))
+        return fail(SSM_ERR_INVALID_ARG, "x, dt, A, B, C and out are required");
+    if (p->seqlen > 0 && (((uintptr_t)p->x | (uintptr_t)p->B | (uintptr_t)p->C) % 16 != 0 || (uintptr_t)p->out % 8 != 0))
+        return fail(SSM_ERR_MISALIGNED, "x, B, C must be 16-byte aligned and out 8-byte aligned");
+    cudaError_t e = ssm::launch_ssd_fwd(p, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "ssm_ssd_fwd launch");
+    return ok();
+}
+
 ssm_status ssm_state_update(const ssm_state_update_params* p, ssm_stream_t stream) {
     if (p == nullptr) return fail(SSM_ERR_INVALID_ARG, "params is NULL");
     if (p->batch < 1 || p->dim < 1 || p->dstate < 1) return fail(SSM_ERR_INVALID_ARG, "bad sizes");

@@ -23,5 +23,6 @@ size_t conv_bwd_workspace_bytes(const ssm_conv_bwd_params* p);
 cudaError_t launch_conv1d_silu_bwd(const ssm_conv_bwd_params* p, void* ws, cudaStream_t st);
 cudaError_t launch_decode_step(const ssm_decode_step_params* p, cudaStream_t st);
 cudaError_t launch_state_update(const ssm_state_update_params* p, cudaStream_t st);
+cudaError_t launch_ssd_fwd(const ssm_ssd_fwd_params* p, cudaStream_t st);
 
 }  // namespace ssm

@@ -142,6 +142,7 @@ def rows_at(seed: int, stream: int, rows: Sequence[int], row_len: int,
 STREAM = {
     "u": 1, "dt": 2, "z": 3, "B": 4, "C": 5, "D": 6, "bias": 7, "w": 8,
     "dout": 9, "h0": 10, "conv_state": 11, "x": 12, "dhN": 13,
+    "ssd_x": 20, "ssd_dt": 21, "ssd_B": 22, "ssd_C": 23, "ssd_A": 24, "ssd_D": 25, "ssd_bias": 26, "ssd_h0": 27,
 }
 
 
@@ -182,6 +183,27 @@ def scan_inputs(seed: int, batch: int, dim: int, seqlen: int, dstate: int,
     g["bias"] = delta_bias(seed, dim, delta_range[0], delta_range[1], device)
     g["h0"] = normal(seed, STREAM["h0"], (batch, dim, dstate), torch.float32, device) if with_h0 else None
     g["dout"] = normal(seed, STREAM["dout"], (batch, dim, seqlen), dtype, device) if with_dout else None
+    return g
+
+
+def ssd_inputs(seed: int, batch: int, seqlen: int, nheads: int, headdim: int, dstate: int, ngroups: int = 1,
+               device="cpu", delta_range=(1e-3, 1e-1), with_h0: bool = False):
+    """Inputs of one Mamba-2 (state-space-duality) layer, in its token-major layouts:
+    x: (batch, L, H, P) bf16; dt: (batch, L, H) bf16; B, C: (batch, L, G, N) bf16,
+    all N(0, 1); A: (H,) f32 = -U with U log-uniform in [1, 16]; D: (H,) f32 N(0, 1);
+    dt_bias: (H,) f32 with softplus(dt_bias) log-uniform in ``delta_range``;
+    h0: (batch, H, N, P) f32 N(0, 1)."""
+    g = {}
+    g["x"] = normal(seed, STREAM["ssd_x"], (batch, seqlen, nheads, headdim), torch.bfloat16, device)
+    g["dt"] = normal(seed, STREAM["ssd_dt"], (batch, seqlen, nheads), torch.bfloat16, device)
+    g["B"] = normal(seed, STREAM["ssd_B"], (batch, seqlen, ngroups, dstate), torch.bfloat16, device)
+    g["C"] = normal(seed, STREAM["ssd_C"], (batch, seqlen, ngroups, dstate), torch.bfloat16, device)
+    uu = uniform(seed, STREAM["ssd_A"], (nheads,), torch.float64, device)
+    g["A"] = (-torch.exp(uu * math.log(16.0))).to(torch.float32)
+    g["D"] = normal(seed, STREAM["ssd_D"], (nheads,), torch.float32, device)
+    g["dt_bias"] = delta_bias(seed, nheads, delta_range[0], delta_range[1], device, stream=STREAM["ssd_bias"])
+    g["h0"] = (normal(seed, STREAM["ssd_h0"], (batch, nheads, dstate, headdim), torch.float32, device)
+               if with_h0 else None)
     return g
 
 

@@ -32,7 +32,7 @@ def test_header_declares_the_entry_points():
     for must in ("ssm_scan_fwd", "ssm_scan_fwd_workspace_size", "ssm_scan_bwd", "ssm_scan_bwd_workspace_size",
                  "ssm_state_update", "ssm_decode_step", "causal_conv1d_silu_bwd",
                  "causal_conv1d_silu", "causal_conv1d_silu_update", "ssm_status_string",
-                 "ssm_last_error", "ssm_abi_version"):
+                 "ssm_last_error", "ssm_abi_version", "ssm_ssd_fwd"):
         assert must in names
 
 
@@ -102,3 +102,23 @@ def test_host_validation_without_gpu():
     assert lib.ssm_decode_step(ctypes.byref(ds), None) == -1           # missing pointers
     ds.width = 5
     assert lib.ssm_decode_step(ctypes.byref(ds), None) == -2           # width > 4
+
+
+def test_ssd_host_validation_without_gpu():
+    """ssm_ssd_fwd rejects bad shapes, unsupported sizes, missing pointers and
+    misaligned buffers on the host."""
+    import selective_state_space_147_b300.binding as B
+    lib = B.lib()
+    assert lib.ssm_ssd_fwd(None, None) == -1
+    p = B.SsdFwdParams()
+    p.batch, p.seqlen, p.nheads, p.headdim, p.dstate, p.ngroups = 1, 64, 2, 64, 16, 1
+    assert lib.ssm_ssd_fwd(ctypes.byref(p), None) == -1                 # missing pointers
+    p.x = p.dt = p.A = p.B = p.C = p.out = 256
+    p.headdim = 32
+    assert lib.ssm_ssd_fwd(ctypes.byref(p), None) == -2                 # head dim 64 only
+    p.headdim, p.dstate = 64, 48
+    assert lib.ssm_ssd_fwd(ctypes.byref(p), None) == -2                 # dstate 16/32/64/128
+    p.dstate, p.ngroups = 16, 3
+    assert lib.ssm_ssd_fwd(ctypes.byref(p), None) == -1                 # groups must divide heads
+    p.ngroups, p.x = 1, 264
+    assert lib.ssm_ssd_fwd(ctypes.byref(p), None) == -3                 # x not 16-byte aligned

@@ -1,0 +1,111 @@
+"""ssm_ssd_fwd (Mamba-2 state-space-duality layer, chunked on the tensor cores)
+against the fp64 oracle's recurrence, on seeded inputs: several chunks with a
+ragged tail, one exact chunk, every supported state size, B/C groups, an
+initial and a final state, softplus on and off, fp32 and bf16 outputs, the
+degenerate lengths, and sampled heads of the Mamba-2-2.7B-shaped layer the
+benchmark times.  Inputs are bf16 with an fp32 state, so the bound is
+2e-3 max|ref| (the products keep about 16 bits; errors are far below it)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic as S
+from helpers import TOL_BF16, assert_close, rel_err, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+def _lib():
+    import selective_state_space_147_b300 as L
+    return L
+
+
+def _run_oracle(g, softplus=True, threads=4):
+    return oracle.ssd_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"], g["dt_bias"], g["h0"],
+                          delta_softplus=softplus, threads=threads)
+
+
+@pytest.mark.parametrize("b,L,H,N,G,h0,out_dtype", [
+    (2, 200, 4, 16, 1, False, torch.float32),     # three chunks and a ragged tail of 8
+    (1, 64, 2, 32, 2, True, torch.float32),       # exactly one chunk, two groups, initial state
+    (2, 130, 4, 64, 2, True, torch.bfloat16),     # bf16 output
+    (1, 257, 2, 128, 1, True, torch.float32),     # largest state, tail of one step
+    (3, 1, 3, 16, 3, True, torch.float32),        # a single step, one head per group
+])
+def test_ssd_matches_oracle(b, L, H, N, G, h0, out_dtype):
+    Lb = _lib()
+    g = S.ssd_inputs(S.config_seed(5) + L + N, b, L, H, 64, N, G, device="cuda", with_h0=h0)
+    y, hN = Lb.ssm_ssd_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], D=g["D"], dt_bias=g["dt_bias"], h0=g["h0"],
+                           out_dtype=out_dtype, return_final_state=True)
+    torch.cuda.synchronize()
+    ref, href = _run_oracle(g)
+    assert_close(y, ref, torch.bfloat16, out_dtype, what="out")
+    assert_close(hN, href, torch.bfloat16, torch.float32, what="final state")
+
+
+def test_ssd_without_softplus_and_without_D():
+    Lb = _lib()
+    g = S.ssd_inputs(S.config_seed(5) + 1, 2, 150, 2, 64, 32, 1, device="cuda")
+    # positive step sizes given directly
+    g["dt"] = (g["dt"].float().abs() * 0.05 + 1e-3).to(torch.bfloat16)
+    g["dt_bias"] = None
+    g["D"] = None
+    y = Lb.ssm_ssd_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], delta_softplus=False, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    ref, _ = _run_oracle(g, softplus=False)
+    assert_close(y, ref, torch.bfloat16, torch.float32, what="out")
+
+
+def test_ssd_chunked_calls_compose():
+    """Running [0, 128) and then [128, 300) from the first call's final state equals one call."""
+    Lb = _lib()
+    g = S.ssd_inputs(S.config_seed(5) + 2, 1, 300, 2, 64, 64, 1, device="cuda", with_h0=True)
+    kw = dict(D=g["D"], dt_bias=g["dt_bias"], out_dtype=torch.float32, return_final_state=True)
+    y, hN = Lb.ssm_ssd_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], h0=g["h0"], **kw)
+    m = 128
+    cut = lambda t, s: t[:, s].contiguous()
+    y1, h1 = Lb.ssm_ssd_fwd(cut(g["x"], slice(0, m)), cut(g["dt"], slice(0, m)), g["A"], cut(g["B"], slice(0, m)),
+                            cut(g["C"], slice(0, m)), h0=g["h0"], **kw)
+    y2, h2 = Lb.ssm_ssd_fwd(cut(g["x"], slice(m, None)), cut(g["dt"], slice(m, None)), g["A"],
+                            cut(g["B"], slice(m, None)), cut(g["C"], slice(m, None)), h0=h1, **kw)
+    torch.cuda.synchronize()
+    assert rel_err(to_np(torch.cat([y1, y2], dim=1)), to_np(y)) <= 1e-4
+    assert rel_err(to_np(h2), to_np(hN)) <= 1e-4
+
+
+def test_ssd_zero_length_copies_the_initial_state():
+    Lb = _lib()
+    g = S.ssd_inputs(S.config_seed(5) + 3, 2, 0, 2, 64, 16, 1, device="cuda", with_h0=True)
+    y, hN = Lb.ssm_ssd_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], D=g["D"], dt_bias=g["dt_bias"], h0=g["h0"],
+                           return_final_state=True)
+    torch.cuda.synchronize()
+    assert y.numel() == 0
+    assert torch.equal(hN, g["h0"])
+
+
+def test_ssd_is_deterministic():
+    Lb = _lib()
+    g = S.ssd_inputs(S.config_seed(5) + 4, 2, 190, 4, 64, 128, 2, device="cuda")
+    y1 = Lb.ssm_ssd_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], D=g["D"], dt_bias=g["dt_bias"])
+    y2 = Lb.ssm_ssd_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], D=g["D"], dt_bias=g["dt_bias"])
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
+
+
+def test_ssd_full_size_sampled_heads():
+    """Mamba-2-2.7B-shaped layer (batch 8, L 2048, 80 heads of 64, N 128), bf16
+    output as the benchmark times it; the oracle recomputes sampled (b, h) pairs."""
+    Lb = _lib()
+    b, L, H, N = 8, 2048, 80, 128
+    g = S.ssd_inputs(S.config_seed(6), b, L, H, 64, N, 1, device="cuda")
+    y = Lb.ssm_ssd_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], D=g["D"], dt_bias=g["dt_bias"])
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(3)
+    for unit in sorted(rng.choice(b * H, size=3, replace=False).tolist()):
+        bb, hh = divmod(unit, H)
+        one = dict(x=g["x"][bb:bb + 1, :, hh:hh + 1].cpu(), dt=g["dt"][bb:bb + 1, :, hh:hh + 1].cpu(),
+                   B=g["B"][bb:bb + 1].cpu(), C=g["C"][bb:bb + 1].cpu(), A=g["A"][hh:hh + 1].cpu(),
+                   D=g["D"][hh:hh + 1].cpu(), dt_bias=g["dt_bias"][hh:hh + 1].cpu(), h0=None)
+        ref, _ = _run_oracle(one, threads=1)
+        assert_close(y[bb:bb + 1, :, hh:hh + 1], ref, torch.bfloat16, torch.bfloat16, what=f"unit {unit}")
