@@ -16,6 +16,13 @@
 
 namespace ssm {
 
+// d / cpg without a division: q = high 64 bits of d * m with m = floor((2^64 - 1) / cpg) + 1,
+// exact while d * cpg < 2^64 (d, cpg < 2^28 here); m = 0 encodes cpg = 1 (q = d).
+static uint64_t group_magic(int64_t cpg) { return cpg <= 1 ? 0ull : (~0ull / (uint64_t)cpg) + 1ull; }
+__device__ __forceinline__ int64_t group_of(int64_t d, uint64_t magic) {
+    return magic ? (int64_t)__umul64hi((uint64_t)d, magic) : d;
+}
+
 struct DecArgs {
     int64_t batch, dim;
     int dstate;
@@ -24,7 +31,8 @@ struct DecArgs {
     const float* A; const float* D; const float* bias;
     float* state;
     int softplus;
-    int64_t cpg, sBg, sCg;        // B/C groups: channel d reads group d / cpg
+    // B/C groups: channel d reads group d / cpg, computed as group_of(d, cpg_magic)
+    uint64_t cpg_magic; int64_t sBg, sCg;
 };
 
 template <typename Tin, typename Tout, bool ZOH, bool ACC>
@@ -50,8 +58,9 @@ __global__ void __launch_bounds__(256) state_update_kernel(const DecArgs a) {
         const int n = g + G * j;
         if (n < a.dstate) {
             const float Av = __ldg(a.A + d * a.dstate + n);
-            const float Bv = Elem<Tin>::load(reinterpret_cast<const Tin*>(a.B) + b * a.sB + (d / a.cpg) * a.sBg + n);
-            const float Cv = Elem<Tin>::load(reinterpret_cast<const Tin*>(a.C) + b * a.sC + (d / a.cpg) * a.sCg + n);
+            const int64_t grp = group_of(d, a.cpg_magic);
+            const float Bv = Elem<Tin>::load(reinterpret_cast<const Tin*>(a.B) + b * a.sB + grp * a.sBg + n);
+            const float Cv = Elem<Tin>::load(reinterpret_cast<const Tin*>(a.C) + b * a.sC + grp * a.sCg + n);
             const float x = dl * Av;
             float ab, coef;
             if (ACC) {
@@ -99,7 +108,7 @@ __global__ void __launch_bounds__(256) state_update16_kernel(const DecArgs a) {
     const float4 s0 = __ldcs(st), s1 = __ldcs(st + 1);
     const float4 a0 = __ldg(reinterpret_cast<const float4*>(a.A + d * 16 + g * 8));
     const float4 a1 = __ldg(reinterpret_cast<const float4*>(a.A + d * 16 + g * 8) + 1);
-    const int64_t grp = (a.cpg >= a.dim) ? 0 : (int)d / (int)a.cpg;   // one group: no division
+    const int64_t grp = group_of(d, a.cpg_magic);
     const uint4 bw = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.B) + b * a.sB + grp * a.sBg + g * 8));
     const uint4 cw = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.C) + b * a.sC + grp * a.sCg + g * 8));
     const float xt = Elem<__nv_bfloat16>::load(reinterpret_cast<const __nv_bfloat16*>(a.x) + b * a.sx + d);
@@ -147,7 +156,8 @@ struct DecStepArgs {
     const float* A; const float* D; const float* bias;
     float* state;
     int softplus;
-    int64_t cpg, sBg, sCg;        // B/C groups: channel d reads group d / cpg
+    // B/C groups: channel d reads group d / cpg, computed as group_of(d, cpg_magic)
+    uint64_t cpg_magic; int64_t sBg, sCg;
 };
 
 // Any layout: one thread per channel, every state and tap in a loop.
@@ -182,8 +192,9 @@ __global__ void __launch_bounds__(256) decode_step_kernel(const DecStepArgs a) {
     float y = 0.f;
     for (int n = 0; n < a.dstate; n++) {
         const float Av = __ldg(a.A + d * a.dstate + n);
-        const float Bv = Elem<Tin>::load(reinterpret_cast<const Tin*>(a.B) + b * a.sB + (d / a.cpg) * a.sBg + n);
-        const float Cv = Elem<Tin>::load(reinterpret_cast<const Tin*>(a.C) + b * a.sC + (d / a.cpg) * a.sCg + n);
+        const int64_t grp = group_of(d, a.cpg_magic);
+        const float Bv = Elem<Tin>::load(reinterpret_cast<const Tin*>(a.B) + b * a.sB + grp * a.sBg + n);
+        const float Cv = Elem<Tin>::load(reinterpret_cast<const Tin*>(a.C) + b * a.sC + grp * a.sCg + n);
         const float x = dl * Av;
         float ab, coef;
         if (ACC) {
@@ -226,7 +237,7 @@ __global__ void __launch_bounds__(256) decode_step16_kernel(const DecStepArgs a)
     const float4 a0 = __ldg(reinterpret_cast<const float4*>(a.A + d * 16 + g * 8));
     const float4 a1 = __ldg(reinterpret_cast<const float4*>(a.A + d * 16 + g * 8) + 1);
     const float4 cw = __ldg(reinterpret_cast<const float4*>(a.cw + d * 4));
-    const int64_t grp = (a.cpg >= a.dim) ? 0 : (int)d / (int)a.cpg;   // one group: no division
+    const int64_t grp = group_of(d, a.cpg_magic);
     const uint4 bw = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.B) + b * a.sB + grp * a.sBg + g * 8));
     const uint4 cwd = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.C) + b * a.sC + grp * a.sCg + g * 8));
     const uint32_t xbits = __ldg(reinterpret_cast<const unsigned short*>(a.x) + b * a.sx + d);
@@ -287,7 +298,7 @@ cudaError_t launch_decode_step(const ssm_decode_step_params* p, cudaStream_t st)
     a.cstate = p->conv_state; a.cw = p->conv_weight; a.cb = p->conv_bias;
     a.A = p->A; a.D = p->D; a.bias = p->delta_bias; a.state = p->state;
     a.softplus = p->delta_softplus ? 1 : 0;
-    a.cpg = p->ngroups > 1 ? p->dim / p->ngroups : p->dim;
+    a.cpg_magic = group_magic(p->ngroups > 1 ? p->dim / p->ngroups : p->dim);
     a.sBg = p->ngroups > 1 ? p->B_group_stride : 0;
     a.sCg = p->ngroups > 1 ? p->C_group_stride : 0;
     const bool zoh = p->bbar_mode == SSM_BBAR_ZOH;
@@ -335,7 +346,7 @@ cudaError_t launch_state_update(const ssm_state_update_params* p, cudaStream_t s
     a.sC = p->C_stride; a.so = p->out_stride;
     a.A = p->A; a.D = p->D; a.bias = p->delta_bias; a.state = p->state;
     a.softplus = p->delta_softplus ? 1 : 0;
-    a.cpg = p->ngroups > 1 ? p->dim / p->ngroups : p->dim;
+    a.cpg_magic = group_magic(p->ngroups > 1 ? p->dim / p->ngroups : p->dim);
     a.sBg = p->ngroups > 1 ? p->B_group_stride : 0;
     a.sCg = p->ngroups > 1 ? p->C_group_stride : 0;
     const bool zoh = p->bbar_mode == SSM_BBAR_ZOH;

@@ -21,7 +21,8 @@
 //   G = C B^T (64 x 64, k = N), then M = G o decay o Delta in registers, reused
 //   directly as the A operand of Y += M X (k = 64 steps);
 //   Y = C H (k = N) before that, rows scaled by exp(s_i);
-//   H' = (B o w)^T X (k = 64) with w_j = exp(s_last - s_j) Delta_j.
+//   H' = (B o w)^T X (k = 64) with w_j = exp(s_last - s_j) Delta_j, its A
+//   fragments built from the staged B rows.
 // Operands that are not bf16 inputs (M, H, w B) are split into a bf16 high part
 // and a bf16 residual and multiplied twice, so the products keep about 16
 // significant bits (the inputs themselves are exact in bf16).  x, B, C tiles
@@ -93,13 +94,11 @@ struct SsdSmem {
     static constexpr int N = 16 * NT;
     static constexpr int LDX = kQ + 8;      // Xt[p][j]
     static constexpr int LDBC = N + 8;      // Bs[j][n], Cs[i][n]
-    static constexpr int LDW = kQ + 8;      // W[n][j]
     static constexpr int LDH = N + 8;       // Ht[p][n]
     static constexpr int kXt = kP * LDX;
     static constexpr int kBC = kQ * LDBC;
-    static constexpr int kW = N * LDW;
     static constexpr int kH = kP * LDH;
-    static constexpr int kHalves = kXt + 2 * kBC + 2 * kW + 2 * kH;
+    static constexpr int kHalves = kXt + 2 * kBC + 2 * kH;
     static constexpr int kBytes = kHalves * 2 + 3 * kQ * 4;   // + Delta, s, w (fp32)
 };
 
@@ -111,9 +110,7 @@ __global__ void __launch_bounds__(kThreads) ssd_fwd_kernel(const SsdArgs a) {
     __nv_bfloat16* Xt = reinterpret_cast<__nv_bfloat16*>(smem_raw);
     __nv_bfloat16* Bs = Xt + L::kXt;
     __nv_bfloat16* Cs = Bs + L::kBC;
-    __nv_bfloat16* Wh = Cs + L::kBC;
-    __nv_bfloat16* Wl = Wh + L::kW;
-    __nv_bfloat16* Hh = Wl + L::kW;
+    __nv_bfloat16* Hh = Cs + L::kBC;
     __nv_bfloat16* Hl = Hh + L::kH;
     float* dlt = reinterpret_cast<float*>(Hl + L::kH);
     float* sc = dlt + kQ;
@@ -205,15 +202,6 @@ __global__ void __launch_bounds__(kThreads) ssd_fwd_kernel(const SsdArgs a) {
             wv[2 * lane + 1] = expf(last - incl) * dlt[2 * lane + 1];
         }
         __syncthreads();
-        // ---- W = (w o B)^T as bf16 high part and residual: W[n][j] = w_j B[j][n]
-        for (int idx = tid; idx < N * kQ; idx += kThreads) {
-            const int n = idx / kQ, j = idx - n * kQ;
-            const float v = wv[j] * __bfloat162float(Bs[j * L::LDBC + n]);
-            __nv_bfloat16 hi, lo;
-            split_bf16(v, hi, lo);
-            Wh[n * L::LDW + j] = hi;
-            Wl[n * L::LDW + j] = lo;
-        }
         // ---- outputs of this warp's 16 rows
         {
             const int i0 = 16 * warp;
@@ -314,8 +302,9 @@ __global__ void __launch_bounds__(kThreads) ssd_fwd_kernel(const SsdArgs a) {
                 }
             }
         }
-        __syncthreads();   // W complete; every warp has read the entering state
-        // ---- state: H' = exp(s_last) H + W X (W as high part + residual)
+        __syncthreads();   // every warp has read the entering state
+        // ---- state: H' = exp(s_last) H + W X with W[n][j] = w_j B[j][n], its A
+        // fragments built from the staged B rows (high part + residual)
         {
             const float dec = expf(sc[kQ - 1]);
 #pragma unroll
@@ -324,12 +313,22 @@ __global__ void __launch_bounds__(kThreads) ssd_fwd_kernel(const SsdArgs a) {
                 for (int e = 0; e < 4; e++) hacc[i][e] *= dec;
 #pragma unroll
             for (int kk = 0; kk < 4; kk++) {
+                uint32_t ah[4], al[4];
 #pragma unroll
                 for (int i = 0; i < 2 * NT; i++) {
                     const int q = warp * 2 * NT + i, mt = q >> 3, pt = q & 7;
-                    const int w0 = (mt * 16 + g) * L::LDW + kk * 16 + 2 * t4, w1 = w0 + 8 * L::LDW;
-                    uint32_t ah[4] = {ld32(Wh + w0), ld32(Wh + w1), ld32(Wh + w0 + 8), ld32(Wh + w1 + 8)};
-                    uint32_t al[4] = {ld32(Wl + w0), ld32(Wl + w1), ld32(Wl + w0 + 8), ld32(Wl + w1 + 8)};
+                    if (i % 8 == 0) {
+                        // a warp's tiles share one row block mt per run of 8 (2 NT = 2, 4: one run)
+                        const int n0 = mt * 16 + g, n1 = n0 + 8;
+                        const int j0 = kk * 16 + 2 * t4, j1 = j0 + 8;
+                        const float wa = wv[j0], wb = wv[j0 + 1], wc = wv[j1], wd = wv[j1 + 1];
+                        const __nv_bfloat16* r0 = Bs + j0 * L::LDBC;
+                        const __nv_bfloat16* r1 = Bs + j1 * L::LDBC;
+                        split2(wa * __bfloat162float(r0[n0]), wb * __bfloat162float(r0[L::LDBC + n0]), ah[0], al[0]);
+                        split2(wa * __bfloat162float(r0[n1]), wb * __bfloat162float(r0[L::LDBC + n1]), ah[1], al[1]);
+                        split2(wc * __bfloat162float(r1[n0]), wd * __bfloat162float(r1[L::LDBC + n0]), ah[2], al[2]);
+                        split2(wc * __bfloat162float(r1[n1]), wd * __bfloat162float(r1[L::LDBC + n1]), ah[3], al[3]);
+                    }
                     const int xrow = (pt * 8 + g) * L::LDX + kk * 16 + 2 * t4;
                     const uint32_t b0 = ld32(Xt + xrow), b1 = ld32(Xt + xrow + 8);
                     mma16816(hacc[i], ah, b0, b1);
