@@ -291,7 +291,7 @@ ssm_status ssm_ssd_fwd(const ssm_ssd_fwd_params* p, ssm_stream_t stream) {
     if (p->dstate != 16 && p->dstate != 32 && p->dstate != 64 && p->dstate != 128)
         return fail(SSM_ERR_UNSUPPORTED, "dstate=%lld (16, 32, 64 or 128 supported)", (long long)p->dstate);
     if (p->nheads % p->ngroups != 0) return fail(SSM_ERR_INVALID_ARG, "ngroups must divide nheads");
-    if (p->batch * p->nheads > 0x7fffffffLL) return fail(SSM_ERR_UNSUPPORTED, "batch * nheads too large");
+    if (p->batch * p->nheads > 0x3fffffffLL) return fail(SSM_ERR_UNSUPPORTED, "batch * nheads too large");
     if (!dtype_ok(p->out_dtype)) return fail(SSM_ERR_INVALID_ARG, "unknown dtype");
     if (!p->A || (p->seqlen > 0 && (!p->x || !p->dt || !p->B || !p->C || !p->out)))
         return fail(SSM_ERR_INVALID_ARG, "x, dt, A, B, C and out are required");

@@ -15,8 +15,10 @@
 //         + D x_i
 //   H'    = exp(s_last) H + sum_j exp(s_last - s_j) Delta_j B_j x_j^T
 //
-// Design for B300: one CTA of four warps per (b, h) walks the chunks in order
-// and keeps H in fp32 registers (mma accumulator fragments).  Every contraction
+// Design for B300: two CTAs of four warps per (b, h), each owning 32 of the 64
+// head-dimension columns (outputs and state columns; both form the full
+// C B^T), walk the chunks in order and keep their half of H in fp32 registers
+// (mma accumulator fragments).  Every contraction
 // is a bf16 m16n8k16 tensor-core MMA with fp32 accumulation:
 //   G = C B^T (64 x 64, k = N), then M = G o decay o Delta in registers, reused
 //   directly as the A operand of Y += M X (k = 64 steps);
@@ -42,6 +44,8 @@ namespace {
 
 constexpr int kQ = 64;            // chunk length (steps)
 constexpr int kP = 64;            // head dimension
+constexpr int kPC = 32;           // head-dimension columns per CTA (two CTAs per head)
+constexpr int kPT = kPC / 8;      // 8-column MMA tiles per CTA
 constexpr int kThreads = 128;     // four warps
 
 __device__ __forceinline__ uint32_t ld32(const __nv_bfloat16* p) { return *reinterpret_cast<const uint32_t*>(p); }
@@ -95,9 +99,9 @@ struct SsdSmem {
     static constexpr int LDX = kQ + 8;      // Xt[p][j]
     static constexpr int LDBC = N + 8;      // Bs[j][n], Cs[i][n]
     static constexpr int LDH = N + 8;       // Ht[p][n]
-    static constexpr int kXt = kP * LDX;
+    static constexpr int kXt = kPC * LDX;
     static constexpr int kBC = kQ * LDBC;
-    static constexpr int kH = kP * LDH;
+    static constexpr int kH = kPC * LDH;
     static constexpr int kHalves = kXt + 2 * kBC + 2 * kH;
     static constexpr int kBytes = kHalves * 2 + 3 * kQ * 4;   // + Delta, s, w (fp32)
 };
@@ -118,7 +122,8 @@ __global__ void __launch_bounds__(kThreads) ssd_fwd_kernel(const SsdArgs a) {
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t4 = lane & 3;
-    const int64_t unit = blockIdx.x;                     // (b, h)
+    const int64_t unit = blockIdx.x >> 1;                // (b, h)
+    const int p0 = (int)(blockIdx.x & 1) * kPC;          // this CTA's head-dimension columns
     const int64_t H = a.nheads;
     const int64_t b = unit / H, h = unit - b * H;
     const int64_t grp = h / (H / a.ngroups);
@@ -126,15 +131,16 @@ __global__ void __launch_bounds__(kThreads) ssd_fwd_kernel(const SsdArgs a) {
     const float Dh = a.D ? __ldg(a.D + h) : 0.f;
     const float bias = a.dt_bias ? __ldg(a.dt_bias + h) : 0.f;
 
-    // state tiles owned by this warp: q = warp * 2NT + i -> rows n in [16 (q / 8), +16), cols p in [8 (q % 8), +8)
-    float hacc[2 * NT][4];
+    // state tiles owned by this warp: q = warp * NT + i -> rows n in [16 (q / kPT), +16),
+    // local columns in [8 (q % kPT), +8)
+    float hacc[NT][4];
 #pragma unroll
-    for (int i = 0; i < 2 * NT; i++) {
-        const int q = warp * 2 * NT + i, mt = q >> 3, pt = q & 7;
+    for (int i = 0; i < NT; i++) {
+        const int q = warp * NT + i, mt = q / kPT, pt = q % kPT;
 #pragma unroll
         for (int e = 0; e < 4; e++) {
             const int n = mt * 16 + g + ((e & 2) ? 8 : 0), p = pt * 8 + 2 * t4 + (e & 1);
-            hacc[i][e] = a.h0 ? __ldg(a.h0 + (unit * N + n) * kP + p) : 0.f;
+            hacc[i][e] = a.h0 ? __ldg(a.h0 + (unit * N + n) * kP + p0 + p) : 0.f;
             __nv_bfloat16 hi, lo;
             split_bf16(hacc[i][e], hi, lo);
             Hh[p * L::LDH + n] = hi;
@@ -148,14 +154,14 @@ __global__ void __launch_bounds__(kThreads) ssd_fwd_kernel(const SsdArgs a) {
         __syncthreads();   // the previous chunk is done with every tile
         // ---- stage x (transposed), B, C rows and Delta of the chunk; zero past L
         {
-            // x: 64 rows of 64 bf16 = 8 x 16 bytes each; thread -> (row, 16-byte chunk) pairs
+            // x: 64 rows of this CTA's 32 bf16 = 4 x 16 bytes each; thread -> (row, 16-byte chunk) pairs
 #pragma unroll
-            for (int k = 0; k < (kQ * 8) / kThreads; k++) {
+            for (int k = 0; k < (kQ * kPT) / kThreads; k++) {
                 const int idx = k * kThreads + tid;
-                const int j = idx >> 3, ch = idx & 7;
+                const int j = idx / kPT, ch = idx % kPT;
                 uint4 v = make_uint4(0, 0, 0, 0);
                 if (t0 + j < a.seqlen)
-                    v = *reinterpret_cast<const uint4*>(a.x + ((b * a.seqlen + t0 + j) * H + h) * kP + ch * 8);
+                    v = *reinterpret_cast<const uint4*>(a.x + ((b * a.seqlen + t0 + j) * H + h) * kP + p0 + ch * 8);
                 const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                 for (int q = 0; q < 4; q++) {
@@ -206,9 +212,9 @@ __global__ void __launch_bounds__(kThreads) ssd_fwd_kernel(const SsdArgs a) {
         {
             const int i0 = 16 * warp;
             const int r0 = i0 + g, r1 = i0 + g + 8;
-            float yacc[8][4];
+            float yacc[kPT][4];
 #pragma unroll
-            for (int pt = 0; pt < 8; pt++)
+            for (int pt = 0; pt < kPT; pt++)
 #pragma unroll
                 for (int e = 0; e < 4; e++) yacc[pt][e] = 0.f;
             // inter-chunk: C H (H as high part + residual), rows scaled by exp(s_i)
@@ -220,7 +226,7 @@ __global__ void __launch_bounds__(kThreads) ssd_fwd_kernel(const SsdArgs a) {
                 af[2] = ld32(Cs + r0 * L::LDBC + kk * 16 + 2 * t4 + 8);
                 af[3] = ld32(Cs + r1 * L::LDBC + kk * 16 + 2 * t4 + 8);
 #pragma unroll
-                for (int pt = 0; pt < 8; pt++) {
+                for (int pt = 0; pt < kPT; pt++) {
                     const int prow = (pt * 8 + g) * L::LDH + kk * 16 + 2 * t4;
                     mma16816(yacc[pt], af, ld32(Hh + prow), ld32(Hh + prow + 8));
                     mma16816(yacc[pt], af, ld32(Hl + prow), ld32(Hl + prow + 8));
@@ -229,7 +235,7 @@ __global__ void __launch_bounds__(kThreads) ssd_fwd_kernel(const SsdArgs a) {
             {
                 const float e0 = expf(sc[r0]), e1 = expf(sc[r1]);
 #pragma unroll
-                for (int pt = 0; pt < 8; pt++) {
+                for (int pt = 0; pt < kPT; pt++) {
                     yacc[pt][0] *= e0; yacc[pt][1] *= e0;
                     yacc[pt][2] *= e1; yacc[pt][3] *= e1;
                 }
@@ -275,7 +281,7 @@ __global__ void __launch_bounds__(kThreads) ssd_fwd_kernel(const SsdArgs a) {
                     split2(gacc[2 * kk + 1][0], gacc[2 * kk + 1][1], ah[2], al[2]);
                     split2(gacc[2 * kk + 1][2], gacc[2 * kk + 1][3], ah[3], al[3]);
 #pragma unroll
-                    for (int pt = 0; pt < 8; pt++) {
+                    for (int pt = 0; pt < kPT; pt++) {
                         const int xrow = (pt * 8 + g) * L::LDX + kk * 16 + 2 * t4;
                         const uint32_t b0 = ld32(Xt + xrow), b1 = ld32(Xt + xrow + 8);
                         mma16816(yacc[pt], ah, b0, b1);
@@ -288,9 +294,9 @@ __global__ void __launch_bounds__(kThreads) ssd_fwd_kernel(const SsdArgs a) {
             for (int half = 0; half < 2; half++) {
                 const int i = half ? r1 : r0;
                 if (t0 + i >= a.seqlen) continue;
-                Tout* orow = reinterpret_cast<Tout*>(a.out) + ((b * a.seqlen + t0 + i) * H + h) * kP;
+                Tout* orow = reinterpret_cast<Tout*>(a.out) + ((b * a.seqlen + t0 + i) * H + h) * kP + p0;
 #pragma unroll
-                for (int pt = 0; pt < 8; pt++) {
+                for (int pt = 0; pt < kPT; pt++) {
                     const int p = pt * 8 + 2 * t4;
                     const float v0 = yacc[pt][2 * half] + Dh * __bfloat162float(Xt[p * L::LDX + i]);
                     const float v1 = yacc[pt][2 * half + 1] + Dh * __bfloat162float(Xt[(p + 1) * L::LDX + i]);
@@ -308,17 +314,17 @@ __global__ void __launch_bounds__(kThreads) ssd_fwd_kernel(const SsdArgs a) {
         {
             const float dec = expf(sc[kQ - 1]);
 #pragma unroll
-            for (int i = 0; i < 2 * NT; i++)
+            for (int i = 0; i < NT; i++)
 #pragma unroll
                 for (int e = 0; e < 4; e++) hacc[i][e] *= dec;
 #pragma unroll
             for (int kk = 0; kk < 4; kk++) {
                 uint32_t ah[4], al[4];
 #pragma unroll
-                for (int i = 0; i < 2 * NT; i++) {
-                    const int q = warp * 2 * NT + i, mt = q >> 3, pt = q & 7;
-                    if (i % 8 == 0) {
-                        // a warp's tiles share one row block mt per run of 8 (2 NT = 2, 4: one run)
+                for (int i = 0; i < NT; i++) {
+                    const int q = warp * NT + i, mt = q / kPT, pt = q % kPT;
+                    if (i % kPT == 0) {
+                        // a warp's tiles share one row block mt per run of kPT (NT = 1, 2: one run)
                         const int n0 = mt * 16 + g, n1 = n0 + 8;
                         const int j0 = kk * 16 + 2 * t4, j1 = j0 + 8;
                         const float wa = wv[j0], wb = wv[j0 + 1], wc = wv[j1], wd = wv[j1 + 1];
@@ -337,8 +343,8 @@ __global__ void __launch_bounds__(kThreads) ssd_fwd_kernel(const SsdArgs a) {
             }
             // the new state as the next chunk's B operand (transposed, high part + residual)
 #pragma unroll
-            for (int i = 0; i < 2 * NT; i++) {
-                const int q = warp * 2 * NT + i, mt = q >> 3, pt = q & 7;
+            for (int i = 0; i < NT; i++) {
+                const int q = warp * NT + i, mt = q / kPT, pt = q % kPT;
 #pragma unroll
                 for (int e = 0; e < 4; e++) {
                     const int n = mt * 16 + g + ((e & 2) ? 8 : 0), p = pt * 8 + 2 * t4 + (e & 1);
@@ -352,12 +358,12 @@ __global__ void __launch_bounds__(kThreads) ssd_fwd_kernel(const SsdArgs a) {
     }
     if (a.final_state != nullptr) {
 #pragma unroll
-        for (int i = 0; i < 2 * NT; i++) {
-            const int q = warp * 2 * NT + i, mt = q >> 3, pt = q & 7;
+        for (int i = 0; i < NT; i++) {
+            const int q = warp * NT + i, mt = q / kPT, pt = q % kPT;
 #pragma unroll
             for (int e = 0; e < 4; e++) {
                 const int n = mt * 16 + g + ((e & 2) ? 8 : 0), p = pt * 8 + 2 * t4 + (e & 1);
-                a.final_state[(unit * N + n) * kP + p] = hacc[i][e];
+                a.final_state[(unit * N + n) * kP + p0 + p] = hacc[i][e];
             }
         }
     }
@@ -368,7 +374,7 @@ cudaError_t launch_ssd_typed(const SsdArgs& a, cudaStream_t st) {
     const int bytes = SsdSmem<NT>::kBytes;
     cudaError_t e = cudaFuncSetAttribute(ssd_fwd_kernel<NT, Tout>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
-    ssd_fwd_kernel<NT, Tout><<<(unsigned)(a.batch * a.nheads), kThreads, bytes, st>>>(a);
+    ssd_fwd_kernel<NT, Tout><<<(unsigned)(2 * a.batch * a.nheads), kThreads, bytes, st>>>(a);
     count_launches(1);
     return cudaGetLastError();
 }
