@@ -285,6 +285,30 @@ def step(L, g, ev=None):
         ev[4].record()
 
 
+def ssd_cpu_baseline(cfg, heads: int = 0):
+    """The fp64 oracle's SSD recurrence on a bounded sample of the same layer: the
+    first ``heads`` heads (all by default) of batch row 0 over the full sequence,
+    heads split over the host threads; reported as tokens/s of the whole layer."""
+    import time
+    import oracle
+    import synthetic as S
+    T, H, P, N, G = (cfg[k] for k in ("seqlen", "nheads", "headdim", "dstate", "ngroups"))
+    heads = heads or H
+    g = S.ssd_inputs(S.config_seed(6), 1, T, H, P, N, G)
+    one = {k: (v[:, :, :heads] if k in ("x", "dt") else v[:heads] if k in ("A", "D", "dt_bias") else v)
+           for k, v in g.items() if v is not None}
+    threads = min(heads, oracle.default_threads())
+    if G > 1 and heads != H:
+        raise ValueError("a sample of heads keeps each head's B/C group only with one group")
+    t0 = time.perf_counter()
+    oracle.ssd_fwd(one["x"], one["dt"], one["A"], one["B"], one["C"], one["D"], one["dt_bias"],
+                   threads=threads)
+    wall = time.perf_counter() - t0
+    return {"value": round(T * heads / H / wall, 1), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{heads} of {H} heads of batch row 0, full L={T}, fp64 recurrence ({wall:.2f} s wall "
+                      f"on {threads} threads)"}
+
+
 def bench_ssd(L, device, cfg, reps: int = 10):
     """Mamba-2 state-space-duality layer forward (ssm_ssd_fwd), bf16 in and out:
     milliseconds per call, its algorithmic HBM bytes (x, dt, B, C in; out) and
@@ -677,6 +701,8 @@ def main(argv=None):
     if not args.no_ssd:
         torch.cuda.empty_cache()
         ssd = bench_ssd(L, device, SSD)
+        if rank == 0 and not args.no_cpu_baseline:
+            ssd["cpu_baseline"] = ssd_cpu_baseline(SSD)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
