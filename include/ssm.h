@@ -63,7 +63,7 @@ typedef struct CUstream_st* ssm_stream_t;
 typedef enum {
     SSM_OK = 0,
     SSM_ERR_INVALID_ARG = -1, /* a NULL required pointer, a negative size, ... */
-    SSM_ERR_UNSUPPORTED = -2, /* a valid request this build does not implement */
+    SSM_ERR_UNSUPPORTED = -2, /* a valid request this library does not implement */
     SSM_ERR_MISALIGNED = -3,  /* a pointer that must be aligned (workspace, checkpoints) is not */
     SSM_ERR_WORKSPACE = -4,   /* workspace missing or smaller than required */
     SSM_ERR_CUDA = -5         /* a CUDA runtime error (see ssm_last_error) */
