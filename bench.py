@@ -49,9 +49,9 @@ SSD = dict(batch=8, seqlen=2048, nheads=80, headdim=64, dstate=128, ngroups=1, c
 # capture at batch 8, d_inner 4096, L 2048 (the command is in profiles/).  The
 # figures hold only while the step's kernel sources hash to TRAFFIC_SOURCES_SHA;
 # after any change to them the traffic is reported as null until it is captured again.
-TRAFFIC_PER_CT = {"ssm_scan_bwd": 35.08, "ssm_scan_fwd": 23.17, "causal_conv1d_silu": 3.19,
-                  "causal_conv1d_silu_bwd": 5.50}
-TRAFFIC_SOURCES_SHA = "07498381fee3b7c2"
+TRAFFIC_PER_CT = {"ssm_scan_bwd": 37.87, "ssm_scan_fwd": 23.17, "causal_conv1d_silu": 3.20,
+                  "causal_conv1d_silu_bwd": 5.51}
+TRAFFIC_SOURCES_SHA = "eba2b381b3037ed6"
 
 SM_FP32_LANES = 128     # FP32 lanes per SM per clock (sm_100 family)
 SM_SFU_EX2 = 32         # MUFU ex2 results per SM per clock on B300 (measured 29.8 at ~2 GHz)

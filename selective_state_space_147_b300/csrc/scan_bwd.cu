@@ -9,15 +9,16 @@
 //   y_t = C_t . h_t + D u_t,  out_t = y_t silu(z_t),
 // with the adjoint G_t = dL/dh_t = dy_t C_t + Abar_{t+1} G_{t+1}.
 //
-// Schedule (B300): checkpoints of h every 8 steps (written by ssm_scan_fwd, or
-// by a checkpoint-only forward pass into the workspace) let every 8-step
-// sub-block be recomputed exactly once, forward, into a per-warp shared-memory
-// buffer of h, and then walked in reverse.  One thread owns one channel and
-// its 16 states in registers; a CTA of 4 warps covers 128 channels of one
+// Schedule (B300): checkpoints of h every 4 steps (written by ssm_scan_fwd, or
+// by a checkpoint-only forward pass into the workspace) let every sub-block
+// (4 steps in the fast kernel, 8 in the accurate one, which reads every second
+// checkpoint) be recomputed exactly once, forward, and then walked in reverse.
+// One thread owns one channel and its 16 states in registers; a CTA covers 64
+// (fast kernel, 2 warps) or 128 (accurate kernel, 4 warps) channels of one
 // batch row and shares the fp32 B/C tile.  The cross-channel sums dB, dC are
 // reduced deterministically: a shared-memory transpose inside each warp, a
-// fixed-order sum over the 4 warps, one partial per CTA in the workspace, and
-// a second kernel that sums the CTA partials in order.  dA, dD and dbias are
+// fixed-order sum over warps into one partial per 64 channels in the
+// workspace, and a second kernel that sums the partials in order.  dA, dD and dbias are
 // per-(b, d) partials summed over the batch by a third kernel.  No atomics:
 // results are bitwise reproducible.
 #include <cstdint>
@@ -28,6 +29,10 @@ namespace ssm {
 
 constexpr int kBwdWarps = 4;
 constexpr int kBwdThreads = 32 * kBwdWarps;
+// the fast kernel's CTA: its channel count is the granularity of the dB/dC partials
+constexpr int kFWarps = 2;
+constexpr int kFThreads = 32 * kFWarps;
+constexpr int kFChans = kFThreads;            // channels per CTA = per dB/dC partial
 constexpr int kBwdK = 4;                    // checkpoint interval the backward consumes
 constexpr int kAccCk = kSub / kBwdK;        // checkpoints per 8-step sub-block of the accurate kernel
 constexpr int kRed2 = 33;                   // padded row of the in-warp transpose
@@ -126,7 +131,6 @@ __device__ __forceinline__ void bwd_channel(const BwdArgs& a, float* sbc, float*
     Tg* durow = reinterpret_cast<Tg*>(a.du) + b * a.sdu_b + d * a.sdu_d;
     Tg* ddrow = reinterpret_cast<Tg*>(a.ddt) + b * a.sddt_b + d * a.sddt_d;
     Tg* dzrow = HAS_Z ? reinterpret_cast<Tg*>(a.dz) + b * a.sdz_b + d * a.sdz_d : nullptr;
-    // B/C group of the CTA's channels (groups span multiples of 128 channels)
     // B/C group of the CTA's channels (groups span multiples of 128 channels)
     const int64_t grp = (a.cpg >= a.dim) ? 0 : d / a.cpg;       // one group: no division
     const Tin* Bb = reinterpret_cast<const Tin*>(a.B) + b * a.sB_b + grp * a.sB_g;
@@ -284,13 +288,18 @@ __device__ __forceinline__ void bwd_channel(const BwdArgs& a, float* sbc, float*
         }
         // fixed-order sum over the CTA's warps -> one partial per CTA
         __syncthreads();
-        for (int idx = tid; idx < kSub * 32; idx += kBwdThreads) {
-            const int j = idx >> 5, v = idx & 31;
-            if (j < cnt) {
+        // the partials are laid out per kFChans channels (the fast kernel's CTA):
+        // this CTA fills kSlots of them, each the sum of kWps warps
+        constexpr int kSlots = kBwdThreads / kFChans, kWps = kBwdWarps / kSlots;
+        for (int idx = tid; idx < kSlots * kSub * 32; idx += kBwdThreads) {
+            const int sl = idx / (kSub * 32), r = idx % (kSub * 32);
+            const int j = r >> 5, v = r & 31;
+            const int64_t slot = (int64_t)blockIdx.x * kSlots + sl;
+            if (j < cnt && slot < a.nblk) {
                 float s = 0.f;
 #pragma unroll
-                for (int w = 0; w < kBwdWarps; w++) s += red[(w * kSub + j) * 32 + v];
-                a.part_bc[(((b * a.nblk + blockIdx.x) * 2 + (v >> 4)) * 16 + (v & 15)) * a.seqlen + t0 + j] = s;
+                for (int w = 0; w < kWps; w++) s += red[((sl * kWps + w) * kSub + j) * 32 + v];
+                a.part_bc[(((b * a.nblk + slot) * 2 + (v >> 4)) * 16 + (v & 15)) * a.seqlen + t0 + j] = s;
             }
         }
         __syncthreads();
@@ -308,7 +317,9 @@ __device__ __forceinline__ void bwd_channel(const BwdArgs& a, float* sbc, float*
 // ---------------------------------------------------------------------------
 // Fast (SFU) backward for bf16 inputs.
 //
-// One thread per channel (a CTA of 4 warps covers 128 channels), the sequence
+// One thread per channel (a CTA of 2 warps covers 64 channels: with 255
+// registers four such CTAs fit an SM, which balances 32768 channels over 148
+// SMs better than 128-channel CTAs), the sequence
 // walked backwards in 4-step sub-blocks, one per forward checkpoint.  The
 // adjoint recurrence G_t = dy_t C_t + Abar_{t+1} G_{t+1} is independent per
 // state, so state pairs are the outer loop, two at a time for instruction-level
@@ -318,15 +329,12 @@ __device__ __forceinline__ void bwd_channel(const BwdArgs& a, float* sbc, float*
 // the gate, the readout y that dz needs) live across pairs, as packed f32x2
 // accumulators.  After each couple of pairs the lane's 32 dB/dC partials
 // (4 steps x 4 states x 2 tensors) are summed over the warp's 32 channels
-// through a shared-memory transpose, and once per sub-block the CTA's 4 warps
+// through a shared-memory transpose, and once per sub-block the CTA's warps
 // in a fixed order into one partial per CTA.  u, delta, dout, z rows (8 steps)
 // and the checkpoints arrive ahead by cp.async into shared memory.
 constexpr int kRowF = 36;                     // B/C row of one step: [pair: B B C C] x 8, pad
 constexpr int kRedF = 36;                     // transpose row (32 floats + pad, 16-byte aligned)
 constexpr int kFSub = kBwdK;                  // steps per sub-block (= checkpoint interval)
-constexpr int kFWarps = 4;
-constexpr int kFThreads = 32 * kFWarps;
-constexpr int kFChans = kFThreads;            // channels per CTA = per dB/dC partial
 constexpr int kFNP = 8;                       // state pairs per thread
 // shared memory (byte offsets)
 constexpr int kFOffRed = kTile * kRowF * 4;                      // float [2][warp][couple][32]
@@ -347,17 +355,21 @@ __device__ __forceinline__ void cp_async8(void* smem, const void* gmem) {
 template <typename Tin>
 __device__ __forceinline__ void stage_bc_pairs(float* sbc, const BwdArgs& a, const Tin* Bb, const Tin* Cb,
                                                int64_t t0, int tid) {
-    const int s = tid & 63, tsr = tid >> 6;
-    const int64_t t = t0 + s;
-    const Tin* base = tsr == 0 ? Bb : Cb;
-    const int64_t sn = tsr == 0 ? a.sB_n : a.sC_n;
-    float2* row = reinterpret_cast<float2*>(sbc + s * kRowF + tsr * 2);
 #pragma unroll
-    for (int p = 0; p < 8; p++) {
-        const int n = 2 * p;
-        const float v0 = (n < a.dstate && t < a.seqlen) ? Elem<Tin>::load(base + n * sn + t) : 0.f;
-        const float v1 = (n + 1 < a.dstate && t < a.seqlen) ? Elem<Tin>::load(base + (n + 1) * sn + t) : 0.f;
-        row[2 * p] = make_float2(v0, v1);
+    for (int k = 0; k < 128 / kFThreads; k++) {
+        const int idx = k * kFThreads + tid;
+        const int s = idx & 63, tsr = idx >> 6;
+        const int64_t t = t0 + s;
+        const Tin* base = tsr == 0 ? Bb : Cb;
+        const int64_t sn = tsr == 0 ? a.sB_n : a.sC_n;
+        float2* row = reinterpret_cast<float2*>(sbc + s * kRowF + tsr * 2);
+#pragma unroll
+        for (int p = 0; p < 8; p++) {
+            const int n = 2 * p;
+            const float v0 = (n < a.dstate && t < a.seqlen) ? Elem<Tin>::load(base + n * sn + t) : 0.f;
+            const float v1 = (n + 1 < a.dstate && t < a.seqlen) ? Elem<Tin>::load(base + (n + 1) * sn + t) : 0.f;
+            row[2 * p] = make_float2(v0, v1);
+        }
     }
 }
 
@@ -432,7 +444,6 @@ scan_bwd_fast_kernel(const BwdArgs a, const int* flag) {
     const Tin* drow = reinterpret_cast<const Tin*>(a.dt) + b * a.sdt_b + d * a.sdt_d;
     const Tin* zrow = HAS_Z ? reinterpret_cast<const Tin*>(a.z) + b * a.sz_b + d * a.sz_d : nullptr;
     const Tin* orow = reinterpret_cast<const Tin*>(a.dout) + b * a.sdo_b + d * a.sdo_d;
-    // B/C group of the CTA's channels (groups span multiples of 128 channels)
     // B/C group of the CTA's channels (groups span multiples of 128 channels)
     const int64_t grp = (a.cpg >= a.dim) ? 0 : d / a.cpg;       // one group: no division
     const Tin* Bb = reinterpret_cast<const Tin*>(a.B) + b * a.sB_b + grp * a.sB_g;
@@ -661,8 +672,10 @@ scan_bwd_fast_kernel(const BwdArgs a, const int* flag) {
         // fixed-order sum over the CTA's warps -> one partial per CTA; thread tid
         // handles (tensor, state n, step j) with j fastest
         __syncthreads();
-        {
-            const int j = tid & 3, n = (tid >> 2) & 15, tsr = tid >> 6;
+#pragma unroll
+        for (int k = 0; k < 128 / kFThreads; k++) {
+            const int idx = k * kFThreads + tid;
+            const int j = idx & 3, n = (idx >> 2) & 15, tsr = idx >> 6;
             if (j < cnt) {
                 const int f = 8 * j + 4 * ((n >> 1) & 1) + 2 * tsr + (n & 1);
                 const int l = ((f & 1) << 4) | (f >> 1);
