@@ -53,8 +53,22 @@ TRAFFIC_PER_CT = {"ssm_scan_bwd": 37.87, "ssm_scan_fwd": 23.17, "causal_conv1d_s
                   "causal_conv1d_silu_bwd": 5.51}
 TRAFFIC_SOURCES_SHA = "eba2b381b3037ed6"
 
-SM_FP32_LANES = 128     # FP32 lanes per SM per clock (sm_100 family)
-SM_SFU_EX2 = 32         # MUFU ex2 results per SM per clock on B300 (measured 29.8 at ~2 GHz)
+SM_FP32_LANES = 128     # FP32 lanes per SM per clock (sm_100 family), nominal
+SM_SFU_EX2 = 32         # MUFU ex2 results per SM per clock, nominal
+# per-SM unit rates used as roofline denominators: replaced by the library's
+# probe kernels' measurement (ssm_probe_unit_rates) when the benchmark runs
+UNIT_RATES = {"fp32": float(SM_FP32_LANES), "ex2": float(SM_SFU_EX2), "source": "nominal"}
+
+
+def measure_unit_rates(L):
+    """Run the library's probe kernels once and use their per-SM rates."""
+    try:
+        r = L.probe_unit_rates()
+    except Exception as exc:  # the nominal figures stay in use
+        return {"error": str(exc)}
+    UNIT_RATES.update(fp32=max(r["fp32_lanes_per_sm_clock"], r["f32x2_lanes_per_sm_clock"]),
+                      ex2=r["ex2_per_sm_clock"], source="measured (probe kernels, SM cycle counter)")
+    return {k: round(v, 2) for k, v in r.items()}
 FALLBACK_HBM_GBS = 6400.0
 
 
@@ -223,19 +237,20 @@ def roofline(work, seconds, hbm_gbs, sms, sm_mhz, hbm_src, clock_src):
     """Slowest of HBM, FP32 pipe and SFU for this kernel's algorithmic work."""
     f = sm_mhz * 1e6
     t_hbm = work["bytes"] / (hbm_gbs * 1e9)
-    t_fp32 = work["fp32"] / (sms * SM_FP32_LANES * f)
-    t_sfu = work["sfu"] / (sms * SM_SFU_EX2 * f)
+    lanes, ex2 = UNIT_RATES["fp32"], UNIT_RATES["ex2"]
+    t_fp32 = work["fp32"] / (sms * lanes * f)
+    t_sfu = work["sfu"] / (sms * ex2 * f)
     bound = max((t_hbm, "hbm"), (t_fp32, "alu"), (t_sfu, "sfu"))[1]
     if bound == "hbm":
         ach, peak, unit = work["bytes"] / seconds / 1e9, hbm_gbs, "GB/s"
         note = f"peak = HBM copy bandwidth, {hbm_src}"
     elif bound == "alu":
-        ach, peak, unit = work["fp32"] / seconds / 1e12, sms * SM_FP32_LANES * f / 1e12, "TFP32op/s"
-        note = (f"peak = {sms} SMs x {SM_FP32_LANES} FP32 lanes x {sm_mhz:.0f} MHz ({clock_src}); "
-                "one FP32 op = one FMA, MUL or ADD lane-instruction")
+        ach, peak, unit = work["fp32"] / seconds / 1e12, sms * lanes * f / 1e12, "TFP32op/s"
+        note = (f"peak = {sms} SMs x {lanes:.1f} FP32 lanes/clock ({UNIT_RATES['source']}) x {sm_mhz:.0f} MHz "
+                f"({clock_src}); one FP32 op = one FMA, MUL or ADD lane-instruction")
     else:
-        ach, peak, unit = work["sfu"] / seconds / 1e12, sms * SM_SFU_EX2 * f / 1e12, "TSFUop/s"
-        note = f"peak = {sms} SMs x {SM_SFU_EX2} SFU ops x {sm_mhz:.0f} MHz ({clock_src})"
+        ach, peak, unit = work["sfu"] / seconds / 1e12, sms * ex2 * f / 1e12, "TSFUop/s"
+        note = f"peak = {sms} SMs x {ex2:.1f} SFU ops/clock ({UNIT_RATES['source']}) x {sm_mhz:.0f} MHz ({clock_src})"
     return {"bound": "alu" if bound in ("alu", "sfu") else bound, "achieved": round(ach, 3),
             "peak": round(peak, 3), "unit": unit, "frac": round(ach / peak, 4),
             "hbm_gbs": round(work["bytes"] / seconds / 1e9, 1),
@@ -563,6 +578,7 @@ def main(argv=None):
                                device=device)
     props = torch.cuda.get_device_properties(device)
     sms = props.multi_processor_count
+    unit_rates = measure_unit_rates(L)
 
     for _ in range(max(3, args.warmup)):
         step(L, g)
@@ -718,7 +734,7 @@ def main(argv=None):
             "fwd_gbs": kern["ssm_scan_fwd"]["roofline"]["hbm_gbs"],
             "fwd_channel_tokens_per_s": kern["ssm_scan_fwd"]["channel_tokens_per_s"],
             "decode": decode, "ssd": ssd, "cpu_baseline": cpu, "e2e": e2e,
-            "clocks": clocks, "gpu_launches": launches, "gpu": props.name,
+            "clocks": clocks, "gpu_launches": launches, "gpu": props.name, "unit_rates": unit_rates,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -434,6 +434,18 @@ typedef struct {
 
 SSM_API ssm_status ssm_ssd_fwd(const ssm_ssd_fwd_params* p, ssm_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Measured unit rates for the roofline (not part of the method): FP32 lanes
+ * per SM per clock through scalar FMA and through packed f32x2 FMA, and SFU
+ * 2^x results per SM per clock, each from a probe kernel of independent
+ * dependency chains timed with the SM's cycle counter (so independent of the
+ * clock).  Runs on the calling thread's current device, synchronously; each
+ * output pointer (host memory) may be NULL to skip that probe.  Allocates
+ * nothing (cycle counts return through a device array built into the
+ * library).  SSM_ERR_CUDA if a launch fails. */
+SSM_API ssm_status ssm_probe_unit_rates(double* fp32_lanes_per_sm_clock, double* f32x2_lanes_per_sm_clock,
+                                        double* ex2_per_sm_clock);
+
 /* ------------------------------------------------------------------------ */
 /* Human-readable name of a status code (static string). */
 SSM_API const char* ssm_status_string(ssm_status s);

@@ -168,6 +168,8 @@ _lib.causal_conv1d_silu.argtypes = [ctypes.POINTER(ConvParams), _vp]
 _lib.causal_conv1d_silu.restype = _int
 _lib.causal_conv1d_silu_update.argtypes = [ctypes.POINTER(ConvUpdateParams), _vp]
 _lib.causal_conv1d_silu_update.restype = _int
+_lib.ssm_probe_unit_rates.argtypes = [ctypes.POINTER(ctypes.c_double)] * 3
+_lib.ssm_probe_unit_rates.restype = _int
 _lib.ssm_ssd_fwd.argtypes = [ctypes.POINTER(SsdFwdParams), _vp]
 _lib.ssm_ssd_fwd.restype = _int
 _lib.ssm_status_string.argtypes = [_int]
@@ -656,3 +658,12 @@ def ssm_ssd_fwd(x, dt, A, B, C, *, D=None, dt_bias=None, h0=None, delta_softplus
     p.out_dtype = _dtype_code(out.dtype)
     _check(_lib.ssm_ssd_fwd(ctypes.byref(p), _stream(stream)))
     return (out, final_state) if (return_final_state or final_state is not None) else out
+
+
+def probe_unit_rates() -> dict:
+    """Measured FP32 lanes per SM per clock (scalar FMA and packed f32x2 FMA) and
+    SFU 2^x results per SM per clock on the current device (synchronous)."""
+    v = [ctypes.c_double(0.0) for _ in range(3)]
+    _check(_lib.ssm_probe_unit_rates(*(ctypes.byref(x) for x in v)))
+    return {"fp32_lanes_per_sm_clock": v[0].value, "f32x2_lanes_per_sm_clock": v[1].value,
+            "ex2_per_sm_clock": v[2].value}

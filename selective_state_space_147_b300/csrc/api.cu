@@ -283,6 +283,12 @@ ssm_status ssm_decode_step(const ssm_decode_step_params* p, ssm_stream_t stream)
     return ok();
 }
 
+ssm_status ssm_probe_unit_rates(double* fp32, double* f32x2, double* ex2) {
+    cudaError_t e = ssm::probe_unit_rates(fp32, f32x2, ex2);
+    if (e != cudaSuccess) return cuda_fail(e, "ssm_probe_unit_rates");
+    return ok();
+}
+
 ssm_status ssm_ssd_fwd(const ssm_ssd_fwd_params* p, ssm_stream_t stream) {
     if (p == nullptr) return fail(SSM_ERR_INVALID_ARG, "params is NULL");
     if (p->batch < 1 || p->seqlen < 0 || p->nheads < 1 || p->ngroups < 1)

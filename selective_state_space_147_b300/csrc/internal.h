@@ -24,5 +24,6 @@ cudaError_t launch_conv1d_silu_bwd(const ssm_conv_bwd_params* p, void* ws, cudaS
 cudaError_t launch_decode_step(const ssm_decode_step_params* p, cudaStream_t st);
 cudaError_t launch_state_update(const ssm_state_update_params* p, cudaStream_t st);
 cudaError_t launch_ssd_fwd(const ssm_ssd_fwd_params* p, cudaStream_t st);
+cudaError_t probe_unit_rates(double* fp32, double* f32x2, double* ex2);
 
 }  // namespace ssm

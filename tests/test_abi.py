@@ -32,7 +32,7 @@ def test_header_declares_the_entry_points():
     for must in ("ssm_scan_fwd", "ssm_scan_fwd_workspace_size", "ssm_scan_bwd", "ssm_scan_bwd_workspace_size",
                  "ssm_state_update", "ssm_decode_step", "causal_conv1d_silu_bwd",
                  "causal_conv1d_silu", "causal_conv1d_silu_update", "ssm_status_string",
-                 "ssm_last_error", "ssm_abi_version", "ssm_ssd_fwd"):
+                 "ssm_last_error", "ssm_abi_version", "ssm_ssd_fwd", "ssm_probe_unit_rates"):
         assert must in names
 
 
