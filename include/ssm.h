@@ -142,6 +142,29 @@ SSM_API size_t ssm_scan_fwd_workspace_size(const ssm_scan_fwd_params* p);
 SSM_API ssm_status ssm_scan_fwd(const ssm_scan_fwd_params* p, void* workspace,
                         size_t workspace_bytes, ssm_stream_t stream);
 
+/* Schedule override of ssm_scan_fwd, for tests and tuning: the same
+ * computation with a forced schedule (results agree with ssm_scan_fwd up to
+ * the order of floating-point sums).  This is not part of the method; it makes
+ * every schedule reachable at any problem size.
+ *   lanes_per_channel : 1, 2 or 4 lanes share a channel's states; 0 = automatic
+ *   generic_path      : 1 = the register-prefetch path even where the cp.async
+ *                       pipeline applies; 0 = automatic
+ *   segments          : cut the sequence into this many segments (at least 256
+ *                       steps each; fewer are used when the sequence is short),
+ *                       scanned in parallel and joined by the carry pass; 0 =
+ *                       automatic, 1 = one sequential pass
+ * Any other value returns SSM_ERR_INVALID_ARG.  The workspace size depends on
+ * the schedule: query it with ssm_scan_fwd_scheduled_workspace_size. */
+typedef struct {
+    int lanes_per_channel;
+    int generic_path;
+    int64_t segments;
+} ssm_fwd_schedule;
+
+SSM_API size_t ssm_scan_fwd_scheduled_workspace_size(const ssm_scan_fwd_params* p, const ssm_fwd_schedule* s);
+SSM_API ssm_status ssm_scan_fwd_scheduled(const ssm_scan_fwd_params* p, const ssm_fwd_schedule* s,
+                                          void* workspace, size_t workspace_bytes, ssm_stream_t stream);
+
 /* ssm_scan_fwd for callers that cannot allocate device memory.  The pages
  * have no counterpart to this entry point: it exists for callers that are
  * not allowed to call cudaMalloc, such as a plugin inside an inference
@@ -158,9 +181,11 @@ SSM_API ssm_status ssm_scan_fwd(const ssm_scan_fwd_params* p, void* workspace,
  *  - All calls on a device share that array: calls that may overlap on the GPU
  *    (other streams, other host threads) race on it and must be ordered by
  *    the caller.  No part of the array needs clearing between calls.
- *  - The first call on each device looks up the array's device address
- *    (cudaGetSymbolAddress, with that device current); make that first call
- *    before any stream capture on the device. */
+ *  - The first call in each CUDA context looks up the array's device address
+ *    (cudaGetSymbolAddress, with that context's device current) and keeps it
+ *    under the context's unique id, so a context created later on the same
+ *    device (for example after cudaDeviceReset) gets its own lookup.  Make the
+ *    first call in a context before any stream capture there. */
 SSM_API ssm_status ssm_scan_fwd_static_ws(const ssm_scan_fwd_params* p, ssm_stream_t stream);
 
 /* ------------------------------------------------------------------------

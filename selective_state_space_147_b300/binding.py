@@ -148,6 +148,15 @@ class SsdFwdParams(ctypes.Structure):
     ]
 
 
+class FwdSchedule(ctypes.Structure):
+    _fields_ = [("lanes_per_channel", _int), ("generic_path", _int), ("segments", _i64)]
+
+
+_lib.ssm_scan_fwd_scheduled.argtypes = [ctypes.POINTER(ScanFwdParams), ctypes.POINTER(FwdSchedule), _vp,
+                                        ctypes.c_size_t, _vp]
+_lib.ssm_scan_fwd_scheduled.restype = _int
+_lib.ssm_scan_fwd_scheduled_workspace_size.argtypes = [ctypes.POINTER(ScanFwdParams), ctypes.POINTER(FwdSchedule)]
+_lib.ssm_scan_fwd_scheduled_workspace_size.restype = ctypes.c_size_t
 _lib.ssm_scan_fwd_workspace_size.argtypes = [ctypes.POINTER(ScanFwdParams)]
 _lib.ssm_scan_fwd_workspace_size.restype = ctypes.c_size_t
 _lib.ssm_scan_fwd.argtypes = [ctypes.POINTER(ScanFwdParams), _vp, ctypes.c_size_t, _vp]
@@ -338,9 +347,11 @@ def ssm_scan_fwd(u, delta, A, B, C, *, D=None, delta_bias=None, z=None, h0=None,
                  out: Optional[torch.Tensor] = None, out_dtype=None,
                  final_state: Optional[torch.Tensor] = None, return_final_state: bool = False,
                  checkpoints: Optional[torch.Tensor] = None, checkpoint_every: int = 0,
-                 workspace: Optional[torch.Tensor] = None, stream=None):
+                 workspace: Optional[torch.Tensor] = None, stream=None, schedule: Optional[dict] = None):
     """Fused selective-scan forward.  u, delta, z: (batch, dim, L); B, C: (batch, N, L)
     (same dtype as u); A: (dim, N) f32; D, delta_bias: (dim,) f32; h0: (batch, dim, N) f32.
+    ``schedule`` (tests and tuning) forces a schedule through ssm_scan_fwd_scheduled:
+    a dict with any of lanes_per_channel, generic_path, segments (0 = automatic).
     Returns ``out`` (and the final state when requested)."""
     for name, t in (("u", u), ("delta", delta), ("B", B), ("C", C), ("z", z)):
         _need_cuda(name, t)
@@ -358,15 +369,35 @@ def ssm_scan_fwd(u, delta, A, B, C, *, D=None, delta_bias=None, z=None, h0=None,
     _check_ckpt(checkpoints, batch, dim, L, N, checkpoint_every)
     p = _fwd_params(u, delta, A, B, C, D, delta_bias, z, h0, bbar_mode, delta_softplus,
                     out, final_state, checkpoints, checkpoint_every)
-    need = _lib.ssm_scan_fwd_workspace_size(ctypes.byref(p))
+    sch = _schedule(schedule)
+    if sch is None:
+        need = _lib.ssm_scan_fwd_workspace_size(ctypes.byref(p))
+    else:
+        need = _lib.ssm_scan_fwd_scheduled_workspace_size(ctypes.byref(p), ctypes.byref(sch))
     if need > 0 and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=u.device)
     ws_ptr = _ptr(workspace)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(_lib.ssm_scan_fwd(ctypes.byref(p), ws_ptr, ws_bytes, _stream(stream)))
+    if sch is None:
+        _check(_lib.ssm_scan_fwd(ctypes.byref(p), ws_ptr, ws_bytes, _stream(stream)))
+    else:
+        _check(_lib.ssm_scan_fwd_scheduled(ctypes.byref(p), ctypes.byref(sch), ws_ptr, ws_bytes, _stream(stream)))
     if return_final_state:
         return out, final_state
     return out
+
+
+def _schedule(schedule: Optional[dict]):
+    if schedule is None:
+        return None
+    unknown = set(schedule) - {"lanes_per_channel", "generic_path", "segments"}
+    if unknown:
+        raise ValueError(f"unknown schedule keys {sorted(unknown)}")
+    s = FwdSchedule()
+    s.lanes_per_channel = int(schedule.get("lanes_per_channel") or 0)
+    s.generic_path = int(bool(schedule.get("generic_path", 0)))
+    s.segments = int(schedule.get("segments") or 0)
+    return s
 
 
 def ssm_scan_fwd_workspace_size(u, A, **kw) -> int:
@@ -379,6 +410,9 @@ def ssm_scan_fwd_workspace_size(u, A, **kw) -> int:
     p.bbar_mode = int(kw.get("bbar_mode", SSM_BBAR_ZOH))
     p.delta_softplus = 1
     p.u = p.delta = p.B = p.C = p.out = p.A = 256   # any aligned non-NULL value: only sizes matter here
+    sch = _schedule(kw.get("schedule"))
+    if sch is not None:
+        return _lib.ssm_scan_fwd_scheduled_workspace_size(ctypes.byref(p), ctypes.byref(sch))
     return _lib.ssm_scan_fwd_workspace_size(ctypes.byref(p))
 
 

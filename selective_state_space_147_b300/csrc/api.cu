@@ -87,6 +87,18 @@ ssm_status check_fwd(const ssm_scan_fwd_params* p) {
     return check_groups(p->ngroups, p->dim, p->B_group_stride, p->C_group_stride, true);
 }
 
+ssm_status check_schedule(const ssm_fwd_schedule* s) {
+    if (s == nullptr) return fail(SSM_ERR_INVALID_ARG, "schedule is NULL");
+    if (s->lanes_per_channel != 0 && s->lanes_per_channel != 1 && s->lanes_per_channel != 2 &&
+        s->lanes_per_channel != 4)
+        return fail(SSM_ERR_INVALID_ARG, "lanes_per_channel=%d (0, 1, 2 or 4)", s->lanes_per_channel);
+    if (s->generic_path != 0 && s->generic_path != 1)
+        return fail(SSM_ERR_INVALID_ARG, "generic_path=%d (0 or 1)", s->generic_path);
+    if (s->segments < 0 || s->segments > (1 << 20))
+        return fail(SSM_ERR_INVALID_ARG, "segments=%lld", (long long)s->segments);
+    return SSM_OK;
+}
+
 ssm_status check_bwd(const ssm_scan_bwd_params* p) {
     if (p == nullptr) return fail(SSM_ERR_INVALID_ARG, "params is NULL");
     if (p->batch < 1 || p->dim < 1 || p->seqlen < 0 || p->dstate < 1)
@@ -132,7 +144,7 @@ const char* ssm_status_string(ssm_status s) {
 
 const char* ssm_last_error(void) { return g_err; }
 
-int ssm_abi_version(void) { return 3; }
+int ssm_abi_version(void) { return 4; }
 
 uint64_t ssm_launch_count(void) { return ssm::ssm_launch_count_value(); }
 
@@ -143,22 +155,41 @@ size_t ssm_scan_fwd_workspace_size(const ssm_scan_fwd_params* p) {
     return ssm::fwd_workspace_bytes(p, sms);
 }
 
-ssm_status ssm_scan_fwd(const ssm_scan_fwd_params* p, void* workspace, size_t workspace_bytes,
-                        ssm_stream_t stream) {
+static ssm_status scan_fwd_common(const ssm_scan_fwd_params* p, const ssm_fwd_schedule* sched, void* workspace,
+                           size_t workspace_bytes, ssm_stream_t stream) {
     ssm_status s = check_fwd(p);
     if (s != SSM_OK) return s;
     int sms = 0;
     if ((s = num_sms(&sms)) != SSM_OK) return s;
-    const size_t need = ssm::fwd_workspace_bytes(p, sms);
+    const size_t need = ssm::fwd_workspace_bytes(p, sms, sched);
     if (need > 0) {
         if (workspace == nullptr || workspace_bytes < need)
             return fail(SSM_ERR_WORKSPACE, "workspace of %zu bytes required, got %zu", need,
                         workspace == nullptr ? (size_t)0 : workspace_bytes);
         if ((uintptr_t)workspace % 256 != 0) return fail(SSM_ERR_MISALIGNED, "workspace must be 256-byte aligned");
     }
-    cudaError_t e = ssm::launch_scan_fwd(p, workspace, sms, reinterpret_cast<cudaStream_t>(stream));
+    cudaError_t e = ssm::launch_scan_fwd(p, workspace, sms, reinterpret_cast<cudaStream_t>(stream), sched);
     if (e != cudaSuccess) return cuda_fail(e, "ssm_scan_fwd launch");
     return ok();
+}
+
+ssm_status ssm_scan_fwd(const ssm_scan_fwd_params* p, void* workspace, size_t workspace_bytes,
+                        ssm_stream_t stream) {
+    return scan_fwd_common(p, nullptr, workspace, workspace_bytes, stream);
+}
+
+ssm_status ssm_scan_fwd_scheduled(const ssm_scan_fwd_params* p, const ssm_fwd_schedule* s, void* workspace,
+                                  size_t workspace_bytes, ssm_stream_t stream) {
+    const ssm_status c = check_schedule(s);
+    if (c != SSM_OK) return c;
+    return scan_fwd_common(p, s, workspace, workspace_bytes, stream);
+}
+
+size_t ssm_scan_fwd_scheduled_workspace_size(const ssm_scan_fwd_params* p, const ssm_fwd_schedule* s) {
+    if (check_fwd(p) != SSM_OK || check_schedule(s) != SSM_OK) return 0;
+    int sms = 0;
+    if (num_sms(&sms) != SSM_OK) return 0;
+    return ssm::fwd_workspace_bytes(p, sms, s);
 }
 
 ssm_status ssm_scan_fwd_static_ws(const ssm_scan_fwd_params* p, ssm_stream_t stream) {

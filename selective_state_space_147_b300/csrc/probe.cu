@@ -69,8 +69,7 @@ __global__ void __launch_bounds__(kProbeThreads) pipe_probe_kernel(int iters) {
 
 template <int KIND>
 cudaError_t probe_one(int sms, double* per_sm_clk) {
-    cudaError_t e = cudaFuncSetAttribute(pipe_probe_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kProbeSmem);
+    cudaError_t e = prepare_kernel<pipe_probe_kernel<KIND>>(kProbeSmem);
     if (e != cudaSuccess) return e;
     for (int rep = 0; rep < 2; rep++) {   // the first run warms the clocks up
         pipe_probe_kernel<KIND><<<sms, kProbeThreads, kProbeSmem>>>(kProbeIters);

@@ -874,31 +874,46 @@ static bool al16(const void* ptr, ssm_strides s, int esize) {
     return ptr != nullptr && ((uintptr_t)ptr % 16 == 0) && ((s.batch * esize) % 16 == 0) && ((s.row * esize) % 16 == 0);
 }
 
+template <auto Kern>
+static cudaError_t launch_bwd_kernel(const BwdArgs& a, int* flag, int threads, int64_t chans_per_cta, int bytes,
+                                     cudaStream_t st) {
+    const dim3 grid((unsigned)ceil_div(a.dim, chans_per_cta), (unsigned)a.batch);
+    cudaError_t e = prepare_kernel<Kern>(bytes);
+    if (e != cudaSuccess) return e;
+    Kern<<<grid, threads, bytes, st>>>(a, flag);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+template <typename Tin, typename Tg, bool ZOH, bool HAS_Z>
+static cudaError_t launch_bwd_acc(const BwdArgs& a, int* flag, cudaStream_t st) {
+    return launch_bwd_kernel<scan_bwd_kernel<Tin, Tg, ZOH, HAS_Z>>(a, flag, kBwdThreads, kBwdThreads,
+                                                                   kBwdAccSmemBytes, st);
+}
+template <typename Tg, bool ZOH, bool HAS_Z>
+static cudaError_t launch_bwd_fast(const BwdArgs& a, int* flag, cudaStream_t st) {
+    return launch_bwd_kernel<scan_bwd_fast_kernel<Tg, ZOH, HAS_Z>>(a, flag, kFThreads, kFChans,
+                                                                   kBwdFastSmemBytes, st);
+}
+
 template <typename Tin, typename Tg>
 static cudaError_t launch_bwd_typed(const BwdArgs& a, bool zoh, bool has_z, int* flag, cudaStream_t st) {
-    auto go = [&](auto kern, int threads, int64_t chans_per_cta, int bytes) -> cudaError_t {
-        const dim3 grid((unsigned)ceil_div(a.dim, chans_per_cta), (unsigned)a.batch);
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-        if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-        if (e != cudaSuccess) return e;
-        kern<<<grid, threads, bytes, st>>>(a, flag);
-        count_launches(1);
-        return cudaGetLastError();
-    };
-    auto acc = [&](auto kern) { return go(kern, kBwdThreads, kBwdThreads, kBwdAccSmemBytes); };
-    auto fast = [&](auto kern) { return go(kern, kFThreads, kFChans, kBwdFastSmemBytes); };
     if constexpr (sizeof(Tin) == 2) {
         // bf16: the fast kernel; with ZOH the accurate one is queued too and runs
         // instead when the device-side check finds an A == 0
         if (zoh) {
-            cudaError_t e = has_z ? fast(scan_bwd_fast_kernel<Tg, true, true>) : fast(scan_bwd_fast_kernel<Tg, true, false>);
+            cudaError_t e = has_z ? launch_bwd_fast<Tg, true, true>(a, flag, st)
+                                  : launch_bwd_fast<Tg, true, false>(a, flag, st);
             if (e != cudaSuccess) return e;
-            return has_z ? acc(scan_bwd_kernel<Tin, Tg, true, true>) : acc(scan_bwd_kernel<Tin, Tg, true, false>);
+            return has_z ? launch_bwd_acc<Tin, Tg, true, true>(a, flag, st)
+                         : launch_bwd_acc<Tin, Tg, true, false>(a, flag, st);
         }
-        return has_z ? fast(scan_bwd_fast_kernel<Tg, false, true>) : fast(scan_bwd_fast_kernel<Tg, false, false>);
+        return has_z ? launch_bwd_fast<Tg, false, true>(a, flag, st) : launch_bwd_fast<Tg, false, false>(a, flag, st);
     } else {
-        if (zoh) return has_z ? acc(scan_bwd_kernel<Tin, Tg, true, true>) : acc(scan_bwd_kernel<Tin, Tg, true, false>);
-        return has_z ? acc(scan_bwd_kernel<Tin, Tg, false, true>) : acc(scan_bwd_kernel<Tin, Tg, false, false>);
+        if (zoh) return has_z ? launch_bwd_acc<Tin, Tg, true, true>(a, flag, st)
+                              : launch_bwd_acc<Tin, Tg, true, false>(a, flag, st);
+        return has_z ? launch_bwd_acc<Tin, Tg, false, true>(a, flag, st)
+                     : launch_bwd_acc<Tin, Tg, false, false>(a, flag, st);
     }
 }
 

@@ -33,16 +33,10 @@
 //    (a1,b1) o (a2,b2) = (a1 a2, a2 b1 + b2)); pass 3 reruns every segment from
 //    its carry-in and writes the outputs.
 #include <cstdint>
-#include <cstdlib>
 
 #include "scan_fwd.cuh"
 
 namespace ssm {
-
-static int env_int(const char* name, int dflt) {
-    const char* s = std::getenv(name);
-    return (s && *s) ? std::atoi(s) : dflt;
-}
 
 static bool aligned16(const void* ptr, int64_t s0, int64_t s1, int esize) {
     return ((uintptr_t)ptr % 16 == 0) && ((s0 * esize) % 16 == 0) && ((s1 * esize) % 16 == 0);
@@ -58,32 +52,34 @@ struct FwdPlan {
     int G;
     int nseg;
     int64_t seg_len;
+    bool generic;   // register-prefetch path even where the cp.async pipeline applies
 };
 
 
-static FwdPlan plan_fwd(const ssm_scan_fwd_params* p, int num_sms) {
+// Schedule: lanes per channel G and the number of sequence segments.  The
+// automatic choice takes the fewest lanes that still give every SM at least 4
+// warps, and segments only when even G = 4 leaves SMs short of work; `s`
+// (tests and tuning) overrides either choice.
+static FwdPlan plan_fwd(const ssm_scan_fwd_params* p, int num_sms, const ssm_fwd_schedule* s) {
     FwdPlan pl;
-    const int64_t chans = p->batch * p->dim;
     const int64_t want_warps = (int64_t)num_sms * 4;
     pl.G = 4;
     for (int G : {1, 2, 4}) {
         const int64_t warps = ceil_div(p->dim, 32 / G) * p->batch;
         if (warps >= want_warps) { pl.G = G; break; }
     }
-    int forced = env_int("SSM_FWD_G", 0);
-    if (forced == 1 || forced == 2 || forced == 4) pl.G = forced;
+    if (s != nullptr && s->lanes_per_channel != 0) pl.G = s->lanes_per_channel;
+    pl.generic = s != nullptr && s->generic_path != 0;
     const int64_t warps = ceil_div(p->dim, 32 / pl.G) * p->batch;
     int64_t nseg = 1;
-    if (warps < (int64_t)num_sms * 4) nseg = ceil_div((int64_t)num_sms * 8, warps);
-    int forced_seg = env_int("SSM_FWD_NSEG", 0);
-    if (forced_seg > 0) nseg = forced_seg;
+    if (warps < want_warps) nseg = ceil_div((int64_t)num_sms * 8, warps);
+    if (s != nullptr && s->segments > 0) nseg = s->segments;
     const int64_t max_seg = ceil_div(p->seqlen, 4 * kTile);   // segments of at least 256 steps
     if (nseg > max_seg) nseg = max_seg;
     if (nseg < 1) nseg = 1;
     pl.seg_len = ceil_div(ceil_div(p->seqlen, nseg), kTile) * kTile;
     pl.nseg = (int)ceil_div(p->seqlen, pl.seg_len);
     if (pl.nseg < 1) pl.nseg = 1;
-    (void)chans;
     return pl;
 }
 
@@ -133,14 +129,15 @@ static cudaError_t launch_fwd_group_finish(const ssm_scan_fwd_params* p, const f
     return cudaGetLastError();
 }
 
-size_t fwd_workspace_bytes(const ssm_scan_fwd_params* p, int num_sms) {
+size_t fwd_workspace_bytes(const ssm_scan_fwd_params* p, int num_sms, const ssm_fwd_schedule* s) {
     if (p->seqlen == 0) return 0;
-    const FwdPlan pl = plan_fwd(p, num_sms);
+    const FwdPlan pl = plan_fwd(p, num_sms, s);
     return seg_ws_bytes(p, pl) + yacc_bytes(p);
 }
 
 
-cudaError_t launch_scan_fwd(const ssm_scan_fwd_params* p, void* ws, int num_sms, cudaStream_t st) {
+cudaError_t launch_scan_fwd(const ssm_scan_fwd_params* p, void* ws, int num_sms, cudaStream_t st,
+                            const ssm_fwd_schedule* s) {
     const int64_t chans = p->batch * p->dim;
     if (p->seqlen == 0) {
         if (p->final_state != nullptr) {
@@ -150,7 +147,7 @@ cudaError_t launch_scan_fwd(const ssm_scan_fwd_params* p, void* ws, int num_sms,
         }
         return cudaGetLastError();
     }
-    const FwdPlan pl = plan_fwd(p, num_sms);
+    const FwdPlan pl = plan_fwd(p, num_sms, s);
     const int isz = (p->in_dtype == SSM_BF16) ? 2 : 4;
     const int osz = (p->out_dtype == SSM_BF16) ? 2 : 4;
     FwdArgs a;
@@ -191,7 +188,7 @@ cudaError_t launch_scan_fwd(const ssm_scan_fwd_params* p, void* ws, int num_sms,
             const bool bc16 = ((uintptr_t)ga.B % 16 == 0) && ((uintptr_t)ga.C % 16 == 0) &&
                               (ga.sB_b % 8 == 0) && (ga.sB_n % 8 == 0) && (ga.sC_b % 8 == 0) && (ga.sC_n % 8 == 0) &&
                               (ga.sB_g % 8 == 0) && (ga.sC_g % 8 == 0);
-            const bool async = ga.vec_u && ga.vec_dt && (!has_z || ga.vec_z) && bc16 && env_int("SSM_FWD_NOASYNC", 0) == 0;
+            const bool async = ga.vec_u && ga.vec_dt && (!has_z || ga.vec_z) && bc16 && !pl.generic;
             if (async) {
                 if (out_bf16) return dispatch_G<__nv_bfloat16, __nv_bfloat16, true>(ga, pl.G, zoh, has_z, st);
                 return dispatch_G<__nv_bfloat16, float, true>(ga, pl.G, zoh, has_z, st);

@@ -3,8 +3,6 @@
 // dtype pair so that the kernels compile in parallel.
 #pragma once
 
-#include <cstdlib>
-
 #include "scan_fwd.cuh"
 
 namespace ssm {
@@ -821,13 +819,10 @@ static cudaError_t launch_one(const FwdArgs& a, int nseg, cudaStream_t st) {
     constexpr int kGenericBytes = (threads / 32) * kTile * kRow * 4;
     constexpr int bytes = (kAsync && AsyncLayout<G>::kBytes > kGenericBytes) ? AsyncLayout<G>::kBytes : kGenericBytes;
     const dim3 grid((unsigned)ceil_div(a.dim, kAsync ? 32 : 32 / G), (unsigned)a.batch, (unsigned)nseg);
-    auto kern = scan_fwd_kernel<Tin, Tout, G, ZOH, HAS_Z, MODE, kAsync>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    // small blocks: the SM spends its whole unified L1/shared array on shared memory
+    cudaError_t e = prepare_kernel<scan_fwd_kernel<Tin, Tout, G, ZOH, HAS_Z, MODE, kAsync>>(bytes);
     if (e != cudaSuccess) return e;
-    // small blocks: let the SM spend its whole unified L1/shared array on shared memory
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    if (e != cudaSuccess) return e;
-    kern<<<grid, threads, bytes, st>>>(a);
+    scan_fwd_kernel<Tin, Tout, G, ZOH, HAS_Z, MODE, kAsync><<<grid, threads, bytes, st>>>(a);
     count_launches(1);
     return cudaGetLastError();
 }

@@ -22,9 +22,11 @@
 //  * Nothing in the array needs to start at zero: every word a call reads was
 //    written earlier by the same call, so leftovers from an earlier call are
 //    harmless.
-//  * The first call on each device looks up the array's device address with
-//    cudaGetSymbolAddress (once per device, with that device current).  Make
-//    that first call before any stream capture on the device.
+//  * The array's device address is looked up with cudaGetSymbolAddress by the
+//    first call in each CUDA context (with the context's device current) and
+//    remembered under the context's unique id; a context created later on the
+//    same device (after cudaDeviceReset, for example) gets a fresh lookup.
+//    Make the first call in a context before any stream capture there.
 #include <cstdint>
 #include <mutex>
 
@@ -40,23 +42,35 @@ constexpr int kMaxDevices = 64;
 // cudaGetSymbolAddress below.
 static __device__ __align__(256) unsigned char g_scan_scratch[kStaticScratchBytes];
 
-static std::mutex g_scratch_mutex;
-static void* g_scratch_addr[kMaxDevices] = {nullptr};
+struct ScratchEntry {
+    unsigned long long ctx_id;   // unique id of the context the address belongs to
+    void* addr;
+};
 
-// Device address of g_scan_scratch on the current device, looked up once.
+static std::mutex g_scratch_mutex;
+static ScratchEntry g_scratch[kMaxDevices] = {};
+
+// Device address of g_scan_scratch in the current context, looked up once per context.
 static cudaError_t scratch_address(void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (g_scratch_addr[dev] == nullptr) {
-        void* ptr = nullptr;
-        e = cudaGetSymbolAddress(&ptr, g_scan_scratch);
-        if (e != cudaSuccess) return e;
-        g_scratch_addr[dev] = ptr;
+    unsigned long long id = 0;
+    if ((e = current_context_id(&id)) != cudaSuccess) return e;
+    if (id != 0 && g_scratch[dev].addr != nullptr && g_scratch[dev].ctx_id == id) {
+        *out = g_scratch[dev].addr;
+        return cudaSuccess;
     }
-    *out = g_scratch_addr[dev];
+    // first call in this context (the lookup also makes the runtime's context current)
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_scan_scratch);
+    if (e != cudaSuccess) return e;
+    if (id == 0 && (e = current_context_id(&id)) != cudaSuccess) return e;
+    g_scratch[dev].ctx_id = id;
+    g_scratch[dev].addr = ptr;
+    *out = ptr;
     return cudaSuccess;
 }
 

@@ -372,7 +372,7 @@ __global__ void __launch_bounds__(kThreads) ssd_fwd_kernel(const SsdArgs a) {
 template <int NT, typename Tout>
 cudaError_t launch_ssd_typed(const SsdArgs& a, cudaStream_t st) {
     const int bytes = SsdSmem<NT>::kBytes;
-    cudaError_t e = cudaFuncSetAttribute(ssd_fwd_kernel<NT, Tout>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    cudaError_t e = prepare_kernel<ssd_fwd_kernel<NT, Tout>>(bytes);
     if (e != cudaSuccess) return e;
     ssd_fwd_kernel<NT, Tout><<<(unsigned)(2 * a.batch * a.nheads), kThreads, bytes, st>>>(a);
     count_launches(1);

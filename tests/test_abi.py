@@ -47,7 +47,7 @@ def test_status_strings_and_version(lib):
     names = {c: lib.ssm_status_string(c).decode() for c in (0, -1, -2, -3, -4, -5, -99)}
     assert names[0] == "SSM_OK" and names[-1] == "SSM_ERR_INVALID_ARG"
     assert names[-5] == "SSM_ERR_CUDA" and names[-99] == "SSM_ERR_UNKNOWN"
-    assert lib.ssm_abi_version() == 3
+    assert lib.ssm_abi_version() == 4
 
 
 def test_host_validation_without_gpu():
@@ -55,6 +55,15 @@ def test_host_validation_without_gpu():
     lib = B.lib()
     # NULL parameter blocks
     assert lib.ssm_scan_fwd(None, None, 0, None) == -1
+    # a forced schedule is validated before anything else
+    p = B.ScanFwdParams()
+    p.batch, p.dim, p.seqlen, p.dstate = 1, 64, 512, 16
+    p.u = p.delta = p.B = p.C = p.out = p.A = 256
+    for bad in (dict(lanes_per_channel=3), dict(generic_path=2), dict(segments=-1)):
+        sch = B.FwdSchedule(**bad)
+        assert lib.ssm_scan_fwd_scheduled(ctypes.byref(p), ctypes.byref(sch), None, 0, None) == -1, bad
+        assert lib.ssm_scan_fwd_scheduled_workspace_size(ctypes.byref(p), ctypes.byref(sch)) == 0
+    assert lib.ssm_scan_fwd_scheduled(ctypes.byref(p), None, None, 0, None) == -1
     assert lib.ssm_state_update(None, None) == -1
     assert lib.ssm_decode_step(None, None) == -1
     assert lib.causal_conv1d_silu_bwd(None, None, 0, None) == -1

@@ -1,6 +1,4 @@
 """ssm_scan_fwd on the GPU against the fp64 oracle, element by element."""
-import os
-
 import numpy as np
 import pytest
 import torch
@@ -42,22 +40,15 @@ def run_oracle(g, zoh=True, softplus=True, use_D=True, use_bias=True):
 
 
 @pytest.fixture
-def schedule(request):
-    """Force a (G, nseg) schedule through the launcher's tuning variables."""
-    old = {k: os.environ.get(k) for k in ("SSM_FWD_G", "SSM_FWD_NSEG")}
+def schedule():
+    """Force a (G, nseg) schedule: the forward then goes through ssm_scan_fwd_scheduled."""
+    state = {}
 
     def set_(G=None, nseg=None):
-        for k, v in (("SSM_FWD_G", G), ("SSM_FWD_NSEG", nseg)):
-            if v is None:
-                os.environ.pop(k, None)
-            else:
-                os.environ[k] = str(v)
-    yield set_
-    for k, v in old.items():
-        if v is None:
-            os.environ.pop(k, None)
-        else:
-            os.environ[k] = v
+        state.clear()
+        state.update(lanes_per_channel=G or 0, segments=nseg or 0)
+    set_.kw = lambda: {"schedule": dict(state)} if state else {}
+    return set_
 
 
 def test_tiny_fp32_config():
@@ -76,7 +67,7 @@ def test_schedules_and_modes(schedule, zoh, dtype, G, nseg):
     schedule(G, nseg)
     # dim 100 is not a multiple of any channel group; L 1000 leaves a ragged tile and sub-block
     g = make(7, 2, 100, 1000, 16, dtype, with_h0=True)
-    out, hN = run_gpu(g, zoh=zoh, final=True)
+    out, hN = run_gpu(g, zoh=zoh, final=True, **schedule.kw())
     ref, href = run_oracle(g, zoh=zoh)
     assert_close(out, ref, dtype, what="out")
     assert_close(hN, href, dtype, what="final_state")
@@ -101,7 +92,7 @@ def test_large_state_with_checkpoints_and_segments(dtype, zoh, schedule):
     g = make(16, 2, 36, L, N, dtype, with_h0=True)
     lib = _lib()
     ck = lib.checkpoint_buffer(2, 36, L, N, every=K).fill_(float("nan"))
-    out, hN = run_gpu(g, final=True, checkpoints=ck, checkpoint_every=K, zoh=zoh)
+    out, hN = run_gpu(g, final=True, checkpoints=ck, checkpoint_every=K, zoh=zoh, **schedule.kw())
     ref, href = run_oracle(g, zoh=zoh)
     assert_close(out, ref, dtype, what="out")
     assert_close(hN, href, dtype, what="final_state")
@@ -187,7 +178,7 @@ def test_checkpoints(schedule, K):
     nck = (L + K - 1) // K
     lib = _lib()
     ck = lib.checkpoint_buffer(2, 40, L, 16, every=K).fill_(float("nan"))
-    run_gpu(g, checkpoints=ck, checkpoint_every=K)
+    run_gpu(g, checkpoints=ck, checkpoint_every=K, **schedule.kw())
     ck = lib.checkpoint_states(ck, 16)
     for k in range(nck):
         t = k * K
