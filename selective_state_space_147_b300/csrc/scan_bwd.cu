@@ -51,9 +51,9 @@ struct BwdArgs {
     int softplus;
     int vec_u, vec_dt, vec_z, vec_do, vec_du, vec_ddt, vec_dz;
     float* part_bc;             // (batch, nblk, 2, 16, seqlen)
-    float* part_A;              // (batch, dim, 16)
-    float* part_D;              // (batch, dim)
-    float* part_bias;           // (batch, dim)
+    float* part_A;              // (nseg, batch, dim, 16)
+    float* part_D;              // (nseg, batch, dim)
+    float* part_bias;           // (nseg, batch, dim)
     int nblk;
     // one group of at most 16 states of a larger state: row strides of A and of
     // the states (dfinal, dh0), checkpoint pairs in total and the group's first
@@ -63,6 +63,13 @@ struct BwdArgs {
     // B/C groups: channel d reads group d / cpg; dB, dC are (batch, ngroups, N, L)
     int64_t cpg, sB_g, sC_g;
     int ngroups;
+    // segments of the sequence (fast kernel): nseg of seg_len steps (a multiple of
+    // 64); the pre-pass leaves each segment's local adjoint (nseg, batch, dim, 16)
+    // and summed delta (nseg, batch, dim)
+    int nseg;
+    int64_t seg_len;
+    float* gloc;
+    float* sumdl;
 };
 
 // Checkpoint k of channel (b, d), state pair `pair`: the forward's layout
@@ -315,34 +322,54 @@ __device__ __forceinline__ void bwd_channel(const BwdArgs& a, float* sbc, float*
 }
 
 // ---------------------------------------------------------------------------
-// Fast (SFU) backward for bf16 inputs.
+// Fast (SFU) backward for bf16 inputs, the sequence cut into segments.
 //
-// One thread per channel (a CTA of 2 warps covers 64 channels: with 255
-// registers four such CTAs fit an SM, which balances 32768 channels over 148
-// SMs better than 128-channel CTAs), the sequence
-// walked backwards in 4-step sub-blocks, one per forward checkpoint.  The
-// adjoint recurrence G_t = dy_t C_t + Abar_{t+1} G_{t+1} is independent per
-// state, so state pairs are the outer loop, two at a time for instruction-level
-// parallelism: the two pairs' 4 steps are recomputed forward from the
-// checkpoint (h, Abar and the input coefficient stay in registers) and then
-// walked in reverse.  Only the per-step sums over states (du, ddelta and, with
-// the gate, the readout y that dz needs) live across pairs, as packed f32x2
-// accumulators.  After each couple of pairs the lane's 32 dB/dC partials
-// (4 steps x 4 states x 2 tensors) are summed over the warp's 32 channels
-// through a shared-memory transpose, and once per sub-block the CTA's warps
-// in a fixed order into one partial per CTA.  u, delta, dout, z rows (8 steps)
-// and the checkpoints arrive ahead by cp.async into shared memory.
+// One thread per channel and its 16 states (a CTA of 2 warps covers 64
+// channels of one batch row; with about 230 registers four such CTAs fit an
+// SM).  When the channels alone cannot fill the GPU (batch 1, or few
+// channels) the sequence is cut into segments that run in different CTAs.
+// The adjoint G_t = dL/dh_t obeys the linear reverse recurrence
+// G_t = dy_t C_t + Abar_{t+1} G_{t+1}, which does not involve h: a pre-pass
+// (bwd_gcarry_kernel) runs it over every segment but the first from G = 0 and
+// keeps the result and the segment's summed delta; a segment then starts from
+// the composition of the segments to its right,
+//   carry_in(s) = exp(A sum_delta(s+1)) carry_in(s+1) + G_local(s+1),
+//   carry_in(last) = dfinal_state,
+// the associative combine of (Abar products, local adjoints).
+//
+// Inside a segment the sequence is walked backwards in 4-step sub-blocks,
+// one per forward checkpoint.  State pairs are the outer loop, two at a time
+// for instruction-level parallelism: the two pairs' 4 steps are recomputed
+// forward from the checkpoint (h, Abar and the ZOH coefficient stay in
+// registers) and then walked in reverse; only the per-step sums over states
+// (du, ddelta and, with the gate, the readout y that dz needs) live across
+// pairs, as packed f32x2 accumulators, and the per-step scalars are duplicated
+// into both halves of a packed register so every update is one f32x2
+// instruction; the dA term (delta Abar - coef)/A keeps its 1/A outside the sum
+// over t.  After each
+// couple of pairs the lane's 32 dB/dC values (4 steps x 2 pairs x 2 states x 2
+// tensors) are summed over the warp's 32 channels by a shared-memory
+// transpose, then over the CTA's 2 warps in a fixed order into one partial per
+// 64 channels.  u, delta, dout, z rows (8 steps) and the checkpoints arrive one
+// sub-block ahead in shared memory by cp.async.
+constexpr int kSThreads = 64;                 // 2 warps, 64 channels
+constexpr int kSWarps = kSThreads / 32;
+constexpr int kSChans = kSThreads;            // channels per CTA = per dB/dC partial
+constexpr int kSPerSM = 4;                    // resident CTAs per SM at the kernel's register use
 constexpr int kRowF = 36;                     // B/C row of one step: [pair: B B C C] x 8, pad
 constexpr int kRedF = 36;                     // transpose row (32 floats + pad, 16-byte aligned)
 constexpr int kFSub = kBwdK;                  // steps per sub-block (= checkpoint interval)
 constexpr int kFNP = 8;                       // state pairs per thread
 // shared memory (byte offsets)
 constexpr int kFOffRed = kTile * kRowF * 4;                      // float [2][warp][couple][32]
-constexpr int kFOffTr = kFOffRed + 2 * kFWarps * 4 * 32 * 4;     // float [warp][32 rows][kRedF]
-constexpr int kFOffCst = kFOffTr + kFWarps * 32 * kRedF * 4;     // ulonglong2 {A, 1/A} [warp][pair][32]
-constexpr int kFOffCk = kFOffCst + kFWarps * kFNP * 32 * 16;     // pf2 checkpoint [warp][2][pair][32]
-constexpr int kFOffRaw = kFOffCk + kFWarps * 2 * kFNP * 32 * 8;  // uint4 u, delta, dout, z [warp][2][4][32]
-constexpr int kBwdFastSmemBytes = kFOffRaw + kFWarps * 2 * 4 * 32 * 16;
+constexpr int kFOffTr = kFOffRed + 2 * kSWarps * 4 * 32 * 4;     // float [warp][32 rows][kRedF]
+constexpr int kFOffCst = kFOffTr + kSWarps * 32 * kRedF * 4;     // ulonglong2 {A, 1/A} [warp][pair][32]
+constexpr int kFOffCk = kFOffCst + kSWarps * kFNP * 32 * 16;     // pf2 checkpoint [warp][2][pair][32]
+constexpr int kFOffRaw = kFOffCk + kSWarps * 2 * kFNP * 32 * 8;  // uint4 u, delta, dout, z [warp][2][4][32]
+constexpr int kBwdSegSmemBytes = kFOffRaw + kSWarps * 2 * 4 * 32 * 16;
+// the pre-pass: C rows of one 32-step tile, [step][C0..C15]
+constexpr int kGcTile = 32;
+constexpr int kGcSmemBytes = kGcTile * 16 * 4;
 
 __device__ __forceinline__ void cp_async8(void* smem, const void* gmem) {
     const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
@@ -356,8 +383,8 @@ template <typename Tin>
 __device__ __forceinline__ void stage_bc_pairs(float* sbc, const BwdArgs& a, const Tin* Bb, const Tin* Cb,
                                                int64_t t0, int tid) {
 #pragma unroll
-    for (int k = 0; k < 128 / kFThreads; k++) {
-        const int idx = k * kFThreads + tid;
+    for (int k = 0; k < 128 / kSThreads; k++) {
+        const int idx = k * kSThreads + tid;
         const int s = idx & 63, tsr = idx >> 6;
         const int64_t t = t0 + s;
         const Tin* base = tsr == 0 ? Bb : Cb;
@@ -373,11 +400,6 @@ __device__ __forceinline__ void stage_bc_pairs(float* sbc, const BwdArgs& a, con
     }
 }
 
-// scalar x packed: (s * v.lo, s * v.hi) and (s * v.lo + c.lo, s * v.hi + c.hi)
-__device__ __forceinline__ pf2 pf2_scale(float s, pf2 v) { return pf2_make(s * pf2_lo(v), s * pf2_hi(v)); }
-__device__ __forceinline__ pf2 pf2_scale_add(float s, pf2 v, pf2 c) {
-    return pf2_make(fmaf(s, pf2_lo(v), pf2_lo(c)), fmaf(s, pf2_hi(v), pf2_hi(c)));
-}
 __device__ __forceinline__ float bf16_of(uint32_t w, int hi) { return hi ? bf16hi(w) : bf16lo(w); }
 
 // four consecutive gradient values (steps t .. t+3) of one row; n of them valid
@@ -398,9 +420,104 @@ __device__ __forceinline__ void store4(Tg* p, int n, bool vec, const float (&v)[
     }
 }
 
+// Pre-pass of the segmented backward: for every segment but the first, the
+// adjoint recurrence over the segment from G = 0 (its local contribution to
+// the carry of the segments to its left) and the segment's summed delta.
+// Needs only delta, dout, z and C.
+template <bool HAS_Z>
+__global__ void __launch_bounds__(kSThreads)
+bwd_gcarry_kernel(const BwdArgs a, const int* flag) {
+    using Tin = __nv_bfloat16;
+    if (*flag) return;   // some A == 0 with ZOH: the accurate, unsegmented kernel takes this call
+    extern __shared__ __align__(16) unsigned char smem_g[];
+    float* sc = reinterpret_cast<float*>(smem_g);
+    const int tid = threadIdx.x;
+    const int64_t b = blockIdx.y;
+    const int seg = (int)blockIdx.z + 1;
+    const int64_t d_raw = (int64_t)blockIdx.x * kSChans + tid;
+    const bool active = d_raw < a.dim;
+    const int64_t d = active ? d_raw : a.dim - 1;
+    const int64_t chans = a.batch * a.dim;
+    const int64_t chan = b * a.dim + d;
+    const int64_t t_begin = (int64_t)seg * a.seg_len;
+    const int64_t t_end = (t_begin + a.seg_len < a.seqlen) ? t_begin + a.seg_len : a.seqlen;
+    const pf2 LOG2E2 = pf2_make(kLog2e, kLog2e);
+    pf2 A2L[kFNP], G[kFNP];
+#pragma unroll
+    for (int p = 0; p < kFNP; p++) {
+        const float a0 = (2 * p < a.dstate) ? __ldg(a.A + d * a.sA + 2 * p) : -1.f;
+        const float a1 = (2 * p + 1 < a.dstate) ? __ldg(a.A + d * a.sA + 2 * p + 1) : -1.f;
+        A2L[p] = pf2_mul(pf2_make(a0, a1), LOG2E2);
+        G[p] = 0ull;
+    }
+    const float bias = a.bias ? __ldg(a.bias + d) : 0.f;
+    const Tin* drow = reinterpret_cast<const Tin*>(a.dt) + b * a.sdt_b + d * a.sdt_d;
+    const Tin* zrow = HAS_Z ? reinterpret_cast<const Tin*>(a.z) + b * a.sz_b + d * a.sz_d : nullptr;
+    const Tin* orow = reinterpret_cast<const Tin*>(a.dout) + b * a.sdo_b + d * a.sdo_d;
+    const int64_t grp = (a.cpg >= a.dim) ? 0 : d / a.cpg;
+    const Tin* Cb = reinterpret_cast<const Tin*>(a.C) + b * a.sC_b + grp * a.sC_g;
+    const bool vec_in = a.vec_dt && a.vec_do && (!HAS_Z || a.vec_z);
+    float sd = 0.f, sdc = 0.f;   // compensated sum of delta
+    int64_t cur_tile = -1;
+#pragma unroll 1
+    for (int64_t t0 = ((t_end - 1) / 8) * 8; t0 >= t_begin; t0 -= 8) {
+        const int64_t tile = t0 / kGcTile;
+        if (tile != cur_tile) {
+            __syncthreads();
+            {
+                const int s = tid & (kGcTile - 1), half = tid / kGcTile;   // half: states 0..7 or 8..15
+                const int64_t t = tile * kGcTile + s;
+#pragma unroll
+                for (int k = 0; k < 8; k++) {
+                    const int n = half * 8 + k;
+                    sc[s * 16 + n] = (n < a.dstate && t < a.seqlen) ? Elem<Tin>::load(Cb + n * a.sC_n + t) : 0.f;
+                }
+            }
+            __syncthreads();
+            cur_tile = tile;
+        }
+        const int64_t r = a.seqlen - t0;
+        const int lim = (int)(r < 8 ? r : 8);
+        Raw8<Tin> rd, ro, rz;
+        rd.load(drow + t0, lim, vec_in);
+        ro.load(orow + t0, lim, vec_in);
+        if constexpr (HAS_Z) rz.load(zrow + t0, lim, vec_in);
+        const float* crow = sc + (t0 - tile * kGcTile) * 16;
+#pragma unroll
+        for (int jj = 0; jj < 8; jj++) {
+            const int j = 7 - jj;
+            const bool in = j < lim;
+            const float v = rd.get(j) + bias;
+            const float dl = in ? (a.softplus ? softplus_fast(v) : v) : 0.f;
+            float dy = (active && in) ? ro.get(j) : 0.f;
+            if constexpr (HAS_Z) {
+                const float zj = rz.get(j);
+                dy *= zj * rcp_approx(1.f + ex2_approx(-zj * kLog2e));
+            }
+            const float yk = dl - sdc;
+            const float tk = sd + yk;
+            sdc = (tk - sd) - yk;
+            sd = tk;
+            const pf2 dl2 = pf2_make(dl, dl), dy2 = pf2_make(dy, dy);
+            const float* cr = crow + j * 16;
+#pragma unroll
+            for (int p = 0; p < kFNP; p++) {
+                const pf2 C2 = *reinterpret_cast<const pf2*>(cr + 2 * p);
+                const pf2 ab = pf2_ex2(pf2_mul(dl2, A2L[p]));
+                G[p] = pf2_mul(pf2_fma(dy2, C2, G[p]), ab);
+            }
+        }
+    }
+    if (!active) return;
+    float* gl = a.gloc + ((int64_t)seg * chans + chan) * 16;
+#pragma unroll
+    for (int p = 0; p < kFNP; p++) reinterpret_cast<pf2*>(gl)[p] = G[p];
+    a.sumdl[(int64_t)seg * chans + chan] = sd;
+}
+
 template <typename Tg, bool ZOH, bool HAS_Z>
-__global__ void __launch_bounds__(kFThreads)
-scan_bwd_fast_kernel(const BwdArgs a, const int* flag) {
+__global__ void __launch_bounds__(kSThreads)
+scan_bwd_seg_kernel(const BwdArgs a, const int* flag) {
     using Tin = __nv_bfloat16;
     if (ZOH && *flag) return;   // some A == 0: the accurate kernel takes this call
     extern __shared__ __align__(16) unsigned char smem_b[];
@@ -412,13 +529,20 @@ scan_bwd_fast_kernel(const BwdArgs a, const int* flag) {
     pf2* ckb = reinterpret_cast<pf2*>(smem_b + kFOffCk) + warp * 2 * kFNP * 32;
     uint4* raw = reinterpret_cast<uint4*>(smem_b + kFOffRaw) + warp * 2 * 4 * 32;
     const int64_t b = blockIdx.y;
-    const int64_t d_raw = (int64_t)blockIdx.x * kFChans + tid;
+    const int seg = (int)blockIdx.z;
+    const int64_t d_raw = (int64_t)blockIdx.x * kSChans + tid;
     const bool active = d_raw < a.dim;
     const int64_t d = active ? d_raw : a.dim - 1;   // idle threads shadow a valid channel
+    const int64_t chans = a.batch * a.dim;
     const int64_t chan = b * a.dim + d;
+    const int64_t t_begin = (int64_t)seg * a.seg_len;
+    const int64_t t_end = (t_begin + a.seg_len < a.seqlen) ? t_begin + a.seg_len : a.seqlen;
+    const int64_t sb_begin = t_begin / kFSub, sb_end = ceil_div(t_end, (int64_t)kFSub);
+    const pf2 LOG2E2 = pf2_make(kLog2e, kLog2e);
 
     // {A, 1/A} per pair in shared memory (own entries only); states past dstate
-    // get A = -1 with B = C = h = G = 0, so they contribute nothing
+    // get A = -1 with B = C = h = G = 0, so they contribute nothing.  Gc: the
+    // adjoint entering the segment from its right (Abar_{t+1} G_{t+1}).
     pf2 Gc[kFNP], dA1[kFNP], dA2[kFNP];
 #pragma unroll
     for (int p = 0; p < kFNP; p++) {
@@ -429,14 +553,33 @@ scan_bwd_fast_kernel(const BwdArgs a, const int* flag) {
             const bool on = n < a.dstate;
             av[q] = on ? __ldg(a.A + d * a.sA + n) : -1.f;
             ia[q] = ZOH ? rcp_approx(av[q]) : 0.f;   // A != 0 here
-            gv[q] = (active && on && a.dhN != nullptr) ? __ldg(a.dhN + chan * a.sst + n) : 0.f;
+            gv[q] = (active && on && a.dhN != nullptr && seg == a.nseg - 1) ? __ldg(a.dhN + chan * a.sst + n) : 0.f;
         }
         cst[p * 32 + lane] = make_ulonglong2(pf2_make(av[0], av[1]), pf2_make(ia[0], ia[1]));
         Gc[p] = pf2_make(gv[0], gv[1]);
         dA1[p] = 0ull;
         dA2[p] = 0ull;
     }
-    const pf2 LOG2E2 = pf2_make(kLog2e, kLog2e);
+    if (active && seg < a.nseg - 1) {
+        // compose the segments to the right, last first, starting from dfinal_state
+#pragma unroll
+        for (int p = 0; p < kFNP; p++) {
+            if (a.dhN == nullptr) break;
+            const int n = 2 * p;
+            Gc[p] = pf2_make(n < a.dstate ? __ldg(a.dhN + chan * a.sst + n) : 0.f,
+                             n + 1 < a.dstate ? __ldg(a.dhN + chan * a.sst + n + 1) : 0.f);
+        }
+        for (int s2 = a.nseg - 1; s2 > seg; --s2) {
+            const float sdl = a.sumdl[(int64_t)s2 * chans + chan];
+            const pf2 sdl2 = pf2_make(sdl, sdl);
+            const pf2* gl = reinterpret_cast<const pf2*>(a.gloc + ((int64_t)s2 * chans + chan) * 16);
+#pragma unroll
+            for (int p = 0; p < kFNP; p++) {
+                const pf2 P = pf2_ex2(pf2_mul(sdl2, pf2_mul(cst[p * 32 + lane].x, LOG2E2)));
+                Gc[p] = pf2_fma(P, Gc[p], gl[p]);
+            }
+        }
+    }
     const float Dd = a.D ? __ldg(a.D + d) : 0.f;
     const float bias = a.bias ? __ldg(a.bias + d) : 0.f;
     float dDacc = 0.f, dbacc = 0.f;
@@ -450,7 +593,6 @@ scan_bwd_fast_kernel(const BwdArgs a, const int* flag) {
     const Tin* Cb = reinterpret_cast<const Tin*>(a.C) + b * a.sC_b + grp * a.sC_g;
     const bool vec_in = a.vec_u && a.vec_dt && a.vec_do && (!HAS_Z || a.vec_z);
     const bool ck16 = a.dstate == 16;
-    const int64_t nsb = ceil_div(a.seqlen, (int64_t)kFSub);
     auto limit = [&](int64_t sb) -> int {
         const int64_t r = a.seqlen - sb * kFSub;
         return (int)(r < kFSub ? r : kFSub);
@@ -459,7 +601,7 @@ scan_bwd_fast_kernel(const BwdArgs a, const int* flag) {
     // when sb is the first sub-block walked of its 8-step block, that block's
     // u, delta, dout, z rows (-> buffer (sb >> 1) & 1)
     auto prefetch = [&](int64_t sb) {
-        if (sb == nsb - 1 || (sb & 1)) {
+        if (sb == sb_end - 1 || (sb & 1)) {
             const int64_t t0 = (sb >> 1) * 8;
             const int64_t r = a.seqlen - t0;
             const int lim = (int)(r < 8 ? r : 8);
@@ -485,7 +627,7 @@ scan_bwd_fast_kernel(const BwdArgs a, const int* flag) {
         }
         cp_async_commit();
     };
-    prefetch(nsb - 1);
+    prefetch(sb_end - 1);
 
     // transpose: lane l sums float columns 2(l&15), 2(l&15)+1 over half the rows,
     // then the halves combine; it keeps column f = 2(l&15) + (l>>4) of the row
@@ -497,11 +639,11 @@ scan_bwd_fast_kernel(const BwdArgs a, const int* flag) {
     int64_t cur_tile = -1;
     int it = 0;
 #pragma unroll 1
-    for (int64_t sb = nsb - 1; sb >= 0; --sb, ++it) {
+    for (int64_t sb = sb_end - 1; sb >= sb_begin; --sb, ++it) {
         const int64_t t0 = sb * kFSub;
         const int cnt = limit(sb);
         const int64_t tile = t0 / kTile;
-        if (sb > 0) prefetch(sb - 1);
+        if (sb > sb_begin) prefetch(sb - 1);
         else cp_async_commit();
         cp_async_wait<1>();                                   // this sub-block's slots have landed
         if (tile != cur_tile) {
@@ -547,10 +689,11 @@ scan_bwd_fast_kernel(const BwdArgs a, const int* flag) {
             u2[j] = pf2_make(uu, uu);
             dy2[j] = pf2_make(dy[j], dy[j]);
         }
+        // per-step sums over states: du, ddelta, readout y
         pf2 du2[kFSub], dd2[kFSub], yv2[kFSub];
 #pragma unroll
         for (int j = 0; j < kFSub; j++) du2[j] = dd2[j] = yv2[j] = 0ull;
-        float* redw = red + ((it & 1) * kFWarps + warp) * 4 * 32;
+        float* redw = red + ((it & 1) * kSWarps + warp) * 4 * 32;
 
 #pragma unroll
         for (int c = 0; c < kFNP / 2; c++) {
@@ -581,10 +724,10 @@ scan_bwd_fast_kernel(const BwdArgs a, const int* flag) {
                     ab[q][j] = pf2_ex2(pf2_mul(dl2[j], A2L[q]));
                     pf2 inc;
                     if constexpr (ZOH) {
-                        cf[q][j] = pf2_fma(ab[q][j], IA[q], NI[q]);          // (Abar - 1) / A
+                        cf[q][j] = pf2_fma(ab[q][j], IA[q], NI[q]);            // (Abar - 1) / A
                         inc = pf2_mul(cf[q][j], pf2_mul(u2[j], bc.x));
                     } else {
-                        inc = pf2_mul(u2[j], bc.x);                          // delta u B
+                        inc = pf2_mul(u2[j], bc.x);                              // delta u B
                     }
                     hs[q][j + 1] = pf2_fma(ab[q][j], hs[q][j], inc);
                     if constexpr (HAS_Z) yv2[j] = pf2_fma(bc.y, hs[q][j + 1], yv2[j]);
@@ -606,20 +749,20 @@ scan_bwd_fast_kernel(const BwdArgs a, const int* flag) {
                     const ulonglong2 bc = *reinterpret_cast<const ulonglong2*>(bc0 + j * kRowF + 4 * (2 * c + q));
                     const pf2 Gt = pf2_fma(dy2[j], bc.y, G[q]);
                     const pf2 dC = pf2_mul(dy2[j], hs[q][j + 1]);
-                    const pf2 da = pf2_mul(Gt, hs[q][j]);                // dL/dAbar
+                    const pf2 da = pf2_mul(Gt, hs[q][j]);                   // dL/dAbar
                     const pf2 gb = pf2_mul(Gt, bc.x);
-                    const pf2 qa = pf2_mul(dl2[j], ab[q][j]);            // dAbar/dA
+                    const pf2 qa = pf2_mul(dl2[j], ab[q][j]);               // dAbar/dA
                     pf2 dB;
                     if constexpr (ZOH) {
                         du2[j] = pf2_fma(gb, cf[q][j], du2[j]);
                         dB = pf2_mul(u2[j], pf2_mul(Gt, cf[q][j]));
-                        const pf2 dcf = pf2_mul(u2[j], gb);              // dL/dcoef
+                        const pf2 dcf = pf2_mul(u2[j], gb);                 // dL/dcoef
                         dd2[j] = pf2_fma(ab[q][j], pf2_fma(da, A2[q], dcf), dd2[j]);
                         a1[q] = pf2_fma(da, qa, a1[q]);
                         a2[q] = pf2_fma(dcf, pf2_sub(qa, cf[q][j]), a2[q]);   // times 1/A at the end
                     } else {
                         du2[j] = pf2_fma(dl2[j], gb, du2[j]);
-                        dB = pf2_mul(u2[j], Gt);                         // delta u G
+                        dB = pf2_mul(u2[j], Gt);                            // delta u G
                         dd2[j] = pf2_fma(pf2_mul(da, A2[q]), ab[q][j], pf2_fma(pf2_make(uj[j], uj[j]), gb, dd2[j]));
                         a1[q] = pf2_fma(da, qa, a1[q]);
                     }
@@ -673,36 +816,37 @@ scan_bwd_fast_kernel(const BwdArgs a, const int* flag) {
         // handles (tensor, state n, step j) with j fastest
         __syncthreads();
 #pragma unroll
-        for (int k = 0; k < 128 / kFThreads; k++) {
-            const int idx = k * kFThreads + tid;
+        for (int k = 0; k < 128 / kSThreads; k++) {
+            const int idx = k * kSThreads + tid;
             const int j = idx & 3, n = (idx >> 2) & 15, tsr = idx >> 6;
             if (j < cnt) {
                 const int f = 8 * j + 4 * ((n >> 1) & 1) + 2 * tsr + (n & 1);
                 const int l = ((f & 1) << 4) | (f >> 1);
-                const float* rs = red + (it & 1) * kFWarps * 4 * 32 + (n >> 2) * 32 + l;
+                const float* rs = red + (it & 1) * kSWarps * 4 * 32 + (n >> 2) * 32 + l;
                 float s2 = 0.f;
 #pragma unroll
-                for (int w = 0; w < kFWarps; w++) s2 += rs[w * 4 * 32];
+                for (int w = 0; w < kSWarps; w++) s2 += rs[w * 4 * 32];
                 a.part_bc[(((b * a.nblk + blockIdx.x) * 2 + tsr) * 16 + n) * a.seqlen + t0 + j] = s2;
             }
         }
     }
     cp_async_wait<0>();
     if (!active) return;
+    const int64_t slot = (int64_t)seg * chans + chan;
 #pragma unroll
     for (int p = 0; p < kFNP; p++) {
         pf2 dA = dA1[p];
         if constexpr (ZOH) dA = pf2_fma(dA2[p], cst[p * 32 + lane].y, dA);
         const int n = 2 * p;
-        if (a.dh0 != nullptr) {
+        if (a.dh0 != nullptr && seg == 0) {
             if (n < a.dstate) a.dh0[chan * a.sst + n] = pf2_lo(Gc[p]);
             if (n + 1 < a.dstate) a.dh0[chan * a.sst + n + 1] = pf2_hi(Gc[p]);
         }
-        a.part_A[chan * 16 + n] = pf2_lo(dA);
-        a.part_A[chan * 16 + n + 1] = pf2_hi(dA);
+        a.part_A[slot * 16 + n] = pf2_lo(dA);
+        a.part_A[slot * 16 + n + 1] = pf2_hi(dA);
     }
-    a.part_D[chan] = dDacc;
-    a.part_bias[chan] = dbacc;
+    a.part_D[slot] = dDacc;
+    a.part_bias[slot] = dbacc;
 }
 
 // flag[0] = 1 when some A[d, n] == 0 (the ZOH limit needs the accurate path)
@@ -760,22 +904,28 @@ __global__ void bwd_reduce_bc_kernel(const BwdArgs a, float* dB, float* dC) {
     if (out) out[((b * a.ngroups + grp) * a.sBo + n) * a.seqlen + t] = s;
 }
 
-// dA[d, n], dD[d], dbias[d]: sums over the batch, in batch order.
-__global__ void bwd_reduce_params_kernel(const BwdArgs a, float* dA, float* dD, float* dbias) {
+// dA[d, n], dD[d], dbias[d]: sums over the segments and the batch, in that
+// order.  The accurate kernel (flag set) writes segment 0 only.
+__global__ void bwd_reduce_params_kernel(const BwdArgs a, const int* flag, float* dA, float* dD, float* dbias) {
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= a.dim * 18) return;
     const int64_t d = i / 18;
     const int k = (int)(i % 18);
+    const int nseg = *flag ? 1 : a.nseg;
+    const int64_t chans = a.batch * a.dim;
     float s = 0.f;
     if (k < 16) {
         if (k >= a.dstate) return;
-        for (int64_t b = 0; b < a.batch; b++) s += a.part_A[(b * a.dim + d) * 16 + k];
+        for (int g = 0; g < nseg; g++)
+            for (int64_t b = 0; b < a.batch; b++) s += a.part_A[(g * chans + b * a.dim + d) * 16 + k];
         if (dA) dA[d * a.sA + k] = s;
     } else if (k == 16) {
-        for (int64_t b = 0; b < a.batch; b++) s += a.part_D[b * a.dim + d];
+        for (int g = 0; g < nseg; g++)
+            for (int64_t b = 0; b < a.batch; b++) s += a.part_D[g * chans + b * a.dim + d];
         if (dD && a.g_first) dD[d] = s;                   // the same in every state group
     } else {
-        for (int64_t b = 0; b < a.batch; b++) s += a.part_bias[b * a.dim + d];
+        for (int g = 0; g < nseg; g++)
+            for (int64_t b = 0; b < a.batch; b++) s += a.part_bias[g * chans + b * a.dim + d];
         if (dbias) dbias[d] = a.g_first ? s : dbias[d] + s;   // summed across state groups
     }
 }
@@ -784,9 +934,29 @@ __global__ void bwd_reduce_params_kernel(const BwdArgs a, float* dA, float* dD, 
 // Host side
 
 struct BwdLayout {
-    size_t ckpt, fwd_ws, part_bc, part_A, part_D, gacc, total;   // gacc: state-group slices
+    size_t ckpt, fwd_ws, part_bc, part_A, part_D, gloc, sumdl, gacc, total;   // gacc: state-group slices
     bool own_ckpt;
+    int nseg;
+    int64_t seg_len;
 };
+
+// Segments of the fast (bf16) backward: enough that one wave of the kernel's
+// CTAs (kSPerSM per SM) is filled, each segment a multiple of 64 steps and
+// at least 256 steps long.  float32 inputs take the accurate kernel, one segment.
+static void bwd_segments(const ssm_scan_bwd_params* p, int num_sms, int* nseg, int64_t* seg_len) {
+    int64_t n = 1;
+    if (p->in_dtype == SSM_BF16 && p->seqlen > 0) {
+        const int64_t ctas = ceil_div(p->dim, (int64_t)kSChans) * p->batch;
+        const int64_t want = ((int64_t)kSPerSM * num_sms) / ctas;
+        const int64_t max_seg = p->seqlen / 256;
+        n = want < max_seg ? want : max_seg;
+        if (n > 64) n = 64;
+        if (n < 1) n = 1;
+    }
+    const int64_t len = ceil_div(ceil_div(p->seqlen > 0 ? p->seqlen : 1, n), (int64_t)64) * 64;
+    *seg_len = len;
+    *nseg = (int)ceil_div(p->seqlen > 0 ? p->seqlen : 1, len);
+}
 
 static size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
@@ -821,13 +991,16 @@ static BwdLayout bwd_layout(const ssm_scan_bwd_params* p, int num_sms) {
         f.checkpoints = reinterpret_cast<float*>(16);   // only sizes matter here
         l.fwd_ws = round256(fwd_workspace_bytes(&f, num_sms));
     }
+    bwd_segments(p, num_sms, &l.nseg, &l.seg_len);
     const int64_t nblk = ceil_div(p->dim, (int64_t)kFChans);
     l.part_bc = round256((size_t)(p->batch * nblk * 2 * 16 * p->seqlen) * 4);
-    l.part_A = round256((size_t)(chans * 16) * 4);
-    l.part_D = round256((size_t)chans * 4);
+    l.part_A = round256((size_t)(l.nseg * chans * 16) * 4);
+    l.part_D = round256((size_t)(l.nseg * chans) * 4);
+    l.gloc = l.nseg > 1 ? round256((size_t)(l.nseg * chans * 16) * 4) : 0;
+    l.sumdl = l.nseg > 1 ? round256((size_t)(l.nseg * chans) * 4) : 0;
     // more than 16 states: du, ddelta, dz of every state group in fp32 slices
     l.gacc = p->dstate > 16 ? round256((size_t)(3 * ceil_div(p->dstate, (int64_t)16) * chans * p->seqlen) * 4) : 0;
-    l.total = l.ckpt + l.fwd_ws + l.part_bc + l.part_A + 2 * l.part_D + 256 + l.gacc;   // + the A == 0 flag
+    l.total = l.ckpt + l.fwd_ws + l.part_bc + l.part_A + 2 * l.part_D + l.gloc + l.sumdl + 256 + l.gacc;   // + the A == 0 flag
     return l;
 }
 
@@ -876,8 +1049,8 @@ static bool al16(const void* ptr, ssm_strides s, int esize) {
 
 template <auto Kern>
 static cudaError_t launch_bwd_kernel(const BwdArgs& a, int* flag, int threads, int64_t chans_per_cta, int bytes,
-                                     cudaStream_t st) {
-    const dim3 grid((unsigned)ceil_div(a.dim, chans_per_cta), (unsigned)a.batch);
+                                     cudaStream_t st, unsigned zdim = 1) {
+    const dim3 grid((unsigned)ceil_div(a.dim, chans_per_cta), (unsigned)a.batch, zdim);
     cudaError_t e = prepare_kernel<Kern>(bytes);
     if (e != cudaSuccess) return e;
     Kern<<<grid, threads, bytes, st>>>(a, flag);
@@ -890,10 +1063,17 @@ static cudaError_t launch_bwd_acc(const BwdArgs& a, int* flag, cudaStream_t st) 
     return launch_bwd_kernel<scan_bwd_kernel<Tin, Tg, ZOH, HAS_Z>>(a, flag, kBwdThreads, kBwdThreads,
                                                                    kBwdAccSmemBytes, st);
 }
+// The fast path: the carry pre-pass (more than one segment), then the
+// segmented kernel over every (channel block, batch row, segment).
 template <typename Tg, bool ZOH, bool HAS_Z>
 static cudaError_t launch_bwd_fast(const BwdArgs& a, int* flag, cudaStream_t st) {
-    return launch_bwd_kernel<scan_bwd_fast_kernel<Tg, ZOH, HAS_Z>>(a, flag, kFThreads, kFChans,
-                                                                   kBwdFastSmemBytes, st);
+    if (a.nseg > 1) {
+        cudaError_t e = launch_bwd_kernel<bwd_gcarry_kernel<HAS_Z>>(a, flag, kSThreads, kSChans, kGcSmemBytes, st,
+                                                                    (unsigned)(a.nseg - 1));
+        if (e != cudaSuccess) return e;
+    }
+    return launch_bwd_kernel<scan_bwd_seg_kernel<Tg, ZOH, HAS_Z>>(a, flag, kSThreads, kSChans, kBwdSegSmemBytes,
+                                                                  st, (unsigned)a.nseg);
 }
 
 template <typename Tin, typename Tg>
@@ -978,9 +1158,13 @@ cudaError_t launch_scan_bwd(const ssm_scan_bwd_params* p, void* ws, int num_sms,
     a.part_A = reinterpret_cast<float*>(wp + l.part_bc);
     a.part_D = reinterpret_cast<float*>(wp + l.part_bc + l.part_A);
     a.part_bias = reinterpret_cast<float*>(wp + l.part_bc + l.part_A + l.part_D);
+    a.nseg = l.nseg;
+    a.seg_len = l.seg_len;
+    a.gloc = l.gloc ? reinterpret_cast<float*>(wp + l.part_bc + l.part_A + 2 * l.part_D) : nullptr;
+    a.sumdl = l.sumdl ? reinterpret_cast<float*>(wp + l.part_bc + l.part_A + 2 * l.part_D + l.gloc) : nullptr;
     const bool zoh = p->bbar_mode == SSM_BBAR_ZOH;
     const bool has_z = p->z != nullptr;
-    int* flag = reinterpret_cast<int*>(wp + l.part_bc + l.part_A + 2 * l.part_D);
+    int* flag = reinterpret_cast<int*>(wp + l.part_bc + l.part_A + 2 * l.part_D + l.gloc + l.sumdl);
     cudaError_t e = cudaMemsetAsync(flag, 0, sizeof(int), st);
     if (e != cudaSuccess) return e;
     if (zoh) {
@@ -994,7 +1178,8 @@ cudaError_t launch_scan_bwd(const ssm_scan_bwd_params* p, void* ws, int num_sms,
     a.sB_g = p->ngroups > 1 ? p->B_group_stride : 0;
     a.sC_g = p->ngroups > 1 ? p->C_group_stride : 0;
     a.ck_P = (p->dstate + 1) / 2; a.ck_p0 = 0;
-    float* gbuf = l.gacc ? reinterpret_cast<float*>(wp + l.part_bc + l.part_A + 2 * l.part_D + 256) : nullptr;
+    float* gbuf = l.gacc ? reinterpret_cast<float*>(wp + l.part_bc + l.part_A + 2 * l.part_D + l.gloc + l.sumdl + 256)
+                         : nullptr;
     // one pass per group of at most 16 states (a single pass for d_state <= 16);
     // with several groups each writes fp32 du, ddelta, dz to its own slices and
     // only the first adds the D skip
@@ -1032,7 +1217,7 @@ cudaError_t launch_scan_bwd(const ssm_scan_bwd_params* p, void* ws, int num_sms,
         bwd_reduce_bc_kernel<<<g2, 256, 0, st>>>(ga, p->dB ? p->dB + (int64_t)n0 * p->seqlen : nullptr,
                                                  p->dC ? p->dC + (int64_t)n0 * p->seqlen : nullptr);
         bwd_reduce_params_kernel<<<(unsigned)ceil_div(p->dim * 18, 256), 256, 0, st>>>(
-            ga, p->dA ? p->dA + n0 : nullptr, p->dD, p->ddelta_bias);
+            ga, flag, p->dA ? p->dA + n0 : nullptr, p->dD, p->ddelta_bias);
         count_launches(2);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;

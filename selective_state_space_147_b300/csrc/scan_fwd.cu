@@ -56,23 +56,23 @@ struct FwdPlan {
 };
 
 
-// Schedule: lanes per channel G and the number of sequence segments.  The
-// automatic choice takes the fewest lanes that still give every SM at least 4
-// warps, and segments only when even G = 4 leaves SMs short of work; `s`
-// (tests and tuning) overrides either choice.
+// Schedule: lanes per channel G and the number of sequence segments.  One lane
+// per channel when the channels give every SM at least 4 warps; else two lanes
+// per channel when that does; else one lane per channel and enough sequence
+// segments for about 16 warps per SM (measured on B300: splitting a channel's
+// states over 4 lanes costs more than the extra segment pass).  `s` (tests and
+// tuning) overrides either choice.
 static FwdPlan plan_fwd(const ssm_scan_fwd_params* p, int num_sms, const ssm_fwd_schedule* s) {
     FwdPlan pl;
     const int64_t want_warps = (int64_t)num_sms * 4;
-    pl.G = 4;
-    for (int G : {1, 2, 4}) {
-        const int64_t warps = ceil_div(p->dim, 32 / G) * p->batch;
-        if (warps >= want_warps) { pl.G = G; break; }
-    }
+    pl.G = 1;
+    if (ceil_div(p->dim, (int64_t)32) * p->batch < want_warps && ceil_div(p->dim, (int64_t)16) * p->batch >= want_warps)
+        pl.G = 2;
     if (s != nullptr && s->lanes_per_channel != 0) pl.G = s->lanes_per_channel;
     pl.generic = s != nullptr && s->generic_path != 0;
     const int64_t warps = ceil_div(p->dim, 32 / pl.G) * p->batch;
     int64_t nseg = 1;
-    if (warps < want_warps) nseg = ceil_div((int64_t)num_sms * 8, warps);
+    if (warps < want_warps) nseg = ceil_div((int64_t)num_sms * 16, warps);
     if (s != nullptr && s->segments > 0) nseg = s->segments;
     const int64_t max_seg = ceil_div(p->seqlen, 4 * kTile);   // segments of at least 256 steps
     if (nseg > max_seg) nseg = max_seg;

@@ -144,3 +144,31 @@ def test_long_sequence_sampled_channels():
         e = rel_err(to_np(y[0, dd]), ref[0, 0])
         eh = rel_err(to_np(hN[0, dd]), href[0, 0])
         assert e <= TOL_BF16 and eh <= TOL_BF16, f"channel {dd}: out {e:.3e}, final state {eh:.3e}"
+
+
+def test_1p4b_whole_batch_row(layer_1p4b):
+    """Every channel of batch row 0 (4096 channels, full L = 16384): forward outputs,
+    du, ddelta, dz, and dB, dC of that row -- the complete cross-channel sums --
+    against the oracle, run multithreaded in chunks of 512 channels."""
+    g, y, gr, (b, d, T, N) = layer_1p4b["g"], layer_1p4b["y"], layer_1p4b["grads"], layer_1p4b["shape"]
+    threads = oracle.default_threads()
+    dB = np.zeros((N, T))
+    dC = np.zeros((N, T))
+    worst = {}
+    for c0 in range(0, d, 512):
+        sl = lambda t: t[0:1, c0:c0 + 512].cpu()
+        u, dt, z, dout = sl(g["u"]), sl(g["dt"]), sl(g["z"]), sl(g["dout"])
+        A, D, bias = g["A"][c0:c0 + 512].cpu(), g["D"][c0:c0 + 512].cpu(), g["bias"][c0:c0 + 512].cpu()
+        Bm, Cm = g["B"][0:1].cpu(), g["C"][0:1].cpu()
+        ref, _ = oracle.scan_fwd(u, dt, A, Bm, Cm, D, bias, z, threads=threads)
+        ok, excess = _bf16_out_ok(to_np(y[0:1, c0:c0 + 512]), ref)
+        assert ok, f"channels {c0}..{c0 + 511}: forward beyond the bf16-output bound by {excess:.3e}"
+        rb = oracle.scan_bwd(u, dt, A, Bm, Cm, dout, D, bias, z, threads=threads)
+        for k, rk in (("du", "du"), ("ddelta", "ddt"), ("dz", "dz")):
+            worst[k] = max(worst.get(k, 0.0), rel_err(to_np(gr[k][0:1, c0:c0 + 512]), rb[rk]))
+        dB += rb["dB"][0]
+        dC += rb["dC"][0]
+    bad = {k: v for k, v in worst.items() if v > TOL_BF16}
+    assert not bad, f"row 0 gradients beyond {TOL_BF16}: {bad}"
+    assert rel_err(to_np(gr["dB"][0]), dB) <= TOL_BF16
+    assert rel_err(to_np(gr["dC"][0]), dC) <= TOL_BF16
