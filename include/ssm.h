@@ -66,7 +66,8 @@ typedef enum {
     SSM_ERR_UNSUPPORTED = -2, /* a valid request this library does not implement */
     SSM_ERR_MISALIGNED = -3,  /* a pointer that must be aligned (workspace, checkpoints) is not */
     SSM_ERR_WORKSPACE = -4,   /* workspace missing or smaller than required */
-    SSM_ERR_CUDA = -5         /* a CUDA runtime error (see ssm_last_error) */
+    SSM_ERR_CUDA = -5,        /* a CUDA runtime error (see ssm_last_error) */
+    SSM_ERR_TIMEOUT = -6      /* a bounded device-side wait gave up (ssm_device_status) */
 } ssm_status;
 
 typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype;
@@ -473,6 +474,54 @@ SSM_API ssm_status ssm_probe_unit_rates(double* fp32_lanes_per_sm_clock, double*
 
 /* ------------------------------------------------------------------------ */
 /* Human-readable name of a status code (static string). */
+/* ------------------------------------------------------------------------
+ * Projections beside the scan, on the tensor cores: x_proj and dt_proj.
+ * "Mamba 模型" (gaos6e.github.io) block flowchart: the conv output Xc_t feeds
+ * the x_proj node, which produces dt_raw_t, B_t and C_t; dt_raw_t feeds the
+ * dt_proj + softplus node, which produces delta_t.  Both are the same batched
+ * product with a weight shared by every token:
+ *
+ *   out[b] (m x n) = W (m x k) X[b] (k x n)        (+ bias, optional softplus)
+ *
+ * with X[b] channel-major and its n tokens contiguous -- the layout of the
+ * scan's inputs -- so x_proj (W = W_x, (R + 2N) x D; X = the conv output
+ * (batch, D, L)) writes dt_raw, B and C as rows [0, R), [R, R+N), [R+N, R+2N)
+ * of one (batch, R + 2N, L) tensor whose B and C rows the scan reads as
+ * (batch, N, L) views, and dt_proj (W = W_dt, D x R; X = those dt_raw rows)
+ * writes delta as (batch, D, L).
+ *
+ *   W    : bf16, row-major, row stride ldw elements (>= k)
+ *   X    : bf16, (batch, k, n) with n contiguous; row stride ldx (>= n) and
+ *          batch stride x_batch_stride, in elements
+ *   out  : bf16, (batch, m, n) with n contiguous; row stride ldo (>= n),
+ *          batch stride out_batch_stride
+ *   bias : (m) float32 or NULL, added to every row of the product
+ *   epilogue : 0 = the product (+ bias); 1 = softplus(product + bias)
+ * W, X and out must be 16-byte aligned and every stride a multiple of 8
+ * elements (SSM_ERR_MISALIGNED otherwise); batch <= 65535.  Products are bf16
+ * x bf16 with fp32 accumulation (tcgen05), rounded to bf16 once.  No
+ * workspace.  The kernel's waits are bounded: if one gives up, the call's
+ * outputs are undefined and ssm_device_status reports SSM_ERR_TIMEOUT. */
+typedef struct {
+    int64_t batch, m, n, k;
+    const void* W;
+    int64_t ldw;
+    const void* X;
+    int64_t ldx, x_batch_stride;
+    void* out;
+    int64_t ldo, out_batch_stride;
+    const float* bias;
+    int epilogue;
+} ssm_proj_params;
+
+SSM_API ssm_status ssm_proj(const ssm_proj_params* p, ssm_stream_t stream);
+
+/* Device-side status of the library's asynchronous kernels on the current
+ * device: *status receives SSM_OK or the first error a kernel recorded (so far
+ * only SSM_ERR_TIMEOUT, from a bounded wait that gave up); clear != 0 resets
+ * it.  Synchronises with the device (it reads a device word). */
+SSM_API ssm_status ssm_device_status(int* status, int clear);
+
 SSM_API const char* ssm_status_string(ssm_status s);
 /* Message describing the calling thread's last failure ("" if none). */
 SSM_API const char* ssm_last_error(void);

@@ -262,3 +262,17 @@ def ssd_fwd(x, dt, A, B, C, D=None, dt_bias=None, h0=None, delta_softplus=True, 
         with ThreadPoolExecutor(len(rs)) as ex:
             list(ex.map(run, rs))
     return out, hN
+
+
+def proj(W, X, bias=None, softplus: bool = False):
+    """The x_proj / dt_proj product of "Mamba 模型" (block flowchart): out[b] =
+    W X[b] for W (m, k) and X (batch, k, n), plus bias[:, None] and a softplus
+    when asked, in fp64.  The product is numpy's matmul (a library primitive);
+    softplus is max(v, 0) + log1p(exp(-|v|))."""
+    W, X, bias = _f64(W), _f64(X), _f64(bias)
+    out = np.matmul(W[None], X)
+    if bias is not None:
+        out = out + bias[None, :, None]
+    if softplus:
+        out = np.maximum(out, 0.0) + np.log1p(np.exp(-np.abs(out)))
+    return out

@@ -30,7 +30,8 @@ SSM_OK = 0
 SSM_F32, SSM_BF16 = 0, 1
 SSM_BBAR_ZOH, SSM_BBAR_SIMPLE = 0, 1
 STATUS_NAMES = {0: "SSM_OK", -1: "SSM_ERR_INVALID_ARG", -2: "SSM_ERR_UNSUPPORTED",
-                -3: "SSM_ERR_MISALIGNED", -4: "SSM_ERR_WORKSPACE", -5: "SSM_ERR_CUDA"}
+                -3: "SSM_ERR_MISALIGNED", -4: "SSM_ERR_WORKSPACE", -5: "SSM_ERR_CUDA",
+                -6: "SSM_ERR_TIMEOUT"}
 
 _i64, _int, _vp, _fp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p
 
@@ -146,6 +147,20 @@ class SsdFwdParams(ctypes.Structure):
         ("dt_bias", _vp), ("delta_softplus", _int), ("out_dtype", _int), ("h0", _vp), ("final_state", _vp),
         ("out", _vp),
     ]
+
+
+class ProjParams(ctypes.Structure):
+    _fields_ = [
+        ("batch", _i64), ("m", _i64), ("n", _i64), ("k", _i64),
+        ("W", _vp), ("ldw", _i64), ("X", _vp), ("ldx", _i64), ("x_batch_stride", _i64),
+        ("out", _vp), ("ldo", _i64), ("out_batch_stride", _i64), ("bias", _vp), ("epilogue", _int),
+    ]
+
+
+_lib.ssm_proj.argtypes = [ctypes.POINTER(ProjParams), _vp]
+_lib.ssm_proj.restype = _int
+_lib.ssm_device_status.argtypes = [ctypes.POINTER(_int), _int]
+_lib.ssm_device_status.restype = _int
 
 
 class FwdSchedule(ctypes.Structure):
@@ -701,3 +716,54 @@ def probe_unit_rates() -> dict:
     _check(_lib.ssm_probe_unit_rates(*(ctypes.byref(x) for x in v)))
     return {"fp32_lanes_per_sm_clock": v[0].value, "f32x2_lanes_per_sm_clock": v[1].value,
             "ex2_per_sm_clock": v[2].value}
+
+
+def ssm_proj(W, X, *, bias=None, softplus: bool = False, out: Optional[torch.Tensor] = None, stream=None):
+    """Batched projection out[b] = W @ X[b] (+ bias[:, None]), softplus'd when asked.
+    W: (m, k) bf16 (row stride a multiple of 8); X: (batch, k, n) bf16 with n contiguous
+    (strided views allowed, strides multiples of 8).  Returns out (batch, m, n) bf16."""
+    _need_cuda("W", W)
+    _need_cuda("X", X)
+    if W.dtype != torch.bfloat16 or X.dtype != torch.bfloat16:
+        raise ValueError("W and X must be bfloat16")
+    if W.dim() != 2 or X.dim() != 3 or W.stride(1) != 1 or X.stride(2) != 1:
+        raise ValueError("W must be (m, k) and X (batch, k, n), both with the last dimension contiguous")
+    m, k = W.shape
+    batch, k2, n = X.shape
+    if k2 != k:
+        raise ValueError(f"W is {tuple(W.shape)} but X has {k2} rows")
+    if out is None:
+        out = torch.empty(batch, m, n, dtype=torch.bfloat16, device=X.device)
+    if out.dtype != torch.bfloat16 or out.stride(2) != 1 or tuple(out.shape) != (batch, m, n):
+        raise ValueError("out must be (batch, m, n) bfloat16 with n contiguous")
+    bias = _f32c("bias", bias)
+    p = ProjParams()
+    p.batch, p.m, p.n, p.k = batch, m, n, k
+    p.W, p.ldw = _ptr(W), W.stride(0)
+    p.X, p.ldx, p.x_batch_stride = _ptr(X), X.stride(1), X.stride(0)
+    p.out, p.ldo, p.out_batch_stride = _ptr(out), out.stride(1), out.stride(0)
+    p.bias = _ptr(bias)
+    p.epilogue = 1 if softplus else 0
+    _check(_lib.ssm_proj(ctypes.byref(p), _stream(stream)))
+    return out
+
+
+def x_dt_proj(xc, W_x, W_dt, dstate: int, *, x_dbl: Optional[torch.Tensor] = None,
+              delta: Optional[torch.Tensor] = None, stream=None):
+    """The x_proj and dt_proj nodes on the conv output xc (batch, D, L): x_dbl = W_x xc
+    with W_x of shape (R + 2 dstate, D), then delta = W_dt x_dbl[:, :R] with W_dt (D, R).
+    Returns (delta (batch, D, L), B, C (batch, dstate, L) views of x_dbl, x_dbl); delta is
+    the projected dt before the per-channel bias and softplus, which the scan applies."""
+    R = W_x.shape[0] - 2 * dstate
+    if R < 1 or tuple(W_dt.shape) != (xc.shape[1], R):
+        raise ValueError("W_x must be (R + 2 dstate, D) and W_dt (D, R)")
+    x_dbl = ssm_proj(W_x, xc, out=x_dbl, stream=stream)
+    delta = ssm_proj(W_dt, x_dbl[:, :R], out=delta, stream=stream)
+    return delta, x_dbl[:, R:R + dstate], x_dbl[:, R + dstate:], x_dbl
+
+
+def device_status(clear: bool = True) -> int:
+    """SSM_OK or the first error a kernel recorded on the current device (synchronises)."""
+    v = _int(0)
+    _check(_lib.ssm_device_status(ctypes.byref(v), 1 if clear else 0))
+    return v.value

@@ -138,13 +138,14 @@ const char* ssm_status_string(ssm_status s) {
         case SSM_ERR_MISALIGNED: return "SSM_ERR_MISALIGNED";
         case SSM_ERR_WORKSPACE: return "SSM_ERR_WORKSPACE";
         case SSM_ERR_CUDA: return "SSM_ERR_CUDA";
+        case SSM_ERR_TIMEOUT: return "SSM_ERR_TIMEOUT";
     }
     return "SSM_ERR_UNKNOWN";
 }
 
 const char* ssm_last_error(void) { return g_err; }
 
-int ssm_abi_version(void) { return 4; }
+int ssm_abi_version(void) { return 5; }
 
 uint64_t ssm_launch_count(void) { return ssm::ssm_launch_count_value(); }
 
@@ -336,6 +337,30 @@ ssm_status ssm_ssd_fwd(const ssm_ssd_fwd_params* p, ssm_stream_t stream) {
         return fail(SSM_ERR_MISALIGNED, "x, B, C must be 16-byte aligned and out 8-byte aligned");
     cudaError_t e = ssm::launch_ssd_fwd(p, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "ssm_ssd_fwd launch");
+    return ok();
+}
+
+ssm_status ssm_proj(const ssm_proj_params* p, ssm_stream_t stream) {
+    if (p == nullptr) return fail(SSM_ERR_INVALID_ARG, "params is NULL");
+    if (p->batch < 1 || p->m < 1 || p->n < 1 || p->k < 1) return fail(SSM_ERR_INVALID_ARG, "bad sizes");
+    if (p->batch > 65535 || p->m > (1LL << 30) || p->n > (1LL << 30) || p->k > (1LL << 30))
+        return fail(SSM_ERR_UNSUPPORTED, "sizes too large");
+    if (!p->W || !p->X || !p->out) return fail(SSM_ERR_INVALID_ARG, "W, X and out are required");
+    if (p->epilogue != 0 && p->epilogue != 1) return fail(SSM_ERR_INVALID_ARG, "epilogue=%d (0 or 1)", p->epilogue);
+    if (p->ldw < p->k || p->ldx < p->n || p->ldo < p->n || p->x_batch_stride < 0 || p->out_batch_stride < 0)
+        return fail(SSM_ERR_INVALID_ARG, "strides smaller than the rows they hold");
+    if (((uintptr_t)p->W | (uintptr_t)p->X | (uintptr_t)p->out) % 16 != 0 ||
+        (p->ldw | p->ldx | p->x_batch_stride | p->ldo | p->out_batch_stride) % 8 != 0)
+        return fail(SSM_ERR_MISALIGNED, "W, X, out must be 16-byte aligned and strides multiples of 8 elements");
+    cudaError_t e = ssm::launch_proj(p, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "ssm_proj launch");
+    return ok();
+}
+
+ssm_status ssm_device_status(int* status, int clear) {
+    if (status == nullptr) return fail(SSM_ERR_INVALID_ARG, "status is NULL");
+    cudaError_t e = ssm::read_device_status(status, clear);
+    if (e != cudaSuccess) return cuda_fail(e, "ssm_device_status");
     return ok();
 }
 

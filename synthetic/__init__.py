@@ -142,6 +142,7 @@ def rows_at(seed: int, stream: int, rows: Sequence[int], row_len: int,
 STREAM = {
     "u": 1, "dt": 2, "z": 3, "B": 4, "C": 5, "D": 6, "bias": 7, "w": 8,
     "dout": 9, "h0": 10, "conv_state": 11, "x": 12, "dhN": 13,
+    "W_x": 30, "W_dt": 31, "dt_proj_bias": 32,
     "ssd_x": 20, "ssd_dt": 21, "ssd_B": 22, "ssd_C": 23, "ssd_A": 24, "ssd_D": 25, "ssd_bias": 26, "ssd_h0": 27,
 }
 
@@ -223,3 +224,12 @@ def conv_inputs(seed: int, batch: int, dim: int, seqlen: int, width: int = 4,
 def decode_stream(kind: str, layer: int, step: int) -> int:
     """Stream id of a per-(layer, step) decode tensor."""
     return ((STREAM[kind] & 0xFF) << 24) | ((layer & 0xFFF) << 12) | (step & 0xFFF)
+
+
+def proj_weights(seed: int, dim: int, dt_rank: int, dstate: int, device="cpu"):
+    """Synthetic x_proj and dt_proj weights (no trained weights exist here):
+    W_x (dt_rank + 2 dstate, dim) ~ N(0, 1/dim) and W_dt (dim, dt_rank) ~ N(0, 1/dt_rank),
+    bf16, so that the projected values are of unit scale for N(0, 1) inputs."""
+    W_x = normal(seed, STREAM["W_x"], (dt_rank + 2 * dstate, dim), torch.bfloat16, device, std=dim ** -0.5)
+    W_dt = normal(seed, STREAM["W_dt"], (dim, dt_rank), torch.bfloat16, device, std=dt_rank ** -0.5)
+    return W_x, W_dt

@@ -47,7 +47,7 @@ def test_status_strings_and_version(lib):
     names = {c: lib.ssm_status_string(c).decode() for c in (0, -1, -2, -3, -4, -5, -99)}
     assert names[0] == "SSM_OK" and names[-1] == "SSM_ERR_INVALID_ARG"
     assert names[-5] == "SSM_ERR_CUDA" and names[-99] == "SSM_ERR_UNKNOWN"
-    assert lib.ssm_abi_version() == 4
+    assert lib.ssm_abi_version() == 5
 
 
 def test_host_validation_without_gpu():
@@ -64,6 +64,14 @@ def test_host_validation_without_gpu():
         assert lib.ssm_scan_fwd_scheduled(ctypes.byref(p), ctypes.byref(sch), None, 0, None) == -1, bad
         assert lib.ssm_scan_fwd_scheduled_workspace_size(ctypes.byref(p), ctypes.byref(sch)) == 0
     assert lib.ssm_scan_fwd_scheduled(ctypes.byref(p), None, None, 0, None) == -1
+    # projections: misaligned strides and unknown epilogues are refused before any launch
+    q = B.ProjParams(batch=1, m=128, n=128, k=64, W=256, ldw=64, X=256, ldx=128, x_batch_stride=0, out=256,
+                     ldo=128, out_batch_stride=0, bias=None, epilogue=0)
+    q.ldx = 130
+    assert lib.ssm_proj(ctypes.byref(q), None) == -3
+    q.ldx, q.epilogue = 128, 2
+    assert lib.ssm_proj(ctypes.byref(q), None) == -1
+    assert lib.ssm_device_status(None, 0) == -1
     assert lib.ssm_state_update(None, None) == -1
     assert lib.ssm_decode_step(None, None) == -1
     assert lib.causal_conv1d_silu_bwd(None, None, 0, None) == -1
