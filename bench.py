@@ -49,9 +49,9 @@ SSD = dict(batch=8, seqlen=2048, nheads=80, headdim=64, dstate=128, ngroups=1, c
 # capture at batch 8, d_inner 4096, L 2048 (the command is in profiles/).  The
 # figures hold only while the step's kernel sources hash to TRAFFIC_SOURCES_SHA;
 # after any change to them the traffic is reported as null until it is captured again.
-TRAFFIC_PER_CT = {"ssm_scan_bwd": 37.87, "ssm_scan_fwd": 23.17, "causal_conv1d_silu": 3.20,
-                  "causal_conv1d_silu_bwd": 5.51}
-TRAFFIC_SOURCES_SHA = "eba2b381b3037ed6"
+TRAFFIC_PER_CT = {"ssm_scan_bwd": 37.89, "ssm_scan_fwd": 23.16, "causal_conv1d_silu": 3.19,
+                  "causal_conv1d_silu_bwd": 5.51, "ssm_scan_fwd_plain": 7.68}
+TRAFFIC_SOURCES_SHA = "e37dc15cb6b39c22"
 
 SM_FP32_LANES = 128     # FP32 lanes per SM per clock (sm_100 family), nominal
 SM_SFU_EX2 = 32         # MUFU ex2 results per SM per clock, nominal
@@ -421,6 +421,7 @@ def bench_forward_plain(L, g, cfg, rc, reps: int = 10):
 
     ms = time_calls(call, reps)          # inputs of 3.2 GB: far larger than L2
     r = roof_line(fwd_work(b, d, Lq, N), ms, rc, b * d * Lq)
+    r["roofline"]["traffic"] = traffic_bytes("ssm_scan_fwd_plain", b * d * Lq)
     r["workload"] = (f"ssm_scan_fwd without checkpoints, batch {b}, d_inner {d}, d_state {N}, L {Lq}, ZOH, "
                      "softplus, D skip, gate, bf16 in/out")
     return r
@@ -489,6 +490,45 @@ def bench_configs(L, device, rc, flush, quick: bool = False):
     e["workload"] = f"long sequence: batch {b}, d_inner {d}, d_state {N}, L {T}, delta in [1e-4, 1e-2], bf16"
     out["long_sequence_fwd"] = e
     del g, y, ws
+    torch.cuda.empty_cache()
+    return out
+
+
+def bench_x_dt_proj(L, device, cfg, reps: int = 10):
+    """The x_proj and dt_proj products (ssm_proj, tensor cores) at the benchmark
+    layer: x_dbl = W_x xc with W_x (dt_rank + 2 d_state, d_inner), then delta =
+    W_dt x_dbl[:, :dt_rank] with W_dt (d_inner, dt_rank); dt_rank = d_inner / 16.
+    Each against its roofline: the slower of its algorithmic HBM bytes (operands
+    read once, output written once) at the measured copy bandwidth and its
+    FLOPs at the measured bf16 tensor peak (burst)."""
+    import synthetic as S
+    b, D, T, N = cfg["batch"], cfg["dim"], cfg["seqlen"], cfg["dstate"]
+    R = D // 16
+    xc = S.normal(S.config_seed(2), S.STREAM["u"], (b, D, T), torch.bfloat16, device)
+    W_x, W_dt = S.proj_weights(S.config_seed(2), D, R, N, device)
+    x_dbl = torch.empty(b, R + 2 * N, T, dtype=torch.bfloat16, device=device)
+    delta = torch.empty(b, D, T, dtype=torch.bfloat16, device=device)
+    hbm, _ = measured_peaks()
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            tpk, tsrc = float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        tpk, tsrc = 1800.0, "fallback"
+    out = {"workload": f"x_proj ({R + 2 * N} x {D}) and dt_proj ({D} x {R}) over batch {b}, L {T}, bf16 in/out, "
+                       "fp32 accumulation", "peaks": f"HBM {hbm} GB/s, bf16 tensor {tpk} TFLOP/s ({tsrc}, burst)"}
+    for name, fn, m, k in (("x_proj", lambda: L.ssm_proj(W_x, xc, out=x_dbl), R + 2 * N, D),
+                           ("dt_proj", lambda: L.ssm_proj(W_dt, x_dbl[:, :R], out=delta), D, R)):
+        ms = time_calls(fn, reps)
+        flops = 2 * m * k * b * T
+        nbytes = 2 * (m * k + k * b * T + m * b * T)
+        t_hbm, t_tc = nbytes / (hbm * 1e9), flops / (tpk * 1e12)
+        out[name] = {"ms": round(ms, 4), "tflops": round(flops / (ms * 1e-3) / 1e12, 1),
+                     "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "bytes": nbytes, "flops": flops,
+                     "bound": "hbm" if t_hbm >= t_tc else "tensor",
+                     "roofline_frac": round(max(t_hbm, t_tc) / (ms * 1e-3), 4),
+                     "tensor_frac": round(t_tc / (ms * 1e-3), 4), "hbm_frac": round(t_hbm / (ms * 1e-3), 4)}
+    out["device_status"] = L.device_status()
+    del xc, x_dbl, delta
     torch.cuda.empty_cache()
     return out
 
@@ -677,6 +717,8 @@ def main(argv=None):
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-ssd", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the other workloads' timed lines")
+    ap.add_argument("--proj-only", action="store_true",
+                    help="time only the x_proj / dt_proj products at --seqlen (for profiling captures)")
     ap.add_argument("--e2e-steps", type=int, default=6)
     ap.add_argument("--seqlen", type=int, default=0,
                     help="shorter sequence for small profiling captures (the headline uses the default)")
@@ -696,6 +738,9 @@ def main(argv=None):
     cfg = dict(WORK)
     if args.seqlen > 0:
         cfg["seqlen"] = args.seqlen
+    if args.proj_only:
+        print(json.dumps({"x_dt_proj": bench_x_dt_proj(L, device, cfg)}), flush=True)
+        return 0
     seed = S.config_seed(2) + 1000 * rank          # every rank its own batch (weak scaling)
     g = make_inputs(device, seed, cfg)
     ws_bytes = L.ssm_scan_fwd_workspace_size(g["xc"], g["A"])
@@ -841,11 +886,12 @@ def main(argv=None):
                "ms_per_step": round(e2e_ms / n, 2), "overlap": "two buffer sets, copy streams beside the compute stream"}
         del host, out_host, g2, sets
 
-    configs = None
+    configs = proj = None
     if not args.no_configs:
         del g
         torch.cuda.empty_cache()
         configs = bench_configs(L, device, rc, L2Flush(device))
+        proj = bench_x_dt_proj(L, device, cfg)
 
     decode = None
     if not args.no_decode:
@@ -877,7 +923,7 @@ def main(argv=None):
             "fwd_channel_tokens_per_s": fwd_plain["channel_tokens_per_s"],
             "fwd_roofline_frac": fwd_plain["roofline"]["frac"],
             "fwd_hbm_frac": fwd_plain["roofline"]["hbm_frac"],
-            "fwd_plain": fwd_plain, "configs": configs,
+            "fwd_plain": fwd_plain, "configs": configs, "x_dt_proj": proj,
             "decode": decode, "ssd": ssd, "cpu_baseline": cpu, "e2e": e2e,
             "clocks": clocks, "gpu_launches": launches, "gpu": props.name, "unit_rates": unit_rates,
         }

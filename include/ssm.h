@@ -154,12 +154,19 @@ SSM_API ssm_status ssm_scan_fwd(const ssm_scan_fwd_params* p, void* workspace,
  *                       steps each; fewer are used when the sequence is short),
  *                       scanned in parallel and joined by the carry pass; 0 =
  *                       automatic, 1 = one sequential pass
+ *   warp_scan         : 1 = one warp per channel, the sequence in chunks of
+ *                       32 x 16 steps whose lanes are joined by a warp-shuffle
+ *                       associative scan (bf16 inputs, d_state <= 16, no
+ *                       checkpoints, and under ZOH every A[d,n] != 0: a zero
+ *                       there is not detected and gives undefined outputs);
+ *                       the other fields are then ignored
  * Any other value returns SSM_ERR_INVALID_ARG.  The workspace size depends on
  * the schedule: query it with ssm_scan_fwd_scheduled_workspace_size. */
 typedef struct {
     int lanes_per_channel;
     int generic_path;
     int64_t segments;
+    int warp_scan;
 } ssm_fwd_schedule;
 
 SSM_API size_t ssm_scan_fwd_scheduled_workspace_size(const ssm_scan_fwd_params* p, const ssm_fwd_schedule* s);

@@ -164,7 +164,7 @@ _lib.ssm_device_status.restype = _int
 
 
 class FwdSchedule(ctypes.Structure):
-    _fields_ = [("lanes_per_channel", _int), ("generic_path", _int), ("segments", _i64)]
+    _fields_ = [("lanes_per_channel", _int), ("generic_path", _int), ("segments", _i64), ("warp_scan", _int)]
 
 
 _lib.ssm_scan_fwd_scheduled.argtypes = [ctypes.POINTER(ScanFwdParams), ctypes.POINTER(FwdSchedule), _vp,
@@ -366,7 +366,7 @@ def ssm_scan_fwd(u, delta, A, B, C, *, D=None, delta_bias=None, z=None, h0=None,
     """Fused selective-scan forward.  u, delta, z: (batch, dim, L); B, C: (batch, N, L)
     (same dtype as u); A: (dim, N) f32; D, delta_bias: (dim,) f32; h0: (batch, dim, N) f32.
     ``schedule`` (tests and tuning) forces a schedule through ssm_scan_fwd_scheduled:
-    a dict with any of lanes_per_channel, generic_path, segments (0 = automatic).
+    a dict with any of lanes_per_channel, generic_path, segments (0 = automatic), warp_scan.
     Returns ``out`` (and the final state when requested)."""
     for name, t in (("u", u), ("delta", delta), ("B", B), ("C", C), ("z", z)):
         _need_cuda(name, t)
@@ -405,13 +405,14 @@ def ssm_scan_fwd(u, delta, A, B, C, *, D=None, delta_bias=None, z=None, h0=None,
 def _schedule(schedule: Optional[dict]):
     if schedule is None:
         return None
-    unknown = set(schedule) - {"lanes_per_channel", "generic_path", "segments"}
+    unknown = set(schedule) - {"lanes_per_channel", "generic_path", "segments", "warp_scan"}
     if unknown:
         raise ValueError(f"unknown schedule keys {sorted(unknown)}")
     s = FwdSchedule()
     s.lanes_per_channel = int(schedule.get("lanes_per_channel") or 0)
     s.generic_path = int(bool(schedule.get("generic_path", 0)))
     s.segments = int(schedule.get("segments") or 0)
+    s.warp_scan = int(bool(schedule.get("warp_scan", 0)))
     return s
 
 

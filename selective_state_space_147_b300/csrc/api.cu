@@ -96,6 +96,7 @@ ssm_status check_schedule(const ssm_fwd_schedule* s) {
         return fail(SSM_ERR_INVALID_ARG, "generic_path=%d (0 or 1)", s->generic_path);
     if (s->segments < 0 || s->segments > (1 << 20))
         return fail(SSM_ERR_INVALID_ARG, "segments=%lld", (long long)s->segments);
+    if (s->warp_scan != 0 && s->warp_scan != 1) return fail(SSM_ERR_INVALID_ARG, "warp_scan=%d (0 or 1)", s->warp_scan);
     return SSM_OK;
 }
 
@@ -183,11 +184,22 @@ ssm_status ssm_scan_fwd_scheduled(const ssm_scan_fwd_params* p, const ssm_fwd_sc
                                   size_t workspace_bytes, ssm_stream_t stream) {
     const ssm_status c = check_schedule(s);
     if (c != SSM_OK) return c;
+    if (s->warp_scan) {
+        const ssm_status f = check_fwd(p);
+        if (f != SSM_OK) return f;
+        if (!ssm::warpscan_supported(p))
+            return fail(SSM_ERR_UNSUPPORTED, "warp_scan needs bf16 inputs, d_state <= 16, no checkpoints, seqlen > 0 "
+                                             "and channels per B/C group a multiple of 4");
+        cudaError_t e = ssm::launch_scan_fwd_warpscan(p, reinterpret_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(e, "ssm_scan_fwd_scheduled (warp scan) launch");
+        return ok();
+    }
     return scan_fwd_common(p, s, workspace, workspace_bytes, stream);
 }
 
 size_t ssm_scan_fwd_scheduled_workspace_size(const ssm_scan_fwd_params* p, const ssm_fwd_schedule* s) {
     if (check_fwd(p) != SSM_OK || check_schedule(s) != SSM_OK) return 0;
+    if (s->warp_scan) return 0;
     int sms = 0;
     if (num_sms(&sms) != SSM_OK) return 0;
     return ssm::fwd_workspace_bytes(p, sms, s);

@@ -53,6 +53,8 @@ cudaError_t launch_state_update(const ssm_state_update_params* p, cudaStream_t s
 cudaError_t launch_ssd_fwd(const ssm_ssd_fwd_params* p, cudaStream_t st);
 cudaError_t probe_unit_rates(double* fp32, double* f32x2, double* ex2);
 cudaError_t launch_proj(const ssm_proj_params* p, cudaStream_t st);
+bool warpscan_supported(const ssm_scan_fwd_params* p);
+cudaError_t launch_scan_fwd_warpscan(const ssm_scan_fwd_params* p, cudaStream_t st);
 cudaError_t read_device_status(int* status, int clear);
 
 }  // namespace ssm

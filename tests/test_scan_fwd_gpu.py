@@ -205,3 +205,37 @@ def test_deterministic():
     a = run_gpu(g)
     b = run_gpu(g)
     assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("zoh", [True, False])
+@pytest.mark.parametrize("L,N,out_dtype", [(1000, 16, torch.float32), (256, 16, torch.bfloat16), (5000, 12, torch.float32),
+                                           (1, 16, torch.float32), (777, 3, torch.bfloat16)])
+def test_warp_scan_schedule(zoh, L, N, out_dtype):
+    """The warp-shuffle chunked schedule: ragged chunks (L not a multiple of 256),
+    d_state below 16, h0 and the final state, both output dtypes."""
+    g = make(17, 2, 40, L, N, torch.bfloat16, with_h0=True)
+    out, hN = run_gpu(g, zoh=zoh, final=True, out_dtype=out_dtype, schedule={"warp_scan": 1})
+    ref, href = run_oracle(g, zoh=zoh)
+    assert_close(out, ref, torch.bfloat16, out_dtype, what="out")
+    assert_close(hN, href, torch.bfloat16, what="final_state")
+
+
+def test_warp_scan_long_sequence_and_groups():
+    """L 2^17 at batch 1 (many chunks: the carry across chunks), and B/C groups."""
+    g = make(18, 1, 8, 1 << 17, 16, torch.bfloat16, delta_range=(1e-4, 1e-2), with_h0=True)
+    out, hN = run_gpu(g, final=True, schedule={"warp_scan": 1})
+    ref, href = run_oracle(g)
+    assert_close(out, ref, torch.bfloat16, what="out")
+    assert_close(hN, href, torch.bfloat16, what="final_state")
+    L = _lib()
+    gg = S.scan_inputs(19, 2, 256, 600, 16, dtype=torch.bfloat16)
+    Bg = S.normal(19, 40, (2, 2, 16, 600), torch.bfloat16)
+    Cg = S.normal(19, 41, (2, 2, 16, 600), torch.bfloat16)
+    dev = {k: (v.cuda() if v is not None else None) for k, v in gg.items()}
+    out = L.ssm_scan_fwd(dev["u"], dev["dt"], dev["A"], Bg.cuda(), Cg.cuda(), D=dev["D"], delta_bias=dev["bias"],
+                         z=dev["z"], out_dtype=torch.float32, schedule={"warp_scan": 1})
+    for grp in range(2):
+        sl = slice(128 * grp, 128 * grp + 128)
+        ref, _ = oracle.scan_fwd(gg["u"][:, sl], gg["dt"][:, sl], gg["A"][sl], Bg[:, grp], Cg[:, grp], gg["D"][sl],
+                                 gg["bias"][sl], gg["z"][:, sl], threads=THREADS)
+        assert_close(out[:, sl], ref, torch.bfloat16, what=f"group {grp}")
