@@ -10,9 +10,14 @@
 // written (plus the small, channel-shared B/C tiles).
 //
 // Design for B300 (not a translation of the A100 design the pages describe):
-//  * The work is FP32-pipe bound, not HBM bound: the zero-order-hold update
-//    costs 6 FP32 operations and one SFU exp per (channel, step, state) and
-//    moves only 0.5 byte of HBM per (channel, step, state) with bf16 I/O.
+//  * Without checkpoints the work is FP32-pipe bound, not HBM bound: the
+//    zero-order-hold update costs 6 FP32 operations and one SFU exp per
+//    (channel, step, state) and moves only 0.5 byte of HBM per (channel, step,
+//    state) with bf16 I/O (1.42 ms of FP32 work vs 0.66 ms of HBM at batch 8,
+//    d_inner 4096, L 16384).  With the backward's checkpoints (16 more bytes per
+//    channel-token) the algorithmic bytes dominate instead.  Either way the
+//    measured kernel is issue/latency limited below both bounds (ncu: ~57%
+//    issue, FMA pipe ~50%, about 6 warps per SM at this shape).
 //    So the kernel minimises FP32 work: log2(e) is folded into A, the ZOH
 //    term is written h' = Abar (h + k) - k with k = B u / A (no separate
 //    Abar - 1), and the arithmetic is issued as packed f32x2 instructions,
@@ -20,7 +25,7 @@
 //  * A warp owns 32/G channels of one batch row; each channel's N (<= 16)
 //    states are split over G lanes.  The readout reduces over those G lanes
 //    with xor shuffles.  G trades parallelism against shuffle work and is
-//    chosen on the host from the channel count.
+//    chosen on the host from the channel count (plan_fwd).
 //  * B[b,:,t] and C[b,:,t] are shared by every channel: each warp stages a
 //    64-step tile of both as fp32 in shared memory (converted once), read back
 //    as broadcast 16-byte loads.
