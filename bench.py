@@ -42,7 +42,7 @@ WORK = dict(batch=8, dim=4096, dstate=16, seqlen=16384, width=4)
 # Mamba-2.8B-shaped decode (64 layers, batch 128)
 DECODE = dict(batch=128, dim=5120, dstate=16, width=4, layers=64, steps=128)
 # Mamba-2-2.7B-shaped state-space-duality layer (d_inner 5120 = 80 heads of 64, state 128)
-SSD = dict(batch=8, seqlen=2048, nheads=80, headdim=64, dstate=128, ngroups=1, chunk=64)
+SSD = dict(batch=8, seqlen=2048, nheads=80, headdim=64, dstate=128, ngroups=1, chunk=128)
 
 # DRAM traffic of each entry point per channel-token (dram__bytes_read.sum +
 # dram__bytes_write.sum summed over the entry point's launches) from one ncu
@@ -332,9 +332,10 @@ def ssd_cpu_baseline(cfg, heads: int = 0):
 def bench_ssd(L, device, cfg, reps: int = 10):
     """Mamba-2 state-space-duality layer forward (ssm_ssd_fwd), bf16 in and out:
     milliseconds per call, its algorithmic HBM bytes (x, dt, B, C in; out) and
-    tensor FLOPs of the chunked algorithm (C B^T, the masked product with x, C H
-    and the state update, full blocks, no operand splits) against the measured
-    copy bandwidth and bf16 tensor peak."""
+    tensor FLOPs of the chunked algorithm at the kernel's chunk length (C B^T,
+    the masked product with x, C H and the state update, full blocks) against
+    the measured copy bandwidth and bf16 tensor peak.  Inputs (346 MB) are larger
+    than L2, and an L2-sized buffer is written between timed calls."""
     import synthetic as S
     b, T, H, P, N, G, Q = (cfg[k] for k in ("batch", "seqlen", "nheads", "headdim", "dstate", "ngroups", "chunk"))
     g = S.ssd_inputs(S.config_seed(6), b, T, H, P, N, G, device=device)
@@ -346,14 +347,7 @@ def bench_ssd(L, device, cfg, reps: int = 10):
     for _ in range(3):
         call()
     torch.cuda.synchronize()
-    st = torch.cuda.current_stream(device)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(st)
-    for _ in range(reps):
-        call()
-    e1.record(st)
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / reps
+    ms = time_calls(call, reps, L2Flush(device))
     nbytes = b * T * (H * (2 * P * 2 + 2) + 2 * G * N * 2)
     flops = b * H * T * (2 * Q * N + 2 * Q * P + 4 * N * P)
     hbm, _ = measured_peaks()

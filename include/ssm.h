@@ -444,11 +444,16 @@ SSM_API ssm_status ssm_decode_step(const ssm_decode_step_params* p, ssm_stream_t
  *   h0     : (batch, nheads, dstate, headdim) fp32 or NULL (zero state)
  *   final_state : same layout, written when not NULL
  *   out    : (batch, seqlen, nheads, headdim), out_dtype (bf16 or fp32), contiguous
- * x, B, C must be 16-byte aligned and out 8-byte aligned (SSM_ERR_MISALIGNED
- * otherwise).  Contractions run on the tensor cores in bf16 with fp32
- * accumulation; operands that are not inputs (decay-weighted C B^T, the state,
- * decay-weighted B) are split into a bf16 value and a bf16 residual, so results
- * carry about 16 significant bits.  No workspace; asynchronous on `stream`. */
+ * x, B, C, out and final_state must be 16-byte aligned (SSM_ERR_MISALIGNED
+ * otherwise).  Contractions run on the tensor cores (tcgen05) in bf16 with
+ * fp32 accumulation, in chunks of 128 steps; the operands that are not inputs
+ * (the decay-weighted C B^T, the decay-weighted x of the state update, the
+ * copy of the fp32 state that multiplies C) are rounded to bf16 once, so an
+ * output is within 2^-7 times the same layer evaluated on absolute values
+ * (|x|, |B|, |C|, |D|, |h0|) and the final state within 2^-8 of it.  No
+ * workspace; asynchronous on `stream`.  The kernel's waits are bounded: if one
+ * gives up, the outputs are undefined and ssm_device_status reports
+ * SSM_ERR_TIMEOUT. */
 typedef struct {
     int64_t batch, seqlen, nheads, headdim, dstate, ngroups;
     const void* x;

@@ -146,7 +146,7 @@ const char* ssm_status_string(ssm_status s) {
 
 const char* ssm_last_error(void) { return g_err; }
 
-int ssm_abi_version(void) { return 5; }
+int ssm_abi_version(void) { return 6; }
 
 uint64_t ssm_launch_count(void) { return ssm::ssm_launch_count_value(); }
 
@@ -345,8 +345,9 @@ ssm_status ssm_ssd_fwd(const ssm_ssd_fwd_params* p, ssm_stream_t stream) {
     if (!dtype_ok(p->out_dtype)) return fail(SSM_ERR_INVALID_ARG, "unknown dtype");
     if (!p->A || (p->seqlen > 0 && (!p->x || !p->dt || !p->B || !p->C || !p->out)))
         return fail(SSM_ERR_INVALID_ARG, "x, dt, A, B, C and out are required");
-    if (p->seqlen > 0 && (((uintptr_t)p->x | (uintptr_t)p->B | (uintptr_t)p->C) % 16 != 0 || (uintptr_t)p->out % 8 != 0))
-        return fail(SSM_ERR_MISALIGNED, "x, B, C must be 16-byte aligned and out 8-byte aligned");
+    if (p->seqlen > 0 && ((uintptr_t)p->x | (uintptr_t)p->B | (uintptr_t)p->C | (uintptr_t)p->out) % 16 != 0)
+        return fail(SSM_ERR_MISALIGNED, "x, B, C and out must be 16-byte aligned");
+    if ((uintptr_t)p->final_state % 16 != 0) return fail(SSM_ERR_MISALIGNED, "final_state must be 16-byte aligned");
     cudaError_t e = ssm::launch_ssd_fwd(p, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "ssm_ssd_fwd launch");
     return ok();

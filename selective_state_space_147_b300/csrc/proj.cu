@@ -13,13 +13,13 @@
 //
 // Kernel: persistent, one CTA per SM walking 128 x 128 output tiles.  A TMA
 // producer thread streams 64-wide K slices of W (K-major) and X (token-major
-// rows, the "MN-major" operand) into a 6-stage shared-memory ring with 128-byte
+// rows, the "MN-major" operand) into a 4-stage shared-memory ring with 128-byte
 // swizzle; one thread issues tcgen05.mma (bf16 x bf16 -> fp32, M 128, N 128,
 // K 16 per instruction) into one of two TMEM accumulators and releases each
-// stage with tcgen05.commit; four epilogue warps drain the other accumulator
-// (warp w owns TMEM lanes 32w..32w+31, i.e. output rows) into a swizzled
-// bf16 tile in shared memory that one thread writes out with bulk tensor
-// stores, while the next tile accumulates.  Every wait
+// stage with tcgen05.commit; eight epilogue warps drain the other accumulator
+// (warp w owns TMEM lanes 32 (w % 4) .. + 31, i.e. output rows, and half of
+// the tokens) into a swizzled bf16 tile in shared memory that one thread
+// writes out with bulk tensor stores, while the next tile accumulates.  Every wait
 // on an mbarrier is bounded: on expiry the kernel records SSM_ERR_TIMEOUT in
 // the device status word (ssm_device_status), drains its outstanding copies
 // with bounded waits, frees its TMEM and returns.
@@ -29,6 +29,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "tc.cuh"
 
 namespace ssm {
 
@@ -36,104 +37,20 @@ constexpr int kPM = 128;                       // output rows per tile (MMA M)
 constexpr int kPN = 128;                       // tokens per tile (MMA N)
 constexpr int kPK = 64;                        // K per stage: one 128-byte swizzle row of bf16
 constexpr int kPStages = 4;
-constexpr int kPEpiWarps = 4;                  // warps 0-3: epilogue (TMEM lane quadrants 0-3)
-constexpr int kPThreads = 32 * (kPEpiWarps + 2);   // + warp 4: TMA producer, warp 5: MMA issuer
+constexpr int kPEpiWarps = 8;                  // warps 0-7: epilogue (warp w: TMEM lane quadrant w % 4, column half w / 4)
+constexpr int kPThreads = 32 * (kPEpiWarps + 2);   // + warp 8: TMA producer, warp 9: MMA issuer
 constexpr int kPTileA = kPM * kPK * 2;         // 16 KB
 constexpr int kPTileB = kPK * kPN * 2;         // 16 KB: two 64-token boxes of 8 KB
 constexpr int kPStage = kPTileA + kPTileB;
 constexpr int kPTileOut = kPM * kPN * 2;       // 32 KB: the bf16 output tile, two 64-token boxes
 constexpr int kPSmem = 1024 + kPStages * kPStage + 2 * kPTileOut + 256;   // slack, ring, staging, barriers
 constexpr uint32_t kPTmemCols = 2 * kPN;       // two fp32 accumulators (one column per token)
-constexpr long long kWaitLimit = 4000000000LL; // cycles (about 2 s) before a wait gives up
+constexpr uint32_t kProjIdesc = tc::idesc_bf16(kPM, kPN, false, true);   // A (W) K-major, B (X) MN-major
 
 // device-side status of the asynchronous kernels (0 = fine, else an ssm_status)
 __device__ int g_device_status = 0;
 
-__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
-                 : "memory");
-}
-// Wait until the phase of parity `parity` has completed; false after kWaitLimit cycles.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-    const uint32_t a = smem_addr(bar);
-    const long long t0 = clock64();
-    while (true) {
-        uint32_t done;
-        asm volatile(
-            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-            : "=r"(done)
-            : "r"(a), "r"(parity)
-            : "memory");
-        if (done) return true;
-        if (clock64() - t0 > kWaitLimit) return false;
-    }
-}
-
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
-        ::"r"(smem_addr(dst)), "l"(map), "r"(smem_addr(bar)), "r"(x), "r"(y)
-        : "memory");
-}
-// bulk tensor store of a staged shared-memory box (completion tracked by bulk groups)
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int x, int y, int z) {
-    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(map),
-                 "r"(smem_addr(src)), "r"(x), "r"(y), "r"(z)
-                 : "memory");
-}
-__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y, int z) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
-        "[%2];" ::"r"(smem_addr(dst)),
-        "l"(map), "r"(smem_addr(bar)), "r"(x), "r"(y), "r"(z)
-        : "memory");
-}
-
-// Shared-memory matrix descriptor of a 128-byte-swizzled operand tile:
-// start address, leading and stride byte offsets (all >> 4), the descriptor
-// version of this architecture and the swizzle mode.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-    uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFF);
-    d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
-    d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
-    d |= (uint64_t)1 << 46;   // descriptor version
-    d |= (uint64_t)2 << 61;   // 128-byte swizzle
-    return d;
-}
-
-// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, A K-major,
-// B MN-major (token-contiguous rows), N >> 3 and M >> 4.
-constexpr uint32_t kProjIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (0u << 15) | (1u << 16) |
-                                ((uint32_t)(kPN >> 3) << 17) | ((uint32_t)(kPM >> 4) << 24);
-
-__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
-        ::"r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(kProjIdesc), "r"(accumulate)
-        : "memory");
-}
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
-                 : "memory");
-}
-
-// 32 consecutive fp32 accumulator columns of this thread's TMEM lane
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
+using namespace tc;
 
 struct ProjArgs {
     int64_t m, n, k;
@@ -168,7 +85,7 @@ __device__ __forceinline__ void record_timeout(int* abort_flag) {
 }
 
 // Persistent: every CTA (one per SM) walks tiles blockIdx.x, blockIdx.x + gridDim.x, ...
-// The producer and the MMA issuer run ahead through a 6-stage shared-memory ring; two
+// The producer and the MMA issuer run ahead through a 4-stage shared-memory ring; two
 // TMEM accumulators let the epilogue warps drain tile i while tile i + 1 accumulates.
 __global__ void __launch_bounds__(kPThreads, 1)
 proj_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
@@ -263,7 +180,7 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
                         // 1024 bytes apart, the second 64 tokens 8 KB further; the K step
                         // of 16 rows is 2 KB.
                         umma_bf16(dcol, sw128_desc(sa + 32 * k, 16, 1024), sw128_desc(sb + 2048 * k, kPTileB / 2, 1024),
-                                  (kb > 0 || k > 0) ? 1u : 0u);
+                                  kProjIdesc, (kb > 0 || k > 0) ? 1u : 0u);
                     }
                     umma_commit(&empty[s]);   // the stage is free once these MMAs have read it
                 }
@@ -272,25 +189,27 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
             }
         }
     } else {
-        // epilogue: warp w reads TMEM lanes (output rows) 32w .. 32w + 31
+        // epilogue: warp w reads TMEM lanes (output rows) 32 (w % 4) .. + 31, tokens
+        // 64 (w / 4) .. + 63 of the tile
+        const int quad = warp & 3, half = warp >> 2;
         int local = 0;
         for (int tile = blockIdx.x; tile < a.tiles; tile += gridDim.x, local++) {
             const int acc = local & 1;
-            // one decision for all four epilogue warps (tcgen05.ld needs whole warps,
-            // and the named barriers below need all four)
+            // one decision for all epilogue warps (tcgen05.ld needs whole warps, and
+            // the named barriers below need all of them)
             const bool waited = mbar_wait(&tfull[acc], (local >> 1) & 1);
             if (!waited) record_timeout(abort_flag);
             if (!epi_all(waited && *(volatile int*)abort_flag == 0)) break;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             int m0, n0, bz;
             tile_coords(a, tile, m0, n0, bz);
-            const int row = m0 + warp * 32 + lane;
+            const int row = m0 + quad * 32 + lane;
             const float bias = (a.bias != nullptr && row < a.m) ? __ldg(a.bias + row) : 0.f;
-            uint32_t w[4][16];
+            uint32_t w[2][16];
 #pragma unroll
-            for (int c = 0; c < kPN / 32; c++) {
+            for (int c = 0; c < 2; c++) {
                 uint32_t r[32];
-                tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(acc * kPN + c * 32), r);
+                tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * kPN + (2 * half + c) * 32), r);
 #pragma unroll
                 for (int i = 0; i < 16; i++) {
                     float v0 = __uint_as_float(r[2 * i]) + bias, v1 = __uint_as_float(r[2 * i + 1]) + bias;
@@ -310,12 +229,12 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
             unsigned char* so = stage_out + (local & 1) * kPTileOut;
             if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
             asm volatile("bar.sync 1, %0;" ::"n"(32 * kPEpiWarps) : "memory");
-            const int rt = warp * 32 + lane;   // row within the tile
+            const int rt = quad * 32 + lane;   // row within the tile
 #pragma unroll
-            for (int c = 0; c < kPN / 32; c++) {
+            for (int c = 0; c < 2; c++) {
 #pragma unroll
                 for (int q = 0; q < 4; q++) {
-                    const int col = 32 * c + 8 * q;            // first token of this 16-byte chunk
+                    const int col = 32 * (2 * half + c) + 8 * q;   // first token of this 16-byte chunk
                     const int box = col >> 6, ch = (col & 63) >> 3;
                     *reinterpret_cast<uint4*>(so + box * (kPTileOut / 2) + rt * 128 + ((ch ^ (rt & 7)) << 4)) =
                         make_uint4(w[c][4 * q], w[c][4 * q + 1], w[c][4 * q + 2], w[c][4 * q + 3]);
@@ -340,65 +259,31 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
 }
 
 // ---------------------------------------------------------------------------
-// Host side: tensor maps through the driver's entry point (the library does not
-// link the driver library), then one launch.
-
-typedef CUresult (*PfnEncodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static cudaError_t encode_fn(PfnEncodeTiled* out) {
-    static PfnEncodeTiled fn = nullptr;
-    if (fn == nullptr) {
-        void* f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q);
-        if (e != cudaSuccess) return e;
-        if (q != cudaDriverEntryPointSuccess || f == nullptr) return cudaErrorSymbolNotFound;
-        fn = reinterpret_cast<PfnEncodeTiled>(f);
-    }
-    *out = fn;
-    return cudaSuccess;
-}
+// Host side: tensor maps, then one launch.
 
 cudaError_t launch_proj(const ssm_proj_params* p, cudaStream_t st) {
-    PfnEncodeTiled enc = nullptr;
-    cudaError_t e = encode_fn(&enc);
-    if (e != cudaSuccess) return e;
-    alignas(64) CUtensorMap tmW, tmX;
+    alignas(64) CUtensorMap tmW, tmX, tmO;
+    cudaError_t e;
     {
-        const cuuint64_t dims[2] = {(cuuint64_t)p->k, (cuuint64_t)p->m};
-        const cuuint64_t strides[1] = {(cuuint64_t)p->ldw * 2};
-        const cuuint32_t box[2] = {(cuuint32_t)kPK, (cuuint32_t)kPM};
-        const cuuint32_t es[2] = {1, 1};
-        if (enc(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p->W), dims, strides, box, es,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
+        const uint64_t dims[2] = {(uint64_t)p->k, (uint64_t)p->m};
+        const uint64_t strides[1] = {(uint64_t)p->ldw * 2};
+        const uint32_t box[2] = {(uint32_t)kPK, (uint32_t)kPM};
+        if ((e = encode_bf16_map(&tmW, p->W, 2, dims, strides, box, true, true)) != cudaSuccess) return e;
     }
     // with one batch row the batch stride is never used: give the maps a valid one
     const int64_t xbs = p->batch > 1 ? p->x_batch_stride : p->ldx * p->k;
     const int64_t obs = p->batch > 1 ? p->out_batch_stride : p->ldo * p->m;
-    alignas(64) CUtensorMap tmO;
     {
-        const cuuint64_t dims[3] = {(cuuint64_t)p->n, (cuuint64_t)p->m, (cuuint64_t)p->batch};
-        const cuuint64_t strides[2] = {(cuuint64_t)p->ldo * 2, (cuuint64_t)obs * 2};
-        const cuuint32_t box[3] = {64, (cuuint32_t)kPM, 1};
-        const cuuint32_t es[3] = {1, 1, 1};
-        if (enc(&tmO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p->out, dims, strides, box, es,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
+        const uint64_t dims[3] = {(uint64_t)p->n, (uint64_t)p->m, (uint64_t)p->batch};
+        const uint64_t strides[2] = {(uint64_t)p->ldo * 2, (uint64_t)obs * 2};
+        const uint32_t box[3] = {64, (uint32_t)kPM, 1};
+        if ((e = encode_bf16_map(&tmO, p->out, 3, dims, strides, box, true, false)) != cudaSuccess) return e;
     }
     {
-        const cuuint64_t dims[3] = {(cuuint64_t)p->n, (cuuint64_t)p->k, (cuuint64_t)p->batch};
-        const cuuint64_t strides[2] = {(cuuint64_t)p->ldx * 2, (cuuint64_t)xbs * 2};
-        const cuuint32_t box[3] = {64, (cuuint32_t)kPK, 1};
-        const cuuint32_t es[3] = {1, 1, 1};
-        if (enc(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(p->X), dims, strides, box, es,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
+        const uint64_t dims[3] = {(uint64_t)p->n, (uint64_t)p->k, (uint64_t)p->batch};
+        const uint64_t strides[2] = {(uint64_t)p->ldx * 2, (uint64_t)xbs * 2};
+        const uint32_t box[3] = {64, (uint32_t)kPK, 1};
+        if ((e = encode_bf16_map(&tmX, p->X, 3, dims, strides, box, true, true)) != cudaSuccess) return e;
     }
     ProjArgs a;
     a.m = p->m; a.n = p->n; a.k = p->k;
@@ -422,6 +307,15 @@ cudaError_t launch_proj(const ssm_proj_params* p, cudaStream_t st) {
     count_launches(1);
     return cudaGetLastError();
 }
+
+namespace tc {
+cudaError_t device_status_word(int** ptr) {
+    void* a = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&a, g_device_status);
+    *ptr = static_cast<int*>(a);
+    return e;
+}
+}  // namespace tc
 
 cudaError_t read_device_status(int* status, int clear) {
     int v = 0;

@@ -203,23 +203,31 @@ __device__ __forceinline__ void scan_block8_steps(pf2 (&h2)[NP], const pf2 (&A2)
         const pf2 dl2 = pf2_make(dl8[j], dl8[j]);
         const pf2 u2 = pf2_make(u8[j], u8[j]);
         const float* row = bc + j * kRow + n_base;
-        pf2 ya = 0ull, yb = 0ull;
+        // every pair's exponential and input term first (none depends on h),
+        // then the NP independent updates, then the readout
+        pf2 ab[NP], kn[NP];
 #pragma unroll
         for (int p = 0; p < NP; p += 2) {
             const ulonglong2 B4 = *reinterpret_cast<const ulonglong2*>(row + 2 * p);
-            const pf2 aba = pf2_ex2(pf2_mul(dl2, A2[p]));
-            const pf2 abb = pf2_ex2(pf2_mul(dl2, A2[p + 1]));
-            const pf2 kna = pf2_mul(pf2_mul(B4.x, u2), I2[p]);          // -k = -B u / A
-            const pf2 knb = pf2_mul(pf2_mul(B4.y, u2), I2[p + 1]);
-            h2[p] = pf2_fma(aba, pf2_sub(h2[p], kna), kna);             // Abar (h + k) - k
-            h2[p + 1] = pf2_fma(abb, pf2_sub(h2[p + 1], knb), knb);
-            if constexpr (READOUT) {
+            ab[p] = pf2_ex2(pf2_mul(dl2, A2[p]));
+            ab[p + 1] = pf2_ex2(pf2_mul(dl2, A2[p + 1]));
+            kn[p] = pf2_mul(pf2_mul(B4.x, u2), I2[p]);                 // -k = -B u / A
+            kn[p + 1] = pf2_mul(pf2_mul(B4.y, u2), I2[p + 1]);
+        }
+#pragma unroll
+        for (int p = 0; p < NP; p++) h2[p] = pf2_fma(ab[p], pf2_sub(h2[p], kn[p]), kn[p]);   // Abar (h + k) - k
+        if constexpr (READOUT) {
+            pf2 ya = 0ull, yb = 0ull;
+#pragma unroll
+            for (int p = 0; p < NP; p += 2) {
                 const ulonglong2 C4 = *reinterpret_cast<const ulonglong2*>(row + 16 + 2 * p);
                 ya = pf2_fma(C4.x, h2[p], ya);
                 yb = pf2_fma(C4.y, h2[p + 1], yb);
             }
+            yacc[j] = pf2_sum(pf2_add(ya, yb));
+        } else {
+            yacc[j] = 0.f;
         }
-        yacc[j] = READOUT ? pf2_sum(pf2_add(ya, yb)) : 0.f;
     }
 }
 

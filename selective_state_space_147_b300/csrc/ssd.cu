@@ -6,30 +6,33 @@
 // whose (i, j) entry is C_i . B_j times the decay between steps j and i.  The
 // sequence is cut into chunks: inside a chunk that product is evaluated with
 // matrix multiplications on the tensor cores, between chunks only the state
-// (N x P per head) is passed on.  Per (batch b, head h), chunk of Q = 64 steps
-// starting at t0, with Delta_t = softplus(dt + dt_bias), s_i = sum_{r<=i}
-// Delta_r A (inclusive, inside the chunk) and H the state entering the chunk:
+// (N x P per head) is passed on.  Per (batch b, head h), chunk of Q = 128
+// steps starting at t0, with Delta_t = softplus(dt + dt_bias), s_i =
+// sum_{r<=i} Delta_r A (inclusive, inside the chunk) and H the state entering
+// the chunk:
 //
-//   y_i   = exp(s_i) C_i^T H                                    (inter-chunk)
-//         + sum_{j<=i} (C_i . B_j) exp(s_i - s_j) Delta_j x_j   (intra-chunk)
-//         + D x_i
-//   H'    = exp(s_last) H + sum_j exp(s_last - s_j) Delta_j B_j x_j^T
+//   y_i = exp(s_i) C_i^T H                                    (inter-chunk)
+//       + sum_{j<=i} (C_i . B_j) exp(s_i - s_j) Delta_j x_j   (intra-chunk)
+//       + D x_i
+//   H'  = exp(s_last) H + sum_j exp(s_last - s_j) Delta_j B_j x_j^T
 //
-// Design for B300: two CTAs of four warps per (b, h), each owning 32 of the 64
-// head-dimension columns (outputs and state columns; both form the full
-// C B^T), walk the chunks in order and keep their half of H in fp32 registers
-// (mma accumulator fragments).  Every contraction
-// is a bf16 m16n8k16 tensor-core MMA with fp32 accumulation:
-//   G = C B^T (64 x 64, k = N), then M = G o decay o Delta in registers, reused
-//   directly as the A operand of Y += M X (k = 64 steps);
-//   Y = C H (k = N) before that, rows scaled by exp(s_i);
-//   H' = (B o w)^T X (k = 64) with w_j = exp(s_last - s_j) Delta_j, its A
-//   fragments built from the staged B rows.
-// Operands that are not bf16 inputs (M, H, w B) are split into a bf16 high part
-// and a bf16 residual and multiplied twice, so the products keep about 16
-// significant bits (the inputs themselves are exact in bf16).  x, B, C tiles
-// are staged in shared memory (x transposed) with padded rows.  The causal
-// mask lets warp w skip the column blocks right of its 16 rows.
+// Design for B300: one CTA per (b, h) walks the chunks in order; every
+// contraction is a tcgen05.mma (bf16 x bf16 -> fp32 in TMEM, M = 128 rows):
+//   G  = C B^T           (128 x 128, K = N)           A = C tile, B = B tile (both K-major)
+//   Yd = M X             (128 x 64,  K = 128 steps)   M = G o decay o Delta (lower triangle)
+//   S  = B^T (w o X)     (N x 64,    K = 128 steps)   A = the B tile read state-major
+//   Yo = C H             (128 x 64,  K = N)           H = the entering state in bf16
+// y = Yd + exp(s_i) Yo + D x, and the fp32 state H' = exp(s_last) H + S stays in
+// the epilogue threads' registers across chunks (its bf16 copy is the next
+// chunk's operand).  Warp 8 streams the C, B and x tiles of a chunk with TMA
+// (128-byte swizzle; rows past the sequence end and states past N read as
+// zero) into a 2-stage ring; warp 9 issues the MMAs -- the next chunk's G
+// while the epilogue warps turn this chunk's G into M -- and eight epilogue
+// warps (warp w: TMEM lanes 32 (w % 4) .. + 31 = chunk rows, half w / 4 of the
+// columns) compute Delta, the in-chunk prefix sums s, M and w o X into shared
+// memory, then the state update and y.  Every mbarrier wait is bounded: on
+// expiry the kernel records SSM_ERR_TIMEOUT in the device status word and the
+// CTA leaves after its own copies and MMAs have landed.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -37,378 +40,433 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "tc.cuh"
 
 namespace ssm {
 
 namespace {
 
-constexpr int kQ = 64;            // chunk length (steps)
-constexpr int kP = 64;            // head dimension
-constexpr int kPC = 32;           // head-dimension columns per CTA (two CTAs per head)
-constexpr int kPT = kPC / 8;      // 8-column MMA tiles per CTA
-constexpr int kThreads = 128;     // four warps
+using namespace tc;
 
-__device__ __forceinline__ uint32_t ld32(const __nv_bfloat16* p) { return *reinterpret_cast<const uint32_t*>(p); }
-
-__device__ __forceinline__ uint32_t pack2(__nv_bfloat16 lo, __nv_bfloat16 hi) {
-    return (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
-}
-
-// v = hi + lo with both parts bf16 (lo carries the rounding residual of hi)
-__device__ __forceinline__ void split_bf16(float v, __nv_bfloat16& hi, __nv_bfloat16& lo) {
-    hi = __float2bfloat16_rn(v);
-    lo = __float2bfloat16_rn(v - __bfloat162float(hi));
-}
-__device__ __forceinline__ void split2(float v0, float v1, uint32_t& hi, uint32_t& lo) {
-    __nv_bfloat16 h0, l0, h1, l1;
-    split_bf16(v0, h0, l0);
-    split_bf16(v1, h1, l1);
-    hi = pack2(h0, h1);
-    lo = pack2(l0, l1);
-}
-
-// D (16x8, fp32) += A (16x16, bf16, row) * B (16x8, bf16, col)
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};\n"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ float softplus_acc(float v) { return v > 20.f ? v : log1pf(expf(v)); }
+constexpr int kQ = 128;                   // chunk length: the MMA's M (rows = steps)
+constexpr int kP = 64;                    // head dimension
+constexpr int kAtom = 128 * 128;          // 16 KB: 128 rows of 128 bytes (64 bf16)
+constexpr int kTileBC = 2 * kAtom;        // a C or B tile: 128 steps x 128 states (two 64-state atoms)
+constexpr int kTileX = kAtom;             // an x tile: 128 steps x 64 head-dimension columns
+constexpr int kStage = 2 * kTileBC + kTileX;
+constexpr int kStages = 2;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 32 * (kEpiWarps + 2);   // + warp 8: TMA producer, warp 9: MMA issuer
+constexpr int kOffM = kStages * kStage;           // M: K-major A operand, two 64-step atoms
+constexpr int kOffWX = kOffM + 2 * kAtom;         // w o x: MN-major B operand
+constexpr int kOffH = kOffWX + kTileX;            // the entering state in bf16: MN-major B operand
+constexpr int kOffAux = kOffH + kTileX;
+// aux: Delta[2][128], s[2][128] (fp32, double-buffered by chunk parity), warp sums [2][4] (+ pad), barriers
+constexpr int kAuxFloats = 2 * kQ * 2 + 16;
+constexpr int kNumBars = 2 + 2 + 2 + 1 + 1 + 1 + 1;   // full, empty, gfull, mready, yfull, yempty, done
+constexpr int kSmem = kOffAux + kAuxFloats * 4 + kNumBars * 8 + 16;
+// TMEM columns: G (two buffers), Yd, Yo, S
+constexpr uint32_t kColG = 0, kColYd = 256, kColYo = 320, kColS = 384, kTmemCols = 512;
 
 struct SsdArgs {
-    int64_t batch, seqlen, nheads, ngroups;
-    const __nv_bfloat16* x;      // (batch, L, H, P)
+    int L, H, heads_per_group, nstate, nbox, nchunks;
+    uint32_t stage_bytes;
     const __nv_bfloat16* dt;     // (batch, L, H)
     const float* A;              // (H)
-    const __nv_bfloat16* B;      // (batch, L, G, N)
-    const __nv_bfloat16* C;
     const float* D;              // (H) or NULL
     const float* dt_bias;        // (H) or NULL
     const float* h0;             // (batch, H, N, P) or NULL
     float* final_state;          // (batch, H, N, P) or NULL
     void* out;                   // (batch, L, H, P)
     int softplus;
+    int* status;                 // device status word
 };
 
-template <int NT>
-struct SsdSmem {
-    static constexpr int N = 16 * NT;
-    static constexpr int LDX = kQ + 8;      // Xt[p][j]
-    static constexpr int LDBC = N + 8;      // Bs[j][n], Cs[i][n]
-    static constexpr int LDH = N + 8;       // Ht[p][n]
-    static constexpr int kXt = kPC * LDX;
-    static constexpr int kBC = kQ * LDBC;
-    static constexpr int kH = kPC * LDH;
-    static constexpr int kHalves = kXt + 2 * kBC + 2 * kH;
-    static constexpr int kBytes = kHalves * 2 + 3 * kQ * 4;   // + Delta, s, w (fp32)
-};
-
-template <int NT, typename Tout>
-__global__ void __launch_bounds__(kThreads) ssd_fwd_kernel(const SsdArgs a) {
-    constexpr int N = 16 * NT;
-    using L = SsdSmem<NT>;
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    __nv_bfloat16* Xt = reinterpret_cast<__nv_bfloat16*>(smem_raw);
-    __nv_bfloat16* Bs = Xt + L::kXt;
-    __nv_bfloat16* Cs = Bs + L::kBC;
-    __nv_bfloat16* Hh = Cs + L::kBC;
-    __nv_bfloat16* Hl = Hh + L::kH;
-    float* dlt = reinterpret_cast<float*>(Hl + L::kH);
-    float* sc = dlt + kQ;
-    float* wv = sc + kQ;
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int g = lane >> 2, t4 = lane & 3;
-    const int64_t unit = blockIdx.x >> 1;                // (b, h)
-    const int p0 = (int)(blockIdx.x & 1) * kPC;          // this CTA's head-dimension columns
-    const int64_t H = a.nheads;
-    const int64_t b = unit / H, h = unit - b * H;
-    const int64_t grp = h / (H / a.ngroups);
-    const float Ah = __ldg(a.A + h);
-    const float Dh = a.D ? __ldg(a.D + h) : 0.f;
-    const float bias = a.dt_bias ? __ldg(a.dt_bias + h) : 0.f;
-
-    // state tiles owned by this warp: q = warp * NT + i -> rows n in [16 (q / kPT), +16),
-    // local columns in [8 (q % kPT), +8)
-    float hacc[NT][4];
-#pragma unroll
-    for (int i = 0; i < NT; i++) {
-        const int q = warp * NT + i, mt = q / kPT, pt = q % kPT;
-#pragma unroll
-        for (int e = 0; e < 4; e++) {
-            const int n = mt * 16 + g + ((e & 2) ? 8 : 0), p = pt * 8 + 2 * t4 + (e & 1);
-            hacc[i][e] = a.h0 ? __ldg(a.h0 + (unit * N + n) * kP + p0 + p) : 0.f;
-            __nv_bfloat16 hi, lo;
-            split_bf16(hacc[i][e], hi, lo);
-            Hh[p * L::LDH + n] = hi;
-            Hl[p * L::LDH + n] = lo;
-        }
-    }
-
-    const int64_t nchunks = (a.seqlen + kQ - 1) / kQ;
-    for (int64_t c = 0; c < nchunks; c++) {
-        const int64_t t0 = c * kQ;
-        __syncthreads();   // the previous chunk is done with every tile
-        // ---- stage x (transposed), B, C rows and Delta of the chunk; zero past L
-        {
-            // x: 64 rows of this CTA's 32 bf16 = 4 x 16 bytes each; thread -> (row, 16-byte chunk) pairs
-#pragma unroll
-            for (int k = 0; k < (kQ * kPT) / kThreads; k++) {
-                const int idx = k * kThreads + tid;
-                const int j = idx / kPT, ch = idx % kPT;
-                uint4 v = make_uint4(0, 0, 0, 0);
-                if (t0 + j < a.seqlen)
-                    v = *reinterpret_cast<const uint4*>(a.x + ((b * a.seqlen + t0 + j) * H + h) * kP + p0 + ch * 8);
-                const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                for (int q = 0; q < 4; q++) {
-                    Xt[(ch * 8 + 2 * q) * L::LDX + j] = __ushort_as_bfloat16((unsigned short)(w4[q] & 0xffffu));
-                    Xt[(ch * 8 + 2 * q + 1) * L::LDX + j] = __ushort_as_bfloat16((unsigned short)(w4[q] >> 16));
-                }
-            }
-            // B, C: 64 rows of N bf16 = N/8 x 16 bytes each
-            constexpr int kPer = N / 8;
-            for (int idx = tid; idx < 2 * kQ * kPer; idx += kThreads) {
-                const int tsr = idx / (kQ * kPer), r = idx - tsr * (kQ * kPer);
-                const int j = r / kPer, ch = r - j * kPer;
-                const __nv_bfloat16* src = tsr == 0 ? a.B : a.C;
-                uint4 v = make_uint4(0, 0, 0, 0);
-                if (t0 + j < a.seqlen)
-                    v = *reinterpret_cast<const uint4*>(src + ((b * a.seqlen + t0 + j) * a.ngroups + grp) * N + ch * 8);
-                __nv_bfloat16* dst = (tsr == 0 ? Bs : Cs) + j * L::LDBC + ch * 8;
-                *reinterpret_cast<uint4*>(dst) = v;
-            }
-            if (tid < kQ) {
-                float d = 0.f;
-                if (t0 + tid < a.seqlen) {
-                    const float v = __bfloat162float(a.dt[(b * a.seqlen + t0 + tid) * H + h]) + bias;
-                    d = a.softplus ? softplus_acc(v) : v;
-                }
-                dlt[tid] = d;
-            }
-        }
-        __syncthreads();
-        // ---- inclusive cumulative sum of Delta A over the chunk, and w_j
-        if (warp == 0) {
-            const float l0 = dlt[2 * lane] * Ah, l1 = dlt[2 * lane + 1] * Ah;
-            float incl = l0 + l1;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float v = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += v;
-            }
-            const float excl = incl - (l0 + l1);
-            sc[2 * lane] = excl + l0;
-            sc[2 * lane + 1] = incl;
-            const float last = __shfl_sync(0xffffffffu, incl, 31);
-            wv[2 * lane] = expf(last - (excl + l0)) * dlt[2 * lane];
-            wv[2 * lane + 1] = expf(last - incl) * dlt[2 * lane + 1];
-        }
-        __syncthreads();
-        // ---- outputs of this warp's 16 rows
-        {
-            const int i0 = 16 * warp;
-            const int r0 = i0 + g, r1 = i0 + g + 8;
-            float yacc[kPT][4];
-#pragma unroll
-            for (int pt = 0; pt < kPT; pt++)
-#pragma unroll
-                for (int e = 0; e < 4; e++) yacc[pt][e] = 0.f;
-            // inter-chunk: C H (H as high part + residual), rows scaled by exp(s_i)
-#pragma unroll
-            for (int kk = 0; kk < NT; kk++) {
-                uint32_t af[4];
-                af[0] = ld32(Cs + r0 * L::LDBC + kk * 16 + 2 * t4);
-                af[1] = ld32(Cs + r1 * L::LDBC + kk * 16 + 2 * t4);
-                af[2] = ld32(Cs + r0 * L::LDBC + kk * 16 + 2 * t4 + 8);
-                af[3] = ld32(Cs + r1 * L::LDBC + kk * 16 + 2 * t4 + 8);
-#pragma unroll
-                for (int pt = 0; pt < kPT; pt++) {
-                    const int prow = (pt * 8 + g) * L::LDH + kk * 16 + 2 * t4;
-                    mma16816(yacc[pt], af, ld32(Hh + prow), ld32(Hh + prow + 8));
-                    mma16816(yacc[pt], af, ld32(Hl + prow), ld32(Hl + prow + 8));
-                }
-            }
-            {
-                const float e0 = expf(sc[r0]), e1 = expf(sc[r1]);
-#pragma unroll
-                for (int pt = 0; pt < kPT; pt++) {
-                    yacc[pt][0] *= e0; yacc[pt][1] *= e0;
-                    yacc[pt][2] *= e1; yacc[pt][3] *= e1;
-                }
-            }
-            // intra-chunk: G = C B^T for column blocks left of / at the diagonal
-            float gacc[8][4];
-#pragma unroll
-            for (int jt = 0; jt < 8; jt++)
-#pragma unroll
-                for (int e = 0; e < 4; e++) gacc[jt][e] = 0.f;
-#pragma unroll
-            for (int kk = 0; kk < NT; kk++) {
-                uint32_t af[4];
-                af[0] = ld32(Cs + r0 * L::LDBC + kk * 16 + 2 * t4);
-                af[1] = ld32(Cs + r1 * L::LDBC + kk * 16 + 2 * t4);
-                af[2] = ld32(Cs + r0 * L::LDBC + kk * 16 + 2 * t4 + 8);
-                af[3] = ld32(Cs + r1 * L::LDBC + kk * 16 + 2 * t4 + 8);
-#pragma unroll
-                for (int jt = 0; jt < 8; jt++) {
-                    if (jt <= 2 * warp + 1) {
-                        const int jrow = (jt * 8 + g) * L::LDBC + kk * 16 + 2 * t4;
-                        mma16816(gacc[jt], af, ld32(Bs + jrow), ld32(Bs + jrow + 8));
-                    }
-                }
-            }
-            // M = G o exp(s_i - s_j) o Delta_j on and below the diagonal
-#pragma unroll
-            for (int jt = 0; jt < 8; jt++) {
-#pragma unroll
-                for (int e = 0; e < 4; e++) {
-                    const int i = (e & 2) ? r1 : r0;
-                    const int j = jt * 8 + 2 * t4 + (e & 1);
-                    gacc[jt][e] = (j <= i) ? gacc[jt][e] * expf(sc[i] - sc[j]) * dlt[j] : 0.f;
-                }
-            }
-            // Y += M X, M reused from the accumulators as A fragments (high part + residual)
-#pragma unroll
-            for (int kk = 0; kk < 4; kk++) {
-                if (kk <= warp) {
-                    uint32_t ah[4], al[4];
-                    split2(gacc[2 * kk][0], gacc[2 * kk][1], ah[0], al[0]);
-                    split2(gacc[2 * kk][2], gacc[2 * kk][3], ah[1], al[1]);
-                    split2(gacc[2 * kk + 1][0], gacc[2 * kk + 1][1], ah[2], al[2]);
-                    split2(gacc[2 * kk + 1][2], gacc[2 * kk + 1][3], ah[3], al[3]);
-#pragma unroll
-                    for (int pt = 0; pt < kPT; pt++) {
-                        const int xrow = (pt * 8 + g) * L::LDX + kk * 16 + 2 * t4;
-                        const uint32_t b0 = ld32(Xt + xrow), b1 = ld32(Xt + xrow + 8);
-                        mma16816(yacc[pt], ah, b0, b1);
-                        mma16816(yacc[pt], al, b0, b1);
-                    }
-                }
-            }
-            // + D x, store rows inside the sequence
-#pragma unroll
-            for (int half = 0; half < 2; half++) {
-                const int i = half ? r1 : r0;
-                if (t0 + i >= a.seqlen) continue;
-                Tout* orow = reinterpret_cast<Tout*>(a.out) + ((b * a.seqlen + t0 + i) * H + h) * kP + p0;
-#pragma unroll
-                for (int pt = 0; pt < kPT; pt++) {
-                    const int p = pt * 8 + 2 * t4;
-                    const float v0 = yacc[pt][2 * half] + Dh * __bfloat162float(Xt[p * L::LDX + i]);
-                    const float v1 = yacc[pt][2 * half + 1] + Dh * __bfloat162float(Xt[(p + 1) * L::LDX + i]);
-                    if constexpr (sizeof(Tout) == 2) {
-                        *reinterpret_cast<uint32_t*>(orow + p) = pack2(__float2bfloat16_rn(v0), __float2bfloat16_rn(v1));
-                    } else {
-                        *reinterpret_cast<float2*>(orow + p) = make_float2(v0, v1);
-                    }
-                }
-            }
-        }
-        __syncthreads();   // every warp has read the entering state
-        // ---- state: H' = exp(s_last) H + W X with W[n][j] = w_j B[j][n], its A
-        // fragments built from the staged B rows (high part + residual)
-        {
-            const float dec = expf(sc[kQ - 1]);
-#pragma unroll
-            for (int i = 0; i < NT; i++)
-#pragma unroll
-                for (int e = 0; e < 4; e++) hacc[i][e] *= dec;
-#pragma unroll
-            for (int kk = 0; kk < 4; kk++) {
-                uint32_t ah[4], al[4];
-#pragma unroll
-                for (int i = 0; i < NT; i++) {
-                    const int q = warp * NT + i, mt = q / kPT, pt = q % kPT;
-                    if (i % kPT == 0) {
-                        // a warp's tiles share one row block mt per run of kPT (NT = 1, 2: one run)
-                        const int n0 = mt * 16 + g, n1 = n0 + 8;
-                        const int j0 = kk * 16 + 2 * t4, j1 = j0 + 8;
-                        const float wa = wv[j0], wb = wv[j0 + 1], wc = wv[j1], wd = wv[j1 + 1];
-                        const __nv_bfloat16* r0 = Bs + j0 * L::LDBC;
-                        const __nv_bfloat16* r1 = Bs + j1 * L::LDBC;
-                        split2(wa * __bfloat162float(r0[n0]), wb * __bfloat162float(r0[L::LDBC + n0]), ah[0], al[0]);
-                        split2(wa * __bfloat162float(r0[n1]), wb * __bfloat162float(r0[L::LDBC + n1]), ah[1], al[1]);
-                        split2(wc * __bfloat162float(r1[n0]), wd * __bfloat162float(r1[L::LDBC + n0]), ah[2], al[2]);
-                        split2(wc * __bfloat162float(r1[n1]), wd * __bfloat162float(r1[L::LDBC + n1]), ah[3], al[3]);
-                    }
-                    const int xrow = (pt * 8 + g) * L::LDX + kk * 16 + 2 * t4;
-                    const uint32_t b0 = ld32(Xt + xrow), b1 = ld32(Xt + xrow + 8);
-                    mma16816(hacc[i], ah, b0, b1);
-                    mma16816(hacc[i], al, b0, b1);
-                }
-            }
-            // the new state as the next chunk's B operand (transposed, high part + residual)
-#pragma unroll
-            for (int i = 0; i < NT; i++) {
-                const int q = warp * NT + i, mt = q / kPT, pt = q % kPT;
-#pragma unroll
-                for (int e = 0; e < 4; e++) {
-                    const int n = mt * 16 + g + ((e & 2) ? 8 : 0), p = pt * 8 + 2 * t4 + (e & 1);
-                    __nv_bfloat16 hi, lo;
-                    split_bf16(hacc[i][e], hi, lo);
-                    Hh[p * L::LDH + n] = hi;
-                    Hl[p * L::LDH + n] = lo;
-                }
-            }
-        }
-    }
-    if (a.final_state != nullptr) {
-#pragma unroll
-        for (int i = 0; i < NT; i++) {
-            const int q = warp * NT + i, mt = q / kPT, pt = q % kPT;
-#pragma unroll
-            for (int e = 0; e < 4; e++) {
-                const int n = mt * 16 + g + ((e & 2) ? 8 : 0), p = pt * 8 + 2 * t4 + (e & 1);
-                a.final_state[(unit * N + n) * kP + p0 + p] = hacc[i][e];
-            }
-        }
-    }
+__device__ __forceinline__ void record_timeout(int* status, int* abort_flag) {
+    atomicExch(status, (int)SSM_ERR_TIMEOUT);
+    *(volatile int*)abort_flag = 1;
 }
 
-template <int NT, typename Tout>
-cudaError_t launch_ssd_typed(const SsdArgs& a, cudaStream_t st) {
-    const int bytes = SsdSmem<NT>::kBytes;
-    cudaError_t e = prepare_kernel<ssd_fwd_kernel<NT, Tout>>(bytes);
-    if (e != cudaSuccess) return e;
-    ssd_fwd_kernel<NT, Tout><<<(unsigned)(2 * a.batch * a.nheads), kThreads, bytes, st>>>(a);
-    count_launches(1);
-    return cudaGetLastError();
+// AND of v over the 256 epilogue threads (named barrier 1); every epilogue thread must call it
+__device__ __forceinline__ bool epi_all(bool v) {
+    uint32_t r;
+    asm volatile("{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, 1, %2, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+                 : "=r"(r)
+                 : "r"((uint32_t)v), "n"(32 * kEpiWarps)
+                 : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&v)[8]) {
+    return make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                      pack_bf16x2(v[6], v[7]));
+}
+
+// the 16-byte chunk `ch` of row `r` of a 128-byte-swizzled tile
+__device__ __forceinline__ unsigned char* swz(unsigned char* tile, int r, int ch) {
+    return tile + r * 128 + ((ch ^ (r & 7)) << 4);
 }
 
 template <typename Tout>
-cudaError_t launch_ssd_n(const SsdArgs& a, int64_t dstate, cudaStream_t st) {
-    switch (dstate) {
-        case 16: return launch_ssd_typed<1, Tout>(a, st);
-        case 32: return launch_ssd_typed<2, Tout>(a, st);
-        case 64: return launch_ssd_typed<4, Tout>(a, st);
-        case 128: return launch_ssd_typed<8, Tout>(a, st);
-        default: return cudaErrorInvalidValue;
+__global__ void __launch_bounds__(kThreads, 1)
+ssd_chunk_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmB,
+                 const __grid_constant__ CUtensorMap tmX, const SsdArgs a) {
+    extern __shared__ __align__(1024) unsigned char smem[];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // the swizzled tiles need a 1024-byte aligned base: refuse (uniformly) otherwise
+    if (smem_addr(smem) & 1023) {
+        if (tid == 0) atomicExch(a.status, (int)SSM_ERR_MISALIGNED);
+        return;
     }
+    float* dl = reinterpret_cast<float*>(smem + kOffAux);   // Delta [2][128]
+    float* s2 = dl + 2 * kQ;                                  // s log2(e) [2][128]
+    float* wsum = s2 + 2 * kQ;                                // [2][4]
+    uint64_t* full = reinterpret_cast<uint64_t*>(wsum + 16);
+    uint64_t* empty = full + 2;
+    uint64_t* gfull = empty + 2;
+    uint64_t* mready = gfull + 2;
+    uint64_t* yfull = mready + 1;
+    uint64_t* yempty = yfull + 1;
+    uint64_t* done = yempty + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+    int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+
+    const int unit = blockIdx.x;
+    const int b = unit / a.H, h = unit % a.H, g = h / a.heads_per_group;
+    const int nc = a.nchunks;
+
+    if (tid == 0) {
+        for (int s = 0; s < 2; s++) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+            mbar_init(&gfull[s], 1);
+        }
+        mbar_init(mready, kEpiWarps);
+        mbar_init(yfull, 1);
+        mbar_init(yempty, kEpiWarps);
+        mbar_init(done, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == kEpiWarps + 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kEpiWarps) {
+        if (lane == 0) {
+            // producer: the C, B (state boxes of 64) and x tiles of each chunk
+            int issued = 0;
+            for (int c = 0; c < nc; c++) {
+                const int s = c & 1;
+                if (c >= 2 && !mbar_wait(&empty[s], ((c >> 1) - 1) & 1)) {
+                    record_timeout(a.status, abort_flag);
+                    break;
+                }
+                if (*(volatile int*)abort_flag) break;
+                unsigned char* st = smem + s * kStage;
+                mbar_expect_tx(&full[s], a.stage_bytes);
+                for (int bx = 0; bx < a.nbox; bx++) {
+                    tma_load_4d(st + bx * kAtom, &tmC, &full[s], 64 * bx, g, c * kQ, b);
+                    tma_load_4d(st + kTileBC + bx * kAtom, &tmB, &full[s], 64 * bx, g, c * kQ, b);
+                }
+                tma_load_3d(st + 2 * kTileBC, &tmX, &full[s], h * kP, c * kQ, b);
+                issued = c + 1;
+            }
+            // copies still in flight must land before the CTA may exit
+            for (int u = (issued > 2 ? issued - 2 : 0); u < issued; u++) mbar_wait(&full[u & 1], (u >> 1) & 1);
+        }
+    } else if (warp == kEpiWarps + 1) {
+        if (lane == 0) {
+            constexpr uint32_t idG = idesc_bf16(128, 128, false, false);
+            constexpr uint32_t idY = idesc_bf16(128, 64, false, true);
+            constexpr uint32_t idS = idesc_bf16(128, 64, true, true);
+            const int ksN = a.nstate / 16;
+            const uint32_t sM = smem_addr(smem + kOffM), sWX = smem_addr(smem + kOffWX), sH = smem_addr(smem + kOffH);
+            // G of chunk c into buffer c & 1 (whose previous contents became M before chunk c - 1's Y)
+            auto issue_g = [&](int c) -> bool {
+                const int s = c & 1;
+                if (!mbar_wait(&full[s], (c >> 1) & 1)) return false;
+                fence_after_sync();
+                const uint32_t sc = smem_addr(smem + s * kStage), sb = sc + kTileBC;
+                for (int k = 0; k < ksN; k++) {
+                    const uint32_t off = (k >> 2) * kAtom + (k & 3) * 32;
+                    umma_bf16(tmem + kColG + s * 128, sw128_desc(sc + off, 16, 1024), sw128_desc(sb + off, 16, 1024),
+                              idG, k > 0 ? 1u : 0u);
+                }
+                umma_commit(&gfull[s]);
+                return true;
+            };
+            bool ok = nc == 0 || issue_g(0);
+            for (int c = 0; ok && c < nc; c++) {
+                if (c + 1 < nc && !(ok = issue_g(c + 1))) break;
+                if (!(ok = mbar_wait(mready, c & 1))) break;
+                if (c > 0 && !(ok = mbar_wait(yempty, (c - 1) & 1))) break;
+                if (*(volatile int*)abort_flag) break;
+                fence_after_sync();
+                const int s = c & 1;
+                const uint32_t sc = smem_addr(smem + s * kStage), sb = sc + kTileBC, sx = sc + 2 * kTileBC;
+                // Yd = M x: A = M (K-major, two 64-step atoms), B = x (MN-major rows of 64 columns)
+                for (int k = 0; k < kQ / 16; k++)
+                    umma_bf16(tmem + kColYd, sw128_desc(sM + (k >> 2) * kAtom + (k & 3) * 32, 16, 1024),
+                              sw128_desc(sx + 2048 * k, 8192, 1024), idY, k > 0 ? 1u : 0u);
+                // S = B^T (w o x): A = the B tile as an MN-major operand (64-state atoms 16 KB apart)
+                for (int k = 0; k < kQ / 16; k++)
+                    umma_bf16(tmem + kColS, sw128_desc(sb + 2048 * k, kAtom, 1024), sw128_desc(sWX + 2048 * k, 8192, 1024),
+                              idS, k > 0 ? 1u : 0u);
+                // Yo = C H: A = C (K-major over states), B = H (MN-major: one row per state)
+                for (int k = 0; k < ksN; k++)
+                    umma_bf16(tmem + kColYo, sw128_desc(sc + (k >> 2) * kAtom + (k & 3) * 32, 16, 1024),
+                              sw128_desc(sH + 2048 * k, 8192, 1024), idY, k > 0 ? 1u : 0u);
+                umma_commit(yfull);
+                umma_commit(&empty[s]);
+            }
+            if (!ok) record_timeout(a.status, abort_flag);
+            // every MMA issued must have completed before TMEM is freed
+            umma_commit(done);
+            mbar_wait(done, 0);
+        }
+    } else {
+        // epilogue warps 0-7: TMEM lane quadrant `quad` (chunk rows / states 32 quad ..), column half `hf`
+        const int quad = warp & 3, hf = warp >> 2, row = quad * 32 + lane;
+        const uint32_t tl = tmem + ((uint32_t)(quad * 32) << 16);
+        const float Al2 = __ldg(a.A + h) * kLog2e;
+        const float Dv = a.D != nullptr ? __ldg(a.D + h) : 0.f;
+        const float bias = a.dt_bias != nullptr ? __ldg(a.dt_bias + h) : 0.f;
+        unsigned char* Mt = smem + kOffM;
+        unsigned char* WXt = smem + kOffWX;
+        unsigned char* Ht = smem + kOffH;
+        // the state rows of this thread: state `row`, head-dimension columns 32 hf .. + 31
+        float Hs[32];
+        const size_t hoff = ((size_t)unit * a.nstate + row) * kP + 32 * hf;
+#pragma unroll
+        for (int p = 0; p < 32; p++) Hs[p] = (a.h0 != nullptr && row < a.nstate) ? a.h0[hoff + p] : 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            float v[8];
+#pragma unroll
+            for (int e = 0; e < 8; e++) v[e] = Hs[8 * q + e];
+            *reinterpret_cast<uint4*>(swz(Ht, row, 4 * hf + q)) = pack8(v);
+        }
+        for (int c = 0; c < nc; c++) {
+            const int buf = c & 1;
+            const int t0 = c * kQ;
+            float* dlb = dl + buf * kQ;
+            float* s2b = s2 + buf * kQ;
+            // ---- Delta and the in-chunk prefix sums of Delta A (log2 units), by warps 0-3
+            if (hf == 0) {
+                const int t = t0 + row;
+                float dv = 0.f;
+                if (t < a.L) {
+                    const float v = __bfloat162float(a.dt[((size_t)b * a.L + t) * a.H + h]) + bias;
+                    dv = a.softplus ? softplus_accurate(v) : v;
+                }
+                float av = dv * Al2;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float y = __shfl_up_sync(0xffffffffu, av, o);
+                    if (lane >= o) av += y;
+                }
+                if (lane == 31) wsum[buf * 4 + quad] = av;
+                asm volatile("bar.sync 2, 128;" ::: "memory");
+                float off = 0.f;
+                for (int q = 0; q < quad; q++) off += wsum[buf * 4 + q];
+                dlb[row] = dv;
+                s2b[row] = av + off;
+            }
+            asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
+            const bool gw = mbar_wait(&gfull[buf], (c >> 1) & 1);
+            if (!gw) record_timeout(a.status, abort_flag);
+            if (!epi_all(gw && *(volatile int*)abort_flag == 0)) break;
+            fence_after_sync();
+            const float si = s2b[row];
+            const float slast = s2b[kQ - 1];
+            // ---- M row `row`, steps j in [64 hf, 64 hf + 64): the K atom hf of the A operand
+            unsigned char* Mrow = Mt + hf * kAtom;
+            if (hf == 1 && quad < 2) {
+                // rows 0..63 against steps 64..127: above the diagonal, all zero
+#pragma unroll
+                for (int ch = 0; ch < 8; ch++) *reinterpret_cast<uint4*>(swz(Mrow, row, ch)) = make_uint4(0, 0, 0, 0);
+            } else {
+#pragma unroll
+                for (int cc = 0; cc < 2; cc++) {
+                    uint32_t r[32];
+                    tmem_ld32(tl + kColG + buf * 128 + 64 * hf + 32 * cc, r);
+#pragma unroll
+                    for (int q = 0; q < 4; q++) {
+                        float v[8];
+#pragma unroll
+                        for (int e = 0; e < 8; e++) {
+                            const int j = 64 * hf + 32 * cc + 8 * q + e;
+                            const float m = __uint_as_float(r[8 * q + e]) * ex2_approx(si - s2b[j]) * dlb[j];
+                            v[e] = j <= row ? m : 0.f;
+                        }
+                        *reinterpret_cast<uint4*>(swz(Mrow, row, 4 * cc + q)) = pack8(v);
+                    }
+                }
+            }
+            // ---- w o x, row j = `row`, columns 32 hf .. + 31, w_j = exp(s_last - s_j) Delta_j;
+            // the same x values stay in registers for this thread's D x term
+            uint32_t xw[16];
+            {
+                // the x tile landed before G(c) was issued; observe its copy directly as well
+                if (!mbar_wait(&full[buf], (c >> 1) & 1)) record_timeout(a.status, abort_flag);
+                const unsigned char* Xt = smem + buf * kStage + 2 * kTileBC;
+                const float wj = ex2_approx(slast - si) * dlb[row];
+#pragma unroll
+                for (int q = 0; q < 4; q++) {
+                    const uint4 xv = *reinterpret_cast<const uint4*>(swz(const_cast<unsigned char*>(Xt), row, 4 * hf + q));
+                    xw[4 * q] = xv.x; xw[4 * q + 1] = xv.y; xw[4 * q + 2] = xv.z; xw[4 * q + 3] = xv.w;
+                    float v[8];
+#pragma unroll
+                    for (int e = 0; e < 4; e++) {
+                        v[2 * e] = wj * bf16lo(xw[4 * q + e]);
+                        v[2 * e + 1] = wj * bf16hi(xw[4 * q + e]);
+                    }
+                    *reinterpret_cast<uint4*>(swz(WXt, row, 4 * hf + q)) = pack8(v);
+                }
+            }
+            fence_async_smem();
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(mready);
+            // ---- wait for Yd, S, Yo of this chunk
+            const bool yw = mbar_wait(yfull, c & 1);
+            if (!yw) record_timeout(a.status, abort_flag);
+            if (!epi_all(yw && *(volatile int*)abort_flag == 0)) break;
+            fence_after_sync();
+            // state: H' = exp(s_last) H + S for state `row`; its bf16 copy is the next chunk's operand
+            {
+                uint32_t r[32];
+                tmem_ld32(tl + kColS + 32 * hf, r);
+                const float dec = ex2_approx(slast);
+#pragma unroll
+                for (int p = 0; p < 32; p++) Hs[p] = fmaf(dec, Hs[p], __uint_as_float(r[p]));
+#pragma unroll
+                for (int q = 0; q < 4; q++) {
+                    float v[8];
+#pragma unroll
+                    for (int e = 0; e < 8; e++) v[e] = Hs[8 * q + e];
+                    *reinterpret_cast<uint4*>(swz(Ht, row, 4 * hf + q)) = pack8(v);
+                }
+            }
+            // outputs: y = Yd + exp(s_i) Yo + D x for step t0 + row, columns 32 hf .. + 31
+            {
+                uint32_t yd[32], yo[32];
+                tmem_ld32(tl + kColYd + 32 * hf, yd);
+                tmem_ld32(tl + kColYo + 32 * hf, yo);
+                const float es = ex2_approx(si);
+                float y[32];
+#pragma unroll
+                for (int e = 0; e < 16; e++) {
+                    y[2 * e] = fmaf(Dv, bf16lo(xw[e]), fmaf(es, __uint_as_float(yo[2 * e]), __uint_as_float(yd[2 * e])));
+                    y[2 * e + 1] =
+                        fmaf(Dv, bf16hi(xw[e]), fmaf(es, __uint_as_float(yo[2 * e + 1]), __uint_as_float(yd[2 * e + 1])));
+                }
+                const int t = t0 + row;
+                if (t < a.L) {
+                    Tout* orow = static_cast<Tout*>(a.out) + (((size_t)b * a.L + t) * a.H + h) * kP + 32 * hf;
+                    if constexpr (sizeof(Tout) == 2) {
+#pragma unroll
+                        for (int q = 0; q < 4; q++) {
+                            float v[8];
+#pragma unroll
+                            for (int e = 0; e < 8; e++) v[e] = y[8 * q + e];
+                            reinterpret_cast<uint4*>(orow)[q] = pack8(v);
+                        }
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 8; q++)
+                            reinterpret_cast<float4*>(orow)[q] = make_float4(y[4 * q], y[4 * q + 1], y[4 * q + 2], y[4 * q + 3]);
+                    }
+                }
+            }
+            fence_async_smem();
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(yempty);
+        }
+        if (a.final_state != nullptr && row < a.nstate && *(volatile int*)abort_flag == 0) {
+#pragma unroll
+            for (int q = 0; q < 8; q++)
+                reinterpret_cast<float4*>(a.final_state + hoff)[q] =
+                    make_float4(Hs[4 * q], Hs[4 * q + 1], Hs[4 * q + 2], Hs[4 * q + 3]);
+        }
+    }
+    fence_before_sync();
+    __syncthreads();
+    if (warp == kEpiWarps + 1) {
+        fence_after_sync();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    }
+}
+
+template <typename Tout>
+cudaError_t launch_typed(const CUtensorMap& tmC, const CUtensorMap& tmB, const CUtensorMap& tmX, const SsdArgs& a,
+                         int units, cudaStream_t st) {
+    cudaError_t e = prepare_kernel<ssd_chunk_kernel<Tout>>(kSmem);
+    if (e != cudaSuccess) return e;
+    ssd_chunk_kernel<Tout><<<units, kThreads, kSmem, st>>>(tmC, tmB, tmX, a);
+    count_launches(1);
+    return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_ssd_fwd(const ssm_ssd_fwd_params* p, cudaStream_t st) {
+    const size_t state_bytes = (size_t)p->batch * p->nheads * p->dstate * kP * sizeof(float);
+    if (p->seqlen == 0) {
+        // no steps: the final state is the initial one
+        if (p->final_state == nullptr) return cudaSuccess;
+        if (p->h0 != nullptr)
+            return cudaMemcpyAsync(p->final_state, p->h0, state_bytes, cudaMemcpyDeviceToDevice, st);
+        return cudaMemsetAsync(p->final_state, 0, state_bytes, st);
+    }
+    alignas(64) CUtensorMap tmC, tmB, tmX;
+    cudaError_t e;
+    {
+        // B and C as (N, groups, L, batch): a box is 64 states of one group over 128 steps
+        const uint64_t N = (uint64_t)p->dstate, G = (uint64_t)p->ngroups, L = (uint64_t)p->seqlen;
+        const uint64_t dims[4] = {N, G, L, (uint64_t)p->batch};
+        const uint64_t strides[3] = {N * 2, G * N * 2, L * G * N * 2};
+        const uint32_t box[4] = {64, 1, (uint32_t)kQ, 1};
+        if ((e = tc::encode_bf16_map(&tmC, p->C, 4, dims, strides, box, true, true)) != cudaSuccess) return e;
+        if ((e = tc::encode_bf16_map(&tmB, p->B, 4, dims, strides, box, true, true)) != cudaSuccess) return e;
+    }
+    {
+        // x as (H P, L, batch): a box is one head's 64 columns over 128 steps
+        const uint64_t HP = (uint64_t)p->nheads * kP, L = (uint64_t)p->seqlen;
+        const uint64_t dims[3] = {HP, L, (uint64_t)p->batch};
+        const uint64_t strides[2] = {HP * 2, L * HP * 2};
+        const uint32_t box[3] = {64, (uint32_t)kQ, 1};
+        if ((e = tc::encode_bf16_map(&tmX, p->x, 3, dims, strides, box, true, false)) != cudaSuccess) return e;
+    }
     SsdArgs a;
-    a.batch = p->batch; a.seqlen = p->seqlen; a.nheads = p->nheads; a.ngroups = p->ngroups;
-    a.x = static_cast<const __nv_bfloat16*>(p->x);
+    a.L = (int)p->seqlen;
+    a.H = (int)p->nheads;
+    a.heads_per_group = (int)(p->nheads / p->ngroups);
+    a.nstate = (int)p->dstate;
+    a.nbox = p->dstate > 64 ? 2 : 1;
+    a.nchunks = (int)ceil_div(p->seqlen, (int64_t)kQ);
+    a.stage_bytes = (uint32_t)(2 * a.nbox * kAtom + kTileX);
     a.dt = static_cast<const __nv_bfloat16*>(p->dt);
     a.A = p->A;
-    a.B = static_cast<const __nv_bfloat16*>(p->B);
-    a.C = static_cast<const __nv_bfloat16*>(p->C);
-    a.D = p->D; a.dt_bias = p->dt_bias; a.h0 = p->h0; a.final_state = p->final_state;
+    a.D = p->D;
+    a.dt_bias = p->dt_bias;
+    a.h0 = p->h0;
+    a.final_state = p->final_state;
     a.out = p->out;
     a.softplus = p->delta_softplus ? 1 : 0;
-    if (p->seqlen == 0) {
-        // no steps: the final state is h0 (or zero); zero chunks run the set-up and the store only
-        if (p->final_state == nullptr) return cudaSuccess;
-    }
-    return p->out_dtype == SSM_BF16 ? launch_ssd_n<__nv_bfloat16>(a, p->dstate, st)
-                                    : launch_ssd_n<float>(a, p->dstate, st);
+    if ((e = tc::device_status_word(&a.status)) != cudaSuccess) return e;
+    const int units = (int)(p->batch * p->nheads);
+    return p->out_dtype == SSM_BF16 ? launch_typed<__nv_bfloat16>(tmC, tmB, tmX, a, units, st)
+                                    : launch_typed<float>(tmC, tmB, tmX, a, units, st);
 }
 
 }  // namespace ssm

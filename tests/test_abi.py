@@ -47,7 +47,7 @@ def test_status_strings_and_version(lib):
     names = {c: lib.ssm_status_string(c).decode() for c in (0, -1, -2, -3, -4, -5, -99)}
     assert names[0] == "SSM_OK" and names[-1] == "SSM_ERR_INVALID_ARG"
     assert names[-5] == "SSM_ERR_CUDA" and names[-99] == "SSM_ERR_UNKNOWN"
-    assert lib.ssm_abi_version() == 5
+    assert lib.ssm_abi_version() == 6
 
 
 def test_host_validation_without_gpu():
