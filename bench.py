@@ -713,6 +713,8 @@ def main(argv=None):
     ap.add_argument("--no-configs", action="store_true", help="skip the other workloads' timed lines")
     ap.add_argument("--proj-only", action="store_true",
                     help="time only the x_proj / dt_proj products at --seqlen (for profiling captures)")
+    ap.add_argument("--ssd-only", action="store_true",
+                    help="time only the Mamba-2 SSD forward (for profiling captures)")
     ap.add_argument("--e2e-steps", type=int, default=6)
     ap.add_argument("--seqlen", type=int, default=0,
                     help="shorter sequence for small profiling captures (the headline uses the default)")
@@ -734,6 +736,9 @@ def main(argv=None):
         cfg["seqlen"] = args.seqlen
     if args.proj_only:
         print(json.dumps({"x_dt_proj": bench_x_dt_proj(L, device, cfg)}), flush=True)
+        return 0
+    if args.ssd_only:
+        print(json.dumps({"ssd": bench_ssd(L, device, SSD, reps=3)}), flush=True)
         return 0
     seed = S.config_seed(2) + 1000 * rank          # every rank its own batch (weak scaling)
     g = make_inputs(device, seed, cfg)

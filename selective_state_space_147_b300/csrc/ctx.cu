@@ -43,9 +43,10 @@ typedef CUresult (*PfnEncodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
 
 namespace tc {
 
-// Tiled bf16 tensor map; elements outside the tensor read as zero.
-cudaError_t encode_bf16_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
-                            const uint64_t* strides_bytes, const uint32_t* box, bool swizzle128, bool l2_promote) {
+// Tiled tensor map; elements outside the tensor read as zero (and are not written by stores).
+cudaError_t encode_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                       const uint64_t* strides_bytes, const uint32_t* box, bool swizzle128, bool l2_promote,
+                       bool fp32) {
     static PfnEncodeTiled fn = nullptr;
     if (fn == nullptr) {
         void* f = nullptr;
@@ -64,7 +65,7 @@ cudaError_t encode_bf16_map(CUtensorMap* map, const void* base, int rank, const 
         es[i] = 1;
         if (i + 1 < rank) st[i] = strides_bytes[i];
     }
-    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), d, st, bx, es,
+    const CUresult r = fn(map, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), d, st, bx, es,
                           CU_TENSOR_MAP_INTERLEAVE_NONE,
                           swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                           l2_promote ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B : CU_TENSOR_MAP_L2_PROMOTION_NONE,

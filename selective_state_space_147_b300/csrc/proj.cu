@@ -150,7 +150,9 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
         }
     } else if (warp == kPEpiWarps + 1) {
         if (lane == 0) {
-            // MMA issuer
+            // MMA issuer; descriptors of stage 0 built once (stage s is s * kPStage bytes further)
+            const uint64_t dA0 = sw128_desc(smem_addr(base), 16, 1024);
+            const uint64_t dB0 = sw128_desc(smem_addr(base + kPTileA), kPTileB / 2, 1024);
             int it = 0, local = 0;
             for (int tile = blockIdx.x; tile < a.tiles; tile += gridDim.x, local++) {
                 if (*(volatile int*)abort_flag) break;
@@ -170,8 +172,6 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
                         break;
                     }
                     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                    const uint32_t sa = smem_addr(base + s * kPStage);
-                    const uint32_t sb = sa + kPTileA;
 #pragma unroll
                     for (int k = 0; k < kPK / 16; k++) {
                         // A: K-major rows of 128 bytes, 8-row groups 1024 bytes apart; the
@@ -179,8 +179,9 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
                         // B: token-major rows of 128 bytes (64 tokens), 8-row groups of K
                         // 1024 bytes apart, the second 64 tokens 8 KB further; the K step
                         // of 16 rows is 2 KB.
-                        umma_bf16(dcol, sw128_desc(sa + 32 * k, 16, 1024), sw128_desc(sb + 2048 * k, kPTileB / 2, 1024),
-                                  kProjIdesc, (kb > 0 || k > 0) ? 1u : 0u);
+                        const uint64_t so = (uint64_t)(s * (kPStage >> 4));
+                        umma_bf16(dcol, dA0 + so + kmajor_step(k, 0), dB0 + so + mnmajor_step(k), kProjIdesc,
+                                  (kb > 0 || k > 0) ? 1u : 0u);
                     }
                     umma_commit(&empty[s]);   // the stage is free once these MMAs have read it
                 }

@@ -61,9 +61,10 @@ constexpr int kOffM = kStages * kStage;           // M: K-major A operand, two 6
 constexpr int kOffWX = kOffM + 2 * kAtom;         // w o x: MN-major B operand
 constexpr int kOffH = kOffWX + kTileX;            // the entering state in bf16: MN-major B operand
 constexpr int kOffAux = kOffH + kTileX;
-// aux: Delta[2][128], s[2][128] (fp32, double-buffered by chunk parity), warp sums [2][4] (+ pad), barriers
-constexpr int kAuxFloats = 2 * kQ * 2 + 16;
-constexpr int kNumBars = 2 + 2 + 2 + 1 + 1 + 1 + 1;   // full, empty, gfull, mready, yfull, yempty, done
+// aux: Delta[2][128], s[2][128] (fp32, double-buffered by chunk parity), warp sums [2][4] (+ pad),
+// the column factors of the blocks below M's diagonal [128], barriers
+constexpr int kAuxFloats = 2 * kQ * 2 + 16 + kQ;
+constexpr int kNumBars = 2 + 2 + 2 + 1 + 1 + 1 + 1 + 1;   // full, empty, gfull, wready, mready, yfull, yempty, done
 constexpr int kSmem = kOffAux + kAuxFloats * 4 + kNumBars * 8 + 16;
 // TMEM columns: G (two buffers), Yd, Yo, S
 constexpr uint32_t kColG = 0, kColYd = 256, kColYo = 320, kColS = 384, kTmemCols = 512;
@@ -110,7 +111,7 @@ __device__ __forceinline__ unsigned char* swz(unsigned char* tile, int r, int ch
 template <typename Tout>
 __global__ void __launch_bounds__(kThreads, 1)
 ssd_chunk_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmB,
-                 const __grid_constant__ CUtensorMap tmX, const SsdArgs a) {
+                 const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmY, const SsdArgs a) {
     extern __shared__ __align__(1024) unsigned char smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // the swizzled tiles need a 1024-byte aligned base: refuse (uniformly) otherwise
@@ -121,10 +122,12 @@ ssd_chunk_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant_
     float* dl = reinterpret_cast<float*>(smem + kOffAux);   // Delta [2][128]
     float* s2 = dl + 2 * kQ;                                  // s log2(e) [2][128]
     float* wsum = s2 + 2 * kQ;                                // [2][4]
-    uint64_t* full = reinterpret_cast<uint64_t*>(wsum + 16);
+    float* cf = wsum + 16;                                    // [128]
+    uint64_t* full = reinterpret_cast<uint64_t*>(cf + kQ);
     uint64_t* empty = full + 2;
     uint64_t* gfull = empty + 2;
-    uint64_t* mready = gfull + 2;
+    uint64_t* wready = gfull + 2;
+    uint64_t* mready = wready + 1;
     uint64_t* yfull = mready + 1;
     uint64_t* yempty = yfull + 1;
     uint64_t* done = yempty + 1;
@@ -141,6 +144,7 @@ ssd_chunk_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant_
             mbar_init(&empty[s], 1);
             mbar_init(&gfull[s], 1);
         }
+        mbar_init(wready, kEpiWarps);
         mbar_init(mready, kEpiWarps);
         mbar_init(yfull, 1);
         mbar_init(yempty, kEpiWarps);
@@ -188,44 +192,64 @@ ssd_chunk_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant_
             constexpr uint32_t idY = idesc_bf16(128, 64, false, true);
             constexpr uint32_t idS = idesc_bf16(128, 64, true, true);
             const int ksN = a.nstate / 16;
-            const uint32_t sM = smem_addr(smem + kOffM), sWX = smem_addr(smem + kOffWX), sH = smem_addr(smem + kOffH);
+            // descriptors built once; a K step adds a constant to the start-address field
+            const uint64_t dM = sw128_desc(smem_addr(smem + kOffM), 16, 1024);
+            const uint64_t dWX = sw128_desc(smem_addr(smem + kOffWX), 8192, 1024);
+            const uint64_t dH = sw128_desc(smem_addr(smem + kOffH), 8192, 1024);
+            // stage 0's tiles; stage s is s * kStage bytes further
+            const uint32_t st0 = smem_addr(smem);
+            const uint64_t dC0 = sw128_desc(st0, 16, 1024);                   // C: K-major over states
+            const uint64_t dB0 = sw128_desc(st0 + kTileBC, 16, 1024);         // B: K-major (G's B operand)
+            const uint64_t dBt0 = sw128_desc(st0 + kTileBC, kAtom, 1024);     // B read state-major (S's A operand)
+            const uint64_t dX0 = sw128_desc(st0 + 2 * kTileBC, 8192, 1024);   // x: MN-major rows of 64 columns
+            auto stage_off = [](int s) { return (uint64_t)(s * (kStage >> 4)); };
             // G of chunk c into buffer c & 1 (whose previous contents became M before chunk c - 1's Y)
             auto issue_g = [&](int c) -> bool {
                 const int s = c & 1;
                 if (!mbar_wait(&full[s], (c >> 1) & 1)) return false;
                 fence_after_sync();
-                const uint32_t sc = smem_addr(smem + s * kStage), sb = sc + kTileBC;
-                for (int k = 0; k < ksN; k++) {
-                    const uint32_t off = (k >> 2) * kAtom + (k & 3) * 32;
-                    umma_bf16(tmem + kColG + s * 128, sw128_desc(sc + off, 16, 1024), sw128_desc(sb + off, 16, 1024),
-                              idG, k > 0 ? 1u : 0u);
-                }
+#pragma unroll
+                for (int k = 0; k < 8; k++)
+                    if (k < ksN)
+                        umma_bf16(tmem + kColG + s * 128, dC0 + stage_off(s) + kmajor_step(k, kAtom),
+                                  dB0 + stage_off(s) + kmajor_step(k, kAtom), idG, k > 0 ? 1u : 0u);
                 umma_commit(&gfull[s]);
                 return true;
             };
             bool ok = nc == 0 || issue_g(0);
             for (int c = 0; ok && c < nc; c++) {
-                if (c + 1 < nc && !(ok = issue_g(c + 1))) break;
-                if (!(ok = mbar_wait(mready, c & 1))) break;
-                if (c > 0 && !(ok = mbar_wait(yempty, (c - 1) & 1))) break;
+                // the next chunk's G goes first if its tiles have landed, else after this chunk's Y
+                bool g_next = c + 1 < nc && mbar_test(&full[(c + 1) & 1], ((c + 1) >> 1) & 1);
+                if (g_next && !(ok = issue_g(c + 1))) break;
+                // the accumulators were read out and the entering state's copy written (phase c:
+                // the epilogue arrives once after writing the initial state, then after each chunk)
+                if (!(ok = mbar_wait(yempty, c & 1))) break;
                 if (*(volatile int*)abort_flag) break;
                 fence_after_sync();
                 const int s = c & 1;
-                const uint32_t sc = smem_addr(smem + s * kStage), sb = sc + kTileBC, sx = sc + 2 * kTileBC;
-                // Yd = M x: A = M (K-major, two 64-step atoms), B = x (MN-major rows of 64 columns)
-                for (int k = 0; k < kQ / 16; k++)
-                    umma_bf16(tmem + kColYd, sw128_desc(sM + (k >> 2) * kAtom + (k & 3) * 32, 16, 1024),
-                              sw128_desc(sx + 2048 * k, 8192, 1024), idY, k > 0 ? 1u : 0u);
-                // S = B^T (w o x): A = the B tile as an MN-major operand (64-state atoms 16 KB apart)
-                for (int k = 0; k < kQ / 16; k++)
-                    umma_bf16(tmem + kColS, sw128_desc(sb + 2048 * k, kAtom, 1024), sw128_desc(sWX + 2048 * k, 8192, 1024),
-                              idS, k > 0 ? 1u : 0u);
                 // Yo = C H: A = C (K-major over states), B = H (MN-major: one row per state)
-                for (int k = 0; k < ksN; k++)
-                    umma_bf16(tmem + kColYo, sw128_desc(sc + (k >> 2) * kAtom + (k & 3) * 32, 16, 1024),
-                              sw128_desc(sH + 2048 * k, 8192, 1024), idY, k > 0 ? 1u : 0u);
+#pragma unroll
+                for (int k = 0; k < 8; k++)
+                    if (k < ksN)
+                        umma_bf16(tmem + kColYo, dC0 + stage_off(s) + kmajor_step(k, kAtom), dH + mnmajor_step(k), idY,
+                                  k > 0 ? 1u : 0u);
+                // S = B^T (w o x): A = the B tile as an MN-major operand (64-state atoms 16 KB apart)
+                if (!(ok = mbar_wait(wready, c & 1))) break;
+                fence_after_sync();
+#pragma unroll
+                for (int k = 0; k < kQ / 16; k++)
+                    umma_bf16(tmem + kColS, dBt0 + stage_off(s) + mnmajor_step(k), dWX + mnmajor_step(k), idS,
+                              k > 0 ? 1u : 0u);
+                // Yd = M x: A = M (K-major, two 64-step atoms), B = x (MN-major rows of 64 columns)
+                if (!(ok = mbar_wait(mready, c & 1))) break;
+                fence_after_sync();
+#pragma unroll
+                for (int k = 0; k < kQ / 16; k++)
+                    umma_bf16(tmem + kColYd, dM + kmajor_step(k, kAtom), dX0 + stage_off(s) + mnmajor_step(k), idY,
+                              k > 0 ? 1u : 0u);
                 umma_commit(yfull);
                 umma_commit(&empty[s]);
+                if (c + 1 < nc && !g_next && !(ok = issue_g(c + 1))) break;
             }
             if (!ok) record_timeout(a.status, abort_flag);
             // every MMA issued must have completed before TMEM is freed
@@ -254,68 +278,55 @@ ssd_chunk_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant_
             for (int e = 0; e < 8; e++) v[e] = Hs[8 * q + e];
             *reinterpret_cast<uint4*>(swz(Ht, row, 4 * hf + q)) = pack8(v);
         }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(yempty);
+        // Delta and the in-chunk prefix sums of Delta A (log2 units) of chunk c into
+        // buffer c & 1, by warps 0-3 (one step each)
+        auto chunk_delta = [&](int c) {
+            if (hf != 0) return;
+            const int t = c * kQ + row;
+            float dv = 0.f;
+            if (t < a.L) {
+                const float v = __bfloat162float(a.dt[((size_t)b * a.L + t) * a.H + h]) + bias;
+                dv = a.softplus ? softplus_accurate(v) : v;
+            }
+            float av = dv * Al2;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, av, o);
+                if (lane >= o) av += y;
+            }
+            float* wsb = wsum + (c & 1) * 4;
+            if (lane == 31) wsb[quad] = av;
+            asm volatile("bar.sync 2, 128;" ::: "memory");
+            float off = 0.f;
+            for (int q = 0; q < quad; q++) off += wsb[q];
+            dl[(c & 1) * kQ + row] = dv;
+            s2[(c & 1) * kQ + row] = av + off;
+        };
+        if (nc > 0) chunk_delta(0);
+        asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
         for (int c = 0; c < nc; c++) {
             const int buf = c & 1;
             const int t0 = c * kQ;
             float* dlb = dl + buf * kQ;
             float* s2b = s2 + buf * kQ;
-            // ---- Delta and the in-chunk prefix sums of Delta A (log2 units), by warps 0-3
-            if (hf == 0) {
-                const int t = t0 + row;
-                float dv = 0.f;
-                if (t < a.L) {
-                    const float v = __bfloat162float(a.dt[((size_t)b * a.L + t) * a.H + h]) + bias;
-                    dv = a.softplus ? softplus_accurate(v) : v;
-                }
-                float av = dv * Al2;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const float y = __shfl_up_sync(0xffffffffu, av, o);
-                    if (lane >= o) av += y;
-                }
-                if (lane == 31) wsum[buf * 4 + quad] = av;
-                asm volatile("bar.sync 2, 128;" ::: "memory");
-                float off = 0.f;
-                for (int q = 0; q < quad; q++) off += wsum[buf * 4 + q];
-                dlb[row] = dv;
-                s2b[row] = av + off;
-            }
-            asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
-            const bool gw = mbar_wait(&gfull[buf], (c >> 1) & 1);
-            if (!gw) record_timeout(a.status, abort_flag);
-            if (!epi_all(gw && *(volatile int*)abort_flag == 0)) break;
-            fence_after_sync();
             const float si = s2b[row];
             const float slast = s2b[kQ - 1];
-            // ---- M row `row`, steps j in [64 hf, 64 hf + 64): the K atom hf of the A operand
-            unsigned char* Mrow = Mt + hf * kAtom;
-            if (hf == 1 && quad < 2) {
-                // rows 0..63 against steps 64..127: above the diagonal, all zero
-#pragma unroll
-                for (int ch = 0; ch < 8; ch++) *reinterpret_cast<uint4*>(swz(Mrow, row, ch)) = make_uint4(0, 0, 0, 0);
-            } else {
-#pragma unroll
-                for (int cc = 0; cc < 2; cc++) {
-                    uint32_t r[32];
-                    tmem_ld32(tl + kColG + buf * 128 + 64 * hf + 32 * cc, r);
-#pragma unroll
-                    for (int q = 0; q < 4; q++) {
-                        float v[8];
-#pragma unroll
-                        for (int e = 0; e < 8; e++) {
-                            const int j = 64 * hf + 32 * cc + 8 * q + e;
-                            const float m = __uint_as_float(r[8 * q + e]) * ex2_approx(si - s2b[j]) * dlb[j];
-                            v[e] = j <= row ? m : 0.f;
-                        }
-                        *reinterpret_cast<uint4*>(swz(Mrow, row, 4 * cc + q)) = pack8(v);
-                    }
-                }
+            // ---- column factors of the blocks below M's diagonal: cf_j = exp(s_e - s_j) Delta_j with
+            // e the last step of j's 32-step block, so that for i in a later block
+            // exp(s_i - s_j) Delta_j = exp(s_i - s_e) cf_j with both exponents <= 0
+            if (hf == 0) cf[row] = ex2_approx(s2b[32 * quad + 31] - si) * dlb[row];
+            // bf16: the previous chunk's output store must have read its staging rows (w o x's buffer)
+            if constexpr (sizeof(Tout) == 2) {
+                if (tid == 0 && c > 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
             }
+            asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
             // ---- w o x, row j = `row`, columns 32 hf .. + 31, w_j = exp(s_last - s_j) Delta_j;
             // the same x values stay in registers for this thread's D x term
             uint32_t xw[16];
             {
-                // the x tile landed before G(c) was issued; observe its copy directly as well
                 if (!mbar_wait(&full[buf], (c >> 1) & 1)) record_timeout(a.status, abort_flag);
                 const unsigned char* Xt = smem + buf * kStage + 2 * kTileBC;
                 const float wj = ex2_approx(slast - si) * dlb[row];
@@ -333,9 +344,61 @@ ssd_chunk_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant_
                 }
             }
             fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(wready);
+            // ---- M row `row`, 32-step column blocks cb = 2 hf, 2 hf + 1 (K atom hf of the A operand)
+            const bool gw = mbar_wait(&gfull[buf], (c >> 1) & 1);
+            if (!gw) record_timeout(a.status, abort_flag);
+            if (!epi_all(gw && *(volatile int*)abort_flag == 0)) break;
+            fence_after_sync();
+            unsigned char* Mrow = Mt + hf * kAtom;
+#pragma unroll
+            for (int cc = 0; cc < 2; cc++) {
+                const int cb = 2 * hf + cc;
+                if (cb > quad) {
+                    // above the diagonal: zero
+#pragma unroll
+                    for (int q = 0; q < 4; q++)
+                        *reinterpret_cast<uint4*>(swz(Mrow, row, 4 * cc + q)) = make_uint4(0, 0, 0, 0);
+                    continue;
+                }
+                uint32_t r[32];
+                tmem_ld32(tl + kColG + buf * 128 + 32 * cb, r);
+                if (cb < quad) {
+                    // below the diagonal block: the factored decay
+                    const float ri = ex2_approx(si - s2b[32 * cb + 31]);
+#pragma unroll
+                    for (int q = 0; q < 4; q++) {
+                        const float4 f0 = *reinterpret_cast<const float4*>(cf + 32 * cb + 8 * q);
+                        const float4 f1 = *reinterpret_cast<const float4*>(cf + 32 * cb + 8 * q + 4);
+                        const float fj[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+                        float v[8];
+#pragma unroll
+                        for (int e = 0; e < 8; e++) v[e] = __uint_as_float(r[8 * q + e]) * ri * fj[e];
+                        *reinterpret_cast<uint4*>(swz(Mrow, row, 4 * cc + q)) = pack8(v);
+                    }
+                } else {
+                    // the diagonal block: the decay per element, zero above the diagonal
+#pragma unroll
+                    for (int q = 0; q < 4; q++) {
+                        float v[8];
+#pragma unroll
+                        for (int e = 0; e < 8; e++) {
+                            const int j = 32 * cb + 8 * q + e;
+                            const float m = __uint_as_float(r[8 * q + e]) * ex2_approx(si - s2b[j]) * dlb[j];
+                            v[e] = j <= row ? m : 0.f;
+                        }
+                        *reinterpret_cast<uint4*>(swz(Mrow, row, 4 * cc + q)) = pack8(v);
+                    }
+                }
+            }
+            fence_async_smem();
             fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(mready);
+            // the next chunk's Delta and prefix sums while this chunk's products run
+            // (buffer (c + 1) & 1 was last read before the barrier that ended chunk c - 1)
+            if (c + 1 < nc) chunk_delta(c + 1);
             // ---- wait for Yd, S, Yo of this chunk
             const bool yw = mbar_wait(yfull, c & 1);
             if (!yw) record_timeout(a.status, abort_flag);
@@ -356,42 +419,64 @@ ssd_chunk_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant_
                     *reinterpret_cast<uint4*>(swz(Ht, row, 4 * hf + q)) = pack8(v);
                 }
             }
+            // the state copy is visible to the tensor core before any global store is in flight
+            // (the proxy fence would otherwise wait for those stores too)
+            fence_async_smem();
             // outputs: y = Yd + exp(s_i) Yo + D x for step t0 + row, columns 32 hf .. + 31
+            float y[32];
             {
                 uint32_t yd[32], yo[32];
                 tmem_ld32(tl + kColYd + 32 * hf, yd);
                 tmem_ld32(tl + kColYo + 32 * hf, yo);
                 const float es = ex2_approx(si);
-                float y[32];
 #pragma unroll
                 for (int e = 0; e < 16; e++) {
                     y[2 * e] = fmaf(Dv, bf16lo(xw[e]), fmaf(es, __uint_as_float(yo[2 * e]), __uint_as_float(yd[2 * e])));
                     y[2 * e + 1] =
                         fmaf(Dv, bf16hi(xw[e]), fmaf(es, __uint_as_float(yo[2 * e + 1]), __uint_as_float(yd[2 * e + 1])));
                 }
-                const int t = t0 + row;
-                if (t < a.L) {
-                    Tout* orow = static_cast<Tout*>(a.out) + (((size_t)b * a.L + t) * a.H + h) * kP + 32 * hf;
-                    if constexpr (sizeof(Tout) == 2) {
-#pragma unroll
-                        for (int q = 0; q < 4; q++) {
-                            float v[8];
-#pragma unroll
-                            for (int e = 0; e < 8; e++) v[e] = y[8 * q + e];
-                            reinterpret_cast<uint4*>(orow)[q] = pack8(v);
-                        }
-                    } else {
-#pragma unroll
-                        for (int q = 0; q < 8; q++)
-                            reinterpret_cast<float4*>(orow)[q] = make_float4(y[4 * q], y[4 * q + 1], y[4 * q + 2], y[4 * q + 3]);
-                    }
-                }
             }
-            fence_async_smem();
+            // TMEM read out: hand the accumulators back
             fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(yempty);
+            // stage the 128 x 64 output tile (128-byte swizzled rows; fp32: two 32-column boxes)
+            // where this chunk's M (fp32) or w o x (bf16) was -- both consumed by now -- and
+            // write it with bulk tensor stores (rows past the sequence end are not written)
+            {
+                unsigned char* Yt = sizeof(Tout) == 2 ? WXt : Mt;
+                if constexpr (sizeof(Tout) == 2) {
+#pragma unroll
+                    for (int q = 0; q < 4; q++) {
+                        float v[8];
+#pragma unroll
+                        for (int e = 0; e < 8; e++) v[e] = y[8 * q + e];
+                        *reinterpret_cast<uint4*>(swz(Yt, row, 4 * hf + q)) = pack8(v);
+                    }
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 8; q++)
+                        *reinterpret_cast<float4*>(swz(Yt + hf * kAtom, row, q)) =
+                            make_float4(y[4 * q], y[4 * q + 1], y[4 * q + 2], y[4 * q + 3]);
+                }
+                fence_async_smem();
+                asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
+                if (tid == 0) {
+                    if constexpr (sizeof(Tout) == 2) {
+                        tma_store_3d(&tmY, Yt, h * kP, t0, b);
+                    } else {
+                        tma_store_3d(&tmY, Yt, h * kP, t0, b);
+                        tma_store_3d(&tmY, Yt + kAtom, h * kP + 32, t0, b);
+                    }
+                    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                    // fp32 staging sits in M's place, which the next chunk rewrites first
+                    if constexpr (sizeof(Tout) != 2) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                }
+            }
+            // the next chunk's Delta and prefix sums are visible; every thread is done with this chunk's
+            asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
         }
+        if (tid == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
         if (a.final_state != nullptr && row < a.nstate && *(volatile int*)abort_flag == 0) {
 #pragma unroll
             for (int q = 0; q < 8; q++)
@@ -409,10 +494,18 @@ ssd_chunk_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant_
 
 template <typename Tout>
 cudaError_t launch_typed(const CUtensorMap& tmC, const CUtensorMap& tmB, const CUtensorMap& tmX, const SsdArgs& a,
-                         int units, cudaStream_t st) {
-    cudaError_t e = prepare_kernel<ssd_chunk_kernel<Tout>>(kSmem);
+                         int64_t batch, int units, cudaStream_t st) {
+    // y as (H P, L, batch): a box is 128 steps of one head's 64 columns (fp32: 32 columns)
+    alignas(64) CUtensorMap tmY;
+    const uint64_t HP = (uint64_t)a.H * kP, L = (uint64_t)a.L, es = sizeof(Tout);
+    const uint64_t dims[3] = {HP, L, (uint64_t)batch};
+    const uint64_t strides[2] = {HP * es, L * HP * es};
+    const uint32_t box[3] = {(uint32_t)(128 / es), (uint32_t)kQ, 1};
+    cudaError_t e = tc::encode_map(&tmY, a.out, 3, dims, strides, box, true, false, es == 4);
     if (e != cudaSuccess) return e;
-    ssd_chunk_kernel<Tout><<<units, kThreads, kSmem, st>>>(tmC, tmB, tmX, a);
+    e = prepare_kernel<ssd_chunk_kernel<Tout>>(kSmem);
+    if (e != cudaSuccess) return e;
+    ssd_chunk_kernel<Tout><<<units, kThreads, kSmem, st>>>(tmC, tmB, tmX, tmY, a);
     count_launches(1);
     return cudaGetLastError();
 }
@@ -465,8 +558,8 @@ cudaError_t launch_ssd_fwd(const ssm_ssd_fwd_params* p, cudaStream_t st) {
     a.softplus = p->delta_softplus ? 1 : 0;
     if ((e = tc::device_status_word(&a.status)) != cudaSuccess) return e;
     const int units = (int)(p->batch * p->nheads);
-    return p->out_dtype == SSM_BF16 ? launch_typed<__nv_bfloat16>(tmC, tmB, tmX, a, units, st)
-                                    : launch_typed<float>(tmC, tmB, tmX, a, units, st);
+    return p->out_dtype == SSM_BF16 ? launch_typed<__nv_bfloat16>(tmC, tmB, tmX, a, p->batch, units, st)
+                                    : launch_typed<float>(tmC, tmB, tmX, a, p->batch, units, st);
 }
 
 }  // namespace ssm

@@ -45,6 +45,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     }
 }
 
+// true if the phase of parity `parity` has completed (does not wait)
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
@@ -90,6 +101,17 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
     return d;
 }
 
+// Start-address offsets (16-byte units, added to a descriptor) of the K step k
+// of 16 elements: K-major tiles of 64-wide atoms `atom_bytes` apart, and
+// MN-major tiles (16 rows of 128 bytes per step).  The issuing thread adds
+// these to descriptors built once, so a tcgen05.mma costs it a few
+// instructions: built per instruction, descriptors made the issue rate, not
+// the tensor core, the bound.
+__host__ __device__ constexpr uint64_t kmajor_step(int k, int atom_bytes) {
+    return (uint64_t)(((k >> 2) * atom_bytes + (k & 3) * 32) >> 4);
+}
+__host__ __device__ constexpr uint64_t mnmajor_step(int k) { return (uint64_t)(k * 128); }
+
 // Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, the
 // major-ness of each operand (true = MN-major), N >> 3 and M >> 4.
 __host__ __device__ constexpr uint32_t idesc_bf16(int m, int n, bool a_mn_major, bool b_mn_major) {
@@ -97,12 +119,20 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int m, int n, bool a_mn_major,
            ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
-// D (TMEM) (+)= A (smem) B (smem), issued by one thread
+// D (TMEM) (+)= A (smem) B (smem), issued by one thread.  Each descriptor is
+// passed as its two 32-bit halves and assembled into a 64-bit register inside
+// the instruction's own asm block: the high half is a per-operand constant
+// (stride offsets, version, swizzle), the low half the start address (plus
+// the leading offset), so a K step is one 32-bit add.  (With both 64-bit
+// descriptors held in registers across the issuing loop, products that shared
+// an A descriptor with an earlier one read the wrong B operand.)
 __device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                           uint32_t accumulate) {
     asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
-        ::"r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        "{\n .reg .pred p;\n .reg .b64 ad, bd;\n mov.b64 ad, {%1, %2};\n mov.b64 bd, {%3, %4};\n"
+        " setp.ne.b32 p, %6, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %5, p;\n}\n"
+        ::"r"(tmem_d), "r"((uint32_t)adesc), "r"((uint32_t)(adesc >> 32)), "r"((uint32_t)bdesc),
+        "r"((uint32_t)(bdesc >> 32)), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 // arrive on `bar` once every tcgen05.mma issued so far by this thread has completed
@@ -129,9 +159,16 @@ __device__ __forceinline__ void fence_after_sync() { asm volatile("tcgen05.fence
 // generic-proxy shared-memory writes become visible to the tensor core / TMA
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-// host: a bf16 tensor map (rank <= 5); strides in bytes for dimensions 1..rank-1
-cudaError_t encode_bf16_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
-                            const uint64_t* strides_bytes, const uint32_t* box, bool swizzle128, bool l2_promote);
+// host: a tiled tensor map (rank <= 5) of bf16 (or fp32 with `fp32`); strides
+// in bytes for dimensions 1..rank-1
+cudaError_t encode_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                       const uint64_t* strides_bytes, const uint32_t* box, bool swizzle128, bool l2_promote,
+                       bool fp32);
+inline cudaError_t encode_bf16_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                                   const uint64_t* strides_bytes, const uint32_t* box, bool swizzle128,
+                                   bool l2_promote) {
+    return encode_map(map, base, rank, dims, strides_bytes, box, swizzle128, l2_promote, false);
+}
 
 // host: the address of the device status word the asynchronous kernels record
 // SSM_ERR_TIMEOUT in (0 = fine)
