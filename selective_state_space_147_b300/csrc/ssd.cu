@@ -26,11 +26,16 @@
 // the epilogue threads' registers across chunks (its bf16 copy is the next
 // chunk's operand).  Warp 8 streams the C, B and x tiles of a chunk with TMA
 // (128-byte swizzle; rows past the sequence end and states past N read as
-// zero) into a 2-stage ring; warp 9 issues the MMAs -- the next chunk's G
-// while the epilogue warps turn this chunk's G into M -- and eight epilogue
-// warps (warp w: TMEM lanes 32 (w % 4) .. + 31 = chunk rows, half w / 4 of the
-// columns) compute Delta, the in-chunk prefix sums s, M and w o X into shared
-// memory, then the state update and y.  Every mbarrier wait is bounded: on
+// zero) into a 2-stage ring and computes each chunk's Delta and in-chunk prefix
+// sums s ahead of time; warp 9 issues the MMAs -- C H while the epilogue warps
+// build w o X, B^T (w o X) while they turn G into M, the next chunk's G after
+// M X -- and eight epilogue warps (warp w: TMEM lanes 32 (w % 4) .. + 31 = chunk
+// rows, half w / 4 of the columns) compute w o X and M into shared memory
+// (exp per element only in the diagonal 32 x 32 blocks; below them the decay
+// factors into exp(s_i - s_e) exp(s_e - s_j), both exponents <= 0), then the
+// state update and y, which leaves through a swizzled staging tile and bulk
+// tensor stores that warp 10 issues (a thread with bulk stores in flight would
+// stall in its next proxy fence, so the fencing epilogue threads issue none).  Every mbarrier wait is bounded: on
 // expiry the kernel records SSM_ERR_TIMEOUT in the device status word and the
 // CTA leaves after its own copies and MMAs have landed.
 #include <cuda_bf16.h>
@@ -56,22 +61,23 @@ constexpr int kTileX = kAtom;             // an x tile: 128 steps x 64 head-dime
 constexpr int kStage = 2 * kTileBC + kTileX;
 constexpr int kStages = 2;
 constexpr int kEpiWarps = 8;
-constexpr int kThreads = 32 * (kEpiWarps + 2);   // + warp 8: TMA producer, warp 9: MMA issuer
+constexpr int kThreads = 32 * (kEpiWarps + 3);   // + warp 8: TMA producer, warp 9: MMA issuer, warp 10: output stores
 constexpr int kOffM = kStages * kStage;           // M: K-major A operand, two 64-step atoms
 constexpr int kOffWX = kOffM + 2 * kAtom;         // w o x: MN-major B operand
 constexpr int kOffH = kOffWX + kTileX;            // the entering state in bf16: MN-major B operand
 constexpr int kOffAux = kOffH + kTileX;
-// aux: Delta[2][128], s[2][128] (fp32, double-buffered by chunk parity), warp sums [2][4] (+ pad),
-// the column factors of the blocks below M's diagonal [128], barriers
-constexpr int kAuxFloats = 2 * kQ * 2 + 16 + kQ;
-constexpr int kNumBars = 2 + 2 + 2 + 1 + 1 + 1 + 1 + 1;   // full, empty, gfull, wready, mready, yfull, yempty, done
+// aux: Delta[2][128], s[2][128] (fp32, double-buffered by chunk parity), the column factors of
+// the blocks below M's diagonal [128], barriers
+constexpr int kAuxFloats = 2 * kQ * 2 + kQ;
+// full, empty (C and B), fullx, emptyx (x), dready, gfull, wready, mready, yfull, yempty, done, ystaged, yfree
+constexpr int kNumBars = 2 + 2 + 2 + 2 + 2 + 2 + 1 + 1 + 1 + 1 + 1 + 1 + 1;
 constexpr int kSmem = kOffAux + kAuxFloats * 4 + kNumBars * 8 + 16;
 // TMEM columns: G (two buffers), Yd, Yo, S
 constexpr uint32_t kColG = 0, kColYd = 256, kColYo = 320, kColS = 384, kTmemCols = 512;
 
 struct SsdArgs {
     int L, H, heads_per_group, nstate, nbox, nchunks;
-    uint32_t stage_bytes;
+    uint32_t cb_bytes;   // C and B bytes of one stage (64 or 128 states per tile row)
     const __nv_bfloat16* dt;     // (batch, L, H)
     const float* A;              // (H)
     const float* D;              // (H) or NULL
@@ -121,17 +127,21 @@ ssd_chunk_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant_
     }
     float* dl = reinterpret_cast<float*>(smem + kOffAux);   // Delta [2][128]
     float* s2 = dl + 2 * kQ;                                  // s log2(e) [2][128]
-    float* wsum = s2 + 2 * kQ;                                // [2][4]
-    float* cf = wsum + 16;                                    // [128]
-    uint64_t* full = reinterpret_cast<uint64_t*>(cf + kQ);
-    uint64_t* empty = full + 2;
-    uint64_t* gfull = empty + 2;
+    float* cf = s2 + 2 * kQ;                                  // [128]
+    uint64_t* full = reinterpret_cast<uint64_t*>(cf + kQ);   // C and B tiles of stage s landed
+    uint64_t* empty = full + 2;                               // ... and read by the chunk's C H and B^T (w o x)
+    uint64_t* fullx = empty + 2;                              // the x tile of stage s landed
+    uint64_t* emptyx = fullx + 2;                             // ... and read by the chunk's M x
+    uint64_t* dready = emptyx + 2;  // Delta and s of chunk c in buffer c & 1
+    uint64_t* gfull = dready + 2;
     uint64_t* wready = gfull + 2;
     uint64_t* mready = wready + 1;
     uint64_t* yfull = mready + 1;
     uint64_t* yempty = yfull + 1;
     uint64_t* done = yempty + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+    uint64_t* ystaged = done + 1;   // the output tile of a chunk is in its staging buffer
+    uint64_t* yfree = ystaged + 1;  // ... and has been read out by its bulk store
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(yfree + 1);
     int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
     const int unit = blockIdx.x;
@@ -142,6 +152,9 @@ ssd_chunk_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant_
         for (int s = 0; s < 2; s++) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
+            mbar_init(&fullx[s], 1);
+            mbar_init(&emptyx[s], 1);
+            mbar_init(&dready[s], 1);
             mbar_init(&gfull[s], 1);
         }
         mbar_init(wready, kEpiWarps);
@@ -149,6 +162,8 @@ ssd_chunk_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant_
         mbar_init(yfull, 1);
         mbar_init(yempty, kEpiWarps);
         mbar_init(done, 1);
+        mbar_init(ystaged, kEpiWarps);
+        mbar_init(yfree, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -164,27 +179,92 @@ ssd_chunk_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant_
     const uint32_t tmem = *tmem_slot;
 
     if (warp == kEpiWarps) {
-        if (lane == 0) {
-            // producer: the C, B (state boxes of 64) and x tiles of each chunk
-            int issued = 0;
-            for (int c = 0; c < nc; c++) {
-                const int s = c & 1;
+        // producer warp: lane 0 streams each chunk's C, B (state boxes of 64) and x tiles into
+        // stage c & 1; then the warp computes the chunk's Delta and in-chunk prefix sums of
+        // Delta A (log2 units), four consecutive steps per lane, into buffer c & 1.
+        const float Al2 = __ldg(a.A + h) * kLog2e;
+        const float bias = a.dt_bias != nullptr ? __ldg(a.dt_bias + h) : 0.f;
+        // the raw step sizes of a chunk are loaded one chunk ahead (their latency is long
+        // next to the tile traffic, and nothing here waits on them early)
+        auto load_dt = [&](int c, float (&r)[4]) {
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                const int t = c * kQ + 4 * lane + i;
+                r[i] = t < a.L ? __bfloat162float(a.dt[((size_t)b * a.L + t) * a.H + h]) : 0.f;
+            }
+        };
+        int issued = 0;
+        // one chunk: its C and B tiles into stage c & 1 once chunk c - 2's C H and B^T (w o x)
+        // have read them, its x tile once chunk c - 2's M x has, then its Delta and s into
+        // buffer c & 1 from the raw step sizes `cur`, while the next chunk's load into `nxt`.
+        // Buffer c & 1 was last read by chunk c - 2's decay matrix, finished before its M x.
+        auto step = [&](int c, const float (&cur)[4], float (&nxt)[4]) -> bool {
+            const int s = c & 1;
+            int go = 1;
+            if (lane == 0) {
                 if (c >= 2 && !mbar_wait(&empty[s], ((c >> 1) - 1) & 1)) {
                     record_timeout(a.status, abort_flag);
-                    break;
+                    go = 0;
                 }
-                if (*(volatile int*)abort_flag) break;
+                if (go && *(volatile int*)abort_flag) go = 0;
                 unsigned char* st = smem + s * kStage;
-                mbar_expect_tx(&full[s], a.stage_bytes);
-                for (int bx = 0; bx < a.nbox; bx++) {
-                    tma_load_4d(st + bx * kAtom, &tmC, &full[s], 64 * bx, g, c * kQ, b);
-                    tma_load_4d(st + kTileBC + bx * kAtom, &tmB, &full[s], 64 * bx, g, c * kQ, b);
+                if (go) {
+                    mbar_expect_tx(&full[s], a.cb_bytes);
+                    for (int bx = 0; bx < a.nbox; bx++) {
+                        tma_load_4d(st + bx * kAtom, &tmC, &full[s], 64 * bx, g, c * kQ, b);
+                        tma_load_4d(st + kTileBC + bx * kAtom, &tmB, &full[s], 64 * bx, g, c * kQ, b);
+                    }
+                    issued = c + 1;
                 }
-                tma_load_3d(st + 2 * kTileBC, &tmX, &full[s], h * kP, c * kQ, b);
-                issued = c + 1;
+                if (go && c >= 2 && !mbar_wait(&emptyx[s], ((c >> 1) - 1) & 1)) {
+                    record_timeout(a.status, abort_flag);
+                    go = 0;
+                }
+                if (go) {
+                    mbar_expect_tx(&fullx[s], kTileX);
+                    tma_load_3d(st + 2 * kTileBC, &tmX, &fullx[s], h * kP, c * kQ, b);
+                }
             }
+            if (!__shfl_sync(0xffffffffu, go, 0)) return false;
+            if (c + 1 < nc) load_dt(c + 1, nxt);
+            float dv[4], av[4];
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                const int t = c * kQ + 4 * lane + i;
+                dv[i] = 0.f;
+                if (t < a.L) {
+                    const float v = cur[i] + bias;
+                    dv[i] = a.softplus ? softplus_accurate(v) : v;
+                }
+                av[i] = dv[i] * Al2 + (i > 0 ? av[i - 1] : 0.f);
+            }
+            float tot = av[3];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, tot, o);
+                if (lane >= o) tot += y;
+            }
+            const float off = tot - av[3];
+            *reinterpret_cast<float4*>(dl + s * kQ + 4 * lane) = make_float4(dv[0], dv[1], dv[2], dv[3]);
+            *reinterpret_cast<float4*>(s2 + s * kQ + 4 * lane) =
+                make_float4(av[0] + off, av[1] + off, av[2] + off, av[3] + off);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&dready[s]);
+            return true;
+        };
+        // two register sets in turn, so a load is first used a whole chunk after it was issued
+        float r0[4] = {0.f, 0.f, 0.f, 0.f}, r1[4] = {0.f, 0.f, 0.f, 0.f};
+        if (nc > 0) load_dt(0, r0);
+        for (int c = 0; c < nc; c += 2) {
+            if (!step(c, r0, r1)) break;
+            if (c + 1 < nc && !step(c + 1, r1, r0)) break;
+        }
+        if (lane == 0) {
             // copies still in flight must land before the CTA may exit
-            for (int u = (issued > 2 ? issued - 2 : 0); u < issued; u++) mbar_wait(&full[u & 1], (u >> 1) & 1);
+            for (int u = (issued > 2 ? issued - 2 : 0); u < issued; u++) {
+                mbar_wait(&full[u & 1], (u >> 1) & 1);
+                mbar_wait(&fullx[u & 1], (u >> 1) & 1);
+            }
         }
     } else if (warp == kEpiWarps + 1) {
         if (lane == 0) {
@@ -240,21 +320,42 @@ ssd_chunk_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant_
                 for (int k = 0; k < kQ / 16; k++)
                     umma_bf16(tmem + kColS, dBt0 + stage_off(s) + mnmajor_step(k), dWX + mnmajor_step(k), idS,
                               k > 0 ? 1u : 0u);
+                umma_commit(&empty[s]);   // C and B of the stage are free once these have read them
                 // Yd = M x: A = M (K-major, two 64-step atoms), B = x (MN-major rows of 64 columns)
                 if (!(ok = mbar_wait(mready, c & 1))) break;
+                if (!(ok = mbar_wait(&fullx[s], (c >> 1) & 1))) break;
                 fence_after_sync();
 #pragma unroll
                 for (int k = 0; k < kQ / 16; k++)
                     umma_bf16(tmem + kColYd, dM + kmajor_step(k, kAtom), dX0 + stage_off(s) + mnmajor_step(k), idY,
                               k > 0 ? 1u : 0u);
                 umma_commit(yfull);
-                umma_commit(&empty[s]);
+                umma_commit(&emptyx[s]);
                 if (c + 1 < nc && !g_next && !(ok = issue_g(c + 1))) break;
             }
             if (!ok) record_timeout(a.status, abort_flag);
             // every MMA issued must have completed before TMEM is freed
             umma_commit(done);
             mbar_wait(done, 0);
+        }
+    } else if (warp == kEpiWarps + 2) {
+        if (lane == 0) {
+            // output stores: each chunk's staged tile leaves by bulk tensor stores (rows past the
+            // sequence end are not written).  This thread issues no proxy fences, so no other
+            // thread's fence waits for these stores.
+            for (int c = 0; c < nc; c++) {
+                if (!mbar_wait(ystaged, c & 1)) {
+                    record_timeout(a.status, abort_flag);
+                    break;
+                }
+                const unsigned char* Yt = smem + kOffM;
+                tma_store_3d(&tmY, Yt, h * kP, c * kQ, b);
+                if constexpr (sizeof(Tout) == 4) tma_store_3d(&tmY, Yt + kAtom, h * kP + 32, c * kQ, b);
+                asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                mbar_arrive(yfree);
+            }
+            asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
         }
     } else {
         // epilogue warps 0-7: TMEM lane quadrant `quad` (chunk rows / states 32 quad ..), column half `hf`
@@ -281,53 +382,25 @@ ssd_chunk_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant_
         fence_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(yempty);
-        // Delta and the in-chunk prefix sums of Delta A (log2 units) of chunk c into
-        // buffer c & 1, by warps 0-3 (one step each)
-        auto chunk_delta = [&](int c) {
-            if (hf != 0) return;
-            const int t = c * kQ + row;
-            float dv = 0.f;
-            if (t < a.L) {
-                const float v = __bfloat162float(a.dt[((size_t)b * a.L + t) * a.H + h]) + bias;
-                dv = a.softplus ? softplus_accurate(v) : v;
-            }
-            float av = dv * Al2;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float y = __shfl_up_sync(0xffffffffu, av, o);
-                if (lane >= o) av += y;
-            }
-            float* wsb = wsum + (c & 1) * 4;
-            if (lane == 31) wsb[quad] = av;
-            asm volatile("bar.sync 2, 128;" ::: "memory");
-            float off = 0.f;
-            for (int q = 0; q < quad; q++) off += wsb[q];
-            dl[(c & 1) * kQ + row] = dv;
-            s2[(c & 1) * kQ + row] = av + off;
-        };
-        if (nc > 0) chunk_delta(0);
-        asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
         for (int c = 0; c < nc; c++) {
             const int buf = c & 1;
             const int t0 = c * kQ;
             float* dlb = dl + buf * kQ;
             float* s2b = s2 + buf * kQ;
+            // (a wait that runs out is caught by the uniform check before M is built)
+            if (!mbar_wait(&dready[buf], (c >> 1) & 1)) record_timeout(a.status, abort_flag);
             const float si = s2b[row];
             const float slast = s2b[kQ - 1];
             // ---- column factors of the blocks below M's diagonal: cf_j = exp(s_e - s_j) Delta_j with
             // e the last step of j's 32-step block, so that for i in a later block
             // exp(s_i - s_j) Delta_j = exp(s_i - s_e) cf_j with both exponents <= 0
+            // (read only while M is built, after the barrier in the check below)
             if (hf == 0) cf[row] = ex2_approx(s2b[32 * quad + 31] - si) * dlb[row];
-            // bf16: the previous chunk's output store must have read its staging rows (w o x's buffer)
-            if constexpr (sizeof(Tout) == 2) {
-                if (tid == 0 && c > 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-            }
-            asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
             // ---- w o x, row j = `row`, columns 32 hf .. + 31, w_j = exp(s_last - s_j) Delta_j;
             // the same x values stay in registers for this thread's D x term
             uint32_t xw[16];
             {
-                if (!mbar_wait(&full[buf], (c >> 1) & 1)) record_timeout(a.status, abort_flag);
+                if (!mbar_wait(&fullx[buf], (c >> 1) & 1)) record_timeout(a.status, abort_flag);
                 const unsigned char* Xt = smem + buf * kStage + 2 * kTileBC;
                 const float wj = ex2_approx(slast - si) * dlb[row];
 #pragma unroll
@@ -347,7 +420,9 @@ ssd_chunk_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant_
             __syncwarp();
             if (lane == 0) mbar_arrive(wready);
             // ---- M row `row`, 32-step column blocks cb = 2 hf, 2 hf + 1 (K atom hf of the A operand)
-            const bool gw = mbar_wait(&gfull[buf], (c >> 1) & 1);
+            // G of this chunk, and the previous chunk's output read out of M's buffer
+            bool gw = mbar_wait(&gfull[buf], (c >> 1) & 1);
+            if (c > 0) gw = gw && mbar_wait(yfree, (c - 1) & 1);
             if (!gw) record_timeout(a.status, abort_flag);
             if (!epi_all(gw && *(volatile int*)abort_flag == 0)) break;
             fence_after_sync();
@@ -396,9 +471,6 @@ ssd_chunk_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant_
             fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(mready);
-            // the next chunk's Delta and prefix sums while this chunk's products run
-            // (buffer (c + 1) & 1 was last read before the barrier that ended chunk c - 1)
-            if (c + 1 < nc) chunk_delta(c + 1);
             // ---- wait for Yd, S, Yo of this chunk
             const bool yw = mbar_wait(yfull, c & 1);
             if (!yw) record_timeout(a.status, abort_flag);
@@ -441,10 +513,10 @@ ssd_chunk_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant_
             __syncwarp();
             if (lane == 0) mbar_arrive(yempty);
             // stage the 128 x 64 output tile (128-byte swizzled rows; fp32: two 32-column boxes)
-            // where this chunk's M (fp32) or w o x (bf16) was -- both consumed by now -- and
-            // write it with bulk tensor stores (rows past the sequence end are not written)
+            // where this chunk's M was -- consumed by now -- and write it with bulk tensor
+            // stores (rows past the sequence end are not written)
             {
-                unsigned char* Yt = sizeof(Tout) == 2 ? WXt : Mt;
+                unsigned char* Yt = Mt;
                 if constexpr (sizeof(Tout) == 2) {
 #pragma unroll
                     for (int q = 0; q < 4; q++) {
@@ -460,23 +532,10 @@ ssd_chunk_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant_
                             make_float4(y[4 * q], y[4 * q + 1], y[4 * q + 2], y[4 * q + 3]);
                 }
                 fence_async_smem();
-                asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
-                if (tid == 0) {
-                    if constexpr (sizeof(Tout) == 2) {
-                        tma_store_3d(&tmY, Yt, h * kP, t0, b);
-                    } else {
-                        tma_store_3d(&tmY, Yt, h * kP, t0, b);
-                        tma_store_3d(&tmY, Yt + kAtom, h * kP + 32, t0, b);
-                    }
-                    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-                    // fp32 staging sits in M's place, which the next chunk rewrites first
-                    if constexpr (sizeof(Tout) != 2) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(ystaged);
             }
-            // the next chunk's Delta and prefix sums are visible; every thread is done with this chunk's
-            asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
         }
-        if (tid == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
         if (a.final_state != nullptr && row < a.nstate && *(volatile int*)abort_flag == 0) {
 #pragma unroll
             for (int q = 0; q < 8; q++)
@@ -547,7 +606,7 @@ cudaError_t launch_ssd_fwd(const ssm_ssd_fwd_params* p, cudaStream_t st) {
     a.nstate = (int)p->dstate;
     a.nbox = p->dstate > 64 ? 2 : 1;
     a.nchunks = (int)ceil_div(p->seqlen, (int64_t)kQ);
-    a.stage_bytes = (uint32_t)(2 * a.nbox * kAtom + kTileX);
+    a.cb_bytes = (uint32_t)(2 * a.nbox * kAtom);
     a.dt = static_cast<const __nv_bfloat16*>(p->dt);
     a.A = p->A;
     a.D = p->D;
