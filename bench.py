@@ -51,7 +51,7 @@ SSD = dict(batch=8, seqlen=2048, nheads=80, headdim=64, dstate=128, ngroups=1, c
 # after any change to them the traffic is reported as null until it is captured again.
 TRAFFIC_PER_CT = {"ssm_scan_bwd": 37.89, "ssm_scan_fwd": 23.16, "causal_conv1d_silu": 3.19,
                   "causal_conv1d_silu_bwd": 5.51, "ssm_scan_fwd_plain": 7.68}
-TRAFFIC_SOURCES_SHA = "e37dc15cb6b39c22"
+TRAFFIC_SOURCES_SHA = "c11cca8e46c6cafc"
 
 SM_FP32_LANES = 128     # FP32 lanes per SM per clock (sm_100 family), nominal
 SM_SFU_EX2 = 32         # MUFU ex2 results per SM per clock, nominal
