@@ -13,13 +13,17 @@
 //
 // Kernel: persistent, one CTA per SM walking 128 x 128 output tiles.  A TMA
 // producer thread streams 64-wide K slices of W (K-major) and X (token-major
-// rows, the "MN-major" operand) into a 4-stage shared-memory ring with 128-byte
+// rows, the "MN-major" operand) into a 6-stage shared-memory ring with 128-byte
 // swizzle; one thread issues tcgen05.mma (bf16 x bf16 -> fp32, M 128, N 128,
 // K 16 per instruction) into one of two TMEM accumulators and releases each
 // stage with tcgen05.commit; eight epilogue warps drain the other accumulator
 // (warp w owns TMEM lanes 32 (w % 4) .. + 31, i.e. output rows, and half of
-// the tokens) into a swizzled bf16 tile in shared memory that one thread
-// writes out with bulk tensor stores, while the next tile accumulates.  Every wait
+// the tokens) into a swizzled bf16 staging tile in shared memory that a store
+// warp writes out with bulk tensor stores, while the next tile accumulates.
+// The loads are latency bound (about 1.4 us per stage round trip out of L2),
+// so the ring gets the shared memory: six 32 KB stages and one staging tile.  (A
+// thread with bulk stores in flight stalls in its next proxy fence, so the
+// fencing epilogue threads issue none.)  Every wait
 // on an mbarrier is bounded: on expiry the kernel records SSM_ERR_TIMEOUT in
 // the device status word (ssm_device_status), drains its outstanding copies
 // with bounded waits, frees its TMEM and returns.
@@ -36,14 +40,14 @@ namespace ssm {
 constexpr int kPM = 128;                       // output rows per tile (MMA M)
 constexpr int kPN = 128;                       // tokens per tile (MMA N)
 constexpr int kPK = 64;                        // K per stage: one 128-byte swizzle row of bf16
-constexpr int kPStages = 4;
+constexpr int kPStages = 6;
 constexpr int kPEpiWarps = 8;                  // warps 0-7: epilogue (warp w: TMEM lane quadrant w % 4, column half w / 4)
-constexpr int kPThreads = 32 * (kPEpiWarps + 2);   // + warp 8: TMA producer, warp 9: MMA issuer
+constexpr int kPThreads = 32 * (kPEpiWarps + 3);   // + warp 8: TMA producer, warp 9: MMA issuer, warp 10: stores
 constexpr int kPTileA = kPM * kPK * 2;         // 16 KB
 constexpr int kPTileB = kPK * kPN * 2;         // 16 KB: two 64-token boxes of 8 KB
 constexpr int kPStage = kPTileA + kPTileB;
 constexpr int kPTileOut = kPM * kPN * 2;       // 32 KB: the bf16 output tile, two 64-token boxes
-constexpr int kPSmem = 1024 + kPStages * kPStage + 2 * kPTileOut + 256;   // slack, ring, staging, barriers
+constexpr int kPSmem = 1024 + kPStages * kPStage + kPTileOut + 256;   // slack, ring, staging, barriers
 constexpr uint32_t kPTmemCols = 2 * kPN;       // two fp32 accumulators (one column per token)
 constexpr uint32_t kProjIdesc = tc::idesc_bf16(kPM, kPN, false, true);   // A (W) K-major, B (X) MN-major
 
@@ -85,19 +89,21 @@ __device__ __forceinline__ void record_timeout(int* abort_flag) {
 }
 
 // Persistent: every CTA (one per SM) walks tiles blockIdx.x, blockIdx.x + gridDim.x, ...
-// The producer and the MMA issuer run ahead through a 4-stage shared-memory ring; two
+// The producer and the MMA issuer run ahead through a 6-stage shared-memory ring; two
 // TMEM accumulators let the epilogue warps drain tile i while tile i + 1 accumulates.
 __global__ void __launch_bounds__(kPThreads, 1)
 proj_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                  const __grid_constant__ CUtensorMap tmO, const ProjArgs a) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    unsigned char* stage_out = base + kPStages * kPStage;                 // 2 x kPTileOut
-    uint64_t* full = reinterpret_cast<uint64_t*>(stage_out + 2 * kPTileOut);
+    unsigned char* stage_out = base + kPStages * kPStage;                 // kPTileOut
+    uint64_t* full = reinterpret_cast<uint64_t*>(stage_out + kPTileOut);
     uint64_t* empty = full + kPStages;
     uint64_t* tfull = empty + kPStages;      // accumulator a ready for the epilogue
     uint64_t* tempty = tfull + 2;            // accumulator a drained by the epilogue
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+    uint64_t* ostaged = tempty + 2;          // output staging buffer s written
+    uint64_t* ofree = ostaged + 2;           // ... and read out by its bulk store
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ofree + 2);
     int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nk = (int)((a.k + kPK - 1) / kPK);
@@ -110,6 +116,8 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
         for (int q = 0; q < 2; q++) {
             mbar_init(&tfull[q], 1);
             mbar_init(&tempty[q], kPEpiWarps);   // one arrival per epilogue warp
+            mbar_init(&ostaged[q], kPEpiWarps);
+            mbar_init(&ofree[q], 1);
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -189,6 +197,28 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
                 umma_commit(&tfull[acc]);
             }
         }
+    } else if (warp == kPEpiWarps + 2) {
+        if (lane == 0) {
+            // stores: each staged tile leaves by two bulk tensor stores; this thread issues no
+            // proxy fences, so no fence elsewhere waits for the stores in flight
+            int local = 0;
+            for (int tile = blockIdx.x; tile < a.tiles; tile += gridDim.x, local++) {
+                const int sb = 0;
+                if (!mbar_wait(&ostaged[sb], local & 1)) {
+                    record_timeout(abort_flag);
+                    break;
+                }
+                int m0, n0, bz;
+                tile_coords(a, tile, m0, n0, bz);
+                unsigned char* so = stage_out + sb * kPTileOut;
+                tma_store_3d(&tmO, so, n0, m0, bz);
+                tma_store_3d(&tmO, so + kPTileOut / 2, n0 + 64, m0, bz);
+                asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                mbar_arrive(&ofree[sb]);
+            }
+            asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+        }
     } else {
         // epilogue: warp w reads TMEM lanes (output rows) 32 (w % 4) .. + 31, tokens
         // 64 (w / 4) .. + 63 of the tile
@@ -226,11 +256,12 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             __syncwarp();
             if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&tempty[acc])) : "memory");
-            // stage the tile (128-byte swizzled rows, two 64-token boxes) for one bulk store;
+            // stage the tile (128-byte swizzled rows, two 64-token boxes) for the store warp;
             // the staging buffer used two tiles ago must have been read out first
-            unsigned char* so = stage_out + (local & 1) * kPTileOut;
-            if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-            asm volatile("bar.sync 1, %0;" ::"n"(32 * kPEpiWarps) : "memory");
+            unsigned char* so = stage_out;
+            const bool freed = local < 1 || mbar_wait(&ofree[0], (local - 1) & 1);
+            if (!freed) record_timeout(abort_flag);
+            if (!epi_all(freed && *(volatile int*)abort_flag == 0)) break;
             const int rt = quad * 32 + lane;   // row within the tile
 #pragma unroll
             for (int c = 0; c < 2; c++) {
@@ -243,14 +274,9 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
                 }
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            asm volatile("bar.sync 1, %0;" ::"n"(32 * kPEpiWarps) : "memory");
-            if (tid == 0) {
-                tma_store_3d(&tmO, so, n0, m0, bz);
-                tma_store_3d(&tmO, so + kPTileOut / 2, n0 + 64, m0, bz);
-                asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ostaged[0]);
         }
-        if (tid == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
