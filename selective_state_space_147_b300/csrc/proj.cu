@@ -101,7 +101,7 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
     uint64_t* empty = full + kPStages;
     uint64_t* tfull = empty + kPStages;      // accumulator a ready for the epilogue
     uint64_t* tempty = tfull + 2;            // accumulator a drained by the epilogue
-    uint64_t* ostaged = tempty + 2;          // output staging buffer s written
+    uint64_t* ostaged = tempty + 2;          // the staging tile written (one buffer: [0] only)
     uint64_t* ofree = ostaged + 2;           // ... and read out by its bulk store
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ofree + 2);
     int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
@@ -257,7 +257,7 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
             __syncwarp();
             if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&tempty[acc])) : "memory");
             // stage the tile (128-byte swizzled rows, two 64-token boxes) for the store warp;
-            // the staging buffer used two tiles ago must have been read out first
+            // the staging tile must have been read out by the previous tile's store
             unsigned char* so = stage_out;
             const bool freed = local < 1 || mbar_wait(&ofree[0], (local - 1) & 1);
             if (!freed) record_timeout(abort_flag);
