@@ -141,18 +141,22 @@ def test_ssd_is_deterministic():
 
 def test_ssd_full_size_sampled_heads():
     """Mamba-2-2.7B-shaped layer (batch 8, L 2048, 80 heads of 64, N 128), bf16
-    output as the benchmark times it; the oracle recomputes sampled (b, h) pairs."""
+    output as the benchmark times it, with an initial and a final state; the
+    oracle recomputes 24 sampled (b, h) pairs (every batch row, spread heads)."""
     Lb = _lib()
     b, L, H, N = 8, 2048, 80, 128
-    g = S.ssd_inputs(S.config_seed(6), b, L, H, 64, N, 1, device="cuda")
-    y = Lb.ssm_ssd_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], D=g["D"], dt_bias=g["dt_bias"])
+    g = S.ssd_inputs(S.config_seed(6), b, L, H, 64, N, 1, device="cuda", with_h0=True)
+    y, hN = Lb.ssm_ssd_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], D=g["D"], dt_bias=g["dt_bias"], h0=g["h0"],
+                           return_final_state=True)
     torch.cuda.synchronize()
     rng = np.random.default_rng(3)
-    for unit in sorted(rng.choice(b * H, size=3, replace=False).tolist()):
-        bb, hh = divmod(unit, H)
+    units = sorted(set((bb, int(hh)) for bb in range(b) for hh in rng.choice(H, size=3, replace=False)))
+    for bb, hh in units:
         one = dict(x=g["x"][bb:bb + 1, :, hh:hh + 1].cpu(), dt=g["dt"][bb:bb + 1, :, hh:hh + 1].cpu(),
                    B=g["B"][bb:bb + 1].cpu(), C=g["C"][bb:bb + 1].cpu(), A=g["A"][hh:hh + 1].cpu(),
-                   D=g["D"][hh:hh + 1].cpu(), dt_bias=g["dt_bias"][hh:hh + 1].cpu(), h0=None)
-        ref, _ = _run_oracle(one, threads=1)
-        yabs, _ = _run_oracle_abs(one, threads=1)
-        assert_ssd_close(y[bb:bb + 1, :, hh:hh + 1], ref, yabs, torch.bfloat16, what=f"unit {unit}")
+                   D=g["D"][hh:hh + 1].cpu(), dt_bias=g["dt_bias"][hh:hh + 1].cpu(),
+                   h0=g["h0"][bb:bb + 1, hh:hh + 1].cpu())
+        ref, href = _run_oracle(one, threads=1)
+        yabs, habs = _run_oracle_abs(one, threads=1)
+        assert_ssd_close(y[bb:bb + 1, :, hh:hh + 1], ref, yabs, torch.bfloat16, what=f"unit ({bb}, {hh})")
+        assert_state_close(hN[bb:bb + 1, hh:hh + 1], href, habs, what=f"final state ({bb}, {hh})")
