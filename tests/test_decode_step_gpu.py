@@ -31,7 +31,8 @@ def _inputs(seed, batch, dim, N, W, dtype):
                 cb=S.normal(seed, S.STREAM["u"], (dim,), torch.float32, std=0.1))
 
 
-def _run(g, zoh=True, use_z=True, use_cb=True, use_D=True, use_bias=True, want_xc=True, x=None, strided=False):
+def _run(g, zoh=True, use_z=True, use_cb=True, use_D=True, use_bias=True, want_xc=True, x=None, strided=False,
+         out_dtype=torch.float32):
     L = _lib()
     dev = {k: v.cuda() for k, v in g.items()}
     st, cs = dev["state"].clone(), dev["conv_state"].clone()
@@ -47,7 +48,7 @@ def _run(g, zoh=True, use_z=True, use_cb=True, use_D=True, use_bias=True, want_x
     out = L.ssm_decode_step(st, cs, xin, dt, dev["A"], dev["B"], dev["C"], dev["w"],
                             conv_bias=dev["cb"] if use_cb else None, D=dev["D"] if use_D else None,
                             delta_bias=dev["bias"] if use_bias else None, z=z if use_z else None,
-                            bbar_mode=L.SSM_BBAR_ZOH if zoh else L.SSM_BBAR_SIMPLE, out_dtype=torch.float32,
+                            bbar_mode=L.SSM_BBAR_ZOH if zoh else L.SSM_BBAR_SIMPLE, out_dtype=out_dtype,
                             xc_out=xc)
     ref, sref, csref, xcref = oracle.decode_step(g["state"], g["conv_state"], g["x"], g["dt"], g["A"], g["B"],
                                                  g["C"], g["w"], g["cb"] if use_cb else None,
@@ -57,7 +58,7 @@ def _run(g, zoh=True, use_z=True, use_cb=True, use_D=True, use_bias=True, want_x
 
 
 def _check(got, ref, dtype):
-    assert_close(got["out"], ref["out"], dtype, what="out")
+    assert_close(got["out"], ref["out"], dtype, got["out"].dtype, what="out")
     assert_close(got["st"], ref["st"], dtype, what="state")
     assert np.array_equal(to_np(got["cs"]), ref["cs"]), "conv window must hold the token bits exactly"
     if got["xc"] is not None:
@@ -65,10 +66,18 @@ def _check(got, ref, dtype):
 
 
 @pytest.mark.parametrize("zoh", [True, False])
-@pytest.mark.parametrize("dim", [64, 70, 1])
+@pytest.mark.parametrize("dim", [64, 70, 1, 256, 768])
 def test_fast_path(zoh, dim):
     g = _inputs(61, 3, dim, 16, 4, torch.bfloat16)
     got, ref = _run(g, zoh=zoh)
+    _check(got, ref, torch.bfloat16)
+
+
+@pytest.mark.parametrize("zoh", [True, False])
+def test_bf16_output(zoh):
+    """The fast kernel writing a bf16 output (the decode benchmark's form)."""
+    g = _inputs(65, 2, 512, 16, 4, torch.bfloat16)
+    got, ref = _run(g, zoh=zoh, out_dtype=torch.bfloat16)
     _check(got, ref, torch.bfloat16)
 
 
