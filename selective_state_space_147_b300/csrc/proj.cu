@@ -11,17 +11,19 @@
 // [R, R+N) and [R+N, R+2N) are B and C as (batch, N, L) views, its first R
 // rows are dt_proj's input, and dt_proj writes delta as (batch, D, L).
 //
-// Kernel: persistent, one CTA per SM walking 128 x 128 output tiles.  A TMA
-// producer thread streams 64-wide K slices of W (K-major) and X (token-major
-// rows, the "MN-major" operand) into a 6-stage shared-memory ring with 128-byte
-// swizzle; one thread issues tcgen05.mma (bf16 x bf16 -> fp32, M 128, N 128,
-// K 16 per instruction) into one of two TMEM accumulators and releases each
-// stage with tcgen05.commit; eight epilogue warps drain the other accumulator
-// (warp w owns TMEM lanes 32 (w % 4) .. + 31, i.e. output rows, and half of
-// the tokens) into a swizzled bf16 staging tile in shared memory that a store
-// warp writes out with bulk tensor stores, while the next tile accumulates.
-// The loads are latency bound (about 1.4 us per stage round trip out of L2),
-// so the ring gets the shared memory: six 32 KB stages and one staging tile.  (A
+// Kernel: persistent, one CTA per SM walking 128 x 256 output tiles (128 rows
+// of W, 256 tokens).  A TMA producer thread streams 64-wide K slices of W
+// (K-major) and X (token-major rows, the "MN-major" operand, four 64-token
+// boxes) into a 4-stage shared-memory ring of 48 KB stages with 128-byte
+// swizzle; one thread issues tcgen05.mma (bf16 x bf16 -> fp32, M 128, N 256,
+// K 16 per instruction) into one of two 256-column TMEM accumulators and
+// releases each stage with tcgen05.commit; eight epilogue warps drain the other
+// accumulator (warp w owns TMEM lanes 32 (w % 4) .. + 31, i.e. output rows,
+// and 64 tokens of each half of the tile) into a swizzled bf16 staging tile of
+// half the tile that a store warp writes out with bulk tensor stores, twice per
+// tile, while the next tile accumulates.  The loads are latency bound (about
+// 1.4 us per stage round trip out of L2): a 256-token tile reads W once for
+// twice the outputs of a 128-token one, a quarter less traffic per output.  (A
 // thread with bulk stores in flight stalls in its next proxy fence, so the
 // fencing epilogue threads issue none.)  Every wait
 // on an mbarrier is bounded: on expiry the kernel records SSM_ERR_TIMEOUT in
@@ -38,15 +40,16 @@
 namespace ssm {
 
 constexpr int kPM = 128;                       // output rows per tile (MMA M)
-constexpr int kPN = 128;                       // tokens per tile (MMA N)
+constexpr int kPN = 256;                       // tokens per tile (MMA N)
 constexpr int kPK = 64;                        // K per stage: one 128-byte swizzle row of bf16
-constexpr int kPStages = 6;
+constexpr int kPStages = 4;
 constexpr int kPEpiWarps = 8;                  // warps 0-7: epilogue (warp w: TMEM lane quadrant w % 4, column half w / 4)
 constexpr int kPThreads = 32 * (kPEpiWarps + 3);   // + warp 8: TMA producer, warp 9: MMA issuer, warp 10: stores
 constexpr int kPTileA = kPM * kPK * 2;         // 16 KB
-constexpr int kPTileB = kPK * kPN * 2;         // 16 KB: two 64-token boxes of 8 KB
+constexpr int kPBox = kPK * 64 * 2;           // 8 KB: one 64-token box of X (64 K rows of 128 bytes)
+constexpr int kPTileB = kPK * kPN * 2;         // 32 KB: four 64-token boxes
 constexpr int kPStage = kPTileA + kPTileB;
-constexpr int kPTileOut = kPM * kPN * 2;       // 32 KB: the bf16 output tile, two 64-token boxes
+constexpr int kPTileOut = kPM * (kPN / 2) * 2; // 32 KB: half the bf16 output tile, two 64-token boxes
 constexpr int kPSmem = 1024 + kPStages * kPStage + kPTileOut + 256;   // slack, ring, staging, barriers
 constexpr uint32_t kPTmemCols = 2 * kPN;       // two fp32 accumulators (one column per token)
 constexpr uint32_t kProjIdesc = tc::idesc_bf16(kPM, kPN, false, true);   // A (W) K-major, B (X) MN-major
@@ -101,8 +104,8 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
     uint64_t* empty = full + kPStages;
     uint64_t* tfull = empty + kPStages;      // accumulator a ready for the epilogue
     uint64_t* tempty = tfull + 2;            // accumulator a drained by the epilogue
-    uint64_t* ostaged = tempty + 2;          // the staging tile written (one buffer: [0] only)
-    uint64_t* ofree = ostaged + 2;           // ... and read out by its bulk store
+    uint64_t* ostaged = tempty + 2;          // the staging tile written (one buffer, [0] only; twice per tile)
+    uint64_t* ofree = ostaged + 2;           // ... and read out by its bulk stores
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ofree + 2);
     int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -135,7 +138,7 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
 
     if (warp == kPEpiWarps) {
         if (lane == 0) {
-            // producer: K slices of W (rows m0..m0+127) and of X[b] (tokens n0..n0+127)
+            // producer: K slices of W (rows m0..m0+127) and of X[b] (tokens n0..n0+255)
             int it = 0;   // stage uses so far
             for (int tile = blockIdx.x; tile < a.tiles && !*(volatile int*)abort_flag; tile += gridDim.x) {
                 int m0, n0, bz;
@@ -149,8 +152,9 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
                     unsigned char* st = base + s * kPStage;
                     mbar_expect_tx(&full[s], kPStage);
                     tma_load_2d(st, &tmW, &full[s], kb * kPK, m0);
-                    tma_load_3d(st + kPTileA, &tmX, &full[s], n0, kb * kPK, bz);
-                    tma_load_3d(st + kPTileA + kPTileB / 2, &tmX, &full[s], n0 + 64, kb * kPK, bz);
+#pragma unroll
+                    for (int j = 0; j < kPN / 64; j++)
+                        tma_load_3d(st + kPTileA + j * kPBox, &tmX, &full[s], n0 + 64 * j, kb * kPK, bz);
                 }
             }
             // copies still in flight must land before the CTA may exit
@@ -160,7 +164,7 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
         if (lane == 0) {
             // MMA issuer; descriptors of stage 0 built once (stage s is s * kPStage bytes further)
             const uint64_t dA0 = sw128_desc(smem_addr(base), 16, 1024);
-            const uint64_t dB0 = sw128_desc(smem_addr(base + kPTileA), kPTileB / 2, 1024);
+            const uint64_t dB0 = sw128_desc(smem_addr(base + kPTileA), kPBox, 1024);
             int it = 0, local = 0;
             for (int tile = blockIdx.x; tile < a.tiles; tile += gridDim.x, local++) {
                 if (*(volatile int*)abort_flag) break;
@@ -185,7 +189,7 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
                         // A: K-major rows of 128 bytes, 8-row groups 1024 bytes apart; the
                         // K step of 16 elements is 32 bytes along the swizzled row.
                         // B: token-major rows of 128 bytes (64 tokens), 8-row groups of K
-                        // 1024 bytes apart, the second 64 tokens 8 KB further; the K step
+                        // 1024 bytes apart, each next 64 tokens 8 KB further; the K step
                         // of 16 rows is 2 KB.
                         const uint64_t so = (uint64_t)(s * (kPStage >> 4));
                         umma_bf16(dcol, dA0 + so + kmajor_step(k, 0), dB0 + so + mnmajor_step(k), kProjIdesc,
@@ -199,30 +203,33 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
         }
     } else if (warp == kPEpiWarps + 2) {
         if (lane == 0) {
-            // stores: each staged tile leaves by two bulk tensor stores; this thread issues no
-            // proxy fences, so no fence elsewhere waits for the stores in flight
-            int local = 0;
-            for (int tile = blockIdx.x; tile < a.tiles; tile += gridDim.x, local++) {
-                const int sb = 0;
-                if (!mbar_wait(&ostaged[sb], local & 1)) {
-                    record_timeout(abort_flag);
-                    break;
-                }
+            // stores: each staged half tile leaves by two bulk tensor stores; this thread issues
+            // no proxy fences, so no fence elsewhere waits for the stores in flight
+            int use = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < a.tiles && ok; tile += gridDim.x) {
                 int m0, n0, bz;
                 tile_coords(a, tile, m0, n0, bz);
-                unsigned char* so = stage_out + sb * kPTileOut;
-                tma_store_3d(&tmO, so, n0, m0, bz);
-                tma_store_3d(&tmO, so + kPTileOut / 2, n0 + 64, m0, bz);
-                asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-                asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-                mbar_arrive(&ofree[sb]);
+                for (int hs = 0; hs < 2; hs++, use++) {
+                    if (!mbar_wait(&ostaged[0], use & 1)) {
+                        record_timeout(abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    tma_store_3d(&tmO, stage_out, n0 + 128 * hs, m0, bz);
+                    tma_store_3d(&tmO, stage_out + kPTileOut / 2, n0 + 128 * hs + 64, m0, bz);
+                    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                    mbar_arrive(&ofree[0]);
+                }
             }
             asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
         }
     } else {
-        // epilogue: warp w reads TMEM lanes (output rows) 32 (w % 4) .. + 31, tokens
-        // 64 (w / 4) .. + 63 of the tile
+        // epilogue: warp w reads TMEM lanes (output rows) 32 (w % 4) .. + 31 and, of each
+        // 128-token half of the tile, tokens 64 (w / 4) .. + 63
         const int quad = warp & 3, half = warp >> 2;
+        int use = 0;   // staging-tile uses so far (two per tile)
         int local = 0;
         for (int tile = blockIdx.x; tile < a.tiles; tile += gridDim.x, local++) {
             const int acc = local & 1;
@@ -236,11 +243,13 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
             tile_coords(a, tile, m0, n0, bz);
             const int row = m0 + quad * 32 + lane;
             const float bias = (a.bias != nullptr && row < a.m) ? __ldg(a.bias + row) : 0.f;
-            uint32_t w[2][16];
+            // w[2 hs + c]: half tile hs, 32-token chunk c of this warp's 64
+            uint32_t w[4][16];
 #pragma unroll
-            for (int c = 0; c < 2; c++) {
+            for (int c = 0; c < 4; c++) {
                 uint32_t r[32];
-                tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * kPN + (2 * half + c) * 32), r);
+                const int col = 128 * (c >> 1) + 64 * half + 32 * (c & 1);
+                tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * kPN + col), r);
 #pragma unroll
                 for (int i = 0; i < 16; i++) {
                     float v0 = __uint_as_float(r[2 * i]) + bias, v1 = __uint_as_float(r[2 * i + 1]) + bias;
@@ -256,26 +265,33 @@ proj_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant_
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             __syncwarp();
             if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&tempty[acc])) : "memory");
-            // stage the tile (128-byte swizzled rows, two 64-token boxes) for the store warp;
-            // the staging tile must have been read out by the previous tile's store
-            unsigned char* so = stage_out;
-            const bool freed = local < 1 || mbar_wait(&ofree[0], (local - 1) & 1);
-            if (!freed) record_timeout(abort_flag);
-            if (!epi_all(freed && *(volatile int*)abort_flag == 0)) break;
+            // stage each half of the tile (128-byte swizzled rows, two 64-token boxes) for the
+            // store warp; the staging tile must have been read out by its previous store
             const int rt = quad * 32 + lane;   // row within the tile
+            bool live = true;
 #pragma unroll
-            for (int c = 0; c < 2; c++) {
-#pragma unroll
-                for (int q = 0; q < 4; q++) {
-                    const int col = 32 * (2 * half + c) + 8 * q;   // first token of this 16-byte chunk
-                    const int box = col >> 6, ch = (col & 63) >> 3;
-                    *reinterpret_cast<uint4*>(so + box * (kPTileOut / 2) + rt * 128 + ((ch ^ (rt & 7)) << 4)) =
-                        make_uint4(w[c][4 * q], w[c][4 * q + 1], w[c][4 * q + 2], w[c][4 * q + 3]);
+            for (int hs = 0; hs < 2; hs++, use++) {
+                const bool freed = use < 1 || mbar_wait(&ofree[0], (use - 1) & 1);
+                if (!freed) record_timeout(abort_flag);
+                if (!epi_all(freed && *(volatile int*)abort_flag == 0)) {
+                    live = false;
+                    break;
                 }
+#pragma unroll
+                for (int c = 0; c < 2; c++) {
+#pragma unroll
+                    for (int q = 0; q < 4; q++) {
+                        const int ch = 4 * c + q;   // 16-byte chunk of this warp's 64-token box
+                        *reinterpret_cast<uint4*>(stage_out + half * (kPTileOut / 2) + rt * 128 + ((ch ^ (rt & 7)) << 4)) =
+                            make_uint4(w[2 * hs + c][4 * q], w[2 * hs + c][4 * q + 1], w[2 * hs + c][4 * q + 2],
+                                       w[2 * hs + c][4 * q + 3]);
+                    }
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ostaged[0]);
             }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ostaged[0]);
+            if (!live) break;
         }
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
