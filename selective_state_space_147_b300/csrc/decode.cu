@@ -221,9 +221,13 @@ __global__ void __launch_bounds__(256) decode_step_kernel(const DecStepArgs a) {
 // lanes compute the channel's conv output from its 8-byte window (one
 // broadcast load) and the first lane writes back the shifted window, the
 // output and, when asked for, the conv output.  Every load is issued before
-// any arithmetic.
+// any arithmetic.  Launched as a programmatic dependent of the previous kernel
+// in the stream: its CTAs are placed while that kernel's last wave runs and
+// wait (griddepcontrol.wait) for it to finish before reading anything, so the
+// launch gap between consecutive layers' kernels is hidden.
 template <typename Tout, bool ZOH>
 __global__ void __launch_bounds__(256) decode_step16_kernel(const DecStepArgs a) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int item = blockIdx.x * blockDim.x + threadIdx.x;      // 2 d + g
     const int64_t b = blockIdx.y;
     const bool active = item < 2 * a.dim;
@@ -232,6 +236,7 @@ __global__ void __launch_bounds__(256) decode_step16_kernel(const DecStepArgs a)
     const int64_t chan = b * a.dim + d;
     float4* st = reinterpret_cast<float4*>(a.state + chan * 16 + g * 8);
     uint2* wp = reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.cstate) + chan * 4);
+    asm volatile("griddepcontrol.wait;" ::: "memory");          // the kernels before have finished
     const float4 s0 = __ldcs(st), s1 = __ldcs(st + 1);
     const uint2 w4 = __ldcs(wp);                                  // [s0 s1 | s2 s3]
     const float4 a0 = __ldg(reinterpret_cast<const float4*>(a.A + d * 16 + g * 8));
@@ -282,6 +287,22 @@ __global__ void __launch_bounds__(256) decode_step16_kernel(const DecStepArgs a)
     }
 }
 
+// launch as a programmatic dependent of the stream's previous kernel
+template <typename Kern>
+static cudaError_t launch_dependent(Kern kern, dim3 grid, cudaStream_t st, const DecStepArgs& a) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
 template <typename Tin, typename Tout>
 static void launch_step_typed(const DecStepArgs& a, bool zoh, unsigned blocks, cudaStream_t st) {
     constexpr bool ACC = sizeof(Tin) == 4;
@@ -309,13 +330,14 @@ cudaError_t launch_decode_step(const ssm_decode_step_params* p, cudaStream_t st)
                         ((uintptr_t)p->conv_state % 8 == 0) && ((uintptr_t)p->conv_weight % 16 == 0);
     if (fast16) {
         const dim3 blocks2((unsigned)ceil_div(p->dim * 2, 256), (unsigned)p->batch);
-        if (p->out_dtype == SSM_BF16) {
-            if (zoh) decode_step16_kernel<__nv_bfloat16, true><<<blocks2, 256, 0, st>>>(a);
-            else decode_step16_kernel<__nv_bfloat16, false><<<blocks2, 256, 0, st>>>(a);
-        } else {
-            if (zoh) decode_step16_kernel<float, true><<<blocks2, 256, 0, st>>>(a);
-            else decode_step16_kernel<float, false><<<blocks2, 256, 0, st>>>(a);
-        }
+        cudaError_t e;
+        if (p->out_dtype == SSM_BF16)
+            e = zoh ? launch_dependent(decode_step16_kernel<__nv_bfloat16, true>, blocks2, st, a)
+                    : launch_dependent(decode_step16_kernel<__nv_bfloat16, false>, blocks2, st, a);
+        else
+            e = zoh ? launch_dependent(decode_step16_kernel<float, true>, blocks2, st, a)
+                    : launch_dependent(decode_step16_kernel<float, false>, blocks2, st, a);
+        if (e != cudaSuccess) return e;
         count_launches(1);
         return cudaGetLastError();
     }
