@@ -21,7 +21,10 @@ def _lib():
 
 
 @pytest.mark.parametrize("batch,m,n,k", [(1, 128, 128, 64), (2, 288, 256, 4096), (1, 100, 200, 200),
-                                         (3, 300, 1000, 520), (2, 4096, 384, 256), (1, 8, 8, 8)])
+                                         (3, 300, 1000, 520), (2, 4096, 384, 256), (1, 8, 8, 8),
+                                         # more tiles than SMs at K <= 256: contiguous tile ranges that
+                                         # cross row tiles, W reloaded inside a CTA
+                                         (2, 4096, 2560, 256), (3, 1000, 3000, 200)])
 def test_products(batch, m, n, k):
     L = _lib()
     W = S.normal(40, 1, (m, k), torch.bfloat16, std=k ** -0.5)
