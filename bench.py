@@ -715,7 +715,7 @@ def main(argv=None):
                     help="time only the x_proj / dt_proj products at --seqlen (for profiling captures)")
     ap.add_argument("--ssd-only", action="store_true",
                     help="time only the Mamba-2 SSD forward (for profiling captures)")
-    ap.add_argument("--e2e-steps", type=int, default=6)
+    ap.add_argument("--e2e-steps", type=int, default=12)
     ap.add_argument("--seqlen", type=int, default=0,
                     help="shorter sequence for small profiling captures (the headline uses the default)")
     ap.add_argument("--decode-layers", type=int, default=0,
@@ -839,8 +839,10 @@ def main(argv=None):
         sets = (g, g2)
 
         def results(gs):
+            # the layer output and every gradient that leaves the step; du (the gradient of
+            # the conv output) stays on the device, where the conv backward consumes it
             o = {"y": gs["y"]}
-            o.update({k: v for k, v in gs["grads"].items() if v is not None and k != "dh0"})
+            o.update({k: v for k, v in gs["grads"].items() if v is not None and k not in ("dh0", "du")})
             o.update({"c_" + k: v for k, v in gs["cgrads"].items() if v is not None})
             return o
 
@@ -882,7 +884,9 @@ def main(argv=None):
         e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, device)
         e2e = {"value": round(ct_step * n * world / (e2e_ms * 1e-3), 1), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
-               "ms_per_step": round(e2e_ms / n, 2), "overlap": "two buffer sets, copy streams beside the compute stream"}
+               "ms_per_step": round(e2e_ms / n, 2), "overlap": "two buffer sets, copy streams beside the compute stream",
+               "d2h": "y and the gradients leaving the step (conv dx, dweight, dbias; ddt, dz, dB, dC, dA, dD, "
+                      "d_delta_bias); du, consumed by the conv backward, stays on the device"}
         del host, out_host, g2, sets
 
     configs = proj = None
