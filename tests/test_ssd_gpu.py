@@ -76,6 +76,11 @@ def assert_state_close(hN, href, habs, what="final state"):
     (2, 640, 4, 128, 2, True, torch.bfloat16),    # five chunks, two groups
     (1, 1000, 3, 64, 1, False, torch.float32),    # eight chunks and a ragged tail, three heads per group
     (2, 385, 2, 32, 2, True, torch.float32),      # four chunks with a tail of one
+    # more (batch, head) units than SMs: each CTA of the persistent grid walks two or three
+    # units as one chunk sequence (the next unit's initial state, first tiles and C B^T
+    # prepared while the current unit ends)
+    (4, 300, 80, 32, 2, True, torch.float32),
+    (5, 129, 64, 64, 1, False, torch.bfloat16),
 ])
 def test_ssd_matches_oracle(b, L, H, N, G, h0, out_dtype):
     Lb = _lib()
