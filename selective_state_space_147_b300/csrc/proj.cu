@@ -92,7 +92,7 @@ __device__ __forceinline__ void record_timeout(int* abort_flag) {
 }
 
 // Persistent: every CTA (one per SM) walks tiles blockIdx.x, blockIdx.x + gridDim.x, ...
-// The producer and the MMA issuer run ahead through a 6-stage shared-memory ring; two
+// The producer and the MMA issuer run ahead through a 4-stage shared-memory ring; two
 // TMEM accumulators let the epilogue warps drain tile i while tile i + 1 accumulates.
 __global__ void __launch_bounds__(kPThreads, 1)
 proj_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
