@@ -124,3 +124,52 @@ def test_mamba2p8b_layer_step():
     g = _inputs(S.config_seed(3), 128, 5120, 16, 4, torch.bfloat16)
     got, ref = _run(g)
     _check(got, ref, torch.bfloat16)
+
+
+def test_graph_of_dependent_launches():
+    """Three layers x four token steps of the fused step captured in one CUDA graph and
+    replayed: each launch is a programmatic dependent of the one before it, so this checks
+    that every layer still sees the previous launches' writes (its own state from the step
+    before) when the launches overlap in the graph."""
+    L = _lib()
+    layers, steps, batch, dim = 3, 4, 4, 512
+    gs = [_inputs(70 + l, batch, dim, 16, 4, torch.bfloat16) for l in range(layers)]
+    tok = [[_inputs(80 + 10 * l + s, batch, dim, 16, 4, torch.bfloat16) for s in range(steps)] for l in range(layers)]
+    st = [g["state"].cuda().clone() for g in gs]
+    cs = [g["conv_state"].cuda().clone() for g in gs]
+    dev = [{k: v.cuda() for k, v in g.items()} for g in gs]
+    tdev = [[{k: tok[l][s][k].cuda() for k in ("x", "dt", "z", "B", "C")} for s in range(steps)] for l in range(layers)]
+    outs = [[torch.empty(batch, dim, dtype=torch.float32, device="cuda") for _ in range(steps)] for _ in range(layers)]
+    st0 = [t.clone() for t in st]
+    cs0 = [t.clone() for t in cs]
+
+    def run():
+        for s in range(steps):
+            for l in range(layers):
+                t = tdev[l][s]
+                L.ssm_decode_step(st[l], cs[l], t["x"], t["dt"], dev[l]["A"], t["B"], t["C"], dev[l]["w"],
+                                  conv_bias=dev[l]["cb"], D=dev[l]["D"], delta_bias=dev[l]["bias"], z=t["z"],
+                                  out=outs[l][s])
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        run()                                   # warm-up outside the graph
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        run()
+    for l in range(layers):                     # replay from the initial states
+        st[l].copy_(st0[l])
+        cs[l].copy_(cs0[l])
+    graph.replay()
+    torch.cuda.synchronize()
+    for l in range(layers):
+        sref, csref = gs[l]["state"], gs[l]["conv_state"]
+        for s in range(steps):
+            t = tok[l][s]
+            ref, sref, csref, _ = oracle.decode_step(sref, csref, t["x"], t["dt"], gs[l]["A"], t["B"], t["C"],
+                                                     gs[l]["w"], gs[l]["cb"], gs[l]["D"], gs[l]["bias"], t["z"])
+            assert_close(outs[l][s], ref, torch.bfloat16, what=f"layer {l} step {s} out")
+        assert_close(st[l], sref, torch.bfloat16, what=f"layer {l} state")
+        assert np.array_equal(to_np(cs[l]), csref), f"layer {l} conv window"
