@@ -19,7 +19,8 @@
 // Design for B300: one CTA per (b, h) walks the chunks in order; every
 // contraction is a tcgen05.mma (bf16 x bf16 -> fp32 in TMEM, M = 128 rows):
 //   G  = C B^T           (128 x 128, K = N)           A = C tile, B = B tile (both K-major)
-//   Yd = M X             (128 x 64,  K = 128 steps)   M = G o decay o Delta (lower triangle)
+//   Yd = M X             (128 x 64,  K = 128 steps)   M = G o decay o Delta (lower triangle),
+//                                                     written to TMEM and read from there
 //   S  = B^T (w o X)     (N x 64,    K = 128 steps)   A = the B tile read state-major
 //   Yo = C H             (128 x 64,  K = N)           H = the entering state in bf16
 // y = Yd + exp(s_i) Yo + D x, and the fp32 state H' = exp(s_last) H + S stays in
@@ -30,8 +31,8 @@
 // sums s ahead of time; warp 9 issues the MMAs -- C H while the epilogue warps
 // build w o X, B^T (w o X) while they turn G into M, the next chunk's G after
 // M X -- and eight epilogue warps (warp w: TMEM lanes 32 (w % 4) .. + 31 = chunk
-// rows, half w / 4 of the columns) compute w o X and M into shared memory
-// (exp per element only in the diagonal 32 x 32 blocks; below them the decay
+// rows, half w / 4 of the columns) compute w o X into shared memory and M into
+// tensor memory (exp per element only in the diagonal 32 x 32 blocks; below them the decay
 // factors into exp(s_i - s_e) exp(s_e - s_j), both exponents <= 0), then the
 // state update and y, which leaves through a swizzled staging tile and bulk
 // tensor stores that warp 10 issues (a thread with bulk stores in flight would
@@ -62,7 +63,7 @@ constexpr int kStage = 2 * kTileBC + kTileX;
 constexpr int kStages = 2;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 32 * (kEpiWarps + 3);   // + warp 8: TMA producer, warp 9: MMA issuer, warp 10: output stores
-constexpr int kOffM = kStages * kStage;           // M: K-major A operand, two 64-step atoms
+constexpr int kOffM = kStages * kStage;           // the output staging tile (y of a chunk)
 constexpr int kOffWX = kOffM + 2 * kAtom;         // w o x: MN-major B operand
 constexpr int kOffH = kOffWX + kTileX;            // the entering state in bf16: MN-major B operand
 constexpr int kOffAux = kOffH + kTileX;
@@ -72,8 +73,8 @@ constexpr int kAuxFloats = 2 * kQ * 2 + kQ;
 // full, empty (C and B), fullx, emptyx (x), dready, gfull, wready, mready, yfull, yempty, done, ystaged, yfree
 constexpr int kNumBars = 2 + 2 + 2 + 2 + 2 + 2 + 1 + 1 + 1 + 1 + 1 + 1 + 1;
 constexpr int kSmem = kOffAux + kAuxFloats * 4 + kNumBars * 8 + 16;
-// TMEM columns: G (two buffers), Yd, Yo, S
-constexpr uint32_t kColG = 0, kColYd = 256, kColYo = 320, kColS = 384, kTmemCols = 512;
+// TMEM columns: G (two buffers), Yd, Yo, S, and M (bf16, two per column: Yd's A operand)
+constexpr uint32_t kColG = 0, kColYd = 256, kColYo = 320, kColS = 384, kColM = 448, kTmemCols = 512;
 
 struct SsdArgs {
     int L, H, heads_per_group, nstate, nbox, nchunks;
@@ -273,7 +274,6 @@ ssd_chunk_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant_
             constexpr uint32_t idS = idesc_bf16(128, 64, true, true);
             const int ksN = a.nstate / 16;
             // descriptors built once; a K step adds a constant to the start-address field
-            const uint64_t dM = sw128_desc(smem_addr(smem + kOffM), 16, 1024);
             const uint64_t dWX = sw128_desc(smem_addr(smem + kOffWX), 8192, 1024);
             const uint64_t dH = sw128_desc(smem_addr(smem + kOffH), 8192, 1024);
             // stage 0's tiles; stage s is s * kStage bytes further
@@ -321,14 +321,14 @@ ssd_chunk_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant_
                     umma_bf16(tmem + kColS, dBt0 + stage_off(s) + mnmajor_step(k), dWX + mnmajor_step(k), idS,
                               k > 0 ? 1u : 0u);
                 umma_commit(&empty[s]);   // C and B of the stage are free once these have read them
-                // Yd = M x: A = M (K-major, two 64-step atoms), B = x (MN-major rows of 64 columns)
+                // Yd = M x: A = M from TMEM (K-major rows), B = x (MN-major rows of 64 columns)
                 if (!(ok = mbar_wait(mready, c & 1))) break;
                 if (!(ok = mbar_wait(&fullx[s], (c >> 1) & 1))) break;
                 fence_after_sync();
 #pragma unroll
                 for (int k = 0; k < kQ / 16; k++)
-                    umma_bf16(tmem + kColYd, dM + kmajor_step(k, kAtom), dX0 + stage_off(s) + mnmajor_step(k), idY,
-                              k > 0 ? 1u : 0u);
+                    umma_bf16_ta(tmem + kColYd, tmem + kColM + 8 * k, dX0 + stage_off(s) + mnmajor_step(k), idY,
+                                 k > 0 ? 1u : 0u);
                 umma_commit(yfull);
                 umma_commit(&emptyx[s]);
                 if (c + 1 < nc && !g_next && !(ok = issue_g(c + 1))) break;
@@ -384,7 +384,6 @@ ssd_chunk_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant_
         if (lane == 0) mbar_arrive(yempty);
         for (int c = 0; c < nc; c++) {
             const int buf = c & 1;
-            const int t0 = c * kQ;
             float* dlb = dl + buf * kQ;
             float* s2b = s2 + buf * kQ;
             // (a wait that runs out is caught by the uniform check before M is built)
@@ -420,54 +419,57 @@ ssd_chunk_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant_
             __syncwarp();
             if (lane == 0) mbar_arrive(wready);
             // ---- M row `row`, 32-step column blocks cb = 2 hf, 2 hf + 1 (K atom hf of the A operand)
-            // G of this chunk, and the previous chunk's output read out of M's buffer
-            bool gw = mbar_wait(&gfull[buf], (c >> 1) & 1);
-            if (c > 0) gw = gw && mbar_wait(yfree, (c - 1) & 1);
+            // G of this chunk
+            const bool gw = mbar_wait(&gfull[buf], (c >> 1) & 1);
             if (!gw) record_timeout(a.status, abort_flag);
             if (!epi_all(gw && *(volatile int*)abort_flag == 0)) break;
             fence_after_sync();
-            unsigned char* Mrow = Mt + hf * kAtom;
+            // M row `row` into TMEM (the A operand of M x): 32-step column block cb as 16 columns
+            // of bf16 pairs at kColM + 16 cb.  Chunk c - 1's M x finished reading them before
+            // its outputs were released (yfull).
 #pragma unroll
             for (int cc = 0; cc < 2; cc++) {
                 const int cb = 2 * hf + cc;
+                uint32_t mp[16];
                 if (cb > quad) {
                     // above the diagonal: zero
 #pragma unroll
-                    for (int q = 0; q < 4; q++)
-                        *reinterpret_cast<uint4*>(swz(Mrow, row, 4 * cc + q)) = make_uint4(0, 0, 0, 0);
-                    continue;
-                }
-                uint32_t r[32];
-                tmem_ld32(tl + kColG + buf * 128 + 32 * cb, r);
-                if (cb < quad) {
-                    // below the diagonal block: the factored decay
-                    const float ri = ex2_approx(si - s2b[32 * cb + 31]);
-#pragma unroll
-                    for (int q = 0; q < 4; q++) {
-                        const float4 f0 = *reinterpret_cast<const float4*>(cf + 32 * cb + 8 * q);
-                        const float4 f1 = *reinterpret_cast<const float4*>(cf + 32 * cb + 8 * q + 4);
-                        const float fj[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
-                        float v[8];
-#pragma unroll
-                        for (int e = 0; e < 8; e++) v[e] = __uint_as_float(r[8 * q + e]) * ri * fj[e];
-                        *reinterpret_cast<uint4*>(swz(Mrow, row, 4 * cc + q)) = pack8(v);
-                    }
+                    for (int i = 0; i < 16; i++) mp[i] = 0u;
                 } else {
-                    // the diagonal block: the decay per element, zero above the diagonal
+                    uint32_t r[32];
+                    tmem_ld32(tl + kColG + buf * 128 + 32 * cb, r);
+                    if (cb < quad) {
+                        // below the diagonal block: the factored decay
+                        const float ri = ex2_approx(si - s2b[32 * cb + 31]);
 #pragma unroll
-                    for (int q = 0; q < 4; q++) {
-                        float v[8];
+                        for (int q = 0; q < 4; q++) {
+                            const float4 f0 = *reinterpret_cast<const float4*>(cf + 32 * cb + 8 * q);
+                            const float4 f1 = *reinterpret_cast<const float4*>(cf + 32 * cb + 8 * q + 4);
+                            const float fj[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
 #pragma unroll
-                        for (int e = 0; e < 8; e++) {
-                            const int j = 32 * cb + 8 * q + e;
-                            const float m = __uint_as_float(r[8 * q + e]) * ex2_approx(si - s2b[j]) * dlb[j];
-                            v[e] = j <= row ? m : 0.f;
+                            for (int e = 0; e < 8; e += 2)
+                                mp[4 * q + e / 2] = pack_bf16x2(__uint_as_float(r[8 * q + e]) * ri * fj[e],
+                                                                __uint_as_float(r[8 * q + e + 1]) * ri * fj[e + 1]);
                         }
-                        *reinterpret_cast<uint4*>(swz(Mrow, row, 4 * cc + q)) = pack8(v);
+                    } else {
+                        // the diagonal block: the decay per element, zero above the diagonal
+#pragma unroll
+                        for (int q = 0; q < 4; q++) {
+                            float v[8];
+#pragma unroll
+                            for (int e = 0; e < 8; e++) {
+                                const int j = 32 * cb + 8 * q + e;
+                                const float m = __uint_as_float(r[8 * q + e]) * ex2_approx(si - s2b[j]) * dlb[j];
+                                v[e] = j <= row ? m : 0.f;
+                            }
+#pragma unroll
+                            for (int e = 0; e < 8; e += 2) mp[4 * q + e / 2] = pack_bf16x2(v[e], v[e + 1]);
+                        }
                     }
                 }
+                tmem_st16(tl + kColM + 16 * cb, mp);
             }
-            fence_async_smem();
+            tmem_st_wait();
             fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(mready);
@@ -513,9 +515,12 @@ ssd_chunk_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant_
             __syncwarp();
             if (lane == 0) mbar_arrive(yempty);
             // stage the 128 x 64 output tile (128-byte swizzled rows; fp32: two 32-column boxes)
-            // where this chunk's M was -- consumed by now -- and write it with bulk tensor
-            // stores (rows past the sequence end are not written)
+            // once the previous chunk's tile has been read out of the staging buffer, and write
+            // it with bulk tensor stores (rows past the sequence end are not written)
             {
+                const bool fw = c == 0 || mbar_wait(yfree, (c - 1) & 1);
+                if (!fw) record_timeout(a.status, abort_flag);
+                if (!epi_all(fw && *(volatile int*)abort_flag == 0)) break;
                 unsigned char* Yt = Mt;
                 if constexpr (sizeof(Tout) == 2) {
 #pragma unroll
