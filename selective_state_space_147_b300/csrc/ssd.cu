@@ -71,7 +71,7 @@ constexpr int kOffAux = kOffH + kTileX;
 // the blocks below M's diagonal [128], barriers
 constexpr int kAuxFloats = 2 * kQ * 2 + kQ;
 // full, empty (C and B), fullx, emptyx (x), dready, gfull, wready, mready, yfull, yempty, done, ystaged, yfree
-constexpr int kNumBars = 2 + 2 + 2 + 2 + 2 + 2 + 1 + 1 + 1 + 1 + 1 + 1 + 1;
+constexpr int kNumBars = 2 + 2 + 2 + 2 + 2 + 2 + 1 + 1 + 1 + 1 + 1 + 1 + 1 + 1;
 constexpr int kSmem = kOffAux + kAuxFloats * 4 + kNumBars * 8 + 16;
 // TMEM columns: G (two buffers), Yd, Yo, S, and M (bf16, two per column: Yd's A operand)
 constexpr uint32_t kColG = 0, kColYd = 256, kColYo = 320, kColS = 384, kColM = 448, kTmemCols = 512;
@@ -142,7 +142,8 @@ ssd_chunk_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant_
     uint64_t* done = yempty + 1;
     uint64_t* ystaged = done + 1;   // the output tile of a chunk is in its staging buffer
     uint64_t* yfree = ystaged + 1;  // ... and has been read out by its bulk store
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(yfree + 1);
+    uint64_t* sfull = yfree + 1;    // S of the chunk (and its C H before it) complete
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sfull + 1);
     int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
     const int unit = blockIdx.x;
@@ -165,6 +166,7 @@ ssd_chunk_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant_
         mbar_init(done, 1);
         mbar_init(ystaged, kEpiWarps);
         mbar_init(yfree, 1);
+        mbar_init(sfull, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -323,6 +325,7 @@ ssd_chunk_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant_
                     umma_bf16(tmem + kColS, dBt0 + stage_off(s) + mnmajor_step(k), dWX + mnmajor_step(k), idS,
                               k > 0 ? 1u : 0u);
                 umma_commit(&empty[s]);   // C and B of the stage are free once these have read them
+                umma_commit(sfull);       // the state update may start before M x
                 // Yd = M x: A = M from TMEM (K-major rows), B = x (MN-major rows of 64 columns)
                 if (!(ok = mbar_wait(mready, c & 1))) break;
                 if (!(ok = mbar_wait(&fullx[s], (c >> 1) & 1))) break;
@@ -477,9 +480,11 @@ ssd_chunk_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant_
             __syncwarp();
             if (lane == 0) mbar_arrive(mready);
             // ---- wait for Yd, S, Yo of this chunk
-            const bool yw = mbar_wait(yfull, c & 1);
-            if (!yw) record_timeout(a.status, abort_flag);
-            if (!epi_all(yw && *(volatile int*)abort_flag == 0)) break;
+            // ---- the state update needs only S (and C H done reading the state copy): it runs
+            // while M x is still on the tensor core
+            const bool sw = mbar_wait(sfull, c & 1);
+            if (!sw) record_timeout(a.status, abort_flag);
+            if (!epi_all(sw && *(volatile int*)abort_flag == 0)) break;
             fence_after_sync();
             // state: H' = exp(s_last) H + S for state `row`; its bf16 copy is the next chunk's operand
             {
@@ -499,6 +504,10 @@ ssd_chunk_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant_
             // the state copy is visible to the tensor core before any global store is in flight
             // (the proxy fence would otherwise wait for those stores too)
             fence_async_smem();
+            const bool yw = mbar_wait(yfull, c & 1);
+            if (!yw) record_timeout(a.status, abort_flag);
+            if (!epi_all(yw && *(volatile int*)abort_flag == 0)) break;
+            fence_after_sync();
             // outputs: y = Yd + exp(s_i) Yo + D x for step t0 + row, columns 32 hf .. + 31
             float y[32];
             {
