@@ -55,9 +55,10 @@ def _load():
             lib.oracle_conv1d_silu_update.argtypes = [i64, i64, i64] + [p] * 5
             lib.oracle_conv1d_silu_bwd.argtypes = [i64, i64, i64, i64] + [p] * 9
             lib.oracle_ssd_fwd.argtypes = [i64] * 6 + [p] * 8 + [i32, p, p, i64, i64]
+            lib.oracle_ssd_bwd.argtypes = [i64] * 6 + [p] * 8 + [i32] + [p] * 10 + [i64, i64]
             for f in (lib.oracle_scan_fwd, lib.oracle_scan_bwd, lib.oracle_state_update,
                       lib.oracle_conv1d_silu, lib.oracle_conv1d_silu_update, lib.oracle_conv1d_silu_bwd,
-                      lib.oracle_ssd_fwd):
+                      lib.oracle_ssd_fwd, lib.oracle_ssd_bwd):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -262,6 +263,46 @@ def ssd_fwd(x, dt, A, B, C, D=None, dt_bias=None, h0=None, delta_softplus=True, 
         with ThreadPoolExecutor(len(rs)) as ex:
             list(ex.map(run, rs))
     return out, hN
+
+
+def ssd_bwd(x, dt, A, B, C, dout, D=None, dt_bias=None, h0=None, dhN=None, delta_softplus=True,
+            threads: int = 1):
+    """Reverse-mode gradients of ssd_fwd for the loss sum(dout*out) + sum(dhN*final_state),
+    by the adjoint of the recurrence.  Returns a dict with dx (batch, L, H, P), ddt
+    (batch, L, H), dA, dD, ddt_bias (H,), dB, dC (batch, L, G, N) and dh0 (batch, H, N, P)
+    as float64 (dD, ddt_bias are returned even when D, dt_bias are absent)."""
+    lib = _load()
+    x, dt, A, B, C, D, dt_bias, h0, dout, dhN = map(_f64, (x, dt, A, B, C, D, dt_bias, h0, dout, dhN))
+    batch, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    dx = np.zeros((batch, L, H, P))
+    ddt = np.zeros((batch, L, H))
+    dh0 = np.zeros((batch, H, N, P))
+    rs = _ranges(batch * H, threads)
+    parts = [dict(dA=np.zeros(H), dB=np.zeros((batch, L, G, N)), dC=np.zeros((batch, L, G, N)),
+                  dD=np.zeros(H), ddt_bias=np.zeros(H)) for _ in rs]
+
+    def run(i):
+        r, pa = rs[i], parts[i]
+        rc = lib.oracle_ssd_bwd(batch, L, H, P, N, G, _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                                _ptr(dt_bias), _ptr(h0), int(bool(delta_softplus)), _ptr(dout), _ptr(dhN),
+                                _ptr(dx), _ptr(ddt), _ptr(pa["dA"]), _ptr(pa["dB"]), _ptr(pa["dC"]),
+                                _ptr(pa["dD"]), _ptr(pa["ddt_bias"]), _ptr(dh0), r[0], r[1])
+        if rc != 0:
+            raise ValueError("oracle_ssd_bwd rejected its arguments")
+
+    if len(rs) <= 1:
+        for i in range(len(rs)):
+            run(i)
+    else:
+        with ThreadPoolExecutor(len(rs)) as ex:
+            list(ex.map(run, range(len(rs))))
+    res = dict(dx=dx, ddt=ddt, dh0=dh0, dA=np.zeros(H), dB=np.zeros((batch, L, G, N)),
+               dC=np.zeros((batch, L, G, N)), dD=np.zeros(H), ddt_bias=np.zeros(H))
+    for pa in parts:
+        for k in ("dA", "dB", "dC", "dD", "ddt_bias"):
+            res[k] += pa[k]
+    return res
 
 
 def proj(W, X, bias=None, softplus: bool = False):

@@ -471,3 +471,121 @@ int oracle_ssd_fwd(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdi
     free(S);
     return 0;
 }
+
+/*
+ * Mamba-2 SSD layer, reverse mode: the gradients of
+ *   loss = sum(dout * out) + sum(dhN * hN)
+ * for the recurrence of oracle_ssd_fwd ("Mamba 与状态空间模型" section 09;
+ * pnsm.cn overview, section "Mamba-2：状态空间对偶性"), by the adjoint of that
+ * recurrence walked backwards one step at a time.  Per (b, head h) the states
+ * H_0 .. H_L (H_t = the state after step t, H_0 = h0) are kept; then, from
+ * t = L - 1 down to 0, with G the adjoint of the state (starting at dhN):
+ *
+ *   y_t = C_t^T H_(t+1) + D x_t         ->  dC_t += H_(t+1) dy_t,  dD += x_t . dy_t,
+ *                                           dx_t  = D dy_t,        G += C_t dy_t^T
+ *   H_(t+1) = a_t H_t + Delta_t B_t x_t^T, a_t = exp(Delta_t A)
+ *                                       ->  dx_t += Delta_t G^T B_t,
+ *                                           dB_t += Delta_t G x_t,
+ *                                           dDelta_t = <G, A a_t H_t + B_t x_t^T>,
+ *                                           dA += <G, Delta_t a_t H_t>,
+ *                                           G <- a_t G
+ *   Delta_t = softplus(v), v = dt + dt_bias  ->  ddt_t = dDelta_t sigmoid(v)
+ *                                           (= dDelta_t without softplus),
+ *                                           ddt_bias += ddt_t
+ *
+ * and dh0 = G at the end.  dx, ddt, dh0 are written for the units in
+ * [u_begin, u_end); dA, dD, ddt_bias (H) and dB, dC (batch, L, G, N) are ADDED
+ * to (so that threads working on disjoint units can keep partial sums).
+ */
+int oracle_ssd_bwd(int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, int64_t dstate,
+                   int64_t ngroups, const double* x, const double* dt, const double* A,
+                   const double* Bm, const double* Cm, const double* Dskip, const double* dt_bias,
+                   const double* h0, int delta_softplus, const double* dout, const double* dhN,
+                   double* dx, double* ddt, double* dA, double* dB, double* dC, double* dD,
+                   double* ddt_bias, double* dh0, int64_t u_begin, int64_t u_end)
+{
+    if (batch < 0 || seqlen < 0 || nheads < 1 || headdim < 1 || dstate < 1 || ngroups < 1) return -1;
+    if (nheads % ngroups != 0) return -1;
+    if (u_begin < 0 || u_end > batch * nheads || u_begin > u_end) return -1;
+    const int64_t P = headdim, N = dstate, H = nheads, G = ngroups, NP = dstate * headdim;
+    double* Hs = (double*)malloc(sizeof(double) * (size_t)((seqlen + 1) * NP));
+    double* Gs = (double*)malloc(sizeof(double) * (size_t)NP);
+    double* delta = (double*)malloc(sizeof(double) * (size_t)(seqlen > 0 ? seqlen : 1));
+    if (!Hs || !Gs || !delta) {
+        free(Hs); free(Gs); free(delta);
+        return -1;
+    }
+    for (int64_t unit = u_begin; unit < u_end; unit++) {
+        const int64_t b = unit / H, h = unit % H, g = h / (H / G);
+        const double Dh = Dskip ? Dskip[h] : 0.0;
+        /* forward: every state of the sequence */
+        for (int64_t i = 0; i < NP; i++) Hs[i] = h0 ? h0[unit * NP + i] : 0.0;
+        for (int64_t t = 0; t < seqlen; t++) {
+            const double v = dt[(b * seqlen + t) * H + h] + (dt_bias ? dt_bias[h] : 0.0);
+            delta[t] = delta_softplus ? o_softplus(v) : v;
+            const double a = exp(delta[t] * A[h]);
+            const double* Bt = Bm + ((b * seqlen + t) * G + g) * N;
+            const double* xt = x + ((b * seqlen + t) * H + h) * P;
+            const double* Hp = Hs + t * NP;
+            double* Hn = Hs + (t + 1) * NP;
+            for (int64_t n = 0; n < N; n++)
+                for (int64_t p = 0; p < P; p++)
+                    Hn[n * P + p] = a * Hp[n * P + p] + delta[t] * Bt[n] * xt[p];
+        }
+        /* reverse */
+        for (int64_t i = 0; i < NP; i++) Gs[i] = dhN ? dhN[unit * NP + i] : 0.0;
+        for (int64_t t = seqlen - 1; t >= 0; t--) {
+            const int64_t row = (b * seqlen + t) * H + h;
+            const double v = dt[row] + (dt_bias ? dt_bias[h] : 0.0);
+            const double a = exp(delta[t] * A[h]);
+            const double* Bt = Bm + ((b * seqlen + t) * G + g) * N;
+            const double* Ct = Cm + ((b * seqlen + t) * G + g) * N;
+            double* dBt = dB + ((b * seqlen + t) * G + g) * N;
+            double* dCt = dC + ((b * seqlen + t) * G + g) * N;
+            const double* xt = x + row * P;
+            const double* dyt = dout + row * P;
+            double* dxt = dx + row * P;
+            const double* Hp = Hs + t * NP;
+            const double* Hn = Hs + (t + 1) * NP;
+            /* readout */
+            for (int64_t n = 0; n < N; n++) {
+                double acc = 0.0;
+                for (int64_t p = 0; p < P; p++) acc += Hn[n * P + p] * dyt[p];
+                dCt[n] += acc;
+            }
+            for (int64_t p = 0; p < P; p++) {
+                dD[h] += xt[p] * dyt[p];
+                dxt[p] = Dh * dyt[p];
+            }
+            for (int64_t n = 0; n < N; n++)
+                for (int64_t p = 0; p < P; p++) Gs[n * P + p] += Ct[n] * dyt[p];
+            /* state update */
+            for (int64_t p = 0; p < P; p++) {
+                double acc = 0.0;
+                for (int64_t n = 0; n < N; n++) acc += Gs[n * P + p] * Bt[n];
+                dxt[p] += delta[t] * acc;
+            }
+            for (int64_t n = 0; n < N; n++) {
+                double acc = 0.0;
+                for (int64_t p = 0; p < P; p++) acc += Gs[n * P + p] * xt[p];
+                dBt[n] += delta[t] * acc;
+            }
+            double dd = 0.0, da = 0.0;
+            for (int64_t n = 0; n < N; n++)
+                for (int64_t p = 0; p < P; p++) {
+                    dd += Gs[n * P + p] * (A[h] * a * Hp[n * P + p] + Bt[n] * xt[p]);
+                    da += Gs[n * P + p] * delta[t] * a * Hp[n * P + p];
+                }
+            dA[h] += da;
+            for (int64_t i = 0; i < NP; i++) Gs[i] *= a;
+            const double dv = delta_softplus ? dd * o_sigmoid(v) : dd;
+            ddt[row] = dv;
+            ddt_bias[h] += dv;
+        }
+        for (int64_t i = 0; i < NP; i++) dh0[unit * NP + i] = Gs[i];
+    }
+    free(Hs);
+    free(Gs);
+    free(delta);
+    return 0;
+}

@@ -577,3 +577,85 @@ def test_ssd_chunk_invariance():
                             cut(g["B"], slice(m, None)), cut(g["C"], slice(m, None)), g["D"], g["dt_bias"], h1)
     assert rel_err(np.concatenate([y1, y2], axis=1), full) <= 1e-12
     assert rel_err(h2, hfull) <= 1e-12
+
+
+# ---------------------------------------------------------------------------
+# Mamba-2 SSD backward (oracle.ssd_bwd, the adjoint of the recurrence)
+
+def _ssd_loss(g, soft, dout, dhN):
+    y, hN = oracle.ssd_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"], g["dt_bias"], g["h0"],
+                           delta_softplus=soft)
+    val = float(np.sum(y * dout))
+    if dhN is not None:
+        val += float(np.sum(hN * dhN))
+    return val
+
+
+@pytest.mark.parametrize("soft", [True, False])
+@pytest.mark.parametrize("with_h0", [True, False])
+@pytest.mark.parametrize("with_dhN", [True, False])
+def test_ssd_backward_matches_finite_differences(soft, with_h0, with_dhN):
+    """Every gradient of oracle.ssd_bwd equals the central difference of the
+    (separately pinned) forward recurrence, on a shape with two groups."""
+    g = _ssd_inputs(41, b=2, L=7, H=4, P=3, N=5, G=2, h0=with_h0)
+    if not soft:
+        g["dt"] = np.abs(g["dt"]) * 0.5 + 0.05
+    r = rng(42)
+    dout = r.normal(size=g["x"].shape)
+    dhN = r.normal(size=(2, 4, 5, 3)) if with_dhN else None
+    grads = oracle.ssd_bwd(g["x"], g["dt"], g["A"], g["B"], g["C"], dout, g["D"], g["dt_bias"], g["h0"], dhN,
+                           delta_softplus=soft)
+    names = {"x": "dx", "dt": "ddt", "A": "dA", "B": "dB", "C": "dC", "D": "dD", "dt_bias": "ddt_bias",
+             "h0": "dh0"}
+    eps = 1e-6
+    for key, gname in names.items():
+        if g[key] is None:
+            continue
+        base = g[key]
+        num = np.zeros_like(base)
+        it = np.nditer(base, flags=["multi_index"])
+        for _ in it:
+            i = it.multi_index
+            old = base[i]
+            base[i] = old + eps
+            fp = _ssd_loss(g, soft, dout, dhN)
+            base[i] = old - eps
+            fm = _ssd_loss(g, soft, dout, dhN)
+            base[i] = old
+            num[i] = (fp - fm) / (2 * eps)
+        assert rel_err(grads[gname], num) < 1e-6, gname
+
+
+def test_ssd_backward_with_one_head_dim_is_the_selective_scan_backward():
+    """P = 1 and one group: each head is a Mamba-1 channel with Bbar = Delta B and
+    all N states sharing A[h], so the gradients are those of the (separately
+    pinned) selective-scan backward, with dA summed over the states."""
+    g = _ssd_inputs(43, b=2, L=13, H=3, P=1, N=4, G=1, h0=True)
+    r = rng(44)
+    dout = r.normal(size=g["x"].shape)
+    dhN = r.normal(size=(2, 3, 4, 1))
+    got = oracle.ssd_bwd(g["x"], g["dt"], g["A"], g["B"], g["C"], dout, g["D"], g["dt_bias"], g["h0"], dhN)
+    u = g["x"][..., 0].transpose(0, 2, 1)
+    dt = g["dt"].transpose(0, 2, 1)
+    A = np.repeat(g["A"][:, None], 4, axis=1)
+    Bm = g["B"][:, :, 0, :].transpose(0, 2, 1)
+    Cm = g["C"][:, :, 0, :].transpose(0, 2, 1)
+    ref = oracle.scan_bwd(u, dt, A, Bm, Cm, dout[..., 0].transpose(0, 2, 1), g["D"], g["dt_bias"], None,
+                          g["h0"][..., 0], dhN[..., 0], zoh=False)
+    assert rel_err(got["dx"][..., 0].transpose(0, 2, 1), ref["du"]) <= 1e-12
+    assert rel_err(got["ddt"].transpose(0, 2, 1), ref["ddt"]) <= 1e-12
+    assert rel_err(got["dA"], ref["dA"].sum(axis=1)) <= 1e-12
+    assert rel_err(got["dB"][:, :, 0, :].transpose(0, 2, 1), ref["dB"]) <= 1e-12
+    assert rel_err(got["dC"][:, :, 0, :].transpose(0, 2, 1), ref["dC"]) <= 1e-12
+    assert rel_err(got["dD"], ref["dD"]) <= 1e-12
+    assert rel_err(got["ddt_bias"], ref["dbias"]) <= 1e-12
+    assert rel_err(got["dh0"][..., 0], ref["dh0"]) <= 1e-12
+
+
+def test_ssd_backward_threads_agree():
+    g = _ssd_inputs(45, b=3, L=9, H=4, P=2, N=3, G=2, h0=True)
+    dout = rng(46).normal(size=g["x"].shape)
+    one = oracle.ssd_bwd(g["x"], g["dt"], g["A"], g["B"], g["C"], dout, g["D"], g["dt_bias"], g["h0"])
+    many = oracle.ssd_bwd(g["x"], g["dt"], g["A"], g["B"], g["C"], dout, g["D"], g["dt_bias"], g["h0"], threads=5)
+    for k in one:
+        assert rel_err(many[k], one[k]) <= 1e-13, k
