@@ -473,6 +473,69 @@ typedef struct {
 SSM_API ssm_status ssm_ssd_fwd(const ssm_ssd_fwd_params* p, ssm_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Mamba-2 SSD layer, backward: the gradients of
+ *   loss = sum(dout * out) + sum(dfinal_state * final_state)
+ * for the layer of ssm_ssd_fwd (same sections), through its chunked form.
+ * Per chunk of 64 steps, with s the in-chunk prefix sums of Delta A, K = C B^T
+ * masked by the decays exp(s_i - s_j) (j <= i), H the state entering the chunk
+ * and G the adjoint of the state leaving it:
+ *   dx_j = Delta_j (sum_i K[i][j] dy_i + exp(s_last - s_j) G^T B_j) + D dy_j,
+ *   dC_i, dB_j from (dy_i . x_j) times the masked decays and Delta_j, plus
+ *   exp(s_i) H dy_i and exp(s_last - s_j) Delta_j G x_j; the step sizes'
+ *   gradient through the prefix sums s; and G of the previous chunk =
+ *   exp(s_last) G + sum_i exp(s_i) C_i dy_i^T.
+ *
+ *   inputs : as ssm_ssd_fwd (x, dt, A, B, C, D, dt_bias, delta_softplus, h0),
+ *            plus dout (batch, seqlen, nheads, headdim) bf16 contiguous and
+ *            dfinal_state (batch, nheads, dstate, headdim) fp32 or NULL (zero)
+ *   dx     : (batch, seqlen, nheads, headdim), grad_dtype (bf16 or fp32)
+ *   ddt    : (batch, seqlen, nheads), grad_dtype (the gradient of dt itself,
+ *            i.e. through the softplus when delta_softplus is set)
+ *   dA     : (nheads) fp32
+ *   dB, dC : (batch, seqlen, ngroups, dstate) fp32, summed over the heads of a group
+ *   dD, ddt_bias : (nheads) fp32 or NULL (not computed); the gradients of D
+ *            and dt_bias at the given values (a NULL D or dt_bias reads as zero)
+ *   dh0    : (batch, nheads, dstate, headdim) fp32 or NULL
+ * headdim = 64; dstate in {16, 32, 64, 128}; x, B, C, dout, dx, dB and dC
+ * must be 16-byte aligned, h0, dfinal_state and dh0 too when given
+ * (SSM_ERR_MISALIGNED otherwise).  Every contraction is a bf16 tensor-core MMA with fp32
+ * accumulation; operands that are not inputs are split into a bf16 value and
+ * a bf16 residual, so results keep about 16 significant bits.  Sums over
+ * heads, batch and chunks are taken in a fixed order (bitwise reproducible).
+ * The workspace (ssm_ssd_bwd_workspace_size bytes, 256-byte aligned, owned by
+ * the caller) holds the states entering and the adjoints leaving every chunk
+ * (fp32, 2 x batch nheads ceil(seqlen/64) dstate 64 x 4 bytes), per-head dB
+ * and dC (2 x batch seqlen nheads dstate x 4 bytes) and per-chunk partial sums.
+ * Asynchronous on `stream`; no device-side waits. */
+typedef struct {
+    int64_t batch, seqlen, nheads, headdim, dstate, ngroups;
+    const void* x;
+    const void* dt;
+    const float* A;
+    const void* B;
+    const void* C;
+    const float* D;
+    const float* dt_bias;
+    int delta_softplus;
+    const float* h0;
+    const void* dout;
+    const float* dfinal_state;
+    ssm_dtype grad_dtype;
+    void* dx;
+    void* ddt;
+    float* dA;
+    float* dB;
+    float* dC;
+    float* dD;
+    float* ddt_bias;
+    float* dh0;
+} ssm_ssd_bwd_params;
+
+SSM_API size_t ssm_ssd_bwd_workspace_size(const ssm_ssd_bwd_params* p);
+SSM_API ssm_status ssm_ssd_bwd(const ssm_ssd_bwd_params* p, void* workspace, size_t workspace_bytes,
+                               ssm_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Measured unit rates for the roofline (not part of the method): FP32 lanes
  * per SM per clock through scalar FMA and through packed f32x2 FMA, and SFU
  * 2^x results per SM per clock, each from a probe kernel of independent

@@ -14,7 +14,7 @@ _EXPORTS = {
     "ssm_scan_fwd_workspace_size", "ssm_state_update", "LIB_PATH", "launch_count",
     "ssm_scan_bwd", "ssm_scan_bwd_workspace_size", "checkpoint_buffer", "checkpoint_states",
     "ssm_decode_step", "causal_conv1d_silu_bwd", "causal_conv1d_silu_bwd_workspace_size", "ssm_ssd_fwd",
-    "probe_unit_rates", "ssm_proj", "x_dt_proj", "device_status",
+    "probe_unit_rates", "ssm_proj", "x_dt_proj", "device_status", "ssm_ssd_bwd", "ssm_ssd_bwd_workspace_size",
 }
 
 

@@ -149,6 +149,16 @@ class SsdFwdParams(ctypes.Structure):
     ]
 
 
+class SsdBwdParams(ctypes.Structure):
+    _fields_ = [
+        ("batch", _i64), ("seqlen", _i64), ("nheads", _i64), ("headdim", _i64), ("dstate", _i64),
+        ("ngroups", _i64), ("x", _vp), ("dt", _vp), ("A", _vp), ("B", _vp), ("C", _vp), ("D", _vp),
+        ("dt_bias", _vp), ("delta_softplus", _int), ("h0", _vp), ("dout", _vp), ("dfinal_state", _vp),
+        ("grad_dtype", _int), ("dx", _vp), ("ddt", _vp), ("dA", _vp), ("dB", _vp), ("dC", _vp), ("dD", _vp),
+        ("ddt_bias", _vp), ("dh0", _vp),
+    ]
+
+
 class ProjParams(ctypes.Structure):
     _fields_ = [
         ("batch", _i64), ("m", _i64), ("n", _i64), ("k", _i64),
@@ -196,6 +206,10 @@ _lib.ssm_probe_unit_rates.argtypes = [ctypes.POINTER(ctypes.c_double)] * 3
 _lib.ssm_probe_unit_rates.restype = _int
 _lib.ssm_ssd_fwd.argtypes = [ctypes.POINTER(SsdFwdParams), _vp]
 _lib.ssm_ssd_fwd.restype = _int
+_lib.ssm_ssd_bwd_workspace_size.argtypes = [ctypes.POINTER(SsdBwdParams)]
+_lib.ssm_ssd_bwd_workspace_size.restype = ctypes.c_size_t
+_lib.ssm_ssd_bwd.argtypes = [ctypes.POINTER(SsdBwdParams), _vp, ctypes.c_size_t, _vp]
+_lib.ssm_ssd_bwd.restype = _int
 _lib.ssm_status_string.argtypes = [_int]
 _lib.ssm_status_string.restype = ctypes.c_char_p
 _lib.ssm_last_error.argtypes = []
@@ -708,6 +722,76 @@ def ssm_ssd_fwd(x, dt, A, B, C, *, D=None, dt_bias=None, h0=None, delta_softplus
     p.out_dtype = _dtype_code(out.dtype)
     _check(_lib.ssm_ssd_fwd(ctypes.byref(p), _stream(stream)))
     return (out, final_state) if (return_final_state or final_state is not None) else out
+
+
+def _ssd_bwd_params(x, dt, A, B, C, dout, D, dt_bias, h0, dfinal_state, delta_softplus, g) -> SsdBwdParams:
+    batch, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    p = SsdBwdParams()
+    p.batch, p.seqlen, p.nheads, p.headdim, p.dstate, p.ngroups = batch, L, H, P, N, G
+    p.x, p.dt, p.A, p.B, p.C, p.dout = _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(dout)
+    p.D, p.dt_bias, p.h0, p.dfinal_state = _ptr(D), _ptr(dt_bias), _ptr(h0), _ptr(dfinal_state)
+    p.delta_softplus = 1 if delta_softplus else 0
+    if g is not None:
+        p.grad_dtype = _dtype_code(g["dx"].dtype)
+        p.dx, p.ddt, p.dA, p.dB, p.dC = _ptr(g["dx"]), _ptr(g["ddt"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"])
+        p.dD, p.ddt_bias, p.dh0 = _ptr(g.get("dD")), _ptr(g.get("ddt_bias")), _ptr(g.get("dh0"))
+    return p
+
+
+def ssm_ssd_bwd_workspace_size(x, B) -> int:
+    """Workspace bytes ssm_ssd_bwd needs for x (batch, L, H, 64) and B (batch, L, G, N)."""
+    batch, L, H, P = x.shape
+    p = SsdBwdParams()
+    p.batch, p.seqlen, p.nheads, p.headdim, p.dstate, p.ngroups = batch, L, H, P, B.shape[3], B.shape[2]
+    return int(_lib.ssm_ssd_bwd_workspace_size(ctypes.byref(p)))
+
+
+def ssm_ssd_bwd(x, dt, A, B, C, dout, *, D=None, dt_bias=None, h0=None, dfinal_state=None,
+                delta_softplus: bool = True, grad_dtype=None, want_dh0: bool = False,
+                grads: Optional[dict] = None, workspace: Optional[torch.Tensor] = None, stream=None):
+    """Backward of ssm_ssd_fwd for the loss sum(dout * out) + sum(dfinal_state * final_state).
+    Returns a dict with dx (batch, L, H, 64) and ddt (batch, L, H) in grad_dtype (default
+    float32), dA (H,), dB, dC (batch, L, G, N), dD and ddt_bias (H,) when D / dt_bias are
+    given, and dh0 (batch, H, N, 64) when want_dh0 -- all float32 but dx, ddt.  ``grads``
+    may hold preallocated outputs under the same names."""
+    for name, t in (("x", x), ("dt", dt), ("B", B), ("C", C), ("dout", dout)):
+        _need_cuda(name, t)
+        if t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bfloat16 tensor")
+    A, D, dt_bias = _f32c("A", A), _f32c("D", D), _f32c("dt_bias", dt_bias)
+    h0, dfinal_state = _f32c("h0", h0), _f32c("dfinal_state", dfinal_state)
+    batch, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    if tuple(dout.shape) != tuple(x.shape) or tuple(dt.shape) != (batch, L, H) or tuple(C.shape) != tuple(B.shape):
+        raise ValueError("dout must match x, dt must be (batch, L, H) and B, C (batch, L, G, N)")
+    g = dict(grads or {})
+    dev = x.device
+    gd = _torch_dtype(grad_dtype or torch.float32)
+    if g.get("dx") is None:
+        g["dx"] = torch.empty(batch, L, H, P, dtype=gd, device=dev)
+    if g.get("ddt") is None:
+        g["ddt"] = torch.empty(batch, L, H, dtype=g["dx"].dtype, device=dev)
+    for k, shape in (("dA", (H,)), ("dB", (batch, L, G, N)), ("dC", (batch, L, G, N))):
+        if g.get(k) is None:
+            g[k] = torch.empty(shape, dtype=torch.float32, device=dev)
+    if D is not None and g.get("dD") is None:
+        g["dD"] = torch.empty(H, dtype=torch.float32, device=dev)
+    if dt_bias is not None and g.get("ddt_bias") is None:
+        g["ddt_bias"] = torch.empty(H, dtype=torch.float32, device=dev)
+    if want_dh0 and g.get("dh0") is None:
+        g["dh0"] = torch.empty(batch, H, N, P, dtype=torch.float32, device=dev)
+    for k in ("dA", "dB", "dC", "dD", "ddt_bias", "dh0"):
+        _f32c(k, g.get(k))
+    if g["ddt"].dtype != g["dx"].dtype:
+        raise ValueError("dx and ddt must have the same dtype")
+    p = _ssd_bwd_params(x, dt, A, B, C, dout, D, dt_bias, h0, dfinal_state, delta_softplus, g)
+    need = int(_lib.ssm_ssd_bwd_workspace_size(ctypes.byref(p)))
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    _check(_lib.ssm_ssd_bwd(ctypes.byref(p), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                            _stream(stream)))
+    return g
 
 
 def probe_unit_rates() -> dict:

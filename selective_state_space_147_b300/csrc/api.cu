@@ -353,6 +353,46 @@ ssm_status ssm_ssd_fwd(const ssm_ssd_fwd_params* p, ssm_stream_t stream) {
     return ok();
 }
 
+static ssm_status check_ssd_bwd(const ssm_ssd_bwd_params* p) {
+    if (p == nullptr) return fail(SSM_ERR_INVALID_ARG, "params is NULL");
+    if (p->batch < 1 || p->seqlen < 0 || p->nheads < 1 || p->ngroups < 1)
+        return fail(SSM_ERR_INVALID_ARG, "bad sizes");
+    if (p->headdim != 64) return fail(SSM_ERR_UNSUPPORTED, "headdim=%lld (64 supported)", (long long)p->headdim);
+    if (p->dstate != 16 && p->dstate != 32 && p->dstate != 64 && p->dstate != 128)
+        return fail(SSM_ERR_UNSUPPORTED, "dstate=%lld (16, 32, 64 or 128 supported)", (long long)p->dstate);
+    if (p->nheads % p->ngroups != 0) return fail(SSM_ERR_INVALID_ARG, "ngroups must divide nheads");
+    if (p->batch * p->nheads > 0x3fffffffLL || p->seqlen > (1LL << 31) ||
+        p->batch * p->nheads * ((p->seqlen + 63) / 64) > 0x7fffffffLL)
+        return fail(SSM_ERR_UNSUPPORTED, "sizes too large");
+    if (!dtype_ok(p->grad_dtype)) return fail(SSM_ERR_INVALID_ARG, "unknown dtype");
+    if (!p->A || !p->dA) return fail(SSM_ERR_INVALID_ARG, "A and dA are required");
+    if (p->seqlen > 0 && (!p->x || !p->dt || !p->B || !p->C || !p->dout || !p->dx || !p->ddt || !p->dB || !p->dC))
+        return fail(SSM_ERR_INVALID_ARG, "x, dt, B, C, dout, dx, ddt, dB and dC are required");
+    if (p->seqlen > 0 && ((uintptr_t)p->x | (uintptr_t)p->B | (uintptr_t)p->C | (uintptr_t)p->dout |
+                          (uintptr_t)p->dx | (uintptr_t)p->dB | (uintptr_t)p->dC) % 16 != 0)
+        return fail(SSM_ERR_MISALIGNED, "x, B, C, dout, dx, dB and dC must be 16-byte aligned");
+    if (((uintptr_t)p->h0 | (uintptr_t)p->dfinal_state | (uintptr_t)p->dh0) % 16 != 0)
+        return fail(SSM_ERR_MISALIGNED, "h0, dfinal_state and dh0 must be 16-byte aligned");
+    return SSM_OK;
+}
+
+size_t ssm_ssd_bwd_workspace_size(const ssm_ssd_bwd_params* p) {
+    if (check_ssd_bwd(p) != SSM_OK) return 0;
+    return ssm::ssd_bwd_workspace_bytes(p);
+}
+
+ssm_status ssm_ssd_bwd(const ssm_ssd_bwd_params* p, void* workspace, size_t workspace_bytes, ssm_stream_t stream) {
+    const ssm_status s = check_ssd_bwd(p);
+    if (s != SSM_OK) return s;
+    const size_t need = ssm::ssd_bwd_workspace_bytes(p);
+    if (workspace_bytes < need || (need > 0 && workspace == nullptr))
+        return fail(SSM_ERR_WORKSPACE, "workspace %zu bytes, %zu needed", workspace_bytes, need);
+    if ((uintptr_t)workspace % 256 != 0) return fail(SSM_ERR_MISALIGNED, "workspace must be 256-byte aligned");
+    cudaError_t e = ssm::launch_ssd_bwd(p, workspace, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "ssm_ssd_bwd launch");
+    return ok();
+}
+
 ssm_status ssm_proj(const ssm_proj_params* p, ssm_stream_t stream) {
     if (p == nullptr) return fail(SSM_ERR_INVALID_ARG, "params is NULL");
     if (p->batch < 1 || p->m < 1 || p->n < 1 || p->k < 1) return fail(SSM_ERR_INVALID_ARG, "bad sizes");

@@ -51,6 +51,8 @@ cudaError_t launch_conv1d_silu_bwd(const ssm_conv_bwd_params* p, void* ws, cudaS
 cudaError_t launch_decode_step(const ssm_decode_step_params* p, cudaStream_t st);
 cudaError_t launch_state_update(const ssm_state_update_params* p, cudaStream_t st);
 cudaError_t launch_ssd_fwd(const ssm_ssd_fwd_params* p, cudaStream_t st);
+size_t ssd_bwd_workspace_bytes(const ssm_ssd_bwd_params* p);
+cudaError_t launch_ssd_bwd(const ssm_ssd_bwd_params* p, void* ws, cudaStream_t st);
 cudaError_t probe_unit_rates(double* fp32, double* f32x2, double* ex2);
 cudaError_t launch_proj(const ssm_proj_params* p, cudaStream_t st);
 bool warpscan_supported(const ssm_scan_fwd_params* p);

@@ -144,6 +144,7 @@ STREAM = {
     "dout": 9, "h0": 10, "conv_state": 11, "x": 12, "dhN": 13,
     "W_x": 30, "W_dt": 31, "dt_proj_bias": 32,
     "ssd_x": 20, "ssd_dt": 21, "ssd_B": 22, "ssd_C": 23, "ssd_A": 24, "ssd_D": 25, "ssd_bias": 26, "ssd_h0": 27,
+    "ssd_dout": 28, "ssd_dhN": 29,
 }
 
 
@@ -206,6 +207,16 @@ def ssd_inputs(seed: int, batch: int, seqlen: int, nheads: int, headdim: int, ds
     g["h0"] = (normal(seed, STREAM["ssd_h0"], (batch, nheads, dstate, headdim), torch.float32, device)
                if with_h0 else None)
     return g
+
+
+def ssd_grad_inputs(seed: int, batch: int, seqlen: int, nheads: int, headdim: int, dstate: int,
+                    device="cpu", with_dhN: bool = False):
+    """The incoming gradients of one Mamba-2 layer's backward: dout (batch, L, H, P)
+    bf16 N(0, 1) and, optionally, the final state's dhN (batch, H, N, P) f32 N(0, 1)."""
+    dout = normal(seed, STREAM["ssd_dout"], (batch, seqlen, nheads, headdim), torch.bfloat16, device)
+    dhN = (normal(seed, STREAM["ssd_dhN"], (batch, nheads, dstate, headdim), torch.float32, device)
+           if with_dhN else None)
+    return dout, dhN
 
 
 def conv_inputs(seed: int, batch: int, dim: int, seqlen: int, width: int = 4,

@@ -32,7 +32,8 @@ def test_header_declares_the_entry_points():
     for must in ("ssm_scan_fwd", "ssm_scan_fwd_workspace_size", "ssm_scan_bwd", "ssm_scan_bwd_workspace_size",
                  "ssm_state_update", "ssm_decode_step", "causal_conv1d_silu_bwd",
                  "causal_conv1d_silu", "causal_conv1d_silu_update", "ssm_status_string",
-                 "ssm_last_error", "ssm_abi_version", "ssm_ssd_fwd", "ssm_probe_unit_rates"):
+                 "ssm_last_error", "ssm_abi_version", "ssm_ssd_fwd", "ssm_probe_unit_rates",
+                 "ssm_ssd_bwd", "ssm_ssd_bwd_workspace_size"):
         assert must in names
 
 
@@ -139,3 +140,31 @@ def test_ssd_host_validation_without_gpu():
     assert lib.ssm_ssd_fwd(ctypes.byref(p), None) == -1                 # groups must divide heads
     p.ngroups, p.x = 1, 264
     assert lib.ssm_ssd_fwd(ctypes.byref(p), None) == -3                 # x not 16-byte aligned
+
+
+def test_ssd_bwd_host_validation_without_gpu():
+    """ssm_ssd_bwd rejects bad shapes, unsupported sizes, missing pointers,
+    misaligned buffers and a short workspace on the host."""
+    import selective_state_space_147_b300.binding as B
+    lib = B.lib()
+    assert lib.ssm_ssd_bwd(None, None, 0, None) == -1
+    p = B.SsdBwdParams()
+    p.batch, p.seqlen, p.nheads, p.headdim, p.dstate, p.ngroups = 1, 64, 2, 64, 16, 1
+    p.A = p.dA = 256
+    assert lib.ssm_ssd_bwd(ctypes.byref(p), None, 0, None) == -1              # missing pointers
+    p.x = p.dt = p.B = p.C = p.dout = p.dx = p.ddt = p.dB = p.dC = 256
+    p.headdim = 32
+    assert lib.ssm_ssd_bwd(ctypes.byref(p), None, 0, None) == -2              # head dim 64 only
+    p.headdim, p.dstate = 64, 48
+    assert lib.ssm_ssd_bwd(ctypes.byref(p), None, 0, None) == -2              # dstate 16/32/64/128
+    p.dstate, p.ngroups = 16, 3
+    assert lib.ssm_ssd_bwd(ctypes.byref(p), None, 0, None) == -1              # groups must divide heads
+    p.ngroups, p.dout = 1, 264
+    assert lib.ssm_ssd_bwd(ctypes.byref(p), None, 0, None) == -3              # dout not 16-byte aligned
+    p.dout = 256
+    need = lib.ssm_ssd_bwd_workspace_size(ctypes.byref(p))
+    # the states entering and the adjoints leaving one chunk of 2 heads (2 x 16 x 64 x 4
+    # bytes each), per-head dB and dC (64 steps x 2 heads x 16 x 4 bytes each) and the
+    # chunk partials (3 x 2 floats), each rounded up to 256 bytes
+    assert need == 8192 + 8192 + 8192 + 8192 + 256
+    assert lib.ssm_ssd_bwd(ctypes.byref(p), None, need - 1, None) == -4      # workspace too small
