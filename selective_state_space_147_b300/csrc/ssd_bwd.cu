@@ -57,7 +57,7 @@ constexpr int kQ = 64;            // chunk length (steps)
 constexpr int kP = 64;            // head dimension
 constexpr int kLDP = kP + 8;      // padded row (bf16 elements) of a tile with 64 head-dim columns
 constexpr int kLDQ = kQ + 8;      // padded row of a Q x Q tile
-constexpr int kPassThreads = 128;
+constexpr int kPassThreads = 256;
 constexpr int kChunkThreads = 256;
 
 struct BwdArgs {
@@ -172,6 +172,29 @@ __device__ __forceinline__ void stage_rows(bf16* dst, const bf16* src, int64_t b
     }
 }
 
+// Asynchronous 16-byte copy global -> shared; nothing is read (zeros land) when !valid.
+__device__ __forceinline__ void cp16(void* dst, const void* src, bool valid) {
+    const uint32_t sa = (uint32_t)__cvta_generic_to_shared(dst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(sa), "l"(src), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int n>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(n) : "memory"); }
+
+// stage_rows by asynchronous copies (completion: cp_commit / cp_wait).
+template <int W, int NTHR>
+__device__ __forceinline__ void stage_rows_async(bf16* dst, const bf16* src, int64_t b, int64_t t0, int64_t L,
+                                                 int64_t R, int64_t r, int tid) {
+    constexpr int kPieces = W / 8;
+    for (int q = tid; q < kQ * kPieces; q += NTHR) {
+        const int row = q / kPieces, pc = q - row * kPieces;
+        const int64_t t = t0 + row;
+        const bool ok = t < L;
+        cp16(dst + row * (W + 8) + pc * 8, ok ? src + ((b * L + t) * R + r) * W + pc * 8 : src, ok);
+    }
+}
+
 // Inclusive prefix sum of v over 64 steps held by threads 0..63 (warps 0 and 1);
 // returns the prefix of the calling thread.  All threads of the block must call it.
 __device__ __forceinline__ float prefix64(float v, int tid, float* wsum) {
@@ -224,16 +247,27 @@ __device__ __forceinline__ float block_sum256(float v, float* scratch, int tid) 
 // before the update.  REV = true (chunks last to first): G = dhN, G_c =
 // exp(s_last) G_(c+1) + C^T (w o dY) with w_i = exp(s_i); G_(c+1) is written
 // before the update and the last G is dh0.
-// The N x 64 state lives in the MMA accumulators: warp w owns tiles q = w N/8
-// + i, i < N/8, tile q covering states [16 (q / 8), +16) and columns [8 (q % 8), +8).
+// The N x 64 state lives in the MMA accumulators: warp w (of 8) owns tiles
+// q = w N/16 + i, i < N/16, tile q covering states [16 (q / 8), +16) and
+// columns [8 (q % 8), +8).
+template <int N>
+struct PassSmem {
+    static constexpr int LDN = N + 8;
+    static constexpr int kV = kQ * LDN;         // V tile [step][state], two buffers
+    static constexpr int kX = kQ * kLDP;        // X tile [step][p], two buffers; weighted value, residual
+    static constexpr int kBytes = (2 * kV + 4 * kX) * 2;
+};
+
 template <int N, bool REV>
-__global__ void __launch_bounds__(kPassThreads) ssd_bwd_pass_kernel(const BwdArgs a) {
-    constexpr int LDN = N + 8;
-    constexpr int TPW = N / 8;
-    __shared__ __align__(16) bf16 Vs[kQ * LDN];
-    __shared__ __align__(16) bf16 Xh[kQ * kLDP];
-    __shared__ __align__(16) bf16 Xl[kQ * kLDP];
-    __shared__ __align__(16) bf16 Xr[kQ * kLDP];
+__global__ void __launch_bounds__(kPassThreads, 2) ssd_bwd_pass_kernel(const BwdArgs a) {
+    using S = PassSmem<N>;
+    constexpr int LDN = S::LDN;
+    constexpr int TPW = N / 16;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    bf16* Vb = reinterpret_cast<bf16*>(smem_raw);          // [2][kV]
+    bf16* Xb = Vb + 2 * S::kV;                              // [2][kX] raw X
+    bf16* Xh = Xb + 2 * S::kX;
+    bf16* Xl = Xh + S::kX;
     __shared__ float wv[kQ];
     __shared__ float wsum[2];
     __shared__ float slast_s;
@@ -259,20 +293,38 @@ __global__ void __launch_bounds__(kPassThreads) ssd_bwd_pass_kernel(const BwdArg
         }
     }
 
+    // chunk k of the walk, its tiles staged one chunk ahead
+    auto chunk_of = [&](int64_t k) { return REV ? nc - 1 - k : k; };
+    auto stage = [&](int64_t k) {
+        const int64_t t0 = chunk_of(k) * kQ;
+        const int buf = (int)(k & 1);
+        stage_rows_async<N, kPassThreads>(Vb + buf * S::kV, V, b, t0, L, a.G, grp, tid);
+        stage_rows_async<kP, kPassThreads>(Xb + buf * S::kX, X, b, t0, L, H, h, tid);
+    };
+    auto delta_of = [&](int64_t k) {
+        const int64_t t = chunk_of(k) * kQ + tid;
+        return (tid < kQ && t < L) ? step_size(a, b, t, h, bias, nullptr) : 0.f;
+    };
+    if (nc > 0) stage(0);
+    cp_commit();
+    float dl_next = nc > 0 ? delta_of(0) : 0.f;
+
     for (int64_t k = 0; k < nc; k++) {
-        const int64_t c = REV ? nc - 1 - k : k;
-        const int64_t t0 = c * kQ;
-        stage_rows<N, kPassThreads>(Vs, V, b, t0, L, a.G, grp, tid);
-        stage_rows<kP, kPassThreads>(Xr, X, b, t0, L, H, h, tid);
-        float dl = 0.f;
-        if (tid < kQ && t0 + tid < L) dl = step_size(a, b, t0 + tid, h, bias, nullptr);
+        const int64_t c = chunk_of(k);
+        const int buf = (int)(k & 1);
+        if (k + 1 < nc) stage(k + 1);
+        cp_commit();
+        const float dl = dl_next;
+        if (k + 1 < nc) dl_next = delta_of(k + 1);
         const float s = prefix64(dl * Ah, tid, wsum);
         if (tid == kQ - 1) slast_s = s;
         __syncthreads();
         const float slast = slast_s;
         if (tid < kQ) wv[tid] = REV ? expf(s) : expf(slast - s) * dl;
+        cp_wait<1>();                           // this chunk's tiles (all but the newest group)
         __syncthreads();
         // weighted X, split into bf16 value + residual
+        const bf16* Xr = Xb + buf * S::kX;
         for (int q = tid; q < kQ * kP / 2; q += kPassThreads) {
             const int row = q / (kP / 2), col = 2 * (q - row * (kP / 2));
             const float2 xv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(Xr + row * kLDP + col));
@@ -290,6 +342,7 @@ __global__ void __launch_bounds__(kPassThreads) ssd_bwd_pass_kernel(const BwdArg
 #pragma unroll
             for (int e = 0; e < 4; e++) st[i][e] *= decay;
         }
+        const bf16* Vs = Vb + buf * S::kV;
 #pragma unroll
         for (int k0 = 0; k0 < kQ; k0 += 16) {
 #pragma unroll
@@ -305,6 +358,7 @@ __global__ void __launch_bounds__(kPassThreads) ssd_bwd_pass_kernel(const BwdArg
         }
         __syncthreads();
     }
+    cp_wait<0>();
     if (REV && a.dh0 != nullptr) {
 #pragma unroll
         for (int i = 0; i < TPW; i++) {
@@ -327,7 +381,7 @@ struct ChunkSmem {
     static constexpr int kXY = kQ * kLDP;      // x, dy tiles [step][p]
     static constexpr int kS = N * kLDP;        // state tile [n][p] (value, residual)
     static constexpr int kQQ = kQ * kLDQ;      // Q x Q tiles (value, residual)
-    static constexpr int kHalves = 2 * kBC + 2 * kXY + 2 * kS + 4 * kQQ;
+    static constexpr int kHalves = 2 * kBC + 2 * kXY + 2 * kS + 2 * kQQ;
     static constexpr int kFloats = 6 * kQ + 8 * kQ + 16;
     static constexpr int kBytes = kHalves * 2 + kFloats * 4;
 };
@@ -344,11 +398,11 @@ __global__ void __launch_bounds__(kChunkThreads) ssd_bwd_chunk_kernel(const BwdA
     bf16* Ys = Xs + S::kXY;                    // dy
     bf16* Sh = Ys + S::kXY;                    // G (then H): value
     bf16* Sl = Sh + S::kS;                     //             residual
-    bf16* K1h = Sl + S::kS;                    // C B^T o L
+    bf16* K1h = Sl + S::kS;                    // C B^T o L, until Z is formed;
     bf16* K1l = K1h + S::kQQ;
-    bf16* K2h = K1l + S::kQQ;                  // (dY X^T) o L o Delta_j
-    bf16* K2l = K2h + S::kQQ;
-    float* dl = reinterpret_cast<float*>(K2l + S::kQQ);   // Delta
+    bf16* K2h = K1h;                           // then (dY X^T) o L o Delta_j in the same tile
+    bf16* K2l = K1l;
+    float* dl = reinterpret_cast<float*>(K1l + S::kQQ);   // Delta
     float* sc = dl + kQ;                       // s
     float* ex = sc + kQ;                       // exp(s)
     float* exl = ex + kQ;                      // exp(s_last - s)
@@ -395,7 +449,9 @@ __global__ void __launch_bounds__(kChunkThreads) ssd_bwd_chunk_kernel(const BwdA
     if (tid < kQ) exl[tid] = expf(slast - sc[tid]);
     __syncthreads();
 
-    // ---- P1: C B^T and dY X^T on rows i of slice rs, column tiles nt = 2 m + ch (nt <= 2 rs + 1)
+    // ---- P1: C B^T and dY X^T on rows i of slice rs, column tiles nt = 2 m + ch (nt <= 2 rs + 1);
+    // (dY X^T) o L o Delta_j stays in registers until the tile it goes to is free
+    float dcb[4][4];
     {
         float cb[4][4], yx[4][4];
 #pragma unroll
@@ -438,7 +494,8 @@ __global__ void __launch_bounds__(kChunkThreads) ssd_bwd_chunk_kernel(const BwdA
                 const float rr = yx[m][2 * hh] * k0v * dl[j] + yx[m][2 * hh + 1] * k1v * dl[j + 1];
                 if (hh == 0) r0 += rr; else r1 += rr;
                 split_store2(K1h, K1l, i * kLDQ + j, k0v, k1v);
-                split_store2(K2h, K2l, i * kLDQ + j, d0, d1);
+                dcb[m][2 * hh] = d0;
+                dcb[m][2 * hh + 1] = d1;
             }
         }
         r0 += __shfl_xor_sync(0xffffffffu, r0, 1);
@@ -552,6 +609,15 @@ __global__ void __launch_bounds__(kChunkThreads) ssd_bwd_chunk_kernel(const BwdA
         for (int m = 0; m < NH; m++) {
             db[m][0] *= f0; db[m][1] *= f0; db[m][2] *= f1; db[m][3] *= f1;
         }
+        __syncthreads();                       // every Z is formed: the Q x Q tile takes (dY X^T) o L o Delta
+#pragma unroll
+        for (int m = 0; m < 4; m++) {
+            if (m > rs) continue;
+            const int j = 8 * (2 * m + ch) + 2 * t4;
+            split_store2(K2h, K2l, (16 * rs + g) * kLDQ + j, dcb[m][0], dcb[m][1]);
+            split_store2(K2h, K2l, (16 * rs + g + 8) * kLDQ + j, dcb[m][2], dcb[m][3]);
+        }
+        __syncthreads();
         for (int k0 = 16 * rs; k0 < kQ; k0 += 16) {
             uint32_t ah[4], al[4];
             fragA_ks(ah, K2h, kLDQ, 16 * rs, k0, g, t4);
@@ -755,8 +821,12 @@ __host__ Layout layout_of(const ssm_ssd_bwd_params* p) {
 template <int N, typename Tg>
 cudaError_t launch_n(const BwdArgs& a, cudaStream_t st) {
     const unsigned units = (unsigned)(a.batch * a.H);
-    ssd_bwd_pass_kernel<N, false><<<units, kPassThreads, 0, st>>>(a);
-    ssd_bwd_pass_kernel<N, true><<<units, kPassThreads, 0, st>>>(a);
+    constexpr int psmem = PassSmem<N>::kBytes;
+    cudaError_t e0 = prepare_kernel<ssd_bwd_pass_kernel<N, false>>(psmem);
+    if (e0 == cudaSuccess) e0 = prepare_kernel<ssd_bwd_pass_kernel<N, true>>(psmem);
+    if (e0 != cudaSuccess) return e0;
+    ssd_bwd_pass_kernel<N, false><<<units, kPassThreads, psmem, st>>>(a);
+    ssd_bwd_pass_kernel<N, true><<<units, kPassThreads, psmem, st>>>(a);
     unsigned launches = 2;
     if (a.nc > 0) {
         constexpr int smem = ChunkSmem<N>::kBytes;
