@@ -504,7 +504,8 @@ SSM_API ssm_status ssm_ssd_fwd(const ssm_ssd_fwd_params* p, ssm_stream_t stream)
  * heads, batch and chunks are taken in a fixed order (bitwise reproducible).
  * The workspace (ssm_ssd_bwd_workspace_size bytes, 256-byte aligned, owned by
  * the caller) holds the states entering and the adjoints leaving every chunk
- * (fp32, 2 x batch nheads ceil(seqlen/64) dstate 64 x 4 bytes), per-head dB
+ * (each as a bf16 value and residual: 2 x batch nheads ceil(seqlen/64) dstate
+ * 64 x 4 bytes), per-head dB
  * and dC (2 x batch seqlen nheads dstate x 4 bytes) and per-chunk partial sums.
  * Asynchronous on `stream`; no device-side waits. */
 typedef struct {

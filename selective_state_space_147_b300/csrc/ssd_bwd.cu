@@ -26,9 +26,10 @@
 // plus C_i . (exp(s_i) H dy_i), so the outputs need not be recomputed.
 //
 // Three stages:
-//   1. ssd_bwd_pass_kernel, one CTA per (b, h): the forward pass writes every
-//      chunk's entering state H_c, the reverse pass every chunk's G_(c+1) and
-//      dh0.  One product per chunk (N x 64, k = 64 steps).
+//   1. ssd_bwd_pass_kernel, two CTAs per (b, h) in one grid: the forward pass
+//      writes every chunk's entering state H_c, the reverse pass every chunk's
+//      G_(c+1) and dh0.  One product per chunk (N x 64, k = 64 steps), the
+//      next chunk's tiles staged by cp.async meanwhile.
 //   2. ssd_bwd_chunk_kernel, one CTA per (b, h, chunk), all independent: the
 //      eight products above, dx, ddt, per-head dB and dC, and per-chunk
 //      partial sums of dA, dD and d(dt_bias).
@@ -82,46 +83,52 @@ struct BwdArgs {
     float* dD;            // (H) or NULL
     float* ddt_bias;      // (H) or NULL
     float* dh0;           // (batch, H, N, P) or NULL
-    float* Hc;            // workspace (batch H, nc, N, P): state entering chunk c
-    float* Gc;            // workspace (batch H, nc, N, P): adjoint of the state leaving chunk c
+    bf16* Hc;             // workspace (batch H, nc, 2, N, P): state entering chunk c, bf16 value + residual
+    bf16* Gc;             // workspace (batch H, nc, 2, N, P): adjoint of the state leaving chunk c
     float* dBp;           // workspace (batch, L, H, N): dB of each head
     float* dCp;
     float* part;          // workspace (3, batch H, nc): dA, dD, d(dt_bias) of each chunk
 };
 
-__device__ __forceinline__ uint32_t lds32(const bf16* p) { return *reinterpret_cast<const uint32_t*>(p); }
-__device__ __forceinline__ uint32_t lds_pair(const bf16* p0, const bf16* p1) {
-    return (uint32_t)__bfloat16_as_ushort(*p0) | ((uint32_t)__bfloat16_as_ushort(*p1) << 16);
+__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const bf16* p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(smem_addr(p)));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const bf16* p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(smem_addr(p)));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t (&r)[2], const bf16* p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];\n"
+                 : "=r"(r[0]), "=r"(r[1]) : "r"(smem_addr(p)));
+}
+__device__ __forceinline__ void ldsm_x2_t(uint32_t (&r)[2], const bf16* p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];\n"
+                 : "=r"(r[0]), "=r"(r[1]) : "r"(smem_addr(p)));
 }
 
 // Fragments of mma.m16n8k16 (g = lane / 4, t = lane % 4).  A (16 x 16): register
 // r holds rows g (r even) or g + 8 (r odd), columns 2t, 2t + 1 (r < 2) or
 // 2t + 8, 2t + 9.  B (16 x 8): register r holds rows 2t, 2t + 1 (+ 8 for r = 1),
 // column g.  "kc": the operand's k index is contiguous in shared memory; "ks":
-// its m (or n) index is.
+// its m (or n) index is.  Each is one ldmatrix: lanes 8 i .. 8 i + 7 give the
+// rows of 8 x 8 block i (16-byte aligned rows); .trans serves the "ks" layouts.
 __device__ __forceinline__ void fragA_kc(uint32_t (&a)[4], const bf16* s, int ld, int m0, int k0, int g, int t) {
-    const bf16* p = s + (m0 + g) * ld + k0 + 2 * t;
-    a[0] = lds32(p);
-    a[1] = lds32(p + 8 * ld);
-    a[2] = lds32(p + 8);
-    a[3] = lds32(p + 8 * ld + 8);
+    const int l = 4 * g + t;
+    ldsm_x4(a, s + (m0 + (l & 7) + 8 * ((l >> 3) & 1)) * ld + k0 + 8 * (l >> 4));
 }
 __device__ __forceinline__ void fragA_ks(uint32_t (&a)[4], const bf16* s, int ld, int m0, int k0, int g, int t) {
-    const bf16* p = s + (k0 + 2 * t) * ld + m0 + g;
-    a[0] = lds_pair(p, p + ld);
-    a[1] = lds_pair(p + 8, p + ld + 8);
-    a[2] = lds_pair(p + 8 * ld, p + 9 * ld);
-    a[3] = lds_pair(p + 8 * ld + 8, p + 9 * ld + 8);
+    const int l = 4 * g + t;
+    ldsm_x4_t(a, s + (k0 + (l & 7) + 8 * (l >> 4)) * ld + m0 + 8 * ((l >> 3) & 1));
 }
 __device__ __forceinline__ void fragB_kc(uint32_t (&b)[2], const bf16* s, int ld, int n0, int k0, int g, int t) {
-    const bf16* p = s + (n0 + g) * ld + k0 + 2 * t;
-    b[0] = lds32(p);
-    b[1] = lds32(p + 8);
+    const int l = 4 * g + t;
+    ldsm_x2(b, s + (n0 + (l & 7)) * ld + k0 + 8 * ((l >> 3) & 1));
 }
 __device__ __forceinline__ void fragB_ks(uint32_t (&b)[2], const bf16* s, int ld, int n0, int k0, int g, int t) {
-    const bf16* p = s + (k0 + 2 * t) * ld + n0 + g;
-    b[0] = lds_pair(p, p + ld);
-    b[1] = lds_pair(p + 8 * ld, p + 9 * ld);
+    const int l = 4 * g + t;
+    ldsm_x2_t(b, s + (k0 + (l & 7) + 8 * ((l >> 3) & 1)) * ld + n0);
 }
 
 // D (16 x 8, fp32) += A (16 x 16, bf16) B (16 x 8, bf16)
@@ -156,22 +163,6 @@ __device__ __forceinline__ float step_size(const BwdArgs& a, int64_t b, int64_t 
     return a.softplus ? softplus_accurate(v) : v;
 }
 
-// Copy rows [t0, t0 + 64) of a (batch, L, rows_per_step, W) bf16 tensor (row r of
-// step t at ((b L + t) R + r) W) into a padded shared tile [64][W + 8]; steps past
-// L are zero.  W is a multiple of 8 (16-byte pieces).
-template <int W, int NTHR>
-__device__ __forceinline__ void stage_rows(bf16* dst, const bf16* src, int64_t b, int64_t t0, int64_t L, int64_t R,
-                                           int64_t r, int tid) {
-    constexpr int kPieces = W / 8;
-    for (int q = tid; q < kQ * kPieces; q += NTHR) {
-        const int row = q / kPieces, pc = q - row * kPieces;
-        const int64_t t = t0 + row;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (t < L) v = *reinterpret_cast<const uint4*>(src + ((b * L + t) * R + r) * W + pc * 8);
-        *reinterpret_cast<uint4*>(dst + row * (W + 8) + pc * 8) = v;
-    }
-}
-
 // Asynchronous 16-byte copy global -> shared; nothing is read (zeros land) when !valid.
 __device__ __forceinline__ void cp16(void* dst, const void* src, bool valid) {
     const uint32_t sa = (uint32_t)__cvta_generic_to_shared(dst);
@@ -182,7 +173,10 @@ __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_grou
 template <int n>
 __device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(n) : "memory"); }
 
-// stage_rows by asynchronous copies (completion: cp_commit / cp_wait).
+// Rows [t0, t0 + 64) of a (batch, L, R, W) bf16 tensor (row r of step t at
+// ((b L + t) R + r) W) into a padded shared tile [64][W + 8], steps past L as
+// zeros, by asynchronous copies (completion: cp_commit / cp_wait).  W is a
+// multiple of 8 (16-byte pieces).
 template <int W, int NTHR>
 __device__ __forceinline__ void stage_rows_async(bf16* dst, const bf16* src, int64_t b, int64_t t0, int64_t L,
                                                  int64_t R, int64_t r, int tid) {
@@ -192,6 +186,17 @@ __device__ __forceinline__ void stage_rows_async(bf16* dst, const bf16* src, int
         const int64_t t = t0 + row;
         const bool ok = t < L;
         cp16(dst + row * (W + 8) + pc * 8, ok ? src + ((b * L + t) * R + r) * W + pc * 8 : src, ok);
+    }
+}
+
+// A state slot (N x 64 bf16 values, then their N x 64 residuals) into the padded
+// shared tiles hi[n][p], lo[n][p] by asynchronous copies.
+template <int N, int NTHR>
+__device__ __forceinline__ void stage_state_async(bf16* hi, bf16* lo, const bf16* src, int tid) {
+    for (int q = tid; q < 2 * N * (kP / 8); q += NTHR) {
+        const int half = q / (N * (kP / 8)), r = q - half * (N * (kP / 8));
+        const int n = r / (kP / 8), pc = r - n * (kP / 8);
+        cp16((half ? lo : hi) + n * kLDP + pc * 8, src + (half * N + n) * kP + pc * 8, true);
     }
 }
 
@@ -255,11 +260,12 @@ struct PassSmem {
     static constexpr int LDN = N + 8;
     static constexpr int kV = kQ * LDN;         // V tile [step][state], two buffers
     static constexpr int kX = kQ * kLDP;        // X tile [step][p], two buffers; weighted value, residual
-    static constexpr int kBytes = (2 * kV + 4 * kX) * 2;
+    static constexpr int kStg = N * kLDP;       // the state on its way out: value, residual [n][p]
+    static constexpr int kBytes = (2 * kV + 4 * kX + 2 * kStg) * 2;
 };
 
 template <int N, bool REV>
-__global__ void __launch_bounds__(kPassThreads, 2) ssd_bwd_pass_kernel(const BwdArgs a) {
+__device__ __forceinline__ void pass_body(const BwdArgs& a, const int64_t unit) {
     using S = PassSmem<N>;
     constexpr int LDN = S::LDN;
     constexpr int TPW = N / 16;
@@ -268,19 +274,20 @@ __global__ void __launch_bounds__(kPassThreads, 2) ssd_bwd_pass_kernel(const Bwd
     bf16* Xb = Vb + 2 * S::kV;                              // [2][kX] raw X
     bf16* Xh = Xb + 2 * S::kX;
     bf16* Xl = Xh + S::kX;
+    bf16* Th = Xl + S::kX;
+    bf16* Tl = Th + S::kStg;
     __shared__ float wv[kQ];
     __shared__ float wsum[2];
     __shared__ float slast_s;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
-    const int64_t unit = blockIdx.x;
     const int64_t H = a.H, L = a.L, nc = a.nc;
     const int64_t b = unit / H, h = unit - b * H, grp = h / (H / a.G);
     const float Ah = a.A[h], bias = a.dt_bias ? a.dt_bias[h] : 0.f;
     const bf16* V = REV ? a.C : a.B;
     const bf16* X = REV ? a.dout : a.x;
     const float* init = REV ? a.dhN : a.h0;
-    float* slots = REV ? a.Gc : a.Hc;
+    bf16* slots = REV ? a.Gc : a.Hc;
 
     float st[TPW][4];
 #pragma unroll
@@ -316,6 +323,14 @@ __global__ void __launch_bounds__(kPassThreads, 2) ssd_bwd_pass_kernel(const Bwd
         cp_commit();
         const float dl = dl_next;
         if (k + 1 < nc) dl_next = delta_of(k + 1);
+        // the state entering this step of the walk, split, into the staging tile
+#pragma unroll
+        for (int i = 0; i < TPW; i++) {
+            const int q = warp * TPW + i, mt = q >> 3, nt = q & 7;
+            const int n = 16 * mt + g, p = 8 * nt + 2 * t4;
+            split_store2(Th, Tl, n * kLDP + p, st[i][0], st[i][1]);
+            split_store2(Th, Tl, (n + 8) * kLDP + p, st[i][2], st[i][3]);
+        }
         const float s = prefix64(dl * Ah, tid, wsum);
         if (tid == kQ - 1) slast_s = s;
         __syncthreads();
@@ -323,6 +338,15 @@ __global__ void __launch_bounds__(kPassThreads, 2) ssd_bwd_pass_kernel(const Bwd
         if (tid < kQ) wv[tid] = REV ? expf(s) : expf(slast - s) * dl;
         cp_wait<1>();                           // this chunk's tiles (all but the newest group)
         __syncthreads();
+        {   // the staged state to its slot in 16-byte pieces
+            bf16* slot = slots + (unit * nc + c) * (int64_t)(2 * N * kP);
+            for (int q = tid; q < 2 * N * (kP / 8); q += kPassThreads) {
+                const int half = q / (N * (kP / 8)), r = q - half * (N * (kP / 8));
+                const int n = r / (kP / 8), pc = r - n * (kP / 8);
+                *reinterpret_cast<uint4*>(slot + (half * N + n) * kP + pc * 8) =
+                    *reinterpret_cast<const uint4*>((half ? Tl : Th) + n * kLDP + pc * 8);
+            }
+        }
         // weighted X, split into bf16 value + residual
         const bf16* Xr = Xb + buf * S::kX;
         for (int q = tid; q < kQ * kP / 2; q += kPassThreads) {
@@ -331,17 +355,11 @@ __global__ void __launch_bounds__(kPassThreads, 2) ssd_bwd_pass_kernel(const Bwd
             split_store2(Xh, Xl, row * kLDP + col, xv.x * wv[row], xv.y * wv[row]);
         }
         __syncthreads();
-        float* slot = slots + (unit * nc + c) * (int64_t)(N * kP);
         const float decay = expf(slast);
 #pragma unroll
-        for (int i = 0; i < TPW; i++) {
-            const int q = warp * TPW + i, mt = q >> 3, nt = q & 7;
-            const int n = 16 * mt + g, p = 8 * nt + 2 * t4;
-            *reinterpret_cast<float2*>(slot + n * kP + p) = make_float2(st[i][0], st[i][1]);
-            *reinterpret_cast<float2*>(slot + (n + 8) * kP + p) = make_float2(st[i][2], st[i][3]);
+        for (int i = 0; i < TPW; i++)
 #pragma unroll
             for (int e = 0; e < 4; e++) st[i][e] *= decay;
-        }
         const bf16* Vs = Vb + buf * S::kV;
 #pragma unroll
         for (int k0 = 0; k0 < kQ; k0 += 16) {
@@ -369,6 +387,14 @@ __global__ void __launch_bounds__(kPassThreads, 2) ssd_bwd_pass_kernel(const Bwd
             *reinterpret_cast<float2*>(d + (n + 8) * kP + p) = make_float2(st[i][2], st[i][3]);
         }
     }
+}
+
+// Both passes in one grid: blocks [0, units) walk forward, the rest backward.
+template <int N>
+__global__ void __launch_bounds__(kPassThreads, 2) ssd_bwd_pass_kernel(const BwdArgs a) {
+    const int64_t units = a.batch * a.H;
+    if ((int64_t)blockIdx.x < units) pass_body<N, false>(a, blockIdx.x);
+    else pass_body<N, true>(a, blockIdx.x - units);
 }
 
 // ---------------------------------------------------------------------------
@@ -421,20 +447,16 @@ __global__ void __launch_bounds__(kChunkThreads) ssd_bwd_chunk_kernel(const BwdA
     const int64_t b = unit / H, h = unit - b * H, grp = h / (H / a.G);
     const int64_t t0 = c * kQ;
     const float Ah = a.A[h], Dh = a.D ? a.D[h] : 0.f, bias = a.dt_bias ? a.dt_bias[h] : 0.f;
-    const float* Gsrc = a.Gc + (unit * nc + c) * (int64_t)(N * kP);
-    const float* Hsrc = a.Hc + (unit * nc + c) * (int64_t)(N * kP);
+    const bf16* Gsrc = a.Gc + (unit * nc + c) * (int64_t)(2 * N * kP);
+    const bf16* Hsrc = a.Hc + (unit * nc + c) * (int64_t)(2 * N * kP);
 
-    // ---- P0: tiles, step sizes, prefix sums, G
-    stage_rows<N, kChunkThreads>(Cs, a.C, b, t0, L, a.G, grp, tid);
-    stage_rows<N, kChunkThreads>(Bs, a.B, b, t0, L, a.G, grp, tid);
-    stage_rows<kP, kChunkThreads>(Xs, a.x, b, t0, L, H, h, tid);
-    stage_rows<kP, kChunkThreads>(Ys, a.dout, b, t0, L, H, h, tid);
-    for (int q = tid; q < N * kP / 4; q += kChunkThreads) {
-        const int n = q / (kP / 4), p = 4 * (q - n * (kP / 4));
-        const float4 v = *reinterpret_cast<const float4*>(Gsrc + n * kP + p);
-        split_store2(Sh, Sl, n * kLDP + p, v.x, v.y);
-        split_store2(Sh, Sl, n * kLDP + p + 2, v.z, v.w);
-    }
+    // ---- P0: tiles and G by asynchronous copies; step sizes and prefix sums meanwhile
+    stage_rows_async<N, kChunkThreads>(Cs, a.C, b, t0, L, a.G, grp, tid);
+    stage_rows_async<N, kChunkThreads>(Bs, a.B, b, t0, L, a.G, grp, tid);
+    stage_rows_async<kP, kChunkThreads>(Xs, a.x, b, t0, L, H, h, tid);
+    stage_rows_async<kP, kChunkThreads>(Ys, a.dout, b, t0, L, H, h, tid);
+    stage_state_async<N, kChunkThreads>(Sh, Sl, Gsrc, tid);
+    cp_commit();
     float d = 0.f, v = 0.f;
     if (tid < kQ && t0 + tid < L) d = step_size(a, b, t0 + tid, h, bias, &v);
     const float s = prefix64(d * Ah, tid, scratch);
@@ -447,6 +469,7 @@ __global__ void __launch_bounds__(kChunkThreads) ssd_bwd_chunk_kernel(const BwdA
     __syncthreads();
     const float slast = sc[kQ - 1];
     if (tid < kQ) exl[tid] = expf(slast - sc[tid]);
+    cp_wait<0>();
     __syncthreads();
 
     // ---- P1: C B^T and dY X^T on rows i of slice rs, column tiles nt = 2 m + ch (nt <= 2 rs + 1);
@@ -609,7 +632,9 @@ __global__ void __launch_bounds__(kChunkThreads) ssd_bwd_chunk_kernel(const BwdA
         for (int m = 0; m < NH; m++) {
             db[m][0] *= f0; db[m][1] *= f0; db[m][2] *= f1; db[m][3] *= f1;
         }
-        __syncthreads();                       // every Z is formed: the Q x Q tile takes (dY X^T) o L o Delta
+        __syncthreads();                       // every Z is formed: the Q x Q tile takes (dY X^T) o L o Delta,
+        stage_state_async<N, kChunkThreads>(Sh, Sl, Hsrc, tid);   // and G is used up: H comes in
+        cp_commit();
 #pragma unroll
         for (int m = 0; m < 4; m++) {
             if (m > rs) continue;
@@ -637,19 +662,29 @@ __global__ void __launch_bounds__(kChunkThreads) ssd_bwd_chunk_kernel(const BwdA
             if (tj1 < L) *reinterpret_cast<float2*>(a.dBp + ((b * L + tj1) * H + h) * N + n) = make_float2(db[m][2], db[m][3]);
         }
     }
+    cp_wait<0>();
     __syncthreads();
 
-    // ---- P3: H into the state tile (and <G, H>); rows i of slice rs: dC_i on states [ch N / 2, + N / 2)
+    // ---- P3: <G, H> (G again from global memory, H from its tile); rows i of slice rs:
+    // dC_i on states [ch N / 2, + N / 2)
     float gh = 0.f;
-    for (int q = tid; q < N * kP / 4; q += kChunkThreads) {
-        const int n = q / (kP / 4), p = 4 * (q - n * (kP / 4));
-        const float4 hv = *reinterpret_cast<const float4*>(Hsrc + n * kP + p);
-        const float4 gv = *reinterpret_cast<const float4*>(Gsrc + n * kP + p);
-        gh += hv.x * gv.x + hv.y * gv.y + hv.z * gv.z + hv.w * gv.w;
-        split_store2(Sh, Sl, n * kLDP + p, hv.x, hv.y);
-        split_store2(Sh, Sl, n * kLDP + p + 2, hv.z, hv.w);
+    for (int q = tid; q < N * (kP / 8); q += kChunkThreads) {
+        const int n = q / (kP / 8), p = 8 * (q - n * (kP / 8));
+        const uint4 g_hi = *reinterpret_cast<const uint4*>(Gsrc + n * kP + p);
+        const uint4 g_lo = *reinterpret_cast<const uint4*>(Gsrc + (N + n) * kP + p);
+        const uint4 h_hi = *reinterpret_cast<const uint4*>(Sh + n * kLDP + p);
+        const uint4 h_lo = *reinterpret_cast<const uint4*>(Sl + n * kLDP + p);
+        const __nv_bfloat162* gh2 = reinterpret_cast<const __nv_bfloat162*>(&g_hi);
+        const __nv_bfloat162* gl2 = reinterpret_cast<const __nv_bfloat162*>(&g_lo);
+        const __nv_bfloat162* hh2 = reinterpret_cast<const __nv_bfloat162*>(&h_hi);
+        const __nv_bfloat162* hl2 = reinterpret_cast<const __nv_bfloat162*>(&h_lo);
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            const float2 gv = __bfloat1622float2(gh2[e]), gr = __bfloat1622float2(gl2[e]);
+            const float2 hv = __bfloat1622float2(hh2[e]), hr = __bfloat1622float2(hl2[e]);
+            gh += (gv.x + gr.x) * (hv.x + hr.x) + (gv.y + gr.y) * (hv.y + hr.y);
+        }
     }
-    __syncthreads();
     {
         float dc[NH][4];
 #pragma unroll
@@ -822,12 +857,10 @@ template <int N, typename Tg>
 cudaError_t launch_n(const BwdArgs& a, cudaStream_t st) {
     const unsigned units = (unsigned)(a.batch * a.H);
     constexpr int psmem = PassSmem<N>::kBytes;
-    cudaError_t e0 = prepare_kernel<ssd_bwd_pass_kernel<N, false>>(psmem);
-    if (e0 == cudaSuccess) e0 = prepare_kernel<ssd_bwd_pass_kernel<N, true>>(psmem);
+    cudaError_t e0 = prepare_kernel<ssd_bwd_pass_kernel<N>>(psmem);
     if (e0 != cudaSuccess) return e0;
-    ssd_bwd_pass_kernel<N, false><<<units, kPassThreads, psmem, st>>>(a);
-    ssd_bwd_pass_kernel<N, true><<<units, kPassThreads, psmem, st>>>(a);
-    unsigned launches = 2;
+    ssd_bwd_pass_kernel<N><<<2 * units, kPassThreads, psmem, st>>>(a);
+    unsigned launches = 1;
     if (a.nc > 0) {
         constexpr int smem = ChunkSmem<N>::kBytes;
         cudaError_t e = prepare_kernel<ssd_bwd_chunk_kernel<N, Tg>>(smem);
@@ -886,8 +919,8 @@ cudaError_t launch_ssd_bwd(const ssm_ssd_bwd_params* p, void* ws, cudaStream_t s
     a.dD = p->dD;
     a.ddt_bias = p->ddt_bias;
     a.dh0 = p->dh0;
-    a.Hc = reinterpret_cast<float*>(w + l.hc);
-    a.Gc = reinterpret_cast<float*>(w + l.gc);
+    a.Hc = reinterpret_cast<bf16*>(w + l.hc);
+    a.Gc = reinterpret_cast<bf16*>(w + l.gc);
     a.dBp = reinterpret_cast<float*>(w + l.dbp);
     a.dCp = reinterpret_cast<float*>(w + l.dcp);
     a.part = reinterpret_cast<float*>(w + l.part);
