@@ -369,6 +369,74 @@ def bench_ssd(L, device, cfg, reps: int = 10):
             "peaks": f"HBM {hbm} GB/s, bf16 tensor {tpk} TFLOP/s ({tsrc}, burst)"}
 
 
+def ssd_bwd_cpu_baseline(cfg, heads: int = 8):
+    """The fp64 oracle's SSD backward (the adjoint of the recurrence) on a bounded
+    sample of the same layer: ``heads`` heads of batch row 0 over the full
+    sequence, split over the host threads; reported as tokens/s of the whole layer."""
+    import time
+    import oracle
+    import synthetic as S
+    T, H, P, N, G = (cfg[k] for k in ("seqlen", "nheads", "headdim", "dstate", "ngroups"))
+    if G != 1:
+        raise ValueError("a sample of heads keeps each head's B/C group only with one group")
+    g = S.ssd_inputs(S.config_seed(6), 1, T, H, P, N, G, with_h0=True)
+    dout, dh = S.ssd_grad_inputs(S.config_seed(6), 1, T, H, P, N, with_dhN=True)
+    pick = lambda t: t[:, :, :heads]
+    threads = min(heads, oracle.default_threads())
+    t0 = time.perf_counter()
+    oracle.ssd_bwd(pick(g["x"]), pick(g["dt"]), g["A"][:heads], g["B"], g["C"], pick(dout), g["D"][:heads],
+                   g["dt_bias"][:heads], g["h0"][:, :heads], dh[:, :heads], threads=threads)
+    wall = time.perf_counter() - t0
+    return {"value": round(T * heads / H / wall, 1), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{heads} of {H} heads of batch row 0, full L={T}, fp64 adjoint of the recurrence "
+                      f"({wall:.2f} s wall on {threads} threads)"}
+
+
+def bench_ssd_bwd(L, device, cfg, reps: int = 10):
+    """Mamba-2 state-space-duality layer backward (ssm_ssd_bwd), bf16 inputs and
+    incoming gradient, bf16 dx / ddt, fp32 dB, dC, dA, dD, d(dt_bias), dh0:
+    milliseconds per call against its algorithmic HBM bytes (x, dt, B, C, dout in;
+    dx, ddt, dB, dC out) and the tensor FLOPs of the chunked adjoint at the
+    kernels' chunk length of 64 (C B^T, dY X^T, K^T dY, B G, the two intra and two
+    state products of dB and dC, and the two state passes; full blocks) against
+    the measured copy bandwidth and bf16 tensor peak.  An L2-sized buffer is
+    written between timed calls."""
+    import synthetic as S
+    b, T, H, P, N, G = (cfg[k] for k in ("batch", "seqlen", "nheads", "headdim", "dstate", "ngroups"))
+    Q = 64
+    g = S.ssd_inputs(S.config_seed(6), b, T, H, P, N, G, device=device, with_h0=True)
+    dout, dh = S.ssd_grad_inputs(S.config_seed(6), b, T, H, P, N, device=device, with_dhN=True)
+    ws = torch.empty(L.ssm_ssd_bwd_workspace_size(g["x"], g["B"]), dtype=torch.uint8, device=device)
+    kw = dict(D=g["D"], dt_bias=g["dt_bias"], h0=g["h0"], dfinal_state=dh, grad_dtype=torch.bfloat16,
+              want_dh0=True, workspace=ws)
+    grads = L.ssm_ssd_bwd(g["x"], g["dt"], g["A"], g["B"], g["C"], dout, **kw)
+
+    def call():
+        L.ssm_ssd_bwd(g["x"], g["dt"], g["A"], g["B"], g["C"], dout, grads=grads, **kw)
+
+    torch.cuda.synchronize()
+    ms = time_calls(call, reps, L2Flush(device))
+    nbytes = b * T * (H * (3 * P * 2 + 2 * 2) + G * N * (2 * 2 + 2 * 4))
+    flops = b * H * T * (6 * Q * N + 4 * Q * P + 12 * N * P)
+    hbm, _ = measured_peaks()
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            tpk, tsrc = float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        tpk, tsrc = 1800.0, "fallback"
+    gbs, tfl = nbytes / (ms * 1e-3) / 1e9, flops / (ms * 1e-3) / 1e12
+    t_hbm, t_tc = nbytes / (hbm * 1e9), flops / (tpk * 1e12)
+    return {"workload": f"mamba2-2.7b-layer SSD backward (batch {b}, L {T}, {H} heads x {P}, d_state {N}, "
+                        f"{G} B/C group, chunk {Q}, bf16 inputs and dx, inputs larger than L2)",
+            "ms": round(ms, 4), "tokens_per_s": round(b * T / (ms * 1e-3), 1),
+            "bytes": nbytes, "flops": flops,
+            "hbm_gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm, 4),
+            "tensor_tflops": round(tfl, 2), "tensor_frac": round(tfl / tpk, 4),
+            "bound": "hbm" if t_hbm >= t_tc else "tensor",
+            "roofline_frac": round(max(t_hbm, t_tc) / (ms * 1e-3), 4),
+            "peaks": f"HBM {hbm} GB/s, bf16 tensor {tpk} TFLOP/s ({tsrc}, burst)"}
+
+
 class L2Flush:
     """Writes a buffer four times the size of L2 (126 MB) between timed launches."""
 
@@ -715,6 +783,8 @@ def main(argv=None):
                     help="time only the x_proj / dt_proj products at --seqlen (for profiling captures)")
     ap.add_argument("--ssd-only", action="store_true",
                     help="time only the Mamba-2 SSD forward (for profiling captures)")
+    ap.add_argument("--ssd-bwd-only", action="store_true",
+                    help="time only the Mamba-2 SSD backward (for profiling captures)")
     ap.add_argument("--e2e-steps", type=int, default=12)
     ap.add_argument("--seqlen", type=int, default=0,
                     help="shorter sequence for small profiling captures (the headline uses the default)")
@@ -739,6 +809,9 @@ def main(argv=None):
         return 0
     if args.ssd_only:
         print(json.dumps({"ssd": bench_ssd(L, device, SSD, reps=3)}), flush=True)
+        return 0
+    if args.ssd_bwd_only:
+        print(json.dumps({"ssd_bwd": bench_ssd_bwd(L, device, SSD, reps=3)}), flush=True)
         return 0
     seed = S.config_seed(2) + 1000 * rank          # every rank its own batch (weak scaling)
     g = make_inputs(device, seed, cfg)
@@ -904,12 +977,15 @@ def main(argv=None):
         decode = bench_decode(L, device, dcfg, dcfg["steps"])
         decode["us_per_token_step"] = max_over_ranks(decode["us_per_token_step"], world, device)
 
-    ssd = None
+    ssd = ssd_bwd = None
     if not args.no_ssd:
         torch.cuda.empty_cache()
         ssd = bench_ssd(L, device, SSD)
+        torch.cuda.empty_cache()
+        ssd_bwd = bench_ssd_bwd(L, device, SSD)
         if rank == 0 and not args.no_cpu_baseline:
             ssd["cpu_baseline"] = ssd_cpu_baseline(SSD)
+            ssd_bwd["cpu_baseline"] = ssd_bwd_cpu_baseline(SSD)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -927,7 +1003,7 @@ def main(argv=None):
             "fwd_roofline_frac": fwd_plain["roofline"]["frac"],
             "fwd_hbm_frac": fwd_plain["roofline"]["hbm_frac"],
             "fwd_plain": fwd_plain, "configs": configs, "x_dt_proj": proj,
-            "decode": decode, "ssd": ssd, "cpu_baseline": cpu, "e2e": e2e,
+            "decode": decode, "ssd": ssd, "ssd_bwd": ssd_bwd, "cpu_baseline": cpu, "e2e": e2e,
             "clocks": clocks, "gpu_launches": launches, "gpu": props.name, "unit_rates": unit_rates,
         }
         print(json.dumps(line), flush=True)

@@ -140,6 +140,52 @@ __device__ __forceinline__ void mma(float (&d)[4], const uint32_t (&a)[4], const
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
+// B fragments of the two n-tiles at n0 and n0 + step in one ldmatrix.x4 (layouts as fragB_*).
+__device__ __forceinline__ void fragB2_kc(uint32_t (&b)[2][2], const bf16* s, int ld, int n0, int step, int k0, int g,
+                                          int t) {
+    const int l = 4 * g + t;
+    uint32_t r[4];
+    ldsm_x4(r, s + (n0 + (l & 7) + step * (l >> 4)) * ld + k0 + 8 * ((l >> 3) & 1));
+    b[0][0] = r[0]; b[0][1] = r[1]; b[1][0] = r[2]; b[1][1] = r[3];
+}
+__device__ __forceinline__ void fragB2_ks(uint32_t (&b)[2][2], const bf16* s, int ld, int n0, int step, int k0, int g,
+                                          int t) {
+    const int l = 4 * g + t;
+    uint32_t r[4];
+    ldsm_x4_t(r, s + (k0 + (l & 7) + 8 * ((l >> 3) & 1)) * ld + n0 + step * (l >> 4));
+    b[0][0] = r[0]; b[0][1] = r[1]; b[1][0] = r[2]; b[1][1] = r[3];
+}
+
+// acc[m] += a1 B_m (+ a2 B_m when TWO) for the M n-tiles B_m at columns base + 8 m of
+// one 16-step (k) slice; B fragments two n-tiles per load.
+template <int M, bool KC, bool TWO>
+__device__ __forceinline__ void mma_row(float (&acc)[M][4], const uint32_t (&a1)[4], const uint32_t (&a2)[4],
+                                        const bf16* s, int ld, int base, int k0, int g, int t) {
+    if constexpr (M % 2 == 0) {
+#pragma unroll
+        for (int m = 0; m < M; m += 2) {
+            uint32_t bb[2][2];
+            if constexpr (KC) fragB2_kc(bb, s, ld, base + 8 * m, 8, k0, g, t);
+            else fragB2_ks(bb, s, ld, base + 8 * m, 8, k0, g, t);
+            mma(acc[m], a1, bb[0]);
+            mma(acc[m + 1], a1, bb[1]);
+            if constexpr (TWO) {
+                mma(acc[m], a2, bb[0]);
+                mma(acc[m + 1], a2, bb[1]);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int m = 0; m < M; m++) {
+            uint32_t bb[2];
+            if constexpr (KC) fragB_kc(bb, s, ld, base + 8 * m, k0, g, t);
+            else fragB_ks(bb, s, ld, base + 8 * m, k0, g, t);
+            mma(acc[m], a1, bb);
+            if constexpr (TWO) mma(acc[m], a2, bb);
+        }
+    }
+}
+
 __device__ __forceinline__ void store1(float* p, float v) { *p = v; }
 __device__ __forceinline__ void store1(bf16* p, float v) { *p = __float2bfloat16_rn(v); }
 __device__ __forceinline__ void store2(float* p, float v0, float v1) {
@@ -278,7 +324,6 @@ __device__ __forceinline__ void pass_body(const BwdArgs& a, const int64_t unit) 
     bf16* Tl = Th + S::kStg;
     __shared__ float wv[kQ];
     __shared__ float wsum[2];
-    __shared__ float slast_s;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
     const int64_t H = a.H, L = a.L, nc = a.nc;
@@ -332,9 +377,7 @@ __device__ __forceinline__ void pass_body(const BwdArgs& a, const int64_t unit) 
             split_store2(Th, Tl, (n + 8) * kLDP + p, st[i][2], st[i][3]);
         }
         const float s = prefix64(dl * Ah, tid, wsum);
-        if (tid == kQ - 1) slast_s = s;
-        __syncthreads();
-        const float slast = slast_s;
+        const float slast = wsum[0] + wsum[1];   // the prefix at the chunk's last step
         if (tid < kQ) wv[tid] = REV ? expf(s) : expf(slast - s) * dl;
         cp_wait<1>();                           // this chunk's tiles (all but the newest group)
         __syncthreads();
@@ -361,18 +404,14 @@ __device__ __forceinline__ void pass_body(const BwdArgs& a, const int64_t unit) 
 #pragma unroll
             for (int e = 0; e < 4; e++) st[i][e] *= decay;
         const bf16* Vs = Vb + buf * S::kV;
+        // a warp's tiles share their 16 states (TPW divides 8): one A fragment per k slice
+        const int mt0 = (warp * TPW) >> 3, nt0 = (warp * TPW) & 7;
 #pragma unroll
         for (int k0 = 0; k0 < kQ; k0 += 16) {
-#pragma unroll
-            for (int i = 0; i < TPW; i++) {
-                const int q = warp * TPW + i, mt = q >> 3, nt = q & 7;
-                uint32_t af[4], bh[2], bl[2];
-                fragA_ks(af, Vs, LDN, 16 * mt, k0, g, t4);
-                fragB_ks(bh, Xh, kLDP, 8 * nt, k0, g, t4);
-                fragB_ks(bl, Xl, kLDP, 8 * nt, k0, g, t4);
-                mma(st[i], af, bh);
-                mma(st[i], af, bl);
-            }
+            uint32_t af[4];
+            fragA_ks(af, Vs, LDN, 16 * mt0, k0, g, t4);
+            mma_row<TPW, false, false>(st, af, af, Xh, kLDP, 8 * nt0, k0, g, t4);
+            mma_row<TPW, false, false>(st, af, af, Xl, kLDP, 8 * nt0, k0, g, t4);
         }
         __syncthreads();
     }
@@ -481,23 +520,32 @@ __global__ void __launch_bounds__(kChunkThreads) ssd_bwd_chunk_kernel(const BwdA
         for (int m = 0; m < 4; m++)
 #pragma unroll
             for (int e = 0; e < 4; e++) cb[m][e] = yx[m][e] = 0.f;
+        // tiles m and m + 1 (columns 16 m + 8 ch and 16 m + 16 + 8 ch) per B load; a tile
+        // right of the diagonal block (m > rs) is loaded (in bounds) but not multiplied
 #pragma unroll
-        for (int m = 0; m < 4; m++) {
-            if (m > rs) continue;
-            const int nt = 2 * m + ch;
+        for (int k0 = 0; k0 < N; k0 += 16) {
+            uint32_t af[4];
+            fragA_kc(af, Cs, LDN, 16 * rs, k0, g, t4);
 #pragma unroll
-            for (int k0 = 0; k0 < N; k0 += 16) {
-                uint32_t af[4], bfr[2];
-                fragA_kc(af, Cs, LDN, 16 * rs, k0, g, t4);
-                fragB_kc(bfr, Bs, LDN, 8 * nt, k0, g, t4);
-                mma(cb[m], af, bfr);
+            for (int m = 0; m < 4; m += 2) {
+                if (m > rs) continue;
+                uint32_t bb[2][2];
+                fragB2_kc(bb, Bs, LDN, 16 * m + 8 * ch, 16, k0, g, t4);
+                mma(cb[m], af, bb[0]);
+                if (m + 1 <= rs) mma(cb[m + 1], af, bb[1]);
             }
+        }
 #pragma unroll
-            for (int k0 = 0; k0 < kP; k0 += 16) {
-                uint32_t af[4], bfr[2];
-                fragA_kc(af, Ys, kLDP, 16 * rs, k0, g, t4);
-                fragB_kc(bfr, Xs, kLDP, 8 * nt, k0, g, t4);
-                mma(yx[m], af, bfr);
+        for (int k0 = 0; k0 < kP; k0 += 16) {
+            uint32_t af[4];
+            fragA_kc(af, Ys, kLDP, 16 * rs, k0, g, t4);
+#pragma unroll
+            for (int m = 0; m < 4; m += 2) {
+                if (m > rs) continue;
+                uint32_t bb[2][2];
+                fragB2_kc(bb, Xs, kLDP, 16 * m + 8 * ch, 16, k0, g, t4);
+                mma(yx[m], af, bb[0]);
+                if (m + 1 <= rs) mma(yx[m + 1], af, bb[1]);
             }
         }
         float r0 = 0.f, r1 = 0.f;
@@ -532,6 +580,7 @@ __global__ void __launch_bounds__(kChunkThreads) ssd_bwd_chunk_kernel(const BwdA
     }
     __syncthreads();
 
+    float dc[NH][4];                           // dC of rows i of slice rs, states [ch N / 2, + N / 2)
     // ---- P2: rows j of slice rs.  W = exp(s_last - s_j) B_j G and Z = K^T dY on columns
     // [32 ch, 32 ch + 32); dx; then dB_j on states [ch N / 2, + N / 2).
     {
@@ -544,14 +593,8 @@ __global__ void __launch_bounds__(kChunkThreads) ssd_bwd_chunk_kernel(const BwdA
         for (int k0 = 0; k0 < N; k0 += 16) {
             uint32_t af[4];
             fragA_kc(af, Bs, LDN, 16 * rs, k0, g, t4);
-#pragma unroll
-            for (int m = 0; m < 4; m++) {
-                uint32_t bh[2], bl[2];
-                fragB_ks(bh, Sh, kLDP, 32 * ch + 8 * m, k0, g, t4);
-                fragB_ks(bl, Sl, kLDP, 32 * ch + 8 * m, k0, g, t4);
-                mma(zw[m], af, bh);
-                mma(zw[m], af, bl);
-            }
+            mma_row<4, false, false>(zw, af, af, Sh, kLDP, 32 * ch, k0, g, t4);
+            mma_row<4, false, false>(zw, af, af, Sl, kLDP, 32 * ch, k0, g, t4);
         }
         const int j0 = 16 * rs + g, j1 = j0 + 8;
         const float e0 = exl[j0], e1 = exl[j1];
@@ -569,13 +612,7 @@ __global__ void __launch_bounds__(kChunkThreads) ssd_bwd_chunk_kernel(const BwdA
             uint32_t ah[4], al[4];
             fragA_ks(ah, K1h, kLDQ, 16 * rs, k0, g, t4);
             fragA_ks(al, K1l, kLDQ, 16 * rs, k0, g, t4);
-#pragma unroll
-            for (int m = 0; m < 4; m++) {
-                uint32_t bfr[2];
-                fragB_ks(bfr, Ys, kLDP, 32 * ch + 8 * m, k0, g, t4);
-                mma(zw[m], ah, bfr);
-                mma(zw[m], al, bfr);
-            }
+            mma_row<4, false, true>(zw, ah, al, Ys, kLDP, 32 * ch, k0, g, t4);
         }
         float q0 = 0.f, q1 = 0.f;
         const float dl0 = dl[j0], dl1 = dl[j1];
@@ -618,14 +655,8 @@ __global__ void __launch_bounds__(kChunkThreads) ssd_bwd_chunk_kernel(const BwdA
         for (int k0 = 0; k0 < kP; k0 += 16) {
             uint32_t af[4];
             fragA_kc(af, Xs, kLDP, 16 * rs, k0, g, t4);
-#pragma unroll
-            for (int m = 0; m < NH; m++) {
-                uint32_t bh[2], bl[2];
-                fragB_kc(bh, Sh, kLDP, ch * (N / 2) + 8 * m, k0, g, t4);
-                fragB_kc(bl, Sl, kLDP, ch * (N / 2) + 8 * m, k0, g, t4);
-                mma(db[m], af, bh);
-                mma(db[m], af, bl);
-            }
+            mma_row<NH, true, false>(db, af, af, Sh, kLDP, ch * (N / 2), k0, g, t4);
+            mma_row<NH, true, false>(db, af, af, Sl, kLDP, ch * (N / 2), k0, g, t4);
         }
         const float f0 = e0 * dl0, f1 = e1 * dl1;
 #pragma unroll
@@ -647,19 +678,25 @@ __global__ void __launch_bounds__(kChunkThreads) ssd_bwd_chunk_kernel(const BwdA
             uint32_t ah[4], al[4];
             fragA_ks(ah, K2h, kLDQ, 16 * rs, k0, g, t4);
             fragA_ks(al, K2l, kLDQ, 16 * rs, k0, g, t4);
-#pragma unroll
-            for (int m = 0; m < NH; m++) {
-                uint32_t bfr[2];
-                fragB_ks(bfr, Cs, LDN, ch * (N / 2) + 8 * m, k0, g, t4);
-                mma(db[m], ah, bfr);
-                mma(db[m], al, bfr);
-            }
+            mma_row<NH, false, true>(db, ah, al, Cs, LDN, ch * (N / 2), k0, g, t4);
         }
 #pragma unroll
         for (int m = 0; m < NH; m++) {
             const int n = ch * (N / 2) + 8 * m + 2 * t4;
             if (tj0 < L) *reinterpret_cast<float2*>(a.dBp + ((b * L + tj0) * H + h) * N + n) = make_float2(db[m][0], db[m][1]);
             if (tj1 < L) *reinterpret_cast<float2*>(a.dBp + ((b * L + tj1) * H + h) * N + n) = make_float2(db[m][2], db[m][3]);
+        }
+        // dC_i's intra-chunk part (rows i of slice rs) in the same phase: its causal shape
+        // mirrors dB's, so every warp does the same number of products here
+#pragma unroll
+        for (int m = 0; m < NH; m++)
+#pragma unroll
+            for (int e = 0; e < 4; e++) dc[m][e] = 0.f;
+        for (int k0 = 0; k0 <= 16 * rs; k0 += 16) {
+            uint32_t ah[4], al[4];
+            fragA_kc(ah, K2h, kLDQ, 16 * rs, k0, g, t4);
+            fragA_kc(al, K2l, kLDQ, 16 * rs, k0, g, t4);
+            mma_row<NH, false, true>(dc, ah, al, Bs, LDN, ch * (N / 2), k0, g, t4);
         }
     }
     cp_wait<0>();
@@ -686,23 +723,17 @@ __global__ void __launch_bounds__(kChunkThreads) ssd_bwd_chunk_kernel(const BwdA
         }
     }
     {
-        float dc[NH][4];
+        float hs[NH][4];                       // exp(s_i) H dy_i
 #pragma unroll
         for (int m = 0; m < NH; m++)
 #pragma unroll
-            for (int e = 0; e < 4; e++) dc[m][e] = 0.f;
+            for (int e = 0; e < 4; e++) hs[m][e] = 0.f;
 #pragma unroll
         for (int k0 = 0; k0 < kP; k0 += 16) {
             uint32_t af[4];
             fragA_kc(af, Ys, kLDP, 16 * rs, k0, g, t4);
-#pragma unroll
-            for (int m = 0; m < NH; m++) {
-                uint32_t bh[2], bl[2];
-                fragB_kc(bh, Sh, kLDP, ch * (N / 2) + 8 * m, k0, g, t4);
-                fragB_kc(bl, Sl, kLDP, ch * (N / 2) + 8 * m, k0, g, t4);
-                mma(dc[m], af, bh);
-                mma(dc[m], af, bl);
-            }
+            mma_row<NH, true, false>(hs, af, af, Sh, kLDP, ch * (N / 2), k0, g, t4);
+            mma_row<NH, true, false>(hs, af, af, Sl, kLDP, ch * (N / 2), k0, g, t4);
         }
         const int i0 = 16 * rs + g, i1 = i0 + 8;
         const float e0 = ex[i0], e1 = ex[i1];
@@ -710,11 +741,13 @@ __global__ void __launch_bounds__(kChunkThreads) ssd_bwd_chunk_kernel(const BwdA
 #pragma unroll
         for (int m = 0; m < NH; m++) {
             const int n = ch * (N / 2) + 8 * m + 2 * t4;
-            dc[m][0] *= e0; dc[m][1] *= e0; dc[m][2] *= e1; dc[m][3] *= e1;
+            hs[m][0] *= e0; hs[m][1] *= e0; hs[m][2] *= e1; hs[m][3] *= e1;
             const float2 c0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(Cs + i0 * LDN + n));
             const float2 c1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(Cs + i1 * LDN + n));
-            o0 += c0.x * dc[m][0] + c0.y * dc[m][1];
-            o1 += c1.x * dc[m][2] + c1.y * dc[m][3];
+            o0 += c0.x * hs[m][0] + c0.y * hs[m][1];
+            o1 += c1.x * hs[m][2] + c1.y * hs[m][3];
+#pragma unroll
+            for (int e = 0; e < 4; e++) dc[m][e] += hs[m][e];
         }
 #pragma unroll
         for (int o = 1; o <= 2; o <<= 1) {
@@ -724,18 +757,6 @@ __global__ void __launch_bounds__(kChunkThreads) ssd_bwd_chunk_kernel(const BwdA
         if (t4 == 0) {
             red_o[ch * kQ + i0] = o0;
             red_o[ch * kQ + i1] = o1;
-        }
-        for (int k0 = 0; k0 <= 16 * rs; k0 += 16) {
-            uint32_t ah[4], al[4];
-            fragA_kc(ah, K2h, kLDQ, 16 * rs, k0, g, t4);
-            fragA_kc(al, K2l, kLDQ, 16 * rs, k0, g, t4);
-#pragma unroll
-            for (int m = 0; m < NH; m++) {
-                uint32_t bfr[2];
-                fragB_ks(bfr, Bs, LDN, ch * (N / 2) + 8 * m, k0, g, t4);
-                mma(dc[m], ah, bfr);
-                mma(dc[m], al, bfr);
-            }
         }
         const int64_t ti0 = t0 + i0, ti1 = t0 + i1;
 #pragma unroll
