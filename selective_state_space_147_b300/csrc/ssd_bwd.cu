@@ -83,8 +83,9 @@ struct BwdArgs {
     float* dD;            // (H) or NULL
     float* ddt_bias;      // (H) or NULL
     float* dh0;           // (batch, H, N, P) or NULL
-    bf16* Hc;             // workspace (batch H, nc, 2, N, P): state entering chunk c, bf16 value + residual
-    bf16* Gc;             // workspace (batch H, nc, 2, N, P): adjoint of the state leaving chunk c
+    bf16* Hc;             // workspace (batch H, nc, slot): state entering chunk c, bf16 value + residual
+    bf16* Gc;             // workspace (batch H, nc, slot): adjoint of the state leaving chunk c
+                          // slot: N/2 accumulator tiles x 32 lanes x 16 bytes (see pass_body)
     float* dBp;           // workspace (batch, L, H, N): dB of each head
     float* dCp;
     float* part;          // workspace (3, batch H, nc): dA, dD, d(dt_bias) of each chunk
@@ -195,6 +196,15 @@ __device__ __forceinline__ void store2(bf16* p, float v0, float v1) {
     *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(v0, v1);
 }
 
+// (v0, v1) -> packed bf16 values (v0 in the low half) and packed bf16 residuals
+__device__ __forceinline__ void split_pair(float v0, float v1, uint32_t& hi, uint32_t& lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(v0, v1);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 r = __floats2bfloat162_rn(v0 - hf.x, v1 - hf.y);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = *reinterpret_cast<const uint32_t*>(&r);
+}
+
 // (v0, v1) -> bf16 values at hi[i], hi[i + 1] and their rounding residuals at lo[i], lo[i + 1]
 __device__ __forceinline__ void split_store2(bf16* hi, bf16* lo, int i, float v0, float v1) {
     const __nv_bfloat162 h = __floats2bfloat162_rn(v0, v1);
@@ -235,14 +245,31 @@ __device__ __forceinline__ void stage_rows_async(bf16* dst, const bf16* src, int
     }
 }
 
-// A state slot (N x 64 bf16 values, then their N x 64 residuals) into the padded
-// shared tiles hi[n][p], lo[n][p] by asynchronous copies.
-template <int N, int NTHR>
-__device__ __forceinline__ void stage_state_async(bf16* hi, bf16* lo, const bf16* src, int tid) {
-    for (int q = tid; q < 2 * N * (kP / 8); q += NTHR) {
-        const int half = q / (N * (kP / 8)), r = q - half * (N * (kP / 8));
-        const int n = r / (kP / 8), pc = r - n * (kP / 8);
-        cp16((half ? lo : hi) + n * kLDP + pc * 8, src + (half * N + n) * kP + pc * 8, true);
+// A state slot is in the layout of the MMA accumulators that produced it: for tile q
+// (16 states from 16 (q / 8), 8 columns from 8 (q % 8)) and lane l (g = l / 4,
+// t = l % 4), 16 bytes = {value, residual} of (row g, columns 2t, 2t + 1), then of
+// row g + 8.  Thread tid of the chunk kernel handles pieces tid + 256 j.
+template <int N>
+__device__ __forceinline__ void load_state_pieces(uint4 (&v)[N / 16], const bf16* src, int tid) {
+#pragma unroll
+    for (int j = 0; j < N / 16; j++) v[j] = __ldcg(reinterpret_cast<const uint4*>(src + (int64_t)(tid + 256 * j) * 8));
+}
+__device__ __forceinline__ void piece_position(int q, int& n, int& p) {
+    const int tile = q >> 5, l = q & 31;
+    n = 16 * (tile >> 3) + (l >> 2);
+    p = 8 * (tile & 7) + 2 * (l & 3);
+}
+// the pieces into the padded shared tiles hi[n][p], lo[n][p]
+template <int N>
+__device__ __forceinline__ void store_state_pieces(bf16* hi, bf16* lo, const uint4 (&v)[N / 16], int tid) {
+#pragma unroll
+    for (int j = 0; j < N / 16; j++) {
+        int n, p;
+        piece_position(tid + 256 * j, n, p);
+        *reinterpret_cast<uint32_t*>(hi + n * kLDP + p) = v[j].x;
+        *reinterpret_cast<uint32_t*>(lo + n * kLDP + p) = v[j].y;
+        *reinterpret_cast<uint32_t*>(hi + (n + 8) * kLDP + p) = v[j].z;
+        *reinterpret_cast<uint32_t*>(lo + (n + 8) * kLDP + p) = v[j].w;
     }
 }
 
@@ -306,8 +333,7 @@ struct PassSmem {
     static constexpr int LDN = N + 8;
     static constexpr int kV = kQ * LDN;         // V tile [step][state], two buffers
     static constexpr int kX = kQ * kLDP;        // X tile [step][p], two buffers; weighted value, residual
-    static constexpr int kStg = N * kLDP;       // the state on its way out: value, residual [n][p]
-    static constexpr int kBytes = (2 * kV + 4 * kX + 2 * kStg) * 2;
+    static constexpr int kBytes = (2 * kV + 4 * kX) * 2;
 };
 
 template <int N, bool REV>
@@ -320,8 +346,6 @@ __device__ __forceinline__ void pass_body(const BwdArgs& a, const int64_t unit) 
     bf16* Xb = Vb + 2 * S::kV;                              // [2][kX] raw X
     bf16* Xh = Xb + 2 * S::kX;
     bf16* Xl = Xh + S::kX;
-    bf16* Th = Xl + S::kX;
-    bf16* Tl = Th + S::kStg;
     __shared__ float wv[kQ];
     __shared__ float wsum[2];
 
@@ -368,28 +392,23 @@ __device__ __forceinline__ void pass_body(const BwdArgs& a, const int64_t unit) 
         cp_commit();
         const float dl = dl_next;
         if (k + 1 < nc) dl_next = delta_of(k + 1);
-        // the state entering this step of the walk, split, into the staging tile
+        {   // the state entering this step of the walk, split, to its slot: one coalesced
+            // 16-byte piece per lane and tile, in the accumulators' own layout
+            bf16* slot = slots + (unit * nc + c) * (int64_t)(2 * N * kP);
 #pragma unroll
-        for (int i = 0; i < TPW; i++) {
-            const int q = warp * TPW + i, mt = q >> 3, nt = q & 7;
-            const int n = 16 * mt + g, p = 8 * nt + 2 * t4;
-            split_store2(Th, Tl, n * kLDP + p, st[i][0], st[i][1]);
-            split_store2(Th, Tl, (n + 8) * kLDP + p, st[i][2], st[i][3]);
+            for (int i = 0; i < TPW; i++) {
+                const int q = warp * TPW + i;
+                uint4 v;
+                split_pair(st[i][0], st[i][1], v.x, v.y);
+                split_pair(st[i][2], st[i][3], v.z, v.w);
+                *reinterpret_cast<uint4*>(slot + ((int64_t)q * 32 + lane) * 8) = v;
+            }
         }
         const float s = prefix64(dl * Ah, tid, wsum);
         const float slast = wsum[0] + wsum[1];   // the prefix at the chunk's last step
         if (tid < kQ) wv[tid] = REV ? expf(s) : expf(slast - s) * dl;
         cp_wait<1>();                           // this chunk's tiles (all but the newest group)
         __syncthreads();
-        {   // the staged state to its slot in 16-byte pieces
-            bf16* slot = slots + (unit * nc + c) * (int64_t)(2 * N * kP);
-            for (int q = tid; q < 2 * N * (kP / 8); q += kPassThreads) {
-                const int half = q / (N * (kP / 8)), r = q - half * (N * (kP / 8));
-                const int n = r / (kP / 8), pc = r - n * (kP / 8);
-                *reinterpret_cast<uint4*>(slot + (half * N + n) * kP + pc * 8) =
-                    *reinterpret_cast<const uint4*>((half ? Tl : Th) + n * kLDP + pc * 8);
-            }
-        }
         // weighted X, split into bf16 value + residual
         const bf16* Xr = Xb + buf * S::kX;
         for (int q = tid; q < kQ * kP / 2; q += kPassThreads) {
@@ -430,7 +449,7 @@ __device__ __forceinline__ void pass_body(const BwdArgs& a, const int64_t unit) 
 
 // Both passes in one grid: blocks [0, units) walk forward, the rest backward.
 template <int N>
-__global__ void __launch_bounds__(kPassThreads, 2) ssd_bwd_pass_kernel(const BwdArgs a) {
+__global__ void __launch_bounds__(kPassThreads, 3) ssd_bwd_pass_kernel(const BwdArgs a) {
     const int64_t units = a.batch * a.H;
     if ((int64_t)blockIdx.x < units) pass_body<N, false>(a, blockIdx.x);
     else pass_body<N, true>(a, blockIdx.x - units);
@@ -452,7 +471,7 @@ struct ChunkSmem {
 };
 
 template <int N, typename Tg>
-__global__ void __launch_bounds__(kChunkThreads) ssd_bwd_chunk_kernel(const BwdArgs a) {
+__global__ void __launch_bounds__(kChunkThreads, 2) ssd_bwd_chunk_kernel(const BwdArgs a) {
     using S = ChunkSmem<N>;
     constexpr int LDN = S::LDN;
     constexpr int NH = N / 16;                 // 8-column state tiles per warp (half of N / 8)
@@ -489,13 +508,18 @@ __global__ void __launch_bounds__(kChunkThreads) ssd_bwd_chunk_kernel(const BwdA
     const bf16* Gsrc = a.Gc + (unit * nc + c) * (int64_t)(2 * N * kP);
     const bf16* Hsrc = a.Hc + (unit * nc + c) * (int64_t)(2 * N * kP);
 
-    // ---- P0: tiles and G by asynchronous copies; step sizes and prefix sums meanwhile
+    // ---- P0: tiles by asynchronous copies, G's pieces into registers; step sizes and
+    // prefix sums meanwhile
     stage_rows_async<N, kChunkThreads>(Cs, a.C, b, t0, L, a.G, grp, tid);
     stage_rows_async<N, kChunkThreads>(Bs, a.B, b, t0, L, a.G, grp, tid);
     stage_rows_async<kP, kChunkThreads>(Xs, a.x, b, t0, L, H, h, tid);
     stage_rows_async<kP, kChunkThreads>(Ys, a.dout, b, t0, L, H, h, tid);
-    stage_state_async<N, kChunkThreads>(Sh, Sl, Gsrc, tid);
     cp_commit();
+    {
+        uint4 gpc[N / 16];
+        load_state_pieces<N>(gpc, Gsrc, tid);
+        store_state_pieces<N>(Sh, Sl, gpc, tid);
+    }
     float d = 0.f, v = 0.f;
     if (tid < kQ && t0 + tid < L) d = step_size(a, b, t0 + tid, h, bias, &v);
     const float s = prefix64(d * Ah, tid, scratch);
@@ -580,7 +604,7 @@ __global__ void __launch_bounds__(kChunkThreads) ssd_bwd_chunk_kernel(const BwdA
     }
     __syncthreads();
 
-    float dc[NH][4];                           // dC of rows i of slice rs, states [ch N / 2, + N / 2)
+    uint4 hpc[N / 16];                         // H's pieces, loaded while dB's products run
     // ---- P2: rows j of slice rs.  W = exp(s_last - s_j) B_j G and Z = K^T dY on columns
     // [32 ch, 32 ch + 32); dx; then dB_j on states [ch N / 2, + N / 2).
     {
@@ -663,9 +687,8 @@ __global__ void __launch_bounds__(kChunkThreads) ssd_bwd_chunk_kernel(const BwdA
         for (int m = 0; m < NH; m++) {
             db[m][0] *= f0; db[m][1] *= f0; db[m][2] *= f1; db[m][3] *= f1;
         }
-        __syncthreads();                       // every Z is formed: the Q x Q tile takes (dY X^T) o L o Delta,
-        stage_state_async<N, kChunkThreads>(Sh, Sl, Hsrc, tid);   // and G is used up: H comes in
-        cp_commit();
+        __syncthreads();                       // every Z is formed: the Q x Q tile takes (dY X^T) o L o Delta
+        load_state_pieces<N>(hpc, Hsrc, tid);
 #pragma unroll
         for (int m = 0; m < 4; m++) {
             if (m > rs) continue;
@@ -686,44 +709,33 @@ __global__ void __launch_bounds__(kChunkThreads) ssd_bwd_chunk_kernel(const BwdA
             if (tj0 < L) *reinterpret_cast<float2*>(a.dBp + ((b * L + tj0) * H + h) * N + n) = make_float2(db[m][0], db[m][1]);
             if (tj1 < L) *reinterpret_cast<float2*>(a.dBp + ((b * L + tj1) * H + h) * N + n) = make_float2(db[m][2], db[m][3]);
         }
-        // dC_i's intra-chunk part (rows i of slice rs) in the same phase: its causal shape
-        // mirrors dB's, so every warp does the same number of products here
+    }
+    // <G, H> from G's tile (nobody reads it any more) and H's pieces, then H takes the tile
+    float gh = 0.f;
 #pragma unroll
-        for (int m = 0; m < NH; m++)
+    for (int j = 0; j < N / 16; j++) {
+        int n, p;
+        piece_position(tid + 256 * j, n, p);
+        const uint32_t gw[4] = {*reinterpret_cast<const uint32_t*>(Sh + n * kLDP + p),
+                                *reinterpret_cast<const uint32_t*>(Sl + n * kLDP + p),
+                                *reinterpret_cast<const uint32_t*>(Sh + (n + 8) * kLDP + p),
+                                *reinterpret_cast<const uint32_t*>(Sl + (n + 8) * kLDP + p)};
+        const uint32_t hw[4] = {hpc[j].x, hpc[j].y, hpc[j].z, hpc[j].w};
 #pragma unroll
-            for (int e = 0; e < 4; e++) dc[m][e] = 0.f;
-        for (int k0 = 0; k0 <= 16 * rs; k0 += 16) {
-            uint32_t ah[4], al[4];
-            fragA_kc(ah, K2h, kLDQ, 16 * rs, k0, g, t4);
-            fragA_kc(al, K2l, kLDQ, 16 * rs, k0, g, t4);
-            mma_row<NH, false, true>(dc, ah, al, Bs, LDN, ch * (N / 2), k0, g, t4);
+        for (int r = 0; r < 2; r++) {
+            const float2 g0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw[2 * r]));
+            const float2 g1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw[2 * r + 1]));
+            const float2 h0v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hw[2 * r]));
+            const float2 h1v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hw[2 * r + 1]));
+            gh += (g0.x + g1.x) * (h0v.x + h1v.x) + (g0.y + g1.y) * (h0v.y + h1v.y);
         }
     }
-    cp_wait<0>();
+    store_state_pieces<N>(Sh, Sl, hpc, tid);
     __syncthreads();
 
-    // ---- P3: <G, H> (G again from global memory, H from its tile); rows i of slice rs:
-    // dC_i on states [ch N / 2, + N / 2)
-    float gh = 0.f;
-    for (int q = tid; q < N * (kP / 8); q += kChunkThreads) {
-        const int n = q / (kP / 8), p = 8 * (q - n * (kP / 8));
-        const uint4 g_hi = *reinterpret_cast<const uint4*>(Gsrc + n * kP + p);
-        const uint4 g_lo = *reinterpret_cast<const uint4*>(Gsrc + (N + n) * kP + p);
-        const uint4 h_hi = *reinterpret_cast<const uint4*>(Sh + n * kLDP + p);
-        const uint4 h_lo = *reinterpret_cast<const uint4*>(Sl + n * kLDP + p);
-        const __nv_bfloat162* gh2 = reinterpret_cast<const __nv_bfloat162*>(&g_hi);
-        const __nv_bfloat162* gl2 = reinterpret_cast<const __nv_bfloat162*>(&g_lo);
-        const __nv_bfloat162* hh2 = reinterpret_cast<const __nv_bfloat162*>(&h_hi);
-        const __nv_bfloat162* hl2 = reinterpret_cast<const __nv_bfloat162*>(&h_lo);
-#pragma unroll
-        for (int e = 0; e < 4; e++) {
-            const float2 gv = __bfloat1622float2(gh2[e]), gr = __bfloat1622float2(gl2[e]);
-            const float2 hv = __bfloat1622float2(hh2[e]), hr = __bfloat1622float2(hl2[e]);
-            gh += (gv.x + gr.x) * (hv.x + hr.x) + (gv.y + gr.y) * (hv.y + hr.y);
-        }
-    }
+    // ---- P3: rows i of slice rs: dC_i on states [ch N / 2, + N / 2)
     {
-        float hs[NH][4];                       // exp(s_i) H dy_i
+        float hs[NH][4];                       // exp(s_i) H dy_i, then + the intra-chunk part
 #pragma unroll
         for (int m = 0; m < NH; m++)
 #pragma unroll
@@ -746,8 +758,6 @@ __global__ void __launch_bounds__(kChunkThreads) ssd_bwd_chunk_kernel(const BwdA
             const float2 c1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(Cs + i1 * LDN + n));
             o0 += c0.x * hs[m][0] + c0.y * hs[m][1];
             o1 += c1.x * hs[m][2] + c1.y * hs[m][3];
-#pragma unroll
-            for (int e = 0; e < 4; e++) dc[m][e] += hs[m][e];
         }
 #pragma unroll
         for (int o = 1; o <= 2; o <<= 1) {
@@ -758,12 +768,18 @@ __global__ void __launch_bounds__(kChunkThreads) ssd_bwd_chunk_kernel(const BwdA
             red_o[ch * kQ + i0] = o0;
             red_o[ch * kQ + i1] = o1;
         }
+        for (int k0 = 0; k0 <= 16 * rs; k0 += 16) {
+            uint32_t ah[4], al[4];
+            fragA_kc(ah, K2h, kLDQ, 16 * rs, k0, g, t4);
+            fragA_kc(al, K2l, kLDQ, 16 * rs, k0, g, t4);
+            mma_row<NH, false, true>(hs, ah, al, Bs, LDN, ch * (N / 2), k0, g, t4);
+        }
         const int64_t ti0 = t0 + i0, ti1 = t0 + i1;
 #pragma unroll
         for (int m = 0; m < NH; m++) {
             const int n = ch * (N / 2) + 8 * m + 2 * t4;
-            if (ti0 < L) *reinterpret_cast<float2*>(a.dCp + ((b * L + ti0) * H + h) * N + n) = make_float2(dc[m][0], dc[m][1]);
-            if (ti1 < L) *reinterpret_cast<float2*>(a.dCp + ((b * L + ti1) * H + h) * N + n) = make_float2(dc[m][2], dc[m][3]);
+            if (ti0 < L) *reinterpret_cast<float2*>(a.dCp + ((b * L + ti0) * H + h) * N + n) = make_float2(hs[m][0], hs[m][1]);
+            if (ti1 < L) *reinterpret_cast<float2*>(a.dCp + ((b * L + ti1) * H + h) * N + n) = make_float2(hs[m][2], hs[m][3]);
         }
     }
 
