@@ -129,3 +129,18 @@ def test_ssd_bwd_mamba2_2p7b_layer_sampled():
     # dB, dC of batch row 0 only depend on that row
     assert_close(got["dB"][:1], ref0["dB"], torch.bfloat16, torch.float32, what="dB")
     assert_close(got["dC"][:1], ref0["dC"], torch.bfloat16, torch.float32, what="dC")
+
+
+def test_ssd_bwd_heads_without_decay():
+    """A = 0 on some heads: every decay is exactly one, the state never forgets."""
+    lib = _lib()
+    g, dout, dh = _case(S.config_seed(5) + 404, 2, 200, 4, 64, 2, True, True)
+    g["A"] = g["A"] * 0.002
+    g["A"][1] = 0.0
+    g["A"][3] = 0.0
+    got = lib.ssm_ssd_bwd(g["x"], g["dt"], g["A"], g["B"], g["C"], dout, D=g["D"], dt_bias=g["dt_bias"],
+                          h0=g["h0"], dfinal_state=dh, want_dh0=True)
+    torch.cuda.synchronize()
+    ref = oracle.ssd_bwd(g["x"], g["dt"], g["A"], g["B"], g["C"], dout, g["D"], g["dt_bias"], g["h0"], dh,
+                         threads=4)
+    _check(got, ref, torch.float32, ("dx", "ddt", "dA", "dB", "dC", "dD", "ddt_bias", "dh0"))
