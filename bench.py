@@ -329,6 +329,26 @@ def ssd_cpu_baseline(cfg, heads: int = 0):
                       f"on {threads} threads)"}
 
 
+def ssd_work(cfg, Q=None):
+    """Algorithmic HBM bytes and tensor FLOPs of the SSD forward at chunk length Q
+    (default: the config's): x, dt in and y out per (b, t, h); B, C per (b, t, g); the
+    products C B^T, M x, C H and the state update on full blocks."""
+    b, T, H, P, N, G = (cfg[k] for k in ("batch", "seqlen", "nheads", "headdim", "dstate", "ngroups"))
+    Q = Q or cfg["chunk"]
+    return {"bytes": b * T * (H * (2 * P * 2 + 2) + 2 * G * N * 2),
+            "flops": b * H * T * (2 * Q * N + 2 * Q * P + 4 * N * P)}
+
+
+def ssd_bwd_work(cfg, Q=64):
+    """Algorithmic HBM bytes and tensor FLOPs of the SSD backward at chunk length Q:
+    x, dout, dt in and dx, ddt out (bf16) per (b, t, h); B, C in (bf16) and dB, dC out
+    (fp32) per (b, t, g); the products C B^T, dY X^T, K^T dY, B G, dB and dC (intra
+    and state parts each) and the two state passes on full blocks."""
+    b, T, H, P, N, G = (cfg[k] for k in ("batch", "seqlen", "nheads", "headdim", "dstate", "ngroups"))
+    return {"bytes": b * T * (H * (3 * P * 2 + 2 * 2) + G * N * (2 * 2 + 2 * 4)),
+            "flops": b * H * T * (6 * Q * N + 4 * Q * P + 10 * N * P)}
+
+
 def bench_ssd(L, device, cfg, reps: int = 10):
     """Mamba-2 state-space-duality layer forward (ssm_ssd_fwd), bf16 in and out:
     milliseconds per call, its algorithmic HBM bytes (x, dt, B, C in; out) and
@@ -348,8 +368,8 @@ def bench_ssd(L, device, cfg, reps: int = 10):
         call()
     torch.cuda.synchronize()
     ms = time_calls(call, reps, L2Flush(device))
-    nbytes = b * T * (H * (2 * P * 2 + 2) + 2 * G * N * 2)
-    flops = b * H * T * (2 * Q * N + 2 * Q * P + 4 * N * P)
+    w = ssd_work(cfg)
+    nbytes, flops = w["bytes"], w["flops"]
     hbm, _ = measured_peaks()
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -416,8 +436,8 @@ def bench_ssd_bwd(L, device, cfg, reps: int = 10):
 
     torch.cuda.synchronize()
     ms = time_calls(call, reps, L2Flush(device))
-    nbytes = b * T * (H * (3 * P * 2 + 2 * 2) + G * N * (2 * 2 + 2 * 4))
-    flops = b * H * T * (6 * Q * N + 4 * Q * P + 12 * N * P)
+    w = ssd_bwd_work(cfg, Q)
+    nbytes, flops = w["bytes"], w["flops"]
     hbm, _ = measured_peaks()
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:

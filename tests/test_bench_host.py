@@ -78,3 +78,34 @@ def test_unit_rates_from_the_probe_and_the_nominal_fallback():
     finally:
         bench.UNIT_RATES.clear()
         bench.UNIT_RATES.update(saved)
+
+
+def _chunk_products(b, T, H, P, N, Q, shapes):
+    """FLOPs of products (m, n, k) per chunk, summed over every (b, h, chunk) of full blocks."""
+    chunks = b * H * (T // Q)
+    return chunks * sum(2 * m * n * k for m, n, k in shapes)
+
+
+def test_ssd_work_counts_the_chunked_products():
+    cfg = dict(bench.SSD)
+    b, T, H, P, N, G, Q = (cfg[k] for k in ("batch", "seqlen", "nheads", "headdim", "dstate", "ngroups", "chunk"))
+    # C B^T (Q x Q, k N), M x (Q x P, k Q), C H (Q x P, k N), state update B^T (w x) (N x P, k Q)
+    assert bench.ssd_work(cfg)["flops"] == _chunk_products(b, T, H, P, N, Q,
+                                                           [(Q, Q, N), (Q, P, Q), (Q, P, N), (N, P, Q)])
+    assert bench.ssd_work(cfg)["bytes"] == 346_554_368                 # x, dt, y, B, C at the 2.7B shape
+
+
+def test_ssd_bwd_work_counts_the_chunked_adjoint_products():
+    cfg = dict(bench.SSD)
+    b, T, H, P, N = (cfg[k] for k in ("batch", "seqlen", "nheads", "headdim", "dstate"))
+    Q = 64
+    shapes = [(Q, Q, N),                     # C B^T
+              (Q, Q, P),                     # dY X^T
+              (Q, P, Q),                     # Z = K^T dY
+              (Q, P, N),                     # B G
+              (Q, N, Q), (Q, N, P),          # dC: intra, state
+              (Q, N, Q), (Q, N, P),          # dB: intra, state
+              (N, P, Q), (N, P, Q)]          # the two state passes
+    assert bench.ssd_bwd_work(cfg, Q)["flops"] == _chunk_products(b, T, H, P, N, Q, shapes)
+    # x, dout, dx (bf16) and dt, ddt (bf16) per (b, t, h); B, C in bf16 and dB, dC in fp32 per (b, t)
+    assert bench.ssd_bwd_work(cfg, Q)["bytes"] == b * T * (H * (3 * 2 * P + 2 * 2) + N * (2 * 2 + 2 * 4))
